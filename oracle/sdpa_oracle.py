@@ -1,0 +1,241 @@
+"""fp64 CPU oracle for scaled dot-product attention (forward and backward).
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and
+``bench.py`` (its ``cpu_baseline`` leg and ``--impl reference`` arm) may import
+this module.  The product path (the CUDA library and its Python binding) never
+imports, calls or links it, and this module imports nothing from the product.
+
+What it computes is the plain definition, written out step by step in float64 on
+the exact input values (fp16 / bf16 upcast exactly; E4M3 bytes decoded by this
+module's own table and multiplied by their descale):
+
+* scores ``S = attn_scale * Q Kᵀ``, a naive matrix product
+  [attention codelab, §1 "How attention works", step 1; §4 "Implementing
+  attention from scratch"; cuDNN 9 blog, "SDPA as a cuDNN graph", Fig. 4: the
+  scale is a pointwise multiply right after BMM1];
+* an explicit mask: with ``causal`` key j is visible to query i iff ``j <= i``
+  (top-left alignment) [codelab §7 "Adding a causal mask": position 0 sees only
+  itself, the last position sees every position];
+* a three-pass softmax over the visible keys: row max, sum of exponentials,
+  normalise [codelab §1 step 2];
+* ``O = P V`` [codelab §1 step 3], output with Q's shape [step 4];
+* the per-row statistics ``LSE_i = m_i + ln l_i`` (natural log) — the reading of the
+  "stats" output that the SDPA node returns for training [cuDNN 9 blog, SDPA
+  walkthrough sample; cuDNN-in-Python post: the second return value is for
+  training];
+* head grouping: query head ``hq`` reads KV head ``hq // (h_q // h_kv)`` (contiguous
+  groups; the codelab's §9 "Comparing MHA, GQA and MQA" broadcasts each KV head to
+  its group of query heads);
+* the backward pass is the analytic derivative of O with respect to Q, K and V
+  (the pages show a backward graph exists but print no formula): with the incoming
+  gradient dO, dV = Pᵀ dO, dP = dO Vᵀ, Delta_i = Σ_j P_ij dP_ij,
+  dS = P ∘ (dP − Delta), dQ = scale·dS K, dK = scale·dSᵀ Q, with dK and dV summed
+  over the query heads of each KV group.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against brute force,
+closed forms, invariants and finite differences; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+from typing import Iterable, Sequence, Tuple
+
+import numpy as np
+
+__all__ = [
+    "visible_mask", "kv_head_of", "head_forward", "forward", "forward_rows",
+    "backward", "backward_dq_rows", "backward_kv_head", "e4m3_decode_table",
+    "decode_e4m3", "to_f64",
+]
+
+
+# ---------------------------------------------------------------------------
+# Format helpers
+# ---------------------------------------------------------------------------
+
+def e4m3_decode_table() -> np.ndarray:
+    """The 256 values of OCP FP8 E4M3 ("FN": no infinities, one NaN pattern per sign).
+
+    Bit layout: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits
+    [codelab §10: E4M3 = 4 exponent bits, 3 mantissa bits, used in the forward pass].
+    Exponent field 0 encodes subnormals m/8 * 2**(1-7); exponent field 15 with
+    mantissa 7 is NaN; every other pattern is (1 + m/8) * 2**(e-7).
+    """
+    tab = np.empty(256, dtype=np.float64)
+    for code in range(256):
+        sign = -1.0 if code & 0x80 else 1.0
+        e = (code >> 3) & 0xF
+        m = code & 0x7
+        if e == 0xF and m == 0x7:
+            tab[code] = math.nan
+        elif e == 0:
+            tab[code] = sign * (m / 8.0) * 2.0 ** (1 - 7)
+        else:
+            tab[code] = sign * (1.0 + m / 8.0) * 2.0 ** (e - 7)
+    return tab
+
+
+_E4M3 = e4m3_decode_table()
+
+
+def decode_e4m3(codes: np.ndarray, descale: float = 1.0) -> np.ndarray:
+    """Exact fp64 value of E4M3 bytes times a per-tensor descale."""
+    return _E4M3[np.asarray(codes, dtype=np.uint8)] * float(descale)
+
+
+def to_f64(t, descale: float = 1.0) -> np.ndarray:
+    """Exact fp64 copy of a CPU torch tensor (fp16 / bf16 / fp32 / float8_e4m3fn)."""
+    import torch  # plumbing only: reads the bytes of a tensor
+
+    t = t.detach().cpu()
+    if t.dtype == torch.float8_e4m3fn:
+        return decode_e4m3(t.contiguous().view(torch.uint8).numpy(), descale)
+    return t.to(torch.float64).numpy() * float(descale)
+
+
+# ---------------------------------------------------------------------------
+# Forward
+# ---------------------------------------------------------------------------
+
+def visible_mask(s_q: int, s_kv: int, causal: bool) -> np.ndarray:
+    """Boolean [s_q, s_kv]: True where key j is visible to query i."""
+    if not causal:
+        return np.ones((s_q, s_kv), dtype=bool)
+    i = np.arange(s_q)[:, None]
+    j = np.arange(s_kv)[None, :]
+    return j <= i
+
+
+def kv_head_of(hq: int, h_q: int, h_kv: int) -> int:
+    """KV head read by query head ``hq`` (contiguous groups of h_q // h_kv)."""
+    if h_kv <= 0 or h_q % h_kv:
+        raise ValueError("h_q must be a positive multiple of h_kv")
+    return hq // (h_q // h_kv)
+
+
+def head_forward(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, scale: float,
+                 mask: np.ndarray):
+    """One (batch, head) slice: returns (O [s_q,d], LSE [s_q], P [s_q,s_kv]).
+
+    Rows with no visible key are undefined for softmax and are rejected."""
+    S = scale * (qh @ kh.T)                                   # step 1 + scale
+    if not mask.any(axis=1).all():
+        raise ValueError("a query row has no visible key")
+    m = np.where(mask, S, -np.inf).max(axis=1)                # pass 1: row max
+    E = np.where(mask, np.exp(S - m[:, None]), 0.0)
+    l = E.sum(axis=1)                                         # pass 2: row sum
+    P = E / l[:, None]                                        # pass 3: normalise
+    O = P @ vh                                                # step 3
+    lse = m + np.log(l)
+    return O, lse, P
+
+
+def forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: bool):
+    """Full forward on logical BHSD fp64 arrays.
+
+    q: [b, h_q, s_q, d]; k, v: [b, h_kv, s_kv, d].  Returns (O [b,h_q,s_q,d],
+    LSE [b,h_q,s_q])."""
+    b, h_q, s_q, d = q.shape
+    h_kv, s_kv = k.shape[1], k.shape[2]
+    mask = visible_mask(s_q, s_kv, causal)
+    O = np.empty((b, h_q, s_q, v.shape[3]), dtype=np.float64)
+    L = np.empty((b, h_q, s_q), dtype=np.float64)
+    for bi in range(b):
+        for hq in range(h_q):
+            hk = kv_head_of(hq, h_q, h_kv)
+            O[bi, hq], L[bi, hq], _ = head_forward(q[bi, hq], k[bi, hk], v[bi, hk], scale, mask)
+    return O, L
+
+
+def forward_rows(q_rows: np.ndarray, rows: Sequence[int], kh: np.ndarray, vh: np.ndarray,
+                 scale: float, causal: bool):
+    """Forward for selected query rows of one (batch, head).
+
+    q_rows: [n, d] fp64 rows of Q; rows: their sequence positions; kh, vh: the
+    row's KV head [s_kv, d].  Returns (O rows [n, d], LSE [n]).  Cost O(n·s_kv·d),
+    which lets large shapes be checked row by row."""
+    s_kv = kh.shape[0]
+    rows = np.asarray(rows)
+    mask = (np.arange(s_kv)[None, :] <= rows[:, None]) if causal else np.ones(
+        (len(rows), s_kv), dtype=bool)
+    O, lse, _ = head_forward(q_rows, kh, vh, scale, mask)
+    return O, lse
+
+
+# ---------------------------------------------------------------------------
+# Backward
+# ---------------------------------------------------------------------------
+
+def _head_backward(qh, kh, vh, doh, scale, mask):
+    _, _, P = head_forward(qh, kh, vh, scale, mask)
+    dV = P.T @ doh
+    dP = doh @ vh.T
+    delta = (P * dP).sum(axis=1)
+    dS = P * (dP - delta[:, None])
+    dQ = scale * (dS @ kh)
+    dK = scale * (dS.T @ qh)
+    return dQ, dK, dV
+
+
+def backward(q, k, v, do, scale: float, causal: bool):
+    """Full backward on logical BHSD fp64 arrays: returns (dQ, dK, dV).
+
+    dK, dV have K's and V's shapes and hold the sum over each KV head's group."""
+    b, h_q, s_q, _ = q.shape
+    h_kv, s_kv = k.shape[1], k.shape[2]
+    mask = visible_mask(s_q, s_kv, causal)
+    dQ = np.empty_like(q, dtype=np.float64)
+    dK = np.zeros(k.shape, dtype=np.float64)
+    dV = np.zeros(v.shape, dtype=np.float64)
+    for bi in range(b):
+        for hq in range(h_q):
+            hk = kv_head_of(hq, h_q, h_kv)
+            gq, gk, gv = _head_backward(q[bi, hq], k[bi, hk], v[bi, hk], do[bi, hq], scale, mask)
+            dQ[bi, hq] = gq
+            dK[bi, hk] += gk
+            dV[bi, hk] += gv
+    return dQ, dK, dV
+
+
+def backward_dq_rows(q_rows, do_rows, rows: Sequence[int], kh, vh, scale: float, causal: bool):
+    """dQ for selected query rows of one (batch, head): [n, d].
+
+    Row i needs only its own P_i, dP_i = dO_i Vᵀ and Delta_i, so the cost is
+    O(n·s_kv·d)."""
+    s_kv = kh.shape[0]
+    rows = np.asarray(rows)
+    mask = (np.arange(s_kv)[None, :] <= rows[:, None]) if causal else np.ones(
+        (len(rows), s_kv), dtype=bool)
+    _, _, P = head_forward(q_rows, kh, vh, scale, mask)
+    dP = do_rows @ vh.T
+    delta = (P * dP).sum(axis=1)
+    dS = P * (dP - delta[:, None])
+    return scale * (dS @ kh)
+
+
+def backward_kv_head(q, k, v, do, scale: float, causal: bool, bi: int, hk: int,
+                     row_chunk: int = 1024):
+    """dK, dV of one (batch, KV head) at any size: [s_kv, d] each.
+
+    Sums over the KV head's group of query heads, visiting query rows in chunks
+    so that at most row_chunk x s_kv scores are held at a time."""
+    b, h_q, s_q, _ = q.shape
+    h_kv, s_kv = k.shape[1], k.shape[2]
+    g = h_q // h_kv
+    kh, vh = k[bi, hk], v[bi, hk]
+    dK = np.zeros_like(kh, dtype=np.float64)
+    dV = np.zeros_like(vh, dtype=np.float64)
+    for hq in range(hk * g, (hk + 1) * g):
+        for r0 in range(0, s_q, row_chunk):
+            r1 = min(s_q, r0 + row_chunk)
+            rows = np.arange(r0, r1)
+            mask = (np.arange(s_kv)[None, :] <= rows[:, None]) if causal else np.ones(
+                (r1 - r0, s_kv), dtype=bool)
+            qh, doh = q[bi, hq, r0:r1], do[bi, hq, r0:r1]
+            _, _, P = head_forward(qh, kh, vh, scale, mask)
+            dV += P.T @ doh
+            dP = doh @ vh.T
+            delta = (P * dP).sum(axis=1)
+            dS = P * (dP - delta[:, None])
+            dK += scale * (dS.T @ qh)
+    return dK, dV

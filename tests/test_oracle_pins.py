@@ -1,0 +1,339 @@
+"""Pins for the fp64 oracle: checks it against things other than itself.
+
+Brute force written as explicit Python loops, hand-worked values (tests/golden),
+closed forms, invariants the definition implies, and central finite differences
+for the backward pass.  Each test is chosen so that a plausible slip in the oracle
+(a dropped scale, a transposed operand, a wrong head index, a mask off by one, a
+missing Delta term) fails at least one of them.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sdpa_workloads import Workload, make_inputs, gpt2_inference, quantize_e4m3
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+RNG = np.random.default_rng(12345)
+
+
+def _rand(*shape):
+    return RNG.standard_normal(shape)
+
+
+# ---------------------------------------------------------------------------
+# brute force: explicit loops straight from the definition
+# ---------------------------------------------------------------------------
+
+def _brute_forward(q, k, v, scale, causal):
+    b, h_q, s_q, d = q.shape
+    h_kv, s_kv, dv = k.shape[1], k.shape[2], v.shape[3]
+    g = h_q // h_kv
+    O = np.zeros((b, h_q, s_q, dv))
+    L = np.zeros((b, h_q, s_q))
+    for bi in range(b):
+        for h in range(h_q):
+            hk = h // g
+            for i in range(s_q):
+                w = []
+                for j in range(s_kv):
+                    if causal and j > i:
+                        w.append(0.0)
+                        continue
+                    dot = 0.0
+                    for t in range(d):
+                        dot += q[bi, h, i, t] * k[bi, hk, j, t]
+                    w.append(math.exp(scale * dot))
+                tot = sum(w)
+                L[bi, h, i] = math.log(tot)
+                for c in range(dv):
+                    O[bi, h, i, c] = sum(w[j] / tot * v[bi, hk, j, c] for j in range(s_kv))
+    return O, L
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("h_q,h_kv", [(2, 2), (4, 2), (3, 1)])
+def test_forward_matches_brute_force(causal, h_q, h_kv):
+    q, k, v = _rand(2, h_q, 5, 3), _rand(2, h_kv, 7, 3), _rand(2, h_kv, 7, 3)
+    O, L = oracle.forward(q, k, v, 0.7, causal)
+    Ob, Lb = _brute_forward(q, k, v, 0.7, causal)
+    np.testing.assert_allclose(O, Ob, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(L, Lb, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_rows_matches_brute_force(causal):
+    q, k, v = _rand(1, 2, 9, 4), _rand(1, 1, 9, 4), _rand(1, 1, 9, 4)
+    Ob, Lb = _brute_forward(q, k, v, 0.5, causal)
+    rows = [0, 3, 8]
+    O, L = oracle.forward_rows(q[0, 1, rows], rows, k[0, 0], v[0, 0], 0.5, causal)
+    np.testing.assert_allclose(O, Ob[0, 1, rows], atol=1e-12)
+    np.testing.assert_allclose(L, Lb[0, 1, rows], atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# hand-worked example (tests/golden/hand_worked_2x2.json)
+# ---------------------------------------------------------------------------
+
+def _num(x):
+    env = {"ln2": math.log(2), "ln3": math.log(3), "ln4": math.log(4)}
+    return float(eval(str(x), {"__builtins__": {}}, env))
+
+
+def test_hand_worked_example():
+    gold = json.load(open(os.path.join(GOLDEN, "hand_worked_2x2.json")))
+    q = np.array([[_num(x) for x in r] for r in gold["q"]])[None, None]
+    k = np.array(gold["k"], dtype=float)[None, None]
+    v = np.array(gold["v"], dtype=float)[None, None]
+    for case, causal in (("full", False), ("causal", True)):
+        O, L = oracle.forward(q, k, v, 1.0, causal)
+        np.testing.assert_allclose(O[0, 0], np.array(gold[case]["o"]), atol=1e-14)
+        np.testing.assert_allclose(L[0, 0], [_num(x) for x in gold[case]["lse"]], atol=1e-14)
+    do = np.array(gold["backward_dO"], dtype=float)[None, None]
+    dQ, dK, dV = oracle.backward(q, k, v, do, 1.0, False)
+    fb = gold["full_backward"]
+    for name, got in (("dq", dQ), ("dk", dK), ("dv", dV)):
+        want = np.array([[_num(x) for x in r] for r in fb[name]])
+        np.testing.assert_allclose(got[0, 0], want, atol=1e-14, err_msg=name)
+
+
+# ---------------------------------------------------------------------------
+# softmax and forward invariants / closed forms
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_softmax_rows_sum_to_one_and_mask_is_exact(causal):
+    q, k, v = _rand(6, 8), _rand(10, 8), _rand(10, 8)
+    mask = oracle.visible_mask(6, 10, causal)
+    _, _, P = oracle.head_forward(q, k, v, 0.35, mask)
+    np.testing.assert_allclose(P.sum(axis=1), 1.0, atol=1e-12)
+    assert (P >= 0).all()
+    assert (P[~mask] == 0).all()
+    if causal:
+        assert mask.sum() == sum(min(i + 1, 10) for i in range(6))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_constant_v_returns_v(causal):
+    q, k = _rand(1, 2, 7, 5), _rand(1, 2, 7, 5)
+    c = _rand(5)
+    v = np.broadcast_to(c, (1, 2, 7, 5)).copy()
+    O, _ = oracle.forward(q, k, v, 1.3, causal)
+    np.testing.assert_allclose(O, np.broadcast_to(c, O.shape), atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_scale_gives_mean_of_visible_values(causal):
+    q, k, v = _rand(1, 1, 6, 3), _rand(1, 1, 6, 3), _rand(1, 1, 6, 3)
+    O, L = oracle.forward(q, k, v, 0.0, causal)
+    for i in range(6):
+        n = i + 1 if causal else 6
+        np.testing.assert_allclose(O[0, 0, i], v[0, 0, :n].mean(axis=0), atol=1e-12)
+        np.testing.assert_allclose(L[0, 0, i], math.log(n), atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_zero_query_lse_is_log_count(causal):
+    q = np.zeros((1, 1, 5, 4))
+    k, v = _rand(1, 1, 8, 4), _rand(1, 1, 8, 4)
+    _, L = oracle.forward(q, k, v, 0.9, causal)
+    want = [math.log(min(i + 1, 8) if causal else 8) for i in range(5)]
+    np.testing.assert_allclose(L[0, 0], want, atol=1e-12)
+
+
+def test_causal_first_and_last_rows():
+    """Row 0 attends only to key 0; the last row sees every key (codelab §7)."""
+    q, k, v = _rand(1, 2, 9, 4), _rand(1, 2, 9, 4), _rand(1, 2, 9, 4)
+    Oc, Lc = oracle.forward(q, k, v, 0.6, True)
+    Of, Lf = oracle.forward(q, k, v, 0.6, False)
+    np.testing.assert_allclose(Oc[:, :, 0], v[:, :, 0], atol=1e-12)
+    np.testing.assert_allclose(Lc[:, :, 0], 0.6 * (q[:, :, 0] * k[:, :, 0]).sum(-1), atol=1e-12)
+    np.testing.assert_allclose(Oc[:, :, -1], Of[:, :, -1], atol=1e-12)
+    assert np.abs(Oc[:, :, 0] - Of[:, :, 0]).max() > 1e-3
+    gold = json.load(open(os.path.join(GOLDEN, "page_shapes.json")))["codelab_causal_effect"]
+    assert np.abs(Oc[:, :, -1] - Of[:, :, -1]).max() < gold["last_position_max_abs_diff_below"]
+
+
+def test_causal_row_ignores_future_keys():
+    q, k, v = _rand(1, 1, 8, 4), _rand(1, 1, 8, 4), _rand(1, 1, 8, 4)
+    O1, L1 = oracle.forward(q, k, v, 0.8, True)
+    k2, v2 = k.copy(), v.copy()
+    i = 3
+    k2[:, :, i + 1:] += 5 * _rand(1, 1, 8 - i - 1, 4)
+    v2[:, :, i + 1:] -= 7.0
+    O2, L2 = oracle.forward(q, k2, v2, 0.8, True)
+    np.testing.assert_array_equal(O1[:, :, : i + 1], O2[:, :, : i + 1])
+    np.testing.assert_array_equal(L1[:, :, : i + 1], L2[:, :, : i + 1])
+    assert np.abs(O1[:, :, i + 1:] - O2[:, :, i + 1:]).max() > 1e-3
+
+
+def test_two_key_closed_form():
+    """With two keys, softmax is a logistic function of the score difference."""
+    q, k, v = _rand(1, 1, 4, 6), _rand(1, 1, 2, 6), _rand(1, 1, 2, 6)
+    O, L = oracle.forward(q, k, v, 0.4, False)
+    s = 0.4 * q[0, 0] @ k[0, 0].T
+    p0 = 1.0 / (1.0 + np.exp(s[:, 1] - s[:, 0]))
+    np.testing.assert_allclose(O[0, 0], p0[:, None] * v[0, 0, 0] + (1 - p0)[:, None] * v[0, 0, 1],
+                               atol=1e-12)
+    np.testing.assert_allclose(L[0, 0], np.logaddexp(s[:, 0], s[:, 1]), atol=1e-12)
+
+
+@pytest.mark.parametrize("h_kv", [1, 2, 4])
+def test_grouped_heads_equal_repeated_mha(h_kv):
+    """GQA/MQA equal MHA with each KV head repeated over its group (codelab §9)."""
+    h_q = 4
+    q, k, v = _rand(2, h_q, 6, 3), _rand(2, h_kv, 6, 3), _rand(2, h_kv, 6, 3)
+    do = _rand(2, h_q, 6, 3)
+    g = h_q // h_kv
+    kr, vr = np.repeat(k, g, axis=1), np.repeat(v, g, axis=1)
+    for causal in (False, True):
+        O, L = oracle.forward(q, k, v, 0.5, causal)
+        Or, Lr = oracle.forward(q, kr, vr, 0.5, causal)
+        np.testing.assert_allclose(O, Or, atol=1e-13)
+        np.testing.assert_allclose(L, Lr, atol=1e-13)
+        dQ, dK, dV = oracle.backward(q, k, v, do, 0.5, causal)
+        dQr, dKr, dVr = oracle.backward(q, kr, vr, do, 0.5, causal)
+        np.testing.assert_allclose(dQ, dQr, atol=1e-13)
+        np.testing.assert_allclose(dK, dKr.reshape(2, h_kv, g, 6, 3).sum(2), atol=1e-13)
+        np.testing.assert_allclose(dV, dVr.reshape(2, h_kv, g, 6, 3).sum(2), atol=1e-13)
+
+
+def test_head_grouping_shapes_from_codelab():
+    gold = json.load(open(os.path.join(GOLDEN, "page_shapes.json")))["codelab_head_grouping"]
+    B, T, N, H = gold["q_btnh"]
+    q = _rand(B, T, N, H).transpose(0, 2, 1, 3)
+    for _, nk in gold["kv_heads"].items():
+        k = _rand(B, T, nk, H).transpose(0, 2, 1, 3)
+        O, _ = oracle.forward(q, k, k, 1 / 8, False)
+        assert list(O.transpose(0, 2, 1, 3).shape) == gold["out_btnh"]
+    with pytest.raises(ValueError):
+        oracle.kv_head_of(0, 8, 3)
+
+
+def test_bshd_view_equals_bhsd_in_the_oracle():
+    """The layout is a view: BSHD-strided logical tensors give the same result."""
+    w = Workload("t", 1, 2, 2, 16, 16, 8, "f16", layout="bshd", causal=True)
+    x = make_inputs(w, seed=3, with_do=False)
+    wc = Workload("t", 1, 2, 2, 16, 16, 8, "f16", layout="bhsd", causal=True)
+    q = oracle.to_f64(x.q.contiguous())
+    qs = oracle.to_f64(x.q)
+    np.testing.assert_array_equal(q, qs)
+    assert x.q.stride() == (16 * 2 * 8, 8, 2 * 8, 1)
+    O1, _ = oracle.forward(qs, oracle.to_f64(x.k), oracle.to_f64(x.v), w.scale, True)
+    O2, _ = oracle.forward(q, oracle.to_f64(x.k.contiguous()), oracle.to_f64(x.v.contiguous()),
+                           wc.scale, True)
+    np.testing.assert_array_equal(O1, O2)
+
+
+def test_gpt2_workload_matches_page():
+    gold = json.load(open(os.path.join(GOLDEN, "page_shapes.json")))["gpt2_like"]
+    w = gpt2_inference()
+    assert (w.b, w.h_q, w.s_q, w.d) == (gold["b"], gold["h"], gold["s"], gold["d"])
+    assert w.causal == gold["causal"] and w.stats == gold["stats"] and w.dtype == gold["dtype"]
+    x = make_inputs(Workload("g", 4, 12, 12, 1024, 1024, 64, "f16", layout="bshd"), with_do=False)
+    assert list(x.q.stride()) == gold["strides"]
+    assert abs(w.scale - 1 / math.sqrt(64)) < 1e-15
+
+
+# ---------------------------------------------------------------------------
+# backward: central finite differences and invariants
+# ---------------------------------------------------------------------------
+
+def _fd_grads(q, k, v, do, scale, causal, h=1e-6):
+    def loss(q_, k_, v_):
+        O, _ = oracle.forward(q_, k_, v_, scale, causal)
+        return float((O * do).sum())
+    grads = []
+    for which in range(3):
+        args = [q.copy(), k.copy(), v.copy()]
+        x = args[which]
+        gx = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + h
+            lp = loss(*args)
+            x[idx] = old - h
+            lm = loss(*args)
+            x[idx] = old
+            gx[idx] = (lp - lm) / (2 * h)
+        grads.append(gx)
+    return grads
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("h_q,h_kv,s_q,s_kv", [(2, 2, 4, 4), (4, 2, 5, 3), (2, 1, 3, 6)])
+def test_backward_matches_finite_differences(causal, h_q, h_kv, s_q, s_kv):
+    if causal and s_kv < 1:
+        pytest.skip()
+    q, k, v, do = _rand(1, h_q, s_q, 3), _rand(1, h_kv, s_kv, 3), _rand(1, h_kv, s_kv, 3), \
+        _rand(1, h_q, s_q, 3)
+    dQ, dK, dV = oracle.backward(q, k, v, do, 0.45, causal)
+    fQ, fK, fV = _fd_grads(q, k, v, do, 0.45, causal)
+    for got, want, name in ((dQ, fQ, "dQ"), (dK, fK, "dK"), (dV, fV, "dV")):
+        err = np.linalg.norm(got - want) / max(np.linalg.norm(want), 1e-30)
+        assert err < 1e-6, (name, err)
+    # the sampled forms agree with the same finite differences
+    rows = list(range(s_q))
+    for hq in range(h_q):
+        hk = oracle.kv_head_of(hq, h_q, h_kv)
+        g = oracle.backward_dq_rows(q[0, hq], do[0, hq], rows, k[0, hk], v[0, hk], 0.45, causal)
+        assert np.linalg.norm(g - fQ[0, hq]) / np.linalg.norm(fQ[0, hq]) < 1e-6
+    for hk in range(h_kv):
+        gk, gv = oracle.backward_kv_head(q, k, v, do, 0.45, causal, 0, hk, row_chunk=2)
+        assert np.linalg.norm(gk - fK[0, hk]) / max(np.linalg.norm(fK[0, hk]), 1e-30) < 1e-6
+        assert np.linalg.norm(gv - fV[0, hk]) / max(np.linalg.norm(fV[0, hk]), 1e-30) < 1e-6
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_invariants(causal):
+    h_q, h_kv = 4, 2
+    q, k, v, do = _rand(2, h_q, 7, 5), _rand(2, h_kv, 7, 5), _rand(2, h_kv, 7, 5), \
+        _rand(2, h_q, 7, 5)
+    dQ, dK, dV = oracle.backward(q, k, v, do, 0.3, causal)
+    # each row of dS sums to zero, so the keys' gradients sum to zero per KV head
+    np.testing.assert_allclose(dK.sum(axis=2), 0.0, atol=1e-12)
+    # each row of P sums to one, so Σ_j dV_j = Σ over the group's rows of dO
+    np.testing.assert_allclose(dV.sum(axis=2),
+                               do.reshape(2, h_kv, 2, 7, 5).sum(axis=(2, 3)), atol=1e-12)
+    # identical keys make P independent of Q, so dQ vanishes
+    kc = np.broadcast_to(k[:, :, :1], k.shape).copy()
+    dQc, _, _ = oracle.backward(q, kc, v, do, 0.3, causal)
+    np.testing.assert_allclose(dQc, 0.0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# E4M3
+# ---------------------------------------------------------------------------
+
+def test_e4m3_table_matches_torch_cast_for_all_codes():
+    tab = oracle.e4m3_decode_table()
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert list(np.nonzero(nan)[0]) == [0x7F, 0xFF]
+    np.testing.assert_array_equal(np.isnan(tab), nan)
+    np.testing.assert_array_equal(tab[~nan], ref[~nan])
+
+
+def test_e4m3_special_values():
+    tab = oracle.e4m3_decode_table()
+    assert tab[0x7E] == 448.0 and tab[0xFE] == -448.0
+    assert tab[0x01] == 2.0 ** -9 and tab[0x08] == 2.0 ** -6 and tab[0x38] == 1.0
+    assert tab[0x80] == 0.0 and math.copysign(1, tab[0x80]) == -1.0
+
+
+def test_e4m3_quantisation_round_trip_within_half_ulp():
+    x = torch.randn(4096, generator=torch.Generator().manual_seed(0))
+    q8, descale = quantize_e4m3(x)
+    y = oracle.to_f64(q8, descale)
+    scale = 1.0 / descale
+    xs = x.double().numpy() * scale
+    ys = y * scale
+    # spacing of E4M3 near |x|: 2**(floor(log2|x|) - 3) for normals, 2**-9 below 2**-6
+    e = np.floor(np.log2(np.maximum(np.abs(xs), 2.0 ** -6)))
+    ulp = 2.0 ** (e - 3)
+    assert (np.abs(ys - xs) <= ulp / 2 + 1e-12).all()
+    assert np.abs(oracle.to_f64(q8)).max() <= 448.0
