@@ -1,0 +1,174 @@
+"""Python binding of the GB300 fused SDPA library (``include/sdpa.h``).
+
+Argument marshalling only: every step of the attention computation runs in the CUDA
+kernels of ``libsdpa_gb300.so``.  PyTorch supplies device memory and the current stream.
+The binding keeps the C names: :func:`sdpa_fwd`, :func:`sdpa_bwd`,
+:func:`sdpa_workspace_size`, :func:`sdpa_last_error_string`, :func:`sdpa_device_error`.
+
+Importing this package loads the library and raises ``ImportError`` if it has not been
+built (``python -m attention_flashattention_sdpa_gb300._build``); there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+from typing import Optional
+
+__all__ = [
+    "SdpaError", "Strides", "Problem", "lib", "LIB_PATH", "dtype_code", "make_problem",
+    "sdpa_workspace_size", "sdpa_fwd", "sdpa_bwd", "sdpa_last_error_string",
+    "sdpa_device_error", "sdpa_version", "STATUS",
+]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsdpa_gb300.so")
+
+STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTED",
+          3: "SDPA_ERR_LAYOUT", 4: "SDPA_ERR_WORKSPACE", 5: "SDPA_ERR_CUDA",
+          6: "SDPA_ERR_TIMEOUT"}
+
+DTYPE_F16, DTYPE_BF16, DTYPE_E4M3 = 0, 1, 2
+
+
+class SdpaError(RuntimeError):
+    """A non-OK status from the library; ``status`` holds the code."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class Strides(ctypes.Structure):
+    _fields_ = [("b", ctypes.c_int64), ("h", ctypes.c_int64), ("s", ctypes.c_int64),
+                ("d", ctypes.c_int64)]
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [
+        ("b", ctypes.c_int32), ("h_q", ctypes.c_int32), ("h_kv", ctypes.c_int32),
+        ("s_q", ctypes.c_int32), ("s_kv", ctypes.c_int32), ("d", ctypes.c_int32),
+        ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+        ("attn_scale", ctypes.c_float), ("causal", ctypes.c_int32),
+        ("q", Strides), ("k", Strides), ("v", Strides), ("o", Strides),
+        ("dout", Strides), ("dq", Strides), ("dk", Strides), ("dv", Strides),
+        ("descale_q", ctypes.c_void_p), ("descale_k", ctypes.c_void_p),
+        ("descale_v", ctypes.c_void_p),
+    ]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -m attention_flashattention_sdpa_gb300._build` (nvcc, sm_103a)")
+    L = ctypes.CDLL(LIB_PATH)
+    P, VP, SZ = ctypes.POINTER(Problem), ctypes.c_void_p, ctypes.c_size_t
+    L.sdpa_workspace_size.argtypes = [P, ctypes.c_int, ctypes.POINTER(SZ)]
+    L.sdpa_workspace_size.restype = ctypes.c_int
+    L.sdpa_fwd.argtypes = [P, VP, VP, VP, VP, VP, VP, SZ, VP]
+    L.sdpa_fwd.restype = ctypes.c_int
+    L.sdpa_bwd.argtypes = [P, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]
+    L.sdpa_bwd.restype = ctypes.c_int
+    L.sdpa_last_error_string.argtypes = []
+    L.sdpa_last_error_string.restype = ctypes.c_char_p
+    L.sdpa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    L.sdpa_device_error.restype = ctypes.c_int
+    L.sdpa_version.argtypes = []
+    L.sdpa_version.restype = ctypes.c_int
+    L.sdpa_problem_struct_size.argtypes = []
+    L.sdpa_problem_struct_size.restype = SZ
+    if L.sdpa_problem_struct_size() != ctypes.sizeof(Problem):
+        raise ImportError("sdpa_problem_t layout mismatch between the library and the binding")
+    return L
+
+
+lib = _load()
+
+
+def sdpa_last_error_string() -> str:
+    return lib.sdpa_last_error_string().decode()
+
+
+def sdpa_version() -> int:
+    return lib.sdpa_version()
+
+
+def _check(status: int):
+    if status != 0:
+        raise SdpaError(status, sdpa_last_error_string())
+
+
+def dtype_code(t) -> int:
+    import torch
+    return {torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16,
+            torch.float8_e4m3fn: DTYPE_E4M3}[t.dtype]
+
+
+def _strides(t) -> Strides:
+    if t is None:
+        return Strides(0, 0, 0, 1)
+    if t.dim() != 4:
+        raise ValueError("tensors are logical [b, h, s, d] views")
+    return Strides(*t.stride())
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def make_problem(q, k, v, o=None, *, attn_scale: Optional[float] = None, causal: bool = False,
+                 dout=None, dq=None, dk=None, dv=None, descale_q=None, descale_k=None,
+                 descale_v=None) -> Problem:
+    """Fills an sdpa_problem_t from logical [b, h, s, d] torch tensors (no copies)."""
+    b, h_q, s_q, d = q.shape
+    h_kv, s_kv = k.shape[1], k.shape[2]
+    p = Problem()
+    p.b, p.h_q, p.h_kv, p.s_q, p.s_kv, p.d = b, h_q, h_kv, s_q, s_kv, d
+    p.in_dtype = dtype_code(q)
+    p.out_dtype = dtype_code(o) if o is not None else p.in_dtype
+    p.attn_scale = (1.0 / math.sqrt(d)) if attn_scale is None else float(attn_scale)
+    p.causal = 1 if causal else 0
+    p.q, p.k, p.v, p.o = _strides(q), _strides(k), _strides(v), _strides(o)
+    p.dout, p.dq, p.dk, p.dv = _strides(dout), _strides(dq), _strides(dk), _strides(dv)
+    p.descale_q, p.descale_k, p.descale_v = _ptr(descale_q), _ptr(descale_k), _ptr(descale_v)
+    return p
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return int(stream)
+
+
+def sdpa_workspace_size(problem: Problem, is_backward: bool) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib.sdpa_workspace_size(ctypes.byref(problem), 1 if is_backward else 0, ctypes.byref(n)))
+    return n.value
+
+
+def sdpa_fwd(q, k, v, o, lse=None, *, attn_scale: Optional[float] = None, causal: bool = False,
+             descale_q=None, descale_k=None, descale_v=None, workspace=None, stream=None) -> None:
+    """O (and LSE when ``lse`` is given: fp32 [b, h_q, s_q] contiguous) from Q, K, V."""
+    p = make_problem(q, k, v, o, attn_scale=attn_scale, causal=causal, descale_q=descale_q,
+                     descale_k=descale_k, descale_v=descale_v)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.sdpa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+                        _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def sdpa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, *, attn_scale: Optional[float] = None,
+             causal: bool = False, stream=None) -> None:
+    """dQ, dK, dV (overwritten) for the incoming gradient ``dout``."""
+    p = make_problem(q, k, v, o, attn_scale=attn_scale, causal=causal, dout=dout, dq=dq, dk=dk,
+                     dv=dv)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.sdpa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def sdpa_device_error() -> int:
+    """Synchronises the device and returns (and clears) the kernels' error word."""
+    f = ctypes.c_uint32(0)
+    _check(lib.sdpa_device_error(ctypes.byref(f)))
+    return f.value

@@ -1,0 +1,336 @@
+// sdpa_api.cu — the C ABI declared in include/sdpa.h: argument validation, TMA tensor-map
+// construction over the caller's strides, workspace sizing and kernel dispatch.
+//
+// Shape of the interface follows the pages' SDPA node: Q, K, V, attn_scale by value, a
+// causal flag, an inference/training switch (here: lse == NULL or not), explicit dims and
+// strides, a workspace the caller queries and allocates, asynchronous execution, and
+// error codes with a last-error string [cuDNN 9 blog, SDPA walkthrough and error
+// reporting; cuDNN-in-Python post, graph build / workspace / execute].  Unsupported
+// requests return an error rather than falling back [attention codelab §6: the cuDNN path
+// raises instead of silently using another implementation].
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/sdpa.h"
+#include "sdpa_internal.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+sdpa_status_t fail(sdpa_status_t st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+sdpa_status_t ok() {
+  g_last_error.clear();
+  return SDPA_OK;
+}
+
+int log_level() {
+  static int lvl = [] {
+    const char* s = getenv("SDPA_LOG_LEVEL");
+    return s ? atoi(s) : 0;
+  }();
+  return lvl;
+}
+
+bool debug_sync() {
+  static bool v = [] {
+    const char* s = getenv("SDPA_DEBUG_SYNC");
+    return s && atoi(s) != 0;
+  }();
+  return v;
+}
+
+int elem_bytes(int dt) { return dt == SDPA_DTYPE_E4M3 ? 1 : 2; }
+
+bool valid_dtype(int dt) {
+  return dt == SDPA_DTYPE_F16 || dt == SDPA_DTYPE_BF16 || dt == SDPA_DTYPE_E4M3;
+}
+
+// ---------------------------------------------------------------------------
+// tensor maps
+// ---------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+CUtensorMapDataType map_dtype(int dt) {
+  switch (dt) {
+    case SDPA_DTYPE_F16: return CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    case SDPA_DTYPE_BF16: return CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    default: return CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  }
+}
+
+// Checks that a logical [b][h][s][d] view can be handed to the TMA unit.
+sdpa_status_t check_view(const char* name, const void* ptr, const sdpa_strides_t& st, int b, int h,
+                         int s, int d, int es) {
+  if (ptr == nullptr) return fail(SDPA_ERR_INVALID_ARG, "%s: null pointer", name);
+  if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0)
+    return fail(SDPA_ERR_LAYOUT, "%s: base address must be 16-byte aligned", name);
+  if (st.d != 1) return fail(SDPA_ERR_LAYOUT, "%s: innermost (d) stride must be 1, got %lld", name,
+                             (long long)st.d);
+  const int64_t strides[3] = {st.s, st.h, st.b};
+  const int64_t sizes[3] = {s, h, b};
+  const char* nm[3] = {"s", "h", "b"};
+  for (int i = 0; i < 3; ++i) {
+    if (sizes[i] == 1) continue;  // stride of a unit dimension is never used
+    if (strides[i] <= 0)
+      return fail(SDPA_ERR_LAYOUT, "%s: stride_%s must be positive, got %lld", name, nm[i],
+                  (long long)strides[i]);
+    if ((strides[i] * es) % 16 != 0)
+      return fail(SDPA_ERR_LAYOUT, "%s: stride_%s * element size must be a multiple of 16 bytes",
+                  name, nm[i]);
+    if (strides[i] * es >= (int64_t(1) << 40))
+      return fail(SDPA_ERR_LAYOUT, "%s: stride_%s too large for the TMA unit", name, nm[i]);
+  }
+  (void)d;
+  return SDPA_OK;
+}
+
+sdpa_status_t make_map(CUtensorMap* map, const char* name, const void* ptr, const sdpa_strides_t& st,
+                       int b, int h, int s, int d, int dt, int box_rows) {
+  auto fn = encode_fn();
+  if (fn == nullptr)
+    return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the CUDA driver");
+  const int es = elem_bytes(dt);
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)s, (cuuint64_t)h, (cuuint64_t)b};
+  // A unit dimension's stride is irrelevant; give it a legal value.
+  const int64_t fallback = (int64_t)d * es * s * h;
+  int64_t sb[3] = {st.s * es, st.h * es, st.b * es};
+  int64_t sizes[3] = {s, h, b};
+  for (int i = 0; i < 3; ++i)
+    if (sizes[i] == 1) sb[i] = ((fallback + 15) / 16) * 16;
+  cuuint64_t strides[3] = {(cuuint64_t)sb[0], (cuuint64_t)sb[1], (cuuint64_t)sb[2]};
+  cuuint32_t box[4] = {(cuuint32_t)(128 / es), (cuuint32_t)box_rows, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, map_dtype(dt), 4, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(SDPA_ERR_LAYOUT, "%s: cuTensorMapEncodeTiled rejected the view (CUresult %d)",
+                name, (int)r);
+  return SDPA_OK;
+}
+
+sdpa_status_t check_problem(const sdpa_problem_t* p, bool backward) {
+  if (p == nullptr) return fail(SDPA_ERR_INVALID_ARG, "problem descriptor is NULL");
+  if (p->b < 1 || p->h_q < 1 || p->h_kv < 1 || p->s_q < 1 || p->s_kv < 1 || p->d < 1)
+    return fail(SDPA_ERR_INVALID_ARG,
+                "sizes must be >= 1 (b=%d h_q=%d h_kv=%d s_q=%d s_kv=%d d=%d)", p->b, p->h_q,
+                p->h_kv, p->s_q, p->s_kv, p->d);
+  if (p->h_q % p->h_kv != 0)
+    return fail(SDPA_ERR_INVALID_ARG, "h_q (%d) must be a multiple of h_kv (%d)", p->h_q, p->h_kv);
+  if (p->d != 64 && p->d != 128 && p->d != 256)
+    return fail(SDPA_ERR_UNSUPPORTED, "head dim %d not supported (64, 128 or 256)", p->d);
+  if (!valid_dtype(p->in_dtype)) return fail(SDPA_ERR_INVALID_ARG, "unknown in_dtype %d", p->in_dtype);
+  if (!valid_dtype(p->out_dtype))
+    return fail(SDPA_ERR_INVALID_ARG, "unknown out_dtype %d", p->out_dtype);
+  if (p->causal != 0 && p->causal != 1)
+    return fail(SDPA_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", p->causal);
+  if (!std::isfinite(p->attn_scale))
+    return fail(SDPA_ERR_INVALID_ARG, "attn_scale must be finite");
+  if (p->in_dtype == SDPA_DTYPE_E4M3) {
+    if (backward)
+      return fail(SDPA_ERR_UNSUPPORTED, "the backward pass takes F16 or BF16 inputs, not E4M3");
+    if (p->out_dtype == SDPA_DTYPE_E4M3)
+      return fail(SDPA_ERR_UNSUPPORTED, "E4M3 inputs give a BF16 or F16 output");
+    if (p->d == 64) return fail(SDPA_ERR_UNSUPPORTED, "E4M3 forward supports d = 128 or 256");
+    if (!p->descale_q || !p->descale_k || !p->descale_v)
+      return fail(SDPA_ERR_INVALID_ARG, "E4M3 inputs need descale_q, descale_k and descale_v");
+  } else if (p->out_dtype != p->in_dtype) {
+    return fail(SDPA_ERR_UNSUPPORTED, "F16/BF16 inputs give an output of the same dtype");
+  }
+  // Row/column counts index int32 coordinates of the TMA unit.
+  if ((int64_t)p->b * p->h_q * p->s_q >= (int64_t(1) << 31))
+    return fail(SDPA_ERR_UNSUPPORTED, "b*h_q*s_q too large");
+  return SDPA_OK;
+}
+
+float scale_log2_of(float attn_scale) {
+  float a = std::fabs(attn_scale);
+  if (a == 0.f) a = 1e-30f;  // exact zero scale: every score maps to exp2(0) = 1
+  return a * 1.4426950408889634f;
+}
+
+sdpa_status_t finish_launch(cudaError_t e, cudaStream_t stream, const char* what) {
+  if (e != cudaSuccess)
+    return fail(SDPA_ERR_CUDA, "%s launch failed: %s", what, cudaGetErrorString(e));
+  if (debug_sync()) {
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    uint32_t flags = sdpa::fwd_take_device_error() | sdpa::bwd_take_device_error();
+    if (flags) return fail(SDPA_ERR_TIMEOUT, "%s: a bounded device wait gave up (flags=%u)", what, flags);
+  }
+  return ok();
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+}  // namespace
+
+extern "C" {
+
+sdpa_status_t sdpa_workspace_size(const sdpa_problem_t* p, int is_backward, size_t* bytes) {
+  if (bytes == nullptr) return fail(SDPA_ERR_INVALID_ARG, "bytes is NULL");
+  sdpa_status_t st = check_problem(p, is_backward != 0);
+  if (st != SDPA_OK) return st;
+  *bytes = is_backward ? sdpa::bwd_workspace_bytes(p->b, p->h_q, p->s_q, p->d) : 0;
+  return ok();
+}
+
+sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const void* k, const void* v, void* o,
+                       float* lse, void* workspace, size_t workspace_bytes, void* stream_) {
+  (void)workspace;
+  (void)workspace_bytes;
+  sdpa_status_t st = check_problem(p, false);
+  if (st != SDPA_OK) return st;
+  const int es = elem_bytes(p->in_dtype);
+  if ((st = check_view("q", q, p->q, p->b, p->h_q, p->s_q, p->d, es)) != SDPA_OK) return st;
+  if ((st = check_view("k", k, p->k, p->b, p->h_kv, p->s_kv, p->d, es)) != SDPA_OK) return st;
+  if ((st = check_view("v", v, p->v, p->b, p->h_kv, p->s_kv, p->d, es)) != SDPA_OK) return st;
+  if ((st = check_view("o", o, p->o, p->b, p->h_q, p->s_q, p->d, 2)) != SDPA_OK) return st;
+  if (lse != nullptr && reinterpret_cast<uintptr_t>(lse) % 4 != 0)
+    return fail(SDPA_ERR_LAYOUT, "lse must be 4-byte aligned");
+
+  sdpa::FwdParams prm;
+  memset(&prm, 0, sizeof(prm));
+  if ((st = make_map(&prm.tm_q, "q", q, p->q, p->b, p->h_q, p->s_q, p->d, p->in_dtype, 128)) != SDPA_OK) return st;
+  if ((st = make_map(&prm.tm_k, "k", k, p->k, p->b, p->h_kv, p->s_kv, p->d, p->in_dtype, 128)) != SDPA_OK) return st;
+  if ((st = make_map(&prm.tm_v, "v", v, p->v, p->b, p->h_kv, p->s_kv, p->d, p->in_dtype, 128)) != SDPA_OK) return st;
+  if ((st = make_map(&prm.tm_o, "o", o, p->o, p->b, p->h_q, p->s_q, p->d, p->out_dtype, 128)) != SDPA_OK) return st;
+  prm.lse = lse;
+  prm.descale_q = p->descale_q;
+  prm.descale_k = p->descale_k;
+  prm.descale_v = p->descale_v;
+  prm.b = p->b;
+  prm.h_q = p->h_q;
+  prm.h_kv = p->h_kv;
+  prm.s_q = p->s_q;
+  prm.s_kv = p->s_kv;
+  prm.group = p->h_q / p->h_kv;
+  prm.causal = p->causal;
+  const int rows_per_cta = 128 * sdpa::fwd_q_tiles(p->d, p->in_dtype);
+  prm.num_m_blocks = (p->s_q + rows_per_cta - 1) / rows_per_cta;
+  prm.scale_log2 = scale_log2_of(p->attn_scale);
+  prm.negate_scores = p->attn_scale < 0.f ? 1 : 0;
+  if ((int64_t)p->b * p->h_q > 0x7fffffff || prm.num_m_blocks > 65535)
+    return fail(SDPA_ERR_UNSUPPORTED, "grid too large");
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (log_level() >= 1)
+    fprintf(stderr, "[sdpa] fwd b=%d h_q=%d h_kv=%d s_q=%d s_kv=%d d=%d dt=%d causal=%d grid=(%d,%d)\n",
+            p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d, p->in_dtype, p->causal, p->b * p->h_q,
+            prm.num_m_blocks);
+  cudaError_t e = sdpa::launch_fwd(prm, p->d, p->in_dtype, p->out_dtype, stream);
+  return finish_launch(e, stream, "sdpa_fwd");
+}
+
+sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, const void* v,
+                       const void* o, const void* dout, const float* lse, void* dq, void* dk,
+                       void* dv, void* workspace, size_t workspace_bytes, void* stream_) {
+  sdpa_status_t st = check_problem(p, true);
+  if (st != SDPA_OK) return st;
+  if (p->d == 256)
+    return fail(SDPA_ERR_UNSUPPORTED, "the backward pass supports d = 64 or 128");
+  const int es = 2;
+  if ((st = check_view("q", q, p->q, p->b, p->h_q, p->s_q, p->d, es)) != SDPA_OK) return st;
+  if ((st = check_view("k", k, p->k, p->b, p->h_kv, p->s_kv, p->d, es)) != SDPA_OK) return st;
+  if ((st = check_view("v", v, p->v, p->b, p->h_kv, p->s_kv, p->d, es)) != SDPA_OK) return st;
+  if ((st = check_view("o", o, p->o, p->b, p->h_q, p->s_q, p->d, es)) != SDPA_OK) return st;
+  if ((st = check_view("dout", dout, p->dout, p->b, p->h_q, p->s_q, p->d, es)) != SDPA_OK) return st;
+  if ((st = check_view("dq", dq, p->dq, p->b, p->h_q, p->s_q, p->d, es)) != SDPA_OK) return st;
+  if ((st = check_view("dk", dk, p->dk, p->b, p->h_kv, p->s_kv, p->d, es)) != SDPA_OK) return st;
+  if ((st = check_view("dv", dv, p->dv, p->b, p->h_kv, p->s_kv, p->d, es)) != SDPA_OK) return st;
+  if (lse == nullptr) return fail(SDPA_ERR_INVALID_ARG, "lse: null pointer (the backward pass needs the forward statistics)");
+  if (reinterpret_cast<uintptr_t>(lse) % 4 != 0) return fail(SDPA_ERR_LAYOUT, "lse must be 4-byte aligned");
+  const size_t need = sdpa::bwd_workspace_bytes(p->b, p->h_q, p->s_q, p->d);
+  if (workspace == nullptr || workspace_bytes < need)
+    return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given%s", need,
+                workspace_bytes, workspace ? "" : " (NULL)");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+    return fail(SDPA_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+
+  sdpa::BwdParams prm;
+  memset(&prm, 0, sizeof(prm));
+  if ((st = make_map(&prm.tm_q, "q", q, p->q, p->b, p->h_q, p->s_q, p->d, p->in_dtype, 128)) != SDPA_OK) return st;
+  if ((st = make_map(&prm.tm_k, "k", k, p->k, p->b, p->h_kv, p->s_kv, p->d, p->in_dtype, 128)) != SDPA_OK) return st;
+  if ((st = make_map(&prm.tm_v, "v", v, p->v, p->b, p->h_kv, p->s_kv, p->d, p->in_dtype, 128)) != SDPA_OK) return st;
+  if ((st = make_map(&prm.tm_do, "dout", dout, p->dout, p->b, p->h_q, p->s_q, p->d, p->in_dtype, 128)) != SDPA_OK) return st;
+  if ((st = make_map(&prm.tm_dk, "dk", dk, p->dk, p->b, p->h_kv, p->s_kv, p->d, p->out_dtype, 128)) != SDPA_OK) return st;
+  if ((st = make_map(&prm.tm_dv, "dv", dv, p->dv, p->b, p->h_kv, p->s_kv, p->d, p->out_dtype, 128)) != SDPA_OK) return st;
+  const int s_q_pad = (p->s_q + 127) / 128 * 128;
+  const size_t acc_bytes = align256((size_t)p->b * p->h_q * s_q_pad * p->d * 4);
+  const size_t vec_bytes = align256((size_t)p->b * p->h_q * s_q_pad * 4);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  prm.o = o;
+  prm.dout = dout;
+  prm.lse = lse;
+  prm.dq = dq;
+  prm.dq_acc = reinterpret_cast<float*>(ws);
+  prm.delta = reinterpret_cast<float*>(ws + acc_bytes);
+  prm.lse2 = reinterpret_cast<float*>(ws + acc_bytes + vec_bytes);
+  prm.o_sb = p->o.b; prm.o_sh = p->o.h; prm.o_ss = p->o.s;
+  prm.do_sb = p->dout.b; prm.do_sh = p->dout.h; prm.do_ss = p->dout.s;
+  prm.dq_sb = p->dq.b; prm.dq_sh = p->dq.h; prm.dq_ss = p->dq.s;
+  prm.b = p->b;
+  prm.h_q = p->h_q;
+  prm.h_kv = p->h_kv;
+  prm.s_q = p->s_q;
+  prm.s_kv = p->s_kv;
+  prm.d = p->d;
+  prm.group = p->h_q / p->h_kv;
+  prm.causal = p->causal;
+  prm.s_q_pad = s_q_pad;
+  prm.scale = p->attn_scale;
+  prm.scale_log2 = p->attn_scale * 1.4426950408889634f;
+  if ((s_q_pad / 128) > 65535 || (p->s_kv + 127) / 128 > 65535)
+    return fail(SDPA_ERR_UNSUPPORTED, "grid too large");
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  if (log_level() >= 1)
+    fprintf(stderr, "[sdpa] bwd b=%d h_q=%d h_kv=%d s_q=%d s_kv=%d d=%d dt=%d causal=%d ws=%zu\n",
+            p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d, p->in_dtype, p->causal, need);
+  cudaError_t e = sdpa::launch_bwd(prm, p->in_dtype, stream);
+  return finish_launch(e, stream, "sdpa_bwd");
+}
+
+const char* sdpa_last_error_string(void) { return g_last_error.c_str(); }
+
+sdpa_status_t sdpa_device_error(uint32_t* flags) {
+  if (flags == nullptr) return fail(SDPA_ERR_INVALID_ARG, "flags is NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "synchronize failed: %s", cudaGetErrorString(e));
+  *flags = sdpa::fwd_take_device_error() | sdpa::bwd_take_device_error();
+  return ok();
+}
+
+int sdpa_version(void) { return 100; }
+
+size_t sdpa_problem_struct_size(void) { return sizeof(sdpa_problem_t); }
+
+}  // extern "C"

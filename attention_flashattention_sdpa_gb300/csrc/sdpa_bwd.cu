@@ -1,0 +1,564 @@
+// sdpa_bwd.cu — SDPA backward pass for sm_103a: dQ, dK, dV from Q, K, V, O, dO and the
+// per-row LSE kept by the forward pass.
+//
+// The pages show that a backward graph exists next to the forward one (cuDNN 9 blog,
+// "SDPA performance", Fig. 2 "forward + backward"; "SDPA as a cuDNN graph": backward
+// graphs offer the same flexibility) but print no formula; the derivative used here is
+// the analytic one of O = softmax(scale·QKᵀ + mask)·V:
+//     P = exp(scale·QKᵀ − LSE)            (recomputed from the forward's statistics)
+//     dV = Pᵀ·dO,  dP = dO·Vᵀ,  Delta_i = Σ_d dO_id·O_id  (= Σ_j P_ij·dP_ij)
+//     dS = P ∘ (dP − Delta),  dQ = scale·dS·K,  dK = scale·dSᵀ·Q
+// with dK, dV summed over the query heads of each KV group.
+//
+// Three launches (the pages note an engine may be "a small set of cooperating kernels"):
+//   1. bwd_pre:   Delta_i, LSE_i·log2(e) and a zeroed fp32 dQ accumulator (workspace).
+//   2. bwd_main:  one CTA per (batch, KV head, 128-row KV block); K and V stay in shared
+//                 memory while the CTA walks every (query head of the group, 128-row query
+//                 block) it can see.  Per step five tcgen05 MMAs (Sᵀ = K·Qᵀ, dPᵀ = V·dOᵀ,
+//                 dV += Pᵀ·dO, dK += dSᵀ·Q, dQ = dS·K) with dV and dK accumulating in TMEM
+//                 for the whole walk and dQ drained from TMEM into the fp32 accumulator with
+//                 vector atomics by a dedicated warpgroup.
+//   3. bwd_dq:    dQ = scale·accumulator, rounded to the output dtype in the caller's strides.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <type_traits>
+
+#include "ptx.cuh"
+#include "sdpa_internal.h"
+
+namespace sdpa {
+namespace {
+
+using namespace ptx;
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+__device__ __forceinline__ float to_f32(const __half v) { return __half2float(v); }
+__device__ __forceinline__ float to_f32(const __nv_bfloat16 v) { return __bfloat162float(v); }
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, int dt) {
+  if (dt == kBF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float2 unpack2(uint32_t u, int dt) {
+  if (dt == kBF16) {
+    __nv_bfloat162 h = *reinterpret_cast<__nv_bfloat162*>(&u);
+    return __bfloat1622float2(h);
+  }
+  __half2 h = *reinterpret_cast<__half2*>(&u);
+  return __half22float2(h);
+}
+
+__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b),
+               "f"(c), "f"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// 1. preprocess: Delta, LSE·log2 e, zeroed dQ accumulator
+// ---------------------------------------------------------------------------
+
+// One group of D/8 threads per row; each thread reads 8 elements (16 bytes) of O and dO.
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
+  constexpr int TPR = D / 8;              // threads per row
+  constexpr int ROWS = 256 / TPR;         // rows per block
+  const int bh = blockIdx.y;
+  const int bi = bh / p.h_q, hq = bh % p.h_q;
+  const int row = blockIdx.x * ROWS + threadIdx.x / TPR;
+  const int part = threadIdx.x % TPR;
+  float acc = 0.f;
+  const bool valid = row < p.s_q;
+  if (valid) {
+    const T* o = reinterpret_cast<const T*>(p.o) + bi * p.o_sb + hq * p.o_sh + row * p.o_ss + part * 8;
+    const T* g = reinterpret_cast<const T*>(p.dout) + bi * p.do_sb + hq * p.do_sh + row * p.do_ss + part * 8;
+    const uint4 ov = *reinterpret_cast<const uint4*>(o);
+    const uint4 gv = *reinterpret_cast<const uint4*>(g);
+    const T* oe = reinterpret_cast<const T*>(&ov);
+    const T* ge = reinterpret_cast<const T*>(&gv);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc += to_f32(oe[i]) * to_f32(ge[i]);
+  }
+#pragma unroll
+  for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  const int64_t vrow = static_cast<int64_t>(bh) * p.s_q_pad + row;
+  if (row < p.s_q_pad) {
+    float* dq = p.dq_acc + vrow * D + part * 8;
+    reinterpret_cast<float4*>(dq)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    reinterpret_cast<float4*>(dq)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (part == 0) {
+      p.delta[vrow] = valid ? acc : 0.f;
+      p.lse2[vrow] = valid ? p.lse[static_cast<int64_t>(bh) * p.s_q + row] * kLog2e : INFINITY;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. dQ = scale * accumulator, in the output dtype and strides
+// ---------------------------------------------------------------------------
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdParams p) {
+  constexpr int TPR = D / 8;
+  constexpr int ROWS = 256 / TPR;
+  const int bh = blockIdx.y;
+  const int bi = bh / p.h_q, hq = bh % p.h_q;
+  const int row = blockIdx.x * ROWS + threadIdx.x / TPR;
+  const int part = threadIdx.x % TPR;
+  if (row >= p.s_q) return;
+  const float* src = p.dq_acc + (static_cast<int64_t>(bh) * p.s_q_pad + row) * D + part * 8;
+  const float4 a = reinterpret_cast<const float4*>(src)[0];
+  const float4 b = reinterpret_cast<const float4*>(src)[1];
+  const float s = p.scale;
+  const int dt = sizeof(T) == 2 && std::is_same<T, __nv_bfloat16>::value ? kBF16 : kF16;
+  uint4 w;
+  w.x = pack2(a.x * s, a.y * s, dt);
+  w.y = pack2(a.z * s, a.w * s, dt);
+  w.z = pack2(b.x * s, b.y * s, dt);
+  w.w = pack2(b.z * s, b.w * s, dt);
+  T* dst = reinterpret_cast<T*>(p.dq) + bi * p.dq_sb + hq * p.dq_sh + row * p.dq_ss + part * 8;
+  *reinterpret_cast<uint4*>(dst) = w;
+}
+
+// ---------------------------------------------------------------------------
+// 2. main kernel
+// ---------------------------------------------------------------------------
+
+template <int D>
+struct BwdCfg {
+  static constexpr int TILE = kBlockM * D * 2;        // one 128-row tile of Q, K, V or dO
+  static constexpr int NCHUNK = D / 64;               // 128-byte chunks along d
+  static constexpr int NSLOT = 4;                     // Q / dO ring
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = TILE;
+  static constexpr int OFF_RING = 2 * TILE;
+  static constexpr int OFF_DS = OFF_RING + NSLOT * TILE;
+  static constexpr int DS_BYTES = kBlockM * kBlockN * 2;
+  static constexpr int OFF_VEC = OFF_DS + DS_BYTES;   // [2 buffers][LSE2, Delta][128] fp32
+  static constexpr int OFF_BAR = OFF_VEC + 2 * 2 * 128 * 4;
+  static constexpr int SMEM_BYTES = OFF_BAR + 512;
+  static constexpr int THREADS = 512;
+  static constexpr int KSTEPS_D = D / 16;             // MMAs over a d reduction
+  static constexpr int R_COL = 0;                     // regions R0 = [0,128), R1 = [128,256)
+  static constexpr int DV_COL = 256;
+  static constexpr int DK_COL = 256 + D;
+  static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+  static_assert(DK_COL + D <= 512, "TMEM budget");
+};
+
+struct alignas(8) BwdBarriers {
+  uint64_t kv_full;
+  uint64_t ring_full[4];
+  uint64_t ring_empty[4];
+  uint64_t s_full[2];
+  uint64_t dp_full[2];
+  uint64_t p_full[2];
+  uint64_t ds_full[2];
+  uint64_t dq_full[2];
+  uint64_t dq_free[2];
+  uint64_t acc_full;
+  uint64_t drain;
+  uint64_t epi_ready[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Query blocks visible to KV block j (top-left causal: query row >= key row).
+__device__ __forceinline__ int first_q_block(const BwdParams& p, int j) {
+  return p.causal ? j : 0;
+}
+
+template <int D, int DT>
+__global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant__ BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  BwdBarriers& bars = *reinterpret_cast<BwdBarriers*>(smem + C::OFF_BAR);
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sRing = smem + C::OFF_RING;
+  uint8_t* sDS = smem + C::OFF_DS;
+  float* sVec = reinterpret_cast<float*>(smem + C::OFF_VEC);
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+  const int bhk = blockIdx.x;
+  const int bi = bhk / p.h_kv;
+  const int hk = bhk % p.h_kv;
+  const int j = blockIdx.y;                                 // KV block
+  const int n_qb = (p.s_q + kBlockM - 1) / kBlockM;
+  const int q_first = first_q_block(p, j);
+  const int per_head = q_first < n_qb ? n_qb - q_first : 0;
+  const int n_iter = per_head * p.group;
+
+  // The 128-byte swizzle of every tile assumes a 1024-byte aligned base (the budget leaves
+  // no room for manual alignment).  If that ever fails, report it and do nothing.
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(&g_device_error, kErrSmemAlign);
+    return;
+  }
+  if (threadIdx.x == 0) {
+    mbar_init(&bars.kv_full, 1);
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bars.ring_full[s], 1);
+      mbar_init(&bars.ring_empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars.s_full[b], 1);
+      mbar_init(&bars.dp_full[b], 1);
+      mbar_init(&bars.dq_full[b], 1);
+      mbar_init(&bars.p_full[b], 256);
+      mbar_init(&bars.ds_full[b], 256);
+      mbar_init(&bars.dq_free[b], 128);
+    }
+    mbar_init(&bars.acc_full, 1);
+    mbar_init(&bars.drain, 1);
+    mbar_init(&bars.epi_ready[0], 128);
+    mbar_init(&bars.epi_ready[1], 128);
+    bars.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  volatile int* abort_flag = &bars.abort;
+
+  // iteration n -> (query head, query block)
+  auto iter_head = [&](int n) { return hk * p.group + n / per_head; };
+  auto iter_qblk = [&](int n) { return q_first + n % per_head; };
+
+  if (warp == 0) {
+    // ================================ TMA producer ====================================
+    if (elect_one_sync()) {
+      mbar_arrive_expect_tx(&bars.kv_full, 2 * C::TILE);
+      for (int c = 0; c < C::NCHUNK; ++c) {
+        tma_load_4d(sK + c * 16384, &p.tm_k, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
+        tma_load_4d(sV + c * 16384, &p.tm_v, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
+      }
+      int it = 0;
+      bool ok = true;
+      for (int n = 0; n < n_iter && ok; ++n) {
+        const int hq = iter_head(n), qb = iter_qblk(n);
+        const int64_t vrow = (static_cast<int64_t>(bi) * p.h_q + hq) * p.s_q_pad + qb * kBlockM;
+        for (int which = 0; which < 2 && ok; ++which) {
+          const int slot = it % C::NSLOT;
+          if (!mbar_wait(&bars.ring_empty[slot], ((it / C::NSLOT) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&bars.ring_full[slot], C::TILE + 512);
+          const CUtensorMap* map = which == 0 ? &p.tm_q : &p.tm_do;
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_4d(sRing + slot * C::TILE + c * 16384, map, &bars.ring_full[slot], c * 64,
+                        qb * kBlockM, hq, bi);
+          const float* vsrc = (which == 0 ? p.lse2 : p.delta) + vrow;
+          bulk_load(sVec + ((n & 1) * 2 + which) * 128, vsrc, 512, &bars.ring_full[slot]);
+          ++it;
+        }
+      }
+      if (!ok || *abort_flag) {
+        // Let copies already issued land before the CTA's shared memory is released.
+        mbar_wait_drain(&bars.kv_full, 0);
+        for (int k = (it > C::NSLOT ? it - C::NSLOT : 0); k < it; ++k)
+          mbar_wait_drain(&bars.ring_full[k % C::NSLOT], (k / C::NSLOT) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ================================ MMA issuer ======================================
+    if (elect_one_sync()) {
+      const uint32_t fmt = (DT == kBF16) ? 1u : 0u;
+      const uint32_t idesc_sq = make_idesc(fmt, 128, 128, false, false);     // Sᵀ, dPᵀ
+      const uint32_t idesc_acc = make_idesc(fmt, 128, D, false, true);       // dV, dK
+      const uint32_t idesc_dq = make_idesc(fmt, 128, D, true, true);         // dQ
+      const uint32_t kA = smem_u32(sK), vA = smem_u32(sV), dsA = smem_u32(sDS);
+      bool ok = mbar_wait(&bars.kv_full, 0, abort_flag);
+      tc_fence_after();
+      int it = 0;
+      for (int n = 0; n < n_iter && ok; ++n) {
+        const int b = n & 1;
+        const uint32_t par = (n >> 1) & 1;
+        const uint32_t X = tmem + C::R_COL + b * 128;
+        const uint32_t Y = tmem + C::R_COL + (b ^ 1) * 128;
+        // ---- Sᵀ = K·Qᵀ ----
+        const int qslot = it % C::NSLOT;
+        if (!mbar_wait(&bars.ring_full[qslot], (it / C::NSLOT) & 1, abort_flag)) { ok = false; break; }
+        ++it;
+        tc_fence_after();
+        const uint32_t qB = smem_u32(sRing + qslot * C::TILE);
+#pragma unroll
+        for (int k = 0; k < C::KSTEPS_D; ++k) {
+          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+          mma_ss(X, make_sdesc_sw128(kA + off, 16, 1024), make_sdesc_sw128(qB + off, 16, 1024),
+                 idesc_sq, k > 0, false);
+        }
+        tc_commit(&bars.s_full[b]);
+        // ---- dPᵀ = V·dOᵀ (into the region dQ of the previous step used) ----
+        const int gslot = it % C::NSLOT;
+        if (!mbar_wait(&bars.ring_full[gslot], (it / C::NSLOT) & 1, abort_flag)) { ok = false; break; }
+        ++it;
+        if (n >= 1 && !mbar_wait(&bars.dq_free[b ^ 1], ((n - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t gB = smem_u32(sRing + gslot * C::TILE);
+#pragma unroll
+        for (int k = 0; k < C::KSTEPS_D; ++k) {
+          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+          mma_ss(Y, make_sdesc_sw128(vA + off, 16, 1024), make_sdesc_sw128(gB + off, 16, 1024),
+                 idesc_sq, k > 0, false);
+        }
+        tc_commit(&bars.dp_full[b]);
+        // ---- dV += Pᵀ·dO  (Pᵀ in TMEM: q 0..63 at X+0.., q 64..127 at X+64..) ----
+        if (!mbar_wait(&bars.p_full[b], par, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t a_col = (k < 4) ? k * 8 : 64 + (k - 4) * 8;
+          mma_ts(tmem + C::DV_COL, X + a_col, make_sdesc_sw128(gB + k * 2048, 16384, 1024),
+                 idesc_acc, (n > 0 || k > 0) ? 1u : 0u, false);
+        }
+        tc_commit(&bars.ring_empty[gslot]);
+        // ---- dK += dSᵀ·Q ; dQ = dS·K ----
+        if (!mbar_wait(&bars.ds_full[b], par, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t a_col = (k < 4) ? k * 8 : 64 + (k - 4) * 8;
+          mma_ts(tmem + C::DK_COL, Y + a_col, make_sdesc_sw128(qB + k * 2048, 16384, 1024),
+                 idesc_acc, (n > 0 || k > 0) ? 1u : 0u, false);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          mma_ss(X, make_sdesc_sw128(dsA + k * 2048, 16384, 1024),
+                 make_sdesc_sw128(kA + k * 2048, 16384, 1024), idesc_dq, k > 0, false);
+        }
+        tc_commit(&bars.dq_full[b]);
+        tc_commit(&bars.ring_empty[qslot]);
+      }
+      tc_commit(&bars.acc_full);
+      tc_commit(&bars.drain);
+      mbar_wait_drain(&bars.drain, 0);
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ============================ Pᵀ / dSᵀ (two column halves) ========================
+    const int h = (warp - 4) / 4;                         // query columns [64h, 64h+64)
+    const int quad = warp % 4;
+    const int r = quad * 32 + lane;                       // key row within the block (TMEM lane)
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int kv_row = j * kBlockN + r;
+    bool ok = true;
+    int it = 0;
+    for (int n = 0; n < n_iter; ++n) {
+      const int b = n & 1;
+      const uint32_t par = (n >> 1) & 1;
+      const uint32_t X = tmem + lane_off + C::R_COL + b * 128;
+      const uint32_t Y = tmem + lane_off + C::R_COL + (b ^ 1) * 128;
+      const int q0 = iter_qblk(n) * kBlockM + 64 * h;     // first query column of this half
+      const float* lse2 = sVec + (b * 2 + 0) * 128 + 64 * h;
+      const float* delta = sVec + (b * 2 + 1) * 128 + 64 * h;
+      // Pᵀ = exp2(Sᵀ·scale·log2e − LSE·log2e), masked where key > query
+      if (!mbar_wait_warp(&bars.ring_full[it % C::NSLOT], (it / C::NSLOT) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars.s_full[b], par, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sv[64];
+      tmem_ld32(X + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld32(X + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_ld_wait();
+      const bool need_mask = p.causal && (q0 < j * kBlockN + kBlockN - 1);
+      const int lim = kv_row - q0;                        // column c visible iff c >= lim
+      uint32_t pk[32];
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        float p0 = ex2(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lse2[c]));
+        float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), p.scale_log2, -lse2[c + 1]));
+        if (need_mask) {
+          if (c < lim) p0 = 0.f;
+          if (c + 1 < lim) p1 = 0.f;
+        }
+        pk[c / 2] = pack2(p0, p1, DT);
+      }
+      tmem_st32(X + 64 * h, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.p_full[b]);
+      ++it;
+      // dSᵀ = Pᵀ ∘ (dPᵀ − Delta)
+      if (!mbar_wait_warp(&bars.ring_full[it % C::NSLOT], (it / C::NSLOT) & 1, abort_flag)) { ok = false; break; }
+      ++it;
+      if (!mbar_wait_warp(&bars.dp_full[b], par, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      tmem_ld32(Y + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld32(Y + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_ld_wait();
+      uint32_t ds[32];
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        const float2 pp = unpack2(pk[c / 2], DT);
+        const float d0 = pp.x * (__uint_as_float(sv[c]) - delta[c]);
+        const float d1 = pp.y * (__uint_as_float(sv[c + 1]) - delta[c + 1]);
+        ds[c / 2] = pack2(d0, d1, DT);
+      }
+      tmem_st32(Y + 64 * h, ds);
+      // dS for the dQ MMA: query-major (MN-major A), chunk h holds query columns 64h..64h+63,
+      // key row r at byte r*128 with the 128-byte swizzle.  The previous step's dQ MMA must
+      // have finished reading the buffer.
+      if (n >= 1 && !mbar_wait_warp(&bars.dq_full[b ^ 1], ((n - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+      uint8_t* rowp = sDS + h * 16384 + r * 128;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        uint4 w = make_uint4(ds[u * 4 + 0], ds[u * 4 + 1], ds[u * 4 + 2], ds[u * 4 + 3]);
+        *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) = w;
+      }
+      fence_proxy_async_smem();
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.ds_full[b]);
+    }
+    // ---- epilogue: dV (h = 0) or dK (h = 1) through shared memory and a TMA store ----
+    ok = ok && mbar_wait_warp(&bars.acc_full, 0, abort_flag);
+    uint8_t* stage = sRing + h * C::TILE;
+    if (ok) {
+      tc_fence_after();
+      const uint32_t acc = tmem + lane_off + (h == 0 ? C::DV_COL : C::DK_COL);
+      const float mul = (h == 0) ? 1.f : p.scale;
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t v[64];
+        if (n_iter > 0) {
+          tmem_ld32(acc + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(acc + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) v[i] = 0u;
+        }
+        uint8_t* rowp = stage + c * 16384 + r * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint4 w;
+          w.x = pack2(__uint_as_float(v[u * 8 + 0]) * mul, __uint_as_float(v[u * 8 + 1]) * mul, DT);
+          w.y = pack2(__uint_as_float(v[u * 8 + 2]) * mul, __uint_as_float(v[u * 8 + 3]) * mul, DT);
+          w.z = pack2(__uint_as_float(v[u * 8 + 4]) * mul, __uint_as_float(v[u * 8 + 5]) * mul, DT);
+          w.w = pack2(__uint_as_float(v[u * 8 + 6]) * mul, __uint_as_float(v[u * 8 + 7]) * mul, DT);
+          *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) = w;
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    // Every thread of the warpgroup arrives exactly once, so the bounded wait below can only
+    // end by completion or timeout.
+    mbar_arrive(&bars.epi_ready[h]);
+    if (r == 0) {
+      const bool all_ok = mbar_wait(&bars.epi_ready[h], 0, abort_flag) && ok && !*abort_flag;
+      if (all_ok) {
+        const CUtensorMap* map = (h == 0) ? &p.tm_dv : &p.tm_dk;
+        for (int c = 0; c < D / 64; ++c)
+          tma_store_4d(map, stage + c * 16384, c * 64, j * kBlockN, hk, bi);
+        tma_store_commit();
+        tma_store_wait_read_all();
+      }
+    }
+  } else if (warp >= 12) {
+    // ============================ dQ drain: TMEM -> fp32 atomics ======================
+    const int quad = warp % 4;
+    const int r = quad * 32 + lane;                       // query row within the block
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    for (int n = 0; n < n_iter; ++n) {
+      const int b = n & 1;
+      if (!mbar_wait_warp(&bars.dq_full[b], (n >> 1) & 1, abort_flag)) break;
+      tc_fence_after();
+      const int hq = iter_head(n);
+      const int qrow = iter_qblk(n) * kBlockM + r;
+      float* dst = p.dq_acc + ((static_cast<int64_t>(bi) * p.h_q + hq) * p.s_q_pad + qrow) * D;
+      const uint32_t X = tmem + lane_off + C::R_COL + b * 128;
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(X + c * 32, v);
+        tmem_ld_wait();
+        if (qrow < p.s_q) {
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            red_add_v4(dst + c * 32 + u * 4, __uint_as_float(v[u * 4]), __uint_as_float(v[u * 4 + 1]),
+                       __uint_as_float(v[u * 4 + 2]), __uint_as_float(v[u * 4 + 3]));
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&bars.dq_free[b]);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int DT>
+cudaError_t launch_t(const BwdParams& p, cudaStream_t st) {
+  using T = typename std::conditional<DT == kBF16, __nv_bfloat16, __half>::type;
+  using C = BwdCfg<D>;
+  constexpr int ROWS = 256 / (D / 8);
+  const int bh = p.b * p.h_q;
+  dim3 gpre((p.s_q_pad + ROWS - 1) / ROWS, bh);
+  bwd_pre_kernel<T, D><<<gpre, 256, 0, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  auto kern = bwd_main_kernel<D, DT>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 gmain(p.b * p.h_kv, (p.s_kv + kBlockN - 1) / kBlockN);
+  kern<<<gmain, C::THREADS, C::SMEM_BYTES, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 gdq((p.s_q + ROWS - 1) / ROWS, bh);
+  bwd_dq_kernel<T, D><<<gdq, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(int b, int h_q, int s_q, int d) {
+  const size_t pad = static_cast<size_t>((s_q + 127) / 128) * 128;
+  auto a = [](size_t x) { return (x + 255) & ~size_t(255); };
+  return a(static_cast<size_t>(b) * h_q * pad * d * 4) + 2 * a(static_cast<size_t>(b) * h_q * pad * 4);
+}
+
+cudaError_t launch_bwd(const BwdParams& p, int dtype, cudaStream_t st) {
+  if (dtype == kBF16) {
+    if (p.d == 64) return launch_t<64, kBF16>(p, st);
+    if (p.d == 128) return launch_t<128, kBF16>(p, st);
+  } else if (dtype == kF16) {
+    if (p.d == 64) return launch_t<64, kF16>(p, st);
+    if (p.d == 128) return launch_t<128, kF16>(p, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+uint32_t bwd_take_device_error() {
+  uint32_t v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, ptx::g_device_error, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(ptx::g_device_error, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace sdpa

@@ -1,0 +1,501 @@
+// sdpa_fwd.cu — fused SDPA forward pass for sm_103a.
+//
+// Computes, per (batch, query head) and per 128-row query tile, O = softmax(scale·QKᵀ +
+// mask)·V and LSE = log Σ exp(scale·QKᵀ) without materialising the score matrix
+// [attention codelab, §1 "How attention works" and §5/§6 (the fused kernel never writes
+// the (B, N, T, S) weights); cuDNN 9 blog, "SDPA as a cuDNN graph", Fig. 4: BMM1 → scale →
+// causal mask → softmax → BMM2 fused into one engine].
+//
+// One CTA owns NQT query tiles (NQT = 2 for 16-bit inputs with d <= 128, else 1) of one
+// (batch, head) and walks the key/value blocks it can see:
+//   warp 0       TMA producer: Q tiles once, then K/V blocks through an NS-slot ring.
+//   warp 1       MMA issuer (one thread): S = Q·Kᵀ into TMEM, O += P·V with P read from
+//                TMEM, completion signalled with tcgen05.commit.
+//   warps 4..    one softmax warpgroup per Q tile; thread r owns query row r (TMEM lane r):
+//                online softmax in the exp2 domain with the scale folded in, P written back
+//                to TMEM over its own scores, O rescaled in TMEM only when the running max
+//                grows by more than a threshold, and the epilogue (O / l via a TMA store,
+//                LSE).
+// Causal: key blocks wholly above a tile's diagonal are never loaded; only blocks that cross
+// the diagonal (or the ragged end of the keys) are masked element-wise [codelab §7: key j
+// is visible to query i iff j <= i].
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include "ptx.cuh"
+#include "sdpa_internal.h"
+
+namespace sdpa {
+namespace {
+
+using namespace ptx;
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+template <int D, int DT>
+struct FwdCfg {
+  static constexpr int ES = (DT == kE4M3) ? 1 : 2;               // input element bytes
+  static constexpr int NQT = (DT != kE4M3 && D <= 128) ? 2 : 1;   // Q tiles per CTA
+  static constexpr int CHUNK_ELEMS = 128 / ES;                    // elements per 128-byte row chunk
+  static constexpr int NCHUNK = D * ES / 128;                     // 128-byte chunks along d
+  static constexpr int TILE_BYTES = kBlockM * D * ES;             // one Q or K or V tile
+  static constexpr int Q_BYTES = NQT * TILE_BYTES;
+  static constexpr int RING_BUDGET = 196608 - Q_BYTES;
+  static constexpr int NS = (RING_BUDGET / TILE_BYTES) > 8 ? 8 : (RING_BUDGET / TILE_BYTES);
+  static constexpr int RING_BYTES = NS * TILE_BYTES;
+  static constexpr int OUT_TILE_BYTES = kBlockM * D * 2;          // 16-bit output tile
+  static constexpr int SMEM_BYTES = Q_BYTES + RING_BYTES + 1024 /*align slack*/;
+  static constexpr int THREADS = 128 + NQT * 128;
+  static constexpr int KSTEPS_S = D * ES / 32;                    // QKᵀ: 32 bytes of d per MMA
+  static constexpr int PV_ROWS = 32 / ES;                         // PV: kv rows per MMA
+  static constexpr int KSTEPS_PV = kBlockN / PV_ROWS;
+  static constexpr int P_COLS = kBlockN * ES / 4;                 // TMEM columns holding P
+  static constexpr int O_COL0 = 256;                              // S slots at 0 and 128
+  static constexpr float THRESH = (DT == kE4M3) ? 0.8f : 8.0f;    // lazy-rescale threshold
+  static constexpr float P_OFFSET = (DT == kE4M3) ? 8.0f : 0.0f;  // P scaled by 2^8 for E4M3
+  static_assert(NS >= 2, "K/V ring needs at least two slots");
+  static_assert(O_COL0 + NQT * D <= 512, "TMEM budget");
+  static_assert(NQT == 2 || OUT_TILE_BYTES <= RING_BYTES, "epilogue staging");
+};
+
+struct alignas(8) FwdBarriers {
+  uint64_t q_full[2];
+  uint64_t kv_full[8];
+  uint64_t kv_empty[8];
+  uint64_t s_full[2];
+  uint64_t p_full[2];
+  uint64_t o_full[2];
+  uint64_t pv_done;
+  uint64_t drain;
+  uint64_t epi_ready[2];
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, int dt) {
+  if (dt == kBF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return (lo & 0xFFFFu) | (hi << 16);
+}
+
+// Number of key blocks a query tile pair starting at row m0 must visit.
+__device__ __forceinline__ int kv_blocks_for(const FwdParams& p, int m0, int rows) {
+  const int nfull = (p.s_kv + kBlockN - 1) / kBlockN;
+  if (!p.causal) return nfull;
+  const int last_row = min(m0 + rows, p.s_q) - 1;
+  const int n = last_row / kBlockN + 1;
+  return n < nfull ? n : nfull;
+}
+
+template <int D, int DT, int OUT_DT>
+__global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
+    sdpa_fwd_kernel(const __grid_constant__ FwdParams p) {
+  using C = FwdCfg<D, DT>;
+  constexpr int NQT = C::NQT;
+  constexpr int NS = C::NS;
+  constexpr bool FP8 = (DT == kE4M3);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sRing = smem + C::Q_BYTES;
+  __shared__ FwdBarriers bars;
+
+  const int warp = threadIdx.x / 32;
+  const int lane = threadIdx.x % 32;
+
+  // ---- tile coordinates: heaviest (latest) query tiles launch first -----------------
+  const int bh = blockIdx.x;
+  const int bi = bh / p.h_q;
+  const int hq = bh % p.h_q;
+  const int hk = hq / p.group;
+  const int m_blk = p.num_m_blocks - 1 - blockIdx.y;
+  const int m0 = m_blk * kBlockM * NQT;
+  const int n_blocks = kv_blocks_for(p, m0, kBlockM * NQT);
+
+  if (threadIdx.x == 0) {
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bars.q_full[t], 1);
+      mbar_init(&bars.s_full[t], 1);
+      mbar_init(&bars.p_full[t], 128);
+      mbar_init(&bars.o_full[t], 1);
+    }
+    for (int s = 0; s < 8; ++s) {
+      mbar_init(&bars.kv_full[s], 1);
+      mbar_init(&bars.kv_empty[s], 1);
+    }
+    mbar_init(&bars.pv_done, 1);
+    mbar_init(&bars.drain, 1);
+    mbar_init(&bars.epi_ready[0], 128);
+    mbar_init(&bars.epi_ready[1], 128);
+    bars.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  volatile int* abort_flag = &bars.abort;
+
+  if (warp == 0) {
+    // ================================ TMA producer ====================================
+    if (elect_one_sync()) {
+      tma_prefetch_desc(&p.tm_q);
+      tma_prefetch_desc(&p.tm_k);
+      tma_prefetch_desc(&p.tm_v);
+      for (int t = 0; t < NQT; ++t) {
+        mbar_arrive_expect_tx(&bars.q_full[t], C::TILE_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_4d(sQ + t * C::TILE_BYTES + c * 16384, &p.tm_q, &bars.q_full[t],
+                      c * C::CHUNK_ELEMS, m0 + t * kBlockM, hq, bi);
+      }
+      int it = 0;
+      bool ok = true;
+      auto load = [&](const CUtensorMap* map, int j) {
+        const int slot = it % NS;
+        const uint32_t ph = (it / NS) & 1;
+        if (!mbar_wait(&bars.kv_empty[slot], ph ^ 1, abort_flag)) return false;
+        mbar_arrive_expect_tx(&bars.kv_full[slot], C::TILE_BYTES);
+        uint8_t* dst = sRing + slot * C::TILE_BYTES;
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_4d(dst + c * 16384, map, &bars.kv_full[slot], c * C::CHUNK_ELEMS,
+                      j * kBlockN, hk, bi);
+        ++it;
+        return true;
+      };
+      if (NQT == 2) {
+        for (int j = 0; j < n_blocks && ok; ++j) {
+          ok = load(&p.tm_k, j);
+          if (ok) ok = load(&p.tm_v, j);
+        }
+      } else {
+        ok = load(&p.tm_k, 0);
+        for (int j = 0; j < n_blocks && ok; ++j) {
+          if (j + 1 < n_blocks) ok = load(&p.tm_k, j + 1);
+          if (ok) ok = load(&p.tm_v, j);
+        }
+      }
+      if (!ok || *abort_flag) {
+        // Let copies already issued land before the CTA's shared memory is released.
+        for (int t = 0; t < NQT; ++t) mbar_wait_drain(&bars.q_full[t], 0);
+        for (int k = (it > NS ? it - NS : 0); k < it; ++k)
+          mbar_wait_drain(&bars.kv_full[k % NS], (k / NS) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ================================ MMA issuer ======================================
+    if (elect_one_sync()) {
+      const uint32_t fmt = (DT == kBF16) ? 1u : 0u;
+      uint32_t idesc_s = make_idesc(fmt, kBlockM, kBlockN, false, false);
+      if (p.negate_scores) idesc_s |= (1u << 13);
+      const uint32_t idesc_pv = make_idesc(fmt, kBlockM, D, false, true);
+      int it = 0;
+      bool ok = true;
+      auto wait_full = [&]() -> int {
+        const int slot = it % NS;
+        if (!mbar_wait(&bars.kv_full[slot], (it / NS) & 1, abort_flag)) return -1;
+        ++it;
+        tc_fence_after();
+        return slot;
+      };
+      auto issue_s = [&](int t_q, int s_slot, int kslot) {
+        const uint32_t qa = smem_u32(sQ + t_q * C::TILE_BYTES);
+        const uint32_t kb = smem_u32(sRing + kslot * C::TILE_BYTES);
+#pragma unroll
+        for (int k = 0; k < C::KSTEPS_S; ++k) {
+          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+          mma_ss(tmem + s_slot * 128, make_sdesc_sw128(qa + off, 16, 1024),
+                 make_sdesc_sw128(kb + off, 16, 1024), idesc_s, k > 0, FP8);
+        }
+        tc_commit(&bars.s_full[s_slot]);
+      };
+      auto issue_pv = [&](int t_q, int s_slot, int vslot, bool first) {
+        const uint32_t vb = smem_u32(sRing + vslot * C::TILE_BYTES);
+        const uint32_t o_col = tmem + C::O_COL0 + t_q * D;
+#pragma unroll
+        for (int k = 0; k < C::KSTEPS_PV; ++k) {
+          mma_ts(o_col, tmem + s_slot * 128 + k * 8,
+                 make_sdesc_sw128(vb + k * C::PV_ROWS * 128, 16384, 1024), idesc_pv,
+                 (!first || k > 0) ? 1u : 0u, FP8);
+        }
+      };
+      for (int t = 0; t < NQT && ok; ++t) ok = mbar_wait(&bars.q_full[t], 0, abort_flag);
+      tc_fence_after();
+      if (NQT == 2) {
+        int kslot = ok ? wait_full() : -1;
+        ok = kslot >= 0;
+        if (ok) {
+          issue_s(0, 0, kslot);
+          issue_s(1, 1, kslot);
+          tc_commit(&bars.kv_empty[kslot]);
+        }
+        for (int j = 0; j < n_blocks && ok; ++j) {
+          const int vslot = wait_full();
+          if (vslot < 0) { ok = false; break; }
+          const uint32_t ph = j & 1;
+          // tile 0
+          if (!mbar_wait(&bars.p_full[0], ph, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(0, 0, vslot, j == 0);
+          if (j + 1 == n_blocks) tc_commit(&bars.o_full[0]);
+          int nk = -1;
+          if (j + 1 < n_blocks) {
+            nk = wait_full();
+            if (nk < 0) { ok = false; break; }
+            issue_s(0, 0, nk);
+          }
+          // tile 1
+          if (!mbar_wait(&bars.p_full[1], ph, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(1, 1, vslot, j == 0);
+          if (j + 1 == n_blocks) tc_commit(&bars.o_full[1]);
+          tc_commit(&bars.kv_empty[vslot]);
+          if (nk >= 0) {
+            issue_s(1, 1, nk);
+            tc_commit(&bars.kv_empty[nk]);
+          }
+        }
+      } else {
+        int k0 = ok ? wait_full() : -1;
+        ok = k0 >= 0;
+        if (ok) {
+          issue_s(0, 0, k0);
+          tc_commit(&bars.kv_empty[k0]);
+        }
+        for (int j = 0; j < n_blocks && ok; ++j) {
+          if (j + 1 < n_blocks) {
+            const int nk = wait_full();
+            if (nk < 0) { ok = false; break; }
+            issue_s(0, (j + 1) & 1, nk);
+            tc_commit(&bars.kv_empty[nk]);
+          }
+          const int vslot = wait_full();
+          if (vslot < 0) { ok = false; break; }
+          if (!mbar_wait(&bars.p_full[j & 1], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(0, j & 1, vslot, j == 0);
+          tc_commit(&bars.pv_done);
+          if (j + 1 == n_blocks) tc_commit(&bars.o_full[0]);
+          tc_commit(&bars.kv_empty[vslot]);
+        }
+      }
+      // Whatever happened, wait for the tensor core to finish before TMEM is released.
+      tc_commit(&bars.drain);
+      mbar_wait_drain(&bars.drain, 0);
+    }
+  } else if (warp >= 4) {
+    // ============================ softmax / epilogue ==================================
+    const int t = (NQT == 2) ? (warp - 4) / 4 : 0;         // Q tile of this warpgroup
+    const int quad = warp % 4;                               // TMEM lane quadrant
+    const int r = quad * 32 + lane;                          // row within the tile
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int q_row = m0 + t * kBlockM + r;
+    const int tile_row0 = m0 + t * kBlockM;
+
+    float c_scale = p.scale_log2;
+    float v_scale = 1.f;
+    if (FP8) {
+      c_scale *= __ldg(p.descale_q) * __ldg(p.descale_k);
+      v_scale = __ldg(p.descale_v);
+    }
+    // Highest key index this row may see.
+    const int row_limit = p.causal ? min(q_row, p.s_kv - 1) : p.s_kv - 1;
+
+    float m_ref = -INFINITY;   // running max (log2 domain, scale folded in)
+    float l = 0.f;             // running sum of exp2(x - m_ref + P_OFFSET)
+    bool ok = true;
+
+    for (int j = 0; j < n_blocks; ++j) {
+      const int slot = (NQT == 2) ? t : (j & 1);
+      const uint32_t ph = (NQT == 2) ? (j & 1) : ((j >> 1) & 1);
+      if (!mbar_wait_warp(&bars.s_full[slot], ph, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t s_addr = tmem + lane_off + slot * 128;
+
+      uint32_t sv[kBlockN];
+#pragma unroll
+      for (int c = 0; c < kBlockN / 32; ++c)
+        tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+      tmem_ld_wait();
+
+      const int kv0 = j * kBlockN;
+      const bool need_mask = (kv0 + kBlockN - 1 > p.s_kv - 1) ||
+                             (p.causal && kv0 + kBlockN - 1 > tile_row0);
+      if (need_mask) {
+        const int lim = row_limit - kv0;
+#pragma unroll
+        for (int c = 0; c < kBlockN; ++c)
+          if (c > lim) sv[c] = __float_as_uint(-INFINITY);
+      }
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kBlockN; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
+      const float m_cand = mx * c_scale;
+      float alpha = 1.f;
+      if (m_cand > m_ref + C::THRESH) {
+        alpha = ex2(m_ref - m_cand);
+        m_ref = m_cand;
+      }
+      const float neg_m = C::P_OFFSET - m_ref;
+
+      float rowsum = 0.f;
+      uint32_t pk[C::P_COLS];
+      if (FP8) {
+#pragma unroll
+        for (int c = 0; c < kBlockN; c += 4) {
+          const float p0 = ex2(fmaf(__uint_as_float(sv[c]), c_scale, neg_m));
+          const float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), c_scale, neg_m));
+          const float p2 = ex2(fmaf(__uint_as_float(sv[c + 2]), c_scale, neg_m));
+          const float p3 = ex2(fmaf(__uint_as_float(sv[c + 3]), c_scale, neg_m));
+          rowsum += (p0 + p1) + (p2 + p3);
+          pk[c / 4] = pack4_e4m3(p0, p1, p2, p3);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kBlockN; c += 2) {
+          const float p0 = ex2(fmaf(__uint_as_float(sv[c]), c_scale, neg_m));
+          const float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), c_scale, neg_m));
+          rowsum += p0 + p1;
+          pk[c / 2] = pack2(p0, p1, DT);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < C::P_COLS / 32; ++c)
+        tmem_st32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[c * 32]));
+      l = l * alpha + rowsum;
+
+      if (NQT == 1 && j > 0) {
+        // O is still being accumulated by the previous block's P·V.
+        if (!mbar_wait_warp(&bars.pv_done, (j - 1) & 1, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+      }
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        const uint32_t o_addr = tmem + lane_off + C::O_COL0 + t * D;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t ov[32];
+          tmem_ld32(o_addr + c * 32, ov);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ov[i] = __float_as_uint(__uint_as_float(ov[i]) * alpha);
+          tmem_st32(o_addr + c * 32, ov);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.p_full[slot]);
+    }
+
+    // ---- epilogue: O / l through shared memory and a TMA store; LSE ------------------
+    ok = ok && mbar_wait_warp(&bars.o_full[t], 0, abort_flag);
+    uint8_t* stage = (NQT == 2) ? (sQ + t * C::TILE_BYTES) : sRing;
+    if (ok) {
+      tc_fence_after();
+      const float inv_l = v_scale / l;
+      const uint32_t o_addr = tmem + lane_off + C::O_COL0 + t * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t ov[64];
+        tmem_ld32(o_addr + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
+        tmem_ld32(o_addr + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
+        tmem_ld_wait();
+        uint8_t* rowp = stage + c * 16384 + r * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint4 w;
+          w.x = pack2(__uint_as_float(ov[u * 8 + 0]) * inv_l, __uint_as_float(ov[u * 8 + 1]) * inv_l, OUT_DT);
+          w.y = pack2(__uint_as_float(ov[u * 8 + 2]) * inv_l, __uint_as_float(ov[u * 8 + 3]) * inv_l, OUT_DT);
+          w.z = pack2(__uint_as_float(ov[u * 8 + 4]) * inv_l, __uint_as_float(ov[u * 8 + 5]) * inv_l, OUT_DT);
+          w.w = pack2(__uint_as_float(ov[u * 8 + 6]) * inv_l, __uint_as_float(ov[u * 8 + 7]) * inv_l, OUT_DT);
+          *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) = w;
+        }
+      }
+      fence_proxy_async_smem();
+      if (p.lse != nullptr && q_row < p.s_q)
+        p.lse[(static_cast<int64_t>(bi) * p.h_q + hq) * p.s_q + q_row] =
+            (m_ref - C::P_OFFSET + __log2f(l)) * kLn2;
+    }
+    // Every thread of the warpgroup arrives exactly once, whatever happened above, so the
+    // bounded wait below can only fail through a timeout, never deadlock.
+    mbar_arrive(&bars.epi_ready[t]);
+    if (r == 0) {
+      const bool all_ok = mbar_wait(&bars.epi_ready[t], 0, abort_flag) && ok && !*abort_flag;
+      if (all_ok) {
+        for (int c = 0; c < D / 64; ++c)
+          tma_store_4d(&p.tm_o, stage + c * 16384, c * 64, tile_row0, hq, bi);
+        tma_store_commit();
+        tma_store_wait_read_all();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D, int DT, int OUT_DT>
+cudaError_t launch_t(const FwdParams& p, cudaStream_t st) {
+  using C = FwdCfg<D, DT>;
+  auto kern = sdpa_fwd_kernel<D, DT, OUT_DT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.b * p.h_q, p.num_m_blocks);
+  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int fwd_q_tiles(int d, int in_dtype) { return (in_dtype != kE4M3 && d <= 128) ? 2 : 1; }
+
+cudaError_t launch_fwd(const FwdParams& p, int d, int in_dtype, int out_dtype, cudaStream_t st) {
+  if (in_dtype == kF16) {
+    if (d == 64) return launch_t<64, kF16, kF16>(p, st);
+    if (d == 128) return launch_t<128, kF16, kF16>(p, st);
+    if (d == 256) return launch_t<256, kF16, kF16>(p, st);
+  } else if (in_dtype == kBF16) {
+    if (d == 64) return launch_t<64, kBF16, kBF16>(p, st);
+    if (d == 128) return launch_t<128, kBF16, kBF16>(p, st);
+    if (d == 256) return launch_t<256, kBF16, kBF16>(p, st);
+  } else if (in_dtype == kE4M3) {
+    if (out_dtype == kBF16) {
+      if (d == 128) return launch_t<128, kE4M3, kBF16>(p, st);
+      if (d == 256) return launch_t<256, kE4M3, kBF16>(p, st);
+    } else {
+      if (d == 128) return launch_t<128, kE4M3, kF16>(p, st);
+      if (d == 256) return launch_t<256, kE4M3, kF16>(p, st);
+    }
+  }
+  return cudaErrorInvalidValue;
+}
+
+uint32_t fwd_take_device_error() {
+  uint32_t v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, ptx::g_device_error, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(ptx::g_device_error, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace sdpa

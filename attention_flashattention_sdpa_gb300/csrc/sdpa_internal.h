@@ -1,0 +1,63 @@
+// sdpa_internal.h — parameter blocks passed from the C-ABI layer to the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace sdpa {
+
+constexpr int kBlockM = 128;  // query rows per Q tile (one TMEM lane per row)
+constexpr int kBlockN = 128;  // key/value rows per KV block
+
+enum DType : int { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
+
+// Forward pass.  Tensor maps are 4-D (d, s, h, b) views over the caller's strides,
+// 128-byte swizzled, box = (128 bytes of d, 128 rows, 1, 1).
+struct FwdParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;
+  float* lse;                 // [b][h_q][s_q] fp32 or nullptr
+  const float* descale_q;     // E4M3 only
+  const float* descale_k;
+  const float* descale_v;
+  int b, h_q, h_kv, s_q, s_kv;
+  int group;                  // h_q / h_kv
+  int causal;
+  int num_m_blocks;           // ceil(s_q / (128 * q tiles per CTA))
+  float scale_log2;           // |attn_scale| * log2(e) (0 is replaced by a tiny positive value)
+  int negate_scores;          // attn_scale < 0: the QK^T MMA negates its A operand
+};
+
+// Number of Q tiles (of 128 rows) one forward CTA processes.
+int fwd_q_tiles(int d, int in_dtype);
+
+cudaError_t launch_fwd(const FwdParams& p, int d, int in_dtype, int out_dtype, cudaStream_t st);
+uint32_t fwd_take_device_error();
+
+// Backward pass.
+struct BwdParams {
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;   // loads (128-byte swizzled)
+  CUtensorMap tm_dk, tm_dv;              // stores
+  const void* o;       // forward output, for Delta
+  const void* dout;    // incoming gradient, for Delta
+  const float* lse;    // [b][h_q][s_q]
+  void* dq;            // output
+  float* dq_acc;       // workspace [b][h_q][s_q_pad][d] fp32
+  float* delta;        // workspace [b][h_q][s_q_pad] fp32 (Delta_i)
+  float* lse2;         // workspace [b][h_q][s_q_pad] fp32 (LSE_i * log2 e)
+  int64_t o_sb, o_sh, o_ss;     // element strides of O
+  int64_t do_sb, do_sh, do_ss;  // element strides of dO
+  int64_t dq_sb, dq_sh, dq_ss;  // element strides of dQ
+  int b, h_q, h_kv, s_q, s_kv, d;
+  int group;
+  int causal;
+  int s_q_pad;                  // s_q rounded up to 128
+  float scale;                  // attn_scale
+  float scale_log2;             // attn_scale * log2(e)
+};
+
+size_t bwd_workspace_bytes(int b, int h_q, int s_q, int d);
+cudaError_t launch_bwd(const BwdParams& p, int dtype, cudaStream_t st);
+uint32_t bwd_take_device_error();
+
+}  // namespace sdpa

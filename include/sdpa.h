@@ -1,0 +1,163 @@
+/*
+ * sdpa.h — C ABI of the GB300 (sm_103a) fused scaled-dot-product attention library.
+ *
+ * What it computes.  For every batch b and query head hq (KV head hk = hq / (h_q / h_kv)):
+ *
+ *     S   = attn_scale * Q K^T                  (scores, then the scale)
+ *     S  += mask   (causal: -inf where key j > query i; otherwise no mask)
+ *     P   = softmax(S) over each row
+ *     O   = P V                                  (O has Q's shape)
+ *     LSE = log(sum_j exp(S_ij))                 (natural log, per query row)
+ *
+ * [attention codelab "Speeding up attention on GPU with cuDNN and TransformerEngine",
+ *  §1 "How attention works" (the four steps) and §7 "Adding a causal mask";
+ *  cuDNN 9 blog "Accelerating Transformers with NVIDIA cuDNN 9", "SDPA as a cuDNN
+ *  graph", Fig. 4 (BMM1 -> scale -> causal mask -> softmax -> BMM2); the SDPA node's
+ *  second output "stats" is the per-row statistic kept for training, read here as the
+ *  log-sum-exp.]  The backward pass returns dQ, dK, dV of O for an incoming dO, using the
+ *  LSE kept by the forward pass (the blog's "fprop + bprop" figure; the pages give no
+ *  formula, the derivative is the analytic one).
+ *
+ * Conventions shared by every entry point
+ *  - All tensors are *logical* BHSD [b][h][s][d] views over caller memory described by
+ *    four element strides (sdpa_strides_t).  The innermost stride must be 1.  A BSHD
+ *    buffer is passed with strides (s*h*d, d, h*d, 1) — no copy is made [cuDNN-in-Python
+ *    post: the GPT-2-like example views a BSHD buffer as BHSD with as_strided].
+ *  - Pointers are DEVICE pointers on the current CUDA device; bases must be 16-byte
+ *    aligned and every non-unit stride, in bytes, a multiple of 16 (they are handed to
+ *    the tensor-memory-accelerator (TMA) unit as is).
+ *  - Ownership: the caller owns every buffer.  The library allocates no device memory,
+ *    frees nothing, does not synchronise the stream and keeps no pointer after return.
+ *  - Work is enqueued asynchronously on `stream` (0 = legacy default stream).
+ *  - Errors: arguments are validated on the host before anything is launched; a non-OK
+ *    status comes with a message from sdpa_last_error_string().  Unsupported inputs are an
+ *    error, never a silent fallback.  Launch failures return SDPA_ERR_CUDA.
+ *  - Thread safety: re-entrant.  Concurrent calls must not share a workspace.
+ */
+#ifndef SDPA_GB300_H
+#define SDPA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SDPA_API __attribute__((visibility("default")))
+#else
+#define SDPA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SDPA_OK = 0,
+  SDPA_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, h_q % h_kv != 0, ... */
+  SDPA_ERR_UNSUPPORTED = 2,   /* valid request this library does not implement (e.g. d=96) */
+  SDPA_ERR_LAYOUT = 3,        /* stride / alignment not expressible to the TMA unit */
+  SDPA_ERR_WORKSPACE = 4,     /* workspace missing or smaller than sdpa_workspace_size() */
+  SDPA_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed (message has the code) */
+  SDPA_ERR_TIMEOUT = 6        /* a bounded device wait gave up (see sdpa_device_error) */
+} sdpa_status_t;
+
+typedef enum {
+  SDPA_DTYPE_F16 = 0,         /* IEEE binary16 */
+  SDPA_DTYPE_BF16 = 1,        /* bfloat16 */
+  SDPA_DTYPE_E4M3 = 2         /* OCP FP8 E4M3 (finite max 448); forward inputs only */
+} sdpa_dtype_t;
+
+/* Element strides of a logical [b][h][s][d] view.  d must be 1. */
+typedef struct {
+  int64_t b, h, s, d;
+} sdpa_strides_t;
+
+/* One attention problem.  Fields not used by a call are ignored. */
+typedef struct {
+  int32_t b;           /* batch, >= 1 */
+  int32_t h_q;         /* query heads, >= 1 */
+  int32_t h_kv;        /* key/value heads, >= 1, h_q % h_kv == 0 (MHA: ==, GQA: <, MQA: 1);
+                          query head hq reads KV head hq / (h_q / h_kv) [codelab §9] */
+  int32_t s_q;         /* query rows, >= 1 */
+  int32_t s_kv;        /* key/value rows, >= 1 */
+  int32_t d;           /* head dim of Q, K and V: 64, 128 or 256 */
+  int32_t in_dtype;    /* sdpa_dtype_t of Q, K, V (and of dO for the backward pass) */
+  int32_t out_dtype;   /* sdpa_dtype_t of O (and dQ/dK/dV): == in_dtype for F16/BF16;
+                          BF16 or F16 for E4M3 inputs */
+  float attn_scale;    /* multiplies Q K^T before the mask and softmax; any finite value
+                          (usually 1/sqrt(d)) [cuDNN 9 blog, Fig. 4: scale node after BMM1] */
+  int32_t causal;      /* 0: no mask.  1: top-left causal, key j visible to query i iff j <= i
+                          (row 0 sees only key 0) [codelab §7] */
+  sdpa_strides_t q, k, v, o;         /* forward and backward */
+  sdpa_strides_t dout, dq, dk, dv;   /* backward only (dout = incoming gradient dO) */
+  const float* descale_q;  /* E4M3 only: DEVICE pointers to one fp32 each; the real value of */
+  const float* descale_k;  /* a stored code x is decode(x) * descale (per-tensor scaling of    */
+  const float* descale_v;  /* the delayed-scaling FP8 recipe, codelab §10).  NULL otherwise.   */
+} sdpa_problem_t;
+
+/*
+ * Workspace bytes that sdpa_fwd (is_backward = 0) or sdpa_bwd (is_backward = 1) needs for
+ * `p`.  Writes *bytes; never launches anything.  The forward pass needs 0 bytes; the
+ * backward pass needs fp32 scratch for dQ accumulation and the per-row Delta term
+ * (4*b*h_q*round_up(s_q,128)*(d+1) bytes plus alignment).
+ * [cuDNN-in-Python post: the workspace size is queried, then allocated by the caller.]
+ */
+SDPA_API sdpa_status_t sdpa_workspace_size(const sdpa_problem_t* p, int is_backward, size_t* bytes);
+
+/*
+ * Forward pass: O (and, when lse != NULL, the per-row log-sum-exp) from Q, K, V.
+ *   q:   [b][h_q][s_q][d]   in_dtype, strides p->q
+ *   k,v: [b][h_kv][s_kv][d] in_dtype, strides p->k, p->v
+ *   o:   [b][h_q][s_q][d]   out_dtype, strides p->o; overwritten
+ *   lse: NULL (inference: no statistics written) or fp32 [b][h_q][s_q] dense row-major;
+ *        lse[(b*h_q + hq)*s_q + i] = ln sum_j exp(S_ij) over the visible keys; overwritten.
+ *        The SDPA node's "stats" output, kept for training [cuDNN 9 blog, SDPA walkthrough;
+ *        cuDNN-in-Python post].
+ *   workspace / workspace_bytes: may be NULL / 0 (the forward pass needs none).
+ * E4M3 inputs require descale_q/k/v and give a BF16 or F16 O.
+ */
+SDPA_API sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const void* k, const void* v,
+                       void* o, float* lse, void* workspace, size_t workspace_bytes,
+                       void* stream /* cudaStream_t */);
+
+/*
+ * Backward pass: dQ, dK, dV of O for the incoming gradient dO, recomputing P from the LSE
+ * written by sdpa_fwd on the same inputs.
+ *   q, k, v, o: as in sdpa_fwd (o is the forward output); dout: [b][h_q][s_q][d], in_dtype
+ *   lse: fp32 [b][h_q][s_q] from sdpa_fwd (required)
+ *   dq: Q's shape, dk/dv: K's/V's shape, all out_dtype (== in_dtype); overwritten.  dK and
+ *       dV hold the sum over the query heads of each KV group (GQA/MQA).
+ *   workspace: >= sdpa_workspace_size(p, 1) bytes, 256-byte aligned; its contents on entry
+ *       do not matter and are clobbered.
+ * F16/BF16 only (an E4M3 backward pass is SDPA_ERR_UNSUPPORTED).
+ */
+SDPA_API sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, const void* v,
+                       const void* o, const void* dout, const float* lse, void* dq, void* dk,
+                       void* dv, void* workspace, size_t workspace_bytes,
+                       void* stream /* cudaStream_t */);
+
+/* Message for the last non-OK status returned on the calling thread ("" if none).  The
+ * pointer stays valid until the next library call on this thread [cuDNN 9 blog: errors
+ * come with a retrievable last-error string]. */
+SDPA_API const char* sdpa_last_error_string(void);
+
+/*
+ * Device-side error word of the current device: bit 0 = a bounded wait inside a kernel
+ * gave up (the kernel then skipped its remaining work and returned without faulting);
+ * bit 1 = shared memory was not 1024-byte aligned (the kernel did nothing).
+ * Synchronises the device, writes the word to *flags and clears it.  Returns SDPA_OK, or
+ * SDPA_ERR_CUDA if the synchronisation or copy failed.
+ */
+SDPA_API sdpa_status_t sdpa_device_error(uint32_t* flags);
+
+/* Library version as major*10000 + minor*100 + patch. */
+SDPA_API int sdpa_version(void);
+
+/* sizeof(sdpa_problem_t) as compiled into the library, so that bindings built from this
+ * header can check their copy of the struct layout. */
+SDPA_API size_t sdpa_problem_struct_size(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SDPA_GB300_H */

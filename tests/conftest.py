@@ -28,3 +28,17 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def _build_library():
+    """Compile libsdpa_gb300.so in-tree if a source is newer (nvcc cross-compiles here)."""
+    import importlib.util
+    path = os.path.join(ROOT, "attention_flashattention_sdpa_gb300", "_build.py")
+    spec = importlib.util.spec_from_file_location("_sdpa_build", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.build()
+
+
+def pytest_sessionstart(session):
+    _build_library()

@@ -1,0 +1,152 @@
+"""Host-side checks of the C ABI: the library loads, exports every declared symbol, and
+rejects bad arguments with the right status and message before launching anything.
+No GPU is needed: validation runs before any CUDA call."""
+import ctypes
+import os
+import re
+import threading
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def m():
+    import attention_flashattention_sdpa_gb300 as mod
+    return mod
+
+
+def _declared_symbols():
+    text = open(os.path.join(ROOT, "include", "sdpa.h")).read()
+    return sorted(set(re.findall(r"SDPA_API\s+[\w\s\*]+?\b(sdpa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    syms = _declared_symbols()
+    for name in ("sdpa_fwd", "sdpa_bwd", "sdpa_workspace_size", "sdpa_last_error_string"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(m):
+    L = ctypes.CDLL(m.LIB_PATH)
+    for name in _declared_symbols():
+        assert hasattr(L, name), f"{name} declared in include/sdpa.h but not exported"
+
+
+def test_struct_layout_and_version(m):
+    assert m.lib.sdpa_problem_struct_size() == ctypes.sizeof(m.Problem)
+    assert m.sdpa_version() >= 100
+
+
+def _problem(m, **over):
+    p = m.Problem()
+    p.b, p.h_q, p.h_kv, p.s_q, p.s_kv, p.d = 1, 2, 2, 128, 128, 64
+    p.in_dtype = p.out_dtype = m.DTYPE_F16
+    p.attn_scale = 0.125
+    p.causal = 0
+    st = m.Strides(2 * 128 * 64, 128 * 64, 64, 1)
+    stk = m.Strides(2 * 128 * 64, 128 * 64, 64, 1)
+    p.q = p.o = p.dout = p.dq = st
+    p.k = p.v = p.dk = p.dv = stk
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+# 16-byte aligned but not a real allocation.  Every call below fails host validation, so
+# no kernel is ever launched on it (these tests must stay safe on a machine with a GPU).
+FAKE = 0x7F0000000000
+
+
+def _fwd(m, p, q=FAKE, k=FAKE, v=FAKE, o=FAKE, lse=None):
+    return m.lib.sdpa_fwd(ctypes.byref(p), q, k, v, o, lse, None, 0, None)
+
+
+def _bwd(m, p, ws=FAKE, ws_bytes=1 << 40, lse=FAKE, q=FAKE):
+    return m.lib.sdpa_bwd(ctypes.byref(p), q, FAKE, FAKE, FAKE, FAKE, lse, FAKE, FAKE, FAKE, ws,
+                          ws_bytes, None)
+
+
+@pytest.mark.parametrize("over,status,msg", [
+    (dict(d=96), 2, "head dim"),
+    (dict(d=0), 1, "sizes"),
+    (dict(s_q=0), 1, "sizes"),
+    (dict(s_kv=0), 1, "sizes"),
+    (dict(h_kv=3, h_q=4), 1, "multiple"),
+    (dict(causal=2), 1, "causal"),
+    (dict(attn_scale=float("nan")), 1, "finite"),
+    (dict(in_dtype=7), 1, "in_dtype"),
+    (dict(out_dtype=1), 2, "same dtype"),
+    (dict(in_dtype=2, out_dtype=1, d=128), 1, "descale"),
+    (dict(in_dtype=2, out_dtype=1), 2, "d = 128 or 256"),
+    (dict(in_dtype=2, out_dtype=2), 2, "output"),
+])
+def test_forward_rejects_bad_problem(m, over, status, msg):
+    assert _fwd(m, _problem(m, **over)) == status
+    assert msg in m.sdpa_last_error_string()
+
+
+def test_forward_rejects_bad_views(m):
+    p = _problem(m)
+    assert _fwd(m, p, q=None) == 1 and "q: null" in m.sdpa_last_error_string()
+    assert _fwd(m, p, o=FAKE + 8) == 3 and "16-byte" in m.sdpa_last_error_string()
+    bad = _problem(m)
+    bad.q = m.Strides(2 * 128 * 64, 128 * 64, 64, 2)
+    assert _fwd(m, bad) == 3 and "innermost" in m.sdpa_last_error_string()
+    bad = _problem(m)
+    bad.k = m.Strides(2 * 128 * 64, 128 * 64, 60, 1)
+    assert _fwd(m, bad) == 3 and "multiple of 16" in m.sdpa_last_error_string()
+    bad = _problem(m)
+    bad.v = m.Strides(2 * 128 * 64, -64, 64, 1)
+    assert _fwd(m, bad) == 3 and "positive" in m.sdpa_last_error_string()
+
+
+def test_unit_dimension_strides_are_ignored(m):
+    # b = 1: the batch stride is never used, so an odd value must not be rejected.
+    # The call is stopped by a later check (a misaligned O) so nothing is launched; the
+    # message names O, which shows Q's odd batch stride passed validation.
+    p = _problem(m)
+    p.q = m.Strides(3, 128 * 64, 64, 1)
+    assert _fwd(m, p, o=FAKE + 8) == 3
+    assert m.sdpa_last_error_string().startswith("o:")
+
+
+def test_backward_rejections(m):
+    assert _bwd(m, _problem(m, in_dtype=2, out_dtype=1)) == 2
+    assert "E4M3" in m.sdpa_last_error_string()
+    assert _bwd(m, _problem(m, d=256)) == 2
+    assert _bwd(m, _problem(m), lse=None) == 1 and "lse" in m.sdpa_last_error_string()
+    assert _bwd(m, _problem(m), ws=None) == 4 and "workspace" in m.sdpa_last_error_string()
+    assert _bwd(m, _problem(m), ws_bytes=100) == 4
+    assert _bwd(m, _problem(m), ws=FAKE + 16) == 4 and "256-byte" in m.sdpa_last_error_string()
+    assert _bwd(m, _problem(m), q=None) == 1
+
+
+def test_workspace_size(m):
+    p = _problem(m)
+    assert m.sdpa_workspace_size(p, False) == 0
+    n = m.sdpa_workspace_size(p, True)
+    # fp32 dQ accumulator + Delta + LSE*log2(e), rows padded to 128, each 256-aligned
+    assert n >= 1 * 2 * 128 * 64 * 4 + 2 * 1 * 2 * 128 * 4
+    p2 = _problem(m, s_q=129)
+    assert m.sdpa_workspace_size(p2, True) >= 1 * 2 * 256 * 64 * 4
+    with pytest.raises(m.SdpaError) as e:
+        m.sdpa_workspace_size(_problem(m, d=100), True)
+    assert e.value.status == 2
+
+
+def test_last_error_is_thread_local(m):
+    assert _fwd(m, _problem(m, d=96)) == 2
+    seen = []
+    t = threading.Thread(target=lambda: seen.append(m.sdpa_last_error_string()))
+    t.start()
+    t.join()
+    assert seen == [""]
+    assert "head dim" in m.sdpa_last_error_string()
+
+
+def test_null_problem(m):
+    assert m.lib.sdpa_fwd(None, FAKE, FAKE, FAKE, FAKE, None, None, 0, None) == 1
+    n = ctypes.c_size_t()
+    assert m.lib.sdpa_workspace_size(None, 0, ctypes.byref(n)) == 1
