@@ -1,0 +1,506 @@
+"""Throughput of the fused SDPA training step on GB300.
+
+One step = the whole hot path over one batch: the forward pass with its per-row LSE,
+then the backward pass (dQ, dK, dV), for the bf16 causal d=128 training workload at
+s = 8192 (b=2, h=16), through the library's C ABI.  FLOPs follow the pages' counting
+convention: 4*b*h*s_q*s_kv*d for the forward pass, halved for causal, backward 2.5x that.
+
+Prints one JSON line (rank 0).  Flags:
+  --gpus N --steps K --warmup W   standard contract (N>1: one rank per GPU under torchrun,
+                                  independent replicas, max time over ranks, weak scaling)
+  --impl reference                time the fp64 CPU oracle instead (bounded row slices of the
+                                  same workload) and print the reference line
+  --profile-step                  run one untimed fwd+bwd (the command profiled with ncu)
+  --sweep                         one line per configuration (tables; not the contract line)
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "SDPA fwd & fwd+bwd TFLOP/s (bf16/fp8) and % of GB300 tensor peak"
+UNIT = "TFLOP/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        d["source"] = "measured"
+        return d
+    d = dict(PEAKS_FALLBACK)
+    d["source"] = "fallback"
+    return d
+
+
+def bench_workload():
+    from sdpa_workloads import training
+    return training(8192)
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (independent replicas; no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if world > 1 else None
+
+
+def aggregate(local_units: float, local_seconds: float, dist=None, device=None):
+    """Whole-job figures: units summed over ranks, time = max over ranks."""
+    import torch
+    if dist is None:
+        return local_units, local_seconds
+    t = torch.tensor([local_units, local_seconds], dtype=torch.float64, device=device)
+    u = t[:1].clone()
+    s = t[1:].clone()
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    dist.all_reduce(s, op=dist.ReduceOp.MAX)
+    return float(u.item()), float(s.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.bus_id = (bus_id or "").lower()
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            if self.bus_id and self.bus_id not in parts[1].lower():
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
+        loaded = [x for x in sm if x > 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------
+
+class Step:
+    """Device buffers and one training step (fwd with LSE, then bwd) of a workload."""
+
+    def __init__(self, w, seed: int, device):
+        import torch
+        import attention_flashattention_sdpa_gb300 as sdpa
+        from sdpa_workloads import make_inputs
+        self.sdpa, self.w, self.torch = sdpa, w, torch
+        x = make_inputs(w, seed=seed, with_do=True)
+        self.host = [t.contiguous().pin_memory() for t in (x.q, x.k, x.v, x.do)]
+        q, k, v, do = (t.to(device) for t in self.host)
+        self.q, self.k, self.v, self.do = q, k, v, do
+        self.o = torch.empty_like(q)
+        self.lse = torch.empty(w.b, w.h_q, w.s_q, dtype=torch.float32, device=device)
+        self.dq, self.dk, self.dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        p = sdpa.make_problem(q, k, v, self.o, attn_scale=w.scale, causal=w.causal, dout=do,
+                              dq=self.dq, dk=self.dk, dv=self.dv)
+        self.ws = torch.empty(sdpa.sdpa_workspace_size(p, True), dtype=torch.uint8, device=device)
+        self.out_host = [torch.empty_like(t, device="cpu").pin_memory()
+                         for t in (self.dq, self.dk, self.dv)]
+
+    def fwd(self):
+        w = self.w
+        self.sdpa.sdpa_fwd(self.q, self.k, self.v, self.o, self.lse, attn_scale=w.scale,
+                           causal=w.causal)
+
+    def bwd(self):
+        w = self.w
+        self.sdpa.sdpa_bwd(self.q, self.k, self.v, self.o, self.do, self.lse, self.dq, self.dk,
+                           self.dv, self.ws, attn_scale=w.scale, causal=w.causal)
+
+    def h2d(self):
+        for dst, src in zip((self.q, self.k, self.v, self.do), self.host):
+            dst.copy_(src, non_blocking=True)
+
+    def d2h(self):
+        for dst, src in zip(self.out_host, (self.dq, self.dk, self.dv)):
+            dst.copy_(src, non_blocking=True)
+
+    def h2d_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.host)
+
+    def d2h_bytes(self):
+        return sum(t.numel() * t.element_size() for t in self.out_host)
+
+
+def time_device(step: "Step", steps: int, warmup: int):
+    """CUDA-event timing on the launching stream: whole steps, and fwd / bwd separately."""
+    import torch
+    st = torch.cuda.current_stream()
+    for _ in range(warmup):
+        step.fwd()
+        step.bwd()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(st)
+    for e0, e1, e2 in ev:
+        e0.record(st)
+        step.fwd()
+        e1.record(st)
+        step.bwd()
+        e2.record(st)
+    end.record(st)
+    torch.cuda.synchronize()
+    total_ms = start.elapsed_time(end)
+    fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
+    bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
+    return total_ms, fwd_ms, bwd_ms
+
+
+def time_e2e(step: "Step", steps: int, warmup: int):
+    """Same metric through the public API with host buffers: per step, H2D of Q, K, V, dO
+    from pinned memory, fwd + bwd, D2H of dQ, dK, dV; all inside the timed region."""
+    import torch
+    st = torch.cuda.current_stream()
+    for _ in range(warmup):
+        step.h2d(); step.fwd(); step.bwd(); step.d2h()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(steps):
+        step.h2d(); step.fwd(); step.bwd(); step.d2h()
+    b.record(st)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)
+
+
+def cpu_oracle_sample(w, seconds: float = 12.0, rows_per_slice: int = 512):
+    """Times the fp64 oracle (as it stands) on row slices of one head of the workload until
+    `seconds` have passed.  Returns (TFLOP/s by the same counting rule, description)."""
+    import numpy as np
+    import oracle
+    from sdpa_workloads import make_inputs, Workload
+    one = Workload(w.name, 1, 1, 1, w.s_q, w.s_kv, w.d, w.dtype, causal=w.causal)
+    x = make_inputs(one, seed=0, with_do=True)
+    q, k, v, do = (oracle.to_f64(t)[0, 0] for t in (x.q, x.k, x.v, x.do))
+    flops, n_slices, t0 = 0.0, 0, time.perf_counter()
+    r1 = w.s_q
+    while time.perf_counter() - t0 < seconds and r1 > 0:
+        r0 = max(0, r1 - rows_per_slice)
+        rows = np.arange(r0, r1)
+        oracle.forward_rows(q[r0:r1], rows, k, v, w.scale, w.causal)
+        oracle.backward_dq_rows(q[r0:r1], do[r0:r1], rows, k, v, w.scale, w.causal)
+        oracle.backward_kv_rows(q[r0:r1], do[r0:r1], rows, k, v, w.scale, w.causal)
+        pairs = float(np.minimum(rows + 1, w.s_kv).sum()) if w.causal else float(len(rows) * w.s_kv)
+        flops += 3.5 * 4.0 * w.d * pairs
+        n_slices += 1
+        r1 = r0
+    dt = time.perf_counter() - t0
+    desc = (f"fp64 numpy oracle: forward rows, dQ rows and dK/dV contributions of {n_slices} "
+            f"slices of {rows_per_slice} query rows (the last, most-visible rows) of one head "
+            f"of {w.name}; counted with the fwd+bwd rule on the visible pairs")
+    return flops / dt / 1e12, desc
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    w = bench_workload()
+    import numpy as np
+    import oracle
+    from sdpa_workloads import make_inputs, Workload
+    one = Workload(w.name, 1, 1, 1, w.s_q, w.s_kv, w.d, w.dtype, causal=w.causal)
+    x = make_inputs(one, seed=0, with_do=True)
+    q, k, v, do = (oracle.to_f64(t)[0, 0] for t in (x.q, x.k, x.v, x.do))
+    rows_per_step = 128
+
+    def one_step(i):
+        r1 = w.s_q - (i * rows_per_step) % w.s_q
+        r0 = max(0, r1 - rows_per_step)
+        rows = np.arange(r0, r1)
+        oracle.forward_rows(q[r0:r1], rows, k, v, w.scale, w.causal)
+        oracle.backward_dq_rows(q[r0:r1], do[r0:r1], rows, k, v, w.scale, w.causal)
+        oracle.backward_kv_rows(q[r0:r1], do[r0:r1], rows, k, v, w.scale, w.causal)
+        pairs = float(np.minimum(rows + 1, w.s_kv).sum()) if w.causal else float(len(rows) * w.s_kv)
+        return 3.5 * 4.0 * w.d * pairs
+
+    for i in range(args.warmup):
+        one_step(i)
+    flops, t0 = 0.0, time.perf_counter()
+    for i in range(args.steps):
+        flops += one_step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt * 1e3 / max(1, args.steps), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name} (bf16 causal d=128, b=2, h=16): one 128-row query "
+                               f"slice of one head per step", "b": w.b, "h": w.h_q, "s": w.s_q,
+                   "d": w.d, "causal": w.causal},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"{rows_per_step} query rows of one head per step "
+                                   f"(fwd rows, dQ rows, dK/dV contributions), fp64 numpy"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_cuda(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = dist_init(world, "nccl")
+    w = bench_workload()
+    step = Step(w, seed=rank, device=device)
+    peaks = load_peaks()
+
+    if args.profile_step:
+        step.fwd()
+        step.bwd()
+        torch.cuda.synchronize()
+        assert step.sdpa.sdpa_device_error() == 0
+        print("profile step done")
+        return 0
+
+    props = torch.cuda.get_device_properties(device)
+    try:  # nvidia-smi prints DDDDDDDD:BB:DD.F; ":BB:DD." identifies the device
+        bus = ":%02x:%02x." % (props.pci_bus_id, props.pci_device_id)
+    except Exception:
+        bus = None
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(bus)
+    clocks.start()
+    total_ms, fwd_ms, bwd_ms = time_device(step, args.steps, args.warmup)
+    clk = clocks.stop()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    assert step.sdpa.sdpa_device_error() == 0, "device-side error during the timed region"
+
+    step_flops = w.fwd_flops() + w.bwd_flops()
+    units, seconds = aggregate(step_flops * args.steps, total_ms / 1e3, dist, device)
+    value = units / seconds / 1e12
+
+    e2e_steps = max(3, args.steps // 4)
+    e2e_ms = time_e2e(step, e2e_steps, max(3, args.warmup))
+    e2e_units, e2e_s = aggregate(step_flops * e2e_steps, e2e_ms / 1e3, dist, device)
+
+    fwd_avg = statistics.mean(fwd_ms)
+    bwd_avg = statistics.mean(bwd_ms)
+    fwd_tflops = w.fwd_flops() / (fwd_avg / 1e3) / 1e12
+    bwd_tflops = w.bwd_flops() / (bwd_avg / 1e3) / 1e12
+    peak = peaks["bf16_tflops"]
+    traffic = _load_traffic()
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "training bf16 causal d=128 s=8192: b=2, h_q=h_kv=16, fwd (O+LSE) "
+                               "+ bwd (dQ,dK,dV) per step",
+                   "b": w.b, "h": w.h_q, "s": w.s_q, "d": w.d, "causal": True,
+                   "l2": "inputs larger than L2 (Q,K,V,dO,O 67 MB each)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "fwd": {"tflops": fwd_tflops, "ms": fwd_avg, "frac_of_bf16_peak": fwd_tflops / peak},
+        "bwd": {"tflops": bwd_tflops, "ms": bwd_avg, "frac_of_bf16_peak": bwd_tflops / peak},
+        "roofline": {"bound": "tensor", "kernel": "sdpa_bwd (bwd_main dominant; pre and dQ-convert "
+                     "launches included in the timed call)",
+                     "achieved": bwd_tflops, "peak": peak, "unit": "TFLOP/s",
+                     "frac": bwd_tflops / peak, "peak_source": f"bf16_tflops ({peaks['source']}, burst)",
+                     "traffic": traffic},
+        "clocks": clk,
+        "e2e": {"value": e2e_units / e2e_s / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": step.h2d_bytes(), "d2h_bytes_per_step": step.d2h_bytes()},
+        "gpu_launches": 4 * args.steps,
+    }
+    if rank == 0 and not args.no_cpu:
+        cval, desc = cpu_oracle_sample(w, seconds=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": cval, "unit": UNIT, "cores": cpu_cores(),
+                                "kind": "oracle", "sample": desc}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def _load_traffic():
+    """DRAM bytes per launch of the backward main kernel from the committed ncu summary, or
+    None when no capture of the current kernel exists."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get("bwd_main_dram_bytes_per_launch")
+    except Exception:
+        return None
+
+
+def run_sweep(args):
+    """One line per configuration (for tables)."""
+    import torch
+    from sdpa_workloads import all_workloads
+    torch.cuda.set_device(0)
+    peaks = load_peaks()
+    for w in all_workloads():
+        if w.name.startswith("tiny"):
+            continue
+        try:
+            line = sweep_one(w, peaks, args)
+        except Exception as e:  # report and continue
+            line = {"workload": w.name, "error": str(e)}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def sweep_one(w, peaks, args):
+    import torch
+    import attention_flashattention_sdpa_gb300 as sdpa
+    from sdpa_workloads import make_inputs
+    x = make_inputs(w, seed=0, with_do=w.backward)
+    dev = lambda t: torch.empty_strided(t.shape, t.stride(), dtype=t.dtype, device="cuda").copy_(t)
+    q, k, v = dev(x.q), dev(x.k), dev(x.v)
+    kw = {}
+    odt = q.dtype if w.dtype != "e4m3" else torch.bfloat16
+    if w.dtype == "e4m3":
+        kw = dict(descale_q=torch.tensor([x.descale_q], device="cuda"),
+                  descale_k=torch.tensor([x.descale_k], device="cuda"),
+                  descale_v=torch.tensor([x.descale_v], device="cuda"))
+    o = torch.empty_strided(q.shape, q.stride(), dtype=odt, device="cuda")
+    lse = torch.empty(w.b, w.h_q, w.s_q, dtype=torch.float32, device="cuda") if (w.stats or w.backward) else None
+    fwd = lambda: sdpa.sdpa_fwd(q, k, v, o, lse, attn_scale=w.scale, causal=w.causal, **kw)
+    st = torch.cuda.current_stream()
+    reps = max(5, min(200, int(2e13 / max(w.fwd_flops(), 1))))
+    for _ in range(3):
+        fwd()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st); fwd(); b.record(st)
+        ts.append((a, b))
+    torch.cuda.synchronize()
+    fwd_ms = statistics.median(a.elapsed_time(b) for a, b in ts)
+    peak = peaks["bf16_tflops"]
+    line = {"workload": w.name, "fwd_ms": fwd_ms, "fwd_tflops": w.fwd_flops() / fwd_ms / 1e9}
+    es = 1 if w.dtype == "e4m3" else 2
+    io_bytes = (q.numel() + k.numel() + v.numel()) * es + o.numel() * o.element_size() + \
+        (lse.numel() * 4 if lse is not None else 0)
+    line["fwd_hbm_gbs"] = io_bytes / fwd_ms / 1e6
+    line["fwd_frac_of_bf16_peak"] = line["fwd_tflops"] / peak if w.dtype != "e4m3" else None
+    if w.backward:
+        do = dev(x.do)
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        p = sdpa.make_problem(q, k, v, o, attn_scale=w.scale, causal=w.causal, dout=do, dq=dq, dk=dk, dv=dv)
+        ws = torch.empty(sdpa.sdpa_workspace_size(p, True), dtype=torch.uint8, device="cuda")
+        bwd = lambda: sdpa.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, attn_scale=w.scale, causal=w.causal)
+        for _ in range(3):
+            bwd()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(max(3, reps // 2)):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st); bwd(); b.record(st)
+            ts.append((a, b))
+        torch.cuda.synchronize()
+        bwd_ms = statistics.median(a.elapsed_time(b) for a, b in ts)
+        line["bwd_ms"] = bwd_ms
+        line["bwd_tflops"] = w.bwd_flops() / bwd_ms / 1e9
+        line["fwdbwd_tflops"] = (w.fwd_flops() + w.bwd_flops()) / (fwd_ms + bwd_ms) / 1e9
+        line["fwdbwd_frac_of_bf16_peak"] = line["fwdbwd_tflops"] / peak
+    assert sdpa.sdpa_device_error() == 0
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--profile-step", action="store_true")
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and not args.profile_step:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
+    return run_cuda(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

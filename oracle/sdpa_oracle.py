@@ -44,7 +44,7 @@ import numpy as np
 
 __all__ = [
     "visible_mask", "kv_head_of", "head_forward", "forward", "forward_rows",
-    "backward", "backward_dq_rows", "backward_kv_head", "e4m3_decode_table",
+    "backward", "backward_dq_rows", "backward_kv_rows", "backward_kv_head", "e4m3_decode_table",
     "decode_e4m3", "to_f64",
 ]
 
@@ -213,6 +213,24 @@ def backward_dq_rows(q_rows, do_rows, rows: Sequence[int], kh, vh, scale: float,
     return scale * (dS @ kh)
 
 
+def backward_kv_rows(q_rows, do_rows, rows: Sequence[int], kh, vh, scale: float, causal: bool):
+    """The contribution of selected query rows of one head to dK and dV: ([s_kv, d], [s_kv, d]).
+
+    dK and dV of a KV head are the sums of these contributions over every query row of
+    every query head in its group."""
+    s_kv = kh.shape[0]
+    rows = np.asarray(rows)
+    mask = (np.arange(s_kv)[None, :] <= rows[:, None]) if causal else np.ones(
+        (len(rows), s_kv), dtype=bool)
+    _, _, P = head_forward(q_rows, kh, vh, scale, mask)
+    dV = P.T @ do_rows
+    dP = do_rows @ vh.T
+    delta = (P * dP).sum(axis=1)
+    dS = P * (dP - delta[:, None])
+    dK = scale * (dS.T @ q_rows)
+    return dK, dV
+
+
 def backward_kv_head(q, k, v, do, scale: float, causal: bool, bi: int, hk: int,
                      row_chunk: int = 1024):
     """dK, dV of one (batch, KV head) at any size: [s_kv, d] each.
@@ -228,14 +246,8 @@ def backward_kv_head(q, k, v, do, scale: float, causal: bool, bi: int, hk: int,
     for hq in range(hk * g, (hk + 1) * g):
         for r0 in range(0, s_q, row_chunk):
             r1 = min(s_q, r0 + row_chunk)
-            rows = np.arange(r0, r1)
-            mask = (np.arange(s_kv)[None, :] <= rows[:, None]) if causal else np.ones(
-                (r1 - r0, s_kv), dtype=bool)
-            qh, doh = q[bi, hq, r0:r1], do[bi, hq, r0:r1]
-            _, _, P = head_forward(qh, kh, vh, scale, mask)
-            dV += P.T @ doh
-            dP = doh @ vh.T
-            delta = (P * dP).sum(axis=1)
-            dS = P * (dP - delta[:, None])
-            dK += scale * (dS.T @ qh)
+            gk, gv = backward_kv_rows(q[bi, hq, r0:r1], do[bi, hq, r0:r1], np.arange(r0, r1),
+                                      kh, vh, scale, causal)
+            dK += gk
+            dV += gv
     return dK, dV
