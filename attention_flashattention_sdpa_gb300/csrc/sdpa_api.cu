@@ -201,7 +201,7 @@ sdpa_status_t sdpa_workspace_size(const sdpa_problem_t* p, int is_backward, size
   if (bytes == nullptr) return fail(SDPA_ERR_INVALID_ARG, "bytes is NULL");
   sdpa_status_t st = check_problem(p, is_backward != 0);
   if (st != SDPA_OK) return st;
-  *bytes = is_backward ? sdpa::bwd_workspace_bytes(p->b, p->h_q, p->s_q, p->d) : 0;
+  *bytes = is_backward ? sdpa::bwd_workspace_bytes(p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d) : 0;
   return ok();
 }
 
@@ -269,7 +269,7 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
   if ((st = check_view("dv", dv, p->dv, p->b, p->h_kv, p->s_kv, p->d, es)) != SDPA_OK) return st;
   if (lse == nullptr) return fail(SDPA_ERR_INVALID_ARG, "lse: null pointer (the backward pass needs the forward statistics)");
   if (reinterpret_cast<uintptr_t>(lse) % 4 != 0) return fail(SDPA_ERR_LAYOUT, "lse must be 4-byte aligned");
-  const size_t need = sdpa::bwd_workspace_bytes(p->b, p->h_q, p->s_q, p->d);
+  const size_t need = sdpa::bwd_workspace_bytes(p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given%s", need,
                 workspace_bytes, workspace ? "" : " (NULL)");
@@ -286,6 +286,21 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
   if ((st = make_map(&prm.tm_dv, "dv", dv, p->dv, p->b, p->h_kv, p->s_kv, p->d, p->out_dtype, 128)) != SDPA_OK) return st;
   const int s_q_pad = (p->s_q + 127) / 128 * 128;
   const size_t acc_bytes = align256((size_t)p->b * p->h_q * s_q_pad * p->d * 4);
+  {
+    // fp32 dQ accumulator [b*h_q*s_q_pad][d]: target of the kernel's TMA reduce-add, in
+    // 32-column (128-byte) chunks of 128 rows.
+    auto fn = encode_fn();
+    if (fn == nullptr) return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    cuuint64_t dims[2] = {(cuuint64_t)p->d, (cuuint64_t)p->b * p->h_q * s_q_pad};
+    cuuint64_t strides[1] = {(cuuint64_t)p->d * 4};
+    cuuint32_t box[2] = {32, 128};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(&prm.tm_dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, workspace, dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(SDPA_ERR_LAYOUT, "dQ accumulator: cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+  }
   const size_t vec_bytes = align256((size_t)p->b * p->h_q * s_q_pad * 4);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   prm.o = o;
@@ -309,6 +324,18 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
   prm.s_q_pad = s_q_pad;
   prm.scale = p->attn_scale;
   prm.scale_log2 = p->attn_scale * 1.4426950408889634f;
+  prm.kv_split = sdpa::bwd_kv_split(p->b, p->h_q, p->h_kv, p->s_kv);
+  prm.heads_per_split = (prm.group + prm.kv_split - 1) / prm.kv_split;
+  prm.s_kv_pad = (p->s_kv + 127) / 128 * 128;
+  prm.dk = dk;
+  prm.dv = dv;
+  prm.dk_sb = p->dk.b; prm.dk_sh = p->dk.h; prm.dk_ss = p->dk.s;
+  prm.dv_sb = p->dv.b; prm.dv_sh = p->dv.h; prm.dv_ss = p->dv.s;
+  if (prm.kv_split > 1) {
+    const size_t kv_bytes = align256((size_t)p->b * p->h_kv * prm.s_kv_pad * p->d * 4);
+    prm.dk_acc = reinterpret_cast<float*>(ws + acc_bytes + 2 * vec_bytes);
+    prm.dv_acc = reinterpret_cast<float*>(ws + acc_bytes + 2 * vec_bytes + kv_bytes);
+  }
   if ((s_q_pad / 128) > 65535 || (p->s_kv + 127) / 128 > 65535)
     return fail(SDPA_ERR_UNSUPPORTED, "grid too large");
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);

@@ -16,8 +16,8 @@
 //                 memory while the CTA walks every (query head of the group, 128-row query
 //                 block) it can see.  Per step five tcgen05 MMAs (Sᵀ = K·Qᵀ, dPᵀ = V·dOᵀ,
 //                 dV += Pᵀ·dO, dK += dSᵀ·Q, dQ = dS·K) with dV and dK accumulating in TMEM
-//                 for the whole walk and dQ drained from TMEM into the fp32 accumulator with
-//                 vector atomics by a dedicated warpgroup.
+//                 for the whole walk, and dQ drained by a dedicated warpgroup from TMEM through
+//                 shared memory into the fp32 accumulator with TMA reduce-add.
 //   3. bwd_dq:    dQ = scale·accumulator, rounded to the output dtype in the caller's strides.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -135,6 +135,45 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdParams p) {
   *reinterpret_cast<uint4*>(dst) = w;
 }
 
+// Split groups only: zero the fp32 dK/dV accumulators before the main kernel, and write
+// dK, dV in the output dtype and strides after it.
+__global__ void __launch_bounds__(256) bwd_zero_kv_kernel(const BwdParams p) {
+  const int64_t n4 = static_cast<int64_t>(p.b) * p.h_kv * p.s_kv_pad * p.d / 4;
+  float4* a = reinterpret_cast<float4*>(p.dk_acc);
+  float4* b = reinterpret_cast<float4*>(p.dv_acc);
+  for (int64_t i = blockIdx.x * 256ll + threadIdx.x; i < n4; i += 256ll * gridDim.x) {
+    a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    b[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) bwd_kv_convert_kernel(const BwdParams p) {
+  constexpr int TPR = D / 8;
+  constexpr int ROWS = 256 / TPR;
+  const int bh = blockIdx.y;
+  const int bi = bh / p.h_kv, hk = bh % p.h_kv;
+  const int row = blockIdx.x * ROWS + threadIdx.x / TPR;
+  const int part = threadIdx.x % TPR;
+  if (row >= p.s_kv) return;
+  const int dt = std::is_same<T, __nv_bfloat16>::value ? kBF16 : kF16;
+  const int64_t off = (static_cast<int64_t>(bh) * p.s_kv_pad + row) * D + part * 8;
+  for (int which = 0; which < 2; ++which) {
+    const float* src = (which == 0 ? p.dk_acc : p.dv_acc) + off;
+    const float4 a = reinterpret_cast<const float4*>(src)[0];
+    const float4 c = reinterpret_cast<const float4*>(src)[1];
+    uint4 w;
+    w.x = pack2(a.x, a.y, dt);
+    w.y = pack2(a.z, a.w, dt);
+    w.z = pack2(c.x, c.y, dt);
+    w.w = pack2(c.z, c.w, dt);
+    T* dst = which == 0
+                 ? reinterpret_cast<T*>(p.dk) + bi * p.dk_sb + hk * p.dk_sh + row * p.dk_ss + part * 8
+                 : reinterpret_cast<T*>(p.dv) + bi * p.dv_sb + hk * p.dv_sh + row * p.dv_ss + part * 8;
+    *reinterpret_cast<uint4*>(dst) = w;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // 2. main kernel
 // ---------------------------------------------------------------------------
@@ -174,6 +213,9 @@ struct alignas(8) BwdBarriers {
   uint64_t acc_full;
   uint64_t drain;
   uint64_t epi_ready[2];
+  uint64_t stage_full;   // dQ staging written by the 128 drain threads
+  uint64_t stage_free;   // the reduce-add of the last staged half has read shared memory
+  uint64_t dsbuf_free;   // the dS buffer (reused as dQ staging) may take the next dS
   uint32_t tmem_base;
   int abort;
 };
@@ -196,14 +238,17 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int bhk = blockIdx.x;
+  const int split = blockIdx.x % p.kv_split;              // share of the KV group's heads
+  const int bhk = blockIdx.x / p.kv_split;
   const int bi = bhk / p.h_kv;
   const int hk = bhk % p.h_kv;
   const int j = blockIdx.y;                                 // KV block
   const int n_qb = (p.s_q + kBlockM - 1) / kBlockM;
   const int q_first = first_q_block(p, j);
   const int per_head = q_first < n_qb ? n_qb - q_first : 0;
-  const int n_iter = per_head * p.group;
+  const int head0 = hk * p.group + split * p.heads_per_split;
+  const int n_heads = max(0, min(p.heads_per_split, (hk + 1) * p.group - head0));
+  const int n_iter = per_head * n_heads;
 
   // The 128-byte swizzle of every tile assumes a 1024-byte aligned base (the budget leaves
   // no room for manual alignment).  If that ever fails, report it and do nothing.
@@ -229,6 +274,9 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     mbar_init(&bars.drain, 1);
     mbar_init(&bars.epi_ready[0], 128);
     mbar_init(&bars.epi_ready[1], 128);
+    mbar_init(&bars.stage_full, 128);
+    mbar_init(&bars.stage_free, 1);
+    mbar_init(&bars.dsbuf_free, 1);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -243,7 +291,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   volatile int* abort_flag = &bars.abort;
 
   // iteration n -> (query head, query block)
-  auto iter_head = [&](int n) { return hk * p.group + n / per_head; };
+  auto iter_head = [&](int n) { return head0 + n / per_head; };
   auto iter_qblk = [&](int n) { return q_first + n % per_head; };
 
   if (warp == 0) {
@@ -417,9 +465,9 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       }
       tmem_st32(Y + 64 * h, ds);
       // dS for the dQ MMA: query-major (MN-major A), chunk h holds query columns 64h..64h+63,
-      // key row r at byte r*128 with the 128-byte swizzle.  The previous step's dQ MMA must
-      // have finished reading the buffer.
-      if (n >= 1 && !mbar_wait_warp(&bars.dq_full[b ^ 1], ((n - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+      // key row r at byte r*128 with the 128-byte swizzle.  The buffer doubles as the dQ
+      // staging area of the previous step, which must have been drained.
+      if (n >= 1 && !mbar_wait_warp(&bars.dsbuf_free, (n - 1) & 1, abort_flag)) { ok = false; break; }
       uint8_t* rowp = sDS + h * 16384 + r * 128;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -434,7 +482,25 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     // ---- epilogue: dV (h = 0) or dK (h = 1) through shared memory and a TMA store ----
     ok = ok && mbar_wait_warp(&bars.acc_full, 0, abort_flag);
     uint8_t* stage = sRing + h * C::TILE;
-    if (ok) {
+    if (ok && p.kv_split > 1) {
+      // Split group: add this CTA's share into the fp32 accumulator (once per CTA).
+      tc_fence_after();
+      const uint32_t acc = tmem + lane_off + (h == 0 ? C::DV_COL : C::DK_COL);
+      const float mul = (h == 0) ? 1.f : p.scale;
+      float* dst = (h == 0 ? p.dv_acc : p.dk_acc) +
+                   ((static_cast<int64_t>(bi) * p.h_kv + hk) * p.s_kv_pad + kv_row) * D;
+#pragma unroll 1
+      for (int c = 0; c < D / 32 && n_iter > 0; ++c) {
+        uint32_t v[32];
+        tmem_ld32(acc + c * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          red_add_v4(dst + c * 32 + u * 4, __uint_as_float(v[u * 4]) * mul,
+                     __uint_as_float(v[u * 4 + 1]) * mul, __uint_as_float(v[u * 4 + 2]) * mul,
+                     __uint_as_float(v[u * 4 + 3]) * mul);
+      }
+    } else if (ok) {
       tc_fence_after();
       const uint32_t acc = tmem + lane_off + (h == 0 ? C::DV_COL : C::DK_COL);
       const float mul = (h == 0) ? 1.f : p.scale;
@@ -467,7 +533,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     mbar_arrive(&bars.epi_ready[h]);
     if (r == 0) {
       const bool all_ok = mbar_wait(&bars.epi_ready[h], 0, abort_flag) && ok && !*abort_flag;
-      if (all_ok) {
+      if (all_ok && p.kv_split == 1) {
         const CUtensorMap* map = (h == 0) ? &p.tm_dv : &p.tm_dk;
         for (int c = 0; c < D / 64; ++c)
           tma_store_4d(map, stage + c * 16384, c * 64, j * kBlockN, hk, bi);
@@ -476,33 +542,71 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       }
     }
   } else if (warp >= 12) {
-    // ============================ dQ drain: TMEM -> fp32 atomics ======================
+    // ===================== dQ drain: TMEM -> shared memory -> TMA reduce-add ===========
+    // dQ of a step sits in TMEM (query row r = lane r, d columns).  It leaves in halves of
+    // d/2 columns: each half is written to the dS buffer (free once the dQ MMA has read it)
+    // as 32-column fp32 chunks of 128 rows x 128 bytes, 128-byte swizzled, then added into
+    // the fp32 accumulator by the TMA unit.  TMEM is released as soon as the last half has
+    // been read into registers.
     const int quad = warp % 4;
     const int r = quad * 32 + lane;                       // query row within the block
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    for (int n = 0; n < n_iter; ++n) {
+    constexpr int HALF = D / 2;                           // columns per round
+    constexpr int CHUNKS = HALF / 32;                     // 16 KB chunks per round
+    bool ok = true;
+    for (int n = 0; n < n_iter && ok; ++n) {
       const int b = n & 1;
-      if (!mbar_wait_warp(&bars.dq_full[b], (n >> 1) & 1, abort_flag)) break;
+      if (!mbar_wait_warp(&bars.dq_full[b], (n >> 1) & 1, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const int hq = iter_head(n);
-      const int qrow = iter_qblk(n) * kBlockM + r;
-      float* dst = p.dq_acc + ((static_cast<int64_t>(bi) * p.h_q + hq) * p.s_q_pad + qrow) * D;
+      const int row0 = (bi * p.h_q + hq) * p.s_q_pad + iter_qblk(n) * kBlockM;
       const uint32_t X = tmem + lane_off + C::R_COL + b * 128;
-#pragma unroll 1
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t v[32];
-        tmem_ld32(X + c * 32, v);
-        tmem_ld_wait();
-        if (qrow < p.s_q) {
+      // Both halves leave TMEM before any wait on the TMA unit, so the region is handed back
+      // to the next step's dPᵀ MMA as early as possible; the second half waits in registers.
+      uint32_t v[HALF];
+#pragma unroll
+      for (int c = 0; c < CHUNKS; ++c)
+        tmem_ld32(X + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
+      tmem_ld_wait();
+      auto stage = [&](const uint32_t(&vals)[HALF]) {
+#pragma unroll
+        for (int c = 0; c < CHUNKS; ++c) {
+          uint8_t* rowp = sDS + c * 16384 + r * 128;
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            red_add_v4(dst + c * 32 + u * 4, __uint_as_float(v[u * 4]), __uint_as_float(v[u * 4 + 1]),
-                       __uint_as_float(v[u * 4 + 2]), __uint_as_float(v[u * 4 + 3]));
+            *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) =
+                make_uint4(vals[c * 32 + u * 4], vals[c * 32 + u * 4 + 1],
+                           vals[c * 32 + u * 4 + 2], vals[c * 32 + u * 4 + 3]);
         }
-      }
+        fence_proxy_async_smem();
+      };
+      stage(v);
+#pragma unroll
+      for (int c = 0; c < CHUNKS; ++c)
+        tmem_ld32(X + HALF + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
+      tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&bars.dq_free[b]);
+      for (int round = 0; round < 2 && ok; ++round) {
+        if (round == 1) {
+          if (!mbar_wait_warp(&bars.stage_free, 0, abort_flag)) { ok = false; break; }
+          stage(v);
+        }
+        mbar_arrive(&bars.stage_full);
+        if (r == 0) {
+          if (!mbar_wait(&bars.stage_full, round, abort_flag)) ok = false;
+          if (ok) {
+            for (int c = 0; c < CHUNKS; ++c)
+              tma_reduce_add_2d(&p.tm_dqacc, sDS + c * 16384, round * HALF + c * 32, row0);
+            tma_store_commit();
+            tma_store_wait_read_all();
+          }
+          mbar_arrive(&bars.stage_free);
+          if (round == 1) mbar_arrive(&bars.dsbuf_free);
+        }
+      }
     }
+    if (r == 0) tma_store_wait_all();
   }
 
   tc_fence_before();
@@ -523,24 +627,48 @@ cudaError_t launch_t(const BwdParams& p, cudaStream_t st) {
   bwd_pre_kernel<T, D><<<gpre, 256, 0, st>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
+  if (p.kv_split > 1) {
+    bwd_zero_kv_kernel<<<1024, 256, 0, st>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   auto kern = bwd_main_kernel<D, DT>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 gmain(p.b * p.h_kv, (p.s_kv + kBlockN - 1) / kBlockN);
+  dim3 gmain(p.b * p.h_kv * p.kv_split, (p.s_kv + kBlockN - 1) / kBlockN);
   kern<<<gmain, C::THREADS, C::SMEM_BYTES, st>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 gdq((p.s_q + ROWS - 1) / ROWS, bh);
   bwd_dq_kernel<T, D><<<gdq, 256, 0, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.kv_split == 1) return e;
+  dim3 gkv((p.s_kv + ROWS - 1) / ROWS, p.b * p.h_kv);
+  bwd_kv_convert_kernel<T, D><<<gkv, 256, 0, st>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-size_t bwd_workspace_bytes(int b, int h_q, int s_q, int d) {
+int bwd_kv_split(int b, int h_q, int h_kv, int s_kv) {
+  // Aim for at least ~4 waves of CTAs on a 152-SM part; never split finer than one head.
+  constexpr long kTargetCtas = 608;
+  const int group = h_q / h_kv;
+  const long ctas = static_cast<long>(b) * h_kv * ((s_kv + 127) / 128);
+  if (group == 1 || ctas >= kTargetCtas) return 1;
+  int want = static_cast<int>((kTargetCtas + ctas - 1) / ctas);
+  if (want > group) want = group;
+  const int per = (group + want - 1) / want;   // heads per CTA
+  return (group + per - 1) / per;
+}
+
+size_t bwd_workspace_bytes(int b, int h_q, int h_kv, int s_q, int s_kv, int d) {
   const size_t pad = static_cast<size_t>((s_q + 127) / 128) * 128;
+  const size_t kv_pad = static_cast<size_t>((s_kv + 127) / 128) * 128;
   auto a = [](size_t x) { return (x + 255) & ~size_t(255); };
-  return a(static_cast<size_t>(b) * h_q * pad * d * 4) + 2 * a(static_cast<size_t>(b) * h_q * pad * 4);
+  size_t n = a(static_cast<size_t>(b) * h_q * pad * d * 4) + 2 * a(static_cast<size_t>(b) * h_q * pad * 4);
+  if (bwd_kv_split(b, h_q, h_kv, s_kv) > 1) n += 2 * a(static_cast<size_t>(b) * h_kv * kv_pad * d * 4);
+  return n;
 }
 
 cudaError_t launch_bwd(const BwdParams& p, int dtype, cudaStream_t st) {

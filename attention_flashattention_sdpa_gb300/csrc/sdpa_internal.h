@@ -38,6 +38,7 @@ uint32_t fwd_take_device_error();
 struct BwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_do;   // loads (128-byte swizzled)
   CUtensorMap tm_dk, tm_dv;              // stores
+  CUtensorMap tm_dqacc;                  // fp32 [b*h_q*s_q_pad][d], reduce-add target
   const void* o;       // forward output, for Delta
   const void* dout;    // incoming gradient, for Delta
   const float* lse;    // [b][h_q][s_q]
@@ -54,9 +55,24 @@ struct BwdParams {
   int s_q_pad;                  // s_q rounded up to 128
   float scale;                  // attn_scale
   float scale_log2;             // attn_scale * log2(e)
+  // Split groups: when a KV head's query heads are shared between `kv_split` CTAs, each CTA
+  // adds its dK/dV partial into fp32 accumulators and a last pass writes dK, dV.
+  int kv_split;                 // CTAs per (batch, KV head, KV block); 1 = no split
+  int heads_per_split;          // query heads one such CTA visits
+  int s_kv_pad;                 // s_kv rounded up to 128
+  float* dk_acc;                // workspace [b][h_kv][s_kv_pad][d] fp32 (split only)
+  float* dv_acc;
+  void* dk;                     // outputs (split only: written by the convert pass)
+  void* dv;
+  int64_t dk_sb, dk_sh, dk_ss;
+  int64_t dv_sb, dv_sh, dv_ss;
 };
 
-size_t bwd_workspace_bytes(int b, int h_q, int s_q, int d);
+// How many CTAs share one (batch, KV head, KV block) in the backward pass.  A fixed policy
+// of the shape alone (no device query), so workspace sizing and launch always agree.
+int bwd_kv_split(int b, int h_q, int h_kv, int s_kv);
+
+size_t bwd_workspace_bytes(int b, int h_q, int h_kv, int s_q, int s_kv, int d);
 cudaError_t launch_bwd(const BwdParams& p, int dtype, cudaStream_t st);
 uint32_t bwd_take_device_error();
 

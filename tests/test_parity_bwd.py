@@ -74,3 +74,14 @@ def test_longer_sequence_and_invariants():
     sv = dv.float().sum(dim=2).cpu().numpy()
     want = x.do.float().reshape(1, 2, 2, 1280, 128).sum(dim=(2, 3)).numpy()
     assert np.abs(sv - want).max() <= 1e-2 * max(1.0, np.abs(want).max())
+
+
+def test_grouped_heads_without_split():
+    """Enough CTAs that each KV head's whole group stays in one CTA (no fp32 dK/dV pass)."""
+    _check(Workload("t", 4, 32, 16, 1280, 1280, 128, "bf16", causal=True, backward=True), seed=17)
+
+
+@pytest.mark.parametrize("h_kv", [1, 2])
+def test_split_groups_small_batch(h_kv):
+    """Few KV heads: the query heads of a group are split over several CTAs."""
+    _check(Workload("t", 1, 16, h_kv, 700, 700, 64, "f16", causal=False, backward=True), seed=h_kv)

@@ -1,0 +1,123 @@
+"""GPU parity at the full workload sizes, on sampled outputs.
+
+Each configuration runs exactly as bench.py launches it (same shapes, dtypes, layouts).
+The oracle then checks what it can compute cheaply and exactly:
+  * O and LSE of seeded (batch, head, row) triples (each row needs only its KV head);
+  * dQ of the same rows;
+  * full dK and dV of seeded (batch, KV head) pairs where the group is small enough;
+  * for MQA, whose single KV head gathers 64 query heads, the exact sums that hold at any
+    size (Σ_j dK_j = 0, Σ_j dV_j = Σ dO over the group) instead of a full dK/dV.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sdpa_workloads import (fp8_large_head, gpt2_inference, grouped, make_inputs,
+                            sample_kv_heads, sample_rows, training)
+from sdpa_testlib import (FP8_REL_L2, FWD_MAX_ABS, GRAD_REL_L2, LSE_ABS, assert_fwd_close,
+                          assert_grad_close, f64, rel_l2, run_bwd, run_fwd)
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+N_ROWS = 64
+
+
+def _rows_f64(t, bi, h, rows, descale=1.0):
+    if t.dtype == torch.float8_e4m3fn:  # CPU float8 tensors cannot be indexed: go via bytes
+        return oracle.decode_e4m3(t.view(torch.uint8)[bi, h, rows].numpy(), descale)
+    return oracle.to_f64(t[bi, h, rows].cpu(), descale)
+
+
+def _check_rows(w, x, o, lse, dq=None, descales=(1.0, 1.0, 1.0), rel=None):
+    dsq, dsk, dsv = descales
+    by_head = {}
+    for bi, h, r in sample_rows(w, N_ROWS):
+        by_head.setdefault((bi, h), []).append(r)
+    got_o, want_o, got_l, want_l, got_q, want_q = [], [], [], [], [], []
+    for (bi, h), rows in by_head.items():
+        rows = sorted(set(rows))
+        hk = oracle.kv_head_of(h, w.h_q, w.h_kv)
+        kh = _rows_f64(x.k, bi, hk, slice(None), dsk)
+        vh = _rows_f64(x.v, bi, hk, slice(None), dsv)
+        qr = _rows_f64(x.q, bi, h, rows, dsq)
+        O, L = oracle.forward_rows(qr, rows, kh, vh, w.scale, w.causal)
+        got_o.append(f64(o[bi, h, rows]))
+        want_o.append(O)
+        if lse is not None:
+            got_l.append(lse[bi, h, rows].cpu().double().numpy())
+            want_l.append(L)
+        if dq is not None:
+            dor = _rows_f64(x.do, bi, h, rows)
+            want_q.append(oracle.backward_dq_rows(qr, dor, rows, kh, vh, w.scale, w.causal))
+            got_q.append(f64(dq[bi, h, rows]))
+    go, wo = np.concatenate(got_o), np.concatenate(want_o)
+    if rel is None:
+        assert_fwd_close(go, wo)
+    else:
+        assert rel_l2(go, wo) <= rel, f"O rel-L2 {rel_l2(go, wo):.3e}"
+    if got_l:
+        err = np.abs(np.concatenate(got_l) - np.concatenate(want_l)).max()
+        assert err <= LSE_ABS, f"LSE max abs err {err:.3e}"
+    if got_q:
+        assert_grad_close(np.concatenate(got_q), np.concatenate(want_q), "dQ rows")
+
+
+def _full_case(w, dkv_pairs: int):
+    x = make_inputs(w, seed=0, with_do=True)
+    o, lse, dev = run_fwd(w, x)
+    dq, dk, dv = run_bwd(w, dev, o, lse, x.do)
+    _check_rows(w, x, o, lse, dq)
+    if dkv_pairs:
+        q64, k64, v64, do64 = (oracle.to_f64(t) for t in (x.q, x.k, x.v, x.do))
+        for bi, hk in sample_kv_heads(w, dkv_pairs)[:dkv_pairs]:
+            gk, gv = oracle.backward_kv_head(q64, k64, v64, do64, w.scale, w.causal, bi, hk)
+            assert_grad_close(f64(dk[bi, hk]), gk, f"dK[{bi},{hk}]")
+            assert_grad_close(f64(dv[bi, hk]), gv, f"dV[{bi},{hk}]")
+    return x, dq, dk, dv
+
+
+def test_training_s8192_as_benchmarked():
+    _full_case(training(8192), dkv_pairs=2)
+
+
+def test_training_s16384_rows():
+    w = training(16384)
+    x = make_inputs(w, seed=0, with_do=True)
+    o, lse, dev = run_fwd(w, x)
+    dq, _, _ = run_bwd(w, dev, o, lse, x.do)
+    _check_rows(w, x, o, lse, dq)
+
+
+def test_gqa_70b():
+    _full_case(grouped(8), dkv_pairs=1)
+
+
+def test_mha_70b():
+    _full_case(grouped(64), dkv_pairs=1)
+
+
+def test_mqa_70b_rows_and_exact_sums():
+    w = grouped(1)
+    x, dq, dk, dv = _full_case(w, dkv_pairs=0)
+    sk = dk.double().sum(dim=2).cpu().numpy()
+    scale_k = np.abs(dk.double().cpu().numpy()).sum(axis=2).max()
+    assert np.abs(sk).max() <= 1e-2 * scale_k
+    sv = dv.double().sum(dim=2).cpu().numpy()[0, 0]
+    want = x.do.double().sum(dim=(1, 2)).numpy()[0]
+    assert rel_l2(sv, want) <= GRAD_REL_L2
+
+
+def test_gpt2_inference_full():
+    w = gpt2_inference()
+    x = make_inputs(w, seed=0, with_do=False)
+    o, lse, _ = run_fwd(w, x, with_lse=False)
+    O, _ = oracle.forward(f64(x.q), f64(x.k), f64(x.v), w.scale, w.causal)
+    assert_fwd_close(f64(o), O)
+
+
+def test_fp8_large_head_rows():
+    w = fp8_large_head()
+    x = make_inputs(w, seed=0, with_do=False)
+    o, lse, _ = run_fwd(w, x)
+    _check_rows(w, x, o, lse, None, (x.descale_q, x.descale_k, x.descale_v), rel=FP8_REL_L2)
