@@ -240,7 +240,7 @@ sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const void* k, co
   prm.num_m_blocks = (p->s_q + rows_per_cta - 1) / rows_per_cta;
   prm.scale_log2 = scale_log2_of(p->attn_scale);
   prm.negate_scores = p->attn_scale < 0.f ? 1 : 0;
-  if ((int64_t)p->b * p->h_q > 0x7fffffff || prm.num_m_blocks > 65535)
+  if ((int64_t)p->b * p->h_q * prm.num_m_blocks > 0x7fffffff)
     return fail(SDPA_ERR_UNSUPPORTED, "grid too large");
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (log_level() >= 1)
@@ -336,8 +336,10 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
     prm.dk_acc = reinterpret_cast<float*>(ws + acc_bytes + 2 * vec_bytes);
     prm.dv_acc = reinterpret_cast<float*>(ws + acc_bytes + 2 * vec_bytes + kv_bytes);
   }
-  if ((s_q_pad / 128) > 65535 || (p->s_kv + 127) / 128 > 65535)
-    return fail(SDPA_ERR_UNSUPPORTED, "grid too large");
+  // The per-row passes put (batch, head) on grid.y.
+  if ((int64_t)p->b * p->h_q > 65535 ||
+      (int64_t)p->b * p->h_kv * prm.kv_split * ((p->s_kv + 127) / 128) > 0x7fffffff)
+    return fail(SDPA_ERR_UNSUPPORTED, "grid too large (b*h_q must be <= 65535 for the backward pass)");
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (log_level() >= 1)
     fprintf(stderr, "[sdpa] bwd b=%d h_q=%d h_kv=%d s_q=%d s_kv=%d d=%d dt=%d causal=%d ws=%zu\n",

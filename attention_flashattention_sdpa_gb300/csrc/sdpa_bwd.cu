@@ -182,13 +182,15 @@ template <int D>
 struct BwdCfg {
   static constexpr int TILE = kBlockM * D * 2;        // one 128-row tile of Q, K, V or dO
   static constexpr int NCHUNK = D / 64;               // 128-byte chunks along d
-  static constexpr int NSLOT = 4;                     // Q / dO ring
+  static constexpr int NSLOT = (D == 64) ? 4 : 3;     // Q / dO ring
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = TILE;
   static constexpr int OFF_RING = 2 * TILE;
   static constexpr int OFF_DS = OFF_RING + NSLOT * TILE;
   static constexpr int DS_BYTES = kBlockM * kBlockN * 2;
-  static constexpr int OFF_VEC = OFF_DS + DS_BYTES;   // [2 buffers][LSE2, Delta][128] fp32
+  static constexpr int OFF_DQ = OFF_DS + DS_BYTES;    // dQ staging: two 32-column fp32 chunks
+  static constexpr int DQ_BYTES = 2 * 16384;
+  static constexpr int OFF_VEC = OFF_DQ + DQ_BYTES;   // [2 buffers][LSE2, Delta][128] fp32
   static constexpr int OFF_BAR = OFF_VEC + 2 * 2 * 128 * 4;
   static constexpr int SMEM_BYTES = OFF_BAR + 512;
   static constexpr int THREADS = 512;
@@ -213,9 +215,9 @@ struct alignas(8) BwdBarriers {
   uint64_t acc_full;
   uint64_t drain;
   uint64_t epi_ready[2];
-  uint64_t stage_full;   // dQ staging written by the 128 drain threads
-  uint64_t stage_free;   // the reduce-add of the last staged half has read shared memory
-  uint64_t dsbuf_free;   // the dS buffer (reused as dQ staging) may take the next dS
+  uint64_t dp_consumed[2];  // the compute warps have read dPᵀ out of TMEM
+  uint64_t stage_full;      // dQ staging written by the 128 drain threads
+  uint64_t stage_free;      // the reduce-add of the last staged half has read shared memory
   uint32_t tmem_base;
   int abort;
 };
@@ -234,15 +236,21 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   uint8_t* sV = smem + C::OFF_V;
   uint8_t* sRing = smem + C::OFF_RING;
   uint8_t* sDS = smem + C::OFF_DS;
+  uint8_t* sDQ = smem + C::OFF_DQ;
   float* sVec = reinterpret_cast<float*>(smem + C::OFF_VEC);
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  const int split = blockIdx.x % p.kv_split;              // share of the KV group's heads
-  const int bhk = blockIdx.x / p.kv_split;
+  // Head-major launch order: all KV blocks of one (batch, KV head, share) before the next,
+  // so resident CTAs share a few heads' Q, dO and dQ accumulator in L2; within a head the
+  // heaviest KV blocks (the first ones, for causal) go first.
+  const int n_kvb = (p.s_kv + kBlockN - 1) / kBlockN;
+  const int j = blockIdx.x % n_kvb;                         // KV block
+  const int unit = blockIdx.x / n_kvb;
+  const int split = unit % p.kv_split;                      // share of the KV group's heads
+  const int bhk = unit / p.kv_split;
   const int bi = bhk / p.h_kv;
   const int hk = bhk % p.h_kv;
-  const int j = blockIdx.y;                                 // KV block
   const int n_qb = (p.s_q + kBlockM - 1) / kBlockM;
   const int q_first = first_q_block(p, j);
   const int per_head = q_first < n_qb ? n_qb - q_first : 0;
@@ -274,9 +282,10 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     mbar_init(&bars.drain, 1);
     mbar_init(&bars.epi_ready[0], 128);
     mbar_init(&bars.epi_ready[1], 128);
+    mbar_init(&bars.dp_consumed[0], 256);
+    mbar_init(&bars.dp_consumed[1], 256);
     mbar_init(&bars.stage_full, 128);
     mbar_init(&bars.stage_free, 1);
-    mbar_init(&bars.dsbuf_free, 1);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -341,24 +350,30 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       bool ok = mbar_wait(&bars.kv_full, 0, abort_flag);
       tc_fence_after();
       int it = 0;
-      for (int n = 0; n < n_iter && ok; ++n) {
-        const int b = n & 1;
-        const uint32_t par = (n >> 1) & 1;
-        const uint32_t X = tmem + C::R_COL + b * 128;
-        const uint32_t Y = tmem + C::R_COL + (b ^ 1) * 128;
-        // ---- Sᵀ = K·Qᵀ ----
-        const int qslot = it % C::NSLOT;
-        if (!mbar_wait(&bars.ring_full[qslot], (it / C::NSLOT) & 1, abort_flag)) { ok = false; break; }
+      // Sᵀ = K·Qᵀ of step m into region `reg`.
+      auto issue_s = [&](int reg, int& qslot) -> bool {
+        qslot = it % C::NSLOT;
+        if (!mbar_wait(&bars.ring_full[qslot], (it / C::NSLOT) & 1, abort_flag)) return false;
         ++it;
         tc_fence_after();
         const uint32_t qB = smem_u32(sRing + qslot * C::TILE);
 #pragma unroll
         for (int k = 0; k < C::KSTEPS_D; ++k) {
           const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
-          mma_ss(X, make_sdesc_sw128(kA + off, 16, 1024), make_sdesc_sw128(qB + off, 16, 1024),
-                 idesc_sq, k > 0, false);
+          mma_ss(tmem + C::R_COL + reg * 128, make_sdesc_sw128(kA + off, 16, 1024),
+                 make_sdesc_sw128(qB + off, 16, 1024), idesc_sq, k > 0, false);
         }
-        tc_commit(&bars.s_full[b]);
+        tc_commit(&bars.s_full[reg]);
+        return true;
+      };
+      int qslot = 0, qslot_next = 0;
+      if (ok && n_iter > 0) ok = issue_s(0, qslot);
+      for (int n = 0; n < n_iter && ok; ++n) {
+        const int b = n & 1;
+        const uint32_t par = (n >> 1) & 1;
+        const uint32_t X = tmem + C::R_COL + b * 128;         // Sᵀ, Pᵀ, then dQ of step n
+        const uint32_t Y = tmem + C::R_COL + (b ^ 1) * 128;   // dPᵀ of step n, then Sᵀ of n+1
+        const uint32_t qB = smem_u32(sRing + qslot * C::TILE);
         // ---- dPᵀ = V·dOᵀ (into the region dQ of the previous step used) ----
         const int gslot = it % C::NSLOT;
         if (!mbar_wait(&bars.ring_full[gslot], (it / C::NSLOT) & 1, abort_flag)) { ok = false; break; }
@@ -383,14 +398,20 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
                  idesc_acc, (n > 0 || k > 0) ? 1u : 0u, false);
         }
         tc_commit(&bars.ring_empty[gslot]);
-        // ---- dK += dSᵀ·Q ; dQ = dS·K ----
+        // ---- Sᵀ of the next step, as soon as dPᵀ has left region Y ----
+        if (n + 1 < n_iter) {
+          if (!mbar_wait(&bars.dp_consumed[b], par, abort_flag)) { ok = false; break; }
+          if (!issue_s(b ^ 1, qslot_next)) { ok = false; break; }
+        }
+        // ---- dK += dSᵀ·Q (dS read K-major from shared memory) ; dQ = dS·K ----
         if (!mbar_wait(&bars.ds_full[b], par, abort_flag)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const uint32_t a_col = (k < 4) ? k * 8 : 64 + (k - 4) * 8;
-          mma_ts(tmem + C::DK_COL, Y + a_col, make_sdesc_sw128(qB + k * 2048, 16384, 1024),
-                 idesc_acc, (n > 0 || k > 0) ? 1u : 0u, false);
+          const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
+          mma_ss(tmem + C::DK_COL, make_sdesc_sw128(dsA + off, 16, 1024),
+                 make_sdesc_sw128(qB + k * 2048, 16384, 1024), idesc_acc,
+                 (n > 0 || k > 0) ? 1u : 0u, false);
         }
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -399,6 +420,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         }
         tc_commit(&bars.dq_full[b]);
         tc_commit(&bars.ring_empty[qslot]);
+        qslot = qslot_next;
       }
       tc_commit(&bars.acc_full);
       tc_commit(&bars.drain);
@@ -455,6 +477,8 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       tmem_ld32(Y + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
       tmem_ld32(Y + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
       tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.dp_consumed[b]);   // region Y may now take the next step's Sᵀ
       uint32_t ds[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
@@ -463,11 +487,11 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         const float d1 = pp.y * (__uint_as_float(sv[c + 1]) - delta[c + 1]);
         ds[c / 2] = pack2(d0, d1, DT);
       }
-      tmem_st32(Y + 64 * h, ds);
-      // dS for the dQ MMA: query-major (MN-major A), chunk h holds query columns 64h..64h+63,
-      // key row r at byte r*128 with the 128-byte swizzle.  The buffer doubles as the dQ
-      // staging area of the previous step, which must have been drained.
-      if (n >= 1 && !mbar_wait_warp(&bars.dsbuf_free, (n - 1) & 1, abort_flag)) { ok = false; break; }
+      // dS in shared memory, one 128-byte swizzled row per key row r, chunk h holding query
+      // columns 64h..64h+63: read K-major (rows = keys) as the A operand of dK += dSᵀ·Q and
+      // MN-major (rows = queries) as the A operand of dQ = dS·K.  The previous step's dK and
+      // dQ MMAs must have finished reading it.
+      if (n >= 1 && !mbar_wait_warp(&bars.dq_full[b ^ 1], ((n - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
       uint8_t* rowp = sDS + h * 16384 + r * 128;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -475,8 +499,6 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) = w;
       }
       fence_proxy_async_smem();
-      tmem_st_wait();
-      tc_fence_before();
       mbar_arrive(&bars.ds_full[b]);
     }
     // ---- epilogue: dV (h = 0) or dK (h = 1) through shared memory and a TMA store ----
@@ -544,10 +566,9 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   } else if (warp >= 12) {
     // ===================== dQ drain: TMEM -> shared memory -> TMA reduce-add ===========
     // dQ of a step sits in TMEM (query row r = lane r, d columns).  It leaves in halves of
-    // d/2 columns: each half is written to the dS buffer (free once the dQ MMA has read it)
-    // as 32-column fp32 chunks of 128 rows x 128 bytes, 128-byte swizzled, then added into
-    // the fp32 accumulator by the TMA unit.  TMEM is released as soon as the last half has
-    // been read into registers.
+    // d/2 columns: each half is written to a staging buffer as 32-column fp32 chunks of
+    // 128 rows x 128 bytes, 128-byte swizzled, then added into the fp32 accumulator by the
+    // TMA unit.  TMEM is released as soon as the last half has been read into registers.
     const int quad = warp % 4;
     const int r = quad * 32 + lane;                       // query row within the block
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -563,15 +584,10 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       const uint32_t X = tmem + lane_off + C::R_COL + b * 128;
       // Both halves leave TMEM before any wait on the TMA unit, so the region is handed back
       // to the next step's dPᵀ MMA as early as possible; the second half waits in registers.
-      uint32_t v[HALF];
-#pragma unroll
-      for (int c = 0; c < CHUNKS; ++c)
-        tmem_ld32(X + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
-      tmem_ld_wait();
       auto stage = [&](const uint32_t(&vals)[HALF]) {
 #pragma unroll
         for (int c = 0; c < CHUNKS; ++c) {
-          uint8_t* rowp = sDS + c * 16384 + r * 128;
+          uint8_t* rowp = sDQ + c * 16384 + r * 128;
 #pragma unroll
           for (int u = 0; u < 8; ++u)
             *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) =
@@ -580,6 +596,13 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         }
         fence_proxy_async_smem();
       };
+      uint32_t v[HALF];
+#pragma unroll
+      for (int c = 0; c < CHUNKS; ++c)
+        tmem_ld32(X + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
+      tmem_ld_wait();
+      // The staging buffer is free once the previous half's reduce-add has read it.
+      if (n >= 1 && !mbar_wait_warp(&bars.stage_free, 1, abort_flag)) { ok = false; break; }
       stage(v);
 #pragma unroll
       for (int c = 0; c < CHUNKS; ++c)
@@ -597,12 +620,11 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
           if (!mbar_wait(&bars.stage_full, round, abort_flag)) ok = false;
           if (ok) {
             for (int c = 0; c < CHUNKS; ++c)
-              tma_reduce_add_2d(&p.tm_dqacc, sDS + c * 16384, round * HALF + c * 32, row0);
+              tma_reduce_add_2d(&p.tm_dqacc, sDQ + c * 16384, round * HALF + c * 32, row0);
             tma_store_commit();
             tma_store_wait_read_all();
           }
           mbar_arrive(&bars.stage_free);
-          if (round == 1) mbar_arrive(&bars.dsbuf_free);
         }
       }
     }
@@ -635,7 +657,7 @@ cudaError_t launch_t(const BwdParams& p, cudaStream_t st) {
   auto kern = bwd_main_kernel<D, DT>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 gmain(p.b * p.h_kv * p.kv_split, (p.s_kv + kBlockN - 1) / kBlockN);
+  const unsigned gmain = static_cast<unsigned>(p.b) * p.h_kv * p.kv_split * ((p.s_kv + kBlockN - 1) / kBlockN);
   kern<<<gmain, C::THREADS, C::SMEM_BYTES, st>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

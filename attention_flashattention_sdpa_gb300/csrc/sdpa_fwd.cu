@@ -117,12 +117,15 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  // ---- tile coordinates: heaviest (latest) query tiles launch first -----------------
-  const int bh = blockIdx.x;
+  // ---- tile coordinates ----------------------------------------------------------------
+  // Launch order: all (batch, head) pairs of the heaviest query tile (the latest, for
+  // causal) first, then the next heaviest, and so on — a longest-first schedule.
+  const int n_bh = p.b * p.h_q;
+  const int bh = blockIdx.x % n_bh;
   const int bi = bh / p.h_q;
   const int hq = bh % p.h_q;
   const int hk = hq / p.group;
-  const int m_blk = p.num_m_blocks - 1 - blockIdx.y;
+  const int m_blk = p.num_m_blocks - 1 - blockIdx.x / n_bh;
   const int m0 = m_blk * kBlockM * NQT;
   const int n_blocks = kv_blocks_for(p, m0, kBlockM * NQT);
 
@@ -461,7 +464,7 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t st) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.b * p.h_q, p.num_m_blocks);
+  const unsigned grid = static_cast<unsigned>(p.b) * p.h_q * p.num_m_blocks;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(p);
   return cudaGetLastError();
 }
