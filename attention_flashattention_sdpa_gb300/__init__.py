@@ -18,7 +18,7 @@ from typing import Optional
 __all__ = [
     "SdpaError", "Strides", "Problem", "lib", "LIB_PATH", "dtype_code", "make_problem",
     "sdpa_workspace_size", "sdpa_fwd", "sdpa_bwd", "sdpa_last_error_string",
-    "sdpa_device_error", "sdpa_version", "STATUS",
+    "sdpa_device_error", "sdpa_version", "sdpa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "STATUS",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsdpa_gb300.so")
@@ -69,6 +69,8 @@ def _load():
     L.sdpa_fwd.restype = ctypes.c_int
     L.sdpa_bwd.argtypes = [P, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]
     L.sdpa_bwd.restype = ctypes.c_int
+    L.sdpa_bwd_noalloc.argtypes = [P, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP]
+    L.sdpa_bwd_noalloc.restype = ctypes.c_int
     L.sdpa_last_error_string.argtypes = []
     L.sdpa_last_error_string.restype = ctypes.c_char_p
     L.sdpa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -165,6 +167,20 @@ def sdpa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, *, attn_scale: Option
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.sdpa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
                         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20  # SDPA_NOALLOC_SCRATCH_BYTES in include/sdpa.h
+
+
+def sdpa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, *, attn_scale: Optional[float] = None,
+                     causal: bool = False, stream=None) -> None:
+    """sdpa_bwd without a workspace, for callers that cannot allocate device memory: the
+    scratch is a fixed 32 MiB array inside the library, shared by every call (calls must not
+    overlap on the GPU; larger problems raise SdpaError with SDPA_ERR_UNSUPPORTED)."""
+    p = make_problem(q, k, v, o, attn_scale=attn_scale, causal=causal, dout=dout, dq=dq, dk=dk,
+                     dv=dv)
+    _check(lib.sdpa_bwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout),
+                                _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
 
 
 def sdpa_device_error() -> int:

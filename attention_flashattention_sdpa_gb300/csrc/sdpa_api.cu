@@ -348,6 +348,53 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
   return finish_launch(e, stream, "sdpa_bwd");
 }
 
+}  // extern "C"
+
+// Scratch for sdpa_bwd_noalloc: a fixed device array, so callers that cannot allocate still
+// get a backward pass.  In host code its name is only a stand-in; the device address comes
+// from cudaGetSymbolAddress, once per device, with that device current.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[SDPA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+extern "C" {
+
+sdpa_status_t sdpa_bwd_noalloc(const sdpa_problem_t* p, const void* q, const void* k,
+                               const void* v, const void* o, const void* dout, const float* lse,
+                               void* dq, void* dk, void* dv, void* stream) {
+  sdpa_status_t st = check_problem(p, true);
+  if (st != SDPA_OK) return st;
+  const size_t need = sdpa::bwd_workspace_bytes(p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d);
+  if (need > SDPA_NOALLOC_SCRATCH_BYTES)
+    return fail(SDPA_ERR_UNSUPPORTED,
+                "sdpa_bwd_noalloc: this problem needs %zu bytes of scratch but the built-in "
+                "scratch holds %zu; call sdpa_bwd with a workspace instead",
+                need, (size_t)SDPA_NOALLOC_SCRATCH_BYTES);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "sdpa_bwd_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices)
+    return fail(SDPA_ERR_UNSUPPORTED, "sdpa_bwd_noalloc: device %d out of range", dev);
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (g_noalloc_ptr[dev] == nullptr) {
+      void* ptr = nullptr;
+      e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+      if (e != cudaSuccess || ptr == nullptr)
+        return fail(SDPA_ERR_CUDA, "sdpa_bwd_noalloc: cudaGetSymbolAddress of the scratch failed: %s",
+                    cudaGetErrorString(e));
+      g_noalloc_ptr[dev] = ptr;
+    }
+    scratch = g_noalloc_ptr[dev];
+  }
+  return sdpa_bwd(p, q, k, v, o, dout, lse, dq, dk, dv, scratch, SDPA_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 const char* sdpa_last_error_string(void) { return g_last_error.c_str(); }
 
 sdpa_status_t sdpa_device_error(uint32_t* flags) {

@@ -135,6 +135,33 @@ SDPA_API sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const vo
                        void* dv, void* workspace, size_t workspace_bytes,
                        void* stream /* cudaStream_t */);
 
+/*
+ * Size of the built-in scratch that sdpa_bwd_noalloc uses: 32 MiB of device memory, held by
+ * every GPU on which the library's kernels are loaded, until the process exits.
+ */
+#define SDPA_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+
+/*
+ * sdpa_bwd_noalloc: the backward pass of sdpa_bwd for callers that cannot allocate device
+ * memory — for example a plugin running inside a host framework that owns all device
+ * memory and offers no allocator, or a latency-critical loop that must not call cudaMalloc
+ * (which can synchronise the device).  Arguments and results are those of sdpa_bwd minus
+ * the workspace: the scratch comes from a fixed array inside the library
+ * (SDPA_NOALLOC_SCRATCH_BYTES), so nothing is allocated or freed.  The pages have no
+ * counterpart of this entry point.
+ *   - Problems whose workspace (sdpa_workspace_size(p, 1)) exceeds the array are rejected
+ *     with SDPA_ERR_UNSUPPORTED and a message giving both sizes; use sdpa_bwd then.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - Every call shares the one array (whatever it held is overwritten; each call clears
+ *     what must start at zero), so calls whose executions overlap on the GPU — on different
+ *     streams, or from different threads — race and give wrong results.  Serialise them.
+ */
+SDPA_API sdpa_status_t sdpa_bwd_noalloc(const sdpa_problem_t* p, const void* q, const void* k,
+                                        const void* v, const void* o, const void* dout,
+                                        const float* lse, void* dq, void* dk, void* dv,
+                                        void* stream /* cudaStream_t */);
+
 /* Message for the last non-OK status returned on the calling thread ("" if none).  The
  * pointer stays valid until the next library call on this thread [cuDNN 9 blog: errors
  * come with a retrievable last-error string]. */
