@@ -395,12 +395,19 @@ def run_cuda(args):
 
 
 def _load_traffic():
-    """DRAM bytes per launch of the backward main kernel from the committed ncu summary, or
-    None when no capture of the current kernel exists."""
+    """DRAM bytes per launch of the backward main kernel from the committed ncu capture, or
+    None when there is none or the kernel's sources changed since it was taken."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
+        m = hashlib.sha256()
+        for rel in d["source_files"]:
+            with open(os.path.join(ROOT, rel), "rb") as f:
+                m.update(f.read())
+        if m.hexdigest() != d["source_sha256"]:
+            return None
         return d.get("bwd_main_dram_bytes_per_launch")
     except Exception:
         return None
