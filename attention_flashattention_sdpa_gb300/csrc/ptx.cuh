@@ -114,6 +114,26 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) 
 }
 
 // ---------------------------------------------------------------------------
+// per-warpgroup register budgets (all four warps of a warpgroup execute these)
+// ---------------------------------------------------------------------------
+
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Wait until at most N committed bulk groups of this thread still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// ---------------------------------------------------------------------------
 // fences / named barriers
 // ---------------------------------------------------------------------------
 
@@ -355,6 +375,24 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// 2^x on the FMA/ALU pipes, to take part of the exponentials off the MUFU unit.
+// x = j + f with j = round(x) and f in [-1/2, 1/2]: adding 1.5 * 2^23 rounds x to an integer
+// held in the low mantissa bits of t.  2^f comes from a cubic fitted (Remez exchange on the
+// relative error) on [-1/2, 1/2]: max relative error 7.5e-5, below half an ulp of the fp16 /
+// bf16 / e4m3 values it feeds.  2^j is added to the exponent field: the low 9 bits of t's
+// pattern hold j, so (bits(t) << 23) is j << 23.  x is clamped at -125 (result >= 2^-125), and
+// must stay below 127.
+__device__ __forceinline__ float exp2_poly(float x) {
+  constexpr float kRound = 12582912.0f;   // 1.5 * 2^23
+  constexpr float c0 = 0.9999280571937561f, c1 = 0.6932609677314758f;
+  constexpr float c2 = 0.2426111251115799f, c3 = 0.0551716685295105f;
+  x = fmaxf(x, -125.0f);
+  const float t = x + kRound;
+  const float f = x - (t - kRound);
+  const float p = fmaf(fmaf(fmaf(c3, f, c2), f, c1), f, c0);
+  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
 }
 
 }  // namespace ptx

@@ -216,8 +216,8 @@ struct alignas(8) BwdBarriers {
   uint64_t drain;
   uint64_t epi_ready[2];
   uint64_t dp_consumed[2];  // the compute warps have read dPᵀ out of TMEM
-  uint64_t stage_full;      // dQ staging written by the 128 drain threads
-  uint64_t stage_free;      // the reduce-add of the last staged half has read shared memory
+  uint64_t stage_full[2];   // dQ staging buffer written by the 128 drain threads
+  uint64_t stage_free[2];   // the reduce-add of that buffer has read shared memory
   uint32_t tmem_base;
   int abort;
 };
@@ -284,8 +284,10 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     mbar_init(&bars.epi_ready[1], 128);
     mbar_init(&bars.dp_consumed[0], 256);
     mbar_init(&bars.dp_consumed[1], 256);
-    mbar_init(&bars.stage_full, 128);
-    mbar_init(&bars.stage_free, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars.stage_full[i], 128);
+      mbar_init(&bars.stage_free[i], 1);
+    }
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -303,6 +305,10 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   auto iter_head = [&](int n) { return head0 + n / per_head; };
   auto iter_qblk = [&](int n) { return q_first + n % per_head; };
 
+  // Register budget per thread: 64 for the producer / MMA warpgroup, 152 for each compute
+  // warpgroup, 144 for the dQ drain (64 + 2 x 152 + 144 = 4 x 128, the launch's budget).
+  if (warp < 4) {
+  regs_dec<64>();
   if (warp == 0) {
     // ================================ TMA producer ====================================
     if (elect_one_sync()) {
@@ -426,7 +432,9 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       tc_commit(&bars.drain);
       mbar_wait_drain(&bars.drain, 0);
     }
-  } else if (warp >= 4 && warp < 12) {
+  }
+  } else if (warp < 12) {
+    regs_inc<152>();
     // ============================ Pᵀ / dSᵀ (two column halves) ========================
     const int h = (warp - 4) / 4;                         // query columns [64h, 64h+64)
     const int quad = warp % 4;
@@ -454,10 +462,19 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       const bool need_mask = p.causal && (q0 < j * kBlockN + kBlockN - 1);
       const int lim = kv_row - q0;                        // column c visible iff c >= lim
       uint32_t pk[32];
+      float lv[64];
+#pragma unroll
+      for (int c = 0; c < 64; c += 4) {
+        const float4 t4 = *reinterpret_cast<const float4*>(lse2 + c);
+        lv[c] = t4.x; lv[c + 1] = t4.y; lv[c + 2] = t4.z; lv[c + 3] = t4.w;
+      }
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
-        float p0 = ex2(fmaf(__uint_as_float(sv[c]), p.scale_log2, -lse2[c]));
-        float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), p.scale_log2, -lse2[c + 1]));
+        // One pair in four is computed on the FMA pipe, the rest on the MUFU unit.
+        const float x0 = fmaf(__uint_as_float(sv[c]), p.scale_log2, -lv[c]);
+        const float x1 = fmaf(__uint_as_float(sv[c + 1]), p.scale_log2, -lv[c + 1]);
+        float p0 = ((c / 2) % 4 == 3) ? exp2_poly(x0) : ex2(x0);
+        float p1 = ((c / 2) % 4 == 3) ? exp2_poly(x1) : ex2(x1);
         if (need_mask) {
           if (c < lim) p0 = 0.f;
           if (c + 1 < lim) p1 = 0.f;
@@ -480,11 +497,17 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       tc_fence_before();
       mbar_arrive(&bars.dp_consumed[b]);   // region Y may now take the next step's Sᵀ
       uint32_t ds[32];
+      float dv4[64];
+#pragma unroll
+      for (int c = 0; c < 64; c += 4) {
+        const float4 t4 = *reinterpret_cast<const float4*>(delta + c);
+        dv4[c] = t4.x; dv4[c + 1] = t4.y; dv4[c + 2] = t4.z; dv4[c + 3] = t4.w;
+      }
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
         const float2 pp = unpack2(pk[c / 2], DT);
-        const float d0 = pp.x * (__uint_as_float(sv[c]) - delta[c]);
-        const float d1 = pp.y * (__uint_as_float(sv[c + 1]) - delta[c + 1]);
+        const float d0 = pp.x * (__uint_as_float(sv[c]) - dv4[c]);
+        const float d1 = pp.y * (__uint_as_float(sv[c + 1]) - dv4[c + 1]);
         ds[c / 2] = pack2(d0, d1, DT);
       }
       // dS in shared memory, one 128-byte swizzled row per key row r, chunk h holding query
@@ -563,18 +586,19 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         tma_store_wait_read_all();
       }
     }
-  } else if (warp >= 12) {
+  } else {
+    regs_inc<144>();
     // ===================== dQ drain: TMEM -> shared memory -> TMA reduce-add ===========
-    // dQ of a step sits in TMEM (query row r = lane r, d columns).  It leaves in halves of
-    // d/2 columns: each half is written to a staging buffer as 32-column fp32 chunks of
-    // 128 rows x 128 bytes, 128-byte swizzled, then added into the fp32 accumulator by the
-    // TMA unit.  TMEM is released as soon as the last half has been read into registers.
+    // dQ of a step sits in TMEM (query row r = lane r, d columns).  All of it is read into
+    // registers first, so the region goes back to the next step's dPᵀ MMA at once; it then
+    // leaves as 32-column fp32 chunks (128 rows x 128 bytes, 128-byte swizzled) through two
+    // staging buffers, so that two TMA reduce-adds into the fp32 accumulator are in flight.
     const int quad = warp % 4;
     const int r = quad * 32 + lane;                       // query row within the block
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
-    constexpr int HALF = D / 2;                           // columns per round
-    constexpr int CHUNKS = HALF / 32;                     // 16 KB chunks per round
+    constexpr int NCH = D / 32;                           // 32-column chunks per step
     bool ok = true;
+    int use[2] = {0, 0};                                  // times each buffer has been filled
     for (int n = 0; n < n_iter && ok; ++n) {
       const int b = n & 1;
       if (!mbar_wait_warp(&bars.dq_full[b], (n >> 1) & 1, abort_flag)) { ok = false; break; }
@@ -582,53 +606,45 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       const int hq = iter_head(n);
       const int row0 = (bi * p.h_q + hq) * p.s_q_pad + iter_qblk(n) * kBlockM;
       const uint32_t X = tmem + lane_off + C::R_COL + b * 128;
-      // Both halves leave TMEM before any wait on the TMA unit, so the region is handed back
-      // to the next step's dPᵀ MMA as early as possible; the second half waits in registers.
-      auto stage = [&](const uint32_t(&vals)[HALF]) {
+      uint32_t v[D];
 #pragma unroll
-        for (int c = 0; c < CHUNKS; ++c) {
-          uint8_t* rowp = sDQ + c * 16384 + r * 128;
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) =
-                make_uint4(vals[c * 32 + u * 4], vals[c * 32 + u * 4 + 1],
-                           vals[c * 32 + u * 4 + 2], vals[c * 32 + u * 4 + 3]);
-        }
-        fence_proxy_async_smem();
-      };
-      uint32_t v[HALF];
-#pragma unroll
-      for (int c = 0; c < CHUNKS; ++c)
+      for (int c = 0; c < NCH; ++c)
         tmem_ld32(X + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
-      tmem_ld_wait();
-      // The staging buffer is free once the previous half's reduce-add has read it.
-      if (n >= 1 && !mbar_wait_warp(&bars.stage_free, 1, abort_flag)) { ok = false; break; }
-      stage(v);
-#pragma unroll
-      for (int c = 0; c < CHUNKS; ++c)
-        tmem_ld32(X + HALF + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&v[c * 32]));
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(&bars.dq_free[b]);
-      for (int round = 0; round < 2 && ok; ++round) {
-        if (round == 1) {
-          if (!mbar_wait_warp(&bars.stage_free, 0, abort_flag)) { ok = false; break; }
-          stage(v);
+#pragma unroll
+      for (int c = 0; c < NCH; ++c) {
+        const int buf = c & 1;
+        // Buffer `buf` is free once the reduce-add of its previous fill has read it.
+        if (use[buf] > 0 && !mbar_wait_warp(&bars.stage_free[buf], (use[buf] - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
         }
-        mbar_arrive(&bars.stage_full);
+        uint8_t* rowp = sDQ + buf * 16384 + r * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) =
+              make_uint4(v[c * 32 + u * 4], v[c * 32 + u * 4 + 1], v[c * 32 + u * 4 + 2],
+                         v[c * 32 + u * 4 + 3]);
+        fence_proxy_async_smem();
+        mbar_arrive(&bars.stage_full[buf]);
         if (r == 0) {
-          if (!mbar_wait(&bars.stage_full, round, abort_flag)) ok = false;
+          if (!mbar_wait(&bars.stage_full[buf], use[buf] & 1, abort_flag)) ok = false;
           if (ok) {
-            for (int c = 0; c < CHUNKS; ++c)
-              tma_reduce_add_2d(&p.tm_dqacc, sDQ + c * 16384, round * HALF + c * 32, row0);
+            tma_reduce_add_2d(&p.tm_dqacc, sDQ + buf * 16384, c * 32, row0);
             tma_store_commit();
-            tma_store_wait_read_all();
+            bulk_wait_read<1>();                          // the other buffer's reduce has read
           }
-          mbar_arrive(&bars.stage_free);
+          if (use[buf ^ 1] > 0 || c > 0) mbar_arrive(&bars.stage_free[buf ^ 1]);
         }
+        ++use[buf];
       }
     }
-    if (r == 0) tma_store_wait_all();
+    if (r == 0) {
+      bulk_wait_read<0>();
+      tma_store_wait_all();
+    }
   }
 
   tc_fence_before();
