@@ -11,7 +11,7 @@
 // with dK, dV summed over the query heads of each KV group.
 //
 // Three launches (the pages note an engine may be "a small set of cooperating kernels"):
-//   1. bwd_pre:   Delta_i, LSE_i·log2(e) and a zeroed fp32 dQ accumulator (workspace).
+//   1. bwd_pre:   -Delta_i, -LSE_i·log2(e) and a zeroed fp32 dQ accumulator (workspace).
 //   2. bwd_main:  one CTA per (batch, KV head, 128-row KV block); K and V stay in shared
 //                 memory while the CTA walks every (query head of the group, 128-row query
 //                 block) it can see.  Per step five tcgen05 MMAs (Sᵀ = K·Qᵀ, dPᵀ = V·dOᵀ,
@@ -102,8 +102,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
     reinterpret_cast<float4*>(dq)[0] = make_float4(0.f, 0.f, 0.f, 0.f);
     reinterpret_cast<float4*>(dq)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (part == 0) {
-      p.delta[vrow] = valid ? acc : 0.f;
-      p.lse2[vrow] = valid ? p.lse[static_cast<int64_t>(bh) * p.s_q + row] * kLog2e : INFINITY;
+      // Stored negated, so the main kernel adds them with paired fp32 instructions.
+      p.delta[vrow] = valid ? -acc : 0.f;
+      p.lse2[vrow] = valid ? -p.lse[static_cast<int64_t>(bh) * p.s_q + row] * kLog2e : -INFINITY;
     }
   }
 }
@@ -177,6 +178,9 @@ __global__ void __launch_bounds__(256) bwd_kv_convert_kernel(const BwdParams p) 
 // ---------------------------------------------------------------------------
 // 2. main kernel
 // ---------------------------------------------------------------------------
+
+// Share of P's exponentials computed on the FMA pipe (one pair in kPolyEvery; 0 = none).
+constexpr int kPolyEvery = 4;
 
 template <int D>
 struct BwdCfg {
@@ -449,8 +453,8 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       const uint32_t X = tmem + lane_off + C::R_COL + b * 128;
       const uint32_t Y = tmem + lane_off + C::R_COL + (b ^ 1) * 128;
       const int q0 = iter_qblk(n) * kBlockM + 64 * h;     // first query column of this half
-      const float* lse2 = sVec + (b * 2 + 0) * 128 + 64 * h;
-      const float* delta = sVec + (b * 2 + 1) * 128 + 64 * h;
+      const float* nlse2 = sVec + (b * 2 + 0) * 128 + 64 * h;    // -LSE·log2 e per column
+      const float* ndelta = sVec + (b * 2 + 1) * 128 + 64 * h;   // -Delta per column
       // Pᵀ = exp2(Sᵀ·scale·log2e − LSE·log2e), masked where key > query
       if (!mbar_wait_warp(&bars.ring_full[it % C::NSLOT], (it / C::NSLOT) & 1, abort_flag)) { ok = false; break; }
       if (!mbar_wait_warp(&bars.s_full[b], par, abort_flag)) { ok = false; break; }
@@ -462,19 +466,15 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       const bool need_mask = p.causal && (q0 < j * kBlockN + kBlockN - 1);
       const int lim = kv_row - q0;                        // column c visible iff c >= lim
       uint32_t pk[32];
-      float lv[64];
-#pragma unroll
-      for (int c = 0; c < 64; c += 4) {
-        const float4 t4 = *reinterpret_cast<const float4*>(lse2 + c);
-        lv[c] = t4.x; lv[c + 1] = t4.y; lv[c + 2] = t4.z; lv[c + 3] = t4.w;
-      }
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
-        // One pair in four is computed on the FMA pipe, the rest on the MUFU unit.
-        const float x0 = fmaf(__uint_as_float(sv[c]), p.scale_log2, -lv[c]);
-        const float x1 = fmaf(__uint_as_float(sv[c + 1]), p.scale_log2, -lv[c + 1]);
-        float p0 = ((c / 2) % 4 == 3) ? exp2_poly(x0) : ex2(x0);
-        float p1 = ((c / 2) % 4 == 3) ? exp2_poly(x1) : ex2(x1);
+        const float2 nl = *reinterpret_cast<const float2*>(nlse2 + c);
+        const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl);
+        // A fixed share of the pairs is computed on the FMA pipe, the rest on the MUFU unit.
+        const bool poly = kPolyEvery > 0 && (c / 2) % (kPolyEvery > 0 ? kPolyEvery : 1) == kPolyEvery - 1;
+        float p0 = poly ? exp2_poly(x.x) : ex2(x.x);
+        float p1 = poly ? exp2_poly(x.y) : ex2(x.y);
         if (need_mask) {
           if (c < lim) p0 = 0.f;
           if (c + 1 < lim) p1 = 0.f;
@@ -497,18 +497,12 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       tc_fence_before();
       mbar_arrive(&bars.dp_consumed[b]);   // region Y may now take the next step's Sᵀ
       uint32_t ds[32];
-      float dv4[64];
-#pragma unroll
-      for (int c = 0; c < 64; c += 4) {
-        const float4 t4 = *reinterpret_cast<const float4*>(delta + c);
-        dv4[c] = t4.x; dv4[c + 1] = t4.y; dv4[c + 2] = t4.z; dv4[c + 3] = t4.w;
-      }
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
-        const float2 pp = unpack2(pk[c / 2], DT);
-        const float d0 = pp.x * (__uint_as_float(sv[c]) - dv4[c]);
-        const float d1 = pp.y * (__uint_as_float(sv[c + 1]) - dv4[c + 1]);
-        ds[c / 2] = pack2(d0, d1, DT);
+        const float2 nd = *reinterpret_cast<const float2*>(ndelta + c);
+        const float2 dd = mul2(unpack2(pk[c / 2], DT),
+                               add2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), nd));
+        ds[c / 2] = pack2(dd.x, dd.y, DT);
       }
       // dS in shared memory, one 128-byte swizzled row per key row r, chunk h holding query
       // columns 64h..64h+63: read K-major (rows = keys) as the A operand of dK += dSᵀ·Q and

@@ -157,6 +157,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort;
 
+  // With two Q tiles (384 threads, 168 registers each at launch) the producer / MMA
+  // warpgroup gives registers to the two softmax warpgroups: 80 + 2 x 208 <= 3 x 168.
+  if (warp < 4) {
+  if constexpr (NQT == 2) regs_dec<80>();
   if (warp == 0) {
     // ================================ TMA producer ====================================
     if (elect_one_sync()) {
@@ -303,7 +307,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       tc_commit(&bars.drain);
       mbar_wait_drain(&bars.drain, 0);
     }
-  } else if (warp >= 4) {
+  }
+  } else {
+    if constexpr (NQT == 2) regs_inc<208>();
     // ============================ softmax / epilogue ==================================
     const int t = (NQT == 2) ? (warp - 4) / 4 : 0;         // Q tile of this warpgroup
     const int quad = warp % 4;                               // TMEM lane quadrant
@@ -347,9 +353,16 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         for (int c = 0; c < kBlockN; ++c)
           if (c > lim) sv[c] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
+      // Row max over four independent chains of three-input max.
+      float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kBlockN; ++c) mx = fmaxf(mx, __uint_as_float(sv[c]));
+      for (int c = 0; c < kBlockN; c += 8) {
+        mx0 = max3(mx0, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+        mx1 = max3(mx1, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
+        mx2 = max3(mx2, __uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5]));
+        mx3 = max3(mx3, __uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7]));
+      }
+      const float mx = max3(mx0, mx1, fmaxf(mx2, mx3));
       const float m_cand = mx * c_scale;
       float alpha = 1.f;
       if (m_cand > m_ref + C::THRESH) {
@@ -358,27 +371,27 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       }
       const float neg_m = C::P_OFFSET - m_ref;
 
-      float rowsum = 0.f;
+      // x = s * scale - m in pairs; P = 2^x; row sums in pairs.
+      const float2 cs2 = make_float2(c_scale, c_scale);
+      const float2 nm2 = make_float2(neg_m, neg_m);
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
       uint32_t pk[C::P_COLS];
-      if (FP8) {
 #pragma unroll
-        for (int c = 0; c < kBlockN; c += 4) {
-          const float p0 = ex2(fmaf(__uint_as_float(sv[c]), c_scale, neg_m));
-          const float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), c_scale, neg_m));
-          const float p2 = ex2(fmaf(__uint_as_float(sv[c + 2]), c_scale, neg_m));
-          const float p3 = ex2(fmaf(__uint_as_float(sv[c + 3]), c_scale, neg_m));
-          rowsum += (p0 + p1) + (p2 + p3);
-          pk[c / 4] = pack4_e4m3(p0, p1, p2, p3);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kBlockN; c += 2) {
-          const float p0 = ex2(fmaf(__uint_as_float(sv[c]), c_scale, neg_m));
-          const float p1 = ex2(fmaf(__uint_as_float(sv[c + 1]), c_scale, neg_m));
-          rowsum += p0 + p1;
-          pk[c / 2] = pack2(p0, p1, DT);
+      for (int c = 0; c < kBlockN; c += 4) {
+        const float2 x01 = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), cs2, nm2);
+        const float2 x23 = fma2(make_float2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), cs2, nm2);
+        const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
+        const float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
+        acc0 = add2(acc0, p01);
+        acc1 = add2(acc1, p23);
+        if (FP8) {
+          pk[c / 4] = pack4_e4m3(p01.x, p01.y, p23.x, p23.y);
+        } else {
+          pk[c / 2] = pack2(p01.x, p01.y, DT);
+          pk[c / 2 + 1] = pack2(p23.x, p23.y, DT);
         }
       }
+      const float rowsum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
 #pragma unroll
       for (int c = 0; c < C::P_COLS / 32; ++c)
         tmem_st32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[c * 32]));

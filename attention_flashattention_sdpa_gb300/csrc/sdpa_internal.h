@@ -44,8 +44,8 @@ struct BwdParams {
   const float* lse;    // [b][h_q][s_q]
   void* dq;            // output
   float* dq_acc;       // workspace [b][h_q][s_q_pad][d] fp32
-  float* delta;        // workspace [b][h_q][s_q_pad] fp32 (Delta_i)
-  float* lse2;         // workspace [b][h_q][s_q_pad] fp32 (LSE_i * log2 e)
+  float* delta;        // workspace [b][h_q][s_q_pad] fp32 (-Delta_i)
+  float* lse2;         // workspace [b][h_q][s_q_pad] fp32 (-LSE_i * log2 e)
   int64_t o_sb, o_sh, o_ss;     // element strides of O
   int64_t do_sb, do_sh, do_ss;  // element strides of dO
   int64_t dq_sb, dq_sh, dq_ss;  // element strides of dQ
