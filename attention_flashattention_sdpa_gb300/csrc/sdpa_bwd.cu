@@ -220,6 +220,7 @@ struct alignas(8) BwdBarriers {
   uint64_t drain;
   uint64_t epi_ready[2];
   uint64_t dp_consumed[2];  // the compute warps have read dPᵀ out of TMEM
+  uint64_t dsbuf_free[2];   // the dQ and dK MMAs of a step have read the dS buffer
   uint64_t stage_full[2];   // dQ staging buffer written by the 128 drain threads
   uint64_t stage_free[2];   // the reduce-add of that buffer has read shared memory
   uint32_t tmem_base;
@@ -288,6 +289,8 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     mbar_init(&bars.epi_ready[1], 128);
     mbar_init(&bars.dp_consumed[0], 256);
     mbar_init(&bars.dp_consumed[1], 256);
+    mbar_init(&bars.dsbuf_free[0], 1);
+    mbar_init(&bars.dsbuf_free[1], 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars.stage_full[i], 128);
       mbar_init(&bars.stage_free[i], 1);
@@ -413,9 +416,16 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
           if (!mbar_wait(&bars.dp_consumed[b], par, abort_flag)) { ok = false; break; }
           if (!issue_s(b ^ 1, qslot_next)) { ok = false; break; }
         }
-        // ---- dK += dSᵀ·Q (dS read K-major from shared memory) ; dQ = dS·K ----
+        // ---- dQ = dS·K first (its drain gates the next dPᵀ), then dK += dSᵀ·Q (dS read
+        //      K-major from shared memory) ----
         if (!mbar_wait(&bars.ds_full[b], par, abort_flag)) { ok = false; break; }
         tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          mma_ss(X, make_sdesc_sw128(dsA + k * 2048, 16384, 1024),
+                 make_sdesc_sw128(kA + k * 2048, 16384, 1024), idesc_dq, k > 0, false);
+        }
+        tc_commit(&bars.dq_full[b]);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = (k / 4) * 16384 + (k % 4) * 32;
@@ -423,12 +433,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
                  make_sdesc_sw128(qB + k * 2048, 16384, 1024), idesc_acc,
                  (n > 0 || k > 0) ? 1u : 0u, false);
         }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          mma_ss(X, make_sdesc_sw128(dsA + k * 2048, 16384, 1024),
-                 make_sdesc_sw128(kA + k * 2048, 16384, 1024), idesc_dq, k > 0, false);
-        }
-        tc_commit(&bars.dq_full[b]);
+        tc_commit(&bars.dsbuf_free[b]);
         tc_commit(&bars.ring_empty[qslot]);
         qslot = qslot_next;
       }
@@ -506,9 +511,9 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       }
       // dS in shared memory, one 128-byte swizzled row per key row r, chunk h holding query
       // columns 64h..64h+63: read K-major (rows = keys) as the A operand of dK += dSᵀ·Q and
-      // MN-major (rows = queries) as the A operand of dQ = dS·K.  The previous step's dK and
-      // dQ MMAs must have finished reading it.
-      if (n >= 1 && !mbar_wait_warp(&bars.dq_full[b ^ 1], ((n - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+      // MN-major (rows = queries) as the A operand of dQ = dS·K.  The previous step's dQ and
+      // dK MMAs must have finished reading it.
+      if (n >= 1 && !mbar_wait_warp(&bars.dsbuf_free[b ^ 1], ((n - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
       uint8_t* rowp = sDS + h * 16384 + r * 128;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
