@@ -256,8 +256,6 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
                        void* dv, void* workspace, size_t workspace_bytes, void* stream_) {
   sdpa_status_t st = check_problem(p, true);
   if (st != SDPA_OK) return st;
-  if (p->d == 256)
-    return fail(SDPA_ERR_UNSUPPORTED, "the backward pass supports d = 64 or 128");
   const int es = 2;
   if ((st = check_view("q", q, p->q, p->b, p->h_q, p->s_q, p->d, es)) != SDPA_OK) return st;
   if ((st = check_view("k", k, p->k, p->b, p->h_kv, p->s_kv, p->d, es)) != SDPA_OK) return st;
@@ -278,10 +276,12 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
 
   sdpa::BwdParams prm;
   memset(&prm, 0, sizeof(prm));
-  if ((st = make_map(&prm.tm_q, "q", q, p->q, p->b, p->h_q, p->s_q, p->d, p->in_dtype, 128)) != SDPA_OK) return st;
+  // d = 256 walks 64-row query blocks (its kernel keeps only half of d of dK/dV in TMEM).
+  const int q_rows = p->d == 256 ? 64 : 128;
+  if ((st = make_map(&prm.tm_q, "q", q, p->q, p->b, p->h_q, p->s_q, p->d, p->in_dtype, q_rows)) != SDPA_OK) return st;
   if ((st = make_map(&prm.tm_k, "k", k, p->k, p->b, p->h_kv, p->s_kv, p->d, p->in_dtype, 128)) != SDPA_OK) return st;
   if ((st = make_map(&prm.tm_v, "v", v, p->v, p->b, p->h_kv, p->s_kv, p->d, p->in_dtype, 128)) != SDPA_OK) return st;
-  if ((st = make_map(&prm.tm_do, "dout", dout, p->dout, p->b, p->h_q, p->s_q, p->d, p->in_dtype, 128)) != SDPA_OK) return st;
+  if ((st = make_map(&prm.tm_do, "dout", dout, p->dout, p->b, p->h_q, p->s_q, p->d, p->in_dtype, q_rows)) != SDPA_OK) return st;
   if ((st = make_map(&prm.tm_dk, "dk", dk, p->dk, p->b, p->h_kv, p->s_kv, p->d, p->out_dtype, 128)) != SDPA_OK) return st;
   if ((st = make_map(&prm.tm_dv, "dv", dv, p->dv, p->b, p->h_kv, p->s_kv, p->d, p->out_dtype, 128)) != SDPA_OK) return st;
   const int s_q_pad = (p->s_q + 127) / 128 * 128;
@@ -291,8 +291,11 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
     // 32-column (128-byte) chunks of 128 rows.
     auto fn = encode_fn();
     if (fn == nullptr) return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-    cuuint64_t dims[2] = {(cuuint64_t)p->d, (cuuint64_t)p->b * p->h_q * s_q_pad};
-    cuuint64_t strides[1] = {(cuuint64_t)p->d * 4};
+    // d = 256 keeps the accumulator transposed, [b*h_q*d][s_q_pad] (its kernel produces dQᵀ).
+    const bool tr = p->d == 256;
+    cuuint64_t dims[2] = {tr ? (cuuint64_t)s_q_pad : (cuuint64_t)p->d,
+                          tr ? (cuuint64_t)p->b * p->h_q * p->d : (cuuint64_t)p->b * p->h_q * s_q_pad};
+    cuuint64_t strides[1] = {tr ? (cuuint64_t)s_q_pad * 4 : (cuuint64_t)p->d * 4};
     cuuint32_t box[2] = {32, 128};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = fn(&prm.tm_dqacc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, workspace, dims, strides,

@@ -654,6 +654,348 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   }
 }
 
+// ---------------------------------------------------------------------------
+// d = 256
+// ---------------------------------------------------------------------------
+// dK and dV of a 128-row KV block at d = 256 would fill all 512 TMEM columns, and K and V
+// alone take 128 KB of shared memory.  So a CTA owns one half of d of dK and dV, walks
+// 64-row query blocks, and computes its half of dQ transposed (dQᵀ = Kᵀ·dSᵀ: rows = its 128
+// d indices, so M stays 128) into a transposed fp32 accumulator [b·h_q][d][s_q_pad].  Both
+// halves compute the full-d reductions Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ.  One thread issues the
+// copies and MMAs and the phases of a step run one after another.
+struct D256 {
+  static constexpr int BQ = 64;                  // query rows per step
+  static constexpr int OFF_K = 0;                // 128 x 256: four 16 KB chunks of 64 columns
+  static constexpr int OFF_V = 65536;
+  static constexpr int OFF_Q = 131072;           // 64 x 256: four 8 KB chunks
+  static constexpr int OFF_DO = 163840;
+  static constexpr int OFF_DS = 196608;          // dS: 128 key rows x 64 queries, 16 KB
+  static constexpr int OFF_ST = 212992;          // dQᵀ staging: 128 rows x 32 fp32, 16 KB
+  static constexpr int OFF_VEC = 229376;         // -LSE·log2e and -Delta of the step, 64 each
+  static constexpr int OFF_BAR = OFF_VEC + 512;
+  static constexpr int SMEM_BYTES = OFF_BAR + 256;
+  static constexpr int COL_S = 0, COL_DP = 64, COL_DQ = 128, COL_DV = 256, COL_DK = 384;
+};
+static_assert(D256::SMEM_BYTES <= 232448, "shared memory budget");
+
+struct alignas(8) D256Barriers {
+  uint64_t kv_full, ld_full, mma_done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+template <int DT>
+__global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant__ BwdParams p) {
+  using C = D256;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  if (smem_u32(smem) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(&g_device_error, kErrSmemAlign);
+    return;
+  }
+  D256Barriers& bars = *reinterpret_cast<D256Barriers*>(smem + C::OFF_BAR);
+  uint8_t* sK = smem + C::OFF_K;
+  uint8_t* sV = smem + C::OFF_V;
+  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sdO = smem + C::OFF_DO;
+  uint8_t* sDS = smem + C::OFF_DS;
+  uint8_t* sST = smem + C::OFF_ST;
+  float* sVec = reinterpret_cast<float*>(smem + C::OFF_VEC);
+  const int warp = threadIdx.x / 32;
+  const int r = threadIdx.x;                     // TMEM lane: key row, or d row of dQᵀ
+  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+
+  // Launch order: the two d-halves of a unit side by side, units fastest, KV blocks slowest
+  // (for causal, the first KV blocks carry the most query blocks and go first).
+  const int dh = blockIdx.x & 1;
+  const int rest = blockIdx.x >> 1;
+  const int units = p.b * p.h_kv * p.kv_split;
+  const int unit = rest % units;
+  const int j = rest / units;
+  const int split = unit % p.kv_split;
+  const int bhk = unit / p.kv_split;
+  const int bi = bhk / p.h_kv;
+  const int hk = bhk % p.h_kv;
+  const int n_qb = (p.s_q + C::BQ - 1) / C::BQ;
+  const int q_first = p.causal ? (j * kBlockN) / C::BQ : 0;
+  const int per_head = q_first < n_qb ? n_qb - q_first : 0;
+  const int head0 = hk * p.group + split * p.heads_per_split;
+  const int n_heads = max(0, min(p.heads_per_split, (hk + 1) * p.group - head0));
+  const int n_iter = per_head * n_heads;
+  const int kv_row = j * kBlockN + r;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&bars.kv_full, 1);
+    mbar_init(&bars.ld_full, 1);
+    mbar_init(&bars.mma_done, 1);
+    bars.abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&bars.tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars.tmem_base;
+  volatile int* abort_flag = &bars.abort;
+  const uint32_t fmt = (DT == kBF16) ? 1u : 0u;
+
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bars.kv_full, 2 * 65536);
+    for (int c = 0; c < 4; ++c) {
+      tma_load_4d(sK + c * 16384, &p.tm_k, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
+      tma_load_4d(sV + c * 16384, &p.tm_v, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
+    }
+  }
+  bool ok = __syncthreads_and(mbar_wait(&bars.kv_full, 0, abort_flag));
+  uint32_t ph_ld = 0, ph_mma = 0;
+  for (int n = 0; n < n_iter && ok; ++n) {
+    const int hq = head0 + n / per_head;
+    const int q0 = (q_first + n % per_head) * C::BQ;
+    const int64_t vrow = (static_cast<int64_t>(bi) * p.h_q + hq) * p.s_q_pad + q0;
+    if (threadIdx.x == 0) {
+      mbar_arrive_expect_tx(&bars.ld_full, 2 * 32768 + 512);
+      for (int c = 0; c < 4; ++c) {
+        tma_load_4d(sQ + c * 8192, &p.tm_q, &bars.ld_full, c * 64, q0, hq, bi);
+        tma_load_4d(sdO + c * 8192, &p.tm_do, &bars.ld_full, c * 64, q0, hq, bi);
+      }
+      bulk_load(sVec, p.lse2 + vrow, 256, &bars.ld_full);
+      bulk_load(sVec + 64, p.delta + vrow, 256, &bars.ld_full);
+    }
+    ok = __syncthreads_and(mbar_wait(&bars.ld_full, ph_ld, abort_flag));
+    ph_ld ^= 1;
+    if (!ok) break;
+    // ---- Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ over all of d ----
+    if (threadIdx.x == 0) {
+      tc_fence_after();
+      const uint32_t idesc_s = make_idesc(fmt, 128, C::BQ, false, false);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const uint32_t oa = (k / 4) * 16384 + (k % 4) * 32, ob = (k / 4) * 8192 + (k % 4) * 32;
+        mma_ss(tmem + C::COL_S, make_sdesc_sw128(smem_u32(sK) + oa, 16, 1024),
+               make_sdesc_sw128(smem_u32(sQ) + ob, 16, 1024), idesc_s, k > 0, false);
+        mma_ss(tmem + C::COL_DP, make_sdesc_sw128(smem_u32(sV) + oa, 16, 1024),
+               make_sdesc_sw128(smem_u32(sdO) + ob, 16, 1024), idesc_s, k > 0, false);
+      }
+      tc_commit(&bars.mma_done);
+    }
+    ok = __syncthreads_and(mbar_wait(&bars.mma_done, ph_mma, abort_flag));
+    ph_mma ^= 1;
+    if (!ok) break;
+    tc_fence_after();
+    // ---- Pᵀ (to TMEM, over Sᵀ) and dS (to shared memory) for key row r ----
+    {
+      uint32_t sv[64], dpv[64];
+      tmem_ld32(tmem + lane_base + C::COL_S, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld32(tmem + lane_base + C::COL_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_ld32(tmem + lane_base + C::COL_DP, *reinterpret_cast<uint32_t(*)[32]>(&dpv[0]));
+      tmem_ld32(tmem + lane_base + C::COL_DP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dpv[32]));
+      tmem_ld_wait();
+      const bool need_mask = p.causal && (q0 < j * kBlockN + kBlockN - 1);
+      const int lim = kv_row - q0;                  // query column c visible iff c >= lim
+      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+      uint32_t pk[32], ds[32];
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2,
+                              *reinterpret_cast<const float2*>(sVec + c));
+        float p0 = ex2(x.x), p1 = ex2(x.y);
+        if (need_mask) {
+          if (c < lim) p0 = 0.f;
+          if (c + 1 < lim) p1 = 0.f;
+        }
+        pk[c / 2] = pack2(p0, p1, DT);
+        const float2 dd = mul2(make_float2(p0, p1),
+                               add2(make_float2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])),
+                                    *reinterpret_cast<const float2*>(sVec + 64 + c)));
+        ds[c / 2] = pack2(dd.x, dd.y, DT);
+      }
+      tmem_st32(tmem + lane_base + C::COL_S, pk);
+      uint8_t* rowp = sDS + r * 128;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) =
+            make_uint4(ds[u * 4], ds[u * 4 + 1], ds[u * 4 + 2], ds[u * 4 + 3]);
+      tmem_st_wait();
+      fence_proxy_async_smem();
+      tc_fence_before();
+    }
+    __syncthreads();
+    // ---- dV_h += Pᵀ·dO_h, dK_h += dSᵀ·Q_h, dQᵀ_h = K_hᵀ·dSᵀ ----
+    if (threadIdx.x == 0) {
+      tc_fence_after();
+      const uint32_t idesc_acc = make_idesc(fmt, 128, 128, false, true);
+      const uint32_t idesc_dq = make_idesc(fmt, 128, C::BQ, true, true);
+      const uint32_t qh = smem_u32(sQ) + dh * 2 * 8192, gh = smem_u32(sdO) + dh * 2 * 8192;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ts(tmem + C::COL_DV, tmem + C::COL_S + k * 8, make_sdesc_sw128(gh + k * 2048, 8192, 1024),
+               idesc_acc, (n > 0 || k > 0) ? 1u : 0u, false);
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ss(tmem + C::COL_DK, make_sdesc_sw128(smem_u32(sDS) + k * 32, 16, 1024),
+               make_sdesc_sw128(qh + k * 2048, 8192, 1024), idesc_acc, (n > 0 || k > 0) ? 1u : 0u,
+               false);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        mma_ss(tmem + C::COL_DQ, make_sdesc_sw128(smem_u32(sK) + dh * 2 * 16384 + k * 2048, 16384, 1024),
+               make_sdesc_sw128(smem_u32(sDS) + k * 2048, 8192, 1024), idesc_dq, k > 0, false);
+      tc_commit(&bars.mma_done);
+    }
+    ok = __syncthreads_and(mbar_wait(&bars.mma_done, ph_mma, abort_flag));
+    ph_mma ^= 1;
+    if (!ok) break;
+    tc_fence_after();
+    // ---- dQᵀ: row r of this half of d, 64 query columns in two 32-column chunks ----
+    {
+      uint32_t v[64];
+      tmem_ld32(tmem + lane_base + C::COL_DQ, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(tmem + lane_base + C::COL_DQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_ld_wait();
+      tc_fence_before();
+      const int drow = (bi * p.h_q + hq) * 256 + dh * 128;
+      for (int ch = 0; ch < 2; ++ch) {
+        uint8_t* rowp = sST + r * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) =
+              make_uint4(v[ch * 32 + u * 4], v[ch * 32 + u * 4 + 1], v[ch * 32 + u * 4 + 2],
+                         v[ch * 32 + u * 4 + 3]);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+          tma_reduce_add_2d(&p.tm_dqacc, sST, q0 + ch * 32, drow);
+          tma_store_commit();
+          bulk_wait_read<0>();
+        }
+        __syncthreads();
+      }
+    }
+  }
+
+  // ---- epilogue: this half of dV and dK ----
+  tc_fence_after();
+  if (ok) {
+    const uint32_t acc_v = tmem + lane_base + C::COL_DV, acc_k = tmem + lane_base + C::COL_DK;
+    if (p.kv_split > 1) {
+      if (n_iter > 0) {
+        float* dvp = p.dv_acc + ((static_cast<int64_t>(bi) * p.h_kv + hk) * p.s_kv_pad + kv_row) * 256 + dh * 128;
+        float* dkp = p.dk_acc + ((static_cast<int64_t>(bi) * p.h_kv + hk) * p.s_kv_pad + kv_row) * 256 + dh * 128;
+        for (int c = 0; c < 4; ++c) {
+          uint32_t a[32], k2[32];
+          tmem_ld32(acc_v + c * 32, a);
+          tmem_ld32(acc_k + c * 32, k2);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            red_add_v4(dvp + c * 32 + u * 4, __uint_as_float(a[u * 4]), __uint_as_float(a[u * 4 + 1]),
+                       __uint_as_float(a[u * 4 + 2]), __uint_as_float(a[u * 4 + 3]));
+            red_add_v4(dkp + c * 32 + u * 4, __uint_as_float(k2[u * 4]) * p.scale,
+                       __uint_as_float(k2[u * 4 + 1]) * p.scale, __uint_as_float(k2[u * 4 + 2]) * p.scale,
+                       __uint_as_float(k2[u * 4 + 3]) * p.scale);
+          }
+        }
+      }
+    } else {
+      // dV_h -> sQ, dK_h -> sdO as two 64-column chunks (128 rows x 128 bytes) each.
+      for (int which = 0; which < 2; ++which) {
+        uint8_t* stage = which == 0 ? sQ : sdO;
+        const uint32_t acc = which == 0 ? acc_v : acc_k;
+        const float mul = which == 0 ? 1.f : p.scale;
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[64];
+          if (n_iter > 0) {
+            tmem_ld32(acc + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+            tmem_ld32(acc + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+            tmem_ld_wait();
+          } else {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) v[i] = 0u;
+          }
+          uint8_t* rowp = stage + c * 16384 + r * 128;
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            uint4 w;
+            w.x = pack2(__uint_as_float(v[u * 8 + 0]) * mul, __uint_as_float(v[u * 8 + 1]) * mul, DT);
+            w.y = pack2(__uint_as_float(v[u * 8 + 2]) * mul, __uint_as_float(v[u * 8 + 3]) * mul, DT);
+            w.z = pack2(__uint_as_float(v[u * 8 + 4]) * mul, __uint_as_float(v[u * 8 + 5]) * mul, DT);
+            w.w = pack2(__uint_as_float(v[u * 8 + 6]) * mul, __uint_as_float(v[u * 8 + 7]) * mul, DT);
+            *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) = w;
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        for (int c = 0; c < 2; ++c) {
+          tma_store_4d(&p.tm_dv, sQ + c * 16384, (dh * 2 + c) * 64, j * kBlockN, hk, bi);
+          tma_store_4d(&p.tm_dk, sdO + c * 16384, (dh * 2 + c) * 64, j * kBlockN, hk, bi);
+        }
+        tma_store_commit();
+        tma_store_wait_read_all();
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// dQ = scale · (transposed accumulator)ᵀ for d = 256, through 32 x 32 shared-memory tiles.
+template <typename T>
+__global__ void __launch_bounds__(256) bwd_dqT_kernel(const BwdParams p) {
+  __shared__ float tile[32][33];
+  const int bh = blockIdx.z;
+  const int bi = bh / p.h_q, hq = bh % p.h_q;
+  const int i0 = blockIdx.x * 32, c0 = blockIdx.y * 32;
+  const int tx = threadIdx.x % 32, ty = threadIdx.x / 32;
+  for (int k = ty; k < 32; k += 8)
+    tile[k][tx] = p.dq_acc[(static_cast<int64_t>(bh) * 256 + c0 + k) * p.s_q_pad + i0 + tx];
+  __syncthreads();
+  for (int k = ty; k < 32; k += 8) {
+    const int i = i0 + k;
+    if (i >= p.s_q) continue;
+    const float v = tile[tx][k] * p.scale;
+    T* dst = reinterpret_cast<T*>(p.dq) + bi * p.dq_sb + hq * p.dq_sh + i * p.dq_ss + c0 + tx;
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) *dst = __float2bfloat16_rn(v);
+    else *dst = __float2half_rn(v);
+  }
+}
+
+template <int DT>
+cudaError_t launch_d256(const BwdParams& p, cudaStream_t st) {
+  using T = typename std::conditional<DT == kBF16, __nv_bfloat16, __half>::type;
+  constexpr int ROWS = 256 / (256 / 8);
+  const int bh = p.b * p.h_q;
+  dim3 gpre((p.s_q_pad + ROWS - 1) / ROWS, bh);
+  bwd_pre_kernel<T, 256><<<gpre, 256, 0, st>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (p.kv_split > 1) {
+    bwd_zero_kv_kernel<<<1024, 256, 0, st>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  auto kern = bwd_d256_kernel<DT>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, D256::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  const unsigned grid = 2u * p.b * p.h_kv * p.kv_split * ((p.s_kv + kBlockN - 1) / kBlockN);
+  kern<<<grid, 128, D256::SMEM_BYTES, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  dim3 gdq(p.s_q_pad / 32, 256 / 32, bh);
+  bwd_dqT_kernel<T><<<gdq, 256, 0, st>>>(p);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || p.kv_split == 1) return e;
+  dim3 gkv((p.s_kv + ROWS - 1) / ROWS, p.b * p.h_kv);
+  bwd_kv_convert_kernel<T, 256><<<gkv, 256, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
 template <int D, int DT>
 cudaError_t launch_t(const BwdParams& p, cudaStream_t st) {
   using T = typename std::conditional<DT == kBF16, __nv_bfloat16, __half>::type;
@@ -712,9 +1054,11 @@ cudaError_t launch_bwd(const BwdParams& p, int dtype, cudaStream_t st) {
   if (dtype == kBF16) {
     if (p.d == 64) return launch_t<64, kBF16>(p, st);
     if (p.d == 128) return launch_t<128, kBF16>(p, st);
+    if (p.d == 256) return launch_d256<kBF16>(p, st);
   } else if (dtype == kF16) {
     if (p.d == 64) return launch_t<64, kF16>(p, st);
     if (p.d == 128) return launch_t<128, kF16>(p, st);
+    if (p.d == 256) return launch_d256<kF16>(p, st);
   }
   return cudaErrorInvalidValue;
 }

@@ -31,7 +31,7 @@ def test_tiny_config(causal):
 
 
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("s", [256, 333])
 def test_head_dims_dtypes_masks(dtype, d, causal, s):
@@ -85,3 +85,16 @@ def test_grouped_heads_without_split():
 def test_split_groups_small_batch(h_kv):
     """Few KV heads: the query heads of a group are split over several CTAs."""
     _check(Workload("t", 1, 16, h_kv, 700, 700, 64, "f16", causal=False, backward=True), seed=h_kv)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("s_q,s_kv", [(100, 300), (300, 130), (1, 1), (65, 200)])
+def test_d256_unequal_lengths(causal, s_q, s_kv):
+    _check(Workload("t", 1, 2, 2, s_q, s_kv, 256, "bf16", causal=causal, backward=True),
+           seed=s_q + 5 * s_kv)
+
+
+@pytest.mark.parametrize("h_q,h_kv", [(4, 2), (8, 1)])
+def test_d256_grouped_heads_and_bshd(h_q, h_kv):
+    _check(Workload("t", 2, h_q, h_kv, 200, 200, 256, "f16", layout="bshd", causal=True,
+                    backward=True), seed=h_q)
