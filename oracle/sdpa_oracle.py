@@ -23,6 +23,12 @@ module's own table and multiplied by their descale):
   "stats" output that the SDPA node returns for training [cuDNN 9 blog, SDPA
   walkthrough sample; cuDNN-in-Python post: the second return value is for
   training];
+* variable lengths (the padding mask and per-batch sequence lengths of the SDPA node's
+  options in the cuDNN 9 blog's walkthrough): for batch b only query rows i < len_q[b] and
+  keys j < len_kv[b] take part; with bottom-right causal alignment key j is visible to query
+  i iff j <= i + len_kv[b] - len_q[b] (the last query sees every key, as in decoding with a
+  KV cache).  A row with no visible key (a padded row, or an early row of a bottom-right
+  mask with len_kv < len_q) gives O = 0 and LSE = -inf, and passes no gradient;
 * head grouping: query head ``hq`` reads KV head ``hq // (h_q // h_kv)`` (contiguous
   groups; the codelab's §9 "Comparing MHA, GQA and MQA" broadcasts each KV head to
   its group of query heads);
@@ -97,13 +103,21 @@ def to_f64(t, descale: float = 1.0) -> np.ndarray:
 # Forward
 # ---------------------------------------------------------------------------
 
-def visible_mask(s_q: int, s_kv: int, causal: bool) -> np.ndarray:
-    """Boolean [s_q, s_kv]: True where key j is visible to query i."""
-    if not causal:
-        return np.ones((s_q, s_kv), dtype=bool)
+def visible_mask(s_q: int, s_kv: int, causal: bool, len_q: int | None = None,
+                 len_kv: int | None = None, bottom_right: bool = False) -> np.ndarray:
+    """Boolean [s_q, s_kv]: True where key j is visible to query i.
+
+    len_q / len_kv: valid rows of this batch (default: all).  causal: top-left (j <= i) or,
+    with bottom_right, j <= i + len_kv - len_q."""
+    lq = s_q if len_q is None else len_q
+    lkv = s_kv if len_kv is None else len_kv
     i = np.arange(s_q)[:, None]
     j = np.arange(s_kv)[None, :]
-    return j <= i
+    m = (i < lq) & (j < lkv)
+    if causal:
+        off = (lkv - lq) if bottom_right else 0
+        m &= j <= i + off
+    return m
 
 
 def kv_head_of(hq: int, h_q: int, h_kv: int) -> int:
@@ -114,36 +128,49 @@ def kv_head_of(hq: int, h_q: int, h_kv: int) -> int:
 
 
 def head_forward(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, scale: float,
-                 mask: np.ndarray):
+                 mask: np.ndarray, allow_empty: bool = False):
     """One (batch, head) slice: returns (O [s_q,d], LSE [s_q], P [s_q,s_kv]).
 
-    Rows with no visible key are undefined for softmax and are rejected."""
+    A row with no visible key has no softmax: it is rejected, or with allow_empty gives
+    O = 0, LSE = -inf and P = 0."""
     S = scale * (qh @ kh.T)                                   # step 1 + scale
-    if not mask.any(axis=1).all():
+    has = mask.any(axis=1)
+    if not allow_empty and not has.all():
         raise ValueError("a query row has no visible key")
     m = np.where(mask, S, -np.inf).max(axis=1)                # pass 1: row max
-    E = np.where(mask, np.exp(S - m[:, None]), 0.0)
+    m_safe = np.where(has, m, 0.0)
+    E = np.where(mask, np.exp(S - m_safe[:, None]), 0.0)
     l = E.sum(axis=1)                                         # pass 2: row sum
-    P = E / l[:, None]                                        # pass 3: normalise
+    P = E / np.where(has, l, 1.0)[:, None]                    # pass 3: normalise
     O = P @ vh                                                # step 3
-    lse = m + np.log(l)
+    with np.errstate(divide="ignore"):
+        lse = np.where(has, m_safe + np.log(np.where(has, l, 1.0)), -np.inf)
     return O, lse, P
 
 
-def forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: bool):
+def _batch_mask(s_q, s_kv, causal, bi, seq_lens_q, seq_lens_kv, bottom_right):
+    lq = None if seq_lens_q is None else int(seq_lens_q[bi])
+    lkv = None if seq_lens_kv is None else int(seq_lens_kv[bi])
+    return visible_mask(s_q, s_kv, causal, lq, lkv, bottom_right)
+
+
+def forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: bool,
+            seq_lens_q=None, seq_lens_kv=None, bottom_right: bool = False):
     """Full forward on logical BHSD fp64 arrays.
 
-    q: [b, h_q, s_q, d]; k, v: [b, h_kv, s_kv, d].  Returns (O [b,h_q,s_q,d],
-    LSE [b,h_q,s_q])."""
+    q: [b, h_q, s_q, d]; k, v: [b, h_kv, s_kv, d]; optional per-batch valid lengths.
+    Returns (O [b,h_q,s_q,d], LSE [b,h_q,s_q])."""
     b, h_q, s_q, d = q.shape
     h_kv, s_kv = k.shape[1], k.shape[2]
-    mask = visible_mask(s_q, s_kv, causal)
+    varlen = seq_lens_q is not None or seq_lens_kv is not None or bottom_right
     O = np.empty((b, h_q, s_q, v.shape[3]), dtype=np.float64)
     L = np.empty((b, h_q, s_q), dtype=np.float64)
     for bi in range(b):
+        mask = _batch_mask(s_q, s_kv, causal, bi, seq_lens_q, seq_lens_kv, bottom_right)
         for hq in range(h_q):
             hk = kv_head_of(hq, h_q, h_kv)
-            O[bi, hq], L[bi, hq], _ = head_forward(q[bi, hq], k[bi, hk], v[bi, hk], scale, mask)
+            O[bi, hq], L[bi, hq], _ = head_forward(q[bi, hq], k[bi, hk], v[bi, hk], scale, mask,
+                                                   allow_empty=varlen)
     return O, L
 
 
@@ -166,8 +193,8 @@ def forward_rows(q_rows: np.ndarray, rows: Sequence[int], kh: np.ndarray, vh: np
 # Backward
 # ---------------------------------------------------------------------------
 
-def _head_backward(qh, kh, vh, doh, scale, mask):
-    _, _, P = head_forward(qh, kh, vh, scale, mask)
+def _head_backward(qh, kh, vh, doh, scale, mask, allow_empty=False):
+    _, _, P = head_forward(qh, kh, vh, scale, mask, allow_empty)
     dV = P.T @ doh
     dP = doh @ vh.T
     delta = (P * dP).sum(axis=1)
@@ -177,20 +204,24 @@ def _head_backward(qh, kh, vh, doh, scale, mask):
     return dQ, dK, dV
 
 
-def backward(q, k, v, do, scale: float, causal: bool):
+def backward(q, k, v, do, scale: float, causal: bool, seq_lens_q=None, seq_lens_kv=None,
+             bottom_right: bool = False):
     """Full backward on logical BHSD fp64 arrays: returns (dQ, dK, dV).
 
-    dK, dV have K's and V's shapes and hold the sum over each KV head's group."""
+    dK, dV have K's and V's shapes and hold the sum over each KV head's group.  With
+    variable lengths, padded rows of dQ, dK and dV are zero."""
     b, h_q, s_q, _ = q.shape
     h_kv, s_kv = k.shape[1], k.shape[2]
-    mask = visible_mask(s_q, s_kv, causal)
+    varlen = seq_lens_q is not None or seq_lens_kv is not None or bottom_right
     dQ = np.empty_like(q, dtype=np.float64)
     dK = np.zeros(k.shape, dtype=np.float64)
     dV = np.zeros(v.shape, dtype=np.float64)
     for bi in range(b):
+        mask = _batch_mask(s_q, s_kv, causal, bi, seq_lens_q, seq_lens_kv, bottom_right)
         for hq in range(h_q):
             hk = kv_head_of(hq, h_q, h_kv)
-            gq, gk, gv = _head_backward(q[bi, hq], k[bi, hk], v[bi, hk], do[bi, hq], scale, mask)
+            gq, gk, gv = _head_backward(q[bi, hq], k[bi, hk], v[bi, hk], do[bi, hq], scale, mask,
+                                        allow_empty=varlen)
             dQ[bi, hq] = gq
             dK[bi, hk] += gk
             dV[bi, hk] += gv

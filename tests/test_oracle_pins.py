@@ -337,3 +337,91 @@ def test_e4m3_quantisation_round_trip_within_half_ulp():
     ulp = 2.0 ** (e - 3)
     assert (np.abs(ys - xs) <= ulp / 2 + 1e-12).all()
     assert np.abs(oracle.to_f64(q8)).max() <= 448.0
+
+
+# ---------------------------------------------------------------------------
+# variable lengths and bottom-right causal alignment
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal,bottom_right", [(False, False), (True, False), (True, True)])
+def test_varlen_equals_unpadded_problem(causal, bottom_right):
+    """Padding changes nothing: each batch equals the problem cut to its own lengths, and
+    padded rows are zero (O, dQ, dK, dV) with LSE = -inf."""
+    b, h_q, h_kv, s_q, s_kv, d = 3, 4, 2, 9, 11, 3
+    q, k, v, do = _rand(b, h_q, s_q, d), _rand(b, h_kv, s_kv, d), _rand(b, h_kv, s_kv, d), \
+        _rand(b, h_q, s_q, d)
+    lq, lkv = [9, 5, 7], [11, 6, 3]
+    O, L = oracle.forward(q, k, v, 0.6, causal, lq, lkv, bottom_right)
+    dQ, dK, dV = oracle.backward(q, k, v, do, 0.6, causal, lq, lkv, bottom_right)
+    for bi in range(b):
+        a, c = lq[bi], lkv[bi]
+        sl = lambda t, n: t[bi:bi + 1, :, :n]
+        if bottom_right and causal and c < a:
+            # rows with no visible key: exactly the first a - c rows
+            n0 = a - c
+            assert (L[bi, :, :n0] == -np.inf).all() and (O[bi, :, :n0] == 0).all()
+            Ou, Lu = oracle.forward(q[bi:bi + 1, :, n0:a], sl(k, c), sl(v, c), 0.6, True)
+            np.testing.assert_allclose(O[bi:bi + 1, :, n0:a], Ou, atol=1e-13)
+            np.testing.assert_allclose(L[bi:bi + 1, :, n0:a], Lu, atol=1e-13)
+        else:
+            shifted = bottom_right and causal and c > a
+            if shifted:
+                # bottom-right with more keys than queries: row i sees keys j <= i + (c - a)
+                Ou, Lu = oracle.forward(sl(q, a), sl(k, c), sl(v, c), 0.6, True, [a], [c], True)
+            else:
+                Ou, Lu = oracle.forward(sl(q, a), sl(k, c), sl(v, c), 0.6, causal)
+            np.testing.assert_allclose(O[bi:bi + 1, :, :a], Ou, atol=1e-13)
+            np.testing.assert_allclose(L[bi:bi + 1, :, :a], Lu, atol=1e-13)
+        assert (O[bi, :, a:] == 0).all() and (L[bi, :, a:] == -np.inf).all()
+        assert (dQ[bi, :, a:] == 0).all() and (dK[bi, :, c:] == 0).all() and (dV[bi, :, c:] == 0).all()
+        if not (bottom_right and causal):
+            gq, gk, gv = oracle.backward(sl(q, a), sl(k, c), sl(v, c), sl(do, a), 0.6, causal)
+            np.testing.assert_allclose(dQ[bi:bi + 1, :, :a], gq, atol=1e-12)
+            np.testing.assert_allclose(dK[bi:bi + 1, :, :c], gk, atol=1e-12)
+            np.testing.assert_allclose(dV[bi:bi + 1, :, :c], gv, atol=1e-12)
+
+
+def test_bottom_right_closed_forms():
+    """Equal lengths: bottom-right = top-left.  One query row (a decoding step): it sees
+    every key, so it equals the unmasked row.  Brute force on a ragged case."""
+    q, k, v = _rand(1, 2, 6, 4), _rand(1, 2, 6, 4), _rand(1, 2, 6, 4)
+    O1, L1 = oracle.forward(q, k, v, 0.5, True, [6], [6], True)
+    O2, L2 = oracle.forward(q, k, v, 0.5, True)
+    np.testing.assert_allclose(O1, O2, atol=1e-14)
+    q1, k9, v9 = _rand(1, 1, 1, 4), _rand(1, 1, 9, 4), _rand(1, 1, 9, 4)
+    Od, Ld = oracle.forward(q1, k9, v9, 0.5, True, [1], [9], True)
+    Of, Lf = oracle.forward(q1, k9, v9, 0.5, False)
+    np.testing.assert_allclose(Od, Of, atol=1e-14)
+    np.testing.assert_allclose(Ld, Lf, atol=1e-14)
+    # brute force: 4 queries, 7 keys, bottom-right: row i sees keys j <= i + 3
+    q4, k7, v7 = _rand(1, 1, 4, 3), _rand(1, 1, 7, 3), _rand(1, 1, 7, 3)
+    O, L = oracle.forward(q4, k7, v7, 0.9, True, [4], [7], True)
+    for i in range(4):
+        w = [math.exp(0.9 * float(q4[0, 0, i] @ k7[0, 0, jj])) for jj in range(i + 4)]
+        tot = sum(w)
+        np.testing.assert_allclose(O[0, 0, i], sum(w[jj] / tot * v7[0, 0, jj] for jj in range(i + 4)),
+                                   atol=1e-12)
+        np.testing.assert_allclose(L[0, 0, i], math.log(tot), atol=1e-12)
+
+
+def test_varlen_backward_matches_finite_differences():
+    q, k, v, do = _rand(2, 2, 5, 3), _rand(2, 2, 6, 3), _rand(2, 2, 6, 3), _rand(2, 2, 5, 3)
+    lq, lkv = [5, 3], [4, 6]
+    dQ, dK, dV = oracle.backward(q, k, v, do, 0.7, True, lq, lkv, True)
+
+    def loss(q_, k_, v_):
+        O, _ = oracle.forward(q_, k_, v_, 0.7, True, lq, lkv, True)
+        return float((O * do).sum())
+    for which, got in ((0, dQ), (1, dK), (2, dV)):
+        args = [q.copy(), k.copy(), v.copy()]
+        x = args[which]
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + 1e-6
+            lp = loss(*args)
+            x[idx] = old - 1e-6
+            lm = loss(*args)
+            x[idx] = old
+            fd[idx] = (lp - lm) / 2e-6
+        assert np.linalg.norm(got - fd) / np.linalg.norm(fd) < 1e-6
