@@ -17,7 +17,7 @@ from typing import Optional
 
 __all__ = [
     "SdpaError", "Strides", "Problem", "lib", "LIB_PATH", "dtype_code", "make_problem",
-    "sdpa_workspace_size", "sdpa_fwd", "sdpa_bwd", "sdpa_last_error_string",
+    "sdpa_workspace_size", "sdpa_fwd", "sdpa_bwd", "sdpa_last_error_string", "causal_code",
     "sdpa_device_error", "sdpa_version", "sdpa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "STATUS",
 ]
 
@@ -53,7 +53,19 @@ class Problem(ctypes.Structure):
         ("dout", Strides), ("dq", Strides), ("dk", Strides), ("dv", Strides),
         ("descale_q", ctypes.c_void_p), ("descale_k", ctypes.c_void_p),
         ("descale_v", ctypes.c_void_p),
+        ("seq_lens_q", ctypes.c_void_p), ("seq_lens_kv", ctypes.c_void_p),
     ]
+
+
+def causal_code(causal) -> int:
+    """False/0: no mask; True/1/"top_left": top-left causal; 2/"bottom_right": bottom-right."""
+    if causal in (False, None, 0):
+        return 0
+    if causal in (True, 1, "top_left"):
+        return 1
+    if causal in (2, "bottom_right"):
+        return 2
+    raise ValueError(f"unknown causal mode {causal!r}")
 
 
 def _load():
@@ -118,9 +130,9 @@ def _ptr(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
 
 
-def make_problem(q, k, v, o=None, *, attn_scale: Optional[float] = None, causal: bool = False,
+def make_problem(q, k, v, o=None, *, attn_scale: Optional[float] = None, causal=False,
                  dout=None, dq=None, dk=None, dv=None, descale_q=None, descale_k=None,
-                 descale_v=None) -> Problem:
+                 descale_v=None, seq_lens_q=None, seq_lens_kv=None) -> Problem:
     """Fills an sdpa_problem_t from logical [b, h, s, d] torch tensors (no copies)."""
     b, h_q, s_q, d = q.shape
     h_kv, s_kv = k.shape[1], k.shape[2]
@@ -129,10 +141,11 @@ def make_problem(q, k, v, o=None, *, attn_scale: Optional[float] = None, causal:
     p.in_dtype = dtype_code(q)
     p.out_dtype = dtype_code(o) if o is not None else p.in_dtype
     p.attn_scale = (1.0 / math.sqrt(d)) if attn_scale is None else float(attn_scale)
-    p.causal = 1 if causal else 0
+    p.causal = causal_code(causal)
     p.q, p.k, p.v, p.o = _strides(q), _strides(k), _strides(v), _strides(o)
     p.dout, p.dq, p.dk, p.dv = _strides(dout), _strides(dq), _strides(dk), _strides(dv)
     p.descale_q, p.descale_k, p.descale_v = _ptr(descale_q), _ptr(descale_k), _ptr(descale_v)
+    p.seq_lens_q, p.seq_lens_kv = _ptr(seq_lens_q), _ptr(seq_lens_kv)
     return p
 
 
@@ -149,21 +162,25 @@ def sdpa_workspace_size(problem: Problem, is_backward: bool) -> int:
     return n.value
 
 
-def sdpa_fwd(q, k, v, o, lse=None, *, attn_scale: Optional[float] = None, causal: bool = False,
-             descale_q=None, descale_k=None, descale_v=None, workspace=None, stream=None) -> None:
-    """O (and LSE when ``lse`` is given: fp32 [b, h_q, s_q] contiguous) from Q, K, V."""
+def sdpa_fwd(q, k, v, o, lse=None, *, attn_scale: Optional[float] = None, causal=False,
+             descale_q=None, descale_k=None, descale_v=None, workspace=None, stream=None,
+             seq_lens_q=None, seq_lens_kv=None) -> None:
+    """O (and LSE when ``lse`` is given: fp32 [b, h_q, s_q] contiguous) from Q, K, V.
+
+    seq_lens_q / seq_lens_kv: optional int32 CUDA tensors of b valid lengths."""
     p = make_problem(q, k, v, o, attn_scale=attn_scale, causal=causal, descale_q=descale_q,
-                     descale_k=descale_k, descale_v=descale_v)
+                     descale_k=descale_k, descale_v=descale_v, seq_lens_q=seq_lens_q,
+                     seq_lens_kv=seq_lens_kv)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.sdpa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                         _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def sdpa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, *, attn_scale: Optional[float] = None,
-             causal: bool = False, stream=None) -> None:
+             causal=False, stream=None, seq_lens_q=None, seq_lens_kv=None) -> None:
     """dQ, dK, dV (overwritten) for the incoming gradient ``dout``."""
     p = make_problem(q, k, v, o, attn_scale=attn_scale, causal=causal, dout=dout, dq=dq, dk=dk,
-                     dv=dv)
+                     dv=dv, seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.sdpa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
                         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream)))
@@ -173,7 +190,7 @@ NOALLOC_SCRATCH_BYTES = 32 << 20  # SDPA_NOALLOC_SCRATCH_BYTES in include/sdpa.h
 
 
 def sdpa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, *, attn_scale: Optional[float] = None,
-                     causal: bool = False, stream=None) -> None:
+                     causal=False, stream=None) -> None:
     """sdpa_bwd without a workspace, for callers that cannot allocate device memory: the
     scratch is a fixed 32 MiB array inside the library, shared by every call (calls must not
     overlap on the GPU; larger problems raise SdpaError with SDPA_ERR_UNSUPPORTED)."""

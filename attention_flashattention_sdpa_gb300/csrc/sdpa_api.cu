@@ -152,8 +152,12 @@ sdpa_status_t check_problem(const sdpa_problem_t* p, bool backward) {
   if (!valid_dtype(p->in_dtype)) return fail(SDPA_ERR_INVALID_ARG, "unknown in_dtype %d", p->in_dtype);
   if (!valid_dtype(p->out_dtype))
     return fail(SDPA_ERR_INVALID_ARG, "unknown out_dtype %d", p->out_dtype);
-  if (p->causal != 0 && p->causal != 1)
-    return fail(SDPA_ERR_INVALID_ARG, "causal must be 0 or 1, got %d", p->causal);
+  if (p->causal < 0 || p->causal > 2)
+    return fail(SDPA_ERR_INVALID_ARG, "causal must be 0 (none), 1 (top-left) or 2 (bottom-right), got %d",
+                p->causal);
+  if ((p->seq_lens_q && reinterpret_cast<uintptr_t>(p->seq_lens_q) % 4) ||
+      (p->seq_lens_kv && reinterpret_cast<uintptr_t>(p->seq_lens_kv) % 4))
+    return fail(SDPA_ERR_LAYOUT, "seq_lens_q / seq_lens_kv must be 4-byte aligned");
   if (!std::isfinite(p->attn_scale))
     return fail(SDPA_ERR_INVALID_ARG, "attn_scale must be finite");
   if (p->in_dtype == SDPA_DTYPE_E4M3) {
@@ -235,7 +239,10 @@ sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const void* k, co
   prm.s_q = p->s_q;
   prm.s_kv = p->s_kv;
   prm.group = p->h_q / p->h_kv;
-  prm.causal = p->causal;
+  prm.causal = p->causal != 0;
+  prm.bottom_right = p->causal == 2;
+  prm.seq_lens_q = p->seq_lens_q;
+  prm.seq_lens_kv = p->seq_lens_kv;
   const int rows_per_cta = 128 * sdpa::fwd_q_tiles(p->d, p->in_dtype);
   prm.num_m_blocks = (p->s_q + rows_per_cta - 1) / rows_per_cta;
   prm.scale_log2 = scale_log2_of(p->attn_scale);
@@ -323,7 +330,10 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
   prm.s_kv = p->s_kv;
   prm.d = p->d;
   prm.group = p->h_q / p->h_kv;
-  prm.causal = p->causal;
+  prm.causal = p->causal != 0;
+  prm.bottom_right = p->causal == 2;
+  prm.seq_lens_q = p->seq_lens_q;
+  prm.seq_lens_kv = p->seq_lens_kv;
   prm.s_q_pad = s_q_pad;
   prm.scale = p->attn_scale;
   prm.scale_log2 = p->attn_scale * 1.4426950408889634f;

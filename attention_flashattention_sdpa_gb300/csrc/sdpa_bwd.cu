@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
   const int row = blockIdx.x * ROWS + threadIdx.x / TPR;
   const int part = threadIdx.x % TPR;
   float acc = 0.f;
-  const bool valid = row < p.s_q;
+  const bool valid = row < batch_lens(p, bi).len_q;   // padded rows take no part
   if (valid) {
     const T* o = reinterpret_cast<const T*>(p.o) + bi * p.o_sb + hq * p.o_sh + row * p.o_ss + part * 8;
     const T* g = reinterpret_cast<const T*>(p.dout) + bi * p.do_sb + hq * p.do_sh + row * p.do_ss + part * 8;
@@ -104,7 +104,9 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
     if (part == 0) {
       // Stored negated, so the main kernel adds them with paired fp32 instructions.
       p.delta[vrow] = valid ? -acc : 0.f;
-      p.lse2[vrow] = valid ? -p.lse[static_cast<int64_t>(bh) * p.s_q + row] * kLog2e : -INFINITY;
+      // Rows with no visible key (LSE = -inf) and padded rows get P = 0 everywhere.
+      const float lse = valid ? p.lse[static_cast<int64_t>(bh) * p.s_q + row] : -INFINITY;
+      p.lse2[vrow] = (lse == -INFINITY) ? -INFINITY : -lse * kLog2e;
     }
   }
 }
@@ -227,9 +229,12 @@ struct alignas(8) BwdBarriers {
   int abort;
 };
 
-// Query blocks visible to KV block j (top-left causal: query row >= key row).
-__device__ __forceinline__ int first_q_block(const BwdParams& p, int j) {
-  return p.causal ? j : 0;
+// First query block (of `bq` rows) that can see key block j of a batch: with a causal mask
+// key row kv is visible to query i iff kv <= i + off.
+__device__ __forceinline__ int first_q_block(const BwdParams& p, const Lens& L, int j, int bq) {
+  if (!p.causal) return 0;
+  const int r0 = j * kBlockN - L.off;
+  return r0 <= 0 ? 0 : r0 / bq;
 }
 
 template <int D, int DT>
@@ -256,9 +261,11 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   const int bhk = unit / p.kv_split;
   const int bi = bhk / p.h_kv;
   const int hk = bhk % p.h_kv;
-  const int n_qb = (p.s_q + kBlockM - 1) / kBlockM;
-  const int q_first = first_q_block(p, j);
-  const int per_head = q_first < n_qb ? n_qb - q_first : 0;
+  const Lens L = batch_lens(p, bi);
+  const int n_qb = (L.len_q + kBlockM - 1) / kBlockM;
+  const int q_first = first_q_block(p, L, j, kBlockM);
+  const bool kv_live = j * kBlockN < L.len_kv;              // this block holds a valid key
+  const int per_head = (kv_live && q_first < n_qb) ? n_qb - q_first : 0;
   const int head0 = hk * p.group + split * p.heads_per_split;
   const int n_heads = max(0, min(p.heads_per_split, (hk + 1) * p.group - head0));
   const int n_iter = per_head * n_heads;
@@ -468,8 +475,12 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       tmem_ld32(X + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
       tmem_ld32(X + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
       tmem_ld_wait();
-      const bool need_mask = p.causal && (q0 < j * kBlockN + kBlockN - 1);
-      const int lim = kv_row - q0;                        // column c visible iff c >= lim
+      // Query column c is visible to key row kv_row iff c >= lim (causal: kv <= q + off);
+      // keys beyond len_kv see nothing.  Padded query columns already have P = 0.
+      const bool need_mask = (p.causal && (q0 + L.off < j * kBlockN + kBlockN - 1)) ||
+                             (j * kBlockN + kBlockN > L.len_kv);
+      int lim = p.causal ? kv_row - q0 - L.off : -(1 << 30);
+      if (kv_row >= L.len_kv) lim = 1 << 30;
       uint32_t pk[32];
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
 #pragma unroll
@@ -715,9 +726,11 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
   const int bhk = unit / p.kv_split;
   const int bi = bhk / p.h_kv;
   const int hk = bhk % p.h_kv;
-  const int n_qb = (p.s_q + C::BQ - 1) / C::BQ;
-  const int q_first = p.causal ? (j * kBlockN) / C::BQ : 0;
-  const int per_head = q_first < n_qb ? n_qb - q_first : 0;
+  const Lens L = batch_lens(p, bi);
+  const int n_qb = (L.len_q + C::BQ - 1) / C::BQ;
+  const int q_first = first_q_block(p, L, j, C::BQ);
+  const bool kv_live = j * kBlockN < L.len_kv;
+  const int per_head = (kv_live && q_first < n_qb) ? n_qb - q_first : 0;
   const int head0 = hk * p.group + split * p.heads_per_split;
   const int n_heads = max(0, min(p.heads_per_split, (hk + 1) * p.group - head0));
   const int n_iter = per_head * n_heads;
@@ -792,8 +805,10 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
       tmem_ld32(tmem + lane_base + C::COL_DP, *reinterpret_cast<uint32_t(*)[32]>(&dpv[0]));
       tmem_ld32(tmem + lane_base + C::COL_DP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dpv[32]));
       tmem_ld_wait();
-      const bool need_mask = p.causal && (q0 < j * kBlockN + kBlockN - 1);
-      const int lim = kv_row - q0;                  // query column c visible iff c >= lim
+      const bool need_mask = (p.causal && (q0 + L.off < j * kBlockN + kBlockN - 1)) ||
+                             (j * kBlockN + kBlockN > L.len_kv);
+      int lim = p.causal ? kv_row - q0 - L.off : -(1 << 30);  // column c visible iff c >= lim
+      if (kv_row >= L.len_kv) lim = 1 << 30;
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
       uint32_t pk[32], ds[32];
 #pragma unroll

@@ -90,13 +90,14 @@ __device__ __forceinline__ uint32_t pack4_e4m3(float a, float b, float c, float 
   return (lo & 0xFFFFu) | (hi << 16);
 }
 
-// Number of key blocks a query tile pair starting at row m0 must visit.
-__device__ __forceinline__ int kv_blocks_for(const FwdParams& p, int m0, int rows) {
-  const int nfull = (p.s_kv + kBlockN - 1) / kBlockN;
-  if (!p.causal) return nfull;
-  const int last_row = min(m0 + rows, p.s_q) - 1;
-  const int n = last_row / kBlockN + 1;
-  return n < nfull ? n : nfull;
+// Number of key blocks the query rows [m0, m0 + rows) of a batch must visit (0 when none of
+// them has a visible key).
+__device__ __forceinline__ int kv_blocks_for(const FwdParams& p, const Lens& L, int m0, int rows) {
+  if (m0 >= L.len_q) return 0;
+  const int last_row = min(m0 + rows, L.len_q) - 1;
+  int lim = L.len_kv - 1;                         // last visible key of any of these rows
+  if (p.causal) lim = min(lim, last_row + L.off);
+  return lim < 0 ? 0 : lim / kBlockN + 1;
 }
 
 template <int D, int DT, int OUT_DT>
@@ -127,7 +128,8 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
   const int hk = hq / p.group;
   const int m_blk = p.num_m_blocks - 1 - blockIdx.x / n_bh;
   const int m0 = m_blk * kBlockM * NQT;
-  const int n_blocks = kv_blocks_for(p, m0, kBlockM * NQT);
+  const Lens L = batch_lens(p, bi);
+  const int n_blocks = kv_blocks_for(p, L, m0, kBlockM * NQT);
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
@@ -163,7 +165,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
   if constexpr (NQT == 2) regs_dec<80>();
   if (warp == 0) {
     // ================================ TMA producer ====================================
-    if (elect_one_sync()) {
+    if (elect_one_sync() && n_blocks > 0) {
       tma_prefetch_desc(&p.tm_q);
       tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
@@ -243,6 +245,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
                  (!first || k > 0) ? 1u : 0u, FP8);
         }
       };
+      ok = n_blocks > 0;
       for (int t = 0; t < NQT && ok; ++t) ok = mbar_wait(&bars.q_full[t], 0, abort_flag);
       tc_fence_after();
       if (NQT == 2) {
@@ -324,8 +327,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       c_scale *= __ldg(p.descale_q) * __ldg(p.descale_k);
       v_scale = __ldg(p.descale_v);
     }
-    // Highest key index this row may see.
-    const int row_limit = p.causal ? min(q_row, p.s_kv - 1) : p.s_kv - 1;
+    // Highest key index this row may see (-1: none, e.g. a padded row).
+    int row_limit = L.len_kv - 1;
+    if (p.causal) row_limit = min(row_limit, q_row + L.off);
+    if (q_row >= L.len_q) row_limit = -1;
 
     float m_ref = -INFINITY;   // running max (log2 domain, scale folded in)
     float l = 0.f;             // running sum of exp2(x - m_ref + P_OFFSET)
@@ -345,8 +350,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       tmem_ld_wait();
 
       const int kv0 = j * kBlockN;
-      const bool need_mask = (kv0 + kBlockN - 1 > p.s_kv - 1) ||
-                             (p.causal && kv0 + kBlockN - 1 > tile_row0);
+      const bool need_mask = (kv0 + kBlockN - 1 > L.len_kv - 1) ||
+                             (p.causal && kv0 + kBlockN - 1 > tile_row0 + L.off) ||
+                             (tile_row0 + kBlockM > L.len_q);
       if (need_mask) {
         const int lim = row_limit - kv0;
 #pragma unroll
@@ -369,7 +375,8 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         alpha = ex2(m_ref - m_cand);
         m_ref = m_cand;
       }
-      const float neg_m = C::P_OFFSET - m_ref;
+      // A row that has seen no visible key yet keeps m_ref = -inf and all its P are 0.
+      const float neg_m = (m_ref == -INFINITY) ? 0.f : C::P_OFFSET - m_ref;
 
       // x = s * scale - m in pairs; P = 2^x; row sums in pairs.
       const float2 cs2 = make_float2(c_scale, c_scale);
@@ -420,18 +427,24 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
     }
 
     // ---- epilogue: O / l through shared memory and a TMA store; LSE ------------------
-    ok = ok && mbar_wait_warp(&bars.o_full[t], 0, abort_flag);
+    // A CTA whose rows see no key at all (padding) skips the pipeline and writes zeros.
+    ok = ok && (n_blocks == 0 || mbar_wait_warp(&bars.o_full[t], 0, abort_flag));
     uint8_t* stage = (NQT == 2) ? (sQ + t * C::TILE_BYTES) : sRing;
     if (ok) {
       tc_fence_after();
-      const float inv_l = v_scale / l;
+      const float inv_l = (l > 0.f) ? v_scale / l : 0.f;   // rows without a visible key: O = 0
       const uint32_t o_addr = tmem + lane_off + C::O_COL0 + t * D;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t ov[64];
-        tmem_ld32(o_addr + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
-        tmem_ld32(o_addr + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
-        tmem_ld_wait();
+        if (n_blocks > 0) {
+          tmem_ld32(o_addr + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
+          tmem_ld32(o_addr + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&ov[32]));
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) ov[i] = 0u;
+        }
         uint8_t* rowp = stage + c * 16384 + r * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
@@ -446,7 +459,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       fence_proxy_async_smem();
       if (p.lse != nullptr && q_row < p.s_q)
         p.lse[(static_cast<int64_t>(bi) * p.h_q + hq) * p.s_q + q_row] =
-            (m_ref - C::P_OFFSET + __log2f(l)) * kLn2;
+            (l > 0.f) ? (m_ref - C::P_OFFSET + __log2f(l)) * kLn2 : -INFINITY;
     }
     // Every thread of the warpgroup arrives exactly once, whatever happened above, so the
     // bounded wait below can only fail through a timeout, never deadlock.

@@ -24,6 +24,9 @@ struct FwdParams {
   int group;                  // h_q / h_kv
   int causal;
   int num_m_blocks;           // ceil(s_q / (128 * q tiles per CTA))
+  const int32_t* seq_lens_q;  // per-batch valid rows, or nullptr
+  const int32_t* seq_lens_kv;
+  int bottom_right;           // causal alignment: key j visible iff j <= i + len_kv - len_q
   float scale_log2;           // |attn_scale| * log2(e) (0 is replaced by a tiny positive value)
   int negate_scores;          // attn_scale < 0: the QK^T MMA negates its A operand
 };
@@ -55,6 +58,9 @@ struct BwdParams {
   int s_q_pad;                  // s_q rounded up to 128
   float scale;                  // attn_scale
   float scale_log2;             // attn_scale * log2(e)
+  const int32_t* seq_lens_q;    // per-batch valid rows, or nullptr
+  const int32_t* seq_lens_kv;
+  int bottom_right;             // causal alignment: key j visible iff j <= i + len_kv - len_q
   // Split groups: when a KV head's query heads are shared between `kv_split` CTAs, each CTA
   // adds its dK/dV partial into fp32 accumulators and a last pass writes dK, dV.
   int kv_split;                 // CTAs per (batch, KV head, KV block); 1 = no split
@@ -75,5 +81,24 @@ int bwd_kv_split(int b, int h_q, int h_kv, int s_kv);
 size_t bwd_workspace_bytes(int b, int h_q, int h_kv, int s_q, int s_kv, int d);
 cudaError_t launch_bwd(const BwdParams& p, int dtype, cudaStream_t st);
 uint32_t bwd_take_device_error();
+
+}  // namespace sdpa
+
+namespace sdpa {
+
+// Valid rows and causal offset of batch `bi`: key j is visible to query i < len_q iff
+// j < len_kv and (no mask, or j <= i + off).
+struct Lens {
+  int len_q, len_kv, off;
+};
+
+template <typename P>
+__device__ __forceinline__ Lens batch_lens(const P& p, int bi) {
+  Lens L;
+  L.len_q = p.seq_lens_q ? min(max(__ldg(p.seq_lens_q + bi), 0), p.s_q) : p.s_q;
+  L.len_kv = p.seq_lens_kv ? min(max(__ldg(p.seq_lens_kv + bi), 0), p.s_kv) : p.s_kv;
+  L.off = p.bottom_right ? L.len_kv - L.len_q : 0;
+  return L;
+}
 
 }  // namespace sdpa

@@ -86,12 +86,22 @@ typedef struct {
   float attn_scale;    /* multiplies Q K^T before the mask and softmax; any finite value
                           (usually 1/sqrt(d)) [cuDNN 9 blog, Fig. 4: scale node after BMM1] */
   int32_t causal;      /* 0: no mask.  1: top-left causal, key j visible to query i iff j <= i
-                          (row 0 sees only key 0) [codelab §7] */
+                          (row 0 sees only key 0) [codelab §7].  2: bottom-right causal, key j
+                          visible to query i iff j <= i + len_kv - len_q (the last query sees
+                          every key, as when decoding against a KV cache) */
   sdpa_strides_t q, k, v, o;         /* forward and backward */
   sdpa_strides_t dout, dq, dk, dv;   /* backward only (dout = incoming gradient dO) */
   const float* descale_q;  /* E4M3 only: DEVICE pointers to one fp32 each; the real value of */
   const float* descale_k;  /* a stored code x is decode(x) * descale (per-tensor scaling of    */
   const float* descale_v;  /* the delayed-scaling FP8 recipe, codelab §10).  NULL otherwise.   */
+  /* Variable lengths (the SDPA node's padding mask with per-batch sequence lengths, cuDNN 9
+   * blog walkthrough).  Optional DEVICE pointers to b int32 values; NULL = every row valid.
+   * For batch b only query rows i < len_q[b] and keys j < len_kv[b] take part (values are
+   * clamped to [0, s_q] and [0, s_kv]).  Rows with no visible key — padded rows, or early rows
+   * of a bottom-right mask with len_kv < len_q — give O = 0 and LSE = -inf, and padded rows of
+   * dQ, dK and dV are 0. */
+  const int32_t* seq_lens_q;
+  const int32_t* seq_lens_kv;
 } sdpa_problem_t;
 
 /*

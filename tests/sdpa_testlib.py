@@ -55,8 +55,15 @@ def f64(t: torch.Tensor, descale: float = 1.0) -> np.ndarray:
     return oracle.to_f64(t.cpu(), descale)
 
 
-def run_fwd(w: Workload, x: Inputs, with_lse: bool = True, out_dtype=torch.bfloat16):
+def run_fwd(w: Workload, x: Inputs, with_lse: bool = True, out_dtype=torch.bfloat16,
+            causal=None, seq_lens_q=None, seq_lens_kv=None):
     m = lib()
+    causal = w.causal if causal is None else causal
+    lens = {}
+    if seq_lens_q is not None:
+        lens["seq_lens_q"] = torch.tensor(seq_lens_q, dtype=torch.int32, device="cuda")
+    if seq_lens_kv is not None:
+        lens["seq_lens_kv"] = torch.tensor(seq_lens_kv, dtype=torch.int32, device="cuda")
     q, k, v = to_dev(x.q), to_dev(x.k), to_dev(x.v)
     odt = out_dtype if w.dtype == "e4m3" else q.dtype
     o, obuf = guarded_empty_like(q, odt)
@@ -68,7 +75,7 @@ def run_fwd(w: Workload, x: Inputs, with_lse: bool = True, out_dtype=torch.bfloa
         kw = dict(descale_q=torch.tensor([x.descale_q], device="cuda"),
                   descale_k=torch.tensor([x.descale_k], device="cuda"),
                   descale_v=torch.tensor([x.descale_v], device="cuda"))
-    m.sdpa_fwd(q, k, v, o, lse, attn_scale=w.scale, causal=w.causal, **kw)
+    m.sdpa_fwd(q, k, v, o, lse, attn_scale=w.scale, causal=causal, **kw, **lens)
     torch.cuda.synchronize()
     assert m.sdpa_device_error() == 0
     check_guard(obuf, "O")
@@ -77,17 +84,24 @@ def run_fwd(w: Workload, x: Inputs, with_lse: bool = True, out_dtype=torch.bfloa
     return o, lse, (q, k, v)
 
 
-def run_bwd(w: Workload, dev_qkv, o, lse, do_cpu: torch.Tensor):
+def run_bwd(w: Workload, dev_qkv, o, lse, do_cpu: torch.Tensor, causal=None, seq_lens_q=None,
+            seq_lens_kv=None):
     m = lib()
+    causal = w.causal if causal is None else causal
+    lens = {}
+    if seq_lens_q is not None:
+        lens["seq_lens_q"] = torch.tensor(seq_lens_q, dtype=torch.int32, device="cuda")
+    if seq_lens_kv is not None:
+        lens["seq_lens_kv"] = torch.tensor(seq_lens_kv, dtype=torch.int32, device="cuda")
     q, k, v = dev_qkv
     do = to_dev(do_cpu)
     dq, dqb = guarded_empty_like(q)
     dk, dkb = guarded_empty_like(k)
     dv, dvb = guarded_empty_like(v)
-    p = m.make_problem(q, k, v, o, attn_scale=w.scale, causal=w.causal, dout=do, dq=dq, dk=dk, dv=dv)
+    p = m.make_problem(q, k, v, o, attn_scale=w.scale, causal=causal, dout=do, dq=dq, dk=dk, dv=dv)
     ws = torch.empty(m.sdpa_workspace_size(p, True), dtype=torch.uint8, device="cuda")
     ws.fill_(0xAB)  # contents on entry must not matter
-    m.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, attn_scale=w.scale, causal=w.causal)
+    m.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, attn_scale=w.scale, causal=causal, **lens)
     torch.cuda.synchronize()
     assert m.sdpa_device_error() == 0
     for b, n in ((dqb, "dQ"), (dkb, "dK"), (dvb, "dV")):

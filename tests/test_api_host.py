@@ -74,7 +74,8 @@ def _bwd(m, p, ws=FAKE, ws_bytes=1 << 40, lse=FAKE, q=FAKE):
     (dict(s_q=0), 1, "sizes"),
     (dict(s_kv=0), 1, "sizes"),
     (dict(h_kv=3, h_q=4), 1, "multiple"),
-    (dict(causal=2), 1, "causal"),
+    (dict(causal=3), 1, "causal"),
+    (dict(causal=-1), 1, "causal"),
     (dict(attn_scale=float("nan")), 1, "finite"),
     (dict(in_dtype=7), 1, "in_dtype"),
     (dict(out_dtype=1), 2, "same dtype"),
