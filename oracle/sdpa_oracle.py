@@ -29,6 +29,10 @@ module's own table and multiplied by their descale):
   i iff j <= i + len_kv[b] - len_q[b] (the last query sees every key, as in decoding with a
   KV cache).  A row with no visible key (a padded row, or an early row of a bottom-right
   mask with len_kv < len_q) gives O = 0 and LSE = -inf, and passes no gradient;
+* ALiBi (the SDPA node's ALiBi-mask option in the cuDNN 9 blog's walkthrough): with one
+  slope m_h per query head, the scaled score of (i, j) gains m_h * (j - i - off), off being
+  the bottom-right offset len_kv - len_q (0 otherwise), before the mask and the softmax — a
+  linear penalty on the distance to the aligned diagonal;
 * head grouping: query head ``hq`` reads KV head ``hq // (h_q // h_kv)`` (contiguous
   groups; the codelab's §9 "Comparing MHA, GQA and MQA" broadcasts each KV head to
   its group of query heads);
@@ -49,7 +53,7 @@ from typing import Iterable, Sequence, Tuple
 import numpy as np
 
 __all__ = [
-    "visible_mask", "kv_head_of", "head_forward", "forward", "forward_rows",
+    "visible_mask", "kv_head_of", "alibi_bias", "head_forward", "forward", "forward_rows",
     "backward", "backward_dq_rows", "backward_kv_rows", "backward_kv_head", "e4m3_decode_table",
     "decode_e4m3", "to_f64",
 ]
@@ -127,13 +131,22 @@ def kv_head_of(hq: int, h_q: int, h_kv: int) -> int:
     return hq // (h_q // h_kv)
 
 
+def alibi_bias(s_q: int, s_kv: int, slope: float, off: int = 0) -> np.ndarray:
+    """[s_q, s_kv] additive bias slope * (j - i - off)."""
+    i = np.arange(s_q)[:, None]
+    j = np.arange(s_kv)[None, :]
+    return slope * (j - i - off).astype(np.float64)
+
+
 def head_forward(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, scale: float,
-                 mask: np.ndarray, allow_empty: bool = False):
+                 mask: np.ndarray, allow_empty: bool = False, bias: np.ndarray | None = None):
     """One (batch, head) slice: returns (O [s_q,d], LSE [s_q], P [s_q,s_kv]).
 
-    A row with no visible key has no softmax: it is rejected, or with allow_empty gives
-    O = 0, LSE = -inf and P = 0."""
+    bias: optional additive term on the scaled scores.  A row with no visible key has no
+    softmax: it is rejected, or with allow_empty gives O = 0, LSE = -inf and P = 0."""
     S = scale * (qh @ kh.T)                                   # step 1 + scale
+    if bias is not None:
+        S = S + bias
     has = mask.any(axis=1)
     if not allow_empty and not has.all():
         raise ValueError("a query row has no visible key")
@@ -154,12 +167,20 @@ def _batch_mask(s_q, s_kv, causal, bi, seq_lens_q, seq_lens_kv, bottom_right):
     return visible_mask(s_q, s_kv, causal, lq, lkv, bottom_right)
 
 
+def _batch_off(s_q, s_kv, bi, seq_lens_q, seq_lens_kv, bottom_right):
+    if not bottom_right:
+        return 0
+    lq = s_q if seq_lens_q is None else int(seq_lens_q[bi])
+    lkv = s_kv if seq_lens_kv is None else int(seq_lens_kv[bi])
+    return lkv - lq
+
+
 def forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: bool,
-            seq_lens_q=None, seq_lens_kv=None, bottom_right: bool = False):
+            seq_lens_q=None, seq_lens_kv=None, bottom_right: bool = False, alibi_slopes=None):
     """Full forward on logical BHSD fp64 arrays.
 
-    q: [b, h_q, s_q, d]; k, v: [b, h_kv, s_kv, d]; optional per-batch valid lengths.
-    Returns (O [b,h_q,s_q,d], LSE [b,h_q,s_q])."""
+    q: [b, h_q, s_q, d]; k, v: [b, h_kv, s_kv, d]; optional per-batch valid lengths and
+    per-query-head ALiBi slopes.  Returns (O [b,h_q,s_q,d], LSE [b,h_q,s_q])."""
     b, h_q, s_q, d = q.shape
     h_kv, s_kv = k.shape[1], k.shape[2]
     varlen = seq_lens_q is not None or seq_lens_kv is not None or bottom_right
@@ -167,10 +188,12 @@ def forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: b
     L = np.empty((b, h_q, s_q), dtype=np.float64)
     for bi in range(b):
         mask = _batch_mask(s_q, s_kv, causal, bi, seq_lens_q, seq_lens_kv, bottom_right)
+        off = _batch_off(s_q, s_kv, bi, seq_lens_q, seq_lens_kv, bottom_right)
         for hq in range(h_q):
             hk = kv_head_of(hq, h_q, h_kv)
+            bias = None if alibi_slopes is None else alibi_bias(s_q, s_kv, float(alibi_slopes[hq]), off)
             O[bi, hq], L[bi, hq], _ = head_forward(q[bi, hq], k[bi, hk], v[bi, hk], scale, mask,
-                                                   allow_empty=varlen)
+                                                   allow_empty=varlen, bias=bias)
     return O, L
 
 
@@ -193,8 +216,8 @@ def forward_rows(q_rows: np.ndarray, rows: Sequence[int], kh: np.ndarray, vh: np
 # Backward
 # ---------------------------------------------------------------------------
 
-def _head_backward(qh, kh, vh, doh, scale, mask, allow_empty=False):
-    _, _, P = head_forward(qh, kh, vh, scale, mask, allow_empty)
+def _head_backward(qh, kh, vh, doh, scale, mask, allow_empty=False, bias=None):
+    _, _, P = head_forward(qh, kh, vh, scale, mask, allow_empty, bias)
     dV = P.T @ doh
     dP = doh @ vh.T
     delta = (P * dP).sum(axis=1)
@@ -205,7 +228,7 @@ def _head_backward(qh, kh, vh, doh, scale, mask, allow_empty=False):
 
 
 def backward(q, k, v, do, scale: float, causal: bool, seq_lens_q=None, seq_lens_kv=None,
-             bottom_right: bool = False):
+             bottom_right: bool = False, alibi_slopes=None):
     """Full backward on logical BHSD fp64 arrays: returns (dQ, dK, dV).
 
     dK, dV have K's and V's shapes and hold the sum over each KV head's group.  With
@@ -218,10 +241,12 @@ def backward(q, k, v, do, scale: float, causal: bool, seq_lens_q=None, seq_lens_
     dV = np.zeros(v.shape, dtype=np.float64)
     for bi in range(b):
         mask = _batch_mask(s_q, s_kv, causal, bi, seq_lens_q, seq_lens_kv, bottom_right)
+        off = _batch_off(s_q, s_kv, bi, seq_lens_q, seq_lens_kv, bottom_right)
         for hq in range(h_q):
             hk = kv_head_of(hq, h_q, h_kv)
+            bias = None if alibi_slopes is None else alibi_bias(s_q, s_kv, float(alibi_slopes[hq]), off)
             gq, gk, gv = _head_backward(q[bi, hq], k[bi, hk], v[bi, hk], do[bi, hq], scale, mask,
-                                        allow_empty=varlen)
+                                        allow_empty=varlen, bias=bias)
             dQ[bi, hq] = gq
             dK[bi, hk] += gk
             dV[bi, hk] += gv

@@ -425,3 +425,56 @@ def test_varlen_backward_matches_finite_differences():
             x[idx] = old
             fd[idx] = (lp - lm) / 2e-6
         assert np.linalg.norm(got - fd) / np.linalg.norm(fd) < 1e-6
+
+
+# ---------------------------------------------------------------------------
+# ALiBi
+# ---------------------------------------------------------------------------
+
+def test_alibi_brute_force_and_limits():
+    """Brute force with explicit loops; zero slopes change nothing; a huge slope makes a
+    causal row attend only to its own key (every earlier key is penalised away)."""
+    q, k, v = _rand(1, 2, 5, 3), _rand(1, 2, 7, 3), _rand(1, 2, 7, 3)
+    slopes = [0.25, 1.5]
+    for causal in (False, True):
+        O, L = oracle.forward(q, k, v, 0.8, causal, alibi_slopes=slopes)
+        for h in range(2):
+            for i in range(5):
+                w = [0.0 if (causal and j > i) else
+                     math.exp(0.8 * float(q[0, h, i] @ k[0, h, j]) + slopes[h] * (j - i)) for j in range(7)]
+                tot = sum(w)
+                np.testing.assert_allclose(O[0, h, i], sum(w[j] / tot * v[0, h, j] for j in range(7)), atol=1e-12)
+                np.testing.assert_allclose(L[0, h, i], math.log(tot), atol=1e-12)
+    O0, _ = oracle.forward(q, k, v, 0.8, True, alibi_slopes=[0.0, 0.0])
+    Oc, _ = oracle.forward(q, k, v, 0.8, True)
+    np.testing.assert_allclose(O0, Oc, atol=1e-14)
+    Oh, _ = oracle.forward(q, k, v, 0.8, True, alibi_slopes=[200.0, 200.0])
+    np.testing.assert_allclose(Oh[0, :, :5], v[0, :, :5], atol=1e-12)
+
+
+def test_alibi_bottom_right_offset_and_gradients():
+    """Bottom-right: the bias is zero on the aligned diagonal (j = i + off).  Backward with
+    ALiBi against finite differences (the bias has no gradient)."""
+    q, k, v, do = _rand(1, 1, 3, 2), _rand(1, 1, 6, 2), _rand(1, 1, 6, 2), _rand(1, 1, 3, 2)
+    O, L = oracle.forward(q, k, v, 0.5, True, None, None, True, alibi_slopes=[0.7])
+    for i in range(3):
+        w = [math.exp(0.5 * float(q[0, 0, i] @ k[0, 0, j]) + 0.7 * (j - i - 3)) for j in range(i + 4)]
+        np.testing.assert_allclose(L[0, 0, i], math.log(sum(w)), atol=1e-12)
+    dQ, dK, dV = oracle.backward(q, k, v, do, 0.5, True, None, None, True, alibi_slopes=[0.7])
+
+    def loss(q_, k_, v_):
+        Ox, _ = oracle.forward(q_, k_, v_, 0.5, True, None, None, True, alibi_slopes=[0.7])
+        return float((Ox * do).sum())
+    for which, got in ((0, dQ), (1, dK), (2, dV)):
+        args = [q.copy(), k.copy(), v.copy()]
+        x = args[which]
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + 1e-6
+            lp = loss(*args)
+            x[idx] = old - 1e-6
+            lm = loss(*args)
+            x[idx] = old
+            fd[idx] = (lp - lm) / 2e-6
+        assert np.linalg.norm(got - fd) / np.linalg.norm(fd) < 1e-6
