@@ -32,7 +32,10 @@ module's own table and multiplied by their descale):
 * ALiBi (the SDPA node's ALiBi-mask option in the cuDNN 9 blog's walkthrough): with one
   slope m_h per query head, the scaled score of (i, j) gains m_h * (j - i - off), off being
   the bottom-right offset len_kv - len_q (0 otherwise), before the mask and the softmax — a
-  linear penalty on the distance to the aligned diagonal;
+  linear penalty on the distance to the aligned diagonal.  The pages name the option but no
+  slopes; without caller slopes the default is the geometric sequence m_h = 2^(-8 (h+1) / H)
+  of the ALiBi paper (Press, Smith and Lewis, "Train Short, Test Long", §3: 1/2 ... 1/256 for
+  8 heads), applied by the same formula to any head count;
 * head grouping: query head ``hq`` reads KV head ``hq // (h_q // h_kv)`` (contiguous
   groups; the codelab's §9 "Comparing MHA, GQA and MQA" broadcasts each KV head to
   its group of query heads);
@@ -53,7 +56,7 @@ from typing import Iterable, Sequence, Tuple
 import numpy as np
 
 __all__ = [
-    "visible_mask", "kv_head_of", "alibi_bias", "head_forward", "forward", "forward_rows",
+    "visible_mask", "kv_head_of", "alibi_default_slopes", "alibi_bias", "head_forward", "forward", "forward_rows",
     "backward", "backward_dq_rows", "backward_kv_rows", "backward_kv_head", "e4m3_decode_table",
     "decode_e4m3", "to_f64",
 ]
@@ -129,6 +132,11 @@ def kv_head_of(hq: int, h_q: int, h_kv: int) -> int:
     if h_kv <= 0 or h_q % h_kv:
         raise ValueError("h_q must be a positive multiple of h_kv")
     return hq // (h_q // h_kv)
+
+
+def alibi_default_slopes(h_q: int) -> np.ndarray:
+    """m_h = 2^(-8 (h + 1) / h_q) for h = 0 .. h_q - 1."""
+    return np.array([2.0 ** (-8.0 * (h + 1) / h_q) for h in range(h_q)], dtype=np.float64)
 
 
 def alibi_bias(s_q: int, s_kv: int, slope: float, off: int = 0) -> np.ndarray:

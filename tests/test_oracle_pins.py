@@ -478,3 +478,13 @@ def test_alibi_bottom_right_offset_and_gradients():
             x[idx] = old
             fd[idx] = (lp - lm) / 2e-6
         assert np.linalg.norm(got - fd) / np.linalg.norm(fd) < 1e-6
+
+
+def test_alibi_default_slopes_match_the_alibi_paper():
+    """Press, Smith and Lewis, "Train Short, Test Long", §3: with 8 heads the slopes are
+    1/2, 1/4, ..., 1/256; with 16 heads they start at 2^-0.5 and halve every two heads."""
+    np.testing.assert_array_equal(oracle.alibi_default_slopes(8), [1 / 2 ** k for k in range(1, 9)])
+    s16 = oracle.alibi_default_slopes(16)
+    np.testing.assert_allclose(s16[0], 2 ** -0.5, rtol=1e-15)
+    np.testing.assert_allclose(s16[1::2], [1 / 2 ** k for k in range(1, 9)], rtol=1e-15)
+    np.testing.assert_allclose(s16[1:] / s16[:-1], 2 ** -0.5, rtol=1e-14)
