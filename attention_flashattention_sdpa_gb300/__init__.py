@@ -54,6 +54,7 @@ class Problem(ctypes.Structure):
         ("descale_q", ctypes.c_void_p), ("descale_k", ctypes.c_void_p),
         ("descale_v", ctypes.c_void_p),
         ("seq_lens_q", ctypes.c_void_p), ("seq_lens_kv", ctypes.c_void_p),
+        ("alibi", ctypes.c_int32), ("alibi_slopes", ctypes.c_void_p),
     ]
 
 
@@ -132,8 +133,12 @@ def _ptr(t) -> Optional[int]:
 
 def make_problem(q, k, v, o=None, *, attn_scale: Optional[float] = None, causal=False,
                  dout=None, dq=None, dk=None, dv=None, descale_q=None, descale_k=None,
-                 descale_v=None, seq_lens_q=None, seq_lens_kv=None) -> Problem:
-    """Fills an sdpa_problem_t from logical [b, h, s, d] torch tensors (no copies)."""
+                 descale_v=None, seq_lens_q=None, seq_lens_kv=None, alibi=False,
+                 alibi_slopes=None) -> Problem:
+    """Fills an sdpa_problem_t from logical [b, h, s, d] torch tensors (no copies).
+
+    ALiBi is on when ``alibi`` is true or ``alibi_slopes`` (fp32 CUDA tensor of h_q slopes)
+    is given; without slopes the library uses 2^(-8 (h + 1) / h_q)."""
     b, h_q, s_q, d = q.shape
     h_kv, s_kv = k.shape[1], k.shape[2]
     p = Problem()
@@ -146,6 +151,8 @@ def make_problem(q, k, v, o=None, *, attn_scale: Optional[float] = None, causal=
     p.dout, p.dq, p.dk, p.dv = _strides(dout), _strides(dq), _strides(dk), _strides(dv)
     p.descale_q, p.descale_k, p.descale_v = _ptr(descale_q), _ptr(descale_k), _ptr(descale_v)
     p.seq_lens_q, p.seq_lens_kv = _ptr(seq_lens_q), _ptr(seq_lens_kv)
+    p.alibi = 1 if (alibi or alibi_slopes is not None) else 0
+    p.alibi_slopes = _ptr(alibi_slopes)
     return p
 
 
@@ -164,23 +171,27 @@ def sdpa_workspace_size(problem: Problem, is_backward: bool) -> int:
 
 def sdpa_fwd(q, k, v, o, lse=None, *, attn_scale: Optional[float] = None, causal=False,
              descale_q=None, descale_k=None, descale_v=None, workspace=None, stream=None,
-             seq_lens_q=None, seq_lens_kv=None) -> None:
+             seq_lens_q=None, seq_lens_kv=None, alibi=False, alibi_slopes=None) -> None:
     """O (and LSE when ``lse`` is given: fp32 [b, h_q, s_q] contiguous) from Q, K, V.
 
-    seq_lens_q / seq_lens_kv: optional int32 CUDA tensors of b valid lengths."""
+    seq_lens_q / seq_lens_kv: optional int32 CUDA tensors of b valid lengths.
+    alibi / alibi_slopes: the linear position bias (see :func:`make_problem`)."""
     p = make_problem(q, k, v, o, attn_scale=attn_scale, causal=causal, descale_q=descale_q,
                      descale_k=descale_k, descale_v=descale_v, seq_lens_q=seq_lens_q,
-                     seq_lens_kv=seq_lens_kv)
+                     seq_lens_kv=seq_lens_kv, alibi=alibi, alibi_slopes=alibi_slopes)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.sdpa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                         _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def sdpa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, *, attn_scale: Optional[float] = None,
-             causal=False, stream=None, seq_lens_q=None, seq_lens_kv=None) -> None:
-    """dQ, dK, dV (overwritten) for the incoming gradient ``dout``."""
+             causal=False, stream=None, seq_lens_q=None, seq_lens_kv=None, alibi=False,
+             alibi_slopes=None) -> None:
+    """dQ, dK, dV (overwritten) for the incoming gradient ``dout``; the masking, lengths and
+    ALiBi options must be those of the forward call that produced ``o`` and ``lse``."""
     p = make_problem(q, k, v, o, attn_scale=attn_scale, causal=causal, dout=dout, dq=dq, dk=dk,
-                     dv=dv, seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv)
+                     dv=dv, seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv, alibi=alibi,
+                     alibi_slopes=alibi_slopes)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.sdpa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
                         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream)))

@@ -160,6 +160,12 @@ sdpa_status_t check_problem(const sdpa_problem_t* p, bool backward) {
     return fail(SDPA_ERR_LAYOUT, "seq_lens_q / seq_lens_kv must be 4-byte aligned");
   if (!std::isfinite(p->attn_scale))
     return fail(SDPA_ERR_INVALID_ARG, "attn_scale must be finite");
+  if (p->alibi != 0 && p->alibi != 1)
+    return fail(SDPA_ERR_INVALID_ARG, "alibi must be 0 or 1, got %d", p->alibi);
+  if (p->alibi && p->alibi_slopes && reinterpret_cast<uintptr_t>(p->alibi_slopes) % 4)
+    return fail(SDPA_ERR_LAYOUT, "alibi_slopes must be 4-byte aligned");
+  if (p->alibi && p->in_dtype == SDPA_DTYPE_E4M3)
+    return fail(SDPA_ERR_UNSUPPORTED, "ALiBi takes F16 or BF16 inputs, not E4M3");
   if (p->in_dtype == SDPA_DTYPE_E4M3) {
     if (backward)
       return fail(SDPA_ERR_UNSUPPORTED, "the backward pass takes F16 or BF16 inputs, not E4M3");
@@ -243,6 +249,8 @@ sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const void* k, co
   prm.bottom_right = p->causal == 2;
   prm.seq_lens_q = p->seq_lens_q;
   prm.seq_lens_kv = p->seq_lens_kv;
+  prm.alibi = p->alibi;
+  prm.alibi_slopes = p->alibi ? p->alibi_slopes : nullptr;
   const int rows_per_cta = 128 * sdpa::fwd_q_tiles(p->d, p->in_dtype);
   prm.num_m_blocks = (p->s_q + rows_per_cta - 1) / rows_per_cta;
   prm.scale_log2 = scale_log2_of(p->attn_scale);
@@ -334,6 +342,8 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
   prm.bottom_right = p->causal == 2;
   prm.seq_lens_q = p->seq_lens_q;
   prm.seq_lens_kv = p->seq_lens_kv;
+  prm.alibi = p->alibi;
+  prm.alibi_slopes = p->alibi ? p->alibi_slopes : nullptr;
   prm.s_q_pad = s_q_pad;
   prm.scale = p->attn_scale;
   prm.scale_log2 = p->attn_scale * 1.4426950408889634f;

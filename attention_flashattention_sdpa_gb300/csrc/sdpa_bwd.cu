@@ -237,7 +237,7 @@ __device__ __forceinline__ int first_q_block(const BwdParams& p, const Lens& L, 
   return r0 <= 0 ? 0 : r0 / bq;
 }
 
-template <int D, int DT>
+template <int D, int DT, bool ALIBI>
 __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -483,9 +483,15 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       if (kv_row >= L.len_kv) lim = 1 << 30;
       uint32_t pk[32];
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+      // ALiBi: slope * (key - query - off) for query q0 + c, i.e. base - slope * c.
+      const float sl2 = ALIBI ? alibi_slope_log2(p, iter_head(n)) : 0.f;
+      const float base = sl2 * static_cast<float>(kv_row - q0 - L.off);
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
-        const float2 nl = *reinterpret_cast<const float2*>(nlse2 + c);
+        float2 nl = *reinterpret_cast<const float2*>(nlse2 + c);
+        if constexpr (ALIBI)
+          nl = add2(nl, make_float2(fmaf(-sl2, static_cast<float>(c), base),
+                                    fmaf(-sl2, static_cast<float>(c + 1), base)));
         const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl);
         // A fixed share of the pairs is computed on the FMA pipe, the rest on the MUFU unit.
         const bool poly = kPolyEvery > 0 && (c / 2) % (kPolyEvery > 0 ? kPolyEvery : 1) == kPolyEvery - 1;
@@ -695,7 +701,7 @@ struct alignas(8) D256Barriers {
   int abort;
 };
 
-template <int DT>
+template <int DT, bool ALIBI>
 __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant__ BwdParams p) {
   using C = D256;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -810,11 +816,17 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
       int lim = p.causal ? kv_row - q0 - L.off : -(1 << 30);  // column c visible iff c >= lim
       if (kv_row >= L.len_kv) lim = 1 << 30;
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+      // ALiBi: slope * (key - query - off) for query q0 + c, i.e. base - slope * c.
+      const float sl2 = ALIBI ? alibi_slope_log2(p, hq) : 0.f;
+      const float base = sl2 * static_cast<float>(kv_row - q0 - L.off);
       uint32_t pk[32], ds[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
-        const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2,
-                              *reinterpret_cast<const float2*>(sVec + c));
+        float2 nl = *reinterpret_cast<const float2*>(sVec + c);
+        if constexpr (ALIBI)
+          nl = add2(nl, make_float2(fmaf(-sl2, static_cast<float>(c), base),
+                                    fmaf(-sl2, static_cast<float>(c + 1), base)));
+        const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl);
         float p0 = ex2(x.x), p1 = ex2(x.y);
         if (need_mask) {
           if (c < lim) p0 = 0.f;
@@ -995,7 +1007,7 @@ cudaError_t launch_d256(const BwdParams& p, cudaStream_t st) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  auto kern = bwd_d256_kernel<DT>;
+  auto kern = p.alibi ? bwd_d256_kernel<DT, true> : bwd_d256_kernel<DT, false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, D256::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const unsigned grid = 2u * p.b * p.h_kv * p.kv_split * ((p.s_kv + kBlockN - 1) / kBlockN);
@@ -1026,7 +1038,7 @@ cudaError_t launch_t(const BwdParams& p, cudaStream_t st) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  auto kern = bwd_main_kernel<D, DT>;
+  auto kern = p.alibi ? bwd_main_kernel<D, DT, true> : bwd_main_kernel<D, DT, false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const unsigned gmain = static_cast<unsigned>(p.b) * p.h_kv * p.kv_split * ((p.s_kv + kBlockN - 1) / kBlockN);

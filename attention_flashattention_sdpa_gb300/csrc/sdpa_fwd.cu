@@ -100,7 +100,7 @@ __device__ __forceinline__ int kv_blocks_for(const FwdParams& p, const Lens& L, 
   return lim < 0 ? 0 : lim / kBlockN + 1;
 }
 
-template <int D, int DT, int OUT_DT>
+template <int D, int DT, int OUT_DT, bool ALIBI>
 __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
     sdpa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D, DT>;
@@ -331,6 +331,8 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
     int row_limit = L.len_kv - 1;
     if (p.causal) row_limit = min(row_limit, q_row + L.off);
     if (q_row >= L.len_q) row_limit = -1;
+    // ALiBi: slope_hq * (key - row - off) joins the scores in the log2 domain.
+    const float sl2 = ALIBI ? alibi_slope_log2(p, hq) : 0.f;
 
     float m_ref = -INFINITY;   // running max (log2 domain, scale folded in)
     float l = 0.f;             // running sum of exp2(x - m_ref + P_OFFSET)
@@ -359,6 +361,19 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         for (int c = 0; c < kBlockN; ++c)
           if (c > lim) sv[c] = __float_as_uint(-INFINITY);
       }
+      if constexpr (ALIBI) {
+        // x = s * scale + slope * (kv0 + c - q_row - off), computed before the row max.
+        const float base = sl2 * static_cast<float>(kv0 - q_row - L.off);
+        const float2 cs2 = make_float2(c_scale, c_scale);
+#pragma unroll
+        for (int c = 0; c < kBlockN; c += 2) {
+          const float2 b2 = make_float2(fmaf(sl2, static_cast<float>(c), base),
+                                        fmaf(sl2, static_cast<float>(c + 1), base));
+          const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), cs2, b2);
+          sv[c] = __float_as_uint(x.x);
+          sv[c + 1] = __float_as_uint(x.y);
+        }
+      }
       // Row max over four independent chains of three-input max.
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
@@ -369,7 +384,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         mx3 = max3(mx3, __uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7]));
       }
       const float mx = max3(mx0, mx1, fmaxf(mx2, mx3));
-      const float m_cand = mx * c_scale;
+      const float m_cand = ALIBI ? mx : mx * c_scale;
       float alpha = 1.f;
       if (m_cand > m_ref + C::THRESH) {
         alpha = ex2(m_ref - m_cand);
@@ -379,7 +394,8 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       const float neg_m = (m_ref == -INFINITY) ? 0.f : C::P_OFFSET - m_ref;
 
       // x = s * scale - m in pairs; P = 2^x; row sums in pairs.
-      const float2 cs2 = make_float2(c_scale, c_scale);
+      const float cs = ALIBI ? 1.f : c_scale;   // with ALiBi the scores are already scaled
+      const float2 cs2 = make_float2(cs, cs);
       const float2 nm2 = make_float2(neg_m, neg_m);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
       uint32_t pk[C::P_COLS];
@@ -486,7 +502,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
 template <int D, int DT, int OUT_DT>
 cudaError_t launch_t(const FwdParams& p, cudaStream_t st) {
   using C = FwdCfg<D, DT>;
-  auto kern = sdpa_fwd_kernel<D, DT, OUT_DT>;
+  auto kern = sdpa_fwd_kernel<D, DT, OUT_DT, false>;
+  if constexpr (DT != kE4M3) {
+    if (p.alibi) kern = sdpa_fwd_kernel<D, DT, OUT_DT, true>;
+  }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);
   if (e != cudaSuccess) return e;

@@ -29,6 +29,8 @@ struct FwdParams {
   int bottom_right;           // causal alignment: key j visible iff j <= i + len_kv - len_q
   float scale_log2;           // |attn_scale| * log2(e) (0 is replaced by a tiny positive value)
   int negate_scores;          // attn_scale < 0: the QK^T MMA negates its A operand
+  int alibi;                  // add slope_hq * (j - i - off) to the scaled scores
+  const float* alibi_slopes;  // [h_q] fp32, or nullptr for the geometric default
 };
 
 // Number of Q tiles (of 128 rows) one forward CTA processes.
@@ -72,6 +74,8 @@ struct BwdParams {
   void* dv;
   int64_t dk_sb, dk_sh, dk_ss;
   int64_t dv_sb, dv_sh, dv_ss;
+  int alibi;                    // add slope_hq * (j - i - off) to the scaled scores
+  const float* alibi_slopes;    // [h_q] fp32, or nullptr for the geometric default
 };
 
 // How many CTAs share one (batch, KV head, KV block) in the backward pass.  A fixed policy
@@ -99,6 +103,15 @@ __device__ __forceinline__ Lens batch_lens(const P& p, int bi) {
   L.len_kv = p.seq_lens_kv ? min(max(__ldg(p.seq_lens_kv + bi), 0), p.s_kv) : p.s_kv;
   L.off = p.bottom_right ? L.len_kv - L.len_q : 0;
   return L;
+}
+
+// ALiBi slope of query head hq, in the log2 domain the kernels exponentiate in: the
+// caller's slope, or the geometric sequence 2^(-8 (hq + 1) / h_q).
+template <typename P>
+__device__ __forceinline__ float alibi_slope_log2(const P& p, int hq) {
+  const float m = p.alibi_slopes ? __ldg(p.alibi_slopes + hq)
+                                 : exp2f(-8.f * static_cast<float>(hq + 1) / static_cast<float>(p.h_q));
+  return m * 1.4426950408889634f;
 }
 
 }  // namespace sdpa

@@ -12,6 +12,8 @@ Prints one JSON line (rank 0).  Flags:
                                   same workload) and print the reference line
   --profile-step                  run one untimed fwd+bwd (the command profiled with ncu)
   --sweep                         one line per configuration (tables; not the contract line)
+  --measure-peaks                 dense GEMM peaks of this GPU through the vendor library:
+                                  bf16 (torch.matmul) and E4M3 (torch._scaled_mm), 8192^3
 """
 from __future__ import annotations
 
@@ -413,12 +415,53 @@ def _load_traffic():
         return None
 
 
+def gemm_peak_tflops(dtype_name: str, n: int = 8192, reps: int = 20) -> float:
+    """Best-of-`reps` dense n^3 GEMM throughput through the vendor library (CUDA events).
+
+    bf16: torch.matmul.  e4m3: torch._scaled_mm with unit scales and a bf16 output (the
+    FP8 denominator: MEASURED_PEAKS.json holds none)."""
+    import torch
+    dt = {"bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn}[dtype_name]
+    g = torch.Generator(device="cuda").manual_seed(0)
+    a = torch.randn(n, n, device="cuda", generator=g).to(dt)
+    b = torch.randn(n, n, device="cuda", generator=g).to(dt).t()
+    one = torch.tensor(1.0, device="cuda")
+    if dtype_name == "bf16":
+        f = lambda: a @ b
+    else:
+        f = lambda: torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+    for _ in range(5):
+        f()
+    torch.cuda.synchronize()
+    best = float("inf")
+    for _ in range(reps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(); f(); e.record()
+        torch.cuda.synchronize()
+        best = min(best, s.elapsed_time(e))
+    return 2.0 * n ** 3 / best / 1e9
+
+
+def run_measure_peaks(args):
+    import torch
+    torch.cuda.set_device(0)
+    line = {"bf16_tflops_burst": gemm_peak_tflops("bf16"),
+            "e4m3_tflops_burst": gemm_peak_tflops("e4m3"),
+            "how": "8192^3 GEMM, best of 20, CUDA events; bf16 torch.matmul, e4m3 torch._scaled_mm"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_sweep(args):
     """One line per configuration (for tables)."""
     import torch
     from sdpa_workloads import all_workloads
     torch.cuda.set_device(0)
     peaks = load_peaks()
+    try:
+        peaks["e4m3_tflops"] = gemm_peak_tflops("e4m3")
+    except Exception:  # no FP8 GEMM in this torch build: report no FP8 fraction
+        peaks["e4m3_tflops"] = None
     for w in all_workloads():
         if w.name.startswith("tiny"):
             continue
@@ -445,7 +488,8 @@ def sweep_one(w, peaks, args):
                   descale_v=torch.tensor([x.descale_v], device="cuda"))
     o = torch.empty_strided(q.shape, q.stride(), dtype=odt, device="cuda")
     lse = torch.empty(w.b, w.h_q, w.s_q, dtype=torch.float32, device="cuda") if (w.stats or w.backward) else None
-    fwd = lambda: sdpa.sdpa_fwd(q, k, v, o, lse, attn_scale=w.scale, causal=w.causal, **kw)
+    fwd = lambda: sdpa.sdpa_fwd(q, k, v, o, lse, attn_scale=w.scale, causal=w.causal, alibi=w.alibi,
+                                **kw)
     st = torch.cuda.current_stream()
     reps = max(5, min(200, int(2e13 / max(w.fwd_flops(), 1))))
     for _ in range(3):
@@ -465,12 +509,16 @@ def sweep_one(w, peaks, args):
         (lse.numel() * 4 if lse is not None else 0)
     line["fwd_hbm_gbs"] = io_bytes / fwd_ms / 1e6
     line["fwd_frac_of_bf16_peak"] = line["fwd_tflops"] / peak if w.dtype != "e4m3" else None
+    if w.dtype == "e4m3" and peaks.get("e4m3_tflops"):
+        line["e4m3_peak_tflops"] = peaks["e4m3_tflops"]
+        line["fwd_frac_of_e4m3_peak"] = line["fwd_tflops"] / peaks["e4m3_tflops"]
     if w.backward:
         do = dev(x.do)
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         p = sdpa.make_problem(q, k, v, o, attn_scale=w.scale, causal=w.causal, dout=do, dq=dq, dk=dk, dv=dv)
         ws = torch.empty(sdpa.sdpa_workspace_size(p, True), dtype=torch.uint8, device="cuda")
-        bwd = lambda: sdpa.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, attn_scale=w.scale, causal=w.causal)
+        bwd = lambda: sdpa.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, attn_scale=w.scale, causal=w.causal,
+                                    alibi=w.alibi)
         for _ in range(3):
             bwd()
         torch.cuda.synchronize()
@@ -497,6 +545,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--profile-step", action="store_true")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--measure-peaks", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args(argv)
@@ -506,6 +555,8 @@ def main(argv=None):
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.measure_peaks:
+        return run_measure_peaks(args)
     return run_cuda(args)
 
 

@@ -102,6 +102,15 @@ typedef struct {
    * dQ, dK and dV are 0. */
   const int32_t* seq_lens_q;
   const int32_t* seq_lens_kv;
+  /* ALiBi (the SDPA node's ALiBi-mask option, cuDNN 9 blog walkthrough; the pages name it but
+   * do not define it, and this is the linear-bias reading).  0 = off.  1 = the scaled score of
+   * (i, j) gains m_hq * (j - i - off) before the mask and softmax, off = len_kv - len_q under
+   * bottom-right causal alignment and 0 otherwise: zero on the aligned diagonal, a penalty
+   * growing linearly with the distance to earlier keys.  m_hq = alibi_slopes[hq] (a DEVICE
+   * pointer to h_q fp32 values), or, when alibi_slopes is NULL, the geometric slopes
+   * 2^(-8 (hq + 1) / h_q).  F16 and BF16 inputs only; the bias has no gradient. */
+  int32_t alibi;
+  const float* alibi_slopes;
 } sdpa_problem_t;
 
 /*

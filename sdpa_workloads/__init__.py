@@ -48,6 +48,7 @@ class Workload:
     backward: bool = False
     stats: bool = True    # forward writes the per-row log-sum-exp
     attn_scale: Optional[float] = None
+    alibi: bool = False   # ALiBi position bias with the default slopes
 
     @property
     def scale(self) -> float:
@@ -88,10 +89,17 @@ def grouped(h_kv: int) -> Workload:
     return Workload(f"{tag}_70b", 1, 64, h_kv, 8192, 8192, 128, "bf16", causal=True, backward=True)
 
 
+def training_alibi(s: int) -> Workload:
+    """The training workload with the ALiBi bias on (default slopes)."""
+    w = training(s)
+    return Workload(f"training_alibi_bf16_causal_d128_s{s}", w.b, w.h_q, w.h_kv, s, s, w.d,
+                    w.dtype, causal=True, backward=True, alibi=True)
+
+
 def all_workloads():
     out = [tiny(False), tiny(True), gpt2_inference()]
     out += [training(s) for s in TRAINING_SEQ_LENS]
-    out += [fp8_large_head(), grouped(8), grouped(1), grouped(64)]
+    out += [fp8_large_head(), grouped(8), grouped(1), grouped(64), training_alibi(8192)]
     return out
 
 

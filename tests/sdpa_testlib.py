@@ -55,11 +55,21 @@ def f64(t: torch.Tensor, descale: float = 1.0) -> np.ndarray:
     return oracle.to_f64(t.cpu(), descale)
 
 
+def _alibi_kwargs(alibi) -> dict:
+    """None: off; "default": the library's geometric slopes; a sequence: per-head slopes."""
+    if alibi is None:
+        return {}
+    if isinstance(alibi, str):
+        assert alibi == "default"
+        return {"alibi": True}
+    return {"alibi_slopes": torch.tensor(list(alibi), dtype=torch.float32, device="cuda")}
+
+
 def run_fwd(w: Workload, x: Inputs, with_lse: bool = True, out_dtype=torch.bfloat16,
-            causal=None, seq_lens_q=None, seq_lens_kv=None):
+            causal=None, seq_lens_q=None, seq_lens_kv=None, alibi=None):
     m = lib()
     causal = w.causal if causal is None else causal
-    lens = {}
+    lens = _alibi_kwargs(alibi)
     if seq_lens_q is not None:
         lens["seq_lens_q"] = torch.tensor(seq_lens_q, dtype=torch.int32, device="cuda")
     if seq_lens_kv is not None:
@@ -85,10 +95,10 @@ def run_fwd(w: Workload, x: Inputs, with_lse: bool = True, out_dtype=torch.bfloa
 
 
 def run_bwd(w: Workload, dev_qkv, o, lse, do_cpu: torch.Tensor, causal=None, seq_lens_q=None,
-            seq_lens_kv=None):
+            seq_lens_kv=None, alibi=None):
     m = lib()
     causal = w.causal if causal is None else causal
-    lens = {}
+    lens = _alibi_kwargs(alibi)
     if seq_lens_q is not None:
         lens["seq_lens_q"] = torch.tensor(seq_lens_q, dtype=torch.int32, device="cuda")
     if seq_lens_kv is not None:

@@ -82,6 +82,10 @@ def _bwd(m, p, ws=FAKE, ws_bytes=1 << 40, lse=FAKE, q=FAKE):
     (dict(in_dtype=2, out_dtype=1, d=128), 1, "descale"),
     (dict(in_dtype=2, out_dtype=1), 2, "d = 128 or 256"),
     (dict(in_dtype=2, out_dtype=2), 2, "output"),
+    (dict(alibi=2), 1, "alibi"),
+    (dict(alibi=1, alibi_slopes=FAKE + 2), 3, "alibi_slopes"),
+    (dict(alibi=1, in_dtype=2, out_dtype=1, d=128, descale_q=FAKE, descale_k=FAKE,
+          descale_v=FAKE), 2, "ALiBi"),
 ])
 def test_forward_rejects_bad_problem(m, over, status, msg):
     assert _fwd(m, _problem(m, **over)) == status
