@@ -106,7 +106,10 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
       p.delta[vrow] = valid ? -acc : 0.f;
       // Rows with no visible key (LSE = -inf) and padded rows get P = 0 everywhere.
       const float lse = valid ? p.lse[static_cast<int64_t>(bh) * p.s_q + row] : -INFINITY;
-      p.lse2[vrow] = (lse == -INFINITY) ? -INFINITY : -lse * kLog2e;
+      // ALiBi's bias slope * (key - row - off) is split: -slope * (row mod 128) joins this
+      // per-row term, and slope * (key - 128-aligned block start - off) is added per key row.
+      const float col_bias = p.alibi ? alibi_slope_log2(p, hq) * static_cast<float>(row % kBlockM) : 0.f;
+      p.lse2[vrow] = (lse == -INFINITY) ? -INFINITY : -lse * kLog2e - col_bias;
     }
   }
 }
@@ -483,15 +486,14 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       if (kv_row >= L.len_kv) lim = 1 << 30;
       uint32_t pk[32];
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-      // ALiBi: slope * (key - query - off) for query q0 + c, i.e. base - slope * c.
-      const float sl2 = ALIBI ? alibi_slope_log2(p, iter_head(n)) : 0.f;
-      const float base = sl2 * static_cast<float>(kv_row - q0 - L.off);
+      // ALiBi: the key-row part of the bias (the column part is in the -LSE vector).
+      const float kr = ALIBI ? alibi_slope_log2(p, iter_head(n)) *
+                                   static_cast<float>(kv_row - iter_qblk(n) * kBlockM - L.off) : 0.f;
+      const float2 kr2 = make_float2(kr, kr);
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
         float2 nl = *reinterpret_cast<const float2*>(nlse2 + c);
-        if constexpr (ALIBI)
-          nl = add2(nl, make_float2(fmaf(-sl2, static_cast<float>(c), base),
-                                    fmaf(-sl2, static_cast<float>(c + 1), base)));
+        if constexpr (ALIBI) nl = add2(nl, kr2);
         const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl);
         // A fixed share of the pairs is computed on the FMA pipe, the rest on the MUFU unit.
         const bool poly = kPolyEvery > 0 && (c / 2) % (kPolyEvery > 0 ? kPolyEvery : 1) == kPolyEvery - 1;
@@ -816,16 +818,16 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
       int lim = p.causal ? kv_row - q0 - L.off : -(1 << 30);  // column c visible iff c >= lim
       if (kv_row >= L.len_kv) lim = 1 << 30;
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
-      // ALiBi: slope * (key - query - off) for query q0 + c, i.e. base - slope * c.
-      const float sl2 = ALIBI ? alibi_slope_log2(p, hq) : 0.f;
-      const float base = sl2 * static_cast<float>(kv_row - q0 - L.off);
+      // ALiBi: the key-row part of the bias (the column part is in the -LSE vector, relative
+      // to the 128-aligned block that holds this 64-row query block).
+      const float kr = ALIBI ? alibi_slope_log2(p, hq) *
+                                   static_cast<float>(kv_row - (q0 / kBlockM) * kBlockM - L.off) : 0.f;
+      const float2 kr2 = make_float2(kr, kr);
       uint32_t pk[32], ds[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
         float2 nl = *reinterpret_cast<const float2*>(sVec + c);
-        if constexpr (ALIBI)
-          nl = add2(nl, make_float2(fmaf(-sl2, static_cast<float>(c), base),
-                                    fmaf(-sl2, static_cast<float>(c + 1), base)));
+        if constexpr (ALIBI) nl = add2(nl, kr2);
         const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl);
         float p0 = ex2(x.x), p1 = ex2(x.y);
         if (need_mask) {

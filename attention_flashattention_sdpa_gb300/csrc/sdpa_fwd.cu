@@ -130,6 +130,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
   const int m0 = m_blk * kBlockM * NQT;
   const Lens L = batch_lens(p, bi);
   const int n_blocks = kv_blocks_for(p, L, m0, kBlockM * NQT);
+  // Key block visited at step j.  With ALiBi the bias of a row only falls with distance from
+  // its diagonal, so the blocks go from the last one down: the first block holds the row
+  // maximum (nearly) and the running max seldom has to rescale O.
+  auto kv_block = [&](int j) { return ALIBI ? n_blocks - 1 - j : j; };
 
   if (threadIdx.x == 0) {
     for (int t = 0; t < 2; ++t) {
@@ -185,7 +189,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         uint8_t* dst = sRing + slot * C::TILE_BYTES;
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_4d(dst + c * 16384, map, &bars.kv_full[slot], c * C::CHUNK_ELEMS,
-                      j * kBlockN, hk, bi);
+                      kv_block(j) * kBlockN, hk, bi);
         ++it;
         return true;
       };
@@ -331,7 +335,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
     int row_limit = L.len_kv - 1;
     if (p.causal) row_limit = min(row_limit, q_row + L.off);
     if (q_row >= L.len_q) row_limit = -1;
-    // ALiBi: slope_hq * (key - row - off) joins the scores in the log2 domain.
+    // ALiBi slope of this head in the log2 domain.
     const float sl2 = ALIBI ? alibi_slope_log2(p, hq) : 0.f;
 
     float m_ref = -INFINITY;   // running max (log2 domain, scale folded in)
@@ -351,7 +355,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
       tmem_ld_wait();
 
-      const int kv0 = j * kBlockN;
+      const int kv0 = kv_block(j) * kBlockN;
       const bool need_mask = (kv0 + kBlockN - 1 > L.len_kv - 1) ||
                              (p.causal && kv0 + kBlockN - 1 > tile_row0 + L.off) ||
                              (tile_row0 + kBlockM > L.len_q);
@@ -362,14 +366,13 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
           if (c > lim) sv[c] = __float_as_uint(-INFINITY);
       }
       if constexpr (ALIBI) {
-        // x = s * scale + slope * (kv0 + c - q_row - off), computed before the row max.
-        const float base = sl2 * static_cast<float>(kv0 - q_row - L.off);
+        // ALiBi splits slope * (key - row - off) into a column part slope * c, added here
+        // before the row max, and a row part slope * (kv0 - row - off) folded into the max.
         const float2 cs2 = make_float2(c_scale, c_scale);
 #pragma unroll
         for (int c = 0; c < kBlockN; c += 2) {
-          const float2 b2 = make_float2(fmaf(sl2, static_cast<float>(c), base),
-                                        fmaf(sl2, static_cast<float>(c + 1), base));
-          const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), cs2, b2);
+          const float2 k2 = make_float2(sl2 * static_cast<float>(c), sl2 * static_cast<float>(c + 1));
+          const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), cs2, k2);
           sv[c] = __float_as_uint(x.x);
           sv[c + 1] = __float_as_uint(x.y);
         }
@@ -384,7 +387,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         mx3 = max3(mx3, __uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7]));
       }
       const float mx = max3(mx0, mx1, fmaxf(mx2, mx3));
-      const float m_cand = ALIBI ? mx : mx * c_scale;
+      // ALiBi row part of this key block: slope * (kv0 - q_row - off).
+      const float row_bias = ALIBI ? sl2 * static_cast<float>(kv0 - q_row - L.off) : 0.f;
+      const float m_cand = ALIBI ? mx + row_bias : mx * c_scale;
       float alpha = 1.f;
       if (m_cand > m_ref + C::THRESH) {
         alpha = ex2(m_ref - m_cand);
@@ -395,8 +400,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
 
       // x = s * scale - m in pairs; P = 2^x; row sums in pairs.
       const float cs = ALIBI ? 1.f : c_scale;   // with ALiBi the scores are already scaled
+      const float nm = ALIBI ? neg_m + row_bias : neg_m;
       const float2 cs2 = make_float2(cs, cs);
-      const float2 nm2 = make_float2(neg_m, neg_m);
+      const float2 nm2 = make_float2(nm, nm);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
       uint32_t pk[C::P_COLS];
 #pragma unroll

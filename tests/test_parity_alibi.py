@@ -90,9 +90,11 @@ def test_decode_shape_with_kv_cache():
 
 
 def test_zero_slopes_equal_plain_attention():
+    """Zero slopes give plain attention up to rounding (the ALiBi kernels visit the key blocks
+    in the opposite order, so the sums are not formed in the same order)."""
     w = Workload("t", 1, 2, 2, 256, 256, 128, "bf16", causal=True)
     x = make_inputs(w, seed=4)
     o0, l0, _ = run_fwd(w, x)
     o1, l1, _ = run_fwd(w, x, alibi=[0.0, 0.0])
-    assert (o0.cpu() == o1.cpu()).all()
+    assert_fwd_close(f64(o1), f64(o0))
     np.testing.assert_allclose(l1.cpu().numpy(), l0.cpu().numpy(), atol=1e-5)
