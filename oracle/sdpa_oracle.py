@@ -36,6 +36,14 @@ module's own table and multiplied by their descale):
   slopes; without caller slopes the default is the geometric sequence m_h = 2^(-8 (h+1) / H)
   of the ALiBi paper (Press, Smith and Lewis, "Train Short, Test Long", §3: 1/2 ... 1/256 for
   8 heads), applied by the same formula to any head count;
+* dropout (the SDPA node's dropout option in the cuDNN 9 blog's walkthrough, named and not
+  defined): after the softmax each probability is kept with a keep mask Z and the kept ones
+  are scaled by 1/(1 - p), so O = (P * Z) V / (1 - p); the LSE is that of the undropped
+  softmax.  The mask is drawn by the counter-based Philox4x64-10 generator (Salmon, Moraes,
+  Dror and Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11): element n of the
+  row-major grid [b*h_q][s_q][s_kv rounded up to 128] takes 16-bit lane n % 4 of word
+  (n % 16) // 4 of the block drawn for counter (n // 16, offset, 0, 0) and key (seed, 0),
+  and is kept iff that value is >= round(p * 65536);
 * head grouping: query head ``hq`` reads KV head ``hq // (h_q // h_kv)`` (contiguous
   groups; the codelab's §9 "Comparing MHA, GQA and MQA" broadcasts each KV head to
   its group of query heads);
@@ -43,7 +51,8 @@ module's own table and multiplied by their descale):
   (the pages show a backward graph exists but print no formula): with the incoming
   gradient dO, dV = Pᵀ dO, dP = dO Vᵀ, Delta_i = Σ_j P_ij dP_ij,
   dS = P ∘ (dP − Delta), dQ = scale·dS K, dK = scale·dSᵀ Q, with dK and dV summed
-  over the query heads of each KV group.
+  over the query heads of each KV group.  With dropout, Z = keep / (1 - p) enters as
+  dV = (P∘Z)ᵀ dO and dP = Z ∘ (dO Vᵀ); the rest is unchanged.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against brute force,
 closed forms, invariants and finite differences; none is "parity unpinned".
@@ -56,6 +65,7 @@ from typing import Iterable, Sequence, Tuple
 import numpy as np
 
 __all__ = [
+    "philox4x64", "dropout_threshold", "dropout_keep",
     "visible_mask", "kv_head_of", "alibi_default_slopes", "alibi_bias", "head_forward", "forward", "forward_rows",
     "backward", "backward_dq_rows", "backward_kv_rows", "backward_kv_head", "e4m3_decode_table",
     "decode_e4m3", "to_f64",
@@ -110,6 +120,65 @@ def to_f64(t, descale: float = 1.0) -> np.ndarray:
 # Forward
 # ---------------------------------------------------------------------------
 
+# Philox4x64-10 constants: the round multipliers and the Weyl key increments of the paper.
+PHILOX_M0 = 0xD2E7470EE14C6C93
+PHILOX_M1 = 0xCA5A826395121157
+PHILOX_W0 = 0x9E3779B97F4A7C15
+PHILOX_W1 = 0xBB67AE8584CAA73B
+_MASK64 = (1 << 64) - 1
+
+
+def philox4x64(counter: Sequence[int], key: Sequence[int], rounds: int = 10) -> Tuple[int, ...]:
+    """One Philox4x64 block: four 64-bit words for a 256-bit counter and a 128-bit key.
+
+    Each round multiplies words 0 and 2 by the two constants (full 128-bit products), and
+    the new words are (hi1 ^ x1 ^ k0, lo1, hi0 ^ x3 ^ k1, lo0); the key gains the Weyl
+    increments between rounds.  Plain Python integers, one block at a time."""
+    x0, x1, x2, x3 = (int(c) & _MASK64 for c in counter)
+    k0, k1 = (int(k) & _MASK64 for k in key)
+    for r in range(rounds):
+        if r > 0:
+            k0 = (k0 + PHILOX_W0) & _MASK64
+            k1 = (k1 + PHILOX_W1) & _MASK64
+        p0 = PHILOX_M0 * x0
+        p1 = PHILOX_M1 * x2
+        hi0, lo0 = p0 >> 64, p0 & _MASK64
+        hi1, lo1 = p1 >> 64, p1 & _MASK64
+        x0, x1, x2, x3 = hi1 ^ x1 ^ k0, lo1, hi0 ^ x3 ^ k1, lo0
+    return x0, x1, x2, x3
+
+
+def dropout_threshold(p: float) -> int:
+    """16-bit drop threshold: an element is dropped iff its 16-bit draw is below it."""
+    if not 0.0 <= p < 1.0:
+        raise ValueError("dropout probability must be in [0, 1)")
+    return min(65536, int(math.floor(p * 65536.0 + 0.5)))
+
+
+def dropout_keep(b: int, h_q: int, s_q: int, s_kv: int, p: float, seed: int, offset: int,
+                 rows: Iterable[Tuple[int, int]] | None = None) -> np.ndarray:
+    """Keep mask [b, h_q, s_q, s_kv] (bool) of the Philox draw defined in the module header.
+
+    rows: optional (b*h_q + h, i) pairs; then only those rows are drawn and the result is
+    [len(rows), s_kv]."""
+    t = dropout_threshold(p)
+    row_pitch = (s_kv + 127) // 128 * 128
+    want = list(rows) if rows is not None else [(bh, i) for bh in range(b * h_q) for i in range(s_q)]
+    out = np.empty((len(want), s_kv), dtype=bool)
+    for r, (bh, i) in enumerate(want):
+        n0 = (bh * s_q + i) * row_pitch           # multiple of 16: rows start a new block
+        for g in range(row_pitch // 16):
+            words = philox4x64((n0 // 16 + g, offset, 0, 0), (seed, 0))
+            for e in range(16):
+                j = g * 16 + e
+                if j < s_kv:
+                    u = (words[e // 4] >> (16 * (e % 4))) & 0xFFFF
+                    out[r, j] = u >= t
+    if rows is None:
+        return out.reshape(b, h_q, s_q, s_kv)
+    return out
+
+
 def visible_mask(s_q: int, s_kv: int, causal: bool, len_q: int | None = None,
                  len_kv: int | None = None, bottom_right: bool = False) -> np.ndarray:
     """Boolean [s_q, s_kv]: True where key j is visible to query i.
@@ -147,11 +216,14 @@ def alibi_bias(s_q: int, s_kv: int, slope: float, off: int = 0) -> np.ndarray:
 
 
 def head_forward(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, scale: float,
-                 mask: np.ndarray, allow_empty: bool = False, bias: np.ndarray | None = None):
+                 mask: np.ndarray, allow_empty: bool = False, bias: np.ndarray | None = None,
+                 zdrop: np.ndarray | None = None):
     """One (batch, head) slice: returns (O [s_q,d], LSE [s_q], P [s_q,s_kv]).
 
-    bias: optional additive term on the scaled scores.  A row with no visible key has no
-    softmax: it is rejected, or with allow_empty gives O = 0, LSE = -inf and P = 0."""
+    bias: optional additive term on the scaled scores.  zdrop: optional dropout factor
+    keep / (1 - p) applied to P for O only (P and LSE are those of the softmax).  A row with
+    no visible key has no softmax: it is rejected, or with allow_empty gives O = 0,
+    LSE = -inf and P = 0."""
     S = scale * (qh @ kh.T)                                   # step 1 + scale
     if bias is not None:
         S = S + bias
@@ -163,7 +235,7 @@ def head_forward(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, scale: float,
     E = np.where(mask, np.exp(S - m_safe[:, None]), 0.0)
     l = E.sum(axis=1)                                         # pass 2: row sum
     P = E / np.where(has, l, 1.0)[:, None]                    # pass 3: normalise
-    O = P @ vh                                                # step 3
+    O = (P if zdrop is None else P * zdrop) @ vh              # step 3 (dropout on P)
     with np.errstate(divide="ignore"):
         lse = np.where(has, m_safe + np.log(np.where(has, l, 1.0)), -np.inf)
     return O, lse, P
@@ -183,12 +255,20 @@ def _batch_off(s_q, s_kv, bi, seq_lens_q, seq_lens_kv, bottom_right):
     return lkv - lq
 
 
+def _zdrop(keep, dropout_p, bi, hq):
+    if keep is None:
+        return None
+    return keep[bi, hq].astype(np.float64) / (1.0 - dropout_p)
+
+
 def forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: bool,
-            seq_lens_q=None, seq_lens_kv=None, bottom_right: bool = False, alibi_slopes=None):
+            seq_lens_q=None, seq_lens_kv=None, bottom_right: bool = False, alibi_slopes=None,
+            dropout_p: float = 0.0, keep=None):
     """Full forward on logical BHSD fp64 arrays.
 
-    q: [b, h_q, s_q, d]; k, v: [b, h_kv, s_kv, d]; optional per-batch valid lengths and
-    per-query-head ALiBi slopes.  Returns (O [b,h_q,s_q,d], LSE [b,h_q,s_q])."""
+    q: [b, h_q, s_q, d]; k, v: [b, h_kv, s_kv, d]; optional per-batch valid lengths,
+    per-query-head ALiBi slopes, and a dropout keep mask [b, h_q, s_q, s_kv] with its
+    probability.  Returns (O [b,h_q,s_q,d], LSE [b,h_q,s_q])."""
     b, h_q, s_q, d = q.shape
     h_kv, s_kv = k.shape[1], k.shape[2]
     varlen = seq_lens_q is not None or seq_lens_kv is not None or bottom_right
@@ -201,7 +281,8 @@ def forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: b
             hk = kv_head_of(hq, h_q, h_kv)
             bias = None if alibi_slopes is None else alibi_bias(s_q, s_kv, float(alibi_slopes[hq]), off)
             O[bi, hq], L[bi, hq], _ = head_forward(q[bi, hq], k[bi, hk], v[bi, hk], scale, mask,
-                                                   allow_empty=varlen, bias=bias)
+                                                   allow_empty=varlen, bias=bias,
+                                                   zdrop=_zdrop(keep, dropout_p, bi, hq))
     return O, L
 
 
@@ -224,10 +305,11 @@ def forward_rows(q_rows: np.ndarray, rows: Sequence[int], kh: np.ndarray, vh: np
 # Backward
 # ---------------------------------------------------------------------------
 
-def _head_backward(qh, kh, vh, doh, scale, mask, allow_empty=False, bias=None):
+def _head_backward(qh, kh, vh, doh, scale, mask, allow_empty=False, bias=None, zdrop=None):
     _, _, P = head_forward(qh, kh, vh, scale, mask, allow_empty, bias)
-    dV = P.T @ doh
-    dP = doh @ vh.T
+    Z = 1.0 if zdrop is None else zdrop
+    dV = (P * Z).T @ doh
+    dP = Z * (doh @ vh.T)
     delta = (P * dP).sum(axis=1)
     dS = P * (dP - delta[:, None])
     dQ = scale * (dS @ kh)
@@ -236,7 +318,7 @@ def _head_backward(qh, kh, vh, doh, scale, mask, allow_empty=False, bias=None):
 
 
 def backward(q, k, v, do, scale: float, causal: bool, seq_lens_q=None, seq_lens_kv=None,
-             bottom_right: bool = False, alibi_slopes=None):
+             bottom_right: bool = False, alibi_slopes=None, dropout_p: float = 0.0, keep=None):
     """Full backward on logical BHSD fp64 arrays: returns (dQ, dK, dV).
 
     dK, dV have K's and V's shapes and hold the sum over each KV head's group.  With
@@ -254,7 +336,8 @@ def backward(q, k, v, do, scale: float, causal: bool, seq_lens_q=None, seq_lens_
             hk = kv_head_of(hq, h_q, h_kv)
             bias = None if alibi_slopes is None else alibi_bias(s_q, s_kv, float(alibi_slopes[hq]), off)
             gq, gk, gv = _head_backward(q[bi, hq], k[bi, hk], v[bi, hk], do[bi, hq], scale, mask,
-                                        allow_empty=varlen, bias=bias)
+                                        allow_empty=varlen, bias=bias,
+                                        zdrop=_zdrop(keep, dropout_p, bi, hq))
             dQ[bi, hq] = gq
             dK[bi, hk] += gk
             dV[bi, hk] += gv

@@ -488,3 +488,96 @@ def test_alibi_default_slopes_match_the_alibi_paper():
     np.testing.assert_allclose(s16[0], 2 ** -0.5, rtol=1e-15)
     np.testing.assert_allclose(s16[1::2], [1 / 2 ** k for k in range(1, 9)], rtol=1e-15)
     np.testing.assert_allclose(s16[1:] / s16[:-1], 2 ** -0.5, rtol=1e-14)
+
+
+# ---------------------------------------------------------------------------
+# Dropout: Philox4x64-10 and the keep mask
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("counter,key", [
+    ([5, 0, 0, 0], [7, 9]),
+    ([2 ** 64 - 1, 5, 0, 0], [2 ** 63 + 11, 2 ** 64 - 3]),      # carry into word 1
+    ([123456789, 2 ** 64 - 1, 2 ** 64 - 1, 3], [0, 0]),
+])
+def test_philox_matches_numpy_bit_generator(counter, key):
+    """numpy's Philox is Philox4x64-10 from the same paper; it increments its 256-bit counter
+    before drawing each block, so its n-th block is ours at counter + n."""
+    bg = np.random.Philox(counter=np.array(counter, dtype=np.uint64), key=np.array(key, dtype=np.uint64))
+    assert [int(w) for w in bg.state["state"]["counter"]] == counter
+    got = bg.random_raw(12)
+    c = sum(int(w) << (64 * i) for i, w in enumerate(counter))
+    want = []
+    for n in range(1, 4):
+        cn = (c + n) % (1 << 256)
+        want += oracle.philox4x64([(cn >> (64 * i)) & ((1 << 64) - 1) for i in range(4)], key)
+    assert [int(x) for x in got] == want
+
+
+def test_dropout_threshold():
+    assert oracle.dropout_threshold(0.0) == 0
+    assert oracle.dropout_threshold(0.5) == 32768
+    assert oracle.dropout_threshold(0.1) == 6554
+    assert oracle.dropout_threshold(1 - 2 ** -20) == 65536
+    with pytest.raises(ValueError):
+        oracle.dropout_threshold(1.0)
+
+
+def test_dropout_keep_mask_properties():
+    """p = 0 keeps everything; the kept fraction is 1 - p within 5 sigma; a larger p drops a
+    superset (same draws, higher threshold); drawing selected rows equals the full draw;
+    seeds and offsets change the draw."""
+    b, h, s_q, s_kv = 1, 2, 40, 300
+    assert oracle.dropout_keep(b, h, s_q, s_kv, 0.0, 1, 0).all()
+    k3 = oracle.dropout_keep(b, h, s_q, s_kv, 0.3, 1234, 7)
+    k6 = oracle.dropout_keep(b, h, s_q, s_kv, 0.6, 1234, 7)
+    n = k3.size
+    for kk, p in ((k3, 0.3), (k6, 0.6)):
+        assert abs(kk.sum() - n * (1 - p)) < 5 * math.sqrt(n * p * (1 - p))
+    assert not (k6 & ~k3).any()
+    rows = [(1, 0), (0, 39), (1, 17)]
+    sub = oracle.dropout_keep(b, h, s_q, s_kv, 0.3, 1234, 7, rows=rows)
+    for r, (bh, i) in enumerate(rows):
+        assert (sub[r] == k3[0, bh, i]).all()
+    assert (oracle.dropout_keep(b, h, s_q, s_kv, 0.3, 1235, 7) != k3).mean() > 0.2
+    assert (oracle.dropout_keep(b, h, s_q, s_kv, 0.3, 1234, 8) != k3).mean() > 0.2
+
+
+def test_dropout_forward_is_unbiased_exactly():
+    """Averaging O over every keep pattern of one row, weighted by its probability, gives the
+    undropped O exactly (E[keep / (1 - p)] = 1); LSE never depends on the mask."""
+    q, k, v = _rand(1, 1, 1, 4), _rand(1, 1, 3, 4), _rand(1, 1, 3, 4)
+    p = 0.35
+    O0, L0 = oracle.forward(q, k, v, 0.7, False)
+    acc = np.zeros_like(O0)
+    for bits in range(8):
+        keep = np.array([[[[bool(bits >> j & 1) for j in range(3)]]]])
+        w = (1 - p) ** keep.sum() * p ** (3 - keep.sum())
+        O, L = oracle.forward(q, k, v, 0.7, False, dropout_p=p, keep=keep)
+        np.testing.assert_allclose(L, L0, atol=1e-15)
+        acc += w * O
+    np.testing.assert_allclose(acc, O0, atol=1e-12)
+
+
+def test_dropout_backward_matches_finite_differences():
+    rng = np.random.default_rng(3)
+    q, k, v, do = _rand(1, 2, 5, 3), _rand(1, 1, 6, 3), _rand(1, 1, 6, 3), _rand(1, 2, 5, 3)
+    keep = rng.random((1, 2, 5, 6)) > 0.4
+    p = 0.4
+    dQ, dK, dV = oracle.backward(q, k, v, do, 0.6, True, dropout_p=p, keep=keep)
+
+    def loss(q_, k_, v_):
+        O, _ = oracle.forward(q_, k_, v_, 0.6, True, dropout_p=p, keep=keep)
+        return float((O * do).sum())
+    for which, got in ((0, dQ), (1, dK), (2, dV)):
+        args = [q.copy(), k.copy(), v.copy()]
+        x = args[which]
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + 1e-6
+            lp = loss(*args)
+            x[idx] = old - 1e-6
+            lm = loss(*args)
+            x[idx] = old
+            fd[idx] = (lp - lm) / 2e-6
+        assert np.linalg.norm(got - fd) / np.linalg.norm(fd) < 1e-6
