@@ -19,6 +19,7 @@ __all__ = [
     "SdpaError", "Strides", "Problem", "lib", "LIB_PATH", "dtype_code", "make_problem",
     "sdpa_workspace_size", "sdpa_fwd", "sdpa_bwd", "sdpa_last_error_string", "causal_code",
     "sdpa_device_error", "sdpa_version", "sdpa_bwd_noalloc", "NOALLOC_SCRATCH_BYTES", "STATUS",
+    "sdpa_dropout_mask_size", "sdpa_dropout_mask",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libsdpa_gb300.so")
@@ -55,6 +56,8 @@ class Problem(ctypes.Structure):
         ("descale_v", ctypes.c_void_p),
         ("seq_lens_q", ctypes.c_void_p), ("seq_lens_kv", ctypes.c_void_p),
         ("alibi", ctypes.c_int32), ("alibi_slopes", ctypes.c_void_p),
+        ("dropout_p", ctypes.c_float), ("dropout_mask", ctypes.c_void_p),
+        ("dropout_mask_t", ctypes.c_void_p),
     ]
 
 
@@ -84,6 +87,10 @@ def _load():
     L.sdpa_bwd.restype = ctypes.c_int
     L.sdpa_bwd_noalloc.argtypes = [P, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP]
     L.sdpa_bwd_noalloc.restype = ctypes.c_int
+    L.sdpa_dropout_mask_size.argtypes = [P, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]
+    L.sdpa_dropout_mask_size.restype = ctypes.c_int
+    L.sdpa_dropout_mask.argtypes = [P, ctypes.c_uint64, ctypes.c_uint64, VP, VP, VP]
+    L.sdpa_dropout_mask.restype = ctypes.c_int
     L.sdpa_last_error_string.argtypes = []
     L.sdpa_last_error_string.restype = ctypes.c_char_p
     L.sdpa_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
@@ -134,7 +141,8 @@ def _ptr(t) -> Optional[int]:
 def make_problem(q, k, v, o=None, *, attn_scale: Optional[float] = None, causal=False,
                  dout=None, dq=None, dk=None, dv=None, descale_q=None, descale_k=None,
                  descale_v=None, seq_lens_q=None, seq_lens_kv=None, alibi=False,
-                 alibi_slopes=None) -> Problem:
+                 alibi_slopes=None, dropout_p: float = 0.0, dropout_mask=None,
+                 dropout_mask_t=None) -> Problem:
     """Fills an sdpa_problem_t from logical [b, h, s, d] torch tensors (no copies).
 
     ALiBi is on when ``alibi`` is true or ``alibi_slopes`` (fp32 CUDA tensor of h_q slopes)
@@ -153,6 +161,8 @@ def make_problem(q, k, v, o=None, *, attn_scale: Optional[float] = None, causal=
     p.seq_lens_q, p.seq_lens_kv = _ptr(seq_lens_q), _ptr(seq_lens_kv)
     p.alibi = 1 if (alibi or alibi_slopes is not None) else 0
     p.alibi_slopes = _ptr(alibi_slopes)
+    p.dropout_p = float(dropout_p)
+    p.dropout_mask, p.dropout_mask_t = _ptr(dropout_mask), _ptr(dropout_mask_t)
     return p
 
 
@@ -171,14 +181,17 @@ def sdpa_workspace_size(problem: Problem, is_backward: bool) -> int:
 
 def sdpa_fwd(q, k, v, o, lse=None, *, attn_scale: Optional[float] = None, causal=False,
              descale_q=None, descale_k=None, descale_v=None, workspace=None, stream=None,
-             seq_lens_q=None, seq_lens_kv=None, alibi=False, alibi_slopes=None) -> None:
+             seq_lens_q=None, seq_lens_kv=None, alibi=False, alibi_slopes=None,
+             dropout_p: float = 0.0, dropout_mask=None) -> None:
     """O (and LSE when ``lse`` is given: fp32 [b, h_q, s_q] contiguous) from Q, K, V.
 
     seq_lens_q / seq_lens_kv: optional int32 CUDA tensors of b valid lengths.
-    alibi / alibi_slopes: the linear position bias (see :func:`make_problem`)."""
+    alibi / alibi_slopes: the linear position bias (see :func:`make_problem`).
+    dropout_p / dropout_mask: dropout with the row-major keep bits of :func:`sdpa_dropout_mask`."""
     p = make_problem(q, k, v, o, attn_scale=attn_scale, causal=causal, descale_q=descale_q,
                      descale_k=descale_k, descale_v=descale_v, seq_lens_q=seq_lens_q,
-                     seq_lens_kv=seq_lens_kv, alibi=alibi, alibi_slopes=alibi_slopes)
+                     seq_lens_kv=seq_lens_kv, alibi=alibi, alibi_slopes=alibi_slopes,
+                     dropout_p=dropout_p, dropout_mask=dropout_mask)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.sdpa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
                         _ptr(workspace), ws_bytes, _stream(stream)))
@@ -186,15 +199,40 @@ def sdpa_fwd(q, k, v, o, lse=None, *, attn_scale: Optional[float] = None, causal
 
 def sdpa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, *, attn_scale: Optional[float] = None,
              causal=False, stream=None, seq_lens_q=None, seq_lens_kv=None, alibi=False,
-             alibi_slopes=None) -> None:
-    """dQ, dK, dV (overwritten) for the incoming gradient ``dout``; the masking, lengths and
-    ALiBi options must be those of the forward call that produced ``o`` and ``lse``."""
+             alibi_slopes=None, dropout_p: float = 0.0, dropout_mask_t=None) -> None:
+    """dQ, dK, dV (overwritten) for the incoming gradient ``dout``; the masking, lengths,
+    ALiBi and dropout options must be those of the forward call that produced ``o`` and
+    ``lse`` (dropout_mask_t: the transposed keep bits of the same draw)."""
     p = make_problem(q, k, v, o, attn_scale=attn_scale, causal=causal, dout=dout, dq=dq, dk=dk,
                      dv=dv, seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv, alibi=alibi,
-                     alibi_slopes=alibi_slopes)
+                     alibi_slopes=alibi_slopes, dropout_p=dropout_p, dropout_mask_t=dropout_mask_t)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.sdpa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
                         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def _mask_problem(b: int, h_q: int, s_q: int, s_kv: int, dropout_p: float) -> Problem:
+    p = Problem()
+    p.b, p.h_q, p.s_q, p.s_kv = b, h_q, s_q, s_kv
+    p.dropout_p = float(dropout_p)
+    return p
+
+
+def sdpa_dropout_mask_size(b: int, h_q: int, s_q: int, s_kv: int):
+    """(bytes of the row-major keep bits, bytes of the transposed ones)."""
+    n, n_t = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(lib.sdpa_dropout_mask_size(ctypes.byref(_mask_problem(b, h_q, s_q, s_kv, 0.0)),
+                                      ctypes.byref(n), ctypes.byref(n_t)))
+    return n.value, n_t.value
+
+
+def sdpa_dropout_mask(b: int, h_q: int, s_q: int, s_kv: int, dropout_p: float, seed: int,
+                      offset: int, mask=None, mask_t=None, stream=None) -> None:
+    """Draws the Philox4x64-10 keep bits into ``mask`` (row-major, for sdpa_fwd) and/or
+    ``mask_t`` (transposed, for sdpa_bwd): CUDA tensors of sdpa_dropout_mask_size bytes."""
+    p = _mask_problem(b, h_q, s_q, s_kv, dropout_p)
+    _check(lib.sdpa_dropout_mask(ctypes.byref(p), int(seed), int(offset), _ptr(mask), _ptr(mask_t),
+                                 _stream(stream)))
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20  # SDPA_NOALLOC_SCRATCH_BYTES in include/sdpa.h

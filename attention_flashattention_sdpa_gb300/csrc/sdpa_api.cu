@@ -166,6 +166,10 @@ sdpa_status_t check_problem(const sdpa_problem_t* p, bool backward) {
     return fail(SDPA_ERR_LAYOUT, "alibi_slopes must be 4-byte aligned");
   if (p->alibi && p->in_dtype == SDPA_DTYPE_E4M3)
     return fail(SDPA_ERR_UNSUPPORTED, "ALiBi takes F16 or BF16 inputs, not E4M3");
+  if (!(p->dropout_p >= 0.f && p->dropout_p < 1.f))
+    return fail(SDPA_ERR_INVALID_ARG, "dropout_p must be in [0, 1), got %g", p->dropout_p);
+  if (p->dropout_p > 0.f && p->in_dtype == SDPA_DTYPE_E4M3)
+    return fail(SDPA_ERR_UNSUPPORTED, "dropout takes F16 or BF16 inputs, not E4M3");
   if (p->in_dtype == SDPA_DTYPE_E4M3) {
     if (backward)
       return fail(SDPA_ERR_UNSUPPORTED, "the backward pass takes F16 or BF16 inputs, not E4M3");
@@ -203,6 +207,22 @@ sdpa_status_t finish_launch(cudaError_t e, cudaStream_t stream, const char* what
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+int words_of(int s) { return (s + 127) / 128 * 4; }   // keep-mask words per row or key
+
+// Dropout mask pointer of a forward or backward call (checked only when dropout is on).
+sdpa_status_t check_drop_mask(const sdpa_problem_t* p, const uint32_t* mask, const char* name) {
+  if (p->dropout_p == 0.f) return SDPA_OK;
+  if (mask == nullptr)
+    return fail(SDPA_ERR_INVALID_ARG, "dropout_p > 0 needs %s (from sdpa_dropout_mask)", name);
+  if (reinterpret_cast<uintptr_t>(mask) % 16)
+    return fail(SDPA_ERR_LAYOUT, "%s must be 16-byte aligned", name);
+  return SDPA_OK;
+}
+
+float drop_scale_of(const sdpa_problem_t* p) {
+  return static_cast<float>(1.0 / (1.0 - static_cast<double>(p->dropout_p)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -228,6 +248,7 @@ sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const void* k, co
   if ((st = check_view("o", o, p->o, p->b, p->h_q, p->s_q, p->d, 2)) != SDPA_OK) return st;
   if (lse != nullptr && reinterpret_cast<uintptr_t>(lse) % 4 != 0)
     return fail(SDPA_ERR_LAYOUT, "lse must be 4-byte aligned");
+  if ((st = check_drop_mask(p, p->dropout_mask, "dropout_mask")) != SDPA_OK) return st;
 
   sdpa::FwdParams prm;
   memset(&prm, 0, sizeof(prm));
@@ -251,6 +272,9 @@ sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const void* k, co
   prm.seq_lens_kv = p->seq_lens_kv;
   prm.alibi = p->alibi;
   prm.alibi_slopes = p->alibi ? p->alibi_slopes : nullptr;
+  prm.drop_scale = drop_scale_of(p);
+  prm.drop_rows = p->dropout_p > 0.f ? p->dropout_mask : nullptr;
+  prm.drop_kv_words = words_of(p->s_kv);
   const int rows_per_cta = 128 * sdpa::fwd_q_tiles(p->d, p->in_dtype);
   prm.num_m_blocks = (p->s_q + rows_per_cta - 1) / rows_per_cta;
   prm.scale_log2 = scale_log2_of(p->attn_scale);
@@ -282,6 +306,7 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
   if ((st = check_view("dv", dv, p->dv, p->b, p->h_kv, p->s_kv, p->d, es)) != SDPA_OK) return st;
   if (lse == nullptr) return fail(SDPA_ERR_INVALID_ARG, "lse: null pointer (the backward pass needs the forward statistics)");
   if (reinterpret_cast<uintptr_t>(lse) % 4 != 0) return fail(SDPA_ERR_LAYOUT, "lse must be 4-byte aligned");
+  if ((st = check_drop_mask(p, p->dropout_mask_t, "dropout_mask_t")) != SDPA_OK) return st;
   const size_t need = sdpa::bwd_workspace_bytes(p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given%s", need,
@@ -344,6 +369,9 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
   prm.seq_lens_kv = p->seq_lens_kv;
   prm.alibi = p->alibi;
   prm.alibi_slopes = p->alibi ? p->alibi_slopes : nullptr;
+  prm.drop_scale = drop_scale_of(p);
+  prm.drop_cols = p->dropout_p > 0.f ? p->dropout_mask_t : nullptr;
+  prm.drop_q_words = words_of(p->s_q);
   prm.s_q_pad = s_q_pad;
   prm.scale = p->attn_scale;
   prm.scale_log2 = p->attn_scale * 1.4426950408889634f;
@@ -416,6 +444,46 @@ sdpa_status_t sdpa_bwd_noalloc(const sdpa_problem_t* p, const void* q, const voi
     scratch = g_noalloc_ptr[dev];
   }
   return sdpa_bwd(p, q, k, v, o, dout, lse, dq, dk, dv, scratch, SDPA_NOALLOC_SCRATCH_BYTES, stream);
+}
+
+sdpa_status_t sdpa_dropout_mask_size(const sdpa_problem_t* p, size_t* bytes, size_t* bytes_t) {
+  if (p == nullptr || bytes == nullptr || bytes_t == nullptr)
+    return fail(SDPA_ERR_INVALID_ARG, "problem, bytes and bytes_t must not be NULL");
+  if (p->b < 1 || p->h_q < 1 || p->s_q < 1 || p->s_kv < 1)
+    return fail(SDPA_ERR_INVALID_ARG, "sizes must be >= 1 (b=%d h_q=%d s_q=%d s_kv=%d)", p->b, p->h_q,
+                p->s_q, p->s_kv);
+  const size_t bh = static_cast<size_t>(p->b) * p->h_q;
+  *bytes = bh * p->s_q * words_of(p->s_kv) * 4;
+  *bytes_t = bh * p->s_kv * words_of(p->s_q) * 4;
+  return ok();
+}
+
+sdpa_status_t sdpa_dropout_mask(const sdpa_problem_t* p, uint64_t seed, uint64_t offset, uint32_t* mask,
+                                uint32_t* mask_t, void* stream_) {
+  size_t n, n_t;
+  sdpa_status_t st = sdpa_dropout_mask_size(p, &n, &n_t);
+  if (st != SDPA_OK) return st;
+  if (!(p->dropout_p >= 0.f && p->dropout_p < 1.f))
+    return fail(SDPA_ERR_INVALID_ARG, "dropout_p must be in [0, 1), got %g", p->dropout_p);
+  if ((mask && reinterpret_cast<uintptr_t>(mask) % 16) || (mask_t && reinterpret_cast<uintptr_t>(mask_t) % 16))
+    return fail(SDPA_ERR_LAYOUT, "mask and mask_t must be 16-byte aligned");
+  if (static_cast<int64_t>(p->b) * p->h_q > 65535)
+    return fail(SDPA_ERR_UNSUPPORTED, "b*h_q = %lld exceeds 65535", static_cast<long long>(p->b) * p->h_q);
+  if (mask == nullptr && mask_t == nullptr) return ok();
+  sdpa::DropoutParams prm;
+  prm.rows = mask;
+  prm.cols = mask_t;
+  prm.seed = seed;
+  prm.offset = offset;
+  const double t = std::floor(static_cast<double>(p->dropout_p) * 65536.0 + 0.5);
+  prm.threshold = static_cast<uint32_t>(t > 65536.0 ? 65536.0 : t);
+  prm.s_q = p->s_q;
+  prm.s_kv = p->s_kv;
+  prm.kv_words = words_of(p->s_kv);
+  prm.q_words = words_of(p->s_q);
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  cudaError_t e = sdpa::launch_dropout_mask(prm, p->b * p->h_q, stream);
+  return finish_launch(e, stream, "sdpa_dropout_mask");
 }
 
 const char* sdpa_last_error_string(void) { return g_last_error.c_str(); }

@@ -240,9 +240,11 @@ __device__ __forceinline__ int first_q_block(const BwdParams& p, const Lens& L, 
   return r0 <= 0 ? 0 : r0 / bq;
 }
 
-template <int D, int DT, bool ALIBI>
+template <int D, int DT, int FEAT>
 __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant__ BwdParams p) {
   using C = BwdCfg<D>;
+  constexpr bool ALIBI = (FEAT & kFeatAlibi) != 0;
+  constexpr bool DROP = (FEAT & kFeatDropout) != 0;
   extern __shared__ __align__(1024) uint8_t smem[];
   BwdBarriers& bars = *reinterpret_cast<BwdBarriers*>(smem + C::OFF_BAR);
   uint8_t* sK = smem + C::OFF_K;
@@ -468,6 +470,12 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       const uint32_t X = tmem + lane_off + C::R_COL + b * 128;
       const uint32_t Y = tmem + lane_off + C::R_COL + (b ^ 1) * 128;
       const int q0 = iter_qblk(n) * kBlockM + 64 * h;     // first query column of this half
+      // Dropout: keep bits of this key row for the 64 query columns (transposed mask).
+      uint2 keep = make_uint2(0u, 0u);
+      if (DROP && kv_row < p.s_kv)
+        keep = __ldg(reinterpret_cast<const uint2*>(
+            p.drop_cols + ((static_cast<int64_t>(bi) * p.h_q + iter_head(n)) * p.s_kv + kv_row) * p.drop_q_words +
+            q0 / 32));
       const float* nlse2 = sVec + (b * 2 + 0) * 128 + 64 * h;    // -LSE·log2 e per column
       const float* ndelta = sVec + (b * 2 + 1) * 128 + 64 * h;   // -Delta per column
       // Pᵀ = exp2(Sᵀ·scale·log2e − LSE·log2e), masked where key > query
@@ -484,7 +492,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
                              (j * kBlockN + kBlockN > L.len_kv);
       int lim = p.causal ? kv_row - q0 - L.off : -(1 << 30);
       if (kv_row >= L.len_kv) lim = 1 << 30;
-      uint32_t pk[32];
+      uint32_t pk[32], pm[DROP ? 32 : 1];
       const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
       // ALiBi: the key-row part of the bias (the column part is in the -LSE vector).
       const float kr = ALIBI ? alibi_slope_log2(p, iter_head(n)) *
@@ -504,8 +512,17 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
           if (c + 1 < lim) p1 = 0.f;
         }
         pk[c / 2] = pack2(p0, p1, DT);
+        if constexpr (DROP) {
+          // dV takes the kept P only; dS below takes every P.
+          const uint32_t w = (c < 32) ? keep.x : keep.y;
+          pm[c / 2] = pack2((w >> (c % 32)) & 1u ? p0 : 0.f, (w >> (c % 32)) & 2u ? p1 : 0.f, DT);
+        }
       }
-      tmem_st32(X + 64 * h, pk);
+      if constexpr (DROP) {
+        tmem_st32(X + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pm[0]));
+      } else {
+        tmem_st32(X + 64 * h, pk);
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.p_full[b]);
@@ -515,18 +532,43 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       ++it;
       if (!mbar_wait_warp(&bars.dp_full[b], par, abort_flag)) { ok = false; break; }
       tc_fence_after();
-      tmem_ld32(Y + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-      tmem_ld32(Y + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&bars.dp_consumed[b]);   // region Y may now take the next step's Sᵀ
       uint32_t ds[32];
+      if constexpr (DROP) {
+        // dP = keep / (1 - p) * dO·Vᵀ.  Half the columns at a time (fewer live registers):
+        // the second half is read before region Y is released.
+        const float2 rk2 = make_float2(p.drop_scale, p.drop_scale);
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        const float2 nd = *reinterpret_cast<const float2*>(ndelta + c);
-        const float2 dd = mul2(unpack2(pk[c / 2], DT),
-                               add2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), nd));
-        ds[c / 2] = pack2(dd.x, dd.y, DT);
+        for (int half = 0; half < 2; ++half) {
+          tmem_ld32(Y + 64 * h + 32 * half, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+          tmem_ld_wait();
+          if (half == 1) {
+            tc_fence_before();
+            mbar_arrive(&bars.dp_consumed[b]);   // region Y may now take the next step's Sᵀ
+          }
+          const uint32_t w = half == 0 ? keep.x : keep.y;
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const float2 nd = *reinterpret_cast<const float2*>(ndelta + 32 * half + c);
+            float2 dpv = make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+            dpv.x = (w >> c) & 1u ? dpv.x : 0.f;
+            dpv.y = (w >> c) & 2u ? dpv.y : 0.f;
+            const float2 dd = mul2(unpack2(pk[16 * half + c / 2], DT), fma2(dpv, rk2, nd));
+            ds[16 * half + c / 2] = pack2(dd.x, dd.y, DT);
+          }
+        }
+      } else {
+        tmem_ld32(Y + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(Y + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&bars.dp_consumed[b]);   // region Y may now take the next step's Sᵀ
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float2 nd = *reinterpret_cast<const float2*>(ndelta + c);
+          const float2 dd = mul2(unpack2(pk[c / 2], DT),
+                                 add2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), nd));
+          ds[c / 2] = pack2(dd.x, dd.y, DT);
+        }
       }
       // dS in shared memory, one 128-byte swizzled row per key row r, chunk h holding query
       // columns 64h..64h+63: read K-major (rows = keys) as the A operand of dK += dSᵀ·Q and
@@ -549,7 +591,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       // Split group: add this CTA's share into the fp32 accumulator (once per CTA).
       tc_fence_after();
       const uint32_t acc = tmem + lane_off + (h == 0 ? C::DV_COL : C::DK_COL);
-      const float mul = (h == 0) ? 1.f : p.scale;
+      const float mul = (h == 0) ? p.drop_scale : p.scale;
       float* dst = (h == 0 ? p.dv_acc : p.dk_acc) +
                    ((static_cast<int64_t>(bi) * p.h_kv + hk) * p.s_kv_pad + kv_row) * D;
 #pragma unroll 1
@@ -566,7 +608,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     } else if (ok) {
       tc_fence_after();
       const uint32_t acc = tmem + lane_off + (h == 0 ? C::DV_COL : C::DK_COL);
-      const float mul = (h == 0) ? 1.f : p.scale;
+      const float mul = (h == 0) ? p.drop_scale : p.scale;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t v[64];
@@ -703,9 +745,11 @@ struct alignas(8) D256Barriers {
   int abort;
 };
 
-template <int DT, bool ALIBI>
+template <int DT, int FEAT>
 __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant__ BwdParams p) {
   using C = D256;
+  constexpr bool ALIBI = (FEAT & kFeatAlibi) != 0;
+  constexpr bool DROP = (FEAT & kFeatDropout) != 0;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) atomicOr(&g_device_error, kErrSmemAlign);
@@ -823,6 +867,12 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
       const float kr = ALIBI ? alibi_slope_log2(p, hq) *
                                    static_cast<float>(kv_row - (q0 / kBlockM) * kBlockM - L.off) : 0.f;
       const float2 kr2 = make_float2(kr, kr);
+      // Dropout: keep bits of this key row for the 64 query columns (transposed mask).
+      uint2 keep = make_uint2(0u, 0u);
+      if (DROP && kv_row < p.s_kv)
+        keep = __ldg(reinterpret_cast<const uint2*>(
+            p.drop_cols + ((static_cast<int64_t>(bi) * p.h_q + hq) * p.s_kv + kv_row) * p.drop_q_words + q0 / 32));
+      const float2 rk2 = make_float2(p.drop_scale, p.drop_scale);
       uint32_t pk[32], ds[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
@@ -834,10 +884,22 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
           if (c < lim) p0 = 0.f;
           if (c + 1 < lim) p1 = 0.f;
         }
-        pk[c / 2] = pack2(p0, p1, DT);
-        const float2 dd = mul2(make_float2(p0, p1),
-                               add2(make_float2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1])),
-                                    *reinterpret_cast<const float2*>(sVec + 64 + c)));
+        float2 dp = make_float2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]));
+        const float2 nd = *reinterpret_cast<const float2*>(sVec + 64 + c);
+        float2 t;
+        if constexpr (DROP) {
+          // dV takes the kept P only; dS = P * (keep / (1 - p) * dO·Vᵀ - Delta) takes every P.
+          const uint32_t w = (c < 32) ? keep.x : keep.y;
+          const bool k0 = (w >> (c % 32)) & 1u, k1 = (w >> (c % 32)) & 2u;
+          pk[c / 2] = pack2(k0 ? p0 : 0.f, k1 ? p1 : 0.f, DT);
+          dp.x = k0 ? dp.x : 0.f;
+          dp.y = k1 ? dp.y : 0.f;
+          t = fma2(dp, rk2, nd);
+        } else {
+          pk[c / 2] = pack2(p0, p1, DT);
+          t = add2(dp, nd);
+        }
+        const float2 dd = mul2(make_float2(p0, p1), t);
         ds[c / 2] = pack2(dd.x, dd.y, DT);
       }
       tmem_st32(tmem + lane_base + C::COL_S, pk);
@@ -918,8 +980,9 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
           tmem_ld_wait();
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            red_add_v4(dvp + c * 32 + u * 4, __uint_as_float(a[u * 4]), __uint_as_float(a[u * 4 + 1]),
-                       __uint_as_float(a[u * 4 + 2]), __uint_as_float(a[u * 4 + 3]));
+            red_add_v4(dvp + c * 32 + u * 4, __uint_as_float(a[u * 4]) * p.drop_scale,
+                       __uint_as_float(a[u * 4 + 1]) * p.drop_scale, __uint_as_float(a[u * 4 + 2]) * p.drop_scale,
+                       __uint_as_float(a[u * 4 + 3]) * p.drop_scale);
             red_add_v4(dkp + c * 32 + u * 4, __uint_as_float(k2[u * 4]) * p.scale,
                        __uint_as_float(k2[u * 4 + 1]) * p.scale, __uint_as_float(k2[u * 4 + 2]) * p.scale,
                        __uint_as_float(k2[u * 4 + 3]) * p.scale);
@@ -931,7 +994,7 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
       for (int which = 0; which < 2; ++which) {
         uint8_t* stage = which == 0 ? sQ : sdO;
         const uint32_t acc = which == 0 ? acc_v : acc_k;
-        const float mul = which == 0 ? 1.f : p.scale;
+        const float mul = which == 0 ? p.drop_scale : p.scale;
         for (int c = 0; c < 2; ++c) {
           uint32_t v[64];
           if (n_iter > 0) {
@@ -1009,7 +1072,11 @@ cudaError_t launch_d256(const BwdParams& p, cudaStream_t st) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  auto kern = p.alibi ? bwd_d256_kernel<DT, true> : bwd_d256_kernel<DT, false>;
+  const int feat = (p.alibi ? kFeatAlibi : 0) | (p.drop_cols ? kFeatDropout : 0);
+  auto kern = bwd_d256_kernel<DT, 0>;
+  if (feat == kFeatAlibi) kern = bwd_d256_kernel<DT, kFeatAlibi>;
+  if (feat == kFeatDropout) kern = bwd_d256_kernel<DT, kFeatDropout>;
+  if (feat == (kFeatAlibi | kFeatDropout)) kern = bwd_d256_kernel<DT, kFeatAlibi | kFeatDropout>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, D256::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const unsigned grid = 2u * p.b * p.h_kv * p.kv_split * ((p.s_kv + kBlockN - 1) / kBlockN);
@@ -1040,7 +1107,11 @@ cudaError_t launch_t(const BwdParams& p, cudaStream_t st) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  auto kern = p.alibi ? bwd_main_kernel<D, DT, true> : bwd_main_kernel<D, DT, false>;
+  const int feat = (p.alibi ? kFeatAlibi : 0) | (p.drop_cols ? kFeatDropout : 0);
+  auto kern = bwd_main_kernel<D, DT, 0>;
+  if (feat == kFeatAlibi) kern = bwd_main_kernel<D, DT, kFeatAlibi>;
+  if (feat == kFeatDropout) kern = bwd_main_kernel<D, DT, kFeatDropout>;
+  if (feat == (kFeatAlibi | kFeatDropout)) kern = bwd_main_kernel<D, DT, kFeatAlibi | kFeatDropout>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const unsigned gmain = static_cast<unsigned>(p.b) * p.h_kv * p.kv_split * ((p.s_kv + kBlockN - 1) / kBlockN);

@@ -100,10 +100,12 @@ __device__ __forceinline__ int kv_blocks_for(const FwdParams& p, const Lens& L, 
   return lim < 0 ? 0 : lim / kBlockN + 1;
 }
 
-template <int D, int DT, int OUT_DT, bool ALIBI>
+template <int D, int DT, int OUT_DT, int FEAT>
 __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
     sdpa_fwd_kernel(const __grid_constant__ FwdParams p) {
   using C = FwdCfg<D, DT>;
+  constexpr bool ALIBI = (FEAT & kFeatAlibi) != 0;
+  constexpr bool DROP = (FEAT & kFeatDropout) != 0;
   constexpr int NQT = C::NQT;
   constexpr int NS = C::NS;
   constexpr bool FP8 = (DT == kE4M3);
@@ -331,12 +333,23 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       c_scale *= __ldg(p.descale_q) * __ldg(p.descale_k);
       v_scale = __ldg(p.descale_v);
     }
+    // Dropout: this row's keep bits (4 words per key block); kept P are scaled at the end.
+    const uint4* drop_row = nullptr;
+    if (DROP) {
+      v_scale *= p.drop_scale;
+      if (q_row < p.s_q)
+        drop_row = reinterpret_cast<const uint4*>(
+            p.drop_rows + (static_cast<int64_t>(bi) * p.h_q * p.s_q + static_cast<int64_t>(hq) * p.s_q + q_row) *
+                              p.drop_kv_words);
+    }
     // Highest key index this row may see (-1: none, e.g. a padded row).
     int row_limit = L.len_kv - 1;
     if (p.causal) row_limit = min(row_limit, q_row + L.off);
     if (q_row >= L.len_q) row_limit = -1;
-    // ALiBi slope of this head in the log2 domain.
-    const float sl2 = ALIBI ? alibi_slope_log2(p, hq) : 0.f;
+    // ALiBi slope of this head in the log2 domain, kept away from 0 so that the scores can be
+    // carried divided by it (a slope below 1e-20 adds at most ~1e-15 to any score).
+    const float sl2 = ALIBI ? fmaxf(alibi_slope_log2(p, hq), 1e-20f) : 0.f;
+    const float u_scale = ALIBI ? c_scale / sl2 : 0.f;
 
     float m_ref = -INFINITY;   // running max (log2 domain, scale folded in)
     float l = 0.f;             // running sum of exp2(x - m_ref + P_OFFSET)
@@ -345,6 +358,8 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
     for (int j = 0; j < n_blocks; ++j) {
       const int slot = (NQT == 2) ? t : (j & 1);
       const uint32_t ph = (NQT == 2) ? (j & 1) : ((j >> 1) & 1);
+      uint4 keep = make_uint4(0u, 0u, 0u, 0u);
+      if (DROP && drop_row != nullptr) keep = __ldg(drop_row + kv_block(j));
       if (!mbar_wait_warp(&bars.s_full[slot], ph, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint32_t s_addr = tmem + lane_off + slot * 128;
@@ -366,16 +381,13 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
           if (c > lim) sv[c] = __float_as_uint(-INFINITY);
       }
       if constexpr (ALIBI) {
-        // ALiBi splits slope * (key - row - off) into a column part slope * c, added here
-        // before the row max, and a row part slope * (kv0 - row - off) folded into the max.
-        const float2 cs2 = make_float2(c_scale, c_scale);
+        // ALiBi splits slope * (key - row - off) into a column part slope * c and a row part
+        // slope * (kv0 - row - off) folded into the max.  The scores are carried divided by
+        // the slope, u = s * scale / slope + c (c an immediate: nothing to keep in registers),
+        // and scaled back by the slope in the max and the exponent.
 #pragma unroll
-        for (int c = 0; c < kBlockN; c += 2) {
-          const float2 k2 = make_float2(sl2 * static_cast<float>(c), sl2 * static_cast<float>(c + 1));
-          const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), cs2, k2);
-          sv[c] = __float_as_uint(x.x);
-          sv[c + 1] = __float_as_uint(x.y);
-        }
+        for (int c = 0; c < kBlockN; ++c)
+          sv[c] = __float_as_uint(fmaf(__uint_as_float(sv[c]), u_scale, static_cast<float>(c)));
       }
       // Row max over four independent chains of three-input max.
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
@@ -389,7 +401,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       const float mx = max3(mx0, mx1, fmaxf(mx2, mx3));
       // ALiBi row part of this key block: slope * (kv0 - q_row - off).
       const float row_bias = ALIBI ? sl2 * static_cast<float>(kv0 - q_row - L.off) : 0.f;
-      const float m_cand = ALIBI ? mx + row_bias : mx * c_scale;
+      const float m_cand = ALIBI ? sl2 * mx + row_bias : mx * c_scale;
       float alpha = 1.f;
       if (m_cand > m_ref + C::THRESH) {
         alpha = ex2(m_ref - m_cand);
@@ -399,7 +411,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       const float neg_m = (m_ref == -INFINITY) ? 0.f : C::P_OFFSET - m_ref;
 
       // x = s * scale - m in pairs; P = 2^x; row sums in pairs.
-      const float cs = ALIBI ? 1.f : c_scale;   // with ALiBi the scores are already scaled
+      const float cs = ALIBI ? sl2 : c_scale;   // with ALiBi the scores are carried as u
       const float nm = ALIBI ? neg_m + row_bias : neg_m;
       const float2 cs2 = make_float2(cs, cs);
       const float2 nm2 = make_float2(nm, nm);
@@ -409,10 +421,19 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       for (int c = 0; c < kBlockN; c += 4) {
         const float2 x01 = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), cs2, nm2);
         const float2 x23 = fma2(make_float2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), cs2, nm2);
-        const float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
-        const float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
+        float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
+        float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
         acc0 = add2(acc0, p01);
         acc1 = add2(acc1, p23);
+        if constexpr (DROP) {
+          // Row sums take every P; P·V only the kept ones.
+          const uint32_t w = (c < 32) ? keep.x : (c < 64) ? keep.y : (c < 96) ? keep.z : keep.w;
+          const uint32_t b4 = w >> (c % 32);
+          p01.x = (b4 & 1u) ? p01.x : 0.f;
+          p01.y = (b4 & 2u) ? p01.y : 0.f;
+          p23.x = (b4 & 4u) ? p23.x : 0.f;
+          p23.y = (b4 & 8u) ? p23.y : 0.f;
+        }
         if (FP8) {
           pk[c / 4] = pack4_e4m3(p01.x, p01.y, p23.x, p23.y);
         } else {
@@ -508,9 +529,12 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
 template <int D, int DT, int OUT_DT>
 cudaError_t launch_t(const FwdParams& p, cudaStream_t st) {
   using C = FwdCfg<D, DT>;
-  auto kern = sdpa_fwd_kernel<D, DT, OUT_DT, false>;
+  auto kern = sdpa_fwd_kernel<D, DT, OUT_DT, 0>;
   if constexpr (DT != kE4M3) {
-    if (p.alibi) kern = sdpa_fwd_kernel<D, DT, OUT_DT, true>;
+    const int feat = (p.alibi ? kFeatAlibi : 0) | (p.drop_rows ? kFeatDropout : 0);
+    if (feat == kFeatAlibi) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatAlibi>;
+    if (feat == kFeatDropout) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatDropout>;
+    if (feat == (kFeatAlibi | kFeatDropout)) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatAlibi | kFeatDropout>;
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);

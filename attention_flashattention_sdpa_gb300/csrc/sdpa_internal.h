@@ -31,6 +31,9 @@ struct FwdParams {
   int negate_scores;          // attn_scale < 0: the QK^T MMA negates its A operand
   int alibi;                  // add slope_hq * (j - i - off) to the scaled scores
   const float* alibi_slopes;  // [h_q] fp32, or nullptr for the geometric default
+  const uint32_t* drop_rows;  // dropout keep bits [b*h_q][s_q][drop_kv_words], or nullptr
+  int drop_kv_words;          // 32-bit words per row: ceil(s_kv / 128) * 4
+  float drop_scale;           // 1 / (1 - p), or 1 without dropout
 };
 
 // Number of Q tiles (of 128 rows) one forward CTA processes.
@@ -76,7 +79,22 @@ struct BwdParams {
   int64_t dv_sb, dv_sh, dv_ss;
   int alibi;                    // add slope_hq * (j - i - off) to the scaled scores
   const float* alibi_slopes;    // [h_q] fp32, or nullptr for the geometric default
+  const uint32_t* drop_cols;    // dropout keep bits, transposed: [b*h_q][s_kv][drop_q_words]
+  int drop_q_words;             // 32-bit words per key row: ceil(s_q / 128) * 4
+  float drop_scale;             // 1 / (1 - p), or 1 without dropout
 };
+
+// Dropout keep mask (see sdpa_dropout.cu for the definition).
+struct DropoutParams {
+  uint32_t* rows;               // [b*h_q][s_q][kv_words] or nullptr
+  uint32_t* cols;               // [b*h_q][s_kv][q_words] or nullptr
+  uint64_t seed, offset;
+  uint32_t threshold;           // keep iff the 16-bit draw >= threshold (<= 65536)
+  int s_q, s_kv;
+  int kv_words, q_words;        // ceil(s_kv / 128) * 4, ceil(s_q / 128) * 4
+};
+
+cudaError_t launch_dropout_mask(const DropoutParams& p, int bh, cudaStream_t st);
 
 // How many CTAs share one (batch, KV head, KV block) in the backward pass.  A fixed policy
 // of the shape alone (no device query), so workspace sizing and launch always agree.
@@ -85,6 +103,10 @@ int bwd_kv_split(int b, int h_q, int h_kv, int s_kv);
 size_t bwd_workspace_bytes(int b, int h_q, int h_kv, int s_q, int s_kv, int d);
 cudaError_t launch_bwd(const BwdParams& p, int dtype, cudaStream_t st);
 uint32_t bwd_take_device_error();
+
+// Kernel feature bits (compile-time variants of the forward and backward kernels).
+constexpr int kFeatAlibi = 1;
+constexpr int kFeatDropout = 2;
 
 }  // namespace sdpa
 
@@ -106,10 +128,10 @@ __device__ __forceinline__ Lens batch_lens(const P& p, int bi) {
 }
 
 // ALiBi slope of query head hq, in the log2 domain the kernels exponentiate in: the
-// caller's slope, or the geometric sequence 2^(-8 (hq + 1) / h_q).
+// caller's slope (a negative one counts as 0), or the geometric sequence 2^(-8 (hq + 1) / h_q).
 template <typename P>
 __device__ __forceinline__ float alibi_slope_log2(const P& p, int hq) {
-  const float m = p.alibi_slopes ? __ldg(p.alibi_slopes + hq)
+  const float m = p.alibi_slopes ? fmaxf(__ldg(p.alibi_slopes + hq), 0.f)
                                  : exp2f(-8.f * static_cast<float>(hq + 1) / static_cast<float>(p.h_q));
   return m * 1.4426950408889634f;
 }

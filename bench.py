@@ -488,9 +488,23 @@ def sweep_one(w, peaks, args):
                   descale_v=torch.tensor([x.descale_v], device="cuda"))
     o = torch.empty_strided(q.shape, q.stride(), dtype=odt, device="cuda")
     lse = torch.empty(w.b, w.h_q, w.s_q, dtype=torch.float32, device="cuda") if (w.stats or w.backward) else None
+    st = torch.cuda.current_stream()
+    mask = mask_t = None
+    mask_ms = None
+    if w.dropout > 0:
+        n, n_t = sdpa.sdpa_dropout_mask_size(w.b, w.h_q, w.s_q, w.s_kv)
+        mask = torch.empty(n // 4, dtype=torch.int32, device="cuda")
+        mask_t = torch.empty(n_t // 4, dtype=torch.int32, device="cuda")
+        gen = lambda: sdpa.sdpa_dropout_mask(w.b, w.h_q, w.s_q, w.s_kv, w.dropout, 1234, 0, mask, mask_t)
+        for _ in range(3):
+            gen()
+        a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st); gen(); b_.record(st)
+        torch.cuda.synchronize()
+        mask_ms = a.elapsed_time(b_)
+        kw["dropout_p"], kw["dropout_mask"] = w.dropout, mask
     fwd = lambda: sdpa.sdpa_fwd(q, k, v, o, lse, attn_scale=w.scale, causal=w.causal, alibi=w.alibi,
                                 **kw)
-    st = torch.cuda.current_stream()
     reps = max(5, min(200, int(2e13 / max(w.fwd_flops(), 1))))
     for _ in range(3):
         fwd()
@@ -504,6 +518,8 @@ def sweep_one(w, peaks, args):
     fwd_ms = statistics.median(a.elapsed_time(b) for a, b in ts)
     peak = peaks["bf16_tflops"]
     line = {"workload": w.name, "fwd_ms": fwd_ms, "fwd_tflops": w.fwd_flops() / fwd_ms / 1e9}
+    if mask_ms is not None:
+        line["dropout_mask_ms"] = mask_ms
     es = 1 if w.dtype == "e4m3" else 2
     io_bytes = (q.numel() + k.numel() + v.numel()) * es + o.numel() * o.element_size() + \
         (lse.numel() * 4 if lse is not None else 0)
@@ -517,8 +533,9 @@ def sweep_one(w, peaks, args):
         dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
         p = sdpa.make_problem(q, k, v, o, attn_scale=w.scale, causal=w.causal, dout=do, dq=dq, dk=dk, dv=dv)
         ws = torch.empty(sdpa.sdpa_workspace_size(p, True), dtype=torch.uint8, device="cuda")
+        dkw = {} if w.dropout == 0 else {"dropout_p": w.dropout, "dropout_mask_t": mask_t}
         bwd = lambda: sdpa.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, attn_scale=w.scale, causal=w.causal,
-                                    alibi=w.alibi)
+                                    alibi=w.alibi, **dkw)
         for _ in range(3):
             bwd()
         torch.cuda.synchronize()

@@ -107,10 +107,20 @@ typedef struct {
    * (i, j) gains m_hq * (j - i - off) before the mask and softmax, off = len_kv - len_q under
    * bottom-right causal alignment and 0 otherwise: zero on the aligned diagonal, a penalty
    * growing linearly with the distance to earlier keys.  m_hq = alibi_slopes[hq] (a DEVICE
-   * pointer to h_q fp32 values), or, when alibi_slopes is NULL, the geometric slopes
-   * 2^(-8 (hq + 1) / h_q).  F16 and BF16 inputs only; the bias has no gradient. */
+   * pointer to h_q finite fp32 values >= 0; a negative slope counts as 0), or, when
+   * alibi_slopes is NULL, the geometric slopes 2^(-8 (hq + 1) / h_q).  F16 and BF16 inputs
+   * only; the bias has no gradient. */
   int32_t alibi;
   const float* alibi_slopes;
+  /* Dropout (the SDPA node's dropout option, cuDNN 9 blog walkthrough; named, not defined by
+   * the pages).  dropout_p in [0, 1); 0 = off.  With p > 0 each softmax probability P_ij is
+   * kept where its keep bit is set and scaled by 1/(1 - p), so O = (P * keep) V / (1 - p); the
+   * LSE is that of the undropped softmax.  The keep bits come from sdpa_dropout_mask: the
+   * forward pass reads `dropout_mask` (row-major), the backward pass `dropout_mask_t` (the
+   * same bits transposed); both DEVICE pointers, 16-byte aligned.  F16/BF16 inputs only. */
+  float dropout_p;
+  const uint32_t* dropout_mask;
+  const uint32_t* dropout_mask_t;
 } sdpa_problem_t;
 
 /*
@@ -180,6 +190,27 @@ SDPA_API sdpa_status_t sdpa_bwd_noalloc(const sdpa_problem_t* p, const void* q, 
                                         const void* v, const void* o, const void* dout,
                                         const float* lse, void* dq, void* dk, void* dv,
                                         void* stream /* cudaStream_t */);
+
+/*
+ * Byte sizes of the two dropout keep-mask arrays of `p` (b, h_q, s_q, s_kv are read):
+ *   mask:   uint32 [b*h_q][s_q][ceil(s_kv/128)*4]   (bit j%32 of word j/32: key j of row i)
+ *   mask_t: uint32 [b*h_q][s_kv][ceil(s_q/128)*4]   (bit i%32 of word i/32: row i of key j)
+ */
+SDPA_API sdpa_status_t sdpa_dropout_mask_size(const sdpa_problem_t* p, size_t* bytes, size_t* bytes_t);
+
+/*
+ * Draws the dropout keep bits for p->dropout_p (in [0, 1)) with the counter-based generator
+ * Philox4x64-10 (Salmon, Moraes, Dror and Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
+ * SC'11).  Element n of the row-major grid [b*h_q][s_q][ceil(s_kv/128)*128] takes 16-bit lane
+ * n%4 of word (n%16)/4 of the block for counter (n/16, offset, 0, 0) and key (seed, 0), and
+ * is kept iff that value is >= round(dropout_p * 65536).  The same (seed, offset) gives the
+ * same bits on every run and device; advance `offset` between steps for fresh draws.
+ *   mask, mask_t: DEVICE arrays of sdpa_dropout_mask_size bytes, 16-byte aligned; either may
+ *   be NULL (not written).  Bits of padded positions (keys >= s_kv in `mask`, rows >= s_q in
+ *   `mask_t`) are written too and are not used.
+ */
+SDPA_API sdpa_status_t sdpa_dropout_mask(const sdpa_problem_t* p, uint64_t seed, uint64_t offset,
+                                         uint32_t* mask, uint32_t* mask_t, void* stream /* cudaStream_t */);
 
 /* Message for the last non-OK status returned on the calling thread ("" if none).  The
  * pointer stays valid until the next library call on this thread [cuDNN 9 blog: errors

@@ -49,6 +49,7 @@ class Workload:
     stats: bool = True    # forward writes the per-row log-sum-exp
     attn_scale: Optional[float] = None
     alibi: bool = False   # ALiBi position bias with the default slopes
+    dropout: float = 0.0  # dropout probability (0 = off)
 
     @property
     def scale(self) -> float:
@@ -96,10 +97,18 @@ def training_alibi(s: int) -> Workload:
                     w.dtype, causal=True, backward=True, alibi=True)
 
 
+def training_dropout(s: int, p: float = 0.1) -> Workload:
+    """The training workload with attention dropout."""
+    w = training(s)
+    return Workload(f"training_dropout{p:g}_bf16_causal_d128_s{s}", w.b, w.h_q, w.h_kv, s, s, w.d,
+                    w.dtype, causal=True, backward=True, dropout=p)
+
+
 def all_workloads():
     out = [tiny(False), tiny(True), gpt2_inference()]
     out += [training(s) for s in TRAINING_SEQ_LENS]
-    out += [fp8_large_head(), grouped(8), grouped(1), grouped(64), training_alibi(8192)]
+    out += [fp8_large_head(), grouped(8), grouped(1), grouped(64), training_alibi(8192),
+            training_dropout(8192)]
     return out
 
 

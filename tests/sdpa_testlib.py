@@ -65,11 +65,27 @@ def _alibi_kwargs(alibi) -> dict:
     return {"alibi_slopes": torch.tensor(list(alibi), dtype=torch.float32, device="cuda")}
 
 
+def dropout_masks(b, h_q, s_q, s_kv, dropout):
+    """(row-major, transposed) keep-bit tensors drawn by the library for dropout = (p, seed,
+    offset), or (None, None)."""
+    if dropout is None:
+        return None, None
+    m = lib()
+    n, n_t = m.sdpa_dropout_mask_size(b, h_q, s_q, s_kv)
+    mask = torch.full((n // 4,), -1, dtype=torch.int32, device="cuda")
+    mask_t = torch.full((n_t // 4,), -1, dtype=torch.int32, device="cuda")
+    m.sdpa_dropout_mask(b, h_q, s_q, s_kv, dropout[0], dropout[1], dropout[2], mask, mask_t)
+    return mask, mask_t
+
+
 def run_fwd(w: Workload, x: Inputs, with_lse: bool = True, out_dtype=torch.bfloat16,
-            causal=None, seq_lens_q=None, seq_lens_kv=None, alibi=None):
+            causal=None, seq_lens_q=None, seq_lens_kv=None, alibi=None, dropout=None):
     m = lib()
     causal = w.causal if causal is None else causal
     lens = _alibi_kwargs(alibi)
+    if dropout is not None:
+        lens["dropout_p"] = dropout[0]
+        lens["dropout_mask"] = dropout_masks(w.b, w.h_q, w.s_q, w.s_kv, dropout)[0]
     if seq_lens_q is not None:
         lens["seq_lens_q"] = torch.tensor(seq_lens_q, dtype=torch.int32, device="cuda")
     if seq_lens_kv is not None:
@@ -95,10 +111,13 @@ def run_fwd(w: Workload, x: Inputs, with_lse: bool = True, out_dtype=torch.bfloa
 
 
 def run_bwd(w: Workload, dev_qkv, o, lse, do_cpu: torch.Tensor, causal=None, seq_lens_q=None,
-            seq_lens_kv=None, alibi=None):
+            seq_lens_kv=None, alibi=None, dropout=None):
     m = lib()
     causal = w.causal if causal is None else causal
     lens = _alibi_kwargs(alibi)
+    if dropout is not None:
+        lens["dropout_p"] = dropout[0]
+        lens["dropout_mask_t"] = dropout_masks(w.b, w.h_q, w.s_q, w.s_kv, dropout)[1]
     if seq_lens_q is not None:
         lens["seq_lens_q"] = torch.tensor(seq_lens_q, dtype=torch.int32, device="cuda")
     if seq_lens_kv is not None:

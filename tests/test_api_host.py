@@ -83,6 +83,13 @@ def _bwd(m, p, ws=FAKE, ws_bytes=1 << 40, lse=FAKE, q=FAKE):
     (dict(in_dtype=2, out_dtype=1), 2, "d = 128 or 256"),
     (dict(in_dtype=2, out_dtype=2), 2, "output"),
     (dict(alibi=2), 1, "alibi"),
+    (dict(dropout_p=-0.1), 1, "dropout_p"),
+    (dict(dropout_p=1.0), 1, "dropout_p"),
+    (dict(dropout_p=float("nan")), 1, "dropout_p"),
+    (dict(dropout_p=0.1), 1, "dropout_mask"),
+    (dict(dropout_p=0.1, dropout_mask=FAKE + 8), 3, "dropout_mask"),
+    (dict(dropout_p=0.1, in_dtype=2, out_dtype=1, d=128, descale_q=FAKE, descale_k=FAKE,
+          descale_v=FAKE), 2, "dropout"),
     (dict(alibi=1, alibi_slopes=FAKE + 2), 3, "alibi_slopes"),
     (dict(alibi=1, in_dtype=2, out_dtype=1, d=128, descale_q=FAKE, descale_k=FAKE,
           descale_v=FAKE), 2, "ALiBi"),
@@ -155,3 +162,20 @@ def test_null_problem(m):
     assert m.lib.sdpa_fwd(None, FAKE, FAKE, FAKE, FAKE, None, None, 0, None) == 1
     n = ctypes.c_size_t()
     assert m.lib.sdpa_workspace_size(None, 0, ctypes.byref(n)) == 1
+
+
+def test_dropout_mask_sizes_and_validation(m):
+    assert m.sdpa_dropout_mask_size(2, 3, 200, 300) == (2 * 3 * 200 * 12 * 4, 2 * 3 * 300 * 8 * 4)
+    assert m.sdpa_dropout_mask_size(1, 1, 1, 1) == (16, 16)
+    p = _problem(m, dropout_p=1.5)
+    assert m.lib.sdpa_dropout_mask(ctypes.byref(p), 1, 2, FAKE, FAKE, None) == 1
+    assert "dropout_p" in m.sdpa_last_error_string()
+    p = _problem(m, dropout_p=0.5)
+    assert m.lib.sdpa_dropout_mask(ctypes.byref(p), 1, 2, FAKE + 4, None, None) == 3
+    p = _problem(m, b=300, h_q=300, h_kv=300, dropout_p=0.5)
+    assert m.lib.sdpa_dropout_mask(ctypes.byref(p), 1, 2, FAKE, FAKE, None) == 2
+
+
+def test_backward_dropout_needs_the_transposed_mask(m):
+    p = _problem(m, dropout_p=0.2, dropout_mask=FAKE)
+    assert _bwd(m, p) == 1 and "dropout_mask_t" in m.sdpa_last_error_string()
