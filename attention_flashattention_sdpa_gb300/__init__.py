@@ -211,10 +211,11 @@ def sdpa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, *, attn_scale: Option
                         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
-def _mask_problem(b: int, h_q: int, s_q: int, s_kv: int, dropout_p: float) -> Problem:
+def _mask_problem(b: int, h_q: int, s_q: int, s_kv: int, dropout_p: float, causal=False) -> Problem:
     p = Problem()
     p.b, p.h_q, p.s_q, p.s_kv = b, h_q, s_q, s_kv
     p.dropout_p = float(dropout_p)
+    p.causal = causal_code(causal)
     return p
 
 
@@ -227,10 +228,11 @@ def sdpa_dropout_mask_size(b: int, h_q: int, s_q: int, s_kv: int):
 
 
 def sdpa_dropout_mask(b: int, h_q: int, s_q: int, s_kv: int, dropout_p: float, seed: int,
-                      offset: int, mask=None, mask_t=None, stream=None) -> None:
+                      offset: int, mask=None, mask_t=None, stream=None, causal=False) -> None:
     """Draws the Philox4x64-10 keep bits into ``mask`` (row-major, for sdpa_fwd) and/or
-    ``mask_t`` (transposed, for sdpa_bwd): CUDA tensors of sdpa_dropout_mask_size bytes."""
-    p = _mask_problem(b, h_q, s_q, s_kv, dropout_p)
+    ``mask_t`` (transposed, for sdpa_bwd): CUDA tensors of sdpa_dropout_mask_size bytes.
+    With ``causal`` (no per-batch lengths) tiles above the diagonal are left unwritten."""
+    p = _mask_problem(b, h_q, s_q, s_kv, dropout_p, causal)
     _check(lib.sdpa_dropout_mask(ctypes.byref(p), int(seed), int(offset), _ptr(mask), _ptr(mask_t),
                                  _stream(stream)))
 

@@ -481,6 +481,9 @@ sdpa_status_t sdpa_dropout_mask(const sdpa_problem_t* p, uint64_t seed, uint64_t
   prm.s_kv = p->s_kv;
   prm.kv_words = words_of(p->s_kv);
   prm.q_words = words_of(p->s_q);
+  // Causal without per-batch lengths: tiles wholly above the diagonal are never read.
+  prm.skip_above = (p->causal == 1 || p->causal == 2) && !p->seq_lens_q && !p->seq_lens_kv;
+  prm.diag_off = p->causal == 2 ? p->s_kv - p->s_q : 0;
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   cudaError_t e = sdpa::launch_dropout_mask(prm, p->b * p->h_q, stream);
   return finish_launch(e, stream, "sdpa_dropout_mask");

@@ -63,6 +63,8 @@ __device__ __forceinline__ uint32_t keep16(uint64_t g, const DropoutParams& p) {
 __global__ void __launch_bounds__(128) dropout_mask_kernel(const DropoutParams p) {
   __shared__ uint32_t tile[128][4];   // [key within block][query word]
   const int kb = blockIdx.x, qb = blockIdx.y, bh = blockIdx.z;
+  // Under a causal mask no row of this tile sees any of its keys: nothing reads these bits.
+  if (p.skip_above && kb * 128 > qb * 128 + 127 + p.diag_off) return;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int row = qb * 128 + threadIdx.x;
   const int64_t row_pitch = static_cast<int64_t>(p.kv_words) * 32;    // s_kv rounded up to 128

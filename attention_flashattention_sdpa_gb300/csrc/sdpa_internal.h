@@ -92,6 +92,8 @@ struct DropoutParams {
   uint32_t threshold;           // keep iff the 16-bit draw >= threshold (<= 65536)
   int s_q, s_kv;
   int kv_words, q_words;        // ceil(s_kv / 128) * 4, ceil(s_q / 128) * 4
+  int skip_above;               // skip 128x128 tiles whose keys all lie beyond row + diag_off
+  int diag_off;                 // causal offset (0 top-left, s_kv - s_q bottom-right)
 };
 
 cudaError_t launch_dropout_mask(const DropoutParams& p, int bh, cudaStream_t st);

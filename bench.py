@@ -495,7 +495,8 @@ def sweep_one(w, peaks, args):
         n, n_t = sdpa.sdpa_dropout_mask_size(w.b, w.h_q, w.s_q, w.s_kv)
         mask = torch.empty(n // 4, dtype=torch.int32, device="cuda")
         mask_t = torch.empty(n_t // 4, dtype=torch.int32, device="cuda")
-        gen = lambda: sdpa.sdpa_dropout_mask(w.b, w.h_q, w.s_q, w.s_kv, w.dropout, 1234, 0, mask, mask_t)
+        gen = lambda: sdpa.sdpa_dropout_mask(w.b, w.h_q, w.s_q, w.s_kv, w.dropout, 1234, 0, mask, mask_t,
+                                             causal=w.causal)
         for _ in range(3):
             gen()
         a, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

@@ -207,7 +207,9 @@ SDPA_API sdpa_status_t sdpa_dropout_mask_size(const sdpa_problem_t* p, size_t* b
  * same bits on every run and device; advance `offset` between steps for fresh draws.
  *   mask, mask_t: DEVICE arrays of sdpa_dropout_mask_size bytes, 16-byte aligned; either may
  *   be NULL (not written).  Bits of padded positions (keys >= s_kv in `mask`, rows >= s_q in
- *   `mask_t`) are written too and are not used.
+ *   `mask_t`) are written too and are not used.  When p->causal is 1 or 2 and no seq_lens
+ *   are given, 128x128 tiles that lie wholly above the causal diagonal are not written (the
+ *   attention kernels never use them); pass causal = 0 for the full grid.
  */
 SDPA_API sdpa_status_t sdpa_dropout_mask(const sdpa_problem_t* p, uint64_t seed, uint64_t offset,
                                          uint32_t* mask, uint32_t* mask_t, void* stream /* cudaStream_t */);

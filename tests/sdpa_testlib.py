@@ -65,16 +65,17 @@ def _alibi_kwargs(alibi) -> dict:
     return {"alibi_slopes": torch.tensor(list(alibi), dtype=torch.float32, device="cuda")}
 
 
-def dropout_masks(b, h_q, s_q, s_kv, dropout):
+def dropout_masks(b, h_q, s_q, s_kv, dropout, causal=False):
     """(row-major, transposed) keep-bit tensors drawn by the library for dropout = (p, seed,
-    offset), or (None, None)."""
+    offset), or (None, None); with `causal` the tiles above the diagonal stay unwritten (-1)."""
     if dropout is None:
         return None, None
     m = lib()
     n, n_t = m.sdpa_dropout_mask_size(b, h_q, s_q, s_kv)
     mask = torch.full((n // 4,), -1, dtype=torch.int32, device="cuda")
     mask_t = torch.full((n_t // 4,), -1, dtype=torch.int32, device="cuda")
-    m.sdpa_dropout_mask(b, h_q, s_q, s_kv, dropout[0], dropout[1], dropout[2], mask, mask_t)
+    m.sdpa_dropout_mask(b, h_q, s_q, s_kv, dropout[0], dropout[1], dropout[2], mask, mask_t,
+                        causal=causal)
     return mask, mask_t
 
 
@@ -85,7 +86,9 @@ def run_fwd(w: Workload, x: Inputs, with_lse: bool = True, out_dtype=torch.bfloa
     lens = _alibi_kwargs(alibi)
     if dropout is not None:
         lens["dropout_p"] = dropout[0]
-        lens["dropout_mask"] = dropout_masks(w.b, w.h_q, w.s_q, w.s_kv, dropout)[0]
+        # a causal draw (tiles above the diagonal unwritten) when no lengths are given
+        dc = causal if seq_lens_q is None and seq_lens_kv is None else False
+        lens["dropout_mask"] = dropout_masks(w.b, w.h_q, w.s_q, w.s_kv, dropout, dc)[0]
     if seq_lens_q is not None:
         lens["seq_lens_q"] = torch.tensor(seq_lens_q, dtype=torch.int32, device="cuda")
     if seq_lens_kv is not None:
@@ -117,7 +120,8 @@ def run_bwd(w: Workload, dev_qkv, o, lse, do_cpu: torch.Tensor, causal=None, seq
     lens = _alibi_kwargs(alibi)
     if dropout is not None:
         lens["dropout_p"] = dropout[0]
-        lens["dropout_mask_t"] = dropout_masks(w.b, w.h_q, w.s_q, w.s_kv, dropout)[1]
+        dc = causal if seq_lens_q is None and seq_lens_kv is None else False
+        lens["dropout_mask_t"] = dropout_masks(w.b, w.h_q, w.s_q, w.s_kv, dropout, dc)[1]
     if seq_lens_q is not None:
         lens["seq_lens_q"] = torch.tensor(seq_lens_q, dtype=torch.int32, device="cuda")
     if seq_lens_kv is not None:

@@ -130,3 +130,22 @@ def test_training_shape_sampled_rows():
         col = mtw[bh, js].cpu().numpy().view(np.uint32)
         bits = ((col[:, i // 32] >> np.uint32(i % 32)) & 1).astype(bool)
         assert (bits == keep[r][js]).all()
+
+
+@pytest.mark.parametrize("causal", [True, "bottom_right"])
+def test_causal_draw_writes_every_visible_tile(causal):
+    """A causal draw skips only tiles wholly above the diagonal: every bit a row can see still
+    equals the oracle's, and the skipped tiles keep their previous contents."""
+    b, h, s_q, s_kv = 1, 2, 300, 400
+    mask, mask_t = dropout_masks(b, h, s_q, s_kv, (0.3, 99, 1), causal=causal)
+    torch.cuda.synchronize()
+    keep = oracle.dropout_keep(b, h, s_q, s_kv, _p32(0.3), 99, 1).reshape(b * h, s_q, s_kv)
+    off = s_kv - s_q if causal == "bottom_right" else 0
+    vis = np.arange(s_kv)[None, :] <= np.arange(s_q)[:, None] + off
+    rows = _unpack(mask, b * h * s_q, 16, s_kv).reshape(b * h, s_q, s_kv)
+    cols = _unpack(mask_t, b * h * s_kv, 12, s_q).reshape(b * h, s_kv, s_q)
+    assert (rows[:, vis] == keep[:, vis]).all()
+    assert (cols.transpose(0, 2, 1)[:, vis] == keep[:, vis]).all()
+    # a tile wholly above the diagonal (rows 0-127, keys 256-383 top-left) is untouched (-1)
+    if causal is True:
+        assert rows[:, :128, 256:384].all()
