@@ -68,7 +68,7 @@ __all__ = [
     "philox4x64", "dropout_threshold", "dropout_keep",
     "visible_mask", "kv_head_of", "alibi_default_slopes", "alibi_bias", "head_forward", "forward", "forward_rows",
     "backward", "backward_dq_rows", "backward_kv_rows", "backward_kv_head", "e4m3_decode_table",
-    "decode_e4m3", "to_f64",
+    "decode_e4m3", "e5m2_decode_table", "decode_e5m2", "to_f64",
 ]
 
 
@@ -106,13 +106,46 @@ def decode_e4m3(codes: np.ndarray, descale: float = 1.0) -> np.ndarray:
     return _E4M3[np.asarray(codes, dtype=np.uint8)] * float(descale)
 
 
+def e5m2_decode_table() -> np.ndarray:
+    """The 256 values of OCP FP8 E5M2 (IEEE-like: infinities and NaNs).
+
+    Bit layout: 1 sign bit, 5 exponent bits (bias 15), 2 mantissa bits — the gradient
+    format of the HYBRID recipe [codelab §10: E4M3 forward, E5M2 backward].  Exponent field
+    0 encodes subnormals m/4 * 2**(1-15); field 31 is infinity (m = 0) or NaN; every other
+    pattern is (1 + m/4) * 2**(e-15).
+    """
+    tab = np.empty(256, dtype=np.float64)
+    for code in range(256):
+        sign = -1.0 if code & 0x80 else 1.0
+        e = (code >> 2) & 0x1F
+        m = code & 0x3
+        if e == 0x1F:
+            tab[code] = sign * math.inf if m == 0 else math.nan
+        elif e == 0:
+            tab[code] = sign * (m / 4.0) * 2.0 ** (1 - 15)
+        else:
+            tab[code] = sign * (1.0 + m / 4.0) * 2.0 ** (e - 15)
+    return tab
+
+
+_E5M2 = e5m2_decode_table()
+
+
+def decode_e5m2(codes: np.ndarray, descale: float = 1.0) -> np.ndarray:
+    """Exact fp64 value of E5M2 bytes times a per-tensor descale."""
+    return _E5M2[np.asarray(codes, dtype=np.uint8)] * float(descale)
+
+
 def to_f64(t, descale: float = 1.0) -> np.ndarray:
-    """Exact fp64 copy of a CPU torch tensor (fp16 / bf16 / fp32 / float8_e4m3fn)."""
+    """Exact fp64 copy of a CPU torch tensor (fp16 / bf16 / fp32 / float8_e4m3fn /
+    float8_e5m2)."""
     import torch  # plumbing only: reads the bytes of a tensor
 
     t = t.detach().cpu()
     if t.dtype == torch.float8_e4m3fn:
         return decode_e4m3(t.contiguous().view(torch.uint8).numpy(), descale)
+    if t.dtype == torch.float8_e5m2:
+        return decode_e5m2(t.contiguous().view(torch.uint8).numpy(), descale)
     return t.to(torch.float64).numpy() * float(descale)
 
 

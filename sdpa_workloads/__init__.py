@@ -30,6 +30,7 @@ from typing import Optional
 import torch
 
 E4M3_MAX = 448.0
+E5M2_MAX = 57344.0
 
 
 @dataclasses.dataclass(frozen=True)
@@ -127,6 +128,16 @@ def _draw(g: torch.Generator, n: int) -> torch.Tensor:
     return torch.randn(n, generator=g, dtype=torch.float32)
 
 
+def quantize_e5m2(x: torch.Tensor):
+    """Per-tensor amax quantisation to E5M2, the gradient format (input preparation).
+
+    Returns (bytes-as-float8 tensor with x's shape/strides, descale float)."""
+    amax = float(x.abs().max())
+    scale = E5M2_MAX / amax if amax > 0 else 1.0
+    q8 = (x.float() * scale).clamp_(-E5M2_MAX, E5M2_MAX).to(torch.float8_e5m2)
+    return q8, 1.0 / scale
+
+
 def quantize_e4m3(x: torch.Tensor):
     """Per-tensor amax quantisation to E4M3 (input preparation, not the method).
 
@@ -147,6 +158,7 @@ class Inputs:
     descale_q: float = 1.0
     descale_k: float = 1.0
     descale_v: float = 1.0
+    descale_do: float = 1.0
 
 
 def make_inputs(w: Workload, seed: int = 0, with_do: Optional[bool] = None) -> Inputs:
@@ -162,10 +174,12 @@ def make_inputs(w: Workload, seed: int = 0, with_do: Optional[bool] = None) -> I
         q8, dq_ = quantize_e4m3(qf)
         k8, dk_ = quantize_e4m3(kf)
         v8, dv_ = quantize_e4m3(vf)
+        do8, ddo_ = quantize_e5m2(dof) if dof is not None else (None, 1.0)
         return Inputs(_logical(q8, w.b, w.h_q, w.s_q, w.d, w.layout),
                       _logical(k8, w.b, w.h_kv, w.s_kv, w.d, w.layout),
                       _logical(v8, w.b, w.h_kv, w.s_kv, w.d, w.layout),
-                      None, dq_, dk_, dv_)
+                      _logical(do8, w.b, w.h_q, w.s_q, w.d, w.layout) if do8 is not None else None,
+                      dq_, dk_, dv_, ddo_)
     dt = _TORCH_DT[w.dtype]
     mk = lambda f, h, s: _logical(f.to(dt), w.b, h, s, w.d, w.layout)
     return Inputs(mk(qf, w.h_q, w.s_q), mk(kf, w.h_kv, w.s_kv), mk(vf, w.h_kv, w.s_kv),

@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle
-from sdpa_workloads import Workload, make_inputs, gpt2_inference, quantize_e4m3
+from sdpa_workloads import Workload, make_inputs, gpt2_inference, quantize_e4m3, quantize_e5m2
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 RNG = np.random.default_rng(12345)
@@ -337,6 +337,39 @@ def test_e4m3_quantisation_round_trip_within_half_ulp():
     ulp = 2.0 ** (e - 3)
     assert (np.abs(ys - xs) <= ulp / 2 + 1e-12).all()
     assert np.abs(oracle.to_f64(q8)).max() <= 448.0
+
+
+# ---------------------------------------------------------------------------
+# E5M2 (gradient format)
+# ---------------------------------------------------------------------------
+
+def test_e5m2_table_matches_torch_cast_for_all_codes():
+    tab = oracle.e5m2_decode_table()
+    ref = torch.arange(256, dtype=torch.uint8).view(torch.float8_e5m2).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert list(np.nonzero(nan)[0]) == [0x7D, 0x7E, 0x7F, 0xFD, 0xFE, 0xFF]
+    np.testing.assert_array_equal(np.isnan(tab), nan)
+    np.testing.assert_array_equal(tab[~nan], ref[~nan])
+
+
+def test_e5m2_special_values():
+    tab = oracle.e5m2_decode_table()
+    assert tab[0x7B] == 57344.0 and tab[0x7C] == math.inf and tab[0xFC] == -math.inf
+    assert tab[0x01] == 2.0 ** -16 and tab[0x04] == 2.0 ** -14 and tab[0x3C] == 1.0
+
+
+def test_e5m2_quantisation_round_trip_within_half_ulp():
+    x = torch.randn(4096, generator=torch.Generator().manual_seed(1))
+    q8, descale = quantize_e5m2(x)
+    y = oracle.to_f64(q8, descale)
+    scale = 1.0 / descale
+    xs = x.double().numpy() * scale
+    ys = y * scale
+    # spacing of E5M2 near |x|: 2**(floor(log2|x|) - 2) for normals, 2**-16 below 2**-14
+    e = np.floor(np.log2(np.maximum(np.abs(xs), 2.0 ** -14)))
+    ulp = 2.0 ** (e - 2)
+    assert (np.abs(ys - xs) <= ulp / 2 + 1e-12).all()
+    assert np.abs(oracle.to_f64(q8)).max() <= 57344.0
 
 
 # ---------------------------------------------------------------------------
