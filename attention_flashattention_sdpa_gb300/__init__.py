@@ -28,7 +28,7 @@ STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTED",
           3: "SDPA_ERR_LAYOUT", 4: "SDPA_ERR_WORKSPACE", 5: "SDPA_ERR_CUDA",
           6: "SDPA_ERR_TIMEOUT"}
 
-DTYPE_F16, DTYPE_BF16, DTYPE_E4M3 = 0, 1, 2
+DTYPE_F16, DTYPE_BF16, DTYPE_E4M3, DTYPE_E5M2 = 0, 1, 2, 3
 
 
 class SdpaError(RuntimeError):
@@ -58,6 +58,7 @@ class Problem(ctypes.Structure):
         ("alibi", ctypes.c_int32), ("alibi_slopes", ctypes.c_void_p),
         ("dropout_p", ctypes.c_float), ("dropout_mask", ctypes.c_void_p),
         ("dropout_mask_t", ctypes.c_void_p),
+        ("dout_dtype", ctypes.c_int32), ("descale_do", ctypes.c_void_p),
     ]
 
 
@@ -123,7 +124,7 @@ def _check(status: int):
 def dtype_code(t) -> int:
     import torch
     return {torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16,
-            torch.float8_e4m3fn: DTYPE_E4M3}[t.dtype]
+            torch.float8_e4m3fn: DTYPE_E4M3, torch.float8_e5m2: DTYPE_E5M2}[t.dtype]
 
 
 def _strides(t) -> Strides:
@@ -142,7 +143,7 @@ def make_problem(q, k, v, o=None, *, attn_scale: Optional[float] = None, causal=
                  dout=None, dq=None, dk=None, dv=None, descale_q=None, descale_k=None,
                  descale_v=None, seq_lens_q=None, seq_lens_kv=None, alibi=False,
                  alibi_slopes=None, dropout_p: float = 0.0, dropout_mask=None,
-                 dropout_mask_t=None) -> Problem:
+                 dropout_mask_t=None, descale_do=None) -> Problem:
     """Fills an sdpa_problem_t from logical [b, h, s, d] torch tensors (no copies).
 
     ALiBi is on when ``alibi`` is true or ``alibi_slopes`` (fp32 CUDA tensor of h_q slopes)
@@ -163,6 +164,10 @@ def make_problem(q, k, v, o=None, *, attn_scale: Optional[float] = None, causal=
     p.alibi_slopes = _ptr(alibi_slopes)
     p.dropout_p = float(dropout_p)
     p.dropout_mask, p.dropout_mask_t = _ptr(dropout_mask), _ptr(dropout_mask_t)
+    p.dout_dtype = dtype_code(dout) if dout is not None else p.in_dtype
+    p.descale_do = _ptr(descale_do)
+    if p.in_dtype == DTYPE_E4M3 and o is None:
+        p.out_dtype = DTYPE_BF16
     return p
 
 
@@ -199,13 +204,17 @@ def sdpa_fwd(q, k, v, o, lse=None, *, attn_scale: Optional[float] = None, causal
 
 def sdpa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, *, attn_scale: Optional[float] = None,
              causal=False, stream=None, seq_lens_q=None, seq_lens_kv=None, alibi=False,
-             alibi_slopes=None, dropout_p: float = 0.0, dropout_mask_t=None) -> None:
+             alibi_slopes=None, dropout_p: float = 0.0, dropout_mask_t=None, descale_q=None,
+             descale_k=None, descale_v=None, descale_do=None) -> None:
     """dQ, dK, dV (overwritten) for the incoming gradient ``dout``; the masking, lengths,
     ALiBi and dropout options must be those of the forward call that produced ``o`` and
-    ``lse`` (dropout_mask_t: the transposed keep bits of the same draw)."""
+    ``lse`` (dropout_mask_t: the transposed keep bits of the same draw).  FP8: E4M3 q, k, v
+    and an E5M2 (or E4M3) dout with their fp32 CUDA descales; o, dq, dk, dv in BF16/F16."""
     p = make_problem(q, k, v, o, attn_scale=attn_scale, causal=causal, dout=dout, dq=dq, dk=dk,
                      dv=dv, seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv, alibi=alibi,
-                     alibi_slopes=alibi_slopes, dropout_p=dropout_p, dropout_mask_t=dropout_mask_t)
+                     alibi_slopes=alibi_slopes, dropout_p=dropout_p, dropout_mask_t=dropout_mask_t,
+                     descale_q=descale_q, descale_k=descale_k, descale_v=descale_v,
+                     descale_do=descale_do)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.sdpa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
                         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream)))

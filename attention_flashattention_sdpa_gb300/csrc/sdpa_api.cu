@@ -56,10 +56,27 @@ bool debug_sync() {
   return v;
 }
 
-int elem_bytes(int dt) { return dt == SDPA_DTYPE_E4M3 ? 1 : 2; }
+int elem_bytes(int dt) { return (dt == SDPA_DTYPE_E4M3 || dt == SDPA_DTYPE_E5M2) ? 1 : 2; }
+
+// Dense 16-bit copies of FP8 Q, K, V and dO that an E4M3 backward pass widens into the
+// workspace after its own scratch (0 for 16-bit inputs).
+size_t widen_bytes(const sdpa_problem_t* p, size_t* off_k, size_t* off_v, size_t* off_do) {
+  auto a = [](size_t x) { return (x + 255) & ~size_t(255); };
+  const size_t nq = a(static_cast<size_t>(p->b) * p->h_q * p->s_q * p->d * 2);
+  const size_t nkv = a(static_cast<size_t>(p->b) * p->h_kv * p->s_kv * p->d * 2);
+  if (off_k) *off_k = nq;
+  if (off_v) *off_v = nq + nkv;
+  if (off_do) *off_do = nq + 2 * nkv;
+  return p->in_dtype == SDPA_DTYPE_E4M3 ? 2 * nq + 2 * nkv : 0;
+}
+
+size_t bwd_total_workspace(const sdpa_problem_t* p) {
+  const size_t base = (sdpa::bwd_workspace_bytes(p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d) + 255) & ~size_t(255);
+  return base + widen_bytes(p, nullptr, nullptr, nullptr);
+}
 
 bool valid_dtype(int dt) {
-  return dt == SDPA_DTYPE_F16 || dt == SDPA_DTYPE_BF16 || dt == SDPA_DTYPE_E4M3;
+  return dt == SDPA_DTYPE_F16 || dt == SDPA_DTYPE_BF16 || dt == SDPA_DTYPE_E4M3 || dt == SDPA_DTYPE_E5M2;
 }
 
 // ---------------------------------------------------------------------------
@@ -170,14 +187,20 @@ sdpa_status_t check_problem(const sdpa_problem_t* p, bool backward) {
     return fail(SDPA_ERR_INVALID_ARG, "dropout_p must be in [0, 1), got %g", p->dropout_p);
   if (p->dropout_p > 0.f && p->in_dtype == SDPA_DTYPE_E4M3)
     return fail(SDPA_ERR_UNSUPPORTED, "dropout takes F16 or BF16 inputs, not E4M3");
+  if (p->in_dtype == SDPA_DTYPE_E5M2 || p->out_dtype == SDPA_DTYPE_E5M2)
+    return fail(SDPA_ERR_UNSUPPORTED, "E5M2 is accepted only as dout_dtype of an FP8 backward pass");
   if (p->in_dtype == SDPA_DTYPE_E4M3) {
-    if (backward)
-      return fail(SDPA_ERR_UNSUPPORTED, "the backward pass takes F16 or BF16 inputs, not E4M3");
     if (p->out_dtype == SDPA_DTYPE_E4M3)
       return fail(SDPA_ERR_UNSUPPORTED, "E4M3 inputs give a BF16 or F16 output");
-    if (p->d == 64) return fail(SDPA_ERR_UNSUPPORTED, "E4M3 forward supports d = 128 or 256");
+    if (!backward && p->d == 64) return fail(SDPA_ERR_UNSUPPORTED, "E4M3 forward supports d = 128 or 256");
     if (!p->descale_q || !p->descale_k || !p->descale_v)
       return fail(SDPA_ERR_INVALID_ARG, "E4M3 inputs need descale_q, descale_k and descale_v");
+    if (backward) {
+      if (p->dout_dtype != SDPA_DTYPE_E5M2 && p->dout_dtype != SDPA_DTYPE_E4M3)
+        return fail(SDPA_ERR_UNSUPPORTED, "an E4M3 backward pass takes dO as E5M2 or E4M3 (dout_dtype %d)",
+                    p->dout_dtype);
+      if (!p->descale_do) return fail(SDPA_ERR_INVALID_ARG, "an FP8 dO needs descale_do");
+    }
   } else if (p->out_dtype != p->in_dtype) {
     return fail(SDPA_ERR_UNSUPPORTED, "F16/BF16 inputs give an output of the same dtype");
   }
@@ -231,7 +254,7 @@ sdpa_status_t sdpa_workspace_size(const sdpa_problem_t* p, int is_backward, size
   if (bytes == nullptr) return fail(SDPA_ERR_INVALID_ARG, "bytes is NULL");
   sdpa_status_t st = check_problem(p, is_backward != 0);
   if (st != SDPA_OK) return st;
-  *bytes = is_backward ? sdpa::bwd_workspace_bytes(p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d) : 0;
+  *bytes = is_backward ? bwd_total_workspace(p) : 0;
   return ok();
 }
 
@@ -295,19 +318,21 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
                        void* dv, void* workspace, size_t workspace_bytes, void* stream_) {
   sdpa_status_t st = check_problem(p, true);
   if (st != SDPA_OK) return st;
-  const int es = 2;
-  if ((st = check_view("q", q, p->q, p->b, p->h_q, p->s_q, p->d, es)) != SDPA_OK) return st;
-  if ((st = check_view("k", k, p->k, p->b, p->h_kv, p->s_kv, p->d, es)) != SDPA_OK) return st;
-  if ((st = check_view("v", v, p->v, p->b, p->h_kv, p->s_kv, p->d, es)) != SDPA_OK) return st;
+  const bool fp8 = p->in_dtype == SDPA_DTYPE_E4M3;
+  const int cdt = fp8 ? p->out_dtype : p->in_dtype;   // dtype the kernels compute in
+  const int es = 2, es_in = fp8 ? 1 : 2;
+  if ((st = check_view("q", q, p->q, p->b, p->h_q, p->s_q, p->d, es_in)) != SDPA_OK) return st;
+  if ((st = check_view("k", k, p->k, p->b, p->h_kv, p->s_kv, p->d, es_in)) != SDPA_OK) return st;
+  if ((st = check_view("v", v, p->v, p->b, p->h_kv, p->s_kv, p->d, es_in)) != SDPA_OK) return st;
   if ((st = check_view("o", o, p->o, p->b, p->h_q, p->s_q, p->d, es)) != SDPA_OK) return st;
-  if ((st = check_view("dout", dout, p->dout, p->b, p->h_q, p->s_q, p->d, es)) != SDPA_OK) return st;
+  if ((st = check_view("dout", dout, p->dout, p->b, p->h_q, p->s_q, p->d, es_in)) != SDPA_OK) return st;
   if ((st = check_view("dq", dq, p->dq, p->b, p->h_q, p->s_q, p->d, es)) != SDPA_OK) return st;
   if ((st = check_view("dk", dk, p->dk, p->b, p->h_kv, p->s_kv, p->d, es)) != SDPA_OK) return st;
   if ((st = check_view("dv", dv, p->dv, p->b, p->h_kv, p->s_kv, p->d, es)) != SDPA_OK) return st;
   if (lse == nullptr) return fail(SDPA_ERR_INVALID_ARG, "lse: null pointer (the backward pass needs the forward statistics)");
   if (reinterpret_cast<uintptr_t>(lse) % 4 != 0) return fail(SDPA_ERR_LAYOUT, "lse must be 4-byte aligned");
   if ((st = check_drop_mask(p, p->dropout_mask_t, "dropout_mask_t")) != SDPA_OK) return st;
-  const size_t need = sdpa::bwd_workspace_bytes(p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d);
+  const size_t need = bwd_total_workspace(p);
   if (workspace == nullptr || workspace_bytes < need)
     return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes required, %zu given%s", need,
                 workspace_bytes, workspace ? "" : " (NULL)");
@@ -316,12 +341,39 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
 
   sdpa::BwdParams prm;
   memset(&prm, 0, sizeof(prm));
+  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+  // FP8: widen Q, K, V and dO exactly into dense 16-bit copies after the scratch; the kernels
+  // read those (the descales are folded into their scale factors).
+  sdpa_strides_t sq = p->q, sk = p->k, sv = p->v, sdo = p->dout;
+  if (fp8) {
+    size_t off_k, off_v, off_do;
+    widen_bytes(p, &off_k, &off_v, &off_do);
+    uint8_t* wbase = static_cast<uint8_t*>(workspace) +
+                     ((sdpa::bwd_workspace_bytes(p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d) + 255) & ~size_t(255));
+    const sdpa_strides_t dq_st = {(int64_t)p->h_q * p->s_q * p->d, (int64_t)p->s_q * p->d, p->d, 1};
+    const sdpa_strides_t dkv_st = {(int64_t)p->h_kv * p->s_kv * p->d, (int64_t)p->s_kv * p->d, p->d, 1};
+    struct W { const void* src; const sdpa_strides_t* st; int h, s, e5m2; uint8_t* dst; };
+    const W ws4[4] = {{q, &p->q, p->h_q, p->s_q, 0, wbase}, {k, &p->k, p->h_kv, p->s_kv, 0, wbase + off_k},
+                      {v, &p->v, p->h_kv, p->s_kv, 0, wbase + off_v},
+                      {dout, &p->dout, p->h_q, p->s_q, p->dout_dtype == SDPA_DTYPE_E5M2, wbase + off_do}};
+    for (const W& w : ws4) {
+      cudaError_t e = sdpa::launch_fp8_widen(w.src, w.st->b, w.st->h, w.st->s, p->b, w.h, w.s, p->d, w.e5m2,
+                                             w.dst, cdt, stream);
+      if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "FP8 widening launch failed: %s", cudaGetErrorString(e));
+    }
+    q = ws4[0].dst; k = ws4[1].dst; v = ws4[2].dst; dout = ws4[3].dst;
+    sq = dq_st; sk = dkv_st; sv = dkv_st; sdo = dq_st;
+    prm.descale_q = p->descale_q;
+    prm.descale_k = p->descale_k;
+    prm.descale_v = p->descale_v;
+    prm.descale_do = p->descale_do;
+  }
   // d = 256 walks 64-row query blocks (its kernel keeps only half of d of dK/dV in TMEM).
   const int q_rows = p->d == 256 ? 64 : 128;
-  if ((st = make_map(&prm.tm_q, "q", q, p->q, p->b, p->h_q, p->s_q, p->d, p->in_dtype, q_rows)) != SDPA_OK) return st;
-  if ((st = make_map(&prm.tm_k, "k", k, p->k, p->b, p->h_kv, p->s_kv, p->d, p->in_dtype, 128)) != SDPA_OK) return st;
-  if ((st = make_map(&prm.tm_v, "v", v, p->v, p->b, p->h_kv, p->s_kv, p->d, p->in_dtype, 128)) != SDPA_OK) return st;
-  if ((st = make_map(&prm.tm_do, "dout", dout, p->dout, p->b, p->h_q, p->s_q, p->d, p->in_dtype, q_rows)) != SDPA_OK) return st;
+  if ((st = make_map(&prm.tm_q, "q", q, sq, p->b, p->h_q, p->s_q, p->d, cdt, q_rows)) != SDPA_OK) return st;
+  if ((st = make_map(&prm.tm_k, "k", k, sk, p->b, p->h_kv, p->s_kv, p->d, cdt, 128)) != SDPA_OK) return st;
+  if ((st = make_map(&prm.tm_v, "v", v, sv, p->b, p->h_kv, p->s_kv, p->d, cdt, 128)) != SDPA_OK) return st;
+  if ((st = make_map(&prm.tm_do, "dout", dout, sdo, p->b, p->h_q, p->s_q, p->d, cdt, q_rows)) != SDPA_OK) return st;
   if ((st = make_map(&prm.tm_dk, "dk", dk, p->dk, p->b, p->h_kv, p->s_kv, p->d, p->out_dtype, 128)) != SDPA_OK) return st;
   if ((st = make_map(&prm.tm_dv, "dv", dv, p->dv, p->b, p->h_kv, p->s_kv, p->d, p->out_dtype, 128)) != SDPA_OK) return st;
   const int s_q_pad = (p->s_q + 127) / 128 * 128;
@@ -354,7 +406,7 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
   prm.delta = reinterpret_cast<float*>(ws + acc_bytes);
   prm.lse2 = reinterpret_cast<float*>(ws + acc_bytes + vec_bytes);
   prm.o_sb = p->o.b; prm.o_sh = p->o.h; prm.o_ss = p->o.s;
-  prm.do_sb = p->dout.b; prm.do_sh = p->dout.h; prm.do_ss = p->dout.s;
+  prm.do_sb = sdo.b; prm.do_sh = sdo.h; prm.do_ss = sdo.s;
   prm.dq_sb = p->dq.b; prm.dq_sh = p->dq.h; prm.dq_ss = p->dq.s;
   prm.b = p->b;
   prm.h_q = p->h_q;
@@ -391,11 +443,10 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
   if ((int64_t)p->b * p->h_q > 65535 ||
       (int64_t)p->b * p->h_kv * prm.kv_split * ((p->s_kv + 127) / 128) > 0x7fffffff)
     return fail(SDPA_ERR_UNSUPPORTED, "grid too large (b*h_q must be <= 65535 for the backward pass)");
-  cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (log_level() >= 1)
     fprintf(stderr, "[sdpa] bwd b=%d h_q=%d h_kv=%d s_q=%d s_kv=%d d=%d dt=%d causal=%d ws=%zu\n",
             p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d, p->in_dtype, p->causal, need);
-  cudaError_t e = sdpa::launch_bwd(prm, p->in_dtype, stream);
+  cudaError_t e = sdpa::launch_bwd(prm, cdt, stream);
   return finish_launch(e, stream, "sdpa_bwd");
 }
 

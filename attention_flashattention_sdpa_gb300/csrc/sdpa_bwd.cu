@@ -20,6 +20,7 @@
 //                 shared memory into the fp32 accumulator with TMA reduce-add.
 //   3. bwd_dq:    dQ = scale·accumulator, rounded to the output dtype in the caller's strides.
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_fp16.h>
 
 #include <type_traits>
@@ -73,6 +74,32 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
 // 1. preprocess: Delta, LSE·log2 e, zeroed dQ accumulator
 // ---------------------------------------------------------------------------
 
+// Scale factors of the backward pass.  With FP8 inputs the kernels read widened copies of
+// the stored codes, so the per-tensor descales enter here: S = scale·d_q·d_k·Q'K'ᵀ,
+// dP = d_do·d_v·dO'V'ᵀ, dV = d_do·Pᵀ dO', dK = scale·d_q·dSᵀ Q', dQ = scale·d_k·dS K',
+// Delta = d_do·rowsum(dO'∘O); dropout's 1/(1 - p) multiplies dP and dV.
+struct BwdScales {
+  float s_log2, dp, dv, dk, dq, delta;
+};
+
+__device__ __forceinline__ BwdScales bwd_scales(const BwdParams& p) {
+  float dq = 1.f, dk = 1.f, dv = 1.f, ddo = 1.f;
+  if (p.descale_q != nullptr) {
+    dq = __ldg(p.descale_q);
+    dk = __ldg(p.descale_k);
+    dv = __ldg(p.descale_v);
+    ddo = __ldg(p.descale_do);
+  }
+  BwdScales s;
+  s.s_log2 = p.scale_log2 * dq * dk;
+  s.dp = ddo * dv * p.drop_scale;
+  s.dv = ddo * p.drop_scale;
+  s.dk = p.scale * dq;
+  s.dq = p.scale * dk;
+  s.delta = ddo;
+  return s;
+}
+
 // One group of D/8 threads per row; each thread reads 8 elements (16 bytes) of O and dO.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
@@ -103,7 +130,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
     reinterpret_cast<float4*>(dq)[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (part == 0) {
       // Stored negated, so the main kernel adds them with paired fp32 instructions.
-      p.delta[vrow] = valid ? -acc : 0.f;
+      p.delta[vrow] = valid ? -acc * bwd_scales(p).delta : 0.f;
       // Rows with no visible key (LSE = -inf) and padded rows get P = 0 everywhere.
       const float lse = valid ? p.lse[static_cast<int64_t>(bh) * p.s_q + row] : -INFINITY;
       // ALiBi's bias slope * (key - row - off) is split: -slope * (row mod 128) joins this
@@ -130,7 +157,7 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdParams p) {
   const float* src = p.dq_acc + (static_cast<int64_t>(bh) * p.s_q_pad + row) * D + part * 8;
   const float4 a = reinterpret_cast<const float4*>(src)[0];
   const float4 b = reinterpret_cast<const float4*>(src)[1];
-  const float s = p.scale;
+  const float s = bwd_scales(p).dq;
   const int dt = sizeof(T) == 2 && std::is_same<T, __nv_bfloat16>::value ? kBF16 : kF16;
   uint4 w;
   w.x = pack2(a.x * s, a.y * s, dt);
@@ -462,6 +489,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     const int r = quad * 32 + lane;                       // key row within the block (TMEM lane)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const int kv_row = j * kBlockN + r;
+    const BwdScales bs = bwd_scales(p);
     bool ok = true;
     int it = 0;
     for (int n = 0; n < n_iter; ++n) {
@@ -493,7 +521,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       int lim = p.causal ? kv_row - q0 - L.off : -(1 << 30);
       if (kv_row >= L.len_kv) lim = 1 << 30;
       uint32_t pk[32], pm[DROP ? 32 : 1];
-      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+      const float2 sc2 = make_float2(bs.s_log2, bs.s_log2);
       // ALiBi: the key-row part of the bias (the column part is in the -LSE vector).
       const float kr = ALIBI ? alibi_slope_log2(p, iter_head(n)) *
                                    static_cast<float>(kv_row - iter_qblk(n) * kBlockM - L.off) : 0.f;
@@ -536,7 +564,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       if constexpr (DROP) {
         // dP = keep / (1 - p) * dO·Vᵀ.  Half the columns at a time (fewer live registers):
         // the second half is read before region Y is released.
-        const float2 rk2 = make_float2(p.drop_scale, p.drop_scale);
+        const float2 rk2 = make_float2(bs.dp, bs.dp);
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           tmem_ld32(Y + 64 * h + 32 * half, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
@@ -562,11 +590,12 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&bars.dp_consumed[b]);   // region Y may now take the next step's Sᵀ
+        const float2 dp2 = make_float2(bs.dp, bs.dp);
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
           const float2 nd = *reinterpret_cast<const float2*>(ndelta + c);
           const float2 dd = mul2(unpack2(pk[c / 2], DT),
-                                 add2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), nd));
+                                 fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), dp2, nd));
           ds[c / 2] = pack2(dd.x, dd.y, DT);
         }
       }
@@ -591,7 +620,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       // Split group: add this CTA's share into the fp32 accumulator (once per CTA).
       tc_fence_after();
       const uint32_t acc = tmem + lane_off + (h == 0 ? C::DV_COL : C::DK_COL);
-      const float mul = (h == 0) ? p.drop_scale : p.scale;
+      const float mul = (h == 0) ? bs.dv : bs.dk;
       float* dst = (h == 0 ? p.dv_acc : p.dk_acc) +
                    ((static_cast<int64_t>(bi) * p.h_kv + hk) * p.s_kv_pad + kv_row) * D;
 #pragma unroll 1
@@ -608,7 +637,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     } else if (ok) {
       tc_fence_after();
       const uint32_t acc = tmem + lane_off + (h == 0 ? C::DV_COL : C::DK_COL);
-      const float mul = (h == 0) ? p.drop_scale : p.scale;
+      const float mul = (h == 0) ? bs.dv : bs.dk;
 #pragma unroll 1
       for (int c = 0; c < D / 64; ++c) {
         uint32_t v[64];
@@ -805,6 +834,7 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort;
   const uint32_t fmt = (DT == kBF16) ? 1u : 0u;
+  const BwdScales bs = bwd_scales(p);
 
   if (threadIdx.x == 0) {
     mbar_arrive_expect_tx(&bars.kv_full, 2 * 65536);
@@ -861,7 +891,7 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
                              (j * kBlockN + kBlockN > L.len_kv);
       int lim = p.causal ? kv_row - q0 - L.off : -(1 << 30);  // column c visible iff c >= lim
       if (kv_row >= L.len_kv) lim = 1 << 30;
-      const float2 sc2 = make_float2(p.scale_log2, p.scale_log2);
+      const float2 sc2 = make_float2(bs.s_log2, bs.s_log2);
       // ALiBi: the key-row part of the bias (the column part is in the -LSE vector, relative
       // to the 128-aligned block that holds this 64-row query block).
       const float kr = ALIBI ? alibi_slope_log2(p, hq) *
@@ -872,7 +902,7 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
       if (DROP && kv_row < p.s_kv)
         keep = __ldg(reinterpret_cast<const uint2*>(
             p.drop_cols + ((static_cast<int64_t>(bi) * p.h_q + hq) * p.s_kv + kv_row) * p.drop_q_words + q0 / 32));
-      const float2 rk2 = make_float2(p.drop_scale, p.drop_scale);
+      const float2 rk2 = make_float2(bs.dp, bs.dp);
       uint32_t pk[32], ds[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
@@ -897,7 +927,7 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
           t = fma2(dp, rk2, nd);
         } else {
           pk[c / 2] = pack2(p0, p1, DT);
-          t = add2(dp, nd);
+          t = fma2(dp, rk2, nd);
         }
         const float2 dd = mul2(make_float2(p0, p1), t);
         ds[c / 2] = pack2(dd.x, dd.y, DT);
@@ -980,12 +1010,12 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
           tmem_ld_wait();
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            red_add_v4(dvp + c * 32 + u * 4, __uint_as_float(a[u * 4]) * p.drop_scale,
-                       __uint_as_float(a[u * 4 + 1]) * p.drop_scale, __uint_as_float(a[u * 4 + 2]) * p.drop_scale,
-                       __uint_as_float(a[u * 4 + 3]) * p.drop_scale);
-            red_add_v4(dkp + c * 32 + u * 4, __uint_as_float(k2[u * 4]) * p.scale,
-                       __uint_as_float(k2[u * 4 + 1]) * p.scale, __uint_as_float(k2[u * 4 + 2]) * p.scale,
-                       __uint_as_float(k2[u * 4 + 3]) * p.scale);
+            red_add_v4(dvp + c * 32 + u * 4, __uint_as_float(a[u * 4]) * bs.dv,
+                       __uint_as_float(a[u * 4 + 1]) * bs.dv, __uint_as_float(a[u * 4 + 2]) * bs.dv,
+                       __uint_as_float(a[u * 4 + 3]) * bs.dv);
+            red_add_v4(dkp + c * 32 + u * 4, __uint_as_float(k2[u * 4]) * bs.dk,
+                       __uint_as_float(k2[u * 4 + 1]) * bs.dk, __uint_as_float(k2[u * 4 + 2]) * bs.dk,
+                       __uint_as_float(k2[u * 4 + 3]) * bs.dk);
           }
         }
       }
@@ -994,7 +1024,7 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
       for (int which = 0; which < 2; ++which) {
         uint8_t* stage = which == 0 ? sQ : sdO;
         const uint32_t acc = which == 0 ? acc_v : acc_k;
-        const float mul = which == 0 ? p.drop_scale : p.scale;
+        const float mul = which == 0 ? bs.dv : bs.dk;
         for (int c = 0; c < 2; ++c) {
           uint32_t v[64];
           if (n_iter > 0) {
@@ -1051,7 +1081,7 @@ __global__ void __launch_bounds__(256) bwd_dqT_kernel(const BwdParams p) {
   for (int k = ty; k < 32; k += 8) {
     const int i = i0 + k;
     if (i >= p.s_q) continue;
-    const float v = tile[tx][k] * p.scale;
+    const float v = tile[tx][k] * bwd_scales(p).dq;
     T* dst = reinterpret_cast<T*>(p.dq) + bi * p.dq_sb + hq * p.dq_sh + i * p.dq_ss + c0 + tx;
     if constexpr (std::is_same<T, __nv_bfloat16>::value) *dst = __float2bfloat16_rn(v);
     else *dst = __float2half_rn(v);
@@ -1161,6 +1191,61 @@ cudaError_t launch_bwd(const BwdParams& p, int dtype, cudaStream_t st) {
     if (p.d == 256) return launch_d256<kF16>(p, st);
   }
   return cudaErrorInvalidValue;
+}
+
+namespace {
+
+// Sixteen FP8 codes (one 16-byte load along d) -> sixteen F16 or BF16 values (32 bytes),
+// exact: every E4M3 and E5M2 value is representable in both.
+template <typename T>
+__global__ void __launch_bounds__(256) fp8_widen_kernel(const uint8_t* src, int64_t sb, int64_t sh, int64_t ss,
+                                                        int b, int h, int s, int d, int e5m2, T* dst) {
+  const int per_row = d / 16;
+  const int64_t n = static_cast<int64_t>(b) * h * s * per_row;
+  const __nv_fp8_interpretation_t fmt = e5m2 ? __NV_E5M2 : __NV_E4M3;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int part = static_cast<int>(t % per_row);
+    int64_t r = t / per_row;
+    const int si = static_cast<int>(r % s);
+    r /= s;
+    const int hi = static_cast<int>(r % h);
+    const int bi = static_cast<int>(r / h);
+    const uint4 v = *reinterpret_cast<const uint4*>(src + bi * sb + hi * sh + si * ss + part * 16);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((w[i / 2] >> (16 * (i % 2))) & 0xFFFFu);
+      const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, fmt);
+      if constexpr (std::is_same<T, __half>::value) {
+        o[i] = static_cast<uint32_t>(hr.x) | (static_cast<uint32_t>(hr.y) << 16);
+      } else {
+        const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+        const __nv_bfloat162 bb = __floats2bfloat162_rn(f.x, f.y);
+        o[i] = *reinterpret_cast<const uint32_t*>(&bb);
+      }
+    }
+    uint4* out = reinterpret_cast<uint4*>(dst + ((static_cast<int64_t>(bi) * h + hi) * s + si) * d + part * 16);
+    out[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    out[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_widen(const void* src, int64_t sb, int64_t sh, int64_t ss, int b, int h, int s,
+                             int d, int src_e5m2, void* dst, int dst_dtype, cudaStream_t st) {
+  const int64_t n = static_cast<int64_t>(b) * h * s * (d / 16);
+  const int64_t want = (n + 255) / 256;
+  const unsigned grid = static_cast<unsigned>(want < 152 * 16 ? want : 152 * 16);
+  const uint8_t* p8 = static_cast<const uint8_t*>(src);
+  if (dst_dtype == kBF16)
+    fp8_widen_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p8, sb, sh, ss, b, h, s, d, src_e5m2,
+                                                          static_cast<__nv_bfloat16*>(dst));
+  else
+    fp8_widen_kernel<__half><<<grid, 256, 0, st>>>(p8, sb, sh, ss, b, h, s, d, src_e5m2, static_cast<__half*>(dst));
+  return cudaGetLastError();
 }
 
 uint32_t bwd_take_device_error() {

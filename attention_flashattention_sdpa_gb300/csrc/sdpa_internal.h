@@ -82,7 +82,18 @@ struct BwdParams {
   const uint32_t* drop_cols;    // dropout keep bits, transposed: [b*h_q][s_kv][drop_q_words]
   int drop_q_words;             // 32-bit words per key row: ceil(s_q / 128) * 4
   float drop_scale;             // 1 / (1 - p), or 1 without dropout
+  // FP8 inputs (widened exactly to the output dtype before the kernels run): per-tensor
+  // descales of Q, K, V and dO, folded into the kernels' scale factors; nullptr otherwise.
+  const float* descale_q;
+  const float* descale_k;
+  const float* descale_v;
+  const float* descale_do;
 };
+
+// Widens a strided FP8 (E4M3 or E5M2) [b][h][s][d] view into a dense F16 or BF16 copy.  Every
+// FP8 value is exact in either 16-bit format; descales are applied later, by the kernels.
+cudaError_t launch_fp8_widen(const void* src, int64_t sb, int64_t sh, int64_t ss, int b, int h, int s,
+                             int d, int src_e5m2, void* dst, int dst_dtype, cudaStream_t st);
 
 // Dropout keep mask (see sdpa_dropout.cu for the definition).
 struct DropoutParams {

@@ -531,10 +531,15 @@ def sweep_one(w, peaks, args):
         line["fwd_frac_of_e4m3_peak"] = line["fwd_tflops"] / peaks["e4m3_tflops"]
     if w.backward:
         do = dev(x.do)
-        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
-        p = sdpa.make_problem(q, k, v, o, attn_scale=w.scale, causal=w.causal, dout=do, dq=dq, dk=dk, dv=dv)
-        ws = torch.empty(sdpa.sdpa_workspace_size(p, True), dtype=torch.uint8, device="cuda")
         dkw = {} if w.dropout == 0 else {"dropout_p": w.dropout, "dropout_mask_t": mask_t}
+        if w.dtype == "e4m3":   # E4M3 Q, K, V and E5M2 dO; O and the gradients in bf16
+            dkw.update(kw)
+            dkw["descale_do"] = torch.tensor([x.descale_do], device="cuda")
+        dq, dk, dv = (torch.empty(t.shape, dtype=odt, device="cuda") for t in (q, k, v))
+        p = sdpa.make_problem(q, k, v, o, attn_scale=w.scale, causal=w.causal, dout=do, dq=dq, dk=dk, dv=dv,
+                              descale_q=dkw.get("descale_q"), descale_k=dkw.get("descale_k"),
+                              descale_v=dkw.get("descale_v"), descale_do=dkw.get("descale_do"))
+        ws = torch.empty(sdpa.sdpa_workspace_size(p, True), dtype=torch.uint8, device="cuda")
         bwd = lambda: sdpa.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, attn_scale=w.scale, causal=w.causal,
                                     alibi=w.alibi, **dkw)
         for _ in range(3):

@@ -63,7 +63,8 @@ typedef enum {
 typedef enum {
   SDPA_DTYPE_F16 = 0,         /* IEEE binary16 */
   SDPA_DTYPE_BF16 = 1,        /* bfloat16 */
-  SDPA_DTYPE_E4M3 = 2         /* OCP FP8 E4M3 (finite max 448); forward inputs only */
+  SDPA_DTYPE_E4M3 = 2,        /* OCP FP8 E4M3 (finite max 448): Q, K, V (forward and backward) */
+  SDPA_DTYPE_E5M2 = 3         /* OCP FP8 E5M2 (max 57344): dO of an FP8 backward pass only */
 } sdpa_dtype_t;
 
 /* Element strides of a logical [b][h][s][d] view.  d must be 1. */
@@ -121,6 +122,14 @@ typedef struct {
   float dropout_p;
   const uint32_t* dropout_mask;
   const uint32_t* dropout_mask_t;
+  /* FP8 backward (the HYBRID recipe of the codelab's TransformerEngine section: E4M3 in the
+   * forward pass, E5M2 for gradients).  Read only when in_dtype is E4M3 and the call is
+   * sdpa_bwd: dO has dout_dtype (E5M2 or E4M3) with the per-tensor descale *descale_do
+   * (DEVICE pointer); Q, K, V are E4M3 with descale_q/k/v; O and dQ, dK, dV have out_dtype
+   * (BF16 or F16).  The codes are widened exactly to out_dtype in the workspace and the
+   * descales folded into the kernels' scale factors; the MMAs run at 16-bit precision. */
+  int32_t dout_dtype;
+  const float* descale_do;
 } sdpa_problem_t;
 
 /*
@@ -157,7 +166,7 @@ SDPA_API sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const vo
  *       dV hold the sum over the query heads of each KV group (GQA/MQA).
  *   workspace: >= sdpa_workspace_size(p, 1) bytes, 256-byte aligned; its contents on entry
  *       do not matter and are clobbered.
- * F16/BF16 only (an E4M3 backward pass is SDPA_ERR_UNSUPPORTED).
+ * F16/BF16, or E4M3 Q/K/V with E5M2 or E4M3 dO (see dout_dtype).
  */
 SDPA_API sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, const void* v,
                        const void* o, const void* dout, const float* lse, void* dq, void* dk,

@@ -105,11 +105,18 @@ def training_dropout(s: int, p: float = 0.1) -> Workload:
                     w.dtype, causal=True, backward=True, dropout=p)
 
 
+def training_fp8(s: int) -> Workload:
+    """The training shape in FP8: E4M3 Q, K, V (bf16 O) and E5M2 dO."""
+    w = training(s)
+    return Workload(f"training_fp8_e4m3_causal_d128_s{s}", w.b, w.h_q, w.h_kv, s, s, w.d, "e4m3",
+                    causal=True, backward=True)
+
+
 def all_workloads():
     out = [tiny(False), tiny(True), gpt2_inference()]
     out += [training(s) for s in TRAINING_SEQ_LENS]
     out += [fp8_large_head(), grouped(8), grouped(1), grouped(64), training_alibi(8192),
-            training_dropout(8192)]
+            training_dropout(8192), training_fp8(8192)]
     return out
 
 

@@ -125,8 +125,18 @@ def test_unit_dimension_strides_are_ignored(m):
 
 
 def test_backward_rejections(m):
-    assert _bwd(m, _problem(m, in_dtype=2, out_dtype=1)) == 2
-    assert "E4M3" in m.sdpa_last_error_string()
+    fp8 = dict(in_dtype=2, out_dtype=1, descale_q=FAKE, descale_k=FAKE, descale_v=FAKE)
+    assert _bwd(m, _problem(m, in_dtype=2, out_dtype=1)) == 1
+    assert "descale" in m.sdpa_last_error_string()
+    assert _bwd(m, _problem(m, dout_dtype=1, descale_do=FAKE, **fp8)) == 2
+    assert "dout_dtype" in m.sdpa_last_error_string()
+    assert _bwd(m, _problem(m, dout_dtype=3, **fp8)) == 1 and "descale_do" in m.sdpa_last_error_string()
+    assert _bwd(m, _problem(m, in_dtype=3, out_dtype=1)) == 2 and "E5M2" in m.sdpa_last_error_string()
+    # a valid FP8 problem is stopped by its workspace size (it needs room for the widened copies)
+    ok8 = _problem(m, dout_dtype=3, descale_do=FAKE, **fp8)
+    need8 = m.sdpa_workspace_size(ok8, True)
+    assert need8 == m.sdpa_workspace_size(_problem(m, in_dtype=1, out_dtype=1), True) + 4 * 2 * 128 * 64 * 2
+    assert _bwd(m, ok8, ws_bytes=need8 - 1) == 4
     assert _bwd(m, _problem(m, d=200)) == 2
     assert _bwd(m, _problem(m), lse=None) == 1 and "lse" in m.sdpa_last_error_string()
     assert _bwd(m, _problem(m), ws=None) == 4 and "workspace" in m.sdpa_last_error_string()
