@@ -37,16 +37,20 @@ constexpr float kLn2 = 0.6931471805599453f;
 template <int D, int DT>
 struct FwdCfg {
   static constexpr int ES = (DT == kE4M3) ? 1 : 2;               // input element bytes
-  static constexpr int NQT = (DT != kE4M3 && D <= 128) ? 2 : 1;   // Q tiles per CTA
+  static constexpr int NQT = (D <= 128) ? 2 : 1;                 // Q tiles per CTA
   static constexpr int CHUNK_ELEMS = 128 / ES;                    // elements per 128-byte row chunk
   static constexpr int NCHUNK = D * ES / 128;                     // 128-byte chunks along d
   static constexpr int TILE_BYTES = kBlockM * D * ES;             // one Q or K or V tile
   static constexpr int Q_BYTES = NQT * TILE_BYTES;
-  static constexpr int RING_BUDGET = 196608 - Q_BYTES;
+  static constexpr int OUT_TILE = kBlockM * D * 2;                // one 16-bit O tile
+  // Two Q tiles stage their O tiles in their own Q buffers, unless those are smaller
+  // (E4M3 inputs): then the O tiles get a buffer of their own.
+  static constexpr int STAGE_BYTES = (NQT == 2 && TILE_BYTES < OUT_TILE) ? NQT * OUT_TILE : 0;
+  static constexpr int RING_BUDGET = 196608 - Q_BYTES - STAGE_BYTES;
   static constexpr int NS = (RING_BUDGET / TILE_BYTES) > 8 ? 8 : (RING_BUDGET / TILE_BYTES);
   static constexpr int RING_BYTES = NS * TILE_BYTES;
   static constexpr int OUT_TILE_BYTES = kBlockM * D * 2;          // 16-bit output tile
-  static constexpr int SMEM_BYTES = Q_BYTES + RING_BYTES + 1024 /*align slack*/;
+  static constexpr int SMEM_BYTES = Q_BYTES + RING_BYTES + STAGE_BYTES + 1024 /*align slack*/;
   static constexpr int THREADS = 128 + NQT * 128;
   static constexpr int KSTEPS_S = D * ES / 32;                    // QKᵀ: 32 bytes of d per MMA
   static constexpr int PV_ROWS = 32 / ES;                         // PV: kv rows per MMA
@@ -472,7 +476,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
     // ---- epilogue: O / l through shared memory and a TMA store; LSE ------------------
     // A CTA whose rows see no key at all (padding) skips the pipeline and writes zeros.
     ok = ok && (n_blocks == 0 || mbar_wait_warp(&bars.o_full[t], 0, abort_flag));
-    uint8_t* stage = (NQT == 2) ? (sQ + t * C::TILE_BYTES) : sRing;
+    uint8_t* stage = (NQT == 1) ? sRing
+                     : (C::STAGE_BYTES > 0) ? sRing + C::RING_BYTES + t * C::OUT_TILE
+                                            : sQ + t * C::TILE_BYTES;
     if (ok) {
       tc_fence_after();
       const float inv_l = (l > 0.f) ? v_scale / l : 0.f;   // rows without a visible key: O = 0
@@ -546,7 +552,10 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t st) {
 
 }  // namespace
 
-int fwd_q_tiles(int d, int in_dtype) { return (in_dtype != kE4M3 && d <= 128) ? 2 : 1; }
+int fwd_q_tiles(int d, int in_dtype) {
+  (void)in_dtype;
+  return d <= 128 ? 2 : 1;
+}
 
 cudaError_t launch_fwd(const FwdParams& p, int d, int in_dtype, int out_dtype, cudaStream_t st) {
   if (in_dtype == kF16) {
