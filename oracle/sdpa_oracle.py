@@ -36,6 +36,9 @@ module's own table and multiplied by their descale):
   slopes; without caller slopes the default is the geometric sequence m_h = 2^(-8 (h+1) / H)
   of the ALiBi paper (Press, Smith and Lewis, "Train Short, Test Long", §3: 1/2 ... 1/256 for
   8 heads), applied by the same formula to any head count;
+* an additive bias (the SDPA node's bias input in the cuDNN 9 blog's walkthrough): a tensor
+  [b or 1, h_q or 1, s_q, s_kv] added to the scaled scores before the mask and the softmax
+  (broadcast over a batch or head dimension of size 1); it is an input without gradient;
 * dropout (the SDPA node's dropout option in the cuDNN 9 blog's walkthrough, named and not
   defined): after the softmax each probability is kept with a keep mask Z and the kept ones
   are scaled by 1/(1 - p), so O = (P * Z) V / (1 - p); the LSE is that of the undropped
@@ -288,6 +291,18 @@ def _batch_off(s_q, s_kv, bi, seq_lens_q, seq_lens_kv, bottom_right):
     return lkv - lq
 
 
+def _bias_of(bias, alibi_slopes, s_q, s_kv, bi, hq, off):
+    """The additive term on the scaled scores of (bi, hq): ALiBi plus a bias tensor."""
+    out = None
+    if alibi_slopes is not None:
+        out = alibi_bias(s_q, s_kv, float(alibi_slopes[hq]), off)
+    if bias is not None:
+        t = np.asarray(bias, dtype=np.float64)
+        term = t[bi if t.shape[0] > 1 else 0, hq if t.shape[1] > 1 else 0]
+        out = term if out is None else out + term
+    return out
+
+
 def _zdrop(keep, dropout_p, bi, hq):
     if keep is None:
         return None
@@ -296,12 +311,13 @@ def _zdrop(keep, dropout_p, bi, hq):
 
 def forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: bool,
             seq_lens_q=None, seq_lens_kv=None, bottom_right: bool = False, alibi_slopes=None,
-            dropout_p: float = 0.0, keep=None):
+            dropout_p: float = 0.0, keep=None, bias=None):
     """Full forward on logical BHSD fp64 arrays.
 
     q: [b, h_q, s_q, d]; k, v: [b, h_kv, s_kv, d]; optional per-batch valid lengths,
-    per-query-head ALiBi slopes, and a dropout keep mask [b, h_q, s_q, s_kv] with its
-    probability.  Returns (O [b,h_q,s_q,d], LSE [b,h_q,s_q])."""
+    per-query-head ALiBi slopes, a dropout keep mask [b, h_q, s_q, s_kv] with its
+    probability, and an additive bias [b|1, h_q|1, s_q, s_kv].  Returns (O [b,h_q,s_q,d],
+    LSE [b,h_q,s_q])."""
     b, h_q, s_q, d = q.shape
     h_kv, s_kv = k.shape[1], k.shape[2]
     varlen = seq_lens_q is not None or seq_lens_kv is not None or bottom_right
@@ -312,9 +328,9 @@ def forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: b
         off = _batch_off(s_q, s_kv, bi, seq_lens_q, seq_lens_kv, bottom_right)
         for hq in range(h_q):
             hk = kv_head_of(hq, h_q, h_kv)
-            bias = None if alibi_slopes is None else alibi_bias(s_q, s_kv, float(alibi_slopes[hq]), off)
+            term = _bias_of(bias, alibi_slopes, s_q, s_kv, bi, hq, off)
             O[bi, hq], L[bi, hq], _ = head_forward(q[bi, hq], k[bi, hk], v[bi, hk], scale, mask,
-                                                   allow_empty=varlen, bias=bias,
+                                                   allow_empty=varlen, bias=term,
                                                    zdrop=_zdrop(keep, dropout_p, bi, hq))
     return O, L
 
@@ -351,7 +367,8 @@ def _head_backward(qh, kh, vh, doh, scale, mask, allow_empty=False, bias=None, z
 
 
 def backward(q, k, v, do, scale: float, causal: bool, seq_lens_q=None, seq_lens_kv=None,
-             bottom_right: bool = False, alibi_slopes=None, dropout_p: float = 0.0, keep=None):
+             bottom_right: bool = False, alibi_slopes=None, dropout_p: float = 0.0, keep=None,
+             bias=None):
     """Full backward on logical BHSD fp64 arrays: returns (dQ, dK, dV).
 
     dK, dV have K's and V's shapes and hold the sum over each KV head's group.  With
@@ -367,9 +384,9 @@ def backward(q, k, v, do, scale: float, causal: bool, seq_lens_q=None, seq_lens_
         off = _batch_off(s_q, s_kv, bi, seq_lens_q, seq_lens_kv, bottom_right)
         for hq in range(h_q):
             hk = kv_head_of(hq, h_q, h_kv)
-            bias = None if alibi_slopes is None else alibi_bias(s_q, s_kv, float(alibi_slopes[hq]), off)
+            term = _bias_of(bias, alibi_slopes, s_q, s_kv, bi, hq, off)
             gq, gk, gv = _head_backward(q[bi, hq], k[bi, hk], v[bi, hk], do[bi, hq], scale, mask,
-                                        allow_empty=varlen, bias=bias,
+                                        allow_empty=varlen, bias=term,
                                         zdrop=_zdrop(keep, dropout_p, bi, hq))
             dQ[bi, hq] = gq
             dK[bi, hk] += gk

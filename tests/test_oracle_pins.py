@@ -614,3 +614,70 @@ def test_dropout_backward_matches_finite_differences():
             x[idx] = old
             fd[idx] = (lp - lm) / 2e-6
         assert np.linalg.norm(got - fd) / np.linalg.norm(fd) < 1e-6
+
+
+# ---------------------------------------------------------------------------
+# Additive bias tensor
+# ---------------------------------------------------------------------------
+
+def test_bias_brute_force_and_broadcast():
+    q, k, v = _rand(2, 3, 4, 3), _rand(2, 3, 5, 3), _rand(2, 3, 5, 3)
+    rng = np.random.default_rng(11)
+    for shape in ((2, 3, 4, 5), (1, 3, 4, 5), (2, 1, 4, 5), (1, 1, 4, 5)):
+        bias = rng.standard_normal(shape)
+        O, L = oracle.forward(q, k, v, 0.9, False, bias=bias)
+        for b in range(2):
+            for h in range(3):
+                bb = bias[b if shape[0] > 1 else 0, h if shape[1] > 1 else 0]
+                for i in range(4):
+                    w = [math.exp(0.9 * float(q[b, h, i] @ k[b, h, j]) + bb[i, j]) for j in range(5)]
+                    np.testing.assert_allclose(O[b, h, i], sum(w[j] / sum(w) * v[b, h, j] for j in range(5)),
+                                               atol=1e-12)
+                    np.testing.assert_allclose(L[b, h, i], math.log(sum(w)), atol=1e-12)
+
+
+def test_bias_invariances():
+    """A bias constant along each row changes O but not P (shift invariance of softmax), and
+    only shifts LSE; a -inf bias above the diagonal is the causal mask; the ALiBi matrix
+    passed as a bias equals the ALiBi option."""
+    q, k, v = _rand(1, 2, 6, 4), _rand(1, 2, 6, 4), _rand(1, 2, 6, 4)
+    O0, L0 = oracle.forward(q, k, v, 0.5, False)
+    rows = np.arange(6, dtype=np.float64)[None, None, :, None] * np.ones((1, 2, 6, 6))
+    O1, L1 = oracle.forward(q, k, v, 0.5, False, bias=rows)
+    np.testing.assert_allclose(O1, O0, atol=1e-13)
+    np.testing.assert_allclose(L1 - L0, np.arange(6.0)[None, None, :] * np.ones((1, 2, 6)), atol=1e-13)
+    neg = np.where(np.arange(6)[None, :] > np.arange(6)[:, None], -np.inf, 0.0)[None, None]
+    Oc, Lc = oracle.forward(q, k, v, 0.5, True)
+    Ob, Lb = oracle.forward(q, k, v, 0.5, False, bias=neg)
+    np.testing.assert_allclose(Ob, Oc, atol=1e-13)
+    np.testing.assert_allclose(Lb, Lc, atol=1e-13)
+    slopes = [0.3, 0.05]
+    al = np.stack([oracle.alibi_bias(6, 6, s) for s in slopes])[None]
+    Oa, La = oracle.forward(q, k, v, 0.5, True, alibi_slopes=slopes)
+    Ot, Lt = oracle.forward(q, k, v, 0.5, True, bias=al)
+    np.testing.assert_allclose(Ot, Oa, atol=1e-13)
+    np.testing.assert_allclose(Lt, La, atol=1e-13)
+
+
+def test_bias_backward_matches_finite_differences():
+    rng = np.random.default_rng(5)
+    q, k, v, do = _rand(1, 2, 4, 3), _rand(1, 1, 5, 3), _rand(1, 1, 5, 3), _rand(1, 2, 4, 3)
+    bias = rng.standard_normal((1, 2, 4, 5))
+    dQ, dK, dV = oracle.backward(q, k, v, do, 0.7, True, bias=bias)
+
+    def loss(q_, k_, v_):
+        O, _ = oracle.forward(q_, k_, v_, 0.7, True, bias=bias)
+        return float((O * do).sum())
+    for which, got in ((0, dQ), (1, dK), (2, dV)):
+        args = [q.copy(), k.copy(), v.copy()]
+        x = args[which]
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            old = x[idx]
+            x[idx] = old + 1e-6
+            lp = loss(*args)
+            x[idx] = old - 1e-6
+            lm = loss(*args)
+            x[idx] = old
+            fd[idx] = (lp - lm) / 2e-6
+        assert np.linalg.norm(got - fd) / np.linalg.norm(fd) < 1e-6
