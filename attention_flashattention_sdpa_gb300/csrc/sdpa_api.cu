@@ -70,9 +70,17 @@ size_t widen_bytes(const sdpa_problem_t* p, size_t* off_k, size_t* off_v, size_t
   return p->in_dtype == SDPA_DTYPE_E4M3 ? 2 * nq + 2 * nkv : 0;
 }
 
+// Transposed bias copy of a backward pass: [1 or b][1 or h_q][s_kv][s_q rounded up to 128].
+size_t bias_t_bytes(const sdpa_problem_t* p) {
+  if (p->bias == nullptr) return 0;
+  const size_t nb = p->bias_strides.b == 0 ? 1 : p->b, nh = p->bias_strides.h == 0 ? 1 : p->h_q;
+  const size_t pad = (p->s_q + 127) / 128 * 128;
+  return (nb * nh * p->s_kv * pad * 2 + 255) & ~size_t(255);
+}
+
 size_t bwd_total_workspace(const sdpa_problem_t* p) {
   const size_t base = (sdpa::bwd_workspace_bytes(p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d) + 255) & ~size_t(255);
-  return base + widen_bytes(p, nullptr, nullptr, nullptr);
+  return base + widen_bytes(p, nullptr, nullptr, nullptr) + bias_t_bytes(p);
 }
 
 bool valid_dtype(int dt) {
@@ -187,6 +195,18 @@ sdpa_status_t check_problem(const sdpa_problem_t* p, bool backward) {
     return fail(SDPA_ERR_INVALID_ARG, "dropout_p must be in [0, 1), got %g", p->dropout_p);
   if (p->dropout_p > 0.f && p->in_dtype == SDPA_DTYPE_E4M3)
     return fail(SDPA_ERR_UNSUPPORTED, "dropout takes F16 or BF16 inputs, not E4M3");
+  if (p->bias != nullptr) {
+    const sdpa_strides_t& bs = p->bias_strides;
+    if (p->in_dtype == SDPA_DTYPE_E4M3)
+      return fail(SDPA_ERR_UNSUPPORTED, "a bias tensor takes F16 or BF16 inputs, not E4M3");
+    if (p->alibi) return fail(SDPA_ERR_UNSUPPORTED, "bias and alibi together: fold ALiBi into the bias");
+    if (reinterpret_cast<uintptr_t>(p->bias) % 16)
+      return fail(SDPA_ERR_LAYOUT, "bias must be 16-byte aligned");
+    if (bs.d != 1 && p->s_kv > 1) return fail(SDPA_ERR_LAYOUT, "bias: the key stride (d field) must be 1");
+    if (bs.b < 0 || bs.h < 0 || bs.s < 0 || bs.b % 8 || bs.h % 8 || bs.s % 8)
+      return fail(SDPA_ERR_LAYOUT, "bias: strides must be non-negative multiples of 8 elements");
+    if (p->s_q > 1 && bs.s < p->s_kv) return fail(SDPA_ERR_LAYOUT, "bias: row stride below s_kv");
+  }
   if (p->in_dtype == SDPA_DTYPE_E5M2 || p->out_dtype == SDPA_DTYPE_E5M2)
     return fail(SDPA_ERR_UNSUPPORTED, "E5M2 is accepted only as dout_dtype of an FP8 backward pass");
   if (p->in_dtype == SDPA_DTYPE_E4M3) {
@@ -298,6 +318,10 @@ sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const void* k, co
   prm.drop_scale = drop_scale_of(p);
   prm.drop_rows = p->dropout_p > 0.f ? p->dropout_mask : nullptr;
   prm.drop_kv_words = words_of(p->s_kv);
+  prm.bias = p->bias;
+  prm.bias_sb = p->bias_strides.b;
+  prm.bias_sh = p->bias_strides.h;
+  prm.bias_ss = p->bias_strides.s;
   const int rows_per_cta = 128 * sdpa::fwd_q_tiles(p->d, p->in_dtype);
   prm.num_m_blocks = (p->s_q + rows_per_cta - 1) / rows_per_cta;
   prm.scale_log2 = scale_log2_of(p->attn_scale);
@@ -367,6 +391,21 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
     prm.descale_k = p->descale_k;
     prm.descale_v = p->descale_v;
     prm.descale_do = p->descale_do;
+  }
+  if (p->bias != nullptr) {
+    // The compute threads own key rows: give them a transposed, dense copy of the bias.
+    const size_t base = (sdpa::bwd_workspace_bytes(p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d) + 255) & ~size_t(255);
+    uint8_t* bt = static_cast<uint8_t*>(workspace) + base + widen_bytes(p, nullptr, nullptr, nullptr);
+    prm.bias_nb = p->bias_strides.b == 0 ? 1 : p->b;
+    prm.bias_nh = p->bias_strides.h == 0 ? 1 : p->h_q;
+    // Causal without per-batch lengths: tiles that no query can see are left unwritten.
+    const int skip = p->causal != 0 && !p->seq_lens_q && !p->seq_lens_kv;
+    const int off = p->causal == 2 ? p->s_kv - p->s_q : 0;
+    cudaError_t e = sdpa::launch_bias_transpose(p->bias, p->bias_strides.b, p->bias_strides.h, p->bias_strides.s,
+                                                prm.bias_nb, prm.bias_nh, p->s_q, p->s_kv,
+                                                (p->s_q + 127) / 128 * 128, skip, off, bt, stream);
+    if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "bias transpose launch failed: %s", cudaGetErrorString(e));
+    prm.bias_t = bt;
   }
   // d = 256 walks 64-row query blocks (its kernel keeps only half of d of dK/dV in TMEM).
   const int q_rows = p->d == 256 ? 64 : 128;

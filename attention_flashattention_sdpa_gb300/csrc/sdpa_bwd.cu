@@ -100,6 +100,30 @@ __device__ __forceinline__ BwdScales bwd_scales(const BwdParams& p) {
   return s;
 }
 
+// 64 bias values of key row kv_row for queries q0..q0+63 from the transposed copy (zero for
+// a key row beyond s_kv, which sees nothing anyway).
+__device__ __forceinline__ void load_bias_t(const BwdParams& p, int bi, int hq, int kv_row, int q0, uint4 (&bz)[8]) {
+  if (kv_row >= p.s_kv) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) bz[e] = make_uint4(0u, 0u, 0u, 0u);
+    return;
+  }
+  const int nb = p.bias_nb > 1 ? bi : 0, nh = p.bias_nh > 1 ? hq : 0;
+  const uint4* src = reinterpret_cast<const uint4*>(
+      static_cast<const uint16_t*>(p.bias_t) +
+      ((static_cast<int64_t>(nb) * p.bias_nh + nh) * p.s_kv + kv_row) * p.s_q_pad + q0);
+#pragma unroll
+  for (int e = 0; e < 8; ++e) bz[e] = __ldg(src + e);
+}
+
+// Columns c, c+1 of eight packed 16-bit bias vectors, as fp32.
+template <int DT>
+__device__ __forceinline__ float2 bias_pair(const uint4 (&bz)[8], int c) {
+  const uint4 v = bz[c / 8];
+  const uint32_t w = (c % 8 == 0) ? v.x : (c % 8 == 2) ? v.y : (c % 8 == 4) ? v.z : v.w;
+  return unpack2(w, DT);
+}
+
 // One group of D/8 threads per row; each thread reads 8 elements (16 bytes) of O and dO.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
@@ -272,6 +296,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   using C = BwdCfg<D>;
   constexpr bool ALIBI = (FEAT & kFeatAlibi) != 0;
   constexpr bool DROP = (FEAT & kFeatDropout) != 0;
+  constexpr bool BIAS = (FEAT & kFeatBias) != 0;
   extern __shared__ __align__(1024) uint8_t smem[];
   BwdBarriers& bars = *reinterpret_cast<BwdBarriers*>(smem + C::OFF_BAR);
   uint8_t* sK = smem + C::OFF_K;
@@ -504,6 +529,9 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         keep = __ldg(reinterpret_cast<const uint2*>(
             p.drop_cols + ((static_cast<int64_t>(bi) * p.h_q + iter_head(n)) * p.s_kv + kv_row) * p.drop_q_words +
             q0 / 32));
+      // Additive bias of this key row for the 64 query columns (transposed copy).
+      uint4 bz[BIAS ? 8 : 1];
+      if constexpr (BIAS) load_bias_t(p, bi, iter_head(n), kv_row, q0, bz);
       const float* nlse2 = sVec + (b * 2 + 0) * 128 + 64 * h;    // -LSE·log2 e per column
       const float* ndelta = sVec + (b * 2 + 1) * 128 + 64 * h;   // -Delta per column
       // Pᵀ = exp2(Sᵀ·scale·log2e − LSE·log2e), masked where key > query
@@ -530,6 +558,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       for (int c = 0; c < 64; c += 2) {
         float2 nl = *reinterpret_cast<const float2*>(nlse2 + c);
         if constexpr (ALIBI) nl = add2(nl, kr2);
+        if constexpr (BIAS) nl = fma2(bias_pair<DT>(bz, c), make_float2(kLog2e, kLog2e), nl);
         const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl);
         // A fixed share of the pairs is computed on the FMA pipe, the rest on the MUFU unit.
         const bool poly = kPolyEvery > 0 && (c / 2) % (kPolyEvery > 0 ? kPolyEvery : 1) == kPolyEvery - 1;
@@ -779,6 +808,7 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
   using C = D256;
   constexpr bool ALIBI = (FEAT & kFeatAlibi) != 0;
   constexpr bool DROP = (FEAT & kFeatDropout) != 0;
+  constexpr bool BIAS = (FEAT & kFeatBias) != 0;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) atomicOr(&g_device_error, kErrSmemAlign);
@@ -903,11 +933,14 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
         keep = __ldg(reinterpret_cast<const uint2*>(
             p.drop_cols + ((static_cast<int64_t>(bi) * p.h_q + hq) * p.s_kv + kv_row) * p.drop_q_words + q0 / 32));
       const float2 rk2 = make_float2(bs.dp, bs.dp);
+      uint4 bz[BIAS ? 8 : 1];
+      if constexpr (BIAS) load_bias_t(p, bi, hq, kv_row, q0, bz);
       uint32_t pk[32], ds[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
         float2 nl = *reinterpret_cast<const float2*>(sVec + c);
         if constexpr (ALIBI) nl = add2(nl, kr2);
+        if constexpr (BIAS) nl = fma2(bias_pair<DT>(bz, c), make_float2(kLog2e, kLog2e), nl);
         const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl);
         float p0 = ex2(x.x), p1 = ex2(x.y);
         if (need_mask) {
@@ -1102,11 +1135,13 @@ cudaError_t launch_d256(const BwdParams& p, cudaStream_t st) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  const int feat = (p.alibi ? kFeatAlibi : 0) | (p.drop_cols ? kFeatDropout : 0);
+  const int feat = (p.alibi ? kFeatAlibi : 0) | (p.drop_cols ? kFeatDropout : 0) | (p.bias_t ? kFeatBias : 0);
   auto kern = bwd_d256_kernel<DT, 0>;
   if (feat == kFeatAlibi) kern = bwd_d256_kernel<DT, kFeatAlibi>;
   if (feat == kFeatDropout) kern = bwd_d256_kernel<DT, kFeatDropout>;
   if (feat == (kFeatAlibi | kFeatDropout)) kern = bwd_d256_kernel<DT, kFeatAlibi | kFeatDropout>;
+  if (feat == kFeatBias) kern = bwd_d256_kernel<DT, kFeatBias>;
+  if (feat == (kFeatBias | kFeatDropout)) kern = bwd_d256_kernel<DT, kFeatBias | kFeatDropout>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, D256::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const unsigned grid = 2u * p.b * p.h_kv * p.kv_split * ((p.s_kv + kBlockN - 1) / kBlockN);
@@ -1137,11 +1172,13 @@ cudaError_t launch_t(const BwdParams& p, cudaStream_t st) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  const int feat = (p.alibi ? kFeatAlibi : 0) | (p.drop_cols ? kFeatDropout : 0);
+  const int feat = (p.alibi ? kFeatAlibi : 0) | (p.drop_cols ? kFeatDropout : 0) | (p.bias_t ? kFeatBias : 0);
   auto kern = bwd_main_kernel<D, DT, 0>;
   if (feat == kFeatAlibi) kern = bwd_main_kernel<D, DT, kFeatAlibi>;
   if (feat == kFeatDropout) kern = bwd_main_kernel<D, DT, kFeatDropout>;
   if (feat == (kFeatAlibi | kFeatDropout)) kern = bwd_main_kernel<D, DT, kFeatAlibi | kFeatDropout>;
+  if (feat == kFeatBias) kern = bwd_main_kernel<D, DT, kFeatBias>;
+  if (feat == (kFeatBias | kFeatDropout)) kern = bwd_main_kernel<D, DT, kFeatBias | kFeatDropout>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const unsigned gmain = static_cast<unsigned>(p.b) * p.h_kv * p.kv_split * ((p.s_kv + kBlockN - 1) / kBlockN);
@@ -1233,6 +1270,62 @@ __global__ void __launch_bounds__(256) fp8_widen_kernel(const uint8_t* src, int6
 }
 
 }  // namespace
+
+namespace {
+
+// [nb][nh][s_q][s_kv] (strided, 16-bit) -> [nb][nh][s_kv][s_q_pad] (dense) through 64 x 64
+// shared-memory tiles, 16-byte loads and stores; padded query columns get zeros.  With
+// skip_above, tiles whose keys all lie beyond every query's causal limit (key > query +
+// diag_off) are not written: the backward pass never reads them.
+__global__ void __launch_bounds__(256) bias_transpose_kernel(const uint16_t* src, int64_t sb, int64_t sh,
+                                                             int64_t ss, int nh, int s_q, int s_kv, int s_q_pad,
+                                                             int skip_above, int diag_off, uint16_t* dst) {
+  __shared__ uint16_t tile[64][72];   // [query][key], rows padded against bank conflicts
+  const int z = blockIdx.z;
+  const int nbi = z / nh, nhi = z % nh;
+  const int i0 = blockIdx.x * 64, j0 = blockIdx.y * 64;
+  if (skip_above && j0 > i0 + 63 + diag_off) return;
+  const uint16_t* s = src + nbi * sb + nhi * sh;
+  for (int t = threadIdx.x; t < 512; t += 256) {   // 64 query rows x 8 chunks of 8 keys
+    const int r = t / 8, c = t % 8;
+    const int i = i0 + r, j = j0 + 8 * c;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (i < s_q) {
+      const uint16_t* row = s + static_cast<int64_t>(i) * ss + j;
+      if (j + 8 <= s_kv) {
+        v = __ldg(reinterpret_cast<const uint4*>(row));
+      } else {
+        uint32_t h[4] = {0u, 0u, 0u, 0u};
+        for (int u = 0; u < 8 && j + u < s_kv; ++u) h[u / 2] |= static_cast<uint32_t>(row[u]) << (16 * (u % 2));
+        v = make_uint4(h[0], h[1], h[2], h[3]);
+      }
+    }
+    *reinterpret_cast<uint4*>(&tile[r][8 * c]) = v;
+  }
+  __syncthreads();
+  uint16_t* d = dst + static_cast<int64_t>(z) * s_kv * s_q_pad;
+  for (int t = threadIdx.x; t < 512; t += 256) {   // 64 key rows x 8 chunks of 8 queries
+    const int r = t / 8, c = t % 8;
+    const int j = j0 + r, i = i0 + 8 * c;
+    if (j >= s_kv || i >= s_q_pad) continue;
+    uint32_t h[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      h[u] = static_cast<uint32_t>(tile[8 * c + 2 * u][r]) | (static_cast<uint32_t>(tile[8 * c + 2 * u + 1][r]) << 16);
+    *reinterpret_cast<uint4*>(d + static_cast<int64_t>(j) * s_q_pad + i) = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_bias_transpose(const void* src, int64_t sb, int64_t sh, int64_t ss, int nb, int nh,
+                                  int s_q, int s_kv, int s_q_pad, int skip_above, int diag_off, void* dst,
+                                  cudaStream_t st) {
+  dim3 grid((s_q_pad + 63) / 64, (s_kv + 63) / 64, nb * nh);
+  bias_transpose_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(src), sb, sh, ss, nh, s_q, s_kv,
+                                              s_q_pad, skip_above, diag_off, static_cast<uint16_t*>(dst));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_fp8_widen(const void* src, int64_t sb, int64_t sh, int64_t ss, int b, int h, int s,
                              int d, int src_e5m2, void* dst, int dst_dtype, cudaStream_t st) {

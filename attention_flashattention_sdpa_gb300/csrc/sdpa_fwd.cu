@@ -34,6 +34,12 @@ using namespace ptx;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
+// Two 16-bit values (F16 or BF16) of a 32-bit word as fp32.
+__device__ __forceinline__ float2 unpack16x2(uint32_t w, int dt) {
+  if (dt == kBF16) return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+  return __half22float2(*reinterpret_cast<const __half2*>(&w));
+}
+
 template <int D, int DT>
 struct FwdCfg {
   static constexpr int ES = (DT == kE4M3) ? 1 : 2;               // input element bytes
@@ -110,6 +116,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
   using C = FwdCfg<D, DT>;
   constexpr bool ALIBI = (FEAT & kFeatAlibi) != 0;
   constexpr bool DROP = (FEAT & kFeatDropout) != 0;
+  constexpr bool BIAS = (FEAT & kFeatBias) != 0;
   constexpr int NQT = C::NQT;
   constexpr int NS = C::NS;
   constexpr bool FP8 = (DT == kE4M3);
@@ -337,6 +344,11 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       c_scale *= __ldg(p.descale_q) * __ldg(p.descale_k);
       v_scale = __ldg(p.descale_v);
     }
+    // Additive bias: this row of the bias tensor (16-bit, 16-byte aligned rows).
+    const uint16_t* bias_row = nullptr;
+    if (BIAS && q_row < p.s_q)
+      bias_row = static_cast<const uint16_t*>(p.bias) + bi * p.bias_sb + hq * p.bias_sh +
+                 static_cast<int64_t>(q_row) * p.bias_ss;
     // Dropout: this row's keep bits (4 words per key block); kept P are scaled at the end.
     const uint4* drop_row = nullptr;
     if (DROP) {
@@ -364,6 +376,23 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       const uint32_t ph = (NQT == 2) ? (j & 1) : ((j >> 1) & 1);
       uint4 keep = make_uint4(0u, 0u, 0u, 0u);
       if (DROP && drop_row != nullptr) keep = __ldg(drop_row + kv_block(j));
+      // The bias of this row and key block, loaded before the scores arrive.
+      uint4 bz[BIAS ? 16 : 1];
+      if constexpr (BIAS) {
+        const int kb0 = kv_block(j) * kBlockN;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+          const int k0 = kb0 + 8 * e;
+          if (bias_row != nullptr && k0 + 8 <= p.s_kv) {
+            bz[e] = __ldg(reinterpret_cast<const uint4*>(bias_row + k0));
+          } else {
+            uint32_t h[4] = {0u, 0u, 0u, 0u};
+            for (int u = 0; bias_row != nullptr && u < 8 && k0 + u < p.s_kv; ++u)
+              h[u / 2] |= static_cast<uint32_t>(bias_row[k0 + u]) << (16 * (u % 2));
+            bz[e] = make_uint4(h[0], h[1], h[2], h[3]);
+          }
+        }
+      }
       if (!mbar_wait_warp(&bars.s_full[slot], ph, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint32_t s_addr = tmem + lane_off + slot * 128;
@@ -383,6 +412,19 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
 #pragma unroll
         for (int c = 0; c < kBlockN; ++c)
           if (c > lim) sv[c] = __float_as_uint(-INFINITY);
+      }
+      if constexpr (BIAS) {
+        // y = s * |scale| + bias in natural-log units; the max and the exponent scale by log2 e.
+        const float2 sn2 = make_float2(c_scale / kLog2e, c_scale / kLog2e);
+#pragma unroll
+        for (int c = 0; c < kBlockN; c += 2) {
+          const uint32_t w = (c % 8 == 0) ? bz[c / 8].x : (c % 8 == 2) ? bz[c / 8].y
+                           : (c % 8 == 4) ? bz[c / 8].z : bz[c / 8].w;
+          const float2 y = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sn2,
+                                unpack16x2(w, DT));
+          sv[c] = __float_as_uint(y.x);
+          sv[c + 1] = __float_as_uint(y.y);
+        }
       }
       if constexpr (ALIBI) {
         // ALiBi splits slope * (key - row - off) into a column part slope * c and a row part
@@ -405,7 +447,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       const float mx = max3(mx0, mx1, fmaxf(mx2, mx3));
       // ALiBi row part of this key block: slope * (kv0 - q_row - off).
       const float row_bias = ALIBI ? sl2 * static_cast<float>(kv0 - q_row - L.off) : 0.f;
-      const float m_cand = ALIBI ? sl2 * mx + row_bias : mx * c_scale;
+      const float m_cand = ALIBI ? sl2 * mx + row_bias : BIAS ? mx * kLog2e : mx * c_scale;
       float alpha = 1.f;
       if (m_cand > m_ref + C::THRESH) {
         alpha = ex2(m_ref - m_cand);
@@ -415,7 +457,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       const float neg_m = (m_ref == -INFINITY) ? 0.f : C::P_OFFSET - m_ref;
 
       // x = s * scale - m in pairs; P = 2^x; row sums in pairs.
-      const float cs = ALIBI ? sl2 : c_scale;   // with ALiBi the scores are carried as u
+      const float cs = ALIBI ? sl2 : BIAS ? kLog2e : c_scale;   // ALiBi: scores carried as u
       const float nm = ALIBI ? neg_m + row_bias : neg_m;
       const float2 cs2 = make_float2(cs, cs);
       const float2 nm2 = make_float2(nm, nm);
@@ -537,10 +579,12 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t st) {
   using C = FwdCfg<D, DT>;
   auto kern = sdpa_fwd_kernel<D, DT, OUT_DT, 0>;
   if constexpr (DT != kE4M3) {
-    const int feat = (p.alibi ? kFeatAlibi : 0) | (p.drop_rows ? kFeatDropout : 0);
+    const int feat = (p.alibi ? kFeatAlibi : 0) | (p.drop_rows ? kFeatDropout : 0) | (p.bias ? kFeatBias : 0);
     if (feat == kFeatAlibi) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatAlibi>;
     if (feat == kFeatDropout) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatDropout>;
     if (feat == (kFeatAlibi | kFeatDropout)) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatAlibi | kFeatDropout>;
+    if (feat == kFeatBias) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatBias>;
+    if (feat == (kFeatBias | kFeatDropout)) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatBias | kFeatDropout>;
   }
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM_BYTES);

@@ -34,6 +34,8 @@ struct FwdParams {
   const uint32_t* drop_rows;  // dropout keep bits [b*h_q][s_q][drop_kv_words], or nullptr
   int drop_kv_words;          // 32-bit words per row: ceil(s_kv / 128) * 4
   float drop_scale;           // 1 / (1 - p), or 1 without dropout
+  const void* bias;           // additive bias [b][h_q][s_q][s_kv] (input dtype), or nullptr
+  int64_t bias_sb, bias_sh, bias_ss;   // element strides (0 broadcasts b or h)
 };
 
 // Number of Q tiles (of 128 rows) one forward CTA processes.
@@ -88,7 +90,16 @@ struct BwdParams {
   const float* descale_k;
   const float* descale_v;
   const float* descale_do;
+  // Additive bias, transposed into the workspace: [bias_nb][bias_nh][s_kv][s_q_pad] in the
+  // input dtype (bias_nb = 1 or b, bias_nh = 1 or h_q), or nullptr.
+  const void* bias_t;
+  int bias_nb, bias_nh;
 };
+
+// Transposes a strided [nb][nh][s_q][s_kv] bias view into dense [nb][nh][s_kv][s_q_pad].
+cudaError_t launch_bias_transpose(const void* src, int64_t sb, int64_t sh, int64_t ss, int nb, int nh,
+                                  int s_q, int s_kv, int s_q_pad, int skip_above, int diag_off, void* dst,
+                                  cudaStream_t st);
 
 // Widens a strided FP8 (E4M3 or E5M2) [b][h][s][d] view into a dense F16 or BF16 copy.  Every
 // FP8 value is exact in either 16-bit format; descales are applied later, by the kernels.
@@ -120,6 +131,7 @@ uint32_t bwd_take_device_error();
 // Kernel feature bits (compile-time variants of the forward and backward kernels).
 constexpr int kFeatAlibi = 1;
 constexpr int kFeatDropout = 2;
+constexpr int kFeatBias = 4;
 
 }  // namespace sdpa
 

@@ -504,6 +504,9 @@ def sweep_one(w, peaks, args):
         torch.cuda.synchronize()
         mask_ms = a.elapsed_time(b_)
         kw["dropout_p"], kw["dropout_mask"] = w.dropout, mask
+    if w.bias:
+        g = torch.Generator(device="cuda").manual_seed(3)
+        kw["bias"] = torch.randn(1, w.h_q, w.s_q, w.s_kv, device="cuda", generator=g).to(q.dtype)
     fwd = lambda: sdpa.sdpa_fwd(q, k, v, o, lse, attn_scale=w.scale, causal=w.causal, alibi=w.alibi,
                                 **kw)
     reps = max(5, min(200, int(2e13 / max(w.fwd_flops(), 1))))
@@ -532,13 +535,16 @@ def sweep_one(w, peaks, args):
     if w.backward:
         do = dev(x.do)
         dkw = {} if w.dropout == 0 else {"dropout_p": w.dropout, "dropout_mask_t": mask_t}
+        if w.bias:
+            dkw["bias"] = kw["bias"]
         if w.dtype == "e4m3":   # E4M3 Q, K, V and E5M2 dO; O and the gradients in bf16
             dkw.update(kw)
             dkw["descale_do"] = torch.tensor([x.descale_do], device="cuda")
         dq, dk, dv = (torch.empty(t.shape, dtype=odt, device="cuda") for t in (q, k, v))
         p = sdpa.make_problem(q, k, v, o, attn_scale=w.scale, causal=w.causal, dout=do, dq=dq, dk=dk, dv=dv,
                               descale_q=dkw.get("descale_q"), descale_k=dkw.get("descale_k"),
-                              descale_v=dkw.get("descale_v"), descale_do=dkw.get("descale_do"))
+                              descale_v=dkw.get("descale_v"), descale_do=dkw.get("descale_do"),
+                              bias=dkw.get("bias"))
         ws = torch.empty(sdpa.sdpa_workspace_size(p, True), dtype=torch.uint8, device="cuda")
         bwd = lambda: sdpa.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, attn_scale=w.scale, causal=w.causal,
                                     alibi=w.alibi, **dkw)

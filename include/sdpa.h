@@ -130,6 +130,16 @@ typedef struct {
    * descales folded into the kernels' scale factors; the MMAs run at 16-bit precision. */
   int32_t dout_dtype;
   const float* descale_do;
+  /* Additive bias (the SDPA node's bias input, cuDNN 9 blog walkthrough).  NULL = none; else
+   * a DEVICE pointer to a logical [b][h_q][s_q][s_kv] tensor of in_dtype (F16/BF16) whose
+   * element strides are bias_strides (b, h, s, and d = the key stride, which must be 1); a
+   * zero b or h stride broadcasts one slice over the batch or the heads.  The bias is added
+   * to the scaled scores before the mask and softmax and is treated as a constant (no
+   * gradient is produced).  Base 16-byte aligned; non-zero b/h/s strides multiples of 8.
+   * Not combined with alibi (fold ALiBi into the tensor instead).  A backward pass with a
+   * bias needs workspace for a transposed copy (sdpa_workspace_size accounts for it). */
+  const void* bias;
+  sdpa_strides_t bias_strides;
 } sdpa_problem_t;
 
 /*

@@ -51,6 +51,7 @@ class Workload:
     attn_scale: Optional[float] = None
     alibi: bool = False   # ALiBi position bias with the default slopes
     dropout: float = 0.0  # dropout probability (0 = off)
+    bias: bool = False    # an additive [1, h_q, s_q, s_kv] bias in the input dtype
 
     @property
     def scale(self) -> float:
@@ -112,11 +113,18 @@ def training_fp8(s: int) -> Workload:
                     causal=True, backward=True)
 
 
+def training_bias(s: int) -> Workload:
+    """The training workload with a per-head additive bias broadcast over the batch."""
+    w = training(s)
+    return Workload(f"training_bias_bf16_causal_d128_s{s}", w.b, w.h_q, w.h_kv, s, s, w.d, w.dtype,
+                    causal=True, backward=True, bias=True)
+
+
 def all_workloads():
     out = [tiny(False), tiny(True), gpt2_inference()]
     out += [training(s) for s in TRAINING_SEQ_LENS]
     out += [fp8_large_head(), grouped(8), grouped(1), grouped(64), training_alibi(8192),
-            training_dropout(8192), training_fp8(8192)]
+            training_dropout(8192), training_fp8(8192), training_bias(8192)]
     return out
 
 

@@ -40,6 +40,11 @@ def test_struct_layout_and_version(m):
 
 
 def _problem(m, **over):
+    if "bias_strides" in over:   # a tuple, or None for a zero (invalid) stride set
+        bst = over.pop("bias_strides")
+        over["bias_strides"] = m.Strides(*(bst or (0, 0, 0, 0)))
+    elif "bias" in over:
+        over["bias_strides"] = m.Strides(0, 128 * 128, 128, 1)
     p = m.Problem()
     p.b, p.h_q, p.h_kv, p.s_q, p.s_kv, p.d = 1, 2, 2, 128, 128, 64
     p.in_dtype = p.out_dtype = m.DTYPE_F16
@@ -83,6 +88,11 @@ def _bwd(m, p, ws=FAKE, ws_bytes=1 << 40, lse=FAKE, q=FAKE):
     (dict(in_dtype=2, out_dtype=1), 2, "d = 128 or 256"),
     (dict(in_dtype=2, out_dtype=2), 2, "output"),
     (dict(alibi=2), 1, "alibi"),
+    (dict(bias=FAKE + 8), 3, "bias"),
+    (dict(bias=FAKE, alibi=1), 2, "alibi"),
+    (dict(bias=FAKE, bias_strides=None), 3, "key stride"),
+    (dict(bias=FAKE, bias_strides=(0, 0, 130, 1)), 3, "multiples of 8"),
+    (dict(bias=FAKE, bias_strides=(0, 0, 120, 1)), 3, "row stride"),
     (dict(dropout_p=-0.1), 1, "dropout_p"),
     (dict(dropout_p=1.0), 1, "dropout_p"),
     (dict(dropout_p=float("nan")), 1, "dropout_p"),
@@ -189,3 +199,10 @@ def test_dropout_mask_sizes_and_validation(m):
 def test_backward_dropout_needs_the_transposed_mask(m):
     p = _problem(m, dropout_p=0.2, dropout_mask=FAKE)
     assert _bwd(m, p) == 1 and "dropout_mask_t" in m.sdpa_last_error_string()
+
+
+def test_bias_workspace_holds_a_transposed_copy(m):
+    base = m.sdpa_workspace_size(_problem(m), True)
+    with_bias = m.sdpa_workspace_size(_problem(m, bias=FAKE), True)   # [1, h_q, 128, 128] bf16
+    assert with_bias - base == 2 * 128 * 128 * 2
+    assert m.sdpa_workspace_size(_problem(m, bias=FAKE), False) == 0
