@@ -1142,7 +1142,7 @@ cudaError_t launch_d256(const BwdParams& p, cudaStream_t st) {
   if (feat == (kFeatAlibi | kFeatDropout)) kern = bwd_d256_kernel<DT, kFeatAlibi | kFeatDropout>;
   if (feat == kFeatBias) kern = bwd_d256_kernel<DT, kFeatBias>;
   if (feat == (kFeatBias | kFeatDropout)) kern = bwd_d256_kernel<DT, kFeatBias | kFeatDropout>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, D256::SMEM_BYTES);
+  e = set_smem_once(reinterpret_cast<const void*>(kern), D256::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const unsigned grid = 2u * p.b * p.h_kv * p.kv_split * ((p.s_kv + kBlockN - 1) / kBlockN);
   kern<<<grid, 128, D256::SMEM_BYTES, st>>>(p);
@@ -1179,7 +1179,7 @@ cudaError_t launch_t(const BwdParams& p, cudaStream_t st) {
   if (feat == (kFeatAlibi | kFeatDropout)) kern = bwd_main_kernel<D, DT, kFeatAlibi | kFeatDropout>;
   if (feat == kFeatBias) kern = bwd_main_kernel<D, DT, kFeatBias>;
   if (feat == (kFeatBias | kFeatDropout)) kern = bwd_main_kernel<D, DT, kFeatBias | kFeatDropout>;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  e = set_smem_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const unsigned gmain = static_cast<unsigned>(p.b) * p.h_kv * p.kv_split * ((p.s_kv + kBlockN - 1) / kBlockN);
   kern<<<gmain, C::THREADS, C::SMEM_BYTES, st>>>(p);

@@ -586,8 +586,7 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t st) {
     if (feat == kFeatBias) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatBias>;
     if (feat == (kFeatBias | kFeatDropout)) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatBias | kFeatDropout>;
   }
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM_BYTES);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.b) * p.h_q * p.num_m_blocks;
   kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(p);

@@ -5,6 +5,10 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+#include <set>
+#include <utility>
+
 namespace sdpa {
 
 constexpr int kBlockM = 128;  // query rows per Q tile (one TMEM lane per row)
@@ -127,6 +131,22 @@ int bwd_kv_split(int b, int h_q, int h_kv, int s_kv);
 size_t bwd_workspace_bytes(int b, int h_q, int h_kv, int s_q, int s_kv, int d);
 cudaError_t launch_bwd(const BwdParams& p, int dtype, cudaStream_t st);
 uint32_t bwd_take_device_error();
+
+// Raises a kernel's dynamic shared-memory limit once per (kernel, device): the setting lasts
+// for the process, and the call costs microseconds that small problems would otherwise pay
+// on every launch.
+inline cudaError_t set_smem_once(const void* kern, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({kern, dev})) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({kern, dev});
+  return e;
+}
 
 // Kernel feature bits (compile-time variants of the forward and backward kernels).
 constexpr int kFeatAlibi = 1;

@@ -473,6 +473,32 @@ def run_sweep(args):
     return 0
 
 
+def graph_ms(fn, calls: int, reps: int = 10) -> float:
+    """Device time of one `fn()` from CUDA-graph replays of `calls` back-to-back calls: no
+    host work (argument marshalling, tensor-map encoding) between kernels, so small problems
+    show their kernels' time rather than the host's.  Median over `reps` replays."""
+    import torch
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        fn()                                  # warm-up on the capture stream
+    torch.cuda.current_stream().wait_stream(st)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(calls):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(); g.replay(); b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b) / calls)
+    return statistics.median(ts)
+
+
 def sweep_one(w, peaks, args):
     import torch
     import attention_flashattention_sdpa_gb300 as sdpa
@@ -522,6 +548,10 @@ def sweep_one(w, peaks, args):
     fwd_ms = statistics.median(a.elapsed_time(b) for a, b in ts)
     peak = peaks["bf16_tflops"]
     line = {"workload": w.name, "fwd_ms": fwd_ms, "fwd_tflops": w.fwd_flops() / fwd_ms / 1e9}
+    calls = max(4, min(64, int(2e12 / max(w.fwd_flops(), 1))))
+    gms = graph_ms(fwd, calls)
+    line["fwd_ms_graph"] = gms
+    line["fwd_tflops_graph"] = w.fwd_flops() / gms / 1e9
     if mask_ms is not None:
         line["dropout_mask_ms"] = mask_ms
     es = 1 if w.dtype == "e4m3" else 2
@@ -559,6 +589,9 @@ def sweep_one(w, peaks, args):
         torch.cuda.synchronize()
         bwd_ms = statistics.median(a.elapsed_time(b) for a, b in ts)
         line["bwd_ms"] = bwd_ms
+        gb = graph_ms(bwd, max(2, calls // 2))
+        line["bwd_ms_graph"] = gb
+        line["bwd_tflops_graph"] = w.bwd_flops() / gb / 1e9
         line["bwd_tflops"] = w.bwd_flops() / bwd_ms / 1e9
         line["fwdbwd_tflops"] = (w.fwd_flops() + w.bwd_flops()) / (fwd_ms + bwd_ms) / 1e9
         line["fwdbwd_frac_of_bf16_peak"] = line["fwdbwd_tflops"] / peak
