@@ -38,7 +38,8 @@ module's own table and multiplied by their descale):
   8 heads), applied by the same formula to any head count;
 * an additive bias (the SDPA node's bias input in the cuDNN 9 blog's walkthrough): a tensor
   [b or 1, h_q or 1, s_q, s_kv] added to the scaled scores before the mask and the softmax
-  (broadcast over a batch or head dimension of size 1); it is an input without gradient;
+  (broadcast over a batch or head dimension of size 1).  Its gradient is dS = ∂L/∂S, the
+  gradient of the scores after the scale, summed over the broadcast dimensions;
 * dropout (the SDPA node's dropout option in the cuDNN 9 blog's walkthrough, named and not
   defined): after the softmax each probability is kept with a keep mask Z and the kept ones
   are scaled by 1/(1 - p), so O = (P * Z) V / (1 - p); the LSE is that of the undropped
@@ -68,7 +69,7 @@ from typing import Iterable, Sequence, Tuple
 import numpy as np
 
 __all__ = [
-    "philox4x64", "dropout_threshold", "dropout_keep",
+    "philox4x64", "dropout_threshold", "dropout_keep", "bias_gradient",
     "visible_mask", "kv_head_of", "alibi_default_slopes", "alibi_bias", "head_forward", "forward", "forward_rows",
     "backward", "backward_dq_rows", "backward_kv_rows", "backward_kv_head", "e4m3_decode_table",
     "decode_e4m3", "e5m2_decode_table", "decode_e5m2", "to_f64",
@@ -363,7 +364,7 @@ def _head_backward(qh, kh, vh, doh, scale, mask, allow_empty=False, bias=None, z
     dS = P * (dP - delta[:, None])
     dQ = scale * (dS @ kh)
     dK = scale * (dS.T @ qh)
-    return dQ, dK, dV
+    return dQ, dK, dV, dS
 
 
 def backward(q, k, v, do, scale: float, causal: bool, seq_lens_q=None, seq_lens_kv=None,
@@ -385,13 +386,35 @@ def backward(q, k, v, do, scale: float, causal: bool, seq_lens_q=None, seq_lens_
         for hq in range(h_q):
             hk = kv_head_of(hq, h_q, h_kv)
             term = _bias_of(bias, alibi_slopes, s_q, s_kv, bi, hq, off)
-            gq, gk, gv = _head_backward(q[bi, hq], k[bi, hk], v[bi, hk], do[bi, hq], scale, mask,
-                                        allow_empty=varlen, bias=term,
-                                        zdrop=_zdrop(keep, dropout_p, bi, hq))
+            gq, gk, gv, _ = _head_backward(q[bi, hq], k[bi, hk], v[bi, hk], do[bi, hq], scale, mask,
+                                           allow_empty=varlen, bias=term,
+                                           zdrop=_zdrop(keep, dropout_p, bi, hq))
             dQ[bi, hq] = gq
             dK[bi, hk] += gk
             dV[bi, hk] += gv
     return dQ, dK, dV
+
+
+def bias_gradient(q, k, v, do, scale: float, causal: bool, bias, seq_lens_q=None, seq_lens_kv=None,
+                  bottom_right: bool = False, dropout_p: float = 0.0, keep=None):
+    """dL/dbias with the bias's shape [b|1, h_q|1, s_q, s_kv]: dS of every (batch, head),
+    summed over the broadcast dimensions."""
+    b, h_q, s_q, _ = q.shape
+    h_kv, s_kv = k.shape[1], k.shape[2]
+    t = np.asarray(bias, dtype=np.float64)
+    out = np.zeros(t.shape, dtype=np.float64)
+    varlen = seq_lens_q is not None or seq_lens_kv is not None or bottom_right
+    for bi in range(b):
+        mask = _batch_mask(s_q, s_kv, causal, bi, seq_lens_q, seq_lens_kv, bottom_right)
+        off = _batch_off(s_q, s_kv, bi, seq_lens_q, seq_lens_kv, bottom_right)
+        for hq in range(h_q):
+            hk = kv_head_of(hq, h_q, h_kv)
+            term = _bias_of(t, None, s_q, s_kv, bi, hq, off)
+            _, _, _, dS = _head_backward(q[bi, hq], k[bi, hk], v[bi, hk], do[bi, hq], scale, mask,
+                                         allow_empty=varlen, bias=term,
+                                         zdrop=_zdrop(keep, dropout_p, bi, hq))
+            out[bi if t.shape[0] > 1 else 0, hq if t.shape[1] > 1 else 0] += dS
+    return out
 
 
 def backward_dq_rows(q_rows, do_rows, rows: Sequence[int], kh, vh, scale: float, causal: bool):

@@ -681,3 +681,24 @@ def test_bias_backward_matches_finite_differences():
             x[idx] = old
             fd[idx] = (lp - lm) / 2e-6
         assert np.linalg.norm(got - fd) / np.linalg.norm(fd) < 1e-6
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 4, 5), (1, 1, 4, 5)])
+def test_bias_gradient_finite_differences_and_row_sums(shape):
+    """dL/dbias against central differences of L = sum(O * dO), for a per-head and a fully
+    broadcast bias; each row of dS sums to zero (sum_j P_ij (dP_ij - Delta_i) = 0)."""
+    rng = np.random.default_rng(21)
+    q, k, v, do = _rand(1, 2, 4, 3), _rand(1, 2, 5, 3), _rand(1, 2, 5, 3), _rand(1, 2, 4, 3)
+    bias = rng.standard_normal(shape)
+    g = oracle.bias_gradient(q, k, v, do, 0.8, False, bias)
+    assert g.shape == bias.shape
+    fd = np.zeros_like(bias)
+    for idx in np.ndindex(bias.shape):
+        bp, bm = bias.copy(), bias.copy()
+        bp[idx] += 1e-6
+        bm[idx] -= 1e-6
+        lp = float((oracle.forward(q, k, v, 0.8, False, bias=bp)[0] * do).sum())
+        lm = float((oracle.forward(q, k, v, 0.8, False, bias=bm)[0] * do).sum())
+        fd[idx] = (lp - lm) / 2e-6
+    assert np.linalg.norm(g - fd) / np.linalg.norm(fd) < 1e-6
+    np.testing.assert_allclose(g.sum(axis=-1), 0.0, atol=1e-12)

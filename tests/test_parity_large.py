@@ -77,6 +77,12 @@ def _full_case(w, dkv_pairs: int):
     return x, dq, dk, dv
 
 
+@pytest.mark.parametrize("s", [512, 1024, 2048, 4096])
+def test_training_sweep_lengths(s):
+    """The rest of the training sweep (b2 h16 d128 bf16 causal), as the sweep launches it."""
+    _full_case(training(s), dkv_pairs=2)
+
+
 def test_training_s8192_as_benchmarked():
     _full_case(training(8192), dkv_pairs=2)
 
