@@ -60,6 +60,7 @@ class Problem(ctypes.Structure):
         ("dropout_mask_t", ctypes.c_void_p),
         ("dout_dtype", ctypes.c_int32), ("descale_do", ctypes.c_void_p),
         ("bias", ctypes.c_void_p), ("bias_strides", Strides),
+        ("dbias", ctypes.c_void_p), ("dbias_strides", Strides),
     ]
 
 
@@ -144,7 +145,7 @@ def make_problem(q, k, v, o=None, *, attn_scale: Optional[float] = None, causal=
                  dout=None, dq=None, dk=None, dv=None, descale_q=None, descale_k=None,
                  descale_v=None, seq_lens_q=None, seq_lens_kv=None, alibi=False,
                  alibi_slopes=None, dropout_p: float = 0.0, dropout_mask=None,
-                 dropout_mask_t=None, descale_do=None, bias=None) -> Problem:
+                 dropout_mask_t=None, descale_do=None, bias=None, dbias=None) -> Problem:
     """Fills an sdpa_problem_t from logical [b, h, s, d] torch tensors (no copies).
 
     ALiBi is on when ``alibi`` is true or ``alibi_slopes`` (fp32 CUDA tensor of h_q slopes)
@@ -165,14 +166,15 @@ def make_problem(q, k, v, o=None, *, attn_scale: Optional[float] = None, causal=
     p.alibi_slopes = _ptr(alibi_slopes)
     p.dropout_p = float(dropout_p)
     p.dropout_mask, p.dropout_mask_t = _ptr(dropout_mask), _ptr(dropout_mask_t)
-    p.bias = _ptr(bias)
-    if bias is not None:   # a [b|1, h|1, s_q, s_kv] view; size-1 batch/head dims broadcast
-        st = list(bias.stride())
-        if bias.shape[0] == 1:
-            st[0] = 0
-        if bias.shape[1] == 1:
-            st[1] = 0
-        p.bias_strides = Strides(*st)
+    p.bias, p.dbias = _ptr(bias), _ptr(dbias)
+    for t, field in ((bias, "bias_strides"), (dbias, "dbias_strides")):
+        if t is not None:   # a [b|1, h|1, s_q, s_kv] view; size-1 batch/head dims broadcast
+            st = list(t.stride())
+            if t.shape[0] == 1:
+                st[0] = 0
+            if t.shape[1] == 1:
+                st[1] = 0
+            setattr(p, field, Strides(*st))
     p.dout_dtype = dtype_code(dout) if dout is not None else p.in_dtype
     p.descale_do = _ptr(descale_do)
     if p.in_dtype == DTYPE_E4M3 and o is None:
@@ -214,7 +216,7 @@ def sdpa_fwd(q, k, v, o, lse=None, *, attn_scale: Optional[float] = None, causal
 def sdpa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, *, attn_scale: Optional[float] = None,
              causal=False, stream=None, seq_lens_q=None, seq_lens_kv=None, alibi=False,
              alibi_slopes=None, dropout_p: float = 0.0, dropout_mask_t=None, descale_q=None,
-             descale_k=None, descale_v=None, descale_do=None, bias=None) -> None:
+             descale_k=None, descale_v=None, descale_do=None, bias=None, dbias=None) -> None:
     """dQ, dK, dV (overwritten) for the incoming gradient ``dout``; the masking, lengths,
     ALiBi and dropout options must be those of the forward call that produced ``o`` and
     ``lse`` (dropout_mask_t: the transposed keep bits of the same draw).  FP8: E4M3 q, k, v
@@ -223,7 +225,7 @@ def sdpa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, *, attn_scale: Option
                      dv=dv, seq_lens_q=seq_lens_q, seq_lens_kv=seq_lens_kv, alibi=alibi,
                      alibi_slopes=alibi_slopes, dropout_p=dropout_p, dropout_mask_t=dropout_mask_t,
                      descale_q=descale_q, descale_k=descale_k, descale_v=descale_v,
-                     descale_do=descale_do, bias=bias)
+                     descale_do=descale_do, bias=bias, dbias=dbias)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.sdpa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
                         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream)))

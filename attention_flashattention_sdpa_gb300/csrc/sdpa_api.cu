@@ -78,9 +78,15 @@ size_t bias_t_bytes(const sdpa_problem_t* p) {
   return (nb * nh * p->s_kv * pad * 2 + 255) & ~size_t(255);
 }
 
+// fp32 bias-gradient accumulator, laid out like the transposed bias copy.
+size_t dbias_acc_bytes(const sdpa_problem_t* p) {
+  if (p->bias == nullptr || p->dbias == nullptr) return 0;
+  return 2 * bias_t_bytes(p);
+}
+
 size_t bwd_total_workspace(const sdpa_problem_t* p) {
   const size_t base = (sdpa::bwd_workspace_bytes(p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d) + 255) & ~size_t(255);
-  return base + widen_bytes(p, nullptr, nullptr, nullptr) + bias_t_bytes(p);
+  return base + widen_bytes(p, nullptr, nullptr, nullptr) + bias_t_bytes(p) + dbias_acc_bytes(p);
 }
 
 bool valid_dtype(int dt) {
@@ -206,6 +212,17 @@ sdpa_status_t check_problem(const sdpa_problem_t* p, bool backward) {
     if (bs.b < 0 || bs.h < 0 || bs.s < 0 || bs.b % 8 || bs.h % 8 || bs.s % 8)
       return fail(SDPA_ERR_LAYOUT, "bias: strides must be non-negative multiples of 8 elements");
     if (p->s_q > 1 && bs.s < p->s_kv) return fail(SDPA_ERR_LAYOUT, "bias: row stride below s_kv");
+  }
+  if (backward && p->dbias != nullptr) {
+    const sdpa_strides_t& ds = p->dbias_strides;
+    if (p->bias == nullptr) return fail(SDPA_ERR_INVALID_ARG, "dbias needs a bias tensor");
+    if (reinterpret_cast<uintptr_t>(p->dbias) % 16) return fail(SDPA_ERR_LAYOUT, "dbias must be 16-byte aligned");
+    if ((ds.b == 0) != (p->bias_strides.b == 0) || (ds.h == 0) != (p->bias_strides.h == 0))
+      return fail(SDPA_ERR_LAYOUT, "dbias must broadcast over the same dimensions as bias");
+    if (ds.d != 1 && p->s_kv > 1) return fail(SDPA_ERR_LAYOUT, "dbias: the key stride (d field) must be 1");
+    if (ds.b < 0 || ds.h < 0 || ds.s < 0 || ds.b % 8 || ds.h % 8 || ds.s % 8)
+      return fail(SDPA_ERR_LAYOUT, "dbias: strides must be non-negative multiples of 8 elements");
+    if (p->s_q > 1 && ds.s < p->s_kv) return fail(SDPA_ERR_LAYOUT, "dbias: row stride below s_kv");
   }
   if (p->in_dtype == SDPA_DTYPE_E5M2 || p->out_dtype == SDPA_DTYPE_E5M2)
     return fail(SDPA_ERR_UNSUPPORTED, "E5M2 is accepted only as dout_dtype of an FP8 backward pass");
@@ -406,6 +423,12 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
                                                 (p->s_q + 127) / 128 * 128, skip, off, bt, stream);
     if (e != cudaSuccess) return fail(SDPA_ERR_CUDA, "bias transpose launch failed: %s", cudaGetErrorString(e));
     prm.bias_t = bt;
+    if (p->dbias != nullptr) {
+      float* acc = reinterpret_cast<float*>(bt + bias_t_bytes(p));
+      cudaError_t e2 = cudaMemsetAsync(acc, 0, dbias_acc_bytes(p), stream);
+      if (e2 != cudaSuccess) return fail(SDPA_ERR_CUDA, "dbias accumulator clear failed: %s", cudaGetErrorString(e2));
+      prm.dbias_acc = acc;
+    }
   }
   // d = 256 walks 64-row query blocks (its kernel keeps only half of d of dK/dV in TMEM).
   const int q_rows = p->d == 256 ? 64 : 128;
@@ -486,6 +509,9 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
     fprintf(stderr, "[sdpa] bwd b=%d h_q=%d h_kv=%d s_q=%d s_kv=%d d=%d dt=%d causal=%d ws=%zu\n",
             p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d, p->in_dtype, p->causal, need);
   cudaError_t e = sdpa::launch_bwd(prm, cdt, stream);
+  if (e == cudaSuccess && prm.dbias_acc != nullptr)
+    e = sdpa::launch_dbias_convert(prm.dbias_acc, prm.bias_nb, prm.bias_nh, p->s_q, p->s_kv, s_q_pad, p->dbias,
+                                   p->dbias_strides.b, p->dbias_strides.h, p->dbias_strides.s, cdt, stream);
   return finish_launch(e, stream, "sdpa_bwd");
 }
 

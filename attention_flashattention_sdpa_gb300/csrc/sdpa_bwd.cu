@@ -116,6 +116,22 @@ __device__ __forceinline__ void load_bias_t(const BwdParams& p, int bi, int hq, 
   for (int e = 0; e < 8; ++e) bz[e] = __ldg(src + e);
 }
 
+// Row of the bias-gradient accumulator for key row kv_row and queries q0.. (nullptr past s_kv).
+__device__ __forceinline__ float* dbias_row(const BwdParams& p, int bi, int hq, int kv_row, int q0) {
+  if (kv_row >= p.s_kv) return nullptr;
+  const int nb = p.bias_nb > 1 ? bi : 0, nh = p.bias_nh > 1 ? hq : 0;
+  return p.dbias_acc + ((static_cast<int64_t>(nb) * p.bias_nh + nh) * p.s_kv + kv_row) * p.s_q_pad + q0;
+}
+
+// dS of columns c, c+1 into the accumulator, four at a time (c is a compile-time constant).
+__device__ __forceinline__ void dbias_emit(float* row, int c, float2 dd, float2& hold) {
+  if (c % 4 == 0) {
+    hold = dd;
+  } else if (row != nullptr) {
+    red_add_v4(row + c - 2, hold.x, hold.y, dd.x, dd.y);
+  }
+}
+
 // Columns c, c+1 of eight packed 16-bit bias vectors, as fp32.
 template <int DT>
 __device__ __forceinline__ float2 bias_pair(const uint4 (&bz)[8], int c) {
@@ -297,6 +313,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   constexpr bool ALIBI = (FEAT & kFeatAlibi) != 0;
   constexpr bool DROP = (FEAT & kFeatDropout) != 0;
   constexpr bool BIAS = (FEAT & kFeatBias) != 0;
+  constexpr bool DBIAS = (FEAT & kFeatDBias) != 0;
   extern __shared__ __align__(1024) uint8_t smem[];
   BwdBarriers& bars = *reinterpret_cast<BwdBarriers*>(smem + C::OFF_BAR);
   uint8_t* sK = smem + C::OFF_K;
@@ -532,6 +549,8 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       // Additive bias of this key row for the 64 query columns (transposed copy).
       uint4 bz[BIAS ? 8 : 1];
       if constexpr (BIAS) load_bias_t(p, bi, iter_head(n), kv_row, q0, bz);
+      // Bias gradient: this key row's 64 query columns of the transposed accumulator.
+      float* dbrow = DBIAS ? dbias_row(p, bi, iter_head(n), kv_row, q0) : nullptr;
       const float* nlse2 = sVec + (b * 2 + 0) * 128 + 64 * h;    // -LSE·log2 e per column
       const float* ndelta = sVec + (b * 2 + 1) * 128 + 64 * h;   // -Delta per column
       // Pᵀ = exp2(Sᵀ·scale·log2e − LSE·log2e), masked where key > query
@@ -590,6 +609,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       if (!mbar_wait_warp(&bars.dp_full[b], par, abort_flag)) { ok = false; break; }
       tc_fence_after();
       uint32_t ds[32];
+      float2 dbhold = make_float2(0.f, 0.f);   // pairs of dS awaiting a 4-wide reduce-add
       if constexpr (DROP) {
         // dP = keep / (1 - p) * dO·Vᵀ.  Half the columns at a time (fewer live registers):
         // the second half is read before region Y is released.
@@ -611,6 +631,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
             dpv.y = (w >> c) & 2u ? dpv.y : 0.f;
             const float2 dd = mul2(unpack2(pk[16 * half + c / 2], DT), fma2(dpv, rk2, nd));
             ds[16 * half + c / 2] = pack2(dd.x, dd.y, DT);
+            if constexpr (DBIAS) dbias_emit(dbrow, 32 * half + c, dd, dbhold);
           }
         }
       } else {
@@ -626,6 +647,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
           const float2 dd = mul2(unpack2(pk[c / 2], DT),
                                  fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), dp2, nd));
           ds[c / 2] = pack2(dd.x, dd.y, DT);
+          if constexpr (DBIAS) dbias_emit(dbrow, c, dd, dbhold);
         }
       }
       // dS in shared memory, one 128-byte swizzled row per key row r, chunk h holding query
@@ -809,6 +831,7 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
   constexpr bool ALIBI = (FEAT & kFeatAlibi) != 0;
   constexpr bool DROP = (FEAT & kFeatDropout) != 0;
   constexpr bool BIAS = (FEAT & kFeatBias) != 0;
+  constexpr bool DBIAS = (FEAT & kFeatDBias) != 0;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (smem_u32(smem) & 1023u) {
     if (threadIdx.x == 0) atomicOr(&g_device_error, kErrSmemAlign);
@@ -935,6 +958,9 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
       const float2 rk2 = make_float2(bs.dp, bs.dp);
       uint4 bz[BIAS ? 8 : 1];
       if constexpr (BIAS) load_bias_t(p, bi, hq, kv_row, q0, bz);
+      // Both d-halves compute the same dS: the first half alone adds it to the bias gradient.
+      float* dbrow = (DBIAS && dh == 0) ? dbias_row(p, bi, hq, kv_row, q0) : nullptr;
+      float2 dbhold = make_float2(0.f, 0.f);
       uint32_t pk[32], ds[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
@@ -964,6 +990,7 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
         }
         const float2 dd = mul2(make_float2(p0, p1), t);
         ds[c / 2] = pack2(dd.x, dd.y, DT);
+        if constexpr (DBIAS) dbias_emit(dbrow, c, dd, dbhold);
       }
       tmem_st32(tmem + lane_base + C::COL_S, pk);
       uint8_t* rowp = sDS + r * 128;
@@ -1135,13 +1162,16 @@ cudaError_t launch_d256(const BwdParams& p, cudaStream_t st) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  const int feat = (p.alibi ? kFeatAlibi : 0) | (p.drop_cols ? kFeatDropout : 0) | (p.bias_t ? kFeatBias : 0);
+  const int feat = (p.alibi ? kFeatAlibi : 0) | (p.drop_cols ? kFeatDropout : 0) | (p.bias_t ? kFeatBias : 0) |
+                   (p.dbias_acc ? kFeatDBias : 0);
   auto kern = bwd_d256_kernel<DT, 0>;
   if (feat == kFeatAlibi) kern = bwd_d256_kernel<DT, kFeatAlibi>;
   if (feat == kFeatDropout) kern = bwd_d256_kernel<DT, kFeatDropout>;
   if (feat == (kFeatAlibi | kFeatDropout)) kern = bwd_d256_kernel<DT, kFeatAlibi | kFeatDropout>;
   if (feat == kFeatBias) kern = bwd_d256_kernel<DT, kFeatBias>;
   if (feat == (kFeatBias | kFeatDropout)) kern = bwd_d256_kernel<DT, kFeatBias | kFeatDropout>;
+  if (feat == (kFeatBias | kFeatDBias)) kern = bwd_d256_kernel<DT, kFeatBias | kFeatDBias>;
+  if (feat == (kFeatBias | kFeatDBias | kFeatDropout)) kern = bwd_d256_kernel<DT, kFeatBias | kFeatDBias | kFeatDropout>;
   e = set_smem_once(reinterpret_cast<const void*>(kern), D256::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const unsigned grid = 2u * p.b * p.h_kv * p.kv_split * ((p.s_kv + kBlockN - 1) / kBlockN);
@@ -1172,13 +1202,16 @@ cudaError_t launch_t(const BwdParams& p, cudaStream_t st) {
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
-  const int feat = (p.alibi ? kFeatAlibi : 0) | (p.drop_cols ? kFeatDropout : 0) | (p.bias_t ? kFeatBias : 0);
+  const int feat = (p.alibi ? kFeatAlibi : 0) | (p.drop_cols ? kFeatDropout : 0) | (p.bias_t ? kFeatBias : 0) |
+                   (p.dbias_acc ? kFeatDBias : 0);
   auto kern = bwd_main_kernel<D, DT, 0>;
   if (feat == kFeatAlibi) kern = bwd_main_kernel<D, DT, kFeatAlibi>;
   if (feat == kFeatDropout) kern = bwd_main_kernel<D, DT, kFeatDropout>;
   if (feat == (kFeatAlibi | kFeatDropout)) kern = bwd_main_kernel<D, DT, kFeatAlibi | kFeatDropout>;
   if (feat == kFeatBias) kern = bwd_main_kernel<D, DT, kFeatBias>;
   if (feat == (kFeatBias | kFeatDropout)) kern = bwd_main_kernel<D, DT, kFeatBias | kFeatDropout>;
+  if (feat == (kFeatBias | kFeatDBias)) kern = bwd_main_kernel<D, DT, kFeatBias | kFeatDBias>;
+  if (feat == (kFeatBias | kFeatDBias | kFeatDropout)) kern = bwd_main_kernel<D, DT, kFeatBias | kFeatDBias | kFeatDropout>;
   e = set_smem_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const unsigned gmain = static_cast<unsigned>(p.b) * p.h_kv * p.kv_split * ((p.s_kv + kBlockN - 1) / kBlockN);
@@ -1324,6 +1357,75 @@ cudaError_t launch_bias_transpose(const void* src, int64_t sb, int64_t sh, int64
   dim3 grid((s_q_pad + 63) / 64, (s_kv + 63) / 64, nb * nh);
   bias_transpose_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(src), sb, sh, ss, nh, s_q, s_kv,
                                               s_q_pad, skip_above, diag_off, static_cast<uint16_t*>(dst));
+  return cudaGetLastError();
+}
+
+namespace {
+
+// Transposed fp32 accumulator [nb][nh][s_kv][s_q_pad] -> dbias [nb][nh][s_q][s_kv] (16-bit,
+// caller strides) through 64 x 64 shared-memory tiles.
+template <typename T>
+__global__ void __launch_bounds__(256) dbias_convert_kernel(const float* acc, int nh, int s_q, int s_kv,
+                                                            int s_q_pad, T* dst, int64_t sb, int64_t sh,
+                                                            int64_t ss) {
+  __shared__ float tile[64][65];   // [key][query]
+  const int z = blockIdx.z;
+  const int nbi = z / nh, nhi = z % nh;
+  const int i0 = blockIdx.x * 64, j0 = blockIdx.y * 64;
+  const float* a = acc + static_cast<int64_t>(z) * s_kv * s_q_pad;
+  for (int t = threadIdx.x; t < 1024; t += 256) {   // 64 key rows x 16 chunks of 4 queries
+    const int r = t / 16, c = t % 16;
+    const int j = j0 + r, i = i0 + 4 * c;
+    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (j < s_kv && i < s_q_pad) v = *reinterpret_cast<const float4*>(a + static_cast<int64_t>(j) * s_q_pad + i);
+    tile[r][4 * c] = v.x;
+    tile[r][4 * c + 1] = v.y;
+    tile[r][4 * c + 2] = v.z;
+    tile[r][4 * c + 3] = v.w;
+  }
+  __syncthreads();
+  T* d = dst + nbi * sb + nhi * sh;
+  for (int t = threadIdx.x; t < 512; t += 256) {    // 64 query rows x 8 chunks of 8 keys
+    const int r = t / 8, c = t % 8;
+    const int i = i0 + r, j = j0 + 8 * c;
+    if (i >= s_q || j >= s_kv) continue;
+    T* row = d + static_cast<int64_t>(i) * ss + j;
+    if (j + 8 <= s_kv) {
+      uint32_t h[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        T lo, hi;
+        if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+          lo = __float2bfloat16_rn(tile[8 * c + 2 * u][r]);
+          hi = __float2bfloat16_rn(tile[8 * c + 2 * u + 1][r]);
+        } else {
+          lo = __float2half_rn(tile[8 * c + 2 * u][r]);
+          hi = __float2half_rn(tile[8 * c + 2 * u + 1][r]);
+        }
+        h[u] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&lo)) |
+               (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&hi)) << 16);
+      }
+      *reinterpret_cast<uint4*>(row) = make_uint4(h[0], h[1], h[2], h[3]);
+    } else {
+      for (int u = 0; j + u < s_kv; ++u) {
+        if constexpr (std::is_same<T, __nv_bfloat16>::value) row[u] = __float2bfloat16_rn(tile[8 * c + u][r]);
+        else row[u] = __float2half_rn(tile[8 * c + u][r]);
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dbias_convert(const float* acc, int nb, int nh, int s_q, int s_kv, int s_q_pad, void* dst,
+                                 int64_t sb, int64_t sh, int64_t ss, int dtype, cudaStream_t st) {
+  dim3 grid((s_q + 63) / 64, (s_kv + 63) / 64, nb * nh);
+  if (dtype == kBF16)
+    dbias_convert_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(acc, nh, s_q, s_kv, s_q_pad,
+                                                              static_cast<__nv_bfloat16*>(dst), sb, sh, ss);
+  else
+    dbias_convert_kernel<__half><<<grid, 256, 0, st>>>(acc, nh, s_q, s_kv, s_q_pad, static_cast<__half*>(dst),
+                                                       sb, sh, ss);
   return cudaGetLastError();
 }
 

@@ -98,7 +98,14 @@ struct BwdParams {
   // input dtype (bias_nb = 1 or b, bias_nh = 1 or h_q), or nullptr.
   const void* bias_t;
   int bias_nb, bias_nh;
+  // Bias gradient: dS reduce-added into a zeroed fp32 workspace laid out like bias_t,
+  // [bias_nb][bias_nh][s_kv][s_q_pad], or nullptr.
+  float* dbias_acc;
 };
+
+// dbias[nb][nh][s_q][s_kv] (16-bit, caller strides) from the transposed fp32 accumulator.
+cudaError_t launch_dbias_convert(const float* acc, int nb, int nh, int s_q, int s_kv, int s_q_pad, void* dst,
+                                 int64_t sb, int64_t sh, int64_t ss, int dtype, cudaStream_t st);
 
 // Transposes a strided [nb][nh][s_q][s_kv] bias view into dense [nb][nh][s_kv][s_q_pad].
 cudaError_t launch_bias_transpose(const void* src, int64_t sb, int64_t sh, int64_t ss, int nb, int nh,
@@ -152,6 +159,7 @@ inline cudaError_t set_smem_once(const void* kern, int bytes) {
 constexpr int kFeatAlibi = 1;
 constexpr int kFeatDropout = 2;
 constexpr int kFeatBias = 4;
+constexpr int kFeatDBias = 8;   // only with kFeatBias
 
 }  // namespace sdpa
 

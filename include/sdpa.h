@@ -137,9 +137,17 @@ typedef struct {
    * to the scaled scores before the mask and softmax and is treated as a constant (no
    * gradient is produced).  Base 16-byte aligned; non-zero b/h/s strides multiples of 8.
    * Not combined with alibi (fold ALiBi into the tensor instead).  A backward pass with a
-   * bias needs workspace for a transposed copy (sdpa_workspace_size accounts for it). */
+   * bias needs workspace for a transposed copy (sdpa_workspace_size accounts for it); its
+   * gradient is available through dbias. */
   const void* bias;
   sdpa_strides_t bias_strides;
+  /* Bias gradient (sdpa_bwd only; needs `bias`): NULL = not wanted; else a DEVICE pointer to
+   * a tensor of the bias's shape and dtype, strides dbias_strides (zero b/h strides exactly
+   * where bias_strides has them), overwritten with dL/dbias = dS — the gradient of the
+   * scaled scores — summed over the broadcast dimensions.  Same alignment rules as bias.
+   * The workspace then also holds an fp32 accumulator (sdpa_workspace_size accounts for it). */
+  void* dbias;
+  sdpa_strides_t dbias_strides;
 } sdpa_problem_t;
 
 /*

@@ -116,12 +116,14 @@ def run_fwd(w: Workload, x: Inputs, with_lse: bool = True, out_dtype=torch.bfloa
 
 
 def run_bwd(w: Workload, dev_qkv, o, lse, do_cpu: torch.Tensor, causal=None, seq_lens_q=None,
-            seq_lens_kv=None, alibi=None, dropout=None, bias=None):
+            seq_lens_kv=None, alibi=None, dropout=None, bias=None, dbias=None):
     m = lib()
     causal = w.causal if causal is None else causal
     lens = _alibi_kwargs(alibi)
     if bias is not None:
         lens["bias"] = bias
+    if dbias is not None:
+        lens["dbias"] = dbias
     if dropout is not None:
         lens["dropout_p"] = dropout[0]
         dc = causal if seq_lens_q is None and seq_lens_kv is None else False
@@ -136,7 +138,7 @@ def run_bwd(w: Workload, dev_qkv, o, lse, do_cpu: torch.Tensor, causal=None, seq
     dk, dkb = guarded_empty_like(k)
     dv, dvb = guarded_empty_like(v)
     p = m.make_problem(q, k, v, o, attn_scale=w.scale, causal=causal, dout=do, dq=dq, dk=dk, dv=dv,
-                       bias=bias)
+                       bias=bias, dbias=dbias)
     ws = torch.empty(m.sdpa_workspace_size(p, True), dtype=torch.uint8, device="cuda")
     ws.fill_(0xAB)  # contents on entry must not matter
     m.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, attn_scale=w.scale, causal=causal, **lens)

@@ -206,3 +206,19 @@ def test_bias_workspace_holds_a_transposed_copy(m):
     with_bias = m.sdpa_workspace_size(_problem(m, bias=FAKE), True)   # [1, h_q, 128, 128] bf16
     assert with_bias - base == 2 * 128 * 128 * 2
     assert m.sdpa_workspace_size(_problem(m, bias=FAKE), False) == 0
+
+
+def test_bias_gradient_validation_and_workspace(m):
+    st = m.Strides(0, 128 * 128, 128, 1)
+    p = _problem(m, dbias=FAKE, dbias_strides=(0, 128 * 128, 128, 1))
+    assert _bwd(m, p) == 1 and "needs a bias" in m.sdpa_last_error_string()
+    p = _problem(m, bias=FAKE, dbias=FAKE + 8, dbias_strides=(0, 128 * 128, 128, 1))
+    p.bias_strides = st
+    assert _bwd(m, p) == 3 and "dbias must be 16-byte" in m.sdpa_last_error_string()
+    p = _problem(m, bias=FAKE, dbias=FAKE, dbias_strides=(2 * 128 * 128, 128 * 128, 128, 1))
+    p.bias_strides = st
+    assert _bwd(m, p) == 3 and "same dimensions" in m.sdpa_last_error_string()
+    base = m.sdpa_workspace_size(_problem(m, bias=FAKE), True)
+    p = _problem(m, bias=FAKE, dbias=FAKE, dbias_strides=(0, 128 * 128, 128, 1))
+    p.bias_strides = st
+    assert m.sdpa_workspace_size(p, True) - base == 2 * 128 * 128 * 4

@@ -91,3 +91,32 @@ def test_split_groups():
 def test_forward_only_inference_shape():
     w = Workload("t", 4, 12, 12, 1024, 1024, 64, "f16", causal=True)
     _case(w, 1, 12, seed=10, backward=False)
+
+
+def _dbias_case(w, nb, nh, seed, dropout=None, lq=None, lkv=None, bottom_right=False):
+    x = make_inputs(w, seed=seed, with_do=True)
+    bdev, bcpu = _bias(w, nb, nh, seed + 1, x.q.dtype)
+    causal = "bottom_right" if bottom_right else w.causal
+    o, lse, dev = run_fwd(w, x, causal=causal, seq_lens_q=lq, seq_lens_kv=lkv, dropout=dropout, bias=bdev)
+    gbuf, _ = _bias(w, nb, nh, seed + 2, x.q.dtype)       # garbage that must be overwritten
+    run_bwd(w, dev, o, lse, x.do, causal=causal, seq_lens_q=lq, seq_lens_kv=lkv, dropout=dropout, bias=bdev,
+            dbias=gbuf)
+    pd = float(np.float32(dropout[0])) if dropout else 0.0
+    keep = None
+    if dropout is not None:
+        keep = oracle.dropout_keep(w.b, w.h_q, w.s_q, w.s_kv, pd, dropout[1], dropout[2])
+    want = oracle.bias_gradient(f64(x.q), f64(x.k), f64(x.v), f64(x.do), w.scale, w.causal or bottom_right,
+                                f64(bcpu), lq, lkv, bottom_right, dropout_p=pd, keep=keep)
+    assert_grad_close(f64(gbuf), want, "dBias")
+
+
+@pytest.mark.parametrize("nb,nh", [(2, 4), (1, 4), (1, 1)])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_bias_gradient(nb, nh, d):
+    w = Workload("t", 2, 4, 2, 200, 333, d, "bf16", causal=True, backward=True)
+    _dbias_case(w, nb, nh, seed=40 + d + nh)
+
+
+def test_bias_gradient_with_dropout_and_lengths():
+    w = Workload("t", 3, 2, 2, 150, 270, 128, "f16", backward=True)
+    _dbias_case(w, 3, 2, seed=50, dropout=(0.3, 1, 2), lq=[150, 40, 1], lkv=[270, 100, 63], bottom_right=True)
