@@ -325,12 +325,20 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
-  // Head-major launch order: all KV blocks of one (batch, KV head, share) before the next,
-  // so resident CTAs share a few heads' Q, dO and dQ accumulator in L2; within a head the
-  // heaviest KV blocks (the first ones, for causal) go first.
+  // Launch order: units (batch, KV head, share) in groups whose Q and dO together take about
+  // 32 MB, so that resident CTAs share them in L2; within a group the heaviest KV blocks of
+  // all its units go first (for causal, the first blocks), then the next block index, which
+  // shortens the tail of long CTAs.  Units of 8 MB or more go one at a time (head-major).
   const int n_kvb = (p.s_kv + kBlockN - 1) / kBlockN;
-  const int j = blockIdx.x % n_kvb;                         // KV block
-  const int unit = blockIdx.x / n_kvb;
+  const int n_units = p.b * p.h_kv * p.kv_split;
+  const long long unit_bytes = 4ll * p.heads_per_split * p.s_q_pad * p.d;
+  int G = static_cast<int>((32ll << 20) / (unit_bytes > 0 ? unit_bytes : 1));
+  G = (unit_bytes >= (8ll << 20) || G < 1) ? 1 : (G > n_units ? n_units : G);
+  const int grp = blockIdx.x / (G * n_kvb);
+  const int gsz = min(G, n_units - grp * G);
+  const int rem = blockIdx.x - grp * G * n_kvb;
+  const int j = rem / gsz;                                  // KV block
+  const int unit = grp * G + rem % gsz;
   const int split = unit % p.kv_split;                      // share of the KV group's heads
   const int bhk = unit / p.kv_split;
   const int bi = bhk / p.h_kv;
