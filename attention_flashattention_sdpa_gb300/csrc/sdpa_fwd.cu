@@ -57,11 +57,15 @@ struct FwdCfg {
   static constexpr int RING_BYTES = NS * TILE_BYTES;
   static constexpr int OUT_TILE_BYTES = kBlockM * D * 2;          // 16-bit output tile
   static constexpr int SMEM_BYTES = Q_BYTES + RING_BYTES + STAGE_BYTES + 1024 /*align slack*/;
-  static constexpr int THREADS = 128 + NQT * 128;
+  // Two softmax warpgroups: one per Q tile, or, with one Q tile, one per half of the 128
+  // score columns of a key block.
+  static constexpr int THREADS = 384;
   static constexpr int KSTEPS_S = D * ES / 32;                    // QKᵀ: 32 bytes of d per MMA
   static constexpr int PV_ROWS = 32 / ES;                         // PV: kv rows per MMA
   static constexpr int KSTEPS_PV = kBlockN / PV_ROWS;
   static constexpr int P_COLS = kBlockN * ES / 4;                 // TMEM columns holding P
+  static constexpr int SCOLS = (NQT == 2) ? kBlockN : kBlockN / 2;  // score columns per thread
+  static constexpr int PW = P_COLS * SCOLS / kBlockN;             // P words per thread
   static constexpr int O_COL0 = 256;                              // S slots at 0 and 128
   static constexpr float THRESH = (DT == kE4M3) ? 0.8f : 8.0f;    // lazy-rescale threshold
   static constexpr float P_OFFSET = (DT == kE4M3) ? 8.0f : 0.0f;  // P scaled by 2^8 for E4M3
@@ -80,6 +84,8 @@ struct alignas(8) FwdBarriers {
   uint64_t pv_done;
   uint64_t drain;
   uint64_t epi_ready[2];
+  uint64_t mx_ready[2];   // column halves: row-max candidates exchanged (per block parity)
+  uint64_t l_ready;       // column halves: row sums exchanged (once)
   uint32_t tmem_base;
   int abort;
 };
@@ -127,6 +133,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
   uint8_t* sQ = smem;
   uint8_t* sRing = smem + C::Q_BYTES;
   __shared__ FwdBarriers bars;
+  // Column halves (one Q tile): per-row exchange of the row-max candidate (by block parity)
+  // and, at the end, of the row sums.
+  __shared__ float xch[NQT == 1 ? 2 : 1][2][kBlockM];
+  __shared__ float xl[2][kBlockM];
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
@@ -152,7 +162,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bars.q_full[t], 1);
       mbar_init(&bars.s_full[t], 1);
-      mbar_init(&bars.p_full[t], 128);
+      mbar_init(&bars.p_full[t], NQT == 2 ? 128 : 256);
       mbar_init(&bars.o_full[t], 1);
     }
     for (int s = 0; s < 8; ++s) {
@@ -161,8 +171,11 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
     }
     mbar_init(&bars.pv_done, 1);
     mbar_init(&bars.drain, 1);
-    mbar_init(&bars.epi_ready[0], 128);
+    mbar_init(&bars.epi_ready[0], NQT == 2 ? 128 : 256);
     mbar_init(&bars.epi_ready[1], 128);
+    mbar_init(&bars.mx_ready[0], 256);
+    mbar_init(&bars.mx_ready[1], 256);
+    mbar_init(&bars.l_ready, 256);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -179,7 +192,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
   // With two Q tiles (384 threads, 168 registers each at launch) the producer / MMA
   // warpgroup gives registers to the two softmax warpgroups: 80 + 2 x 208 <= 3 x 168.
   if (warp < 4) {
-  if constexpr (NQT == 2) regs_dec<80>();
+  regs_dec<80>();
   if (warp == 0) {
     // ================================ TMA producer ====================================
     if (elect_one_sync() && n_blocks > 0) {
@@ -329,9 +342,12 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
     }
   }
   } else {
-    if constexpr (NQT == 2) regs_inc<208>();
+    regs_inc<208>();
     // ============================ softmax / epilogue ==================================
+    constexpr int SC = C::SCOLS;
     const int t = (NQT == 2) ? (warp - 4) / 4 : 0;         // Q tile of this warpgroup
+    const int hc = (NQT == 1) ? (warp - 4) / 4 : 0;        // column half (one Q tile)
+    const int col0 = hc * SC;                                // first score column of this thread
     const int quad = warp % 4;                               // TMEM lane quadrant
     const int r = quad * 32 + lane;                          // row within the tile
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -377,11 +393,11 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       uint4 keep = make_uint4(0u, 0u, 0u, 0u);
       if (DROP && drop_row != nullptr) keep = __ldg(drop_row + kv_block(j));
       // The bias of this row and key block, loaded before the scores arrive.
-      uint4 bz[BIAS ? 16 : 1];
+      uint4 bz[BIAS ? SC / 8 : 1];
       if constexpr (BIAS) {
-        const int kb0 = kv_block(j) * kBlockN;
+        const int kb0 = kv_block(j) * kBlockN + col0;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+        for (int e = 0; e < SC / 8; ++e) {
           const int k0 = kb0 + 8 * e;
           if (bias_row != nullptr && k0 + 8 <= p.s_kv) {
             bz[e] = __ldg(reinterpret_cast<const uint4*>(bias_row + k0));
@@ -397,10 +413,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       tc_fence_after();
       const uint32_t s_addr = tmem + lane_off + slot * 128;
 
-      uint32_t sv[kBlockN];
+      uint32_t sv[SC];
 #pragma unroll
-      for (int c = 0; c < kBlockN / 32; ++c)
-        tmem_ld32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
+      for (int c = 0; c < SC / 32; ++c)
+        tmem_ld32(s_addr + col0 + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[c * 32]));
       tmem_ld_wait();
 
       const int kv0 = kv_block(j) * kBlockN;
@@ -408,16 +424,16 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
                              (p.causal && kv0 + kBlockN - 1 > tile_row0 + L.off) ||
                              (tile_row0 + kBlockM > L.len_q);
       if (need_mask) {
-        const int lim = row_limit - kv0;
+        const int lim = row_limit - kv0 - col0;
 #pragma unroll
-        for (int c = 0; c < kBlockN; ++c)
+        for (int c = 0; c < SC; ++c)
           if (c > lim) sv[c] = __float_as_uint(-INFINITY);
       }
       if constexpr (BIAS) {
         // y = s * |scale| + bias in natural-log units; the max and the exponent scale by log2 e.
         const float2 sn2 = make_float2(c_scale / kLog2e, c_scale / kLog2e);
 #pragma unroll
-        for (int c = 0; c < kBlockN; c += 2) {
+        for (int c = 0; c < SC; c += 2) {
           const uint32_t w = (c % 8 == 0) ? bz[c / 8].x : (c % 8 == 2) ? bz[c / 8].y
                            : (c % 8 == 4) ? bz[c / 8].z : bz[c / 8].w;
           const float2 y = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sn2,
@@ -432,22 +448,30 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         // the slope, u = s * scale / slope + c (c an immediate: nothing to keep in registers),
         // and scaled back by the slope in the max and the exponent.
 #pragma unroll
-        for (int c = 0; c < kBlockN; ++c)
+        for (int c = 0; c < SC; ++c)
           sv[c] = __float_as_uint(fmaf(__uint_as_float(sv[c]), u_scale, static_cast<float>(c)));
       }
       // Row max over four independent chains of three-input max.
       float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kBlockN; c += 8) {
+      for (int c = 0; c < SC; c += 8) {
         mx0 = max3(mx0, __uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
         mx1 = max3(mx1, __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
         mx2 = max3(mx2, __uint_as_float(sv[c + 4]), __uint_as_float(sv[c + 5]));
         mx3 = max3(mx3, __uint_as_float(sv[c + 6]), __uint_as_float(sv[c + 7]));
       }
       const float mx = max3(mx0, mx1, fmaxf(mx2, mx3));
-      // ALiBi row part of this key block: slope * (kv0 - q_row - off).
-      const float row_bias = ALIBI ? sl2 * static_cast<float>(kv0 - q_row - L.off) : 0.f;
-      const float m_cand = ALIBI ? sl2 * mx + row_bias : BIAS ? mx * kLog2e : mx * c_scale;
+      // ALiBi row part of this key block: slope * (kv0 + col0 - q_row - off).
+      const float row_bias = ALIBI ? sl2 * static_cast<float>(kv0 + col0 - q_row - L.off) : 0.f;
+      float m_cand = ALIBI ? sl2 * mx + row_bias : BIAS ? mx * kLog2e : mx * c_scale;
+      if constexpr (NQT == 1) {
+        // Both column halves take the larger of their two candidates, so they keep the same
+        // running max (and rescale O together).
+        xch[j & 1][hc][r] = m_cand;
+        mbar_arrive(&bars.mx_ready[j & 1]);
+        if (!mbar_wait_warp(&bars.mx_ready[j & 1], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+        m_cand = fmaxf(m_cand, xch[j & 1][hc ^ 1][r]);
+      }
       float alpha = 1.f;
       if (m_cand > m_ref + C::THRESH) {
         alpha = ex2(m_ref - m_cand);
@@ -462,9 +486,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       const float2 cs2 = make_float2(cs, cs);
       const float2 nm2 = make_float2(nm, nm);
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-      uint32_t pk[C::P_COLS];
+      uint32_t pk[C::PW];
 #pragma unroll
-      for (int c = 0; c < kBlockN; c += 4) {
+      for (int c = 0; c < SC; c += 4) {
         const float2 x01 = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), cs2, nm2);
         const float2 x23 = fma2(make_float2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), cs2, nm2);
         float2 p01 = make_float2(ex2(x01.x), ex2(x01.y));
@@ -473,7 +497,8 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         acc1 = add2(acc1, p23);
         if constexpr (DROP) {
           // Row sums take every P; P·V only the kept ones.
-          const uint32_t w = (c < 32) ? keep.x : (c < 64) ? keep.y : (c < 96) ? keep.z : keep.w;
+          const int cg = c + col0;   // column within the key block
+          const uint32_t w = (cg < 32) ? keep.x : (cg < 64) ? keep.y : (cg < 96) ? keep.z : keep.w;
           const uint32_t b4 = w >> (c % 32);
           p01.x = (b4 & 1u) ? p01.x : 0.f;
           p01.y = (b4 & 2u) ? p01.y : 0.f;
@@ -488,9 +513,16 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         }
       }
       const float rowsum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+      // P over this thread's columns (P words start at col0 * bytes per element / 4).
+      const uint32_t p_addr = s_addr + col0 * C::ES / 4;
+      if constexpr (C::PW % 32 == 0) {
 #pragma unroll
-      for (int c = 0; c < C::P_COLS / 32; ++c)
-        tmem_st32(s_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[c * 32]));
+        for (int c = 0; c < C::PW / 32; ++c)
+          tmem_st32(p_addr + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&pk[c * 32]));
+      } else {
+        static_assert(C::PW == 16, "P words per thread");
+        tmem_st16(p_addr, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+      }
       l = l * alpha + rowsum;
 
       if (NQT == 1 && j > 0) {
@@ -499,9 +531,11 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         tc_fence_after();
       }
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-        const uint32_t o_addr = tmem + lane_off + C::O_COL0 + t * D;
+        // Each column half rescales its half of O.
+        constexpr int OC = (NQT == 2) ? D : D / 2;
+        const uint32_t o_addr = tmem + lane_off + C::O_COL0 + t * D + hc * OC;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < OC / 32; ++c) {
           uint32_t ov[32];
           tmem_ld32(o_addr + c * 32, ov);
           tmem_ld_wait();
@@ -521,12 +555,22 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
     uint8_t* stage = (NQT == 1) ? sRing
                      : (C::STAGE_BYTES > 0) ? sRing + C::RING_BYTES + t * C::OUT_TILE
                                             : sQ + t * C::TILE_BYTES;
+    if constexpr (NQT == 1) {
+      // The row sum is the sum of the two halves' partial sums.  Both halves arrive whatever
+      // happened, so the bounded wait can only fail through a timeout.
+      xl[hc][r] = l;
+      mbar_arrive(&bars.l_ready);
+      ok = ok && mbar_wait_warp(&bars.l_ready, 0, abort_flag);
+      if (ok) l += xl[hc ^ 1][r];
+    }
     if (ok) {
       tc_fence_after();
       const float inv_l = (l > 0.f) ? v_scale / l : 0.f;   // rows without a visible key: O = 0
       const uint32_t o_addr = tmem + lane_off + C::O_COL0 + t * D;
+      // O leaves in 64-column chunks; with column halves each writes half of them.
+      constexpr int NCK = (NQT == 2) ? D / 64 : D / 128;
 #pragma unroll 1
-      for (int c = 0; c < D / 64; ++c) {
+      for (int c = hc * NCK; c < (hc + 1) * NCK; ++c) {
         uint32_t ov[64];
         if (n_blocks > 0) {
           tmem_ld32(o_addr + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
@@ -548,14 +592,14 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         }
       }
       fence_proxy_async_smem();
-      if (p.lse != nullptr && q_row < p.s_q)
+      if (p.lse != nullptr && q_row < p.s_q && hc == 0)
         p.lse[(static_cast<int64_t>(bi) * p.h_q + hq) * p.s_q + q_row] =
             (l > 0.f) ? (m_ref - C::P_OFFSET + __log2f(l)) * kLn2 : -INFINITY;
     }
     // Every thread of the warpgroup arrives exactly once, whatever happened above, so the
     // bounded wait below can only fail through a timeout, never deadlock.
     mbar_arrive(&bars.epi_ready[t]);
-    if (r == 0) {
+    if (r == 0 && hc == 0) {
       const bool all_ok = mbar_wait(&bars.epi_ready[t], 0, abort_flag) && ok && !*abort_flag;
       if (all_ok) {
         for (int c = 0; c < D / 64; ++c)
