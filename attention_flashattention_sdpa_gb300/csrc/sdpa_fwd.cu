@@ -142,14 +142,26 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
   const int lane = threadIdx.x % 32;
 
   // ---- tile coordinates ----------------------------------------------------------------
-  // Launch order: all (batch, head) pairs of the heaviest query tile (the latest, for
-  // causal) first, then the next heaviest, and so on — a longest-first schedule.
+  // Launch order: longest first — the heaviest query tile (the latest, for causal) of every
+  // (batch, head) pair, then the next heaviest, and so on.  When the heads' K and V together
+  // exceed ~64 MB (they would stream from HBM once per tile), this runs over groups of query
+  // heads whose K and V take ~32 MB instead, one group after another, so that a group's K/V
+  // stays in L2 while all its tiles run.
   const int n_bh = p.b * p.h_q;
-  const int bh = blockIdx.x % n_bh;
+  const long long kv_bytes = 2ll * p.s_kv * D * C::ES;             // K and V of one KV head
+  int G = n_bh;                                                     // query heads per group
+  if (kv_bytes * (n_bh / p.group) > (64ll << 20)) {
+    G = static_cast<int>((32ll << 20) / kv_bytes) * p.group;
+    G = G < p.group ? p.group : (G > n_bh ? n_bh : G);
+  }
+  const int grp = blockIdx.x / (G * p.num_m_blocks);
+  const int gsz = min(G, n_bh - grp * G);
+  const int rem = blockIdx.x - grp * G * p.num_m_blocks;
+  const int bh = grp * G + rem % gsz;
   const int bi = bh / p.h_q;
   const int hq = bh % p.h_q;
   const int hk = hq / p.group;
-  const int m_blk = p.num_m_blocks - 1 - blockIdx.x / n_bh;
+  const int m_blk = p.num_m_blocks - 1 - rem / gsz;
   const int m0 = m_blk * kBlockM * NQT;
   const Lens L = batch_lens(p, bi);
   const int n_blocks = kv_blocks_for(p, L, m0, kBlockM * NQT);

@@ -11,6 +11,7 @@ Prints one JSON line (rank 0).  Flags:
   --impl reference                time the fp64 CPU oracle instead (bounded row slices of the
                                   same workload) and print the reference line
   --profile-step                  run one untimed fwd+bwd (the command profiled with ncu)
+  --profile-workload NAME         one untimed fwd (+bwd) of a --sweep workload, for ncu
   --sweep                         one line per configuration (tables; not the contract line)
   --measure-peaks                 dense GEMM peaks of this GPU through the vendor library:
                                   bf16 (torch.matmul) and E4M3 (torch._scaled_mm), 8192^3
@@ -359,6 +360,23 @@ def run_reference(args):
     return 0
 
 
+def run_profile_workload(args):
+    """One untimed forward (and backward, for training workloads) of a named sweep workload:
+    the command an ncu capture of that workload's kernels runs."""
+    import torch
+    from sdpa_workloads import all_workloads
+    torch.cuda.set_device(0)
+    ws = [w for w in all_workloads() if w.name == args.profile_workload]
+    if not ws:
+        print("unknown workload; choose one of: " + ", ".join(w.name for w in all_workloads()))
+        return 2
+    # A short sweep_one (3 warm-up + 3 timed calls each way, no graphs); a capture picks its
+    # launches with -k / -s / -c.
+    line = sweep_one(ws[0], load_peaks(), args, quick=True)
+    print(json.dumps(line))
+    return 0
+
+
 def run_cuda(args):
     import torch
     world, rank, local = dist_env()
@@ -545,7 +563,7 @@ def graph_ms(fn, calls: int, reps: int = 10) -> float:
     return statistics.median(ts)
 
 
-def sweep_one(w, peaks, args):
+def sweep_one(w, peaks, args, quick: bool = False):
     import torch
     import attention_flashattention_sdpa_gb300 as sdpa
     from sdpa_workloads import make_inputs
@@ -581,7 +599,7 @@ def sweep_one(w, peaks, args):
         kw["bias"] = torch.randn(1, w.h_q, w.s_q, w.s_kv, device="cuda", generator=g).to(q.dtype)
     fwd = lambda: sdpa.sdpa_fwd(q, k, v, o, lse, attn_scale=w.scale, causal=w.causal, alibi=w.alibi,
                                 **kw)
-    reps = max(5, min(200, int(2e13 / max(w.fwd_flops(), 1))))
+    reps = 3 if quick else max(5, min(200, int(2e13 / max(w.fwd_flops(), 1))))
     for _ in range(3):
         fwd()
     torch.cuda.synchronize()
@@ -595,9 +613,10 @@ def sweep_one(w, peaks, args):
     peak = peaks["bf16_tflops"]
     line = {"workload": w.name, "fwd_ms": fwd_ms, "fwd_tflops": w.fwd_flops() / fwd_ms / 1e9}
     calls = max(4, min(64, int(2e12 / max(w.fwd_flops(), 1))))
-    gms = graph_ms(fwd, calls)
-    line["fwd_ms_graph"] = gms
-    line["fwd_tflops_graph"] = w.fwd_flops() / gms / 1e9
+    if not quick:
+        gms = graph_ms(fwd, calls)
+        line["fwd_ms_graph"] = gms
+        line["fwd_tflops_graph"] = w.fwd_flops() / gms / 1e9
     if mask_ms is not None:
         line["dropout_mask_ms"] = mask_ms
     es = 1 if w.dtype == "e4m3" else 2
@@ -635,9 +654,10 @@ def sweep_one(w, peaks, args):
         torch.cuda.synchronize()
         bwd_ms = statistics.median(a.elapsed_time(b) for a, b in ts)
         line["bwd_ms"] = bwd_ms
-        gb = graph_ms(bwd, max(2, calls // 2))
-        line["bwd_ms_graph"] = gb
-        line["bwd_tflops_graph"] = w.bwd_flops() / gb / 1e9
+        if not quick:
+            gb = graph_ms(bwd, max(2, calls // 2))
+            line["bwd_ms_graph"] = gb
+            line["bwd_tflops_graph"] = w.bwd_flops() / gb / 1e9
         line["bwd_tflops"] = w.bwd_flops() / bwd_ms / 1e9
         line["fwdbwd_tflops"] = (w.fwd_flops() + w.bwd_flops()) / (fwd_ms + bwd_ms) / 1e9
         line["fwdbwd_frac_of_bf16_peak"] = line["fwdbwd_tflops"] / peak
@@ -652,6 +672,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--profile-step", action="store_true")
+    ap.add_argument("--profile-workload", default=None)
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--measure-peaks", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
@@ -663,6 +684,8 @@ def main(argv=None):
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.profile_workload:
+        return run_profile_workload(args)
     if args.measure_peaks:
         return run_measure_peaks(args)
     return run_cuda(args)
