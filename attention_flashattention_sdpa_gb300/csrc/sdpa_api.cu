@@ -267,6 +267,20 @@ sdpa_status_t finish_launch(cudaError_t e, cudaStream_t stream, const char* what
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Streaming multiprocessors of the current device (cached per device).
+int num_sms() {
+  static std::mutex mu;
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    cache[dev] = (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0) ? n : 152;
+  }
+  return cache[dev];
+}
+
 int words_of(int s) { return (s + 127) / 128 * 4; }   // keep-mask words per row or key
 
 // Dropout mask pointer of a forward or backward call (checked only when dropout is on).
@@ -339,7 +353,9 @@ sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const void* k, co
   prm.bias_sb = p->bias_strides.b;
   prm.bias_sh = p->bias_strides.h;
   prm.bias_ss = p->bias_strides.s;
-  const int rows_per_cta = 128 * sdpa::fwd_q_tiles(p->d, p->in_dtype);
+  prm.one_tile = sdpa::fwd_prefer_one_tile(p->b, p->h_q, p->s_q, p->d, p->in_dtype,
+                                          !prm.alibi && !prm.drop_rows && !prm.bias, num_sms()) ? 1 : 0;
+  const int rows_per_cta = 128 * (prm.one_tile ? 1 : sdpa::fwd_q_tiles(p->d, p->in_dtype));
   prm.num_m_blocks = (p->s_q + rows_per_cta - 1) / rows_per_cta;
   prm.scale_log2 = scale_log2_of(p->attn_scale);
   prm.negate_scores = p->attn_scale < 0.f ? 1 : 0;

@@ -40,10 +40,10 @@ __device__ __forceinline__ float2 unpack16x2(uint32_t w, int dt) {
   return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
-template <int D, int DT>
+template <int D, int DT, bool ONE = false>
 struct FwdCfg {
   static constexpr int ES = (DT == kE4M3) ? 1 : 2;               // input element bytes
-  static constexpr int NQT = (D <= 128) ? 2 : 1;                 // Q tiles per CTA
+  static constexpr int NQT = (!ONE && D <= 128) ? 2 : 1;         // Q tiles per CTA
   static constexpr int CHUNK_ELEMS = 128 / ES;                    // elements per 128-byte row chunk
   static constexpr int NCHUNK = D * ES / 128;                     // 128-byte chunks along d
   static constexpr int TILE_BYTES = kBlockM * D * ES;             // one Q or K or V tile
@@ -119,7 +119,7 @@ __device__ __forceinline__ int kv_blocks_for(const FwdParams& p, const Lens& L, 
 template <int D, int DT, int OUT_DT, int FEAT>
 __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
     sdpa_fwd_kernel(const __grid_constant__ FwdParams p) {
-  using C = FwdCfg<D, DT>;
+  using C = FwdCfg<D, DT, (FEAT & kFeatOneTile) != 0>;
   constexpr bool ALIBI = (FEAT & kFeatAlibi) != 0;
   constexpr bool DROP = (FEAT & kFeatDropout) != 0;
   constexpr bool BIAS = (FEAT & kFeatBias) != 0;
@@ -579,10 +579,12 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       tc_fence_after();
       const float inv_l = (l > 0.f) ? v_scale / l : 0.f;   // rows without a visible key: O = 0
       const uint32_t o_addr = tmem + lane_off + C::O_COL0 + t * D;
-      // O leaves in 64-column chunks; with column halves each writes half of them.
-      constexpr int NCK = (NQT == 2) ? D / 64 : D / 128;
+      // O leaves in 64-column chunks; with column halves each writes half of them (at d = 64
+      // the single chunk is the first half's).
+      constexpr int NCK = (NQT == 2) ? D / 64 : (D / 128 > 0 ? D / 128 : 1);
+      const int c_end = min((hc + 1) * NCK, D / 64);
 #pragma unroll 1
-      for (int c = hc * NCK; c < (hc + 1) * NCK; ++c) {
+      for (int c = hc * NCK; c < c_end; ++c) {
         uint32_t ov[64];
         if (n_blocks > 0) {
           tmem_ld32(o_addr + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&ov[0]));
@@ -632,8 +634,14 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
 
 template <int D, int DT, int OUT_DT>
 cudaError_t launch_t(const FwdParams& p, cudaStream_t st) {
-  using C = FwdCfg<D, DT>;
+  int smem = FwdCfg<D, DT>::SMEM_BYTES;
   auto kern = sdpa_fwd_kernel<D, DT, OUT_DT, 0>;
+  if constexpr (DT != kE4M3 && D <= 128) {
+    if (p.one_tile) {
+      kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatOneTile>;
+      smem = FwdCfg<D, DT, true>::SMEM_BYTES;
+    }
+  }
   if constexpr (DT != kE4M3) {
     const int feat = (p.alibi ? kFeatAlibi : 0) | (p.drop_rows ? kFeatDropout : 0) | (p.bias ? kFeatBias : 0);
     if (feat == kFeatAlibi) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatAlibi>;
@@ -642,14 +650,20 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t st) {
     if (feat == kFeatBias) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatBias>;
     if (feat == (kFeatBias | kFeatDropout)) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatBias | kFeatDropout>;
   }
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;
   const unsigned grid = static_cast<unsigned>(p.b) * p.h_q * p.num_m_blocks;
-  kern<<<grid, C::THREADS, C::SMEM_BYTES, st>>>(p);
+  kern<<<grid, FwdCfg<D, DT>::THREADS, smem, st>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
+
+bool fwd_prefer_one_tile(int b, int h_q, int s_q, int d, int in_dtype, bool plain, int num_sms) {
+  if (!plain || in_dtype == kE4M3 || d > 128) return false;
+  const long long two_tile_ctas = static_cast<long long>(b) * h_q * ((s_q + 255) / 256);
+  return two_tile_ctas < num_sms;
+}
 
 int fwd_q_tiles(int d, int in_dtype) {
   (void)in_dtype;
