@@ -353,8 +353,14 @@ sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const void* k, co
   prm.bias_sb = p->bias_strides.b;
   prm.bias_sh = p->bias_strides.h;
   prm.bias_ss = p->bias_strides.s;
-  prm.one_tile = sdpa::fwd_prefer_one_tile(p->b, p->h_q, p->s_q, p->d, p->in_dtype,
-                                          !prm.alibi && !prm.drop_rows && !prm.bias, num_sms()) ? 1 : 0;
+  const bool plain = !prm.alibi && !prm.drop_rows && !prm.bias;
+  prm.one_tile = sdpa::fwd_prefer_one_tile(p->b, p->h_q, p->s_q, p->d, p->in_dtype, plain, num_sms()) ? 1 : 0;
+  // SDPA_FWD_Q_TILES=1 or 2 overrides the choice where both schedules exist (plain 16-bit,
+  // d <= 128): a switch for testing and tuning.
+  if (const char* qt = std::getenv("SDPA_FWD_Q_TILES")) {
+    if (plain && p->in_dtype != SDPA_DTYPE_E4M3 && p->d <= 128 && (qt[0] == '1' || qt[0] == '2'))
+      prm.one_tile = qt[0] == '1' ? 1 : 0;
+  }
   const int rows_per_cta = 128 * (prm.one_tile ? 1 : sdpa::fwd_q_tiles(p->d, p->in_dtype));
   prm.num_m_blocks = (p->s_q + rows_per_cta - 1) / rows_per_cta;
   prm.scale_log2 = scale_log2_of(p->attn_scale);
