@@ -95,7 +95,9 @@ class ClockSampler:
     def __init__(self, bus_id: str | None):
         self.bus_id = (bus_id or "").lower()
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        import tempfile
+        fd, self.path = tempfile.mkstemp(prefix="sdpa_clocks_", suffix=".csv")
+        os.close(fd)
 
     def start(self):
         try:
@@ -124,6 +126,10 @@ class ClockSampler:
             if self.bus_id and self.bus_id not in parts[1].lower():
                 continue
             rows.append(parts)
+        try:
+            os.unlink(self.path)
+        except OSError:
+            pass
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
         sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
