@@ -4,9 +4,11 @@
  * What it computes.  For every batch b and query head hq (KV head hk = hq / (h_q / h_kv)):
  *
  *     S   = attn_scale * Q K^T                  (scores, then the scale)
- *     S  += mask   (causal: -inf where key j > query i; otherwise no mask)
+ *     S  += bias                                 (optional: ALiBi, or a bias tensor)
+ *     S  += mask   (causal: -inf where key j > query i, top-left or bottom-right aligned;
+ *                   variable lengths: -inf on padded keys; otherwise no mask)
  *     P   = softmax(S) over each row
- *     O   = P V                                  (O has Q's shape)
+ *     O   = (P * keep / (1 - p)) V               (optional dropout; O has Q's shape)
  *     LSE = log(sum_j exp(S_ij))                 (natural log, per query row)
  *
  * [attention codelab "Speeding up attention on GPU with cuDNN and TransformerEngine",
@@ -14,9 +16,11 @@
  *  cuDNN 9 blog "Accelerating Transformers with NVIDIA cuDNN 9", "SDPA as a cuDNN
  *  graph", Fig. 4 (BMM1 -> scale -> causal mask -> softmax -> BMM2); the SDPA node's
  *  second output "stats" is the per-row statistic kept for training, read here as the
- *  log-sum-exp.]  The backward pass returns dQ, dK, dV of O for an incoming dO, using the
- *  LSE kept by the forward pass (the blog's "fprop + bprop" figure; the pages give no
- *  formula, the derivative is the analytic one).
+ *  log-sum-exp; the walkthrough's options bias, use_alibi_mask, use_padding_mask with
+ *  seq_len_q / seq_len_kv, and dropout; the codelab's §10 FP8 recipe.]  The backward pass
+ *  returns dQ, dK, dV (and, on request, the bias gradient) for an incoming dO, using the LSE
+ *  kept by the forward pass (the blog's "fprop + bprop" figure; the pages give no formula,
+ *  the derivative is the analytic one).
  *
  * Conventions shared by every entry point
  *  - All tensors are *logical* BHSD [b][h][s][d] views over caller memory described by
