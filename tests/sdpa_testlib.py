@@ -171,10 +171,12 @@ def assert_lse_close(l_gpu: np.ndarray, l_ref: np.ndarray):
 ZERO_GRAD_ABS = 1e-4
 
 
-def assert_grad_close(g_gpu: np.ndarray, g_ref: np.ndarray, what: str):
+def assert_grad_close(g_gpu: np.ndarray, g_ref: np.ndarray, what: str, zero_tol: float = ZERO_GRAD_ABS):
+    """Relative L2 within GRAD_REL_L2; where the exact gradient is identically zero, every
+    entry within zero_tol (the caller may pass a bound derived from its inputs)."""
     assert np.isfinite(g_gpu).all(), f"{what}: non-finite values"
     if np.abs(g_ref).max() == 0.0:
-        assert np.abs(g_gpu).max() <= ZERO_GRAD_ABS, f"{what}: should vanish, max {np.abs(g_gpu).max():.3e}"
+        assert np.abs(g_gpu).max() <= zero_tol, f"{what}: should vanish, max {np.abs(g_gpu).max():.3e}"
         return
     e = rel_l2(g_gpu, g_ref)
     assert e <= GRAD_REL_L2, f"{what}: rel-L2 {e:.3e}"
