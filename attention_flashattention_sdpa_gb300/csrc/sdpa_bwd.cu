@@ -258,7 +258,11 @@ template <int D>
 struct BwdCfg {
   static constexpr int TILE = kBlockM * D * 2;        // one 128-row tile of Q, K, V or dO
   static constexpr int NCHUNK = D / 64;               // 128-byte chunks along d
-  static constexpr int NSLOT = (D == 64) ? 4 : 3;     // Q / dO ring
+  // Q / dO tiles: slots 0 and 1 hold Q of alternate steps (Q is read until dK of its step),
+  // the remaining NDO slots hold dO (read until dV, early in its step), so the next step's dO
+  // can load while the current step's dQ and dK run.
+  static constexpr int NSLOT = (D == 64) ? 4 : 3;
+  static constexpr int NDO = NSLOT - 2;
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = TILE;
   static constexpr int OFF_RING = 2 * TILE;
@@ -413,14 +417,16 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         tma_load_4d(sK + c * 16384, &p.tm_k, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
         tma_load_4d(sV + c * 16384, &p.tm_v, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
       }
-      int it = 0;
+      int nq = 0, nd = 0;   // Q and dO tiles issued
       bool ok = true;
       for (int n = 0; n < n_iter && ok; ++n) {
         const int hq = iter_head(n), qb = iter_qblk(n);
         const int64_t vrow = (static_cast<int64_t>(bi) * p.h_q + hq) * p.s_q_pad + qb * kBlockM;
         for (int which = 0; which < 2 && ok; ++which) {
-          const int slot = it % C::NSLOT;
-          if (!mbar_wait(&bars.ring_empty[slot], ((it / C::NSLOT) & 1) ^ 1, abort_flag)) {
+          // Q(n) -> slot n % 2 (use n / 2); dO(n) -> slot 2 + n % NDO (use n / NDO).
+          const int slot = which == 0 ? (n & 1) : 2 + n % C::NDO;
+          const int use = which == 0 ? (n >> 1) : n / C::NDO;
+          if (!mbar_wait(&bars.ring_empty[slot], (use & 1) ^ 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -431,14 +437,15 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
                         qb * kBlockM, hq, bi);
           const float* vsrc = (which == 0 ? p.lse2 : p.delta) + vrow;
           bulk_load(sVec + ((n & 1) * 2 + which) * 128, vsrc, 512, &bars.ring_full[slot]);
-          ++it;
+          if (which == 0) ++nq; else ++nd;
         }
       }
       if (!ok || *abort_flag) {
         // Let copies already issued land before the CTA's shared memory is released.
         mbar_wait_drain(&bars.kv_full, 0);
-        for (int k = (it > C::NSLOT ? it - C::NSLOT : 0); k < it; ++k)
-          mbar_wait_drain(&bars.ring_full[k % C::NSLOT], (k / C::NSLOT) & 1);
+        for (int m = (nq > 2 ? nq - 2 : 0); m < nq; ++m) mbar_wait_drain(&bars.ring_full[m & 1], (m >> 1) & 1);
+        for (int m = (nd > C::NDO ? nd - C::NDO : 0); m < nd; ++m)
+          mbar_wait_drain(&bars.ring_full[2 + m % C::NDO], (m / C::NDO) & 1);
       }
     }
   } else if (warp == 1) {
@@ -451,12 +458,10 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       const uint32_t kA = smem_u32(sK), vA = smem_u32(sV), dsA = smem_u32(sDS);
       bool ok = mbar_wait(&bars.kv_full, 0, abort_flag);
       tc_fence_after();
-      int it = 0;
-      // Sᵀ = K·Qᵀ of step m into region `reg`.
-      auto issue_s = [&](int reg, int& qslot) -> bool {
-        qslot = it % C::NSLOT;
-        if (!mbar_wait(&bars.ring_full[qslot], (it / C::NSLOT) & 1, abort_flag)) return false;
-        ++it;
+      // Sᵀ = K·Qᵀ of step m into region `reg` (Q of step m is in slot m % 2).
+      auto issue_s = [&](int reg, int m, int& qslot) -> bool {
+        qslot = m & 1;
+        if (!mbar_wait(&bars.ring_full[qslot], (m >> 1) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t qB = smem_u32(sRing + qslot * C::TILE);
 #pragma unroll
@@ -469,7 +474,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         return true;
       };
       int qslot = 0, qslot_next = 0;
-      if (ok && n_iter > 0) ok = issue_s(0, qslot);
+      if (ok && n_iter > 0) ok = issue_s(0, 0, qslot);
       for (int n = 0; n < n_iter && ok; ++n) {
         const int b = n & 1;
         const uint32_t par = (n >> 1) & 1;
@@ -477,9 +482,8 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         const uint32_t Y = tmem + C::R_COL + (b ^ 1) * 128;   // dPᵀ of step n, then Sᵀ of n+1
         const uint32_t qB = smem_u32(sRing + qslot * C::TILE);
         // ---- dPᵀ = V·dOᵀ (into the region dQ of the previous step used) ----
-        const int gslot = it % C::NSLOT;
-        if (!mbar_wait(&bars.ring_full[gslot], (it / C::NSLOT) & 1, abort_flag)) { ok = false; break; }
-        ++it;
+        const int gslot = 2 + n % C::NDO;
+        if (!mbar_wait(&bars.ring_full[gslot], (n / C::NDO) & 1, abort_flag)) { ok = false; break; }
         if (n >= 1 && !mbar_wait(&bars.dq_free[b ^ 1], ((n - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
         tc_fence_after();
         const uint32_t gB = smem_u32(sRing + gslot * C::TILE);
@@ -503,7 +507,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         // ---- Sᵀ of the next step, as soon as dPᵀ has left region Y ----
         if (n + 1 < n_iter) {
           if (!mbar_wait(&bars.dp_consumed[b], par, abort_flag)) { ok = false; break; }
-          if (!issue_s(b ^ 1, qslot_next)) { ok = false; break; }
+          if (!issue_s(b ^ 1, n + 1, qslot_next)) { ok = false; break; }
         }
         // ---- dQ = dS·K first (its drain gates the next dPᵀ), then dK += dSᵀ·Q (dS read
         //      K-major from shared memory) ----
@@ -541,7 +545,6 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     const int kv_row = j * kBlockN + r;
     const BwdScales bs = bwd_scales(p);
     bool ok = true;
-    int it = 0;
     for (int n = 0; n < n_iter; ++n) {
       const int b = n & 1;
       const uint32_t par = (n >> 1) & 1;
@@ -562,7 +565,11 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       const float* nlse2 = sVec + (b * 2 + 0) * 128 + 64 * h;    // -LSE·log2 e per column
       const float* ndelta = sVec + (b * 2 + 1) * 128 + 64 * h;   // -Delta per column
       // Pᵀ = exp2(Sᵀ·scale·log2e − LSE·log2e), masked where key > query
-      if (!mbar_wait_warp(&bars.ring_full[it % C::NSLOT], (it / C::NSLOT) & 1, abort_flag)) { ok = false; break; }
+      // This step's -LSE and -Delta vectors arrive with its Q and dO tiles.  Both waits come
+      // before Pᵀ is released: dO's slot is refilled once dV of this step has read it, and
+      // dV needs Pᵀ, so the refill cannot overtake these waits.
+      if (!mbar_wait_warp(&bars.ring_full[n & 1], (n >> 1) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars.ring_full[2 + n % C::NDO], (n / C::NDO) & 1, abort_flag)) { ok = false; break; }
       if (!mbar_wait_warp(&bars.s_full[b], par, abort_flag)) { ok = false; break; }
       tc_fence_after();
       uint32_t sv[64];
@@ -610,10 +617,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.p_full[b]);
-      ++it;
       // dSᵀ = Pᵀ ∘ (dPᵀ − Delta)
-      if (!mbar_wait_warp(&bars.ring_full[it % C::NSLOT], (it / C::NSLOT) & 1, abort_flag)) { ok = false; break; }
-      ++it;
       if (!mbar_wait_warp(&bars.dp_full[b], par, abort_flag)) { ok = false; break; }
       tc_fence_after();
       uint32_t ds[32];
