@@ -252,7 +252,9 @@ __global__ void __launch_bounds__(256) bwd_kv_convert_kernel(const BwdParams p) 
 // ---------------------------------------------------------------------------
 
 // Share of P's exponentials computed on the FMA pipe (one pair in kPolyEvery; 0 = none).
-constexpr int kPolyEvery = 4;
+// With the Q/dO ring keeping the tensor core fed, the FMA pipe is the busier one: every
+// exponential on the MUFU unit measured fastest (1 in 4 on the FMA pipe: -6%).
+constexpr int kPolyEvery = 0;
 
 template <int D>
 struct BwdCfg {
