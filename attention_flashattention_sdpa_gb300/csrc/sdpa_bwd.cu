@@ -1244,8 +1244,9 @@ cudaError_t launch_t(const BwdParams& p, cudaStream_t st) {
 }  // namespace
 
 int bwd_kv_split(int b, int h_q, int h_kv, int s_kv) {
-  // Aim for at least ~4 waves of CTAs on a 152-SM part; never split finer than one head.
-  constexpr long kTargetCtas = 608;
+  // Aim for at least ~8 waves of CTAs on a 152-SM part; never split finer than one head.
+  // (A/B on GB300: 8 waves beat 4 by 4-7% on GQA/MQA 70B shapes; 16 was no better.)
+  constexpr long kTargetCtas = 1216;
   const int group = h_q / h_kv;
   const long ctas = static_cast<long>(b) * h_kv * ((s_kv + 127) / 128);
   if (group == 1 || ctas >= kTargetCtas) return 1;
