@@ -606,9 +606,12 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         }
         pk[c / 2] = pack2(p0, p1, DT);
         if constexpr (DROP) {
-          // dV takes the kept P only; dS below takes every P.
+          // dV takes the kept P only; dS below takes every P.  A zero of either 16-bit type
+          // is all zero bits, so the kept pair is the packed pair with dropped halves cleared:
+          // the two keep bits spread to 0x0000FFFF / 0xFFFF0000 lane masks.
           const uint32_t w = (c < 32) ? keep.x : keep.y;
-          pm[c / 2] = pack2((w >> (c % 32)) & 1u ? p0 : 0.f, (w >> (c % 32)) & 2u ? p1 : 0.f, DT);
+          const uint32_t bits = (w >> (c % 32)) & 3u;
+          pm[c / 2] = pk[c / 2] & (((bits * 0x8001u) & 0x00010001u) * 0xFFFFu);
         }
       }
       if constexpr (DROP) {

@@ -13,6 +13,7 @@ Prints one JSON line (rank 0).  Flags:
   --profile-step                  run one untimed fwd+bwd (the command profiled with ncu)
   --profile-workload NAME         one untimed fwd (+bwd) of a --sweep workload, for ncu
   --sweep                         one line per configuration (tables; not the contract line)
+  --only A,B                      with --sweep: only the named configurations
   --measure-peaks                 dense GEMM peaks of this GPU through the vendor library:
                                   bf16 (torch.matmul) and E4M3 (torch._scaled_mm), 8192^3
 """
@@ -532,8 +533,9 @@ def run_sweep(args):
         peaks["e4m3_tflops"] = gemm_peak_tflops("e4m3")
     except Exception:  # no FP8 GEMM in this torch build: report no FP8 fraction
         peaks["e4m3_tflops"] = None
+    only = set(args.only.split(",")) if args.only else None
     for w in all_workloads():
-        if w.name.startswith("tiny"):
+        if w.name.startswith("tiny") or (only is not None and w.name not in only):
             continue
         try:
             line = sweep_one(w, peaks, args)
@@ -680,6 +682,7 @@ def main(argv=None):
     ap.add_argument("--profile-step", action="store_true")
     ap.add_argument("--profile-workload", default=None)
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--only", default=None, help="--sweep: comma-separated workload names")
     ap.add_argument("--measure-peaks", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
