@@ -820,7 +820,8 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
 // 64-row query blocks, and computes its half of dQ transposed (dQᵀ = Kᵀ·dSᵀ: rows = its 128
 // d indices, so M stays 128) into a transposed fp32 accumulator [b·h_q][d][s_q_pad].  Both
 // halves compute the full-d reductions Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ.  One thread issues the
-// copies and MMAs and the phases of a step run one after another.
+// copies and MMAs and the phases of a step run one after another, except that the next
+// step's Q and dO tiles are loaded while this step's dQᵀ is drained.
 struct D256 {
   static constexpr int BQ = 64;                  // query rows per step
   static constexpr int OFF_K = 0;                // 128 x 256: four 16 KB chunks of 64 columns
@@ -906,28 +907,35 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
   const uint32_t fmt = (DT == kBF16) ? 1u : 0u;
   const BwdScales bs = bwd_scales(p);
 
+  // Q, dO and the -LSE/-Delta vectors of step n (one thread).
+  auto load_step = [&](int n) {
+    const int hq = head0 + n / per_head;
+    const int q0 = (q_first + n % per_head) * C::BQ;
+    const int64_t vrow = (static_cast<int64_t>(bi) * p.h_q + hq) * p.s_q_pad + q0;
+    mbar_arrive_expect_tx(&bars.ld_full, 2 * 32768 + 512);
+    for (int c = 0; c < 4; ++c) {
+      tma_load_4d(sQ + c * 8192, &p.tm_q, &bars.ld_full, c * 64, q0, hq, bi);
+      tma_load_4d(sdO + c * 8192, &p.tm_do, &bars.ld_full, c * 64, q0, hq, bi);
+    }
+    bulk_load(sVec, p.lse2 + vrow, 256, &bars.ld_full);
+    bulk_load(sVec + 64, p.delta + vrow, 256, &bars.ld_full);
+  };
   if (threadIdx.x == 0) {
     mbar_arrive_expect_tx(&bars.kv_full, 2 * 65536);
     for (int c = 0; c < 4; ++c) {
       tma_load_4d(sK + c * 16384, &p.tm_k, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
       tma_load_4d(sV + c * 16384, &p.tm_v, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
     }
+    if (n_iter > 0) load_step(0);
   }
   bool ok = __syncthreads_and(mbar_wait(&bars.kv_full, 0, abort_flag));
   uint32_t ph_ld = 0, ph_mma = 0;
   for (int n = 0; n < n_iter && ok; ++n) {
     const int hq = head0 + n / per_head;
     const int q0 = (q_first + n % per_head) * C::BQ;
-    const int64_t vrow = (static_cast<int64_t>(bi) * p.h_q + hq) * p.s_q_pad + q0;
-    if (threadIdx.x == 0) {
-      mbar_arrive_expect_tx(&bars.ld_full, 2 * 32768 + 512);
-      for (int c = 0; c < 4; ++c) {
-        tma_load_4d(sQ + c * 8192, &p.tm_q, &bars.ld_full, c * 64, q0, hq, bi);
-        tma_load_4d(sdO + c * 8192, &p.tm_do, &bars.ld_full, c * 64, q0, hq, bi);
-      }
-      bulk_load(sVec, p.lse2 + vrow, 256, &bars.ld_full);
-      bulk_load(sVec + 64, p.delta + vrow, 256, &bars.ld_full);
-    }
+    // The previous step's dQᵀ reduce-adds read the staging buffer and the dS buffer: both
+    // are rewritten below, after this barrier.
+    if (threadIdx.x == 0) bulk_wait_read<0>();
     ok = __syncthreads_and(mbar_wait(&bars.ld_full, ph_ld, abort_flag));
     ph_ld ^= 1;
     if (!ok) break;
@@ -1045,7 +1053,11 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
     ph_mma ^= 1;
     if (!ok) break;
     tc_fence_after();
-    // ---- dQᵀ: row r of this half of d, 64 query columns in two 32-column chunks ----
+    // Every MMA of this step has read Q, dO and dS, and the vectors were read above: the
+    // next step's tiles may land while dQᵀ is drained.
+    if (threadIdx.x == 0 && n + 1 < n_iter) load_step(n + 1);
+    // ---- dQᵀ: row r of this half of d, 64 query columns as two 32-column chunks, staged
+    // in the staging buffer and in the (now free) dS buffer ----
     {
       uint32_t v[64];
       tmem_ld32(tmem + lane_base + C::COL_DQ, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
@@ -1053,23 +1065,27 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
       tmem_ld_wait();
       tc_fence_before();
       const int drow = (bi * p.h_q + hq) * 256 + dh * 128;
+#pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
-        uint8_t* rowp = sST + r * 128;
+        uint8_t* rowp = (ch == 0 ? sST : sDS) + r * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
           *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) =
               make_uint4(v[ch * 32 + u * 4], v[ch * 32 + u * 4 + 1], v[ch * 32 + u * 4 + 2],
                          v[ch * 32 + u * 4 + 3]);
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-          tma_reduce_add_2d(&p.tm_dqacc, sST, q0 + ch * 32, drow);
-          tma_store_commit();
-          bulk_wait_read<0>();
-        }
-        __syncthreads();
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        tma_reduce_add_2d(&p.tm_dqacc, sST, q0, drow);
+        tma_reduce_add_2d(&p.tm_dqacc, sDS, q0 + 32, drow);
+        tma_store_commit();
       }
     }
+  }
+  if (threadIdx.x == 0) {
+    bulk_wait_read<0>();
+    tma_store_wait_all();
   }
 
   // ---- epilogue: this half of dV and dK ----
