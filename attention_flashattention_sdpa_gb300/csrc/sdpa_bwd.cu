@@ -820,8 +820,9 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
 // 64-row query blocks, and computes its half of dQ transposed (dQᵀ = Kᵀ·dSᵀ: rows = its 128
 // d indices, so M stays 128) into a transposed fp32 accumulator [b·h_q][d][s_q_pad].  Both
 // halves compute the full-d reductions Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ.  One thread issues the
-// copies and MMAs and the phases of a step run one after another, except that the next
-// step's Q and dO tiles are loaded while this step's dQᵀ is drained.
+// copies and MMAs.  Within a step, Pᵀ is computed while the dPᵀ MMAs run and dS while the dV
+// MMAs run; the next step's Q and dO tiles are loaded while this step's dS and dQᵀ are
+// computed and drained.
 struct D256 {
   static constexpr int BQ = 64;                  // query rows per step
   static constexpr int OFF_K = 0;                // 128 x 256: four 16 KB chunks of 64 columns
@@ -838,13 +839,13 @@ struct D256 {
 static_assert(D256::SMEM_BYTES <= 232448, "shared memory budget");
 
 struct alignas(8) D256Barriers {
-  uint64_t kv_full, ld_full, mma_done;
+  uint64_t kv_full, ld_far, ld_near, s_done, dp_done, mma_done;
   uint32_t tmem_base;
   int abort;
 };
 
 template <int DT, int FEAT>
-__global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant__ BwdParams p) {
   using C = D256;
   constexpr bool ALIBI = (FEAT & kFeatAlibi) != 0;
   constexpr bool DROP = (FEAT & kFeatDropout) != 0;
@@ -865,6 +866,10 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
   float* sVec = reinterpret_cast<float*>(smem + C::OFF_VEC);
   const int warp = threadIdx.x / 32;
   const int r = threadIdx.x;                     // TMEM lane: key row, or d row of dQᵀ
+  // Warps 0-3 compute (one key row, or one d row of dQᵀ, per thread); one thread of warp 4
+  // issues every copy and MMA, so that no compute warp waits on the issue.
+  constexpr int kIssuer = 128;
+  const bool compute = threadIdx.x < 128;
   const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
 
   // Launch order: the two d-halves of a unit side by side, units fastest, KV blocks slowest
@@ -890,7 +895,10 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
 
   if (threadIdx.x == 0) {
     mbar_init(&bars.kv_full, 1);
-    mbar_init(&bars.ld_full, 1);
+    mbar_init(&bars.ld_far, 1);
+    mbar_init(&bars.ld_near, 1);
+    mbar_init(&bars.s_done, 1);
+    mbar_init(&bars.dp_done, 1);
     mbar_init(&bars.mma_done, 1);
     bars.abort = 0;
     fence_mbar_init();
@@ -907,26 +915,40 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
   const uint32_t fmt = (DT == kBF16) ? 1u : 0u;
   const BwdScales bs = bwd_scales(p);
 
-  // Q, dO and the -LSE/-Delta vectors of step n (one thread).
-  auto load_step = [&](int n) {
+  // Q and dO tiles of step n (one thread), in two parts: the d-half this CTA does not own
+  // (read only by the Sᵀ and dPᵀ MMAs, so it can be refilled once those are done), and its
+  // own d-half with the -LSE/-Delta vectors (refilled after the step's last MMAs).
+  auto load_far = [&](int n) {
+    const int hq = head0 + n / per_head;
+    const int q0 = (q_first + n % per_head) * C::BQ;
+    mbar_arrive_expect_tx(&bars.ld_far, 32768);
+    for (int c = 2 * (1 - dh); c < 2 * (1 - dh) + 2; ++c) {
+      tma_load_4d(sQ + c * 8192, &p.tm_q, &bars.ld_far, c * 64, q0, hq, bi);
+      tma_load_4d(sdO + c * 8192, &p.tm_do, &bars.ld_far, c * 64, q0, hq, bi);
+    }
+  };
+  auto load_near = [&](int n) {
     const int hq = head0 + n / per_head;
     const int q0 = (q_first + n % per_head) * C::BQ;
     const int64_t vrow = (static_cast<int64_t>(bi) * p.h_q + hq) * p.s_q_pad + q0;
-    mbar_arrive_expect_tx(&bars.ld_full, 2 * 32768 + 512);
-    for (int c = 0; c < 4; ++c) {
-      tma_load_4d(sQ + c * 8192, &p.tm_q, &bars.ld_full, c * 64, q0, hq, bi);
-      tma_load_4d(sdO + c * 8192, &p.tm_do, &bars.ld_full, c * 64, q0, hq, bi);
+    mbar_arrive_expect_tx(&bars.ld_near, 32768 + 512);
+    for (int c = 2 * dh; c < 2 * dh + 2; ++c) {
+      tma_load_4d(sQ + c * 8192, &p.tm_q, &bars.ld_near, c * 64, q0, hq, bi);
+      tma_load_4d(sdO + c * 8192, &p.tm_do, &bars.ld_near, c * 64, q0, hq, bi);
     }
-    bulk_load(sVec, p.lse2 + vrow, 256, &bars.ld_full);
-    bulk_load(sVec + 64, p.delta + vrow, 256, &bars.ld_full);
+    bulk_load(sVec, p.lse2 + vrow, 256, &bars.ld_near);
+    bulk_load(sVec + 64, p.delta + vrow, 256, &bars.ld_near);
   };
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == kIssuer) {
     mbar_arrive_expect_tx(&bars.kv_full, 2 * 65536);
     for (int c = 0; c < 4; ++c) {
       tma_load_4d(sK + c * 16384, &p.tm_k, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
       tma_load_4d(sV + c * 16384, &p.tm_v, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
     }
-    if (n_iter > 0) load_step(0);
+    if (n_iter > 0) {
+      load_far(0);
+      load_near(0);
+    }
   }
   bool ok = __syncthreads_and(mbar_wait(&bars.kv_full, 0, abort_flag));
   uint32_t ph_ld = 0, ph_mma = 0;
@@ -935,12 +957,14 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
     const int q0 = (q_first + n % per_head) * C::BQ;
     // The previous step's dQᵀ reduce-adds read the staging buffer and the dS buffer: both
     // are rewritten below, after this barrier.
-    if (threadIdx.x == 0) bulk_wait_read<0>();
-    ok = __syncthreads_and(mbar_wait(&bars.ld_full, ph_ld, abort_flag));
+    if (threadIdx.x == kIssuer) bulk_wait_read<0>();
+    ok = __syncthreads_and(mbar_wait(&bars.ld_far, ph_ld, abort_flag) &&
+                           mbar_wait(&bars.ld_near, ph_ld, abort_flag));
     ph_ld ^= 1;
     if (!ok) break;
-    // ---- Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ over all of d ----
-    if (threadIdx.x == 0) {
+    // ---- Sᵀ = K·Qᵀ, then dPᵀ = V·dOᵀ, over all of d: committed separately, so that Pᵀ is
+    // computed while the dPᵀ MMAs run ----
+    if (threadIdx.x == kIssuer) {
       tc_fence_after();
       const uint32_t idesc_s = make_idesc(fmt, 128, C::BQ, false, false);
 #pragma unroll
@@ -948,45 +972,43 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
         const uint32_t oa = (k / 4) * 16384 + (k % 4) * 32, ob = (k / 4) * 8192 + (k % 4) * 32;
         mma_ss(tmem + C::COL_S, make_sdesc_sw128(smem_u32(sK) + oa, 16, 1024),
                make_sdesc_sw128(smem_u32(sQ) + ob, 16, 1024), idesc_s, k > 0, false);
+      }
+      tc_commit(&bars.s_done);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const uint32_t oa = (k / 4) * 16384 + (k % 4) * 32, ob = (k / 4) * 8192 + (k % 4) * 32;
         mma_ss(tmem + C::COL_DP, make_sdesc_sw128(smem_u32(sV) + oa, 16, 1024),
                make_sdesc_sw128(smem_u32(sdO) + ob, 16, 1024), idesc_s, k > 0, false);
       }
-      tc_commit(&bars.mma_done);
+      tc_commit(&bars.dp_done);
     }
-    ok = __syncthreads_and(mbar_wait(&bars.mma_done, ph_mma, abort_flag));
-    ph_mma ^= 1;
-    if (!ok) break;
-    tc_fence_after();
-    // ---- Pᵀ (to TMEM, over Sᵀ) and dS (to shared memory) for key row r ----
-    {
-      uint32_t sv[64], dpv[64];
+    const bool need_mask = (p.causal && (q0 + L.off < j * kBlockN + kBlockN - 1)) ||
+                           (j * kBlockN + kBlockN > L.len_kv);
+    int lim = p.causal ? kv_row - q0 - L.off : -(1 << 30);  // column c visible iff c >= lim
+    if (kv_row >= L.len_kv) lim = 1 << 30;
+    // Dropout: keep bits of this key row for the 64 query columns (transposed mask).
+    uint2 keep = make_uint2(0u, 0u);
+    if (DROP && compute && kv_row < p.s_kv)
+      keep = __ldg(reinterpret_cast<const uint2*>(
+          p.drop_cols + ((static_cast<int64_t>(bi) * p.h_q + hq) * p.s_kv + kv_row) * p.drop_q_words + q0 / 32));
+    float pf[64];                                  // Pᵀ of key row r (every P, for dS)
+    // ---- Pᵀ for key row r, over Sᵀ in TMEM (the kept P under dropout: dV's operand) ----
+    bool w_ok = !compute || mbar_wait(&bars.s_done, ph_mma, abort_flag);
+    if (w_ok && compute) {
+      tc_fence_after();
+      uint32_t sv[64];
       tmem_ld32(tmem + lane_base + C::COL_S, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
       tmem_ld32(tmem + lane_base + C::COL_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-      tmem_ld32(tmem + lane_base + C::COL_DP, *reinterpret_cast<uint32_t(*)[32]>(&dpv[0]));
-      tmem_ld32(tmem + lane_base + C::COL_DP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dpv[32]));
       tmem_ld_wait();
-      const bool need_mask = (p.causal && (q0 + L.off < j * kBlockN + kBlockN - 1)) ||
-                             (j * kBlockN + kBlockN > L.len_kv);
-      int lim = p.causal ? kv_row - q0 - L.off : -(1 << 30);  // column c visible iff c >= lim
-      if (kv_row >= L.len_kv) lim = 1 << 30;
       const float2 sc2 = make_float2(bs.s_log2, bs.s_log2);
       // ALiBi: the key-row part of the bias (the column part is in the -LSE vector, relative
       // to the 128-aligned block that holds this 64-row query block).
       const float kr = ALIBI ? alibi_slope_log2(p, hq) *
                                    static_cast<float>(kv_row - (q0 / kBlockM) * kBlockM - L.off) : 0.f;
       const float2 kr2 = make_float2(kr, kr);
-      // Dropout: keep bits of this key row for the 64 query columns (transposed mask).
-      uint2 keep = make_uint2(0u, 0u);
-      if (DROP && kv_row < p.s_kv)
-        keep = __ldg(reinterpret_cast<const uint2*>(
-            p.drop_cols + ((static_cast<int64_t>(bi) * p.h_q + hq) * p.s_kv + kv_row) * p.drop_q_words + q0 / 32));
-      const float2 rk2 = make_float2(bs.dp, bs.dp);
       uint4 bz[BIAS ? 8 : 1];
       if constexpr (BIAS) load_bias_t(p, bi, hq, kv_row, q0, bz);
-      // Both d-halves compute the same dS: the first half alone adds it to the bias gradient.
-      float* dbrow = (DBIAS && dh == 0) ? dbias_row(p, bi, hq, kv_row, q0) : nullptr;
-      float2 dbhold = make_float2(0.f, 0.f);
-      uint32_t pk[32], ds[32];
+      uint32_t pk[32];
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
         float2 nl = *reinterpret_cast<const float2*>(sVec + c);
@@ -998,46 +1020,75 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
           if (c < lim) p0 = 0.f;
           if (c + 1 < lim) p1 = 0.f;
         }
-        float2 dp = make_float2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]));
-        const float2 nd = *reinterpret_cast<const float2*>(sVec + 64 + c);
-        float2 t;
+        pf[c] = p0;
+        pf[c + 1] = p1;
         if constexpr (DROP) {
-          // dV takes the kept P only; dS = P * (keep / (1 - p) * dO·Vᵀ - Delta) takes every P.
           const uint32_t w = (c < 32) ? keep.x : keep.y;
-          const bool k0 = (w >> (c % 32)) & 1u, k1 = (w >> (c % 32)) & 2u;
-          pk[c / 2] = pack2(k0 ? p0 : 0.f, k1 ? p1 : 0.f, DT);
-          dp.x = k0 ? dp.x : 0.f;
-          dp.y = k1 ? dp.y : 0.f;
-          t = fma2(dp, rk2, nd);
+          pk[c / 2] = pack2((w >> (c % 32)) & 1u ? p0 : 0.f, (w >> (c % 32)) & 2u ? p1 : 0.f, DT);
         } else {
           pk[c / 2] = pack2(p0, p1, DT);
-          t = fma2(dp, rk2, nd);
         }
-        const float2 dd = mul2(make_float2(p0, p1), t);
+      }
+      tmem_st32(tmem + lane_base + C::COL_S, pk);
+      tmem_st_wait();
+      tc_fence_before();
+    }
+    ok = __syncthreads_and(w_ok);
+    if (!ok) break;
+    // ---- dV_h += Pᵀ·dO_h (runs while dS is computed) ----
+    const uint32_t idesc_acc = make_idesc(fmt, 128, 128, false, true);
+    if (threadIdx.x == kIssuer) {
+      tc_fence_after();
+      const uint32_t gh = smem_u32(sdO) + dh * 2 * 8192;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        mma_ts(tmem + C::COL_DV, tmem + C::COL_S + k * 8, make_sdesc_sw128(gh + k * 2048, 8192, 1024),
+               idesc_acc, (n > 0 || k > 0) ? 1u : 0u, false);
+    }
+    // ---- dS = P ∘ (dPᵀ − Delta) for key row r, to shared memory ----
+    w_ok = mbar_wait(&bars.dp_done, ph_mma, abort_flag);
+    // The Sᵀ and dPᵀ MMAs are done: the other d-half of Q and dO may be refilled.
+    if (threadIdx.x == kIssuer && w_ok && n + 1 < n_iter) load_far(n + 1);
+    if (w_ok && compute) {
+      tc_fence_after();
+      uint32_t dpv[64];
+      tmem_ld32(tmem + lane_base + C::COL_DP, *reinterpret_cast<uint32_t(*)[32]>(&dpv[0]));
+      tmem_ld32(tmem + lane_base + C::COL_DP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dpv[32]));
+      tmem_ld_wait();
+      const float2 rk2 = make_float2(bs.dp, bs.dp);
+      // Both d-halves compute the same dS: the first half alone adds it to the bias gradient.
+      float* dbrow = (DBIAS && dh == 0) ? dbias_row(p, bi, hq, kv_row, q0) : nullptr;
+      float2 dbhold = make_float2(0.f, 0.f);
+      uint32_t ds[32];
+#pragma unroll
+      for (int c = 0; c < 64; c += 2) {
+        float2 dp = make_float2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]));
+        const float2 nd = *reinterpret_cast<const float2*>(sVec + 64 + c);
+        if constexpr (DROP) {
+          // dS = P * (keep / (1 - p) * dO·Vᵀ - Delta) takes every P.
+          const uint32_t w = (c < 32) ? keep.x : keep.y;
+          dp.x = (w >> (c % 32)) & 1u ? dp.x : 0.f;
+          dp.y = (w >> (c % 32)) & 2u ? dp.y : 0.f;
+        }
+        const float2 dd = mul2(make_float2(pf[c], pf[c + 1]), fma2(dp, rk2, nd));
         ds[c / 2] = pack2(dd.x, dd.y, DT);
         if constexpr (DBIAS) dbias_emit(dbrow, c, dd, dbhold);
       }
-      tmem_st32(tmem + lane_base + C::COL_S, pk);
       uint8_t* rowp = sDS + r * 128;
 #pragma unroll
       for (int u = 0; u < 8; ++u)
         *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) =
             make_uint4(ds[u * 4], ds[u * 4 + 1], ds[u * 4 + 2], ds[u * 4 + 3]);
-      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
     }
-    __syncthreads();
-    // ---- dV_h += Pᵀ·dO_h, dK_h += dSᵀ·Q_h, dQᵀ_h = K_hᵀ·dSᵀ ----
-    if (threadIdx.x == 0) {
+    ok = __syncthreads_and(w_ok);
+    if (!ok) break;
+    // ---- dK_h += dSᵀ·Q_h, dQᵀ_h = K_hᵀ·dSᵀ ----
+    if (threadIdx.x == kIssuer) {
       tc_fence_after();
-      const uint32_t idesc_acc = make_idesc(fmt, 128, 128, false, true);
       const uint32_t idesc_dq = make_idesc(fmt, 128, C::BQ, true, true);
-      const uint32_t qh = smem_u32(sQ) + dh * 2 * 8192, gh = smem_u32(sdO) + dh * 2 * 8192;
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ts(tmem + C::COL_DV, tmem + C::COL_S + k * 8, make_sdesc_sw128(gh + k * 2048, 8192, 1024),
-               idesc_acc, (n > 0 || k > 0) ? 1u : 0u, false);
+      const uint32_t qh = smem_u32(sQ) + dh * 2 * 8192;
 #pragma unroll
       for (int k = 0; k < 4; ++k)
         mma_ss(tmem + C::COL_DK, make_sdesc_sw128(smem_u32(sDS) + k * 32, 16, 1024),
@@ -1054,17 +1105,16 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
     if (!ok) break;
     tc_fence_after();
     // Every MMA of this step has read Q, dO and dS, and the vectors were read above: the
-    // next step's tiles may land while dQᵀ is drained.
-    if (threadIdx.x == 0 && n + 1 < n_iter) load_step(n + 1);
+    // rest of the next step's tiles may land while dQᵀ is drained.
+    if (threadIdx.x == kIssuer && n + 1 < n_iter) load_near(n + 1);
     // ---- dQᵀ: row r of this half of d, 64 query columns as two 32-column chunks, staged
     // in the staging buffer and in the (now free) dS buffer ----
-    {
+    if (compute) {
       uint32_t v[64];
       tmem_ld32(tmem + lane_base + C::COL_DQ, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
       tmem_ld32(tmem + lane_base + C::COL_DQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       tmem_ld_wait();
       tc_fence_before();
-      const int drow = (bi * p.h_q + hq) * 256 + dh * 128;
 #pragma unroll
       for (int ch = 0; ch < 2; ++ch) {
         uint8_t* rowp = (ch == 0 ? sST : sDS) + r * 128;
@@ -1075,15 +1125,16 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
                          v[ch * 32 + u * 4 + 3]);
       }
       fence_proxy_async_smem();
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        tma_reduce_add_2d(&p.tm_dqacc, sST, q0, drow);
-        tma_reduce_add_2d(&p.tm_dqacc, sDS, q0 + 32, drow);
-        tma_store_commit();
-      }
+    }
+    __syncthreads();
+    if (threadIdx.x == kIssuer) {
+      const int drow = (bi * p.h_q + hq) * 256 + dh * 128;
+      tma_reduce_add_2d(&p.tm_dqacc, sST, q0, drow);
+      tma_reduce_add_2d(&p.tm_dqacc, sDS, q0 + 32, drow);
+      tma_store_commit();
     }
   }
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == kIssuer) {
     bulk_wait_read<0>();
     tma_store_wait_all();
   }
@@ -1093,7 +1144,7 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
   if (ok) {
     const uint32_t acc_v = tmem + lane_base + C::COL_DV, acc_k = tmem + lane_base + C::COL_DK;
     if (p.kv_split > 1) {
-      if (n_iter > 0) {
+      if (n_iter > 0 && compute) {
         float* dvp = p.dv_acc + ((static_cast<int64_t>(bi) * p.h_kv + hk) * p.s_kv_pad + kv_row) * 256 + dh * 128;
         float* dkp = p.dk_acc + ((static_cast<int64_t>(bi) * p.h_kv + hk) * p.s_kv_pad + kv_row) * 256 + dh * 128;
         for (int c = 0; c < 4; ++c) {
@@ -1114,7 +1165,7 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
       }
     } else {
       // dV_h -> sQ, dK_h -> sdO as two 64-column chunks (128 rows x 128 bytes) each.
-      for (int which = 0; which < 2; ++which) {
+      for (int which = 0; which < 2 && compute; ++which) {
         uint8_t* stage = which == 0 ? sQ : sdO;
         const uint32_t acc = which == 0 ? acc_v : acc_k;
         const float mul = which == 0 ? bs.dv : bs.dk;
@@ -1142,7 +1193,7 @@ __global__ void __launch_bounds__(128, 1) bwd_d256_kernel(const __grid_constant_
       }
       fence_proxy_async_smem();
       __syncthreads();
-      if (threadIdx.x == 0) {
+      if (threadIdx.x == kIssuer) {
         for (int c = 0; c < 2; ++c) {
           tma_store_4d(&p.tm_dv, sQ + c * 16384, (dh * 2 + c) * 64, j * kBlockN, hk, bi);
           tma_store_4d(&p.tm_dk, sdO + c * 16384, (dh * 2 + c) * 64, j * kBlockN, hk, bi);
@@ -1208,7 +1259,7 @@ cudaError_t launch_d256(const BwdParams& p, cudaStream_t st) {
   e = set_smem_once(reinterpret_cast<const void*>(kern), D256::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const unsigned grid = 2u * p.b * p.h_kv * p.kv_split * ((p.s_kv + kBlockN - 1) / kBlockN);
-  kern<<<grid, 128, D256::SMEM_BYTES, st>>>(p);
+  kern<<<grid, 160, D256::SMEM_BYTES, st>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 gdq(p.s_q_pad / 32, 256 / 32, bh);
