@@ -13,6 +13,7 @@ from __future__ import annotations
 import ctypes
 import math
 import os
+import struct
 from typing import Optional
 
 __all__ = [
@@ -62,6 +63,29 @@ class Problem(ctypes.Structure):
         ("bias", ctypes.c_void_p), ("bias_strides", Strides),
         ("dbias", ctypes.c_void_p), ("dbias_strides", Strides),
     ]
+
+
+def _packer():
+    """One struct.Struct that lays out a whole Problem at the offsets ctypes gives it, so
+    that a problem is marshalled by a single pack instead of one ctypes assignment per field."""
+    fmt, pos = ["="], 0
+    codes = {ctypes.c_int32: "i", ctypes.c_float: "f", ctypes.c_void_p: "Q"}
+    for name, typ in Problem._fields_:
+        off = getattr(Problem, name).offset
+        fmt.append("x" * (off - pos))
+        if typ is Strides:
+            fmt.append("qqqq")
+        else:
+            fmt.append(codes[typ])
+        pos = off + ctypes.sizeof(typ)
+    fmt.append("x" * (ctypes.sizeof(Problem) - pos))
+    st = struct.Struct("".join(fmt))
+    assert st.size == ctypes.sizeof(Problem)
+    return st
+
+
+_PACK = _packer()
+_NO_STRIDES = (0, 0, 0, 1)
 
 
 def causal_code(causal) -> int:
@@ -123,22 +147,43 @@ def _check(status: int):
         raise SdpaError(status, sdpa_last_error_string())
 
 
+_DTYPES = {}
+
+
 def dtype_code(t) -> int:
-    import torch
-    return {torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16,
-            torch.float8_e4m3fn: DTYPE_E4M3, torch.float8_e5m2: DTYPE_E5M2}[t.dtype]
-
-
-def _strides(t) -> Strides:
-    if t is None:
-        return Strides(0, 0, 0, 1)
-    if t.dim() != 4:
-        raise ValueError("tensors are logical [b, h, s, d] views")
-    return Strides(*t.stride())
+    if not _DTYPES:
+        import torch
+        _DTYPES.update({torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16,
+                        torch.float8_e4m3fn: DTYPE_E4M3, torch.float8_e5m2: DTYPE_E5M2})
+    return _DTYPES[t.dtype]
 
 
 def _ptr(t) -> Optional[int]:
     return None if t is None else t.data_ptr()
+
+
+def _st4(t):
+    if t is None:
+        return _NO_STRIDES
+    if t.dim() != 4:
+        raise ValueError("tensors are logical [b, h, s, d] views")
+    return t.stride()
+
+
+def _bst(t):
+    """Strides of a [b|1, h|1, s_q, s_kv] bias view; size-1 batch/head dims broadcast."""
+    if t is None:
+        return (0, 0, 0, 0)
+    st = list(t.stride())
+    if t.shape[0] == 1:
+        st[0] = 0
+    if t.shape[1] == 1:
+        st[1] = 0
+    return st
+
+
+def _p0(t) -> int:
+    return 0 if t is None else t.data_ptr()
 
 
 def make_problem(q, k, v, o=None, *, attn_scale: Optional[float] = None, causal=False,
@@ -152,34 +197,20 @@ def make_problem(q, k, v, o=None, *, attn_scale: Optional[float] = None, causal=
     is given; without slopes the library uses 2^(-8 (h + 1) / h_q)."""
     b, h_q, s_q, d = q.shape
     h_kv, s_kv = k.shape[1], k.shape[2]
-    p = Problem()
-    p.b, p.h_q, p.h_kv, p.s_q, p.s_kv, p.d = b, h_q, h_kv, s_q, s_kv, d
-    p.in_dtype = dtype_code(q)
-    p.out_dtype = dtype_code(o) if o is not None else p.in_dtype
-    p.attn_scale = (1.0 / math.sqrt(d)) if attn_scale is None else float(attn_scale)
-    p.causal = causal_code(causal)
-    p.q, p.k, p.v, p.o = _strides(q), _strides(k), _strides(v), _strides(o)
-    p.dout, p.dq, p.dk, p.dv = _strides(dout), _strides(dq), _strides(dk), _strides(dv)
-    p.descale_q, p.descale_k, p.descale_v = _ptr(descale_q), _ptr(descale_k), _ptr(descale_v)
-    p.seq_lens_q, p.seq_lens_kv = _ptr(seq_lens_q), _ptr(seq_lens_kv)
-    p.alibi = 1 if (alibi or alibi_slopes is not None) else 0
-    p.alibi_slopes = _ptr(alibi_slopes)
-    p.dropout_p = float(dropout_p)
-    p.dropout_mask, p.dropout_mask_t = _ptr(dropout_mask), _ptr(dropout_mask_t)
-    p.bias, p.dbias = _ptr(bias), _ptr(dbias)
-    for t, field in ((bias, "bias_strides"), (dbias, "dbias_strides")):
-        if t is not None:   # a [b|1, h|1, s_q, s_kv] view; size-1 batch/head dims broadcast
-            st = list(t.stride())
-            if t.shape[0] == 1:
-                st[0] = 0
-            if t.shape[1] == 1:
-                st[1] = 0
-            setattr(p, field, Strides(*st))
-    p.dout_dtype = dtype_code(dout) if dout is not None else p.in_dtype
-    p.descale_do = _ptr(descale_do)
-    if p.in_dtype == DTYPE_E4M3 and o is None:
-        p.out_dtype = DTYPE_BF16
-    return p
+    in_dt = dtype_code(q)
+    if o is not None:
+        out_dt = dtype_code(o)
+    else:
+        out_dt = DTYPE_BF16 if in_dt == DTYPE_E4M3 else in_dt
+    scale = (1.0 / math.sqrt(d)) if attn_scale is None else float(attn_scale)
+    return Problem.from_buffer_copy(_PACK.pack(
+        b, h_q, h_kv, s_q, s_kv, d, in_dt, out_dt, scale, causal_code(causal),
+        *_st4(q), *_st4(k), *_st4(v), *_st4(o), *_st4(dout), *_st4(dq), *_st4(dk), *_st4(dv),
+        _p0(descale_q), _p0(descale_k), _p0(descale_v), _p0(seq_lens_q), _p0(seq_lens_kv),
+        1 if (alibi or alibi_slopes is not None) else 0, _p0(alibi_slopes),
+        float(dropout_p), _p0(dropout_mask), _p0(dropout_mask_t),
+        dtype_code(dout) if dout is not None else in_dt, _p0(descale_do),
+        _p0(bias), *_bst(bias), _p0(dbias), *_bst(dbias)))
 
 
 def _stream(stream) -> int:

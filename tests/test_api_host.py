@@ -222,3 +222,95 @@ def test_bias_gradient_validation_and_workspace(m):
     p = _problem(m, bias=FAKE, dbias=FAKE, dbias_strides=(0, 128 * 128, 128, 1))
     p.bias_strides = st
     assert m.sdpa_workspace_size(p, True) - base == 2 * 128 * 128 * 4
+
+
+def _problem_by_fields(m, q, k, v, o, causal, scale, dout=None, dq=None, dk=None, dv=None, descale=None,
+                       lens=None, alibi=None, drop=None, bias=None, dbias=None):
+    """Field-by-field construction of the sdpa_problem_t that make_problem must produce."""
+    P = m.Problem()
+    P.b, P.h_q, P.s_q, P.d = q.shape
+    P.h_kv, P.s_kv = k.shape[1], k.shape[2]
+    P.in_dtype = m.dtype_code(q)
+    P.out_dtype = m.dtype_code(o) if o is not None else (
+        m.DTYPE_BF16 if P.in_dtype == m.DTYPE_E4M3 else P.in_dtype)
+    P.attn_scale = scale
+    P.causal = m.causal_code(causal)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout), ("dq", dq), ("dk", dk), ("dv", dv)):
+        setattr(P, name, m.Strides(*(t.stride() if t is not None else (0, 0, 0, 1))))
+    if descale is not None:
+        P.descale_q, P.descale_k, P.descale_v = (descale.data_ptr() + 4 * i for i in range(3))
+        P.descale_do = descale.data_ptr() + 12
+    if lens is not None:
+        P.seq_lens_q, P.seq_lens_kv = lens[0].data_ptr(), lens[1].data_ptr()
+    if alibi is not None:
+        P.alibi, P.alibi_slopes = 1, alibi.data_ptr()
+    if drop is not None:
+        P.dropout_p, P.dropout_mask, P.dropout_mask_t = drop[0], drop[1].data_ptr(), drop[2].data_ptr()
+    P.dout_dtype = m.dtype_code(dout) if dout is not None else P.in_dtype
+    for t, pf, sf in ((bias, "bias", "bias_strides"), (dbias, "dbias", "dbias_strides")):
+        if t is not None:
+            st = list(t.stride())
+            st[0] = 0 if t.shape[0] == 1 else st[0]
+            st[1] = 0 if t.shape[1] == 1 else st[1]
+            setattr(P, pf, t.data_ptr())
+            setattr(P, sf, m.Strides(*st))
+    return P
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_make_problem_matches_field_by_field_struct(m, seed):
+    """make_problem packs the whole struct at once; every byte must equal the struct that
+    assigning each field through ctypes gives (CPU tensors: only shapes, strides, dtypes and
+    addresses are read)."""
+    import random
+    import torch
+    rnd = random.Random(seed)
+    dts = [torch.float16, torch.bfloat16, torch.float8_e4m3fn]
+    dt = rnd.choice(dts)
+    b, h_kv = rnd.randint(1, 3), rnd.randint(1, 3)
+    h_q, s_q, s_kv, d = h_kv * rnd.choice([1, 2, 4]), rnd.randint(1, 300), rnd.randint(1, 300), rnd.choice([64, 128, 256])
+
+    def t4(h, s):
+        if rnd.random() < 0.5:
+            return torch.empty(b, h, s, d, dtype=dt)
+        return torch.empty(b, s, h, d, dtype=dt).permute(0, 2, 1, 3)   # BSHD view
+    q, k, v = t4(h_q, s_q), t4(h_kv, s_kv), t4(h_kv, s_kv)
+    o = None if (dt == torch.float8_e4m3fn and rnd.random() < 0.5) else \
+        torch.empty(b, h_q, s_q, d, dtype=torch.bfloat16 if dt == torch.float8_e4m3fn else dt)
+    causal = rnd.choice([False, True, "bottom_right"])
+    scale = rnd.choice([None, 0.3])
+    kw, ref = {}, {}
+    if rnd.random() < 0.5:
+        kw.update(dout=torch.empty_like(q), dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v))
+        ref.update(kw)
+    if dt == torch.float8_e4m3fn:
+        ds = torch.ones(4)
+        kw.update(descale_q=ds[0:1], descale_k=ds[1:2], descale_v=ds[2:3], descale_do=ds[3:4])
+        ref["descale"] = ds
+    if rnd.random() < 0.4:
+        lq, lkv = torch.zeros(b, dtype=torch.int32), torch.zeros(b, dtype=torch.int32)
+        kw.update(seq_lens_q=lq, seq_lens_kv=lkv)
+        ref["lens"] = (lq, lkv)
+    if rnd.random() < 0.3:
+        sl = torch.ones(h_q)
+        kw["alibi_slopes"] = sl
+        ref["alibi"] = sl
+    if rnd.random() < 0.3:
+        mk, mt = torch.zeros(8, dtype=torch.int32), torch.zeros(8, dtype=torch.int32)
+        kw.update(dropout_p=0.25, dropout_mask=mk, dropout_mask_t=mt)
+        ref["drop"] = (0.25, mk, mt)
+    if rnd.random() < 0.4:
+        bias = torch.empty(rnd.choice([1, b]), rnd.choice([1, h_q]), s_q, s_kv, dtype=torch.float16)
+        kw["bias"] = ref["bias"] = bias
+        if rnd.random() < 0.5:
+            kw["dbias"] = ref["dbias"] = torch.empty_like(bias)
+    got = m.make_problem(q, k, v, o, attn_scale=scale, causal=causal, **kw)
+    want = _problem_by_fields(m, q, k, v, o, causal, (1.0 / d ** 0.5) if scale is None else scale, **ref)
+    assert bytes(got) == bytes(want)
+
+
+def test_make_problem_rejects_non_4d(m):
+    import torch
+    k = torch.empty(2, 8, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        m.make_problem(torch.empty(1, 2, 8, 64, dtype=torch.float16), k, k, None)
