@@ -116,6 +116,14 @@ __device__ __forceinline__ void load_bias_t(const BwdParams& p, int bi, int hq, 
   for (int e = 0; e < 8; ++e) bz[e] = __ldg(src + e);
 }
 
+// Starts moving the same 128-byte bias row into L2 (a later step's row: its loads then hit L2).
+__device__ __forceinline__ void prefetch_bias_t(const BwdParams& p, int bi, int hq, int kv_row, int q0) {
+  if (kv_row >= p.s_kv) return;
+  const int nb = p.bias_nb > 1 ? bi : 0, nh = p.bias_nh > 1 ? hq : 0;
+  prefetch_l2(static_cast<const uint16_t*>(p.bias_t) +
+              ((static_cast<int64_t>(nb) * p.bias_nh + nh) * p.s_kv + kv_row) * p.s_q_pad + q0);
+}
+
 // Row of the bias-gradient accumulator for key row kv_row and queries q0.. (nullptr past s_kv).
 __device__ __forceinline__ float* dbias_row(const BwdParams& p, int bi, int hq, int kv_row, int q0) {
   if (kv_row >= p.s_kv) return nullptr;
@@ -546,6 +554,16 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const int kv_row = j * kBlockN + r;
     const BwdScales bs = bwd_scales(p);
+    // Dropout: keep bits of this key row for step n's 64 query columns (transposed mask).
+    // They are loaded one step ahead: a step outlasts the latency of the (uncoalesced) load.
+    auto load_keep = [&](int n) {
+      if (!DROP || kv_row >= p.s_kv || n >= n_iter) return make_uint2(0u, 0u);
+      return __ldg(reinterpret_cast<const uint2*>(
+          p.drop_cols + ((static_cast<int64_t>(bi) * p.h_q + iter_head(n)) * p.s_kv + kv_row) * p.drop_q_words +
+          (iter_qblk(n) * kBlockM + 64 * h) / 32));
+    };
+    uint2 keep_next = load_keep(0);
+    if (BIAS && n_iter > 0) prefetch_bias_t(p, bi, iter_head(0), kv_row, iter_qblk(0) * kBlockM + 64 * h);
     bool ok = true;
     for (int n = 0; n < n_iter; ++n) {
       const int b = n & 1;
@@ -553,15 +571,16 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       const uint32_t X = tmem + lane_off + C::R_COL + b * 128;
       const uint32_t Y = tmem + lane_off + C::R_COL + (b ^ 1) * 128;
       const int q0 = iter_qblk(n) * kBlockM + 64 * h;     // first query column of this half
-      // Dropout: keep bits of this key row for the 64 query columns (transposed mask).
-      uint2 keep = make_uint2(0u, 0u);
-      if (DROP && kv_row < p.s_kv)
-        keep = __ldg(reinterpret_cast<const uint2*>(
-            p.drop_cols + ((static_cast<int64_t>(bi) * p.h_q + iter_head(n)) * p.s_kv + kv_row) * p.drop_q_words +
-            q0 / 32));
-      // Additive bias of this key row for the 64 query columns (transposed copy).
+      const uint2 keep = keep_next;
+      if constexpr (DROP) keep_next = load_keep(n + 1);
+      // Additive bias of this key row for the 64 query columns (transposed copy); the next
+      // step's row is sent to L2 first.
       uint4 bz[BIAS ? 8 : 1];
-      if constexpr (BIAS) load_bias_t(p, bi, iter_head(n), kv_row, q0, bz);
+      if constexpr (BIAS) {
+        if (n + 1 < n_iter)
+          prefetch_bias_t(p, bi, iter_head(n + 1), kv_row, iter_qblk(n + 1) * kBlockM + 64 * h);
+        load_bias_t(p, bi, iter_head(n), kv_row, q0, bz);
+      }
       // Bias gradient: this key row's 64 query columns of the transposed accumulator.
       float* dbrow = DBIAS ? dbias_row(p, bi, iter_head(n), kv_row, q0) : nullptr;
       const float* nlse2 = sVec + (b * 2 + 0) * 128 + 64 * h;    // -LSE·log2 e per column

@@ -404,9 +404,18 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       const uint32_t ph = (NQT == 2) ? (j & 1) : ((j >> 1) & 1);
       uint4 keep = make_uint4(0u, 0u, 0u, 0u);
       if (DROP && drop_row != nullptr) keep = __ldg(drop_row + kv_block(j));
-      // The bias of this row and key block, loaded before the scores arrive.
+      // The bias of this row and key block, loaded before the scores arrive; the next key
+      // block's part of the row is sent to L2 first, so those loads find it there.
       uint4 bz[BIAS ? SC / 8 : 1];
       if constexpr (BIAS) {
+        if (bias_row != nullptr && j + 1 < n_blocks) {
+          const int kn = kv_block(j + 1) * kBlockN + col0;
+          if (kn + SC <= p.s_kv) {
+#pragma unroll
+            for (int o = 0; o < SC; o += 64) prefetch_l2(bias_row + kn + o);
+            prefetch_l2(bias_row + kn + SC - 1);
+          }
+        }
         const int kb0 = kv_block(j) * kBlockN + col0;
 #pragma unroll
         for (int e = 0; e < SC / 8; ++e) {
