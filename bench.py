@@ -571,6 +571,25 @@ def graph_ms(fn, calls: int, reps: int = 10) -> float:
     return statistics.median(ts)
 
 
+def fwd_flops(w) -> float:
+    """Forward FLOPs of a workload: its own counting rule, except that workloads with
+    per-batch lengths or a bottom-right diagonal count 4*d FLOPs for every (row, key) pair
+    a row can see."""
+    if w.lens_q is None and not w.bottom_right:
+        return w.fwd_flops()
+    lq_all = w.lens_q or (w.s_q,) * w.b
+    lkv_all = w.lens_kv or (w.s_kv,) * w.b
+    pairs = 0
+    for lq, lkv in zip(lq_all, lkv_all):
+        if not w.causal:
+            pairs += lq * lkv
+            continue
+        off = lkv - lq if w.bottom_right else 0
+        for i in range(lq):   # row i sees keys j <= i + off
+            pairs += min(max(i + off + 1, 0), lkv)
+    return 4.0 * w.h_q * w.d * pairs
+
+
 def sweep_one(w, peaks, args, quick: bool = False):
     import torch
     import attention_flashattention_sdpa_gb300 as sdpa
@@ -587,6 +606,12 @@ def sweep_one(w, peaks, args, quick: bool = False):
     o = torch.empty_strided(q.shape, q.stride(), dtype=odt, device="cuda")
     lse = torch.empty(w.b, w.h_q, w.s_q, dtype=torch.float32, device="cuda") if (w.stats or w.backward) else None
     st = torch.cuda.current_stream()
+    causal = "bottom_right" if w.bottom_right else w.causal
+    if w.lens_q is not None:
+        kw["seq_lens_q"] = torch.tensor(w.lens_q, dtype=torch.int32, device="cuda")
+        kw["seq_lens_kv"] = torch.tensor(w.lens_kv, dtype=torch.int32, device="cuda")
+    ff = fwd_flops(w)
+    bf = 2.5 * ff
     mask = mask_t = None
     mask_ms = None
     if w.dropout > 0:
@@ -605,9 +630,9 @@ def sweep_one(w, peaks, args, quick: bool = False):
     if w.bias:
         g = torch.Generator(device="cuda").manual_seed(3)
         kw["bias"] = torch.randn(1, w.h_q, w.s_q, w.s_kv, device="cuda", generator=g).to(q.dtype)
-    fwd = lambda: sdpa.sdpa_fwd(q, k, v, o, lse, attn_scale=w.scale, causal=w.causal, alibi=w.alibi,
+    fwd = lambda: sdpa.sdpa_fwd(q, k, v, o, lse, attn_scale=w.scale, causal=causal, alibi=w.alibi,
                                 **kw)
-    reps = 3 if quick else max(5, min(200, int(2e13 / max(w.fwd_flops(), 1))))
+    reps = 3 if quick else max(5, min(200, int(2e13 / max(ff, 1))))
     for _ in range(3):
         fwd()
     torch.cuda.synchronize()
@@ -619,12 +644,12 @@ def sweep_one(w, peaks, args, quick: bool = False):
     torch.cuda.synchronize()
     fwd_ms = statistics.median(a.elapsed_time(b) for a, b in ts)
     peak = peaks["bf16_tflops"]
-    line = {"workload": w.name, "fwd_ms": fwd_ms, "fwd_tflops": w.fwd_flops() / fwd_ms / 1e9}
-    calls = max(4, min(64, int(2e12 / max(w.fwd_flops(), 1))))
+    line = {"workload": w.name, "fwd_ms": fwd_ms, "fwd_tflops": ff / fwd_ms / 1e9}
+    calls = max(4, min(64, int(2e12 / max(ff, 1))))
     if not quick:
         gms = graph_ms(fwd, calls)
         line["fwd_ms_graph"] = gms
-        line["fwd_tflops_graph"] = w.fwd_flops() / gms / 1e9
+        line["fwd_tflops_graph"] = ff / gms / 1e9
     if mask_ms is not None:
         line["dropout_mask_ms"] = mask_ms
     es = 1 if w.dtype == "e4m3" else 2
@@ -638,18 +663,21 @@ def sweep_one(w, peaks, args, quick: bool = False):
     if w.backward:
         do = dev(x.do)
         dkw = {} if w.dropout == 0 else {"dropout_p": w.dropout, "dropout_mask_t": mask_t}
+        if w.lens_q is not None:
+            dkw["seq_lens_q"], dkw["seq_lens_kv"] = kw["seq_lens_q"], kw["seq_lens_kv"]
         if w.bias:
             dkw["bias"] = kw["bias"]
         if w.dtype == "e4m3":   # E4M3 Q, K, V and E5M2 dO; O and the gradients in bf16
             dkw.update(kw)
             dkw["descale_do"] = torch.tensor([x.descale_do], device="cuda")
         dq, dk, dv = (torch.empty(t.shape, dtype=odt, device="cuda") for t in (q, k, v))
-        p = sdpa.make_problem(q, k, v, o, attn_scale=w.scale, causal=w.causal, dout=do, dq=dq, dk=dk, dv=dv,
+        p = sdpa.make_problem(q, k, v, o, attn_scale=w.scale, causal=causal, dout=do, dq=dq, dk=dk, dv=dv,
                               descale_q=dkw.get("descale_q"), descale_k=dkw.get("descale_k"),
                               descale_v=dkw.get("descale_v"), descale_do=dkw.get("descale_do"),
-                              bias=dkw.get("bias"))
+                              bias=dkw.get("bias"), seq_lens_q=dkw.get("seq_lens_q"),
+                              seq_lens_kv=dkw.get("seq_lens_kv"))
         ws = torch.empty(sdpa.sdpa_workspace_size(p, True), dtype=torch.uint8, device="cuda")
-        bwd = lambda: sdpa.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, attn_scale=w.scale, causal=w.causal,
+        bwd = lambda: sdpa.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, attn_scale=w.scale, causal=causal,
                                     alibi=w.alibi, **dkw)
         for _ in range(3):
             bwd()
@@ -665,9 +693,9 @@ def sweep_one(w, peaks, args, quick: bool = False):
         if not quick:
             gb = graph_ms(bwd, max(2, calls // 2))
             line["bwd_ms_graph"] = gb
-            line["bwd_tflops_graph"] = w.bwd_flops() / gb / 1e9
-        line["bwd_tflops"] = w.bwd_flops() / bwd_ms / 1e9
-        line["fwdbwd_tflops"] = (w.fwd_flops() + w.bwd_flops()) / (fwd_ms + bwd_ms) / 1e9
+            line["bwd_tflops_graph"] = bf / gb / 1e9
+        line["bwd_tflops"] = bf / bwd_ms / 1e9
+        line["fwdbwd_tflops"] = (ff + bf) / (fwd_ms + bwd_ms) / 1e9
         line["fwdbwd_frac_of_bf16_peak"] = line["fwdbwd_tflops"] / peak
     assert sdpa.sdpa_device_error() == 0
     return line

@@ -25,7 +25,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
-from typing import Optional
+from typing import Optional, Tuple
 
 import torch
 
@@ -52,13 +52,17 @@ class Workload:
     alibi: bool = False   # ALiBi position bias with the default slopes
     dropout: float = 0.0  # dropout probability (0 = off)
     bias: bool = False    # an additive [1, h_q, s_q, s_kv] bias in the input dtype
+    lens_q: Optional[Tuple[int, ...]] = None    # valid query rows per batch (padding mask)
+    lens_kv: Optional[Tuple[int, ...]] = None   # valid keys per batch
+    bottom_right: bool = False   # causal diagonal aligned to the end of each key sequence
 
     @property
     def scale(self) -> float:
         return self.attn_scale if self.attn_scale is not None else 1.0 / math.sqrt(self.d)
 
     def fwd_flops(self) -> float:
-        """4*b*h_q*s_q*s_kv*d, halved for causal (the benchmark's counting rule)."""
+        """4*b*h_q*s_q*s_kv*d, halved for causal (the benchmark's counting rule).  Workloads
+        with lengths or a bottom-right diagonal are counted by the benchmark itself."""
         f = 4.0 * self.b * self.h_q * self.s_q * self.s_kv * self.d
         return f / 2 if self.causal else f
 
@@ -120,11 +124,30 @@ def training_bias(s: int) -> Workload:
                     causal=True, backward=True, bias=True)
 
 
+VARLEN_LENS = (8192, 7168, 6144, 5120, 4096, 3072, 2048, 1024)
+
+
+def training_varlen() -> Workload:
+    """A padded batch of eight sequences of 1K..8K tokens (4.5 full 8K sequences of work),
+    self-attention with a causal mask, bf16 d=128, 16 heads."""
+    n = len(VARLEN_LENS)
+    return Workload("training_varlen_bf16_causal_d128_s1k-8k", n, 16, 16, 8192, 8192, 128, "bf16",
+                    causal=True, backward=True, lens_q=VARLEN_LENS, lens_kv=VARLEN_LENS)
+
+
+def prefill_bottom_right() -> Workload:
+    """A 2K-token chunk attending to an 8K-token context (the chunk's rows see the whole
+    prefix): bottom-right causal, s_q = 2048, s_kv = 8192, bf16 d=128, GQA 32/8 heads."""
+    return Workload("prefill_bottom_right_bf16_d128_q2k_kv8k", 2, 32, 8, 2048, 8192, 128, "bf16",
+                    causal=True, bottom_right=True, stats=False)
+
+
 def all_workloads():
     out = [tiny(False), tiny(True), gpt2_inference()]
     out += [training(s) for s in TRAINING_SEQ_LENS]
     out += [fp8_large_head(), grouped(8), grouped(1), grouped(64), training_alibi(8192),
-            training_dropout(8192), training_fp8(8192), training_bias(8192)]
+            training_dropout(8192), training_fp8(8192), training_bias(8192), training_varlen(),
+            prefill_bottom_right()]
     return out
 
 

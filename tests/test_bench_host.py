@@ -63,3 +63,23 @@ def test_cpu_oracle_sample_is_bounded():
     from sdpa_workloads import training
     v, desc = bench.cpu_oracle_sample(training(1024), seconds=0.2, rows_per_slice=128)
     assert v > 0 and "oracle" in desc
+
+
+def test_visible_pair_flops_for_lengths_and_bottom_right():
+    """The sweep's exact count of visible (row, key) pairs: full lengths with a top-left
+    diagonal give s(s+1)/2 per head; a bottom-right diagonal with s_q = s_kv is the same;
+    s_q < s_kv bottom-right adds the whole prefix to every row; no mask gives l_q*l_kv."""
+    import bench
+    from sdpa_workloads import Workload
+    per = 4.0 * 3 * 64
+    w = Workload("t", 2, 3, 3, 100, 100, 64, "bf16", causal=True, lens_q=(100, 40), lens_kv=(100, 40))
+    assert bench.fwd_flops(w) == per * (100 * 101 // 2 + 40 * 41 // 2)
+    w = Workload("t", 1, 3, 3, 100, 100, 64, "bf16", causal=True, bottom_right=True)
+    assert bench.fwd_flops(w) == per * (100 * 101 // 2)
+    w = Workload("t", 1, 3, 3, 30, 100, 64, "bf16", causal=True, bottom_right=True)
+    assert bench.fwd_flops(w) == per * sum(70 + i + 1 for i in range(30))
+    w = Workload("t", 2, 3, 3, 50, 80, 64, "bf16", lens_q=(50, 7), lens_kv=(80, 0))
+    assert bench.fwd_flops(w) == per * (50 * 80)
+    # a row whose diagonal falls before the first key sees nothing (bottom-right, l_q > l_kv)
+    w = Workload("t", 1, 3, 3, 10, 4, 64, "bf16", causal=True, bottom_right=True)
+    assert bench.fwd_flops(w) == per * sum(min(max(i - 6 + 1, 0), 4) for i in range(10))

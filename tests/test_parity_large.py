@@ -14,7 +14,8 @@ import torch
 
 import oracle
 from sdpa_workloads import (fp8_large_head, gpt2_inference, grouped, make_inputs,
-                            sample_kv_heads, sample_rows, training)
+                            prefill_bottom_right, sample_kv_heads, sample_rows, training,
+                            training_varlen)
 from sdpa_testlib import (FP8_REL_L2, FWD_MAX_ABS, GRAD_REL_L2, LSE_ABS, assert_fwd_close,
                           assert_grad_close, f64, rel_l2, run_bwd, run_fwd)
 
@@ -127,3 +128,76 @@ def test_fp8_large_head_rows():
     x = make_inputs(w, seed=0, with_do=False)
     o, lse, _ = run_fwd(w, x)
     _check_rows(w, x, o, lse, None, (x.descale_q, x.descale_k, x.descale_v), rel=FP8_REL_L2)
+
+
+def test_training_varlen_as_benchmarked():
+    """Eight padded sequences of 1K..8K tokens, causal, forward and backward as the sweep runs
+    them.  Valid rows: O, LSE and dQ of sampled rows against the oracle on the batch's own
+    length; dK/dV of one KV head of the two shortest batches in full.  Padded rows: O = 0 and
+    LSE = -inf exactly, gradients vanish."""
+    w = training_varlen()
+    lens = list(w.lens_q)
+    x = make_inputs(w, seed=0, with_do=True)
+    o, lse, dev = run_fwd(w, x, seq_lens_q=lens, seq_lens_kv=lens)
+    dq, dk, dv = run_bwd(w, dev, o, lse, x.do, seq_lens_q=lens, seq_lens_kv=lens)
+    g = torch.Generator().manual_seed(7)
+    by_head = {}
+    for n in range(N_ROWS):
+        bi = int(torch.randint(0, w.b, (1,), generator=g))
+        h = int(torch.randint(0, w.h_q, (1,), generator=g))
+        r = lens[bi] - 1 if n % 8 == 0 else int(torch.randint(0, lens[bi], (1,), generator=g))
+        by_head.setdefault((bi, h), set()).add(r)
+    got_o, want_o, got_l, want_l, got_q, want_q = [], [], [], [], [], []
+    for (bi, h), rows in by_head.items():
+        rows, L = sorted(rows), lens[bi]
+        hk = oracle.kv_head_of(h, w.h_q, w.h_kv)
+        kh, vh = _rows_f64(x.k, bi, hk, slice(0, L)), _rows_f64(x.v, bi, hk, slice(0, L))
+        qr, dor = _rows_f64(x.q, bi, h, rows), _rows_f64(x.do, bi, h, rows)
+        O, Lse = oracle.forward_rows(qr, rows, kh, vh, w.scale, True)
+        got_o.append(f64(o[bi, h, rows])); want_o.append(O)
+        got_l.append(lse[bi, h, rows].cpu().double().numpy()); want_l.append(Lse)
+        want_q.append(oracle.backward_dq_rows(qr, dor, rows, kh, vh, w.scale, True))
+        got_q.append(f64(dq[bi, h, rows]))
+    assert_fwd_close(np.concatenate(got_o), np.concatenate(want_o))
+    err = np.abs(np.concatenate(got_l) - np.concatenate(want_l)).max()
+    assert err <= LSE_ABS, f"LSE max abs err {err:.3e}"
+    assert_grad_close(np.concatenate(got_q), np.concatenate(want_q), "dQ rows")
+    for bi in (w.b - 2, w.b - 1):
+        L = lens[bi]
+        sl = lambda t: oracle.to_f64(t[bi:bi + 1, :, :L])
+        gk, gv = oracle.backward_kv_head(sl(x.q), sl(x.k), sl(x.v), sl(x.do), w.scale, True, 0, 3)
+        assert_grad_close(f64(dk[bi, 3, :L]), gk, f"dK[{bi},3]")
+        assert_grad_close(f64(dv[bi, 3, :L]), gv, f"dV[{bi},3]")
+    for bi, L in enumerate(lens):
+        if L == w.s_q:
+            continue
+        assert (o[bi, :, L:] == 0).all(), "padded rows of O must be zero"
+        assert torch.isneginf(lse[bi, :, L:]).all(), "padded rows of LSE must be -inf"
+        for t, name in ((dq, "dQ"), (dk, "dK"), (dv, "dV")):
+            pad = t[bi, :, L:].abs().max().item()
+            ref = t[bi, :, :L].abs().max().item()
+            assert pad <= 1e-3 * ref, f"padded rows of {name}: {pad} (valid max {ref})"
+
+
+def test_prefill_bottom_right_rows():
+    """A 2K-token chunk against an 8K context, bottom-right causal (GQA 32/8), as the sweep
+    runs it: query row r sees keys j <= r + (s_kv - s_q), i.e. top-left rows shifted by 6144."""
+    w = prefill_bottom_right()
+    x = make_inputs(w, seed=0, with_do=False)
+    o, lse, _ = run_fwd(w, x, causal="bottom_right")
+    off = w.s_kv - w.s_q
+    by_head = {}
+    for bi, h, r in sample_rows(w, N_ROWS):
+        by_head.setdefault((bi, h), set()).add(r)
+    got_o, want_o, got_l, want_l = [], [], [], []
+    for (bi, h), rows in by_head.items():
+        rows = sorted(rows)
+        hk = oracle.kv_head_of(h, w.h_q, w.h_kv)
+        kh, vh = _rows_f64(x.k, bi, hk, slice(None)), _rows_f64(x.v, bi, hk, slice(None))
+        O, Lse = oracle.forward_rows(_rows_f64(x.q, bi, h, rows), [r + off for r in rows], kh, vh,
+                                     w.scale, True)
+        got_o.append(f64(o[bi, h, rows])); want_o.append(O)
+        got_l.append(lse[bi, h, rows].cpu().double().numpy()); want_l.append(Lse)
+    assert_fwd_close(np.concatenate(got_o), np.concatenate(want_o))
+    err = np.abs(np.concatenate(got_l) - np.concatenate(want_l)).max()
+    assert err <= LSE_ABS, f"LSE max abs err {err:.3e}"
