@@ -213,11 +213,22 @@ def make_problem(q, k, v, o=None, *, attn_scale: Optional[float] = None, causal=
         _p0(bias), *_bst(bias), _p0(dbias), *_bst(dbias)))
 
 
-def _stream(stream) -> int:
-    if stream is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
-    return int(stream)
+_RAW_STREAM = None
+
+
+def _stream(stream, like=None) -> int:
+    """The cudaStream_t to launch on: ``stream`` if given, else PyTorch's current stream on the
+    device of tensor ``like`` (read through torch's raw accessor when it has one: a few µs
+    cheaper per call than building a Stream object)."""
+    global _RAW_STREAM
+    if stream is not None:
+        return int(stream)
+    import torch
+    if _RAW_STREAM is None:
+        _RAW_STREAM = getattr(torch._C, "_cuda_getCurrentRawStream", False)
+    if _RAW_STREAM and like is not None and like.device.index is not None:
+        return _RAW_STREAM(like.device.index)
+    return torch.cuda.current_stream().cuda_stream
 
 
 def sdpa_workspace_size(problem: Problem, is_backward: bool) -> int:
@@ -241,7 +252,7 @@ def sdpa_fwd(q, k, v, o, lse=None, *, attn_scale: Optional[float] = None, causal
                      dropout_p=dropout_p, dropout_mask=dropout_mask, bias=bias)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.sdpa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
-                        _ptr(workspace), ws_bytes, _stream(stream)))
+                        _ptr(workspace), ws_bytes, _stream(stream, q)))
 
 
 def sdpa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, *, attn_scale: Optional[float] = None,
@@ -259,7 +270,7 @@ def sdpa_bwd(q, k, v, o, dout, lse, dq, dk, dv, workspace, *, attn_scale: Option
                      descale_do=descale_do, bias=bias, dbias=dbias)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.sdpa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
-                        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream)))
+                        _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace), ws_bytes, _stream(stream, q)))
 
 
 def _mask_problem(b: int, h_q: int, s_q: int, s_kv: int, dropout_p: float, causal=False) -> Problem:
@@ -285,7 +296,7 @@ def sdpa_dropout_mask(b: int, h_q: int, s_q: int, s_kv: int, dropout_p: float, s
     With ``causal`` (no per-batch lengths) tiles above the diagonal are left unwritten."""
     p = _mask_problem(b, h_q, s_q, s_kv, dropout_p, causal)
     _check(lib.sdpa_dropout_mask(ctypes.byref(p), int(seed), int(offset), _ptr(mask), _ptr(mask_t),
-                                 _stream(stream)))
+                                 _stream(stream, mask if mask is not None else mask_t)))
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20  # SDPA_NOALLOC_SCRATCH_BYTES in include/sdpa.h
@@ -299,7 +310,7 @@ def sdpa_bwd_noalloc(q, k, v, o, dout, lse, dq, dk, dv, *, attn_scale: Optional[
     p = make_problem(q, k, v, o, attn_scale=attn_scale, causal=causal, dout=dout, dq=dq, dk=dk,
                      dv=dv)
     _check(lib.sdpa_bwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout),
-                                _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream)))
+                                _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _stream(stream, q)))
 
 
 def sdpa_device_error() -> int:
