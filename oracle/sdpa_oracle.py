@@ -269,7 +269,7 @@ def head_forward(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, scale: float,
         raise ValueError("a query row has no visible key")
     m = np.where(mask, S, -np.inf).max(axis=1)                # pass 1: row max
     m_safe = np.where(has, m, 0.0)
-    E = np.where(mask, np.exp(S - m_safe[:, None]), 0.0)
+    E = np.exp(np.where(mask, S - m_safe[:, None], -np.inf))  # masked: exp(-inf) = 0
     l = E.sum(axis=1)                                         # pass 2: row sum
     P = E / np.where(has, l, 1.0)[:, None]                    # pass 3: normalise
     O = (P if zdrop is None else P * zdrop) @ vh              # step 3 (dropout on P)
