@@ -702,3 +702,37 @@ def test_bias_gradient_finite_differences_and_row_sums(shape):
         fd[idx] = (lp - lm) / 2e-6
     assert np.linalg.norm(g - fd) / np.linalg.norm(fd) < 1e-6
     np.testing.assert_allclose(g.sum(axis=-1), 0.0, atol=1e-12)
+
+
+def test_row_forms_reproduce_lengths_and_bottom_right():
+    """The reductions the full-size sampled tests rely on: a bottom-right row r of a
+    [s_q, s_kv] problem is the top-left row r + (s_kv - s_q) of the row form, and a valid row
+    of a padded batch is the row form over that batch's own keys.  Checked against the full
+    forward (with its own explicit mask) and dQ against the full backward."""
+    q, k, v, do = _rand(2, 2, 5, 4), _rand(2, 2, 9, 4), _rand(2, 2, 9, 4), _rand(2, 2, 5, 4)
+    O, L = oracle.forward(q, k, v, 0.6, True, bottom_right=True)
+    dQ, _, _ = oracle.backward(q, k, v, do, 0.6, True, bottom_right=True)
+    rows = [0, 2, 4]
+    for bi in range(2):
+        for h in range(2):
+            Or, Lr = oracle.forward_rows(q[bi, h, rows], [r + 4 for r in rows], k[bi, h], v[bi, h], 0.6, True)
+            np.testing.assert_allclose(Or, O[bi, h, rows], atol=1e-13)
+            np.testing.assert_allclose(Lr, L[bi, h, rows], atol=1e-13)
+            dqr = oracle.backward_dq_rows(q[bi, h, rows], do[bi, h, rows], [r + 4 for r in rows], k[bi, h],
+                                          v[bi, h], 0.6, True)
+            np.testing.assert_allclose(dqr, dQ[bi, h, rows], atol=1e-12)
+    q, k, v, do = _rand(2, 2, 9, 4), _rand(2, 2, 9, 4), _rand(2, 2, 9, 4), _rand(2, 2, 9, 4)
+    lens = [9, 6]
+    O, L = oracle.forward(q, k, v, 0.6, True, lens, lens)
+    dQ, dK, dV = oracle.backward(q, k, v, do, 0.6, True, lens, lens)
+    bi, n = 1, lens[1]
+    rows = list(range(n))
+    Or, Lr = oracle.forward_rows(q[bi, 1, rows], rows, k[bi, 1, :n], v[bi, 1, :n], 0.6, True)
+    np.testing.assert_allclose(Or, O[bi, 1, :n], atol=1e-13)
+    np.testing.assert_allclose(Lr, L[bi, 1, :n], atol=1e-13)
+    gk, gv = oracle.backward_kv_head(q[bi:bi + 1, :, :n], k[bi:bi + 1, :, :n], v[bi:bi + 1, :, :n],
+                                     do[bi:bi + 1, :, :n], 0.6, True, 0, 1)
+    np.testing.assert_allclose(gk, dK[bi, 1, :n], atol=1e-12)
+    np.testing.assert_allclose(gv, dV[bi, 1, :n], atol=1e-12)
+    assert (O[bi, :, n:] == 0).all() and np.isneginf(L[bi, :, n:]).all()
+    assert (dK[bi, :, n:] == 0).all() and (dV[bi, :, n:] == 0).all() and (dQ[bi, :, n:] == 0).all()
