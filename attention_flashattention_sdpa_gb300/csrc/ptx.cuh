@@ -149,6 +149,15 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
 // TMA (cp.async.bulk.tensor), no multicast
 // ---------------------------------------------------------------------------
 
+// Byte permute with sign replication (PTX prmt.b32, default mode): byte k of the result is
+// byte (sel >> 4k) & 7 of {b, a}, or, when bit 3 of that selector nibble is set, eight copies
+// of that byte's top bit.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
 // Brings the L2 line holding `ptr` into L2 (no registers, no completion to wait for).
 __device__ __forceinline__ void prefetch_l2(const void* ptr) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(ptr)));

@@ -626,11 +626,11 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         pk[c / 2] = pack2(p0, p1, DT);
         if constexpr (DROP) {
           // dV takes the kept P only; dS below takes every P.  A zero of either 16-bit type
-          // is all zero bits, so the kept pair is the packed pair with dropped halves cleared:
-          // the two keep bits spread to 0x0000FFFF / 0xFFFF0000 lane masks.
+          // is all zero bits, so the kept pair is the packed pair with dropped halves cleared.
+          // The pair's keep bits sit at bits i and i + 16 of its word: shifted to bits 15 and
+          // 31, a sign-replicating byte permute spreads them to the two 16-bit lanes.
           const uint32_t w = (c < 32) ? keep.x : keep.y;
-          const uint32_t bits = (w >> (c % 32)) & 3u;
-          pm[c / 2] = pk[c / 2] & (((bits * 0x8001u) & 0x00010001u) * 0xFFFFu);
+          pm[c / 2] = pk[c / 2] & prmt(w << (15 - (c % 32) / 2), 0u, 0xBB99u);
         }
       }
       if constexpr (DROP) {
@@ -662,9 +662,10 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
 #pragma unroll
           for (int c = 0; c < 32; c += 2) {
             const float2 nd = *reinterpret_cast<const float2*>(ndelta + 32 * half + c);
-            float2 dpv = make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
-            dpv.x = (w >> c) & 1u ? dpv.x : 0.f;
-            dpv.y = (w >> c) & 2u ? dpv.y : 0.f;
+            // The pair's keep bits (bits c/2 and c/2 + 16) as two all-ones / all-zeros masks.
+            const uint32_t kx = w << (15 - c / 2);
+            const float2 dpv = make_float2(__uint_as_float(sv[c] & prmt(kx, 0u, 0x9999u)),
+                                           __uint_as_float(sv[c + 1] & prmt(kx, 0u, 0xBBBBu)));
             const float2 dd = mul2(unpack2(pk[16 * half + c / 2], DT), fma2(dpv, rk2, nd));
             ds[16 * half + c / 2] = pack2(dd.x, dd.y, DT);
             if constexpr (DBIAS) dbias_emit(dbrow, 32 * half + c, dd, dbhold);
@@ -1042,8 +1043,8 @@ __global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant_
         pf[c] = p0;
         pf[c + 1] = p1;
         if constexpr (DROP) {
-          const uint32_t w = (c < 32) ? keep.x : keep.y;
-          pk[c / 2] = pack2((w >> (c % 32)) & 1u ? p0 : 0.f, (w >> (c % 32)) & 2u ? p1 : 0.f, DT);
+          const uint32_t w = (c < 32) ? keep.x : keep.y;   // the pair: bits i and i + 16
+          pk[c / 2] = pack2((w >> ((c % 32) / 2)) & 1u ? p0 : 0.f, (w >> ((c % 32) / 2 + 16)) & 1u ? p1 : 0.f, DT);
         } else {
           pk[c / 2] = pack2(p0, p1, DT);
         }
@@ -1086,8 +1087,8 @@ __global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant_
         if constexpr (DROP) {
           // dS = P * (keep / (1 - p) * dO·Vᵀ - Delta) takes every P.
           const uint32_t w = (c < 32) ? keep.x : keep.y;
-          dp.x = (w >> (c % 32)) & 1u ? dp.x : 0.f;
-          dp.y = (w >> (c % 32)) & 2u ? dp.y : 0.f;
+          dp.x = (w >> ((c % 32) / 2)) & 1u ? dp.x : 0.f;
+          dp.y = (w >> ((c % 32) / 2 + 16)) & 1u ? dp.y : 0.f;
         }
         const float2 dd = mul2(make_float2(pf[c], pf[c + 1]), fma2(dp, rk2, nd));
         ds[c / 2] = pack2(dd.x, dd.y, DT);

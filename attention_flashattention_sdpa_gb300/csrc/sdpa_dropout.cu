@@ -10,7 +10,9 @@
 //
 // One kernel writes the bits twice: row-major for the forward pass (a thread owns a query
 // row) and transposed for the backward pass (a thread owns a key row), so neither attention
-// kernel runs the generator.
+// kernel runs the generator.  In the transposed words the two rows of an even/odd pair sit
+// 16 bits apart (row i at bit 16 * (i % 2) + (i % 32) / 2 of word i / 32): the backward pass
+// keeps or drops a packed pair of 16-bit values with one shift and one byte permute.
 #include <cstdint>
 
 #include "sdpa_internal.h"
@@ -90,6 +92,15 @@ __global__ void __launch_bounds__(128) dropout_mask_kernel(const DropoutParams p
       const uint32_t col = __ballot_sync(0xffffffffu, (w[i] >> c) & 1u);
       if (lane == c) mine = col;
     }
+    // Unshuffle: even rows to the low half, odd rows to the high half (four delta swaps).
+    uint32_t t = (mine ^ (mine >> 1)) & 0x22222222u;
+    mine ^= t ^ (t << 1);
+    t = (mine ^ (mine >> 2)) & 0x0C0C0C0Cu;
+    mine ^= t ^ (t << 2);
+    t = (mine ^ (mine >> 4)) & 0x00F000F0u;
+    mine ^= t ^ (t << 4);
+    t = (mine ^ (mine >> 8)) & 0x0000FF00u;
+    mine ^= t ^ (t << 8);
     tile[32 * i + lane][warp] = mine;
   }
   __syncthreads();

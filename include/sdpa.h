@@ -225,7 +225,8 @@ SDPA_API sdpa_status_t sdpa_bwd_noalloc(const sdpa_problem_t* p, const void* q, 
 /*
  * Byte sizes of the two dropout keep-mask arrays of `p` (b, h_q, s_q, s_kv are read):
  *   mask:   uint32 [b*h_q][s_q][ceil(s_kv/128)*4]   (bit j%32 of word j/32: key j of row i)
- *   mask_t: uint32 [b*h_q][s_kv][ceil(s_q/128)*4]   (bit i%32 of word i/32: row i of key j)
+ *   mask_t: uint32 [b*h_q][s_kv][ceil(s_q/128)*4]   (row i of key j at bit 16*(i%2) + (i%32)/2
+ *           of word i/32: the two rows of an even/odd pair sit 16 bits apart)
  */
 SDPA_API sdpa_status_t sdpa_dropout_mask_size(const sdpa_problem_t* p, size_t* bytes, size_t* bytes_t);
 

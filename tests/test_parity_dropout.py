@@ -19,9 +19,24 @@ MODES = {"none": (False, False), "top_left": (True, False), "bottom_right": (Tru
 
 
 def _unpack(words: torch.Tensor, n_rows: int, n_words: int, n_valid: int) -> np.ndarray:
+    """Row-major keep bits: element j at bit j % 32 of word j / 32."""
     w = words.cpu().numpy().view(np.uint32).reshape(n_rows, n_words)
     j = np.arange(n_valid)
     return ((w[:, j // 32] >> (j % 32).astype(np.uint32)) & 1).astype(bool)
+
+
+def _tbit(i):
+    """Bit of query row i within its word of the transposed mask (an even/odd pair of rows
+    sits 16 bits apart): 16 * (i % 2) + (i % 32) / 2."""
+    i = np.asarray(i)
+    return (16 * (i % 2) + (i % 32) // 2).astype(np.uint32)
+
+
+def _unpack_t(words: torch.Tensor, n_rows: int, n_words: int, n_valid: int) -> np.ndarray:
+    """Transposed keep bits: query row i of a key at bit _tbit(i) of word i / 32."""
+    w = words.cpu().numpy().view(np.uint32).reshape(n_rows, n_words)
+    i = np.arange(n_valid)
+    return ((w[:, i // 32] >> _tbit(i)) & 1).astype(bool)
 
 
 def _p32(p):
@@ -39,7 +54,7 @@ def test_mask_bits_equal_the_oracle_draw(b, h, s_q, s_kv, p, seed, offset):
     kvw, qw = (s_kv + 127) // 128 * 4, (s_q + 127) // 128 * 4
     rows = _unpack(mask, b * h * s_q, kvw, s_kv).reshape(b * h, s_q, s_kv)
     assert (rows == keep).all()
-    cols = _unpack(mask_t, b * h * s_kv, qw, s_q).reshape(b * h, s_kv, s_q)
+    cols = _unpack_t(mask_t, b * h * s_kv, qw, s_q).reshape(b * h, s_kv, s_q)
     assert (cols == keep.transpose(0, 2, 1)).all()
 
 
@@ -48,7 +63,7 @@ def test_mask_p_zero_keeps_everything_and_sizes():
     n, n_t = m.sdpa_dropout_mask_size(2, 3, 200, 300)
     assert n == 2 * 3 * 200 * 12 * 4 and n_t == 2 * 3 * 300 * 8 * 4
     mask, mask_t = dropout_masks(2, 3, 200, 300, (0.0, 5, 6))
-    assert _unpack(mask, 6 * 200, 12, 300).all() and _unpack(mask_t, 6 * 300, 8, 200).all()
+    assert _unpack(mask, 6 * 200, 12, 300).all() and _unpack_t(mask_t, 6 * 300, 8, 200).all()
 
 
 def _case(w, mode, p, seed, offset, lq=None, lkv=None, alibi=None, backward=False):
@@ -128,7 +143,7 @@ def test_training_shape_sampled_rows():
         # transposed: bit i of key j's words for j in a sample of columns
         js = np.array([0, 1, 31, 32, 4096, 8191])
         col = mtw[bh, js].cpu().numpy().view(np.uint32)
-        bits = ((col[:, i // 32] >> np.uint32(i % 32)) & 1).astype(bool)
+        bits = ((col[:, i // 32] >> _tbit(i)) & 1).astype(bool)
         assert (bits == keep[r][js]).all()
 
 
@@ -143,7 +158,7 @@ def test_causal_draw_writes_every_visible_tile(causal):
     off = s_kv - s_q if causal == "bottom_right" else 0
     vis = np.arange(s_kv)[None, :] <= np.arange(s_q)[:, None] + off
     rows = _unpack(mask, b * h * s_q, 16, s_kv).reshape(b * h, s_q, s_kv)
-    cols = _unpack(mask_t, b * h * s_kv, 12, s_q).reshape(b * h, s_kv, s_q)
+    cols = _unpack_t(mask_t, b * h * s_kv, 12, s_q).reshape(b * h, s_kv, s_q)
     assert (rows[:, vis] == keep[:, vis]).all()
     assert (cols.transpose(0, 2, 1)[:, vis] == keep[:, vis]).all()
     # a tile wholly above the diagonal (rows 0-127, keys 256-383 top-left) is untouched (-1)
