@@ -557,7 +557,9 @@ sdpa_status_t sdpa_bwd_noalloc(const sdpa_problem_t* p, const void* q, const voi
                                void* dq, void* dk, void* dv, void* stream) {
   sdpa_status_t st = check_problem(p, true);
   if (st != SDPA_OK) return st;
-  const size_t need = sdpa::bwd_workspace_bytes(p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d);
+  // The whole workspace sdpa_bwd needs: the base scratch plus, where the problem asks for
+  // them, the widened FP8 copies, the transposed bias and the bias-gradient accumulator.
+  const size_t need = bwd_total_workspace(p);
   if (need > SDPA_NOALLOC_SCRATCH_BYTES)
     return fail(SDPA_ERR_UNSUPPORTED,
                 "sdpa_bwd_noalloc: this problem needs %zu bytes of scratch but the built-in "

@@ -212,7 +212,9 @@ SDPA_API sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const vo
  *   - Problems whose workspace (sdpa_workspace_size(p, 1)) exceeds the array are rejected
  *     with SDPA_ERR_UNSUPPORTED and a message giving both sizes; use sdpa_bwd then.
  *   - The first call on a device looks up the array's device address (with that device
- *     current); make that first call before any stream capture.
+ *     current); make that first call before any stream capture.  The address is kept for
+ *     the life of the process, so do not call this entry point again on a device after
+ *     cudaDeviceReset() there (the reset unloads the module that holds the array).
  *   - Every call shares the one array (whatever it held is overwritten; each call clears
  *     what must start at zero), so calls whose executions overlap on the GPU — on different
  *     streams, or from different threads — race and give wrong results.  Serialise them.
