@@ -35,7 +35,10 @@ module's own table and multiplied by their descale):
   linear penalty on the distance to the aligned diagonal.  The pages name the option but no
   slopes; without caller slopes the default is the geometric sequence m_h = 2^(-8 (h+1) / H)
   of the ALiBi paper (Press, Smith and Lewis, "Train Short, Test Long", §3: 1/2 ... 1/256 for
-  8 heads), applied by the same formula to any head count;
+  8 heads), applied by the same formula to any head count.  That paper defines the bias for
+  causal attention only, as a penalty growing with a query's distance to the earlier keys it
+  sees; without a causal mask the linear term would reward later keys more the farther they
+  are, so ALiBi without a causal mask is not defined here and is refused (ValueError);
 * an additive bias (the SDPA node's bias input in the cuDNN 9 blog's walkthrough): a tensor
   [b or 1, h_q or 1, s_q, s_kv] added to the scaled scores before the mask and the softmax
   (broadcast over a batch or head dimension of size 1).  Its gradient is dS = ∂L/∂S, the
@@ -252,6 +255,13 @@ def alibi_bias(s_q: int, s_kv: int, slope: float, off: int = 0) -> np.ndarray:
     return slope * (j - i - off).astype(np.float64)
 
 
+def _check_alibi(causal: bool, alibi_slopes) -> None:
+    """ALiBi is a distance penalty on the keys before a query (the ALiBi paper, §3): it needs
+    a causal mask, which keeps every visible key at or before the aligned diagonal."""
+    if alibi_slopes is not None and not causal:
+        raise ValueError("ALiBi is defined for causal attention only")
+
+
 def head_forward(qh: np.ndarray, kh: np.ndarray, vh: np.ndarray, scale: float,
                  mask: np.ndarray, allow_empty: bool = False, bias: np.ndarray | None = None,
                  zdrop: np.ndarray | None = None):
@@ -319,6 +329,7 @@ def forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: b
     per-query-head ALiBi slopes, a dropout keep mask [b, h_q, s_q, s_kv] with its
     probability, and an additive bias [b|1, h_q|1, s_q, s_kv].  Returns (O [b,h_q,s_q,d],
     LSE [b,h_q,s_q])."""
+    _check_alibi(causal, alibi_slopes)
     b, h_q, s_q, d = q.shape
     h_kv, s_kv = k.shape[1], k.shape[2]
     varlen = seq_lens_q is not None or seq_lens_kv is not None or bottom_right
@@ -374,6 +385,7 @@ def backward(q, k, v, do, scale: float, causal: bool, seq_lens_q=None, seq_lens_
 
     dK, dV have K's and V's shapes and hold the sum over each KV head's group.  With
     variable lengths, padded rows of dQ, dK and dV are zero."""
+    _check_alibi(causal, alibi_slopes)
     b, h_q, s_q, _ = q.shape
     h_kv, s_kv = k.shape[1], k.shape[2]
     varlen = seq_lens_q is not None or seq_lens_kv is not None or bottom_right

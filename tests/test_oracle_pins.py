@@ -469,12 +469,12 @@ def test_alibi_brute_force_and_limits():
     causal row attend only to its own key (every earlier key is penalised away)."""
     q, k, v = _rand(1, 2, 5, 3), _rand(1, 2, 7, 3), _rand(1, 2, 7, 3)
     slopes = [0.25, 1.5]
-    for causal in (False, True):
+    for causal in (True,):
         O, L = oracle.forward(q, k, v, 0.8, causal, alibi_slopes=slopes)
         for h in range(2):
             for i in range(5):
                 w = [0.0 if (causal and j > i) else
-                     math.exp(0.8 * float(q[0, h, i] @ k[0, h, j]) + slopes[h] * (j - i)) for j in range(7)]
+                     math.exp(0.8 * float(q[0, h, i] @ k[0, h, j]) - slopes[h] * (i - j)) for j in range(7)]
                 tot = sum(w)
                 np.testing.assert_allclose(O[0, h, i], sum(w[j] / tot * v[0, h, j] for j in range(7)), atol=1e-12)
                 np.testing.assert_allclose(L[0, h, i], math.log(tot), atol=1e-12)
@@ -483,6 +483,45 @@ def test_alibi_brute_force_and_limits():
     np.testing.assert_allclose(O0, Oc, atol=1e-14)
     Oh, _ = oracle.forward(q, k, v, 0.8, True, alibi_slopes=[200.0, 200.0])
     np.testing.assert_allclose(Oh[0, :, :5], v[0, :, :5], atol=1e-12)
+
+
+def test_alibi_needs_a_causal_mask():
+    """ALiBi penalises the distance to earlier keys (the ALiBi paper, §3); with no causal mask
+    there would be later keys, which the linear term rewards: the oracle refuses that case."""
+    q, k, v, do = _rand(1, 1, 4, 2), _rand(1, 1, 4, 2), _rand(1, 1, 4, 2), _rand(1, 1, 4, 2)
+    with pytest.raises(ValueError):
+        oracle.forward(q, k, v, 0.5, False, alibi_slopes=[0.3])
+    with pytest.raises(ValueError):
+        oracle.backward(q, k, v, do, 0.5, False, alibi_slopes=[0.3])
+
+
+@pytest.mark.parametrize("bottom_right,s_q,s_kv", [(False, 9, 9), (False, 5, 12), (True, 5, 12), (True, 12, 5)])
+def test_alibi_weights_fall_geometrically_with_distance(bottom_right, s_q, s_kv):
+    """With Q = 0 every score is 0, so the weights are the softmax of the ALiBi term alone: a
+    penalty m per key of distance from the aligned diagonal.  Row i's visible keys j = i + off,
+    i + off - 1, ..., 0 then get the truncated geometric weights r^t (1 - r) / (1 - r^n) with
+    r = e^-m, t the distance and n the number of visible keys, largest on the diagonal and never
+    rising with distance; V = I reads the weights out of O."""
+    m = 0.4
+    q = np.zeros((1, 1, s_q, 2))
+    k = _rand(1, 1, s_kv, 2)
+    v = np.eye(s_kv)[None, None]
+    O, L = oracle.forward(q, k, v, 0.7, True, None, None, bottom_right, alibi_slopes=[m])
+    off = (s_kv - s_q) if bottom_right else 0
+    r = math.exp(-m)
+    for i in range(s_q):
+        last = min(i + off, s_kv - 1)
+        if last < 0:
+            assert np.isneginf(L[0, 0, i]) and not O[0, 0, i].any()
+            continue
+        n = last + 1
+        want = np.zeros(s_kv)
+        for j in range(n):
+            t = i + off - j
+            want[j] = r ** (t - (i + off - last)) * (1 - r) / (1 - r ** n)
+        np.testing.assert_allclose(O[0, 0, i], want, atol=1e-13)
+        w = O[0, 0, i, :n]
+        assert np.all(np.diff(w) >= 0), "weights must not rise with distance from the diagonal"
 
 
 def test_alibi_bottom_right_offset_and_gradients():
