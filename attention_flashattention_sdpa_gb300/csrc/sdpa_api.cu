@@ -195,6 +195,10 @@ sdpa_status_t check_problem(const sdpa_problem_t* p, bool backward) {
     return fail(SDPA_ERR_INVALID_ARG, "alibi must be 0 or 1, got %d", p->alibi);
   if (p->alibi && p->alibi_slopes && reinterpret_cast<uintptr_t>(p->alibi_slopes) % 4)
     return fail(SDPA_ERR_LAYOUT, "alibi_slopes must be 4-byte aligned");
+  // ALiBi penalises a query's distance to the earlier keys it sees (the ALiBi paper, §3);
+  // without a causal mask the linear term would favour the farthest later keys instead.
+  if (p->alibi && p->causal == 0)
+    return fail(SDPA_ERR_UNSUPPORTED, "ALiBi needs a causal mask (causal = 1 or 2)");
   if (p->alibi && p->in_dtype == SDPA_DTYPE_E4M3)
     return fail(SDPA_ERR_UNSUPPORTED, "ALiBi takes F16 or BF16 inputs, not E4M3");
   if (!(p->dropout_p >= 0.f && p->dropout_p < 1.f))

@@ -111,7 +111,9 @@ typedef struct {
    * do not define it, and this is the linear-bias reading).  0 = off.  1 = the scaled score of
    * (i, j) gains m_hq * (j - i - off) before the mask and softmax, off = len_kv - len_q under
    * bottom-right causal alignment and 0 otherwise: zero on the aligned diagonal, a penalty
-   * growing linearly with the distance to earlier keys.  m_hq = alibi_slopes[hq] (a DEVICE
+   * growing linearly with the distance to earlier keys.  ALiBi needs a causal mask (causal 1
+   * or 2: every visible key is then at or before the aligned diagonal); with causal = 0 it is
+   * refused with SDPA_ERR_UNSUPPORTED.  m_hq = alibi_slopes[hq] (a DEVICE
    * pointer to h_q finite fp32 values >= 0; a negative slope counts as 0), or, when
    * alibi_slopes is NULL, the geometric slopes 2^(-8 (hq + 1) / h_q).  F16 and BF16 inputs
    * only; the bias has no gradient. */

@@ -89,7 +89,9 @@ def _bwd(m, p, ws=FAKE, ws_bytes=1 << 40, lse=FAKE, q=FAKE):
     (dict(in_dtype=2, out_dtype=2), 2, "output"),
     (dict(alibi=2), 1, "alibi"),
     (dict(bias=FAKE + 8), 3, "bias"),
-    (dict(bias=FAKE, alibi=1), 2, "alibi"),
+    (dict(bias=FAKE, alibi=1, causal=1), 2, "alibi"),
+    (dict(alibi=1), 2, "ALiBi needs a causal mask"),
+    (dict(alibi=1, causal=0, alibi_slopes=FAKE), 2, "ALiBi needs a causal mask"),
     (dict(bias=FAKE, bias_strides=None), 3, "key stride"),
     (dict(bias=FAKE, bias_strides=(0, 0, 130, 1)), 3, "multiples of 8"),
     (dict(bias=FAKE, bias_strides=(0, 0, 120, 1)), 3, "row stride"),

@@ -1,7 +1,7 @@
 """GPU parity of the ALiBi position bias against the fp64 oracle.
 
 Caller slopes (one per query head, mixing gentle and steep ones) and the library's default
-geometric slopes; no mask, top-left and bottom-right causal; every head dim; grouped heads
+geometric slopes; top-left and bottom-right causal (no mask is refused); every head dim; grouped heads
 (including the split-group backward, where one CTA visits several query heads with
 different slopes); variable lengths.  The bias joins the scaled scores before the softmax,
 so O, LSE and all three gradients change; tolerances are those of the unbiased tests."""
@@ -48,14 +48,37 @@ def _case(w, mode, alibi, seed, lq=None, lkv=None, backward=False):
         assert_grad_close(f64(dv), dV, "dV")
 
 
-@pytest.mark.parametrize("mode", ["none", "top_left", "bottom_right"])
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_no_mask_is_refused(d):
+    """ALiBi is a penalty on the distance to earlier keys: without a causal mask both entry
+    points refuse it (SDPA_ERR_UNSUPPORTED) before anything runs."""
+    import torch
+    from sdpa_testlib import lib, to_dev
+    m = lib()
+    w = Workload("t", 1, 2, 2, 130, 130, d, "bf16", backward=True)
+    x = make_inputs(w, seed=d, with_do=True)
+    q, k, v, do = to_dev(x.q), to_dev(x.k), to_dev(x.v), to_dev(x.do)
+    o = torch.zeros_like(q)
+    lse = torch.zeros(1, 2, 130, device="cuda")
+    with pytest.raises(m.SdpaError) as e:
+        m.sdpa_fwd(q, k, v, o, lse, causal=False, alibi=True)
+    assert e.value.status == 2 and "causal" in m.sdpa_last_error_string()
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(m.SdpaError) as e:
+        m.sdpa_bwd(q, k, v, o, do, lse, torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), ws,
+                   causal=False, alibi=True)
+    assert e.value.status == 2
+    assert not o.any(), "nothing may run before the refusal"
+
+
+@pytest.mark.parametrize("mode", ["top_left", "bottom_right"])
 @pytest.mark.parametrize("d", [64, 128, 256])
 def test_forward_caller_slopes(mode, d):
     w = Workload("t", 2, 4, 2, 300, 333, d, "bf16")
     _case(w, mode, _slopes(4, d), seed=d)
 
 
-@pytest.mark.parametrize("mode", ["none", "top_left", "bottom_right"])
+@pytest.mark.parametrize("mode", ["top_left", "bottom_right"])
 @pytest.mark.parametrize("d", [64, 128, 256])
 def test_backward_caller_slopes(mode, d):
     w = Workload("t", 2, 4, 2, 260, 300, d, "f16", backward=True)

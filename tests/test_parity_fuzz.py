@@ -36,6 +36,8 @@ def _draw(i):
     if mode == "top_left" and lens is None:
         s_kv = max(s_kv, s_q)   # every row keeps at least one key
     extra = str(rng.choice(["plain", "alibi", "bias", "dbias"]))
+    if extra == "alibi" and mode == "none":
+        extra = "plain"   # ALiBi needs a causal mask
     dropout = (float(rng.choice([0.1, 0.4])), int(rng.integers(0, 2 ** 63)), int(rng.integers(0, 1000))) \
         if rng.random() < 0.35 else None
     return dict(d=d, dtype=dtype, layout=layout, h_kv=h_kv, h_q=h_q, b=b, s_q=s_q, s_kv=s_kv,
