@@ -74,7 +74,8 @@ import numpy as np
 __all__ = [
     "philox4x64", "dropout_threshold", "dropout_keep", "bias_gradient",
     "visible_mask", "kv_head_of", "alibi_default_slopes", "alibi_bias", "head_forward", "forward", "forward_rows",
-    "backward", "backward_dq_rows", "backward_kv_rows", "backward_kv_head", "e4m3_decode_table",
+    "backward", "backward_dq_rows", "backward_ds_rows", "backward_kv_rows", "backward_kv_head",
+    "e4m3_decode_table",
     "decode_e4m3", "e5m2_decode_table", "decode_e5m2", "to_f64",
 ]
 
@@ -248,9 +249,10 @@ def alibi_default_slopes(h_q: int) -> np.ndarray:
     return np.array([2.0 ** (-8.0 * (h + 1) / h_q) for h in range(h_q)], dtype=np.float64)
 
 
-def alibi_bias(s_q: int, s_kv: int, slope: float, off: int = 0) -> np.ndarray:
-    """[s_q, s_kv] additive bias slope * (j - i - off)."""
-    i = np.arange(s_q)[:, None]
+def alibi_bias(s_q: int, s_kv: int, slope: float, off: int = 0, rows=None) -> np.ndarray:
+    """[s_q, s_kv] additive bias slope * (j - i - off); with ``rows``, only those query rows
+    ([len(rows), s_kv])."""
+    i = (np.arange(s_q) if rows is None else np.asarray(rows))[:, None]
     j = np.arange(s_kv)[None, :]
     return slope * (j - i - off).astype(np.float64)
 
@@ -347,18 +349,22 @@ def forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: b
     return O, L
 
 
+def _rows_mask(rows, s_kv: int, causal: bool) -> np.ndarray:
+    rows = np.asarray(rows)
+    if causal:
+        return np.arange(s_kv)[None, :] <= rows[:, None]
+    return np.ones((len(rows), s_kv), dtype=bool)
+
+
 def forward_rows(q_rows: np.ndarray, rows: Sequence[int], kh: np.ndarray, vh: np.ndarray,
-                 scale: float, causal: bool):
+                 scale: float, causal: bool, bias: np.ndarray | None = None):
     """Forward for selected query rows of one (batch, head).
 
     q_rows: [n, d] fp64 rows of Q; rows: their sequence positions; kh, vh: the
-    row's KV head [s_kv, d].  Returns (O rows [n, d], LSE [n]).  Cost O(n·s_kv·d),
-    which lets large shapes be checked row by row."""
-    s_kv = kh.shape[0]
-    rows = np.asarray(rows)
-    mask = (np.arange(s_kv)[None, :] <= rows[:, None]) if causal else np.ones(
-        (len(rows), s_kv), dtype=bool)
-    O, lse, _ = head_forward(q_rows, kh, vh, scale, mask)
+    row's KV head [s_kv, d]; bias: optional [n, s_kv] additive term on these rows' scaled
+    scores (a slice of a bias tensor, or ALiBi's rows).  Returns (O rows [n, d], LSE [n]).
+    Cost O(n·s_kv·d), which lets large shapes be checked row by row."""
+    O, lse, _ = head_forward(q_rows, kh, vh, scale, _rows_mask(rows, kh.shape[0], causal), bias=bias)
     return O, lse
 
 
@@ -429,32 +435,33 @@ def bias_gradient(q, k, v, do, scale: float, causal: bool, bias, seq_lens_q=None
     return out
 
 
-def backward_dq_rows(q_rows, do_rows, rows: Sequence[int], kh, vh, scale: float, causal: bool):
-    """dQ for selected query rows of one (batch, head): [n, d].
+def backward_ds_rows(q_rows, do_rows, rows: Sequence[int], kh, vh, scale: float, causal: bool,
+                     bias: np.ndarray | None = None):
+    """dS = P ∘ (dP − Delta) for selected query rows of one (batch, head): [n, s_kv] — the
+    gradient of the scaled scores, and so of an additive bias on them.
 
-    Row i needs only its own P_i, dP_i = dO_i Vᵀ and Delta_i, so the cost is
+    Row i needs only its own P_i, dP_i = dO_i Vᵀ and Delta_i = Σ_j P_ij dP_ij, so the cost is
     O(n·s_kv·d)."""
-    s_kv = kh.shape[0]
-    rows = np.asarray(rows)
-    mask = (np.arange(s_kv)[None, :] <= rows[:, None]) if causal else np.ones(
-        (len(rows), s_kv), dtype=bool)
-    _, _, P = head_forward(q_rows, kh, vh, scale, mask)
+    _, _, P = head_forward(q_rows, kh, vh, scale, _rows_mask(rows, kh.shape[0], causal), bias=bias)
     dP = do_rows @ vh.T
     delta = (P * dP).sum(axis=1)
-    dS = P * (dP - delta[:, None])
-    return scale * (dS @ kh)
+    return P * (dP - delta[:, None])
 
 
-def backward_kv_rows(q_rows, do_rows, rows: Sequence[int], kh, vh, scale: float, causal: bool):
+def backward_dq_rows(q_rows, do_rows, rows: Sequence[int], kh, vh, scale: float, causal: bool,
+                     bias: np.ndarray | None = None):
+    """dQ = scale · dS K for selected query rows of one (batch, head): [n, d] (bias as in
+    forward_rows)."""
+    return scale * (backward_ds_rows(q_rows, do_rows, rows, kh, vh, scale, causal, bias) @ kh)
+
+
+def backward_kv_rows(q_rows, do_rows, rows: Sequence[int], kh, vh, scale: float, causal: bool,
+                     bias: np.ndarray | None = None):
     """The contribution of selected query rows of one head to dK and dV: ([s_kv, d], [s_kv, d]).
 
     dK and dV of a KV head are the sums of these contributions over every query row of
-    every query head in its group."""
-    s_kv = kh.shape[0]
-    rows = np.asarray(rows)
-    mask = (np.arange(s_kv)[None, :] <= rows[:, None]) if causal else np.ones(
-        (len(rows), s_kv), dtype=bool)
-    _, _, P = head_forward(q_rows, kh, vh, scale, mask)
+    every query head in its group (bias as in forward_rows)."""
+    _, _, P = head_forward(q_rows, kh, vh, scale, _rows_mask(rows, kh.shape[0], causal), bias=bias)
     dV = P.T @ do_rows
     dP = do_rows @ vh.T
     delta = (P * dP).sum(axis=1)
@@ -464,11 +471,13 @@ def backward_kv_rows(q_rows, do_rows, rows: Sequence[int], kh, vh, scale: float,
 
 
 def backward_kv_head(q, k, v, do, scale: float, causal: bool, bi: int, hk: int,
-                     row_chunk: int = 1024):
+                     row_chunk: int = 1024, bias_rows=None):
     """dK, dV of one (batch, KV head) at any size: [s_kv, d] each.
 
     Sums over the KV head's group of query heads, visiting query rows in chunks
-    so that at most row_chunk x s_kv scores are held at a time."""
+    so that at most row_chunk x s_kv scores are held at a time.  bias_rows: optional
+    function (hq, r0, r1) -> [r1 - r0, s_kv] fp64, the additive term on the scaled scores of
+    query rows r0..r1-1 of head hq (a bias tensor's slice, or ALiBi's rows)."""
     b, h_q, s_q, _ = q.shape
     h_kv, s_kv = k.shape[1], k.shape[2]
     g = h_q // h_kv
@@ -478,8 +487,9 @@ def backward_kv_head(q, k, v, do, scale: float, causal: bool, bi: int, hk: int,
     for hq in range(hk * g, (hk + 1) * g):
         for r0 in range(0, s_q, row_chunk):
             r1 = min(s_q, r0 + row_chunk)
+            bias = None if bias_rows is None else bias_rows(hq, r0, r1)
             gk, gv = backward_kv_rows(q[bi, hq, r0:r1], do[bi, hq, r0:r1], np.arange(r0, r1),
-                                      kh, vh, scale, causal)
+                                      kh, vh, scale, causal, bias)
             dK += gk
             dV += gv
     return dK, dV

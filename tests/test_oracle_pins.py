@@ -775,3 +775,60 @@ def test_row_forms_reproduce_lengths_and_bottom_right():
     np.testing.assert_allclose(gv, dV[bi, 1, :n], atol=1e-12)
     assert (O[bi, :, n:] == 0).all() and np.isneginf(L[bi, :, n:]).all()
     assert (dK[bi, :, n:] == 0).all() and (dV[bi, :, n:] == 0).all() and (dQ[bi, :, n:] == 0).all()
+
+
+def test_row_forms_with_a_bias_or_alibi():
+    """The row forms with an additive term, as the full-size ALiBi and bias tests use them:
+    rows of the full forward (O, LSE), of the full backward (dQ), of the bias gradient (dS
+    summed over the batch of a broadcast bias) and whole KV heads of dK, dV, for ALiBi rows
+    (top-left and bottom-right) and for slices of a bias tensor."""
+    rng = np.random.default_rng(17)
+    b, h, s = 2, 2, 7
+    q, k, v, do = _rand(b, h, s, 3), _rand(b, h, s, 3), _rand(b, h, s, 3), _rand(b, h, s, 3)
+    slopes = [0.35, 1.2]
+    rows = [0, 3, 6]
+    for br in (False, True):
+        s_q = 4 if br else s
+        qq, dd = q[:, :, :s_q], do[:, :, :s_q]
+        off = s - s_q if br else 0
+        O, L = oracle.forward(qq, k, v, 0.6, True, None, None, br, alibi_slopes=slopes)
+        dQ, dK, dV = oracle.backward(qq, k, v, dd, 0.6, True, None, None, br, alibi_slopes=slopes)
+        rr = [r for r in rows if r < s_q]
+        for bi in range(b):
+            for hq in range(h):
+                al = oracle.alibi_bias(s_q, s, slopes[hq], off, rows=rr)
+                np.testing.assert_allclose(al, oracle.alibi_bias(s_q, s, slopes[hq], off)[rr], atol=0)
+                shifted = [r + off for r in rr]
+                Or, Lr = oracle.forward_rows(qq[bi, hq, rr], shifted, k[bi, hq], v[bi, hq], 0.6, True, al)
+                np.testing.assert_allclose(Or, O[bi, hq, rr], atol=1e-13)
+                np.testing.assert_allclose(Lr, L[bi, hq, rr], atol=1e-13)
+                g = oracle.backward_dq_rows(qq[bi, hq, rr], dd[bi, hq, rr], shifted, k[bi, hq], v[bi, hq], 0.6,
+                                            True, al)
+                np.testing.assert_allclose(g, dQ[bi, hq, rr], atol=1e-12)
+        if not br:
+            fn = lambda hq, r0, r1: oracle.alibi_bias(s, s, slopes[hq], 0, rows=np.arange(r0, r1))
+            gk, gv = oracle.backward_kv_head(q, k, v, do, 0.6, True, 1, 1, row_chunk=3, bias_rows=fn)
+            np.testing.assert_allclose(gk, dK[1, 1], atol=1e-12)
+            np.testing.assert_allclose(gv, dV[1, 1], atol=1e-12)
+    # a bias tensor broadcast over the batch, GQA (2 query heads on 1 KV head)
+    k1, v1 = k[:, :1], v[:, :1]
+    bias = rng.standard_normal((1, h, s, s))
+    O, L = oracle.forward(q, k1, v1, 0.6, True, bias=bias)
+    dQ, dK, dV = oracle.backward(q, k1, v1, do, 0.6, True, bias=bias)
+    dB = oracle.bias_gradient(q, k1, v1, do, 0.6, True, bias)
+    for hq in range(h):
+        acc = np.zeros((len(rows), s))
+        for bi in range(b):
+            Or, Lr = oracle.forward_rows(q[bi, hq, rows], rows, k1[bi, 0], v1[bi, 0], 0.6, True, bias[0, hq, rows])
+            np.testing.assert_allclose(Or, O[bi, hq, rows], atol=1e-13)
+            np.testing.assert_allclose(Lr, L[bi, hq, rows], atol=1e-13)
+            g = oracle.backward_dq_rows(q[bi, hq, rows], do[bi, hq, rows], rows, k1[bi, 0], v1[bi, 0], 0.6, True,
+                                        bias[0, hq, rows])
+            np.testing.assert_allclose(g, dQ[bi, hq, rows], atol=1e-12)
+            acc += oracle.backward_ds_rows(q[bi, hq, rows], do[bi, hq, rows], rows, k1[bi, 0], v1[bi, 0], 0.6,
+                                           True, bias[0, hq, rows])
+        np.testing.assert_allclose(acc, dB[0, hq, rows], atol=1e-12)
+    fn = lambda hq, r0, r1: bias[0, hq, r0:r1]
+    gk, gv = oracle.backward_kv_head(q, k1, v1, do, 0.6, True, 0, 0, row_chunk=2, bias_rows=fn)
+    np.testing.assert_allclose(gk, dK[0, 0], atol=1e-12)
+    np.testing.assert_allclose(gv, dV[0, 0], atol=1e-12)
