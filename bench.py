@@ -628,8 +628,8 @@ def sweep_one(w, peaks, args, quick: bool = False):
         mask_ms = a.elapsed_time(b_)
         kw["dropout_p"], kw["dropout_mask"] = w.dropout, mask
     if w.bias:
-        g = torch.Generator(device="cuda").manual_seed(3)
-        kw["bias"] = torch.randn(1, w.h_q, w.s_q, w.s_kv, device="cuda", generator=g).to(q.dtype)
+        from sdpa_workloads import make_bias
+        kw["bias"] = make_bias(w).cuda()
     fwd = lambda: sdpa.sdpa_fwd(q, k, v, o, lse, attn_scale=w.scale, causal=causal, alibi=w.alibi,
                                 **kw)
     reps = 3 if quick else max(5, min(200, int(2e13 / max(ff, 1))))

@@ -124,6 +124,25 @@ def training_bias(s: int) -> Workload:
                     causal=True, backward=True, bias=True)
 
 
+def backward_d256(causal: bool = True) -> Workload:
+    """The large-head shape of the FP8 forward (b4 h16 s4096 d256) in bf16, forward with the
+    statistics and then the backward pass."""
+    return Workload(f"backward_d256_bf16{'_causal' if causal else ''}_s4096", 4, 16, 16, 4096, 4096, 256,
+                    "bf16", causal=causal, backward=True)
+
+
+def make_bias(w: Workload, seed: int = 3) -> torch.Tensor:
+    """The additive bias of a ``bias`` workload: a [1, h_q, s_q, s_kv] tensor in the input
+    dtype, broadcast over the batch, iid N(0, 1) from a CPU generator seeded with ``seed``,
+    drawn head by head in fp32 and rounded to nearest even (as Q, K, V are)."""
+    g = torch.Generator().manual_seed(seed)
+    dt = _TORCH_DT[w.dtype]
+    out = torch.empty(1, w.h_q, w.s_q, w.s_kv, dtype=dt)
+    for h in range(w.h_q):
+        out[0, h] = torch.randn(w.s_q, w.s_kv, generator=g, dtype=torch.float32).to(dt)
+    return out
+
+
 VARLEN_LENS = (8192, 7168, 6144, 5120, 4096, 3072, 2048, 1024)
 
 

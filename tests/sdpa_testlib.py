@@ -180,3 +180,26 @@ def assert_grad_close(g_gpu: np.ndarray, g_ref: np.ndarray, what: str, zero_tol:
         return
     e = rel_l2(g_gpu, g_ref)
     assert e <= GRAD_REL_L2, f"{what}: rel-L2 {e:.3e}"
+
+
+def run_bwd_fp8(w: Workload, x: Inputs, o, lse, out_dtype=torch.bfloat16):
+    """FP8 backward pass (E4M3 Q, K, V with their descales; dO in x.do's FP8 format with
+    x.descale_do) through the C ABI, gradients in out_dtype."""
+    m = lib()
+    q, k, v, do = to_dev(x.q), to_dev(x.k), to_dev(x.v), to_dev(x.do)
+    ds = {n: torch.tensor([getattr(x, "descale_" + n)], dtype=torch.float32, device="cuda")
+          for n in ("q", "k", "v", "do")}
+    dq, dqb = guarded_empty_like(q, out_dtype)
+    dk, dkb = guarded_empty_like(k, out_dtype)
+    dv, dvb = guarded_empty_like(v, out_dtype)
+    p = m.make_problem(q, k, v, o, attn_scale=w.scale, causal=w.causal, dout=do, dq=dq, dk=dk, dv=dv,
+                       descale_q=ds["q"], descale_k=ds["k"], descale_v=ds["v"], descale_do=ds["do"])
+    ws = torch.empty(m.sdpa_workspace_size(p, True), dtype=torch.uint8, device="cuda")
+    ws.fill_(0xAB)
+    m.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, attn_scale=w.scale, causal=w.causal,
+               descale_q=ds["q"], descale_k=ds["k"], descale_v=ds["v"], descale_do=ds["do"])
+    torch.cuda.synchronize()
+    assert m.sdpa_device_error() == 0
+    for b, n in ((dqb, "dQ"), (dkb, "dK"), (dvb, "dV")):
+        check_guard(b, n)
+    return dq, dk, dv

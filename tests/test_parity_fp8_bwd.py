@@ -12,32 +12,13 @@ import torch
 
 import oracle
 from sdpa_workloads import Workload, make_inputs
-from sdpa_testlib import (FP8_REL_L2, assert_grad_close, check_guard, f64, guarded_empty_like, lib,
-                          rel_l2, run_fwd, to_dev)
+from sdpa_testlib import FP8_REL_L2, assert_grad_close, f64, rel_l2, run_bwd_fp8, run_fwd
 
 pytestmark = pytest.mark.gpu
 
 
-def _fp8_bwd(w, x, o, lse, out_dtype, dout=None):
-    m = lib()
-    q, k, v = to_dev(x.q), to_dev(x.k), to_dev(x.v)
-    do = to_dev(x.do if dout is None else dout)
-    ds = {n: torch.tensor([getattr(x, "descale_" + n)], dtype=torch.float32, device="cuda")
-          for n in ("q", "k", "v", "do")}
-    dq, dqb = guarded_empty_like(q, out_dtype)
-    dk, dkb = guarded_empty_like(k, out_dtype)
-    dv, dvb = guarded_empty_like(v, out_dtype)
-    p = m.make_problem(q, k, v, o, attn_scale=w.scale, causal=w.causal, dout=do, dq=dq, dk=dk, dv=dv,
-                       descale_q=ds["q"], descale_k=ds["k"], descale_v=ds["v"], descale_do=ds["do"])
-    ws = torch.empty(m.sdpa_workspace_size(p, True), dtype=torch.uint8, device="cuda")
-    ws.fill_(0xAB)
-    m.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, attn_scale=w.scale, causal=w.causal,
-               descale_q=ds["q"], descale_k=ds["k"], descale_v=ds["v"], descale_do=ds["do"])
-    torch.cuda.synchronize()
-    assert m.sdpa_device_error() == 0
-    for b, n in ((dqb, "dQ"), (dkb, "dK"), (dvb, "dV")):
-        check_guard(b, n)
-    return dq, dk, dv
+def _fp8_bwd(w, x, o, lse, out_dtype):
+    return run_bwd_fp8(w, x, o, lse, out_dtype)
 
 
 def _decoded(x):

@@ -13,11 +13,12 @@ import pytest
 import torch
 
 import oracle
-from sdpa_workloads import (fp8_large_head, gpt2_inference, grouped, make_inputs,
-                            prefill_bottom_right, sample_kv_heads, sample_rows, training,
-                            training_varlen)
+from sdpa_workloads import (backward_d256, fp8_large_head, gpt2_inference, grouped, make_bias,
+                            make_inputs, prefill_bottom_right, sample_kv_heads, sample_rows, training,
+                            training_alibi, training_bias, training_fp8, training_varlen)
 from sdpa_testlib import (FP8_REL_L2, FWD_MAX_ABS, GRAD_REL_L2, LSE_ABS, assert_fwd_close,
-                          assert_grad_close, f64, rel_l2, run_bwd, run_fwd)
+                          assert_grad_close, f64, guarded_empty_like, check_guard, rel_l2, run_bwd,
+                          run_bwd_fp8, run_fwd)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -25,13 +26,20 @@ N_ROWS = 64
 
 
 def _rows_f64(t, bi, h, rows, descale=1.0):
-    if t.dtype == torch.float8_e4m3fn:  # CPU float8 tensors cannot be indexed: go via bytes
+    # CPU float8 tensors cannot be indexed with a list: go through their bytes
+    if t.dtype == torch.float8_e4m3fn:
         return oracle.decode_e4m3(t.view(torch.uint8)[bi, h, rows].numpy(), descale)
+    if t.dtype == torch.float8_e5m2:
+        return oracle.decode_e5m2(t.view(torch.uint8)[bi, h, rows].numpy(), descale)
     return oracle.to_f64(t[bi, h, rows].cpu(), descale)
 
 
-def _check_rows(w, x, o, lse, dq=None, descales=(1.0, 1.0, 1.0), rel=None):
-    dsq, dsk, dsv = descales
+def _check_rows(w, x, o, lse, dq=None, descales=(1.0, 1.0, 1.0, 1.0), rel=None, bias_rows=None,
+                grad_rel=None):
+    """O, LSE (and dQ) of the sampled rows against the row forms.  bias_rows: optional
+    function (bi, hq, rows) -> [len(rows), s_kv] fp64 additive term (ALiBi or a bias tensor).
+    rel / grad_rel: relative-L2 bounds replacing the 16-bit ones (FP8)."""
+    dsq, dsk, dsv, dsdo = descales
     by_head = {}
     for bi, h, r in sample_rows(w, N_ROWS):
         by_head.setdefault((bi, h), []).append(r)
@@ -42,15 +50,16 @@ def _check_rows(w, x, o, lse, dq=None, descales=(1.0, 1.0, 1.0), rel=None):
         kh = _rows_f64(x.k, bi, hk, slice(None), dsk)
         vh = _rows_f64(x.v, bi, hk, slice(None), dsv)
         qr = _rows_f64(x.q, bi, h, rows, dsq)
-        O, L = oracle.forward_rows(qr, rows, kh, vh, w.scale, w.causal)
+        br = None if bias_rows is None else bias_rows(bi, h, rows)
+        O, L = oracle.forward_rows(qr, rows, kh, vh, w.scale, w.causal, br)
         got_o.append(f64(o[bi, h, rows]))
         want_o.append(O)
         if lse is not None:
             got_l.append(lse[bi, h, rows].cpu().double().numpy())
             want_l.append(L)
         if dq is not None:
-            dor = _rows_f64(x.do, bi, h, rows)
-            want_q.append(oracle.backward_dq_rows(qr, dor, rows, kh, vh, w.scale, w.causal))
+            dor = _rows_f64(x.do, bi, h, rows, dsdo)
+            want_q.append(oracle.backward_dq_rows(qr, dor, rows, kh, vh, w.scale, w.causal, br))
             got_q.append(f64(dq[bi, h, rows]))
     go, wo = np.concatenate(got_o), np.concatenate(want_o)
     if rel is None:
@@ -61,7 +70,26 @@ def _check_rows(w, x, o, lse, dq=None, descales=(1.0, 1.0, 1.0), rel=None):
         err = np.abs(np.concatenate(got_l) - np.concatenate(want_l)).max()
         assert err <= LSE_ABS, f"LSE max abs err {err:.3e}"
     if got_q:
-        assert_grad_close(np.concatenate(got_q), np.concatenate(want_q), "dQ rows")
+        gq, wq = np.concatenate(got_q), np.concatenate(want_q)
+        if grad_rel is None:
+            assert_grad_close(gq, wq, "dQ rows")
+        else:
+            assert rel_l2(gq, wq) <= grad_rel, f"dQ rows rel-L2 {rel_l2(gq, wq):.3e}"
+
+
+def _check_kv_heads(w, x, dk, dv, n_pairs, descales=(1.0, 1.0, 1.0, 1.0), kv_bias_rows=None, grad_rel=None):
+    """Whole dK, dV of seeded (batch, KV head) pairs.  kv_bias_rows: optional function
+    (bi, hq, r0, r1) -> fp64 additive term of query rows r0..r1-1."""
+    q64, k64, v64, do64 = (oracle.to_f64(t, ds) for t, ds in zip((x.q, x.k, x.v, x.do), descales))
+    for bi, hk in sample_kv_heads(w, n_pairs)[:n_pairs]:
+        fn = None if kv_bias_rows is None else (lambda hq, r0, r1, bi=bi: kv_bias_rows(bi, hq, r0, r1))
+        gk, gv = oracle.backward_kv_head(q64, k64, v64, do64, w.scale, w.causal, bi, hk, bias_rows=fn)
+        for got, want, n in ((dk, gk, "dK"), (dv, gv, "dV")):
+            if grad_rel is None:
+                assert_grad_close(f64(got[bi, hk]), want, f"{n}[{bi},{hk}]")
+            else:
+                e = rel_l2(f64(got[bi, hk]), want)
+                assert e <= grad_rel, f"{n}[{bi},{hk}] rel-L2 {e:.3e}"
 
 
 def _full_case(w, dkv_pairs: int):
@@ -70,11 +98,7 @@ def _full_case(w, dkv_pairs: int):
     dq, dk, dv = run_bwd(w, dev, o, lse, x.do)
     _check_rows(w, x, o, lse, dq)
     if dkv_pairs:
-        q64, k64, v64, do64 = (oracle.to_f64(t) for t in (x.q, x.k, x.v, x.do))
-        for bi, hk in sample_kv_heads(w, dkv_pairs)[:dkv_pairs]:
-            gk, gv = oracle.backward_kv_head(q64, k64, v64, do64, w.scale, w.causal, bi, hk)
-            assert_grad_close(f64(dk[bi, hk]), gk, f"dK[{bi},{hk}]")
-            assert_grad_close(f64(dv[bi, hk]), gv, f"dV[{bi},{hk}]")
+        _check_kv_heads(w, x, dk, dv, dkv_pairs)
     return x, dq, dk, dv
 
 
@@ -201,3 +225,70 @@ def test_prefill_bottom_right_rows():
     assert_fwd_close(np.concatenate(got_o), np.concatenate(want_o))
     err = np.abs(np.concatenate(got_l) - np.concatenate(want_l)).max()
     assert err <= LSE_ABS, f"LSE max abs err {err:.3e}"
+
+
+def test_training_alibi_s8192_as_benchmarked():
+    """The training step with ALiBi (default slopes), as the sweep runs it: its key blocks are
+    visited from the diagonal outward, a schedule only long rows exercise."""
+    w = training_alibi(8192)
+    x = make_inputs(w, seed=0, with_do=True)
+    o, lse, dev = run_fwd(w, x, alibi="default")
+    dq, dk, dv = run_bwd(w, dev, o, lse, x.do, alibi="default")
+    slopes = oracle.alibi_default_slopes(w.h_q)
+    rows_fn = lambda bi, hq, rows: oracle.alibi_bias(w.s_q, w.s_kv, slopes[hq], 0, rows=rows)
+    _check_rows(w, x, o, lse, dq, bias_rows=rows_fn)
+    _check_kv_heads(w, x, dk, dv, 2,
+                    kv_bias_rows=lambda bi, hq, r0, r1: rows_fn(bi, hq, np.arange(r0, r1)))
+
+
+def test_training_bias_s8192_as_benchmarked():
+    """The training step with a [1, 16, 8192, 8192] bf16 bias and its gradient, as the sweep runs
+    it: sampled rows of O, LSE, dQ and of dbias (dS summed over the batch), and two whole KV
+    heads of dK, dV."""
+    w = training_bias(8192)
+    x = make_inputs(w, seed=0, with_do=True)
+    bias_cpu = make_bias(w)
+    bias = bias_cpu.cuda()
+    dbias, dbuf = guarded_empty_like(bias)
+    o, lse, dev = run_fwd(w, x, bias=bias)
+    dq, dk, dv = run_bwd(w, dev, o, lse, x.do, bias=bias, dbias=dbias)
+    check_guard(dbuf, "dbias")
+    rows_fn = lambda bi, hq, rows: oracle.to_f64(bias_cpu[0, hq, rows])
+    _check_rows(w, x, o, lse, dq, bias_rows=rows_fn)
+    # dbias rows: the sum over the batch of each sampled row's dS
+    by_head = {}
+    for _, h, r in sample_rows(w, 16, seed=5):
+        by_head.setdefault(h, set()).add(r)
+    got, want = [], []
+    for h, rows in by_head.items():
+        rows = sorted(rows)
+        acc = np.zeros((len(rows), w.s_kv))
+        for bi in range(w.b):
+            hk = oracle.kv_head_of(h, w.h_q, w.h_kv)
+            acc += oracle.backward_ds_rows(_rows_f64(x.q, bi, h, rows), _rows_f64(x.do, bi, h, rows), rows,
+                                           _rows_f64(x.k, bi, hk, slice(None)), _rows_f64(x.v, bi, hk, slice(None)),
+                                           w.scale, True, rows_fn(bi, h, rows))
+        want.append(acc)
+        got.append(f64(dbias[0, h, rows]))
+    assert_grad_close(np.concatenate(got), np.concatenate(want), "dbias rows")
+    _check_kv_heads(w, x, dk, dv, 2, kv_bias_rows=lambda bi, hq, r0, r1: oracle.to_f64(bias_cpu[0, hq, r0:r1]))
+
+
+def test_training_fp8_s8192_as_benchmarked():
+    """The FP8 training step (E4M3 Q, K, V with a bf16 O; E5M2 dO; bf16 gradients) as the sweep
+    runs it, against the oracle on the decoded inputs.  The forward's E4M3 rounding of P enters
+    O and, through Delta = rowsum(dO∘O), the gradients: FP8 tolerances throughout, except the
+    LSE, which the kernel sums from unrounded P."""
+    w = training_fp8(8192)
+    x = make_inputs(w, seed=0, with_do=True)
+    o, lse, _ = run_fwd(w, x)
+    dq, dk, dv = run_bwd_fp8(w, x, o, lse)
+    ds = (x.descale_q, x.descale_k, x.descale_v, x.descale_do)
+    _check_rows(w, x, o, lse, dq, descales=ds, rel=FP8_REL_L2, grad_rel=FP8_REL_L2)
+    _check_kv_heads(w, x, dk, dv, 2, descales=ds, grad_rel=FP8_REL_L2)
+
+
+def test_backward_d256_as_benchmarked():
+    """The d = 256 backward pass at b4 h16 s4096 (bf16, causal): sampled rows and two whole KV
+    heads."""
+    _full_case(backward_d256(True), dkv_pairs=2)
