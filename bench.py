@@ -89,58 +89,91 @@ def aggregate(local_units: float, local_seconds: float, dist=None, device=None):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
-    FIELDS = ("index,pci.bus_id,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples the GPU's SM clock, power draw and clock-event (throttle) reasons every few
+    milliseconds from a background thread, through NVML's read-only queries (ctypes on the
+    driver's libnvidia-ml; no setting is changed).  ``mark(True/False)`` brackets the timed
+    regions: only samples taken inside them count as "under load"."""
 
-    def __init__(self, bus_id: str | None):
-        self.bus_id = (bus_id or "").lower()
-        self.proc = None
-        import tempfile
-        fd, self.path = tempfile.mkstemp(prefix="sdpa_clocks_", suffix=".csv")
-        os.close(fd)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: str | None, bus_id: str | None, period_s: float = 0.002):
+        import threading
+        self.period = period_s
+        self.samples = []          # (t, in_timed_region, sm_mhz, power_w, reasons_bits)
+        self.timed = False
+        self.stop_ev = threading.Event()
+        self.thread = None
+        self.err = None
+        self.nvml = self.dev = None
+        try:
+            import ctypes
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit failed")
+            dev = ctypes.c_void_p()
+            rc = -1
+            if uuid:
+                rc = nv.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(dev))
+            if rc != 0 and bus_id:
+                rc = nv.nvmlDeviceGetHandleByPciBusId_v2(bus_id.encode(), ctypes.byref(dev))
+            if rc != 0:
+                raise RuntimeError(f"no NVML handle for {uuid} / {bus_id}")
+            self.nvml, self.dev, self.ct = nv, dev, ctypes
+            self.reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint(0)
+            nv.nvmlDeviceGetMaxClockInfo(dev, 1, ctypes.byref(mx))   # NVML_CLOCK_SM
+            self.max_mhz = float(mx.value) or None
+        except Exception as e:  # no NVML: the line says so
+            self.err = str(e)
+
+    def _poll(self):
+        ct, nv, dev = self.ct, self.nvml, self.dev
+        clk, pw, rs = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        while not self.stop_ev.is_set():
+            nv.nvmlDeviceGetClockInfo(dev, 1, ct.byref(clk))
+            nv.nvmlDeviceGetPowerUsage(dev, ct.byref(pw))
+            self.reason_fn(dev, ct.byref(rs))
+            self.samples.append((time.perf_counter(), self.timed, float(clk.value), pw.value / 1e3,
+                                 int(rs.value)))
+            self.stop_ev.wait(self.period)
 
     def start(self):
-        try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
-        except Exception:
-            self.proc = None
+        if self.nvml is None:
+            return
+        import threading
+        self.thread = threading.Thread(target=self._poll, daemon=True)
+        self.thread.start()
+
+    def mark(self, timed: bool):
+        self.timed = timed
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        self.proc.terminate()
+        if self.thread is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"],
+                    "how": f"NVML unavailable: {self.err}"}
+        self.stop_ev.set()
+        self.thread.join(timeout=5)
         try:
-            self.proc.wait(timeout=5)
+            self.nvml.nvmlShutdown()
         except Exception:
-            self.proc.kill()
-        self.f.close()
-        rows = []
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 10:
-                continue
-            if self.bus_id and self.bus_id not in parts[1].lower():
-                continue
-            rows.append(parts)
-        try:
-            os.unlink(self.path)
-        except OSError:
             pass
-        if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
-        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
-        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i].lower() == "active"})
-        loaded = [x for x in sm if x > 0.5 * max(sm)] if sm else []
-        return {"sm_mhz": statistics.median(loaded) if loaded else None,
-                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
-                "samples": len(rows)}
+        under = [x for x in self.samples if x[1]]
+        if not under:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"],
+                    "samples": len(self.samples), "samples_under_load": 0}
+        bits = 0
+        for x in under:
+            bits |= x[4]
+        reasons = sorted(name for b, name in self.REASONS.items() if bits & b)
+        return {"sm_mhz": statistics.median(x[2] for x in under), "sm_max_mhz": self.max_mhz,
+                "sm_mhz_min": min(x[2] for x in under), "reasons": reasons,
+                "power_w_median": statistics.median(x[3] for x in under),
+                "power_w_max": max(x[3] for x in under),
+                "samples": len(self.samples), "samples_under_load": len(under),
+                "how": f"NVML read-only queries every {self.period * 1e3:.0f} ms from a thread, over the "
+                       "device-timed and end-to-end timed regions"}
 
 
 # ---------------------------------------------------------------------------
@@ -199,7 +232,7 @@ class Step:
         return sum(t.numel() * t.element_size() for t in self.out_host)
 
 
-def time_device(step: "Step", steps: int, warmup: int):
+def time_device(step: "Step", steps: int, warmup: int, clocks=None):
     """CUDA-event timing on the launching stream: whole steps, and fwd / bwd separately."""
     import torch
     st = torch.cuda.current_stream()
@@ -210,6 +243,8 @@ def time_device(step: "Step", steps: int, warmup: int):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
            torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clocks is not None:
+        clocks.mark(True)
     start.record(st)
     for e0, e1, e2 in ev:
         e0.record(st)
@@ -219,13 +254,15 @@ def time_device(step: "Step", steps: int, warmup: int):
         e2.record(st)
     end.record(st)
     torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.mark(False)
     total_ms = start.elapsed_time(end)
     fwd_ms = [a.elapsed_time(b) for a, b, _ in ev]
     bwd_ms = [b.elapsed_time(c) for _, b, c in ev]
     return total_ms, fwd_ms, bwd_ms
 
 
-def time_e2e(pair, steps: int, warmup: int):
+def time_e2e(pair, steps: int, warmup: int, clocks=None):
     """Same metric through the public API with host buffers: every step copies its Q, K, V,
     dO in from pinned memory, runs fwd + bwd, and copies dQ, dK, dV out, all inside the
     timed region.  Two buffer sets and three streams (H2D, compute, D2H) let step n+1's
@@ -270,6 +307,8 @@ def time_e2e(pair, steps: int, warmup: int):
     finish()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if clocks is not None:
+        clocks.mark(True)
     a.record(comp)
     h2d_st.wait_stream(comp)
     d2h_st.wait_stream(comp)
@@ -278,6 +317,8 @@ def time_e2e(pair, steps: int, warmup: int):
     finish()
     b.record(comp)
     torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.mark(False)
     return a.elapsed_time(b)
 
 
@@ -403,17 +444,19 @@ def run_cuda(args):
         return 0
 
     props = torch.cuda.get_device_properties(device)
-    try:  # nvidia-smi prints DDDDDDDD:BB:DD.F; ":BB:DD." identifies the device
-        bus = ":%02x:%02x." % (props.pci_bus_id, props.pci_device_id)
+    uuid = bus = None
+    try:
+        uuid = "GPU-" + str(props.uuid)
+        bus = "%08x:%02x:%02x.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id, props.pci_device_id)
     except Exception:
-        bus = None
+        pass
+    twin = step.twin(device)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    clocks = ClockSampler(bus)
+    clocks = ClockSampler(uuid, bus)
     clocks.start()
-    total_ms, fwd_ms, bwd_ms = time_device(step, args.steps, args.warmup)
-    clk = clocks.stop()
+    total_ms, fwd_ms, bwd_ms = time_device(step, args.steps, args.warmup, clocks)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -423,8 +466,10 @@ def run_cuda(args):
     units, seconds = aggregate(step_flops * args.steps, total_ms / 1e3, dist, device)
     value = units / seconds / 1e12
 
-    e2e_steps = max(3, args.steps // 4)
-    e2e_ms = time_e2e((step, step.twin(device)), e2e_steps, max(3, args.warmup))
+    # The end-to-end leg times as many steps as the device leg.
+    e2e_steps = args.steps
+    e2e_ms = time_e2e((step, twin), e2e_steps, max(3, args.warmup), clocks)
+    clk = clocks.stop()
     e2e_units, e2e_s = aggregate(step_flops * e2e_steps, e2e_ms / 1e3, dist, device)
 
     fwd_avg = statistics.mean(fwd_ms)
