@@ -23,10 +23,16 @@ static __device__ uint32_t g_device_error = 0;
 constexpr uint32_t kErrTimeout = 1u;
 constexpr uint32_t kErrSmemAlign = 2u;  // dynamic shared memory not 1024-byte aligned
 
-// Upper bound on one wait, in SM clock cycles (~2^31 cycles is about a second at
-// 2 GHz).  After it, the waiting role gives up, records kErrTimeout and lets the
-// kernel run to its clean exit.
-constexpr long long kWaitLimitCycles = 1ll << 31;
+// Waits are bounded: after Waiter::limit SM cycles (a kernel parameter, about a second by
+// default) the waiting role gives up, records kErrTimeout and lets the kernel run to its
+// clean exit.
+
+// What a waiting role needs: its CTA's shared abort flag (set by whichever role gives up
+// first) and the wait bound in SM cycles.
+struct Waiter {
+  volatile int* abort;
+  long long limit;
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -77,18 +83,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with parity `parity` of `bar` has completed.  Gives up after
-// kWaitLimitCycles or as soon as *abort becomes non-zero (another role gave up);
-// returns false then, after recording the timeout in g_device_error and *abort.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+// w.limit cycles or as soon as *w.abort becomes non-zero (another role gave up); returns
+// false then, after recording the timeout in g_device_error and *w.abort.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Waiter& w) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   uint32_t n = 0;
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((++n & 63u) == 0) {
-      if (*abort) return false;
-      if (clock64() - t0 > kWaitLimitCycles) {
-        *abort = 1;
+      if (*w.abort) return false;
+      if (clock64() - t0 > w.limit) {
+        *w.abort = 1;
         atomicOr(&g_device_error, kErrTimeout);
         return false;
       }
@@ -99,8 +105,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // Warp-uniform form of mbar_wait, for code that goes on to warp-collective
 // (.sync.aligned) instructions: every lane waits, and the warp proceeds only if all
 // lanes saw the phase complete.
-__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  const bool ok = mbar_wait(bar, parity, abort);
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const Waiter& w) {
+  const bool ok = mbar_wait(bar, parity, w);
   return __all_sync(0xffffffffu, ok) != 0;
 }
 

@@ -56,6 +56,15 @@ bool debug_sync() {
   return v;
 }
 
+// Bound on every mbarrier wait inside the kernels, in SM cycles: about a second by default;
+// SDPA_WAIT_LIMIT_CYCLES overrides it (read at every call), e.g. to make waits run out on
+// purpose and check that a kernel gives up cleanly and reports SDPA_ERR_TIMEOUT.
+long long wait_limit_cycles() {
+  const char* s = getenv("SDPA_WAIT_LIMIT_CYCLES");
+  const long long x = s ? atoll(s) : 0;
+  return x > 0 ? x : sdpa::ptx_default_wait_limit();
+}
+
 int elem_bytes(int dt) { return (dt == SDPA_DTYPE_E4M3 || dt == SDPA_DTYPE_E5M2) ? 1 : 2; }
 
 // Dense 16-bit copies of FP8 Q, K, V and dO that an E4M3 backward pass widens into the
@@ -357,6 +366,7 @@ sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const void* k, co
   prm.bias_sb = p->bias_strides.b;
   prm.bias_sh = p->bias_strides.h;
   prm.bias_ss = p->bias_strides.s;
+  prm.wait_limit = wait_limit_cycles();
   const bool plain = !prm.alibi && !prm.drop_rows && !prm.bias;
   prm.one_tile = sdpa::fwd_prefer_one_tile(p->b, p->h_q, p->s_q, p->d, p->in_dtype, plain, num_sms()) ? 1 : 0;
   // SDPA_FWD_Q_TILES=1 or 2 overrides the choice where both schedules exist (plain 16-bit,
@@ -513,6 +523,7 @@ sdpa_status_t sdpa_bwd(const sdpa_problem_t* p, const void* q, const void* k, co
   prm.drop_cols = p->dropout_p > 0.f ? p->dropout_mask_t : nullptr;
   prm.drop_q_words = words_of(p->s_q);
   prm.s_q_pad = s_q_pad;
+  prm.wait_limit = wait_limit_cycles();
   prm.scale = p->attn_scale;
   prm.scale_log2 = p->attn_scale * 1.4426950408889634f;
   prm.kv_split = sdpa::bwd_kv_split(p->b, p->h_q, p->h_kv, p->s_kv);

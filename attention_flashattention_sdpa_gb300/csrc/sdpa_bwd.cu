@@ -410,10 +410,15 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort;
+  const Waiter wt{abort_flag, p.wait_limit};
 
   // iteration n -> (query head, query block)
   auto iter_head = [&](int n) { return head0 + n / per_head; };
   auto iter_qblk = [&](int n) { return q_first + n % per_head; };
+
+  // Copies the producer has issued (for the drain at the end, should a role give up).
+  bool producer = false;
+  int nq = 0, nd = 0;   // Q and dO tiles issued
 
   // Register budget per thread: 64 for the producer / MMA warpgroup, 152 for each compute
   // warpgroup, 144 for the dQ drain (64 + 2 x 152 + 144 = 4 x 128, the launch's budget).
@@ -422,12 +427,12 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   if (warp == 0) {
     // ================================ TMA producer ====================================
     if (elect_one_sync()) {
+      producer = true;
       mbar_arrive_expect_tx(&bars.kv_full, 2 * C::TILE);
       for (int c = 0; c < C::NCHUNK; ++c) {
         tma_load_4d(sK + c * 16384, &p.tm_k, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
         tma_load_4d(sV + c * 16384, &p.tm_v, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
       }
-      int nq = 0, nd = 0;   // Q and dO tiles issued
       bool ok = true;
       for (int n = 0; n < n_iter && ok; ++n) {
         const int hq = iter_head(n), qb = iter_qblk(n);
@@ -436,7 +441,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
           // Q(n) -> slot n % 2 (use n / 2); dO(n) -> slot 2 + n % NDO (use n / NDO).
           const int slot = which == 0 ? (n & 1) : 2 + n % C::NDO;
           const int use = which == 0 ? (n >> 1) : n / C::NDO;
-          if (!mbar_wait(&bars.ring_empty[slot], (use & 1) ^ 1, abort_flag)) {
+          if (!mbar_wait(&bars.ring_empty[slot], (use & 1) ^ 1, wt)) {
             ok = false;
             break;
           }
@@ -450,13 +455,6 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
           if (which == 0) ++nq; else ++nd;
         }
       }
-      if (!ok || *abort_flag) {
-        // Let copies already issued land before the CTA's shared memory is released.
-        mbar_wait_drain(&bars.kv_full, 0);
-        for (int m = (nq > 2 ? nq - 2 : 0); m < nq; ++m) mbar_wait_drain(&bars.ring_full[m & 1], (m >> 1) & 1);
-        for (int m = (nd > C::NDO ? nd - C::NDO : 0); m < nd; ++m)
-          mbar_wait_drain(&bars.ring_full[2 + m % C::NDO], (m / C::NDO) & 1);
-      }
     }
   } else if (warp == 1) {
     // ================================ MMA issuer ======================================
@@ -466,12 +464,12 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       const uint32_t idesc_acc = make_idesc(fmt, 128, D, false, true);       // dV, dK
       const uint32_t idesc_dq = make_idesc(fmt, 128, D, true, true);         // dQ
       const uint32_t kA = smem_u32(sK), vA = smem_u32(sV), dsA = smem_u32(sDS);
-      bool ok = mbar_wait(&bars.kv_full, 0, abort_flag);
+      bool ok = mbar_wait(&bars.kv_full, 0, wt);
       tc_fence_after();
       // Sᵀ = K·Qᵀ of step m into region `reg` (Q of step m is in slot m % 2).
       auto issue_s = [&](int reg, int m, int& qslot) -> bool {
         qslot = m & 1;
-        if (!mbar_wait(&bars.ring_full[qslot], (m >> 1) & 1, abort_flag)) return false;
+        if (!mbar_wait(&bars.ring_full[qslot], (m >> 1) & 1, wt)) return false;
         tc_fence_after();
         const uint32_t qB = smem_u32(sRing + qslot * C::TILE);
 #pragma unroll
@@ -493,8 +491,8 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         const uint32_t qB = smem_u32(sRing + qslot * C::TILE);
         // ---- dPᵀ = V·dOᵀ (into the region dQ of the previous step used) ----
         const int gslot = 2 + n % C::NDO;
-        if (!mbar_wait(&bars.ring_full[gslot], (n / C::NDO) & 1, abort_flag)) { ok = false; break; }
-        if (n >= 1 && !mbar_wait(&bars.dq_free[b ^ 1], ((n - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&bars.ring_full[gslot], (n / C::NDO) & 1, wt)) { ok = false; break; }
+        if (n >= 1 && !mbar_wait(&bars.dq_free[b ^ 1], ((n - 1) >> 1) & 1, wt)) { ok = false; break; }
         tc_fence_after();
         const uint32_t gB = smem_u32(sRing + gslot * C::TILE);
 #pragma unroll
@@ -505,7 +503,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         }
         tc_commit(&bars.dp_full[b]);
         // ---- dV += Pᵀ·dO  (Pᵀ in TMEM: q 0..63 at X+0.., q 64..127 at X+64..) ----
-        if (!mbar_wait(&bars.p_full[b], par, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&bars.p_full[b], par, wt)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -516,12 +514,12 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         tc_commit(&bars.ring_empty[gslot]);
         // ---- Sᵀ of the next step, as soon as dPᵀ has left region Y ----
         if (n + 1 < n_iter) {
-          if (!mbar_wait(&bars.dp_consumed[b], par, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&bars.dp_consumed[b], par, wt)) { ok = false; break; }
           if (!issue_s(b ^ 1, n + 1, qslot_next)) { ok = false; break; }
         }
         // ---- dQ = dS·K first (its drain gates the next dPᵀ), then dK += dSᵀ·Q (dS read
         //      K-major from shared memory) ----
-        if (!mbar_wait(&bars.ds_full[b], par, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&bars.ds_full[b], par, wt)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -589,9 +587,9 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       // This step's -LSE and -Delta vectors arrive with its Q and dO tiles.  Both waits come
       // before Pᵀ is released: dO's slot is refilled once dV of this step has read it, and
       // dV needs Pᵀ, so the refill cannot overtake these waits.
-      if (!mbar_wait_warp(&bars.ring_full[n & 1], (n >> 1) & 1, abort_flag)) { ok = false; break; }
-      if (!mbar_wait_warp(&bars.ring_full[2 + n % C::NDO], (n / C::NDO) & 1, abort_flag)) { ok = false; break; }
-      if (!mbar_wait_warp(&bars.s_full[b], par, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars.ring_full[n & 1], (n >> 1) & 1, wt)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars.ring_full[2 + n % C::NDO], (n / C::NDO) & 1, wt)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars.s_full[b], par, wt)) { ok = false; break; }
       tc_fence_after();
       uint32_t sv[64];
       tmem_ld32(X + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
@@ -642,7 +640,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       tc_fence_before();
       mbar_arrive(&bars.p_full[b]);
       // dSᵀ = Pᵀ ∘ (dPᵀ − Delta)
-      if (!mbar_wait_warp(&bars.dp_full[b], par, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars.dp_full[b], par, wt)) { ok = false; break; }
       tc_fence_after();
       uint32_t ds[32];
       float2 dbhold = make_float2(0.f, 0.f);   // pairs of dS awaiting a 4-wide reduce-add
@@ -691,7 +689,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       // columns 64h..64h+63: read K-major (rows = keys) as the A operand of dK += dSᵀ·Q and
       // MN-major (rows = queries) as the A operand of dQ = dS·K.  The previous step's dQ and
       // dK MMAs must have finished reading it.
-      if (n >= 1 && !mbar_wait_warp(&bars.dsbuf_free[b ^ 1], ((n - 1) >> 1) & 1, abort_flag)) { ok = false; break; }
+      if (n >= 1 && !mbar_wait_warp(&bars.dsbuf_free[b ^ 1], ((n - 1) >> 1) & 1, wt)) { ok = false; break; }
       uint8_t* rowp = sDS + h * 16384 + r * 128;
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -702,7 +700,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       mbar_arrive(&bars.ds_full[b]);
     }
     // ---- epilogue: dV (h = 0) or dK (h = 1) through shared memory and a TMA store ----
-    ok = ok && mbar_wait_warp(&bars.acc_full, 0, abort_flag);
+    ok = ok && mbar_wait_warp(&bars.acc_full, 0, wt);
     uint8_t* stage = sRing + h * C::TILE;
     if (ok && p.kv_split > 1) {
       // Split group: add this CTA's share into the fp32 accumulator (once per CTA).
@@ -754,7 +752,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     // end by completion or timeout.
     mbar_arrive(&bars.epi_ready[h]);
     if (r == 0) {
-      const bool all_ok = mbar_wait(&bars.epi_ready[h], 0, abort_flag) && ok && !*abort_flag;
+      const bool all_ok = mbar_wait(&bars.epi_ready[h], 0, wt) && ok && !*abort_flag;
       if (all_ok && p.kv_split == 1) {
         const CUtensorMap* map = (h == 0) ? &p.tm_dv : &p.tm_dk;
         for (int c = 0; c < D / 64; ++c)
@@ -778,7 +776,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     int use[2] = {0, 0};                                  // times each buffer has been filled
     for (int n = 0; n < n_iter && ok; ++n) {
       const int b = n & 1;
-      if (!mbar_wait_warp(&bars.dq_full[b], (n >> 1) & 1, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars.dq_full[b], (n >> 1) & 1, wt)) { ok = false; break; }
       tc_fence_after();
       const int hq = iter_head(n);
       const int row0 = (bi * p.h_q + hq) * p.s_q_pad + iter_qblk(n) * kBlockM;
@@ -794,7 +792,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       for (int c = 0; c < NCH; ++c) {
         const int buf = c & 1;
         // Buffer `buf` is free once the reduce-add of its previous fill has read it.
-        if (use[buf] > 0 && !mbar_wait_warp(&bars.stage_free[buf], (use[buf] - 1) & 1, abort_flag)) {
+        if (use[buf] > 0 && !mbar_wait_warp(&bars.stage_free[buf], (use[buf] - 1) & 1, wt)) {
           ok = false;
           break;
         }
@@ -807,7 +805,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         fence_proxy_async_smem();
         mbar_arrive(&bars.stage_full[buf]);
         if (r == 0) {
-          if (!mbar_wait(&bars.stage_full[buf], use[buf] & 1, abort_flag)) ok = false;
+          if (!mbar_wait(&bars.stage_full[buf], use[buf] & 1, wt)) ok = false;
           if (ok) {
             tma_reduce_add_2d(&p.tm_dqacc, sDQ + buf * 16384, c * 32, row0);
             tma_store_commit();
@@ -826,6 +824,15 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
 
   tc_fence_before();
   __syncthreads();
+  // Every role is done.  If one gave up (the abort flag, visible to all after the barrier),
+  // copies the producer issued may still be in flight: let them land before the CTA's shared
+  // memory is released.  (Each ring slot holds at most one copy in flight.)
+  if (producer && *abort_flag) {
+    mbar_wait_drain(&bars.kv_full, 0);
+    for (int m = (nq > 2 ? nq - 2 : 0); m < nq; ++m) mbar_wait_drain(&bars.ring_full[m & 1], (m >> 1) & 1);
+    for (int m = (nd > C::NDO ? nd - C::NDO : 0); m < nd; ++m)
+      mbar_wait_drain(&bars.ring_full[2 + m % C::NDO], (m / C::NDO) & 1);
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -859,7 +866,7 @@ struct D256 {
 static_assert(D256::SMEM_BYTES <= 232448, "shared memory budget");
 
 struct alignas(8) D256Barriers {
-  uint64_t kv_full, ld_far, ld_near, s_done, dp_done, mma_done;
+  uint64_t kv_full, ld_far, ld_near, s_done, dp_done, mma_done, drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -920,6 +927,7 @@ __global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant_
     mbar_init(&bars.s_done, 1);
     mbar_init(&bars.dp_done, 1);
     mbar_init(&bars.mma_done, 1);
+    mbar_init(&bars.drain, 1);
     bars.abort = 0;
     fence_mbar_init();
   }
@@ -932,13 +940,16 @@ __global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort;
+  const Waiter wt{abort_flag, p.wait_limit};
   const uint32_t fmt = (DT == kBF16) ? 1u : 0u;
   const BwdScales bs = bwd_scales(p);
 
   // Q and dO tiles of step n (one thread), in two parts: the d-half this CTA does not own
   // (read only by the Sᵀ and dPᵀ MMAs, so it can be refilled once those are done), and its
   // own d-half with the -LSE/-Delta vectors (refilled after the step's last MMAs).
+  int n_far = 0, n_near = 0;   // loads issued on ld_far / ld_near (one in flight at a time)
   auto load_far = [&](int n) {
+    ++n_far;
     const int hq = head0 + n / per_head;
     const int q0 = (q_first + n % per_head) * C::BQ;
     mbar_arrive_expect_tx(&bars.ld_far, 32768);
@@ -948,6 +959,7 @@ __global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant_
     }
   };
   auto load_near = [&](int n) {
+    ++n_near;
     const int hq = head0 + n / per_head;
     const int q0 = (q_first + n % per_head) * C::BQ;
     const int64_t vrow = (static_cast<int64_t>(bi) * p.h_q + hq) * p.s_q_pad + q0;
@@ -970,7 +982,7 @@ __global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant_
       load_near(0);
     }
   }
-  bool ok = __syncthreads_and(mbar_wait(&bars.kv_full, 0, abort_flag));
+  bool ok = __syncthreads_and(mbar_wait(&bars.kv_full, 0, wt));
   uint32_t ph_ld = 0, ph_mma = 0;
   for (int n = 0; n < n_iter && ok; ++n) {
     const int hq = head0 + n / per_head;
@@ -978,8 +990,8 @@ __global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant_
     // The previous step's dQᵀ reduce-adds read the staging buffer and the dS buffer: both
     // are rewritten below, after this barrier.
     if (threadIdx.x == kIssuer) bulk_wait_read<0>();
-    ok = __syncthreads_and(mbar_wait(&bars.ld_far, ph_ld, abort_flag) &&
-                           mbar_wait(&bars.ld_near, ph_ld, abort_flag));
+    ok = __syncthreads_and(mbar_wait(&bars.ld_far, ph_ld, wt) &&
+                           mbar_wait(&bars.ld_near, ph_ld, wt));
     ph_ld ^= 1;
     if (!ok) break;
     // ---- Sᵀ = K·Qᵀ, then dPᵀ = V·dOᵀ, over all of d: committed separately, so that Pᵀ is
@@ -1013,7 +1025,7 @@ __global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant_
           p.drop_cols + ((static_cast<int64_t>(bi) * p.h_q + hq) * p.s_kv + kv_row) * p.drop_q_words + q0 / 32));
     float pf[64];                                  // Pᵀ of key row r (every P, for dS)
     // ---- Pᵀ for key row r, over Sᵀ in TMEM (the kept P under dropout: dV's operand) ----
-    bool w_ok = !compute || mbar_wait(&bars.s_done, ph_mma, abort_flag);
+    bool w_ok = !compute || mbar_wait(&bars.s_done, ph_mma, wt);
     if (w_ok && compute) {
       tc_fence_after();
       uint32_t sv[64];
@@ -1066,7 +1078,7 @@ __global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant_
                idesc_acc, (n > 0 || k > 0) ? 1u : 0u, false);
     }
     // ---- dS = P ∘ (dPᵀ − Delta) for key row r, to shared memory ----
-    w_ok = mbar_wait(&bars.dp_done, ph_mma, abort_flag);
+    w_ok = mbar_wait(&bars.dp_done, ph_mma, wt);
     // The Sᵀ and dPᵀ MMAs are done: the other d-half of Q and dO may be refilled.
     if (threadIdx.x == kIssuer && w_ok && n + 1 < n_iter) load_far(n + 1);
     if (w_ok && compute) {
@@ -1120,7 +1132,7 @@ __global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant_
                make_sdesc_sw128(smem_u32(sDS) + k * 2048, 8192, 1024), idesc_dq, k > 0, false);
       tc_commit(&bars.mma_done);
     }
-    ok = __syncthreads_and(mbar_wait(&bars.mma_done, ph_mma, abort_flag));
+    ok = __syncthreads_and(mbar_wait(&bars.mma_done, ph_mma, wt));
     ph_mma ^= 1;
     if (!ok) break;
     tc_fence_after();
@@ -1157,6 +1169,15 @@ __global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant_
   if (threadIdx.x == kIssuer) {
     bulk_wait_read<0>();
     tma_store_wait_all();
+    if (!ok) {
+      // A role gave up: let every MMA and copy this thread issued finish before TMEM and
+      // shared memory are released.
+      tc_commit(&bars.drain);
+      mbar_wait_drain(&bars.drain, 0);
+      mbar_wait_drain(&bars.kv_full, 0);
+      if (n_far > 0) mbar_wait_drain(&bars.ld_far, (n_far - 1) & 1);
+      if (n_near > 0) mbar_wait_drain(&bars.ld_near, (n_near - 1) & 1);
+    }
   }
 
   // ---- epilogue: this half of dV and dK ----

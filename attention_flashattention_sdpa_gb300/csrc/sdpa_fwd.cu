@@ -200,6 +200,11 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort;
+  const Waiter wt{abort_flag, p.wait_limit};
+
+  // Copies the producer has issued (for the drain at the end, should a role give up).
+  bool producer = false;
+  int kv_issued = 0;
 
   // With two Q tiles (384 threads, 168 registers each at launch) the producer / MMA
   // warpgroup gives registers to the two softmax warpgroups: 80 + 2 x 208 <= 3 x 168.
@@ -222,7 +227,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       auto load = [&](const CUtensorMap* map, int j) {
         const int slot = it % NS;
         const uint32_t ph = (it / NS) & 1;
-        if (!mbar_wait(&bars.kv_empty[slot], ph ^ 1, abort_flag)) return false;
+        if (!mbar_wait(&bars.kv_empty[slot], ph ^ 1, wt)) return false;
         mbar_arrive_expect_tx(&bars.kv_full[slot], C::TILE_BYTES);
         uint8_t* dst = sRing + slot * C::TILE_BYTES;
         for (int c = 0; c < C::NCHUNK; ++c)
@@ -231,6 +236,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         ++it;
         return true;
       };
+      producer = true;
       if (NQT == 2) {
         for (int j = 0; j < n_blocks && ok; ++j) {
           ok = load(&p.tm_k, j);
@@ -243,12 +249,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
           if (ok) ok = load(&p.tm_v, j);
         }
       }
-      if (!ok || *abort_flag) {
-        // Let copies already issued land before the CTA's shared memory is released.
-        for (int t = 0; t < NQT; ++t) mbar_wait_drain(&bars.q_full[t], 0);
-        for (int k = (it > NS ? it - NS : 0); k < it; ++k)
-          mbar_wait_drain(&bars.kv_full[k % NS], (k / NS) & 1);
-      }
+      kv_issued = it;
     }
   } else if (warp == 1) {
     // ================================ MMA issuer ======================================
@@ -261,7 +262,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       bool ok = true;
       auto wait_full = [&]() -> int {
         const int slot = it % NS;
-        if (!mbar_wait(&bars.kv_full[slot], (it / NS) & 1, abort_flag)) return -1;
+        if (!mbar_wait(&bars.kv_full[slot], (it / NS) & 1, wt)) return -1;
         ++it;
         tc_fence_after();
         return slot;
@@ -288,7 +289,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         }
       };
       ok = n_blocks > 0;
-      for (int t = 0; t < NQT && ok; ++t) ok = mbar_wait(&bars.q_full[t], 0, abort_flag);
+      for (int t = 0; t < NQT && ok; ++t) ok = mbar_wait(&bars.q_full[t], 0, wt);
       tc_fence_after();
       if (NQT == 2) {
         int kslot = ok ? wait_full() : -1;
@@ -303,7 +304,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
           if (vslot < 0) { ok = false; break; }
           const uint32_t ph = j & 1;
           // tile 0
-          if (!mbar_wait(&bars.p_full[0], ph, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&bars.p_full[0], ph, wt)) { ok = false; break; }
           tc_fence_after();
           issue_pv(0, 0, vslot, j == 0);
           if (j + 1 == n_blocks) tc_commit(&bars.o_full[0]);
@@ -314,7 +315,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
             issue_s(0, 0, nk);
           }
           // tile 1
-          if (!mbar_wait(&bars.p_full[1], ph, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&bars.p_full[1], ph, wt)) { ok = false; break; }
           tc_fence_after();
           issue_pv(1, 1, vslot, j == 0);
           if (j + 1 == n_blocks) tc_commit(&bars.o_full[1]);
@@ -340,7 +341,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
           }
           const int vslot = wait_full();
           if (vslot < 0) { ok = false; break; }
-          if (!mbar_wait(&bars.p_full[j & 1], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(&bars.p_full[j & 1], (j >> 1) & 1, wt)) { ok = false; break; }
           tc_fence_after();
           issue_pv(0, j & 1, vslot, j == 0);
           tc_commit(&bars.pv_done);
@@ -430,7 +431,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
           }
         }
       }
-      if (!mbar_wait_warp(&bars.s_full[slot], ph, abort_flag)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars.s_full[slot], ph, wt)) { ok = false; break; }
       tc_fence_after();
       const uint32_t s_addr = tmem + lane_off + slot * 128;
 
@@ -490,7 +491,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         // running max (and rescale O together).
         xch[j & 1][hc][r] = m_cand;
         mbar_arrive(&bars.mx_ready[j & 1]);
-        if (!mbar_wait_warp(&bars.mx_ready[j & 1], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp(&bars.mx_ready[j & 1], (j >> 1) & 1, wt)) { ok = false; break; }
         m_cand = fmaxf(m_cand, xch[j & 1][hc ^ 1][r]);
       }
       float alpha = 1.f;
@@ -548,7 +549,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
 
       if (NQT == 1 && j > 0) {
         // O is still being accumulated by the previous block's P·V.
-        if (!mbar_wait_warp(&bars.pv_done, (j - 1) & 1, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp(&bars.pv_done, (j - 1) & 1, wt)) { ok = false; break; }
         tc_fence_after();
       }
       if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
@@ -572,7 +573,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
 
     // ---- epilogue: O / l through shared memory and a TMA store; LSE ------------------
     // A CTA whose rows see no key at all (padding) skips the pipeline and writes zeros.
-    ok = ok && (n_blocks == 0 || mbar_wait_warp(&bars.o_full[t], 0, abort_flag));
+    ok = ok && (n_blocks == 0 || mbar_wait_warp(&bars.o_full[t], 0, wt));
     uint8_t* stage = (NQT == 1) ? sRing
                      : (C::STAGE_BYTES > 0) ? sRing + C::RING_BYTES + t * C::OUT_TILE
                                             : sQ + t * C::TILE_BYTES;
@@ -581,7 +582,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       // happened, so the bounded wait can only fail through a timeout.
       xl[hc][r] = l;
       mbar_arrive(&bars.l_ready);
-      ok = ok && mbar_wait_warp(&bars.l_ready, 0, abort_flag);
+      ok = ok && mbar_wait_warp(&bars.l_ready, 0, wt);
       if (ok) l += xl[hc ^ 1][r];
     }
     if (ok) {
@@ -623,7 +624,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
     // bounded wait below can only fail through a timeout, never deadlock.
     mbar_arrive(&bars.epi_ready[t]);
     if (r == 0 && hc == 0) {
-      const bool all_ok = mbar_wait(&bars.epi_ready[t], 0, abort_flag) && ok && !*abort_flag;
+      const bool all_ok = mbar_wait(&bars.epi_ready[t], 0, wt) && ok && !*abort_flag;
       if (all_ok) {
         for (int c = 0; c < D / 64; ++c)
           tma_store_4d(&p.tm_o, stage + c * 16384, c * 64, tile_row0, hq, bi);
@@ -635,6 +636,14 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  // Every role is done.  If one gave up (the abort flag, visible to all after the barrier),
+  // copies the producer issued may still be in flight: let them land before the CTA's shared
+  // memory is released.  (Each ring slot holds at most one copy in flight.)
+  if (producer && *abort_flag) {
+    for (int t = 0; t < NQT; ++t) mbar_wait_drain(&bars.q_full[t], 0);
+    for (int k = (kv_issued > NS ? kv_issued - NS : 0); k < kv_issued; ++k)
+      mbar_wait_drain(&bars.kv_full[k % NS], (k / NS) & 1);
+  }
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);

@@ -41,6 +41,7 @@ struct FwdParams {
   float drop_scale;           // 1 / (1 - p), or 1 without dropout
   const void* bias;           // additive bias [b][h_q][s_q][s_kv] (input dtype), or nullptr
   int64_t bias_sb, bias_sh, bias_ss;   // element strides (0 broadcasts b or h)
+  long long wait_limit;       // bound on one mbarrier wait, SM cycles
 };
 
 // Number of Q tiles (of 128 rows) one forward CTA processes.
@@ -107,6 +108,7 @@ struct BwdParams {
   // Bias gradient: dS reduce-added into a zeroed fp32 workspace laid out like bias_t,
   // [bias_nb][bias_nh][s_kv][s_q_pad], or nullptr.
   float* dbias_acc;
+  long long wait_limit;         // bound on one mbarrier wait, SM cycles
 };
 
 // dbias[nb][nh][s_q][s_kv] (16-bit, caller strides) from the transposed fp32 accumulator.
@@ -160,6 +162,9 @@ inline cudaError_t set_smem_once(const void* kern, int bytes) {
   if (e == cudaSuccess) done.insert({kern, dev});
   return e;
 }
+
+// Default bound on one mbarrier wait, in SM cycles (about a second).
+constexpr long long ptx_default_wait_limit() { return 1ll << 31; }
 
 // Kernel feature bits (compile-time variants of the forward and backward kernels).
 constexpr int kFeatAlibi = 1;

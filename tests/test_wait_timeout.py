@@ -1,0 +1,73 @@
+"""Failure detection without a GPU fault: every wait inside the kernels is bounded, and a
+wait that runs out makes its kernel give up cleanly (the other roles drop out, copies and
+MMAs already issued are drained, tensor memory is freed) and report SDPA_ERR_TIMEOUT.
+
+A child process shortens the bound to a thousand SM cycles (SDPA_WAIT_LIMIT_CYCLES), so that
+the waits for the first tiles of a normal problem run out, and checks the status of the
+forward pass and of both backward kernels (d = 128 and d = 256) under SDPA_DEBUG_SYNC.  It
+then restores the default bound in the same process and checks that the same calls give
+correct results: the context is still usable."""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+CHILD = r'''
+import os, sys
+sys.path.insert(0, os.path.join(ROOT, "tests")); sys.path.insert(0, ROOT)
+import numpy as np, torch
+import attention_flashattention_sdpa_gb300 as m
+import oracle
+from sdpa_workloads import Workload, make_inputs
+from sdpa_testlib import assert_fwd_close, assert_grad_close, f64, to_dev
+
+def step(w, x):
+    q, k, v, do = to_dev(x.q), to_dev(x.k), to_dev(x.v), to_dev(x.do)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.b, w.h_q, w.s_q, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    p = m.make_problem(q, k, v, o, attn_scale=w.scale, causal=True, dout=do, dq=dq, dk=dk, dv=dv)
+    ws = torch.empty(m.sdpa_workspace_size(p, True), dtype=torch.uint8, device="cuda")
+    st = []
+    for f in (lambda: m.sdpa_fwd(q, k, v, o, lse, attn_scale=w.scale, causal=True),
+              lambda: m.sdpa_bwd(q, k, v, o, do, lse, dq, dk, dv, ws, attn_scale=w.scale, causal=True)):
+        try:
+            f()
+            st.append(0)
+        except m.SdpaError as e:
+            st.append(e.status)
+    torch.cuda.synchronize()
+    return st, (o, lse, dq, dk, dv)
+
+for d in (128, 256):
+    w = Workload("t", 1, 4, 4, 1024, 1024, d, "bf16", causal=True, backward=True)
+    x = make_inputs(w, seed=d, with_do=True)
+    os.environ["SDPA_WAIT_LIMIT_CYCLES"] = "1000"
+    st, _ = step(w, x)
+    assert st == [6, 6], f"d={d}: statuses {st}, want SDPA_ERR_TIMEOUT for both passes"
+    assert "bounded device wait" in m.sdpa_last_error_string()
+    assert m.sdpa_device_error() == 0, "the flag is reported once and then cleared"
+    del os.environ["SDPA_WAIT_LIMIT_CYCLES"]
+    st, (o, lse, dq, dk, dv) = step(w, x)
+    assert st == [0, 0], f"d={d}: statuses {st} after restoring the bound"
+    q64, k64, v64, do64 = f64(x.q), f64(x.k), f64(x.v), f64(x.do)
+    O, L = oracle.forward(q64, k64, v64, w.scale, True)
+    assert_fwd_close(f64(o), O)
+    dQ, dK, dV = oracle.backward(q64, k64, v64, do64, w.scale, True)
+    for g, r, n in ((dq, dQ, "dQ"), (dk, dK, "dK"), (dv, dV, "dV")):
+        assert_grad_close(f64(g), r, n)
+print("WAIT_TIMEOUT_OK")
+'''
+
+
+@pytest.mark.gpu
+def test_waits_that_run_out_report_a_timeout_and_leave_the_context_usable():
+    env = dict(os.environ, SDPA_DEBUG_SYNC="1")
+    env.pop("SDPA_WAIT_LIMIT_CYCLES", None)
+    r = subprocess.run([sys.executable, "-c", f"ROOT = {ROOT!r}\n" + CHILD], env=env, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0 and "WAIT_TIMEOUT_OK" in r.stdout, r.stdout[-3000:] + r.stderr[-3000:]
+
