@@ -82,23 +82,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait until the phase with parity `parity` of `bar` has completed.  Gives up after
-// w.limit cycles or as soon as *w.abort becomes non-zero (another role gave up); returns
-// false then, after recording the timeout in g_device_error and *w.abort.
+// Non-blocking test of the same condition.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait until the phase with parity `parity` of `bar` has completed.  Gives up once w.limit
+// cycles have passed since a first non-blocking test found the phase incomplete, or as soon
+// as *w.abort becomes non-zero (another role gave up); returns false then, after recording
+// the timeout in g_device_error and *w.abort.  Both are checked before every potentially
+// suspending try_wait, so a bound of a cycle or two gives up at the first incomplete phase.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const Waiter& w) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_test_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  uint32_t n = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++n & 63u) == 0) {
-      if (*w.abort) return false;
-      if (clock64() - t0 > w.limit) {
-        *w.abort = 1;
-        atomicOr(&g_device_error, kErrTimeout);
-        return false;
-      }
+    if (*w.abort) return false;
+    if (clock64() - t0 > w.limit) {
+      *w.abort = 1;
+      atomicOr(&g_device_error, kErrTimeout);
+      return false;
     }
+    if (mbar_try_wait(bar, parity)) return true;
   }
 }
 

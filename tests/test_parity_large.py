@@ -151,7 +151,7 @@ def test_fp8_large_head_rows():
     w = fp8_large_head()
     x = make_inputs(w, seed=0, with_do=False)
     o, lse, _ = run_fwd(w, x)
-    _check_rows(w, x, o, lse, None, (x.descale_q, x.descale_k, x.descale_v), rel=FP8_REL_L2)
+    _check_rows(w, x, o, lse, None, (x.descale_q, x.descale_k, x.descale_v, 1.0), rel=FP8_REL_L2)
 
 
 def test_training_varlen_as_benchmarked():
