@@ -441,23 +441,5 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return d;
 }
 
-// 2^x on the FMA/ALU pipes, to take part of the exponentials off the MUFU unit.
-// x = j + f with j = round(x) and f in [-1/2, 1/2]: adding 1.5 * 2^23 rounds x to an integer
-// held in the low mantissa bits of t.  2^f comes from a cubic fitted (Remez exchange on the
-// relative error) on [-1/2, 1/2]: max relative error 7.5e-5, below half an ulp of the fp16 /
-// bf16 / e4m3 values it feeds.  2^j is added to the exponent field: the low 9 bits of t's
-// pattern hold j, so (bits(t) << 23) is j << 23.  x is clamped at -125 (result >= 2^-125), and
-// must stay below 127.
-__device__ __forceinline__ float exp2_poly(float x) {
-  constexpr float kRound = 12582912.0f;   // 1.5 * 2^23
-  constexpr float c0 = 0.9999280571937561f, c1 = 0.6932609677314758f;
-  constexpr float c2 = 0.2426111251115799f, c3 = 0.0551716685295105f;
-  x = fmaxf(x, -125.0f);
-  const float t = x + kRound;
-  const float f = x - (t - kRound);
-  const float p = fmaf(fmaf(fmaf(c3, f, c2), f, c1), f, c0);
-  return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-}
-
 }  // namespace ptx
 }  // namespace sdpa

@@ -259,11 +259,6 @@ __global__ void __launch_bounds__(256) bwd_kv_convert_kernel(const BwdParams p) 
 // 2. main kernel
 // ---------------------------------------------------------------------------
 
-// Share of P's exponentials computed on the FMA pipe (one pair in kPolyEvery; 0 = none).
-// With the Q/dO ring keeping the tensor core fed, the FMA pipe is the busier one: every
-// exponential on the MUFU unit measured fastest (1 in 4 on the FMA pipe: -6%).
-constexpr int kPolyEvery = 0;
-
 template <int D>
 struct BwdCfg {
   static constexpr int TILE = kBlockM * D * 2;        // one 128-row tile of Q, K, V or dO
@@ -613,10 +608,8 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         if constexpr (ALIBI) nl = add2(nl, kr2);
         if constexpr (BIAS) nl = fma2(bias_pair<DT>(bz, c), make_float2(kLog2e, kLog2e), nl);
         const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl);
-        // A fixed share of the pairs is computed on the FMA pipe, the rest on the MUFU unit.
-        const bool poly = kPolyEvery > 0 && (c / 2) % (kPolyEvery > 0 ? kPolyEvery : 1) == kPolyEvery - 1;
-        float p0 = poly ? exp2_poly(x.x) : ex2(x.x);
-        float p1 = poly ? exp2_poly(x.y) : ex2(x.y);
+        float p0 = ex2(x.x);
+        float p1 = ex2(x.y);
         if (need_mask) {
           if (c < lim) p0 = 0.f;
           if (c + 1 < lim) p1 = 0.f;
