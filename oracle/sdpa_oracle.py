@@ -46,11 +46,12 @@ module's own table and multiplied by their descale):
 * dropout (the SDPA node's dropout option in the cuDNN 9 blog's walkthrough, named and not
   defined): after the softmax each probability is kept with a keep mask Z and the kept ones
   are scaled by 1/(1 - p), so O = (P * Z) V / (1 - p); the LSE is that of the undropped
-  softmax.  The mask is drawn by the counter-based Philox4x64-10 generator (Salmon, Moraes,
+  softmax.  The mask is drawn by the counter-based Philox4x32-10 generator (Salmon, Moraes,
   Dror and Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11): element n of the
-  row-major grid [b*h_q][s_q][s_kv rounded up to 128] takes 16-bit lane n % 4 of word
-  (n % 16) // 4 of the block drawn for counter (n // 16, offset, 0, 0) and key (seed, 0),
-  and is kept iff that value is >= round(p * 65536);
+  row-major grid [b*h_q][s_q][s_kv rounded up to 128] takes 16-bit half n % 2 (0 = low) of
+  32-bit word (n % 8) // 2 of the block drawn for the 128-bit counter (n // 8, offset) and the
+  64-bit key seed (each split into 32-bit words, low word first), and is kept iff that value
+  is >= round(p * 65536);
 * head grouping: query head ``hq`` reads KV head ``hq // (h_q // h_kv)`` (contiguous
   groups; the codelab's §9 "Comparing MHA, GQA and MQA" broadcasts each KV head to
   its group of query heads);
@@ -72,7 +73,7 @@ from typing import Iterable, Sequence, Tuple
 import numpy as np
 
 __all__ = [
-    "philox4x64", "dropout_threshold", "dropout_keep", "bias_gradient",
+    "philox4x32", "dropout_threshold", "dropout_keep", "bias_gradient",
     "visible_mask", "kv_head_of", "alibi_default_slopes", "alibi_bias", "head_forward", "forward", "forward_rows",
     "backward", "backward_dq_rows", "backward_ds_rows", "backward_kv_rows", "backward_kv_head",
     "e4m3_decode_table",
@@ -161,30 +162,30 @@ def to_f64(t, descale: float = 1.0) -> np.ndarray:
 # Forward
 # ---------------------------------------------------------------------------
 
-# Philox4x64-10 constants: the round multipliers and the Weyl key increments of the paper.
-PHILOX_M0 = 0xD2E7470EE14C6C93
-PHILOX_M1 = 0xCA5A826395121157
-PHILOX_W0 = 0x9E3779B97F4A7C15
-PHILOX_W1 = 0xBB67AE8584CAA73B
-_MASK64 = (1 << 64) - 1
+# Philox4x32-10 constants: the round multipliers and the Weyl key increments of the paper.
+PHILOX_M0 = 0xD2511F53
+PHILOX_M1 = 0xCD9E8D57
+PHILOX_W0 = 0x9E3779B9
+PHILOX_W1 = 0xBB67AE85
+_MASK32 = (1 << 32) - 1
 
 
-def philox4x64(counter: Sequence[int], key: Sequence[int], rounds: int = 10) -> Tuple[int, ...]:
-    """One Philox4x64 block: four 64-bit words for a 256-bit counter and a 128-bit key.
+def philox4x32(counter: Sequence[int], key: Sequence[int], rounds: int = 10) -> Tuple[int, ...]:
+    """One Philox4x32 block: four 32-bit words for a 128-bit counter and a 64-bit key.
 
-    Each round multiplies words 0 and 2 by the two constants (full 128-bit products), and
+    Each round multiplies words 0 and 2 by the two constants (full 64-bit products), and
     the new words are (hi1 ^ x1 ^ k0, lo1, hi0 ^ x3 ^ k1, lo0); the key gains the Weyl
     increments between rounds.  Plain Python integers, one block at a time."""
-    x0, x1, x2, x3 = (int(c) & _MASK64 for c in counter)
-    k0, k1 = (int(k) & _MASK64 for k in key)
+    x0, x1, x2, x3 = (int(c) & _MASK32 for c in counter)
+    k0, k1 = (int(k) & _MASK32 for k in key)
     for r in range(rounds):
         if r > 0:
-            k0 = (k0 + PHILOX_W0) & _MASK64
-            k1 = (k1 + PHILOX_W1) & _MASK64
+            k0 = (k0 + PHILOX_W0) & _MASK32
+            k1 = (k1 + PHILOX_W1) & _MASK32
         p0 = PHILOX_M0 * x0
         p1 = PHILOX_M1 * x2
-        hi0, lo0 = p0 >> 64, p0 & _MASK64
-        hi1, lo1 = p1 >> 64, p1 & _MASK64
+        hi0, lo0 = p0 >> 32, p0 & _MASK32
+        hi1, lo1 = p1 >> 32, p1 & _MASK32
         x0, x1, x2, x3 = hi1 ^ x1 ^ k0, lo1, hi0 ^ x3 ^ k1, lo0
     return x0, x1, x2, x3
 
@@ -206,14 +207,17 @@ def dropout_keep(b: int, h_q: int, s_q: int, s_kv: int, p: float, seed: int, off
     row_pitch = (s_kv + 127) // 128 * 128
     want = list(rows) if rows is not None else [(bh, i) for bh in range(b * h_q) for i in range(s_q)]
     out = np.empty((len(want), s_kv), dtype=bool)
+    key = (seed & _MASK32, (seed >> 32) & _MASK32)
+    off = (offset & _MASK32, (offset >> 32) & _MASK32)
     for r, (bh, i) in enumerate(want):
-        n0 = (bh * s_q + i) * row_pitch           # multiple of 16: rows start a new block
-        for g in range(row_pitch // 16):
-            words = philox4x64((n0 // 16 + g, offset, 0, 0), (seed, 0))
-            for e in range(16):
-                j = g * 16 + e
+        n0 = (bh * s_q + i) * row_pitch           # multiple of 8: rows start a new block
+        for g in range(row_pitch // 8):
+            blk = n0 // 8 + g
+            words = philox4x32((blk & _MASK32, blk >> 32, off[0], off[1]), key)
+            for e in range(8):
+                j = g * 8 + e
                 if j < s_kv:
-                    u = (words[e // 4] >> (16 * (e % 4))) & 0xFFFF
+                    u = (words[e // 2] >> (16 * (e % 2))) & 0xFFFF
                     out[r, j] = u >= t
     if rows is None:
         return out.reshape(b, h_q, s_q, s_kv)

@@ -9,6 +9,8 @@ missing Delta term) fails at least one of them.
 import json
 import math
 import os
+import subprocess
+import sys
 
 import numpy as np
 import pytest
@@ -563,26 +565,71 @@ def test_alibi_default_slopes_match_the_alibi_paper():
 
 
 # ---------------------------------------------------------------------------
-# Dropout: Philox4x64-10 and the keep mask
+# Dropout: Philox4x32-10 and the keep mask
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("counter,key", [
-    ([5, 0, 0, 0], [7, 9]),
-    ([2 ** 64 - 1, 5, 0, 0], [2 ** 63 + 11, 2 ** 64 - 3]),      # carry into word 1
-    ([123456789, 2 ** 64 - 1, 2 ** 64 - 1, 3], [0, 0]),
-])
-def test_philox_matches_numpy_bit_generator(counter, key):
-    """numpy's Philox is Philox4x64-10 from the same paper; it increments its 256-bit counter
-    before drawing each block, so its n-th block is ours at counter + n."""
-    bg = np.random.Philox(counter=np.array(counter, dtype=np.uint64), key=np.array(key, dtype=np.uint64))
-    assert [int(w) for w in bg.state["state"]["counter"]] == counter
-    got = bg.random_raw(12)
-    c = sum(int(w) << (64 * i) for i, w in enumerate(counter))
-    want = []
-    for n in range(1, 4):
-        cn = (c + n) % (1 << 256)
-        want += oracle.philox4x64([(cn >> (64 * i)) & ((1 << 64) - 1) for i in range(4)], key)
-    assert [int(x) for x in got] == want
+def test_philox4x32_known_answers():
+    """The generator's published known-answer vectors (tests/golden/philox4x32_10_kat.json)."""
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.json")) as f:
+        kat = json.load(f)
+    for v in kat["vectors"]:
+        c = [int(x, 16) for x in v["counter"]]
+        k = [int(x, 16) for x in v["key"]]
+        assert list(oracle.philox4x32(c, k)) == [int(x, 16) for x in v["out"]]
+
+
+_TRITON_PHILOX = r"""
+import os, sys, json
+os.environ["TRITON_INTERPRET"] = "1"
+import torch, triton, triton.language as tl
+from triton.language.random import philox_impl
+
+@triton.jit
+def kern(c_ptr, k_ptr, o_ptr, N: tl.constexpr):
+    i = tl.arange(0, N)
+    r = philox_impl(tl.load(c_ptr + 4 * i), tl.load(c_ptr + 4 * i + 1), tl.load(c_ptr + 4 * i + 2),
+                    tl.load(c_ptr + 4 * i + 3), tl.load(k_ptr + 2 * i), tl.load(k_ptr + 2 * i + 1), 10)
+    for w in tl.static_range(4):
+        tl.store(o_ptr + 4 * i + w, r[w])
+
+cs, ks = json.loads(sys.argv[1])
+n = len(ks)
+c = torch.tensor(sum(cs, []), dtype=torch.int64).to(torch.uint32)
+k = torch.tensor(sum(ks, []), dtype=torch.int64).to(torch.uint32)
+o = torch.zeros(4 * n, dtype=torch.uint32)
+kern[(1,)](c, k, o, N=n)
+print(json.dumps([int(x) & 0xffffffff for x in o.to(torch.int64)]))
+"""
+
+
+def test_philox4x32_matches_triton_interpreter():
+    """Triton's own Philox4x32 (its language library, run by its CPU interpreter in a child
+    process) on seeded counters and keys, including all-ones words."""
+    pytest.importorskip("triton")
+    rng = np.random.default_rng(11)
+    cs = [[int(x) for x in rng.integers(0, 2 ** 32, size=4)] for _ in range(14)] + [[2 ** 32 - 1] * 4, [0, 1, 2, 3]]
+    ks = [[int(x) for x in rng.integers(0, 2 ** 32, size=2)] for _ in range(14)] + [[2 ** 32 - 1, 0], [5, 2 ** 31]]
+    r = subprocess.run([sys.executable, "-c", _TRITON_PHILOX, json.dumps([cs, ks])], capture_output=True, text=True,
+                       timeout=600)
+    if r.returncode != 0:
+        pytest.skip("Triton's interpreter is unavailable here: " + r.stderr[-300:])
+    got = json.loads(r.stdout.strip().splitlines()[-1])
+    for n, (c, k) in enumerate(zip(cs, ks)):
+        assert list(oracle.philox4x32(c, k)) == got[4 * n:4 * n + 4]
+
+
+def test_keep_mask_layout_of_one_block():
+    """Element n of a row takes the 16-bit half n % 2 of word (n % 8) // 2 of block n // 8:
+    the 8 elements of one block, drawn through dropout_keep, against the block's words."""
+    seed, offset = 0x1234_5678_9ABC_DEF0, 0x0000_0003_0000_0007
+    b, h, s_q, s_kv = 1, 1, 2, 128
+    keep_lo = oracle.dropout_keep(b, h, s_q, s_kv, 0.5, seed, offset)[0, 0]
+    for i in range(s_q):
+        for g in (0, 5, 15):
+            blk = (i * 128) // 8 + g
+            words = oracle.philox4x32((blk, 0, offset & 0xFFFFFFFF, offset >> 32), (seed & 0xFFFFFFFF, seed >> 32))
+            halves = [(words[e // 2] >> (16 * (e % 2))) & 0xFFFF for e in range(8)]
+            assert [bool(x >= 32768) for x in halves] == list(keep_lo[i, 8 * g:8 * g + 8])
 
 
 def test_dropout_threshold():
