@@ -291,7 +291,7 @@ def sdpa_dropout_mask_size(b: int, h_q: int, s_q: int, s_kv: int):
 
 def sdpa_dropout_mask(b: int, h_q: int, s_q: int, s_kv: int, dropout_p: float, seed: int,
                       offset: int, mask=None, mask_t=None, stream=None, causal=False) -> None:
-    """Draws the Philox4x64-10 keep bits into ``mask`` (row-major, for sdpa_fwd) and/or
+    """Draws the Philox4x32-10 keep bits into ``mask`` (row-major, for sdpa_fwd) and/or
     ``mask_t`` (transposed, for sdpa_bwd): CUDA tensors of sdpa_dropout_mask_size bytes.
     With ``causal`` (no per-batch lengths) tiles above the diagonal are left unwritten."""
     p = _mask_problem(b, h_q, s_q, s_kv, dropout_p, causal)

@@ -1,12 +1,13 @@
-// sdpa_dropout.cu — the dropout keep mask, drawn with Philox4x64-10.
+// sdpa_dropout.cu — the dropout keep mask, drawn with Philox4x32-10.
 //
 // The SDPA node of the cuDNN 9 blog's walkthrough has a dropout option that the pages do not
 // define.  Here dropout keeps each softmax probability P_ij with a mask bit and scales kept
-// ones by 1/(1 - p).  The bits come from the counter-based generator Philox4x64-10 (Salmon,
+// ones by 1/(1 - p).  The bits come from the counter-based generator Philox4x32-10 (Salmon,
 // Moraes, Dror and Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11): element n of
-// the row-major grid [b*h_q][s_q][s_kv rounded up to 128] takes 16-bit lane n % 4 of word
-// (n % 16) / 4 of the block for counter (n / 16, offset, 0, 0) and key (seed, 0); it is kept
-// iff that 16-bit value is >= the threshold round(p * 65536).
+// the row-major grid [b*h_q][s_q][s_kv rounded up to 128] takes the 16-bit half n % 2 (0 =
+// low) of word (n % 8) / 2 of the block for the 128-bit counter (n / 8, offset) and the 64-bit
+// key seed (each as 32-bit words, low word first); it is kept iff that 16-bit value is >= the
+// threshold round(p * 65536).  Each round needs two 32 x 32 -> 64-bit products.
 //
 // One kernel writes the bits twice: row-major for the forward pass (a thread owns a query
 // row) and transposed for the backward pass (a thread owns a key row), so neither attention
@@ -20,47 +21,52 @@
 namespace sdpa {
 namespace {
 
-constexpr uint64_t kPhiloxM0 = 0xD2E7470EE14C6C93ull;   // round multipliers
-constexpr uint64_t kPhiloxM1 = 0xCA5A826395121157ull;
-constexpr uint64_t kPhiloxW0 = 0x9E3779B97F4A7C15ull;   // Weyl key increments
-constexpr uint64_t kPhiloxW1 = 0xBB67AE8584CAA73Bull;
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u;   // round multipliers
+constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;   // Weyl key increments
+constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
 
-struct U64x4 {
-  uint64_t x[4];
+// The ten round keys of a 64-bit key (the same for every block of a draw).
+struct RoundKeys {
+  uint32_t k0[10], k1[10];
 };
 
-__device__ __forceinline__ U64x4 philox4x64_10(uint64_t c0, uint64_t c1, uint64_t k0, uint64_t k1) {
-  uint64_t x0 = c0, x1 = c1, x2 = 0, x3 = 0;
+__device__ __forceinline__ RoundKeys round_keys(uint64_t seed) {
+  RoundKeys rk;
+  uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
 #pragma unroll
   for (int r = 0; r < 10; ++r) {
-    if (r > 0) {
-      k0 += kPhiloxW0;
-      k1 += kPhiloxW1;
-    }
-    const uint64_t hi0 = __umul64hi(kPhiloxM0, x0), lo0 = kPhiloxM0 * x0;
-    const uint64_t hi1 = __umul64hi(kPhiloxM1, x2), lo1 = kPhiloxM1 * x2;
-    x0 = hi1 ^ x1 ^ k0;
-    x1 = lo1;
-    x2 = hi0 ^ x3 ^ k1;
-    x3 = lo0;
+    rk.k0[r] = k0;
+    rk.k1[r] = k1;
+    k0 += kPhiloxW0;
+    k1 += kPhiloxW1;
   }
-  return U64x4{{x0, x1, x2, x3}};
+  return rk;
 }
 
-// 16 keep bits (bit e = element 16g + e) of counter block g.
-__device__ __forceinline__ uint32_t keep16(uint64_t g, const DropoutParams& p) {
-  const U64x4 w = philox4x64_10(g, p.offset, p.seed, 0);
+// 8 keep bits (bit e = element 8g + e) of counter block g: keep iff the 16-bit draw u is at
+// least the threshold T, i.e. iff u + (65536 - T) reaches bit 16.
+__device__ __forceinline__ uint32_t keep8(uint64_t g, uint32_t off_lo, uint32_t off_hi, const RoundKeys& rk,
+                                          uint32_t c) {
+  uint32_t x0 = static_cast<uint32_t>(g), x1 = static_cast<uint32_t>(g >> 32), x2 = off_lo, x3 = off_hi;
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint64_t p0 = static_cast<uint64_t>(kPhiloxM0) * x0;
+    const uint64_t p1 = static_cast<uint64_t>(kPhiloxM1) * x2;
+    x0 = static_cast<uint32_t>(p1 >> 32) ^ x1 ^ rk.k0[r];
+    x1 = static_cast<uint32_t>(p1);
+    x2 = static_cast<uint32_t>(p0 >> 32) ^ x3 ^ rk.k1[r];
+    x3 = static_cast<uint32_t>(p0);
+  }
+  const uint32_t w[4] = {x0, x1, x2, x3};
   uint32_t bits = 0;
 #pragma unroll
-  for (int e = 0; e < 16; ++e) {
-    const uint32_t u = static_cast<uint32_t>(w.x[e / 4] >> (16 * (e % 4))) & 0xFFFFu;
-    bits |= (u >= p.threshold ? 1u : 0u) << e;
-  }
+  for (int e = 0; e < 8; ++e) bits |= (((w[e / 2] >> (16 * (e % 2))) & 0xFFFFu) + c) >> 16 << e;
   return bits;
 }
 
 // One CTA of 128 threads per (b*h_q, 128-row query block, 128-key block).  Lane L of warp w
-// draws row 32w + L: 8 Philox blocks give its 128 bits, stored as four row-major words.  The
+// draws row 32w + L: 16 Philox blocks give its 128 bits, stored as four row-major words.  The
 // transposed words come from 32 ballots per 32x32 bit block and a 2 KB exchange.
 __global__ void __launch_bounds__(128) dropout_mask_kernel(const DropoutParams p) {
   __shared__ uint32_t tile[128][4];   // [key within block][query word]
@@ -73,9 +79,14 @@ __global__ void __launch_bounds__(128) dropout_mask_kernel(const DropoutParams p
   uint32_t w[4] = {0u, 0u, 0u, 0u};
   if (row < p.s_q) {
     const uint64_t g0 = static_cast<uint64_t>((static_cast<int64_t>(bh) * p.s_q + row) * row_pitch +
-                                              kb * 128) / 16;
+                                              kb * 128) / 8;
+    const RoundKeys rk = round_keys(p.seed);
+    const uint32_t off_lo = static_cast<uint32_t>(p.offset), off_hi = static_cast<uint32_t>(p.offset >> 32);
+    const uint32_t c = 65536u - p.threshold;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) w[i] = keep16(g0 + 2 * i, p) | (keep16(g0 + 2 * i + 1, p) << 16);
+    for (int i = 0; i < 4; ++i)
+      w[i] = keep8(g0 + 4 * i, off_lo, off_hi, rk, c) | (keep8(g0 + 4 * i + 1, off_lo, off_hi, rk, c) << 8) |
+             (keep8(g0 + 4 * i + 2, off_lo, off_hi, rk, c) << 16) | (keep8(g0 + 4 * i + 3, off_lo, off_hi, rk, c) << 24);
     if (p.rows != nullptr) {
       uint4* dst = reinterpret_cast<uint4*>(p.rows + (static_cast<int64_t>(bh) * p.s_q + row) * p.kv_words +
                                             kb * 4);

@@ -236,11 +236,12 @@ SDPA_API sdpa_status_t sdpa_dropout_mask_size(const sdpa_problem_t* p, size_t* b
 
 /*
  * Draws the dropout keep bits for p->dropout_p (in [0, 1)) with the counter-based generator
- * Philox4x64-10 (Salmon, Moraes, Dror and Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
- * SC'11).  Element n of the row-major grid [b*h_q][s_q][ceil(s_kv/128)*128] takes 16-bit lane
- * n%4 of word (n%16)/4 of the block for counter (n/16, offset, 0, 0) and key (seed, 0), and
- * is kept iff that value is >= round(dropout_p * 65536).  The same (seed, offset) gives the
- * same bits on every run and device; advance `offset` between steps for fresh draws.
+ * Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
+ * SC'11).  Element n of the row-major grid [b*h_q][s_q][ceil(s_kv/128)*128] takes the 16-bit
+ * half n%2 (0 = low) of 32-bit word (n%8)/2 of the block for the 128-bit counter (n/8, offset)
+ * and the 64-bit key seed (each as 32-bit words, low word first), and is kept iff that value
+ * is >= round(dropout_p * 65536).  The same (seed, offset) gives the same bits on every run
+ * and device; advance `offset` between steps for fresh draws.
  *   mask, mask_t: DEVICE arrays of sdpa_dropout_mask_size bytes, 16-byte aligned; either may
  *   be NULL (not written).  Bits of padded positions (keys >= s_kv in `mask`, rows >= s_q in
  *   `mask_t`) are written too and are not used.  When p->causal is 1 or 2 and no seq_lens

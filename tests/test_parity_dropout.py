@@ -1,4 +1,4 @@
-"""GPU parity of dropout: the Philox4x64-10 keep bits bit for bit, then forward and backward
+"""GPU parity of dropout: the Philox4x32-10 keep bits bit for bit, then forward and backward
 against the fp64 oracle driven by the oracle's own keep mask.
 
 The mask kernel must reproduce the oracle's draw exactly (row-major and transposed, ragged
