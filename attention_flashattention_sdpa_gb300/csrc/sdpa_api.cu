@@ -377,6 +377,16 @@ sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const void* k, co
   }
   const int rows_per_cta = 128 * (prm.one_tile ? 1 : sdpa::fwd_q_tiles(p->d, p->in_dtype));
   prm.num_m_blocks = (p->s_q + rows_per_cta - 1) / rows_per_cta;
+  const long long units = static_cast<long long>(p->b) * p->h_q * prm.num_m_blocks;
+  prm.ctas = sdpa::fwd_persistent_ctas(units, p->d, p->in_dtype, plain, num_sms());
+  // SDPA_FWD_PERSIST=N overrides the choice where both schedules exist (plain 16-bit,
+  // d <= 128): 0 = one CTA per work unit, N >= 1 = min(N, units) CTAs walking the units (a
+  // switch for testing and tuning).
+  if (const char* ps = std::getenv("SDPA_FWD_PERSIST")) {
+    const long long n = atoll(ps);
+    if (plain && p->in_dtype != SDPA_DTYPE_E4M3 && p->d <= 128 && n >= 0)
+      prm.ctas = static_cast<int>(n < units ? n : units);
+  }
   prm.scale_log2 = scale_log2_of(p->attn_scale);
   prm.negate_scores = p->attn_scale < 0.f ? 1 : 0;
   if ((int64_t)p->b * p->h_q * prm.num_m_blocks > 0x7fffffff)

@@ -29,6 +29,8 @@ struct FwdParams {
   int causal;
   int num_m_blocks;           // ceil(s_q / (128 * q tiles per CTA))
   int one_tile;               // small problem: one Q tile per CTA even where two fit
+  int ctas;                   // 0: one CTA per work unit; else this many persistent CTAs, each
+                              // walking several units (plain 16-bit inputs, d <= 128)
   const int32_t* seq_lens_q;  // per-batch valid rows, or nullptr
   const int32_t* seq_lens_kv;
   int bottom_right;           // causal alignment: key j visible iff j <= i + len_kv - len_q
@@ -51,6 +53,11 @@ int fwd_q_tiles(int d, int in_dtype);
 // two-tile CTAs would not fill one wave of the GPU, twice as many CTAs of half the work
 // finish sooner (measured: 64 CTAs +33%, 128 CTAs +5%; at 192 and 256 two tiles win).
 bool fwd_prefer_one_tile(int b, int h_q, int s_q, int d, int in_dtype, bool plain, int num_sms);
+
+// Persistent CTAs for a forward pass of `units` work units: the SM count when the units fill
+// between one and four waves of the GPU (a launch with one CTA per unit would leave the last
+// wave ragged and pay every CTA's set-up), else 0 (one CTA per unit).
+int fwd_persistent_ctas(long long units, int d, int in_dtype, bool plain, int num_sms);
 
 cudaError_t launch_fwd(const FwdParams& p, int d, int in_dtype, int out_dtype, cudaStream_t st);
 uint32_t fwd_take_device_error();
@@ -171,7 +178,8 @@ constexpr int kFeatAlibi = 1;
 constexpr int kFeatDropout = 2;
 constexpr int kFeatBias = 4;
 constexpr int kFeatDBias = 8;   // only with kFeatBias
-constexpr int kFeatOneTile = 16;  // forward: one Q tile per CTA at d <= 128
+constexpr int kFeatOneTile = 16;  // forward: one Q tile per work unit at d <= 128
+constexpr int kFeatPersist = 32;  // forward: persistent CTAs, each walking several work units
 
 }  // namespace sdpa
 
