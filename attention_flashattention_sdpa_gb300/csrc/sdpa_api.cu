@@ -393,9 +393,11 @@ sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const void* k, co
     return fail(SDPA_ERR_UNSUPPORTED, "grid too large");
   cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
   if (log_level() >= 1)
-    fprintf(stderr, "[sdpa] fwd b=%d h_q=%d h_kv=%d s_q=%d s_kv=%d d=%d dt=%d causal=%d grid=(%d,%d)\n",
-            p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d, p->in_dtype, p->causal, p->b * p->h_q,
-            prm.num_m_blocks);
+    fprintf(stderr, "[sdpa] fwd b=%d h_q=%d h_kv=%d s_q=%d s_kv=%d d=%d dt=%d causal=%d units=%lld "
+            "(%d query tile(s) each) ctas=%lld%s\n",
+            p->b, p->h_q, p->h_kv, p->s_q, p->s_kv, p->d, p->in_dtype, p->causal, units,
+            prm.one_tile ? 1 : sdpa::fwd_q_tiles(p->d, p->in_dtype), prm.ctas ? (long long)prm.ctas : units,
+            prm.ctas ? " persistent" : "");
   cudaError_t e = sdpa::launch_fwd(prm, p->d, p->in_dtype, p->out_dtype, stream);
   return finish_launch(e, stream, "sdpa_fwd");
 }

@@ -55,7 +55,11 @@ struct FwdCfg {
   // (unless those are smaller: E4M3 inputs) and one Q tile in the K/V ring.
   static constexpr bool OWN_STAGE = PERSIST || (NQT == 2 && TILE_BYTES < OUT_TILE);
   static constexpr int STAGE_BYTES = OWN_STAGE ? NQT * OUT_TILE : 0;
-  static constexpr int RING_BUDGET = (PERSIST ? 229376 : 196608) - Q_BYTES - STAGE_BYTES;
+  // Shared memory: the per-SM limit (227 KB) less the static arrays (the barriers, and with
+  // one Q tile the column halves' exchange arrays) and the 1 KB alignment slack.
+  static constexpr int STATIC_BYTES = NQT == 2 ? 512 : 3584;
+  static constexpr int RING_BUDGET =
+      (PERSIST ? 232448 - STATIC_BYTES - 1024 : 196608) - Q_BYTES - STAGE_BYTES;
   static constexpr int NS = (RING_BUDGET / TILE_BYTES) > 8 ? 8 : (RING_BUDGET / TILE_BYTES);
   static constexpr int RING_BYTES = NS * TILE_BYTES;
   static constexpr int OUT_TILE_BYTES = kBlockM * D * 2;          // 16-bit output tile
@@ -73,6 +77,7 @@ struct FwdCfg {
   static constexpr float THRESH = (DT == kE4M3) ? 0.8f : 8.0f;    // lazy-rescale threshold
   static constexpr float P_OFFSET = (DT == kE4M3) ? 8.0f : 0.0f;  // P scaled by 2^8 for E4M3
   static_assert(NS >= 2, "K/V ring needs at least two slots");
+  static_assert(SMEM_BYTES + STATIC_BYTES <= 232448, "shared memory budget");
   static_assert(O_COL0 + NQT * D <= 512, "TMEM budget");
   static_assert(OWN_STAGE || NQT == 2 || OUT_TILE_BYTES <= RING_BYTES, "epilogue staging");
 };
@@ -149,8 +154,9 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
   __shared__ FwdBarriers bars;
   // Column halves (one Q tile): per-row exchange of the row-max candidate (by block parity)
   // and, at the end of a unit, of the row sums.
-  __shared__ float xch[NQT == 1 ? 2 : 1][2][kBlockM];
-  __shared__ float xl[2][kBlockM];
+  __shared__ float xch[NQT == 1 ? 2 : 1][2][NQT == 1 ? kBlockM : 1];
+  __shared__ float xl[2][NQT == 1 ? kBlockM : 1];
+  static_assert(sizeof(FwdBarriers) + sizeof(xch) + sizeof(xl) <= C::STATIC_BYTES, "static shared memory");
 
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
