@@ -377,16 +377,16 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       mbar_init(&bars.s_full[b], 1);
       mbar_init(&bars.dp_full[b], 1);
       mbar_init(&bars.dq_full[b], 1);
-      mbar_init(&bars.p_full[b], 256);    // the Pᵀ role (Pᵀ written), the dSᵀ role (dO slot seen)
-      mbar_init(&bars.ds_full[b], 128);
+      mbar_init(&bars.p_full[b], 256);
+      mbar_init(&bars.ds_full[b], 256);
       mbar_init(&bars.dq_free[b], 128);
     }
     mbar_init(&bars.acc_full, 1);
     mbar_init(&bars.drain, 1);
     mbar_init(&bars.epi_ready[0], 128);
     mbar_init(&bars.epi_ready[1], 128);
-    mbar_init(&bars.dp_consumed[0], 128);
-    mbar_init(&bars.dp_consumed[1], 128);
+    mbar_init(&bars.dp_consumed[0], 256);
+    mbar_init(&bars.dp_consumed[1], 256);
     mbar_init(&bars.dsbuf_free[0], 1);
     mbar_init(&bars.dsbuf_free[1], 1);
     for (int i = 0; i < 2; ++i) {
@@ -415,8 +415,8 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   bool producer = false;
   int nq = 0, nd = 0;   // Q and dO tiles issued
 
-  // Register budget per thread: 64 for the producer / MMA warpgroup, 128 for the Pᵀ role, 176
-  // for the dSᵀ role, 144 for the dQ drain (64 + 128 + 176 + 144 = 4 x 128, the launch's budget).
+  // Register budget per thread: 64 for the producer / MMA warpgroup, 152 for each compute
+  // warpgroup, 144 for the dQ drain (64 + 2 x 152 + 144 = 4 x 128, the launch's budget).
   if (warp < 4) {
   regs_dec<64>();
   if (warp == 0) {
@@ -539,163 +539,158 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     }
   }
   } else if (warp < 12) {
-    // ======================= Pᵀ role and dSᵀ role (one warpgroup each) =================
-    // Both own one key row per thread (TMEM lane) over all 128 query columns of a step.  The
-    // Pᵀ role turns Sᵀ into Pᵀ (the dV MMA's operand, and the dSᵀ role's input); the dSᵀ role
-    // turns dPᵀ and Pᵀ into dSᵀ.  They work on different steps at once: while the dSᵀ role
-    // finishes step n, the Pᵀ role already computes step n + 1.
-    const int h = (warp - 4) / 4;                         // 0: Pᵀ role (then dV), 1: dSᵀ role (then dK)
-    if (h == 0) regs_inc<128>(); else regs_inc<176>();
+    regs_inc<152>();
+    // ============================ Pᵀ / dSᵀ (two column halves) ========================
+    const int h = (warp - 4) / 4;                         // query columns [64h, 64h+64)
     const int quad = warp % 4;
     const int r = quad * 32 + lane;                       // key row within the block (TMEM lane)
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
     const int kv_row = j * kBlockN + r;
     const BwdScales bs = bwd_scales(p);
-    // Dropout: keep bits of this key row for step n's 128 query columns (transposed mask), one
-    // step ahead: a step outlasts the latency of the (uncoalesced) load.
+    // Dropout: keep bits of this key row for step n's 64 query columns (transposed mask).
+    // They are loaded one step ahead: a step outlasts the latency of the (uncoalesced) load.
     auto load_keep = [&](int n) {
-      if (!DROP || kv_row >= p.s_kv || n >= n_iter) return make_uint4(0u, 0u, 0u, 0u);
-      return __ldg(reinterpret_cast<const uint4*>(
+      if (!DROP || kv_row >= p.s_kv || n >= n_iter) return make_uint2(0u, 0u);
+      return __ldg(reinterpret_cast<const uint2*>(
           p.drop_cols + ((static_cast<int64_t>(bi) * p.h_q + iter_head(n)) * p.s_kv + kv_row) * p.drop_q_words +
-          iter_qblk(n) * (kBlockM / 32)));
+          (iter_qblk(n) * kBlockM + 64 * h) / 32));
     };
-    uint4 keep_next = load_keep(0);
-    if (h == 0 && BIAS && n_iter > 0) prefetch_bias_t(p, bi, iter_head(0), kv_row, iter_qblk(0) * kBlockM);
+    uint2 keep_next = load_keep(0);
+    if (BIAS && n_iter > 0) prefetch_bias_t(p, bi, iter_head(0), kv_row, iter_qblk(0) * kBlockM + 64 * h);
     bool ok = true;
     for (int n = 0; n < n_iter; ++n) {
       const int b = n & 1;
       const uint32_t par = (n >> 1) & 1;
       const uint32_t X = tmem + lane_off + C::R_COL + b * 128;
       const uint32_t Y = tmem + lane_off + C::R_COL + (b ^ 1) * 128;
-      const int q0 = iter_qblk(n) * kBlockM;              // first query column of the step
-      const uint4 keep = keep_next;
+      const int q0 = iter_qblk(n) * kBlockM + 64 * h;     // first query column of this half
+      const uint2 keep = keep_next;
       if constexpr (DROP) keep_next = load_keep(n + 1);
+      // Additive bias of this key row for the 64 query columns (transposed copy); the next
+      // step's row is sent to L2 first.
+      uint4 bz[BIAS ? 8 : 1];
+      if constexpr (BIAS) {
+        if (n + 1 < n_iter)
+          prefetch_bias_t(p, bi, iter_head(n + 1), kv_row, iter_qblk(n + 1) * kBlockM + 64 * h);
+        load_bias_t(p, bi, iter_head(n), kv_row, q0, bz);
+      }
+      // Bias gradient: this key row's 64 query columns of the transposed accumulator.
+      float* dbrow = DBIAS ? dbias_row(p, bi, iter_head(n), kv_row, q0) : nullptr;
+      const float* nlse2 = sVec + (b * 2 + 0) * 128 + 64 * h;    // -LSE·log2 e per column
+      const float* ndelta = sVec + (b * 2 + 1) * 128 + 64 * h;   // -Delta per column
+      // Pᵀ = exp2(Sᵀ·scale·log2e − LSE·log2e), masked where key > query
+      // This step's -LSE and -Delta vectors arrive with its Q and dO tiles.  Both waits come
+      // before Pᵀ is released: dO's slot is refilled once dV of this step has read it, and
+      // dV needs Pᵀ, so the refill cannot overtake these waits.
+      if (!mbar_wait_warp(&bars.ring_full[n & 1], (n >> 1) & 1, wt)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars.ring_full[2 + n % C::NDO], (n / C::NDO) & 1, wt)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars.s_full[b], par, wt)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sv[64];
+      tmem_ld32(X + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld32(X + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_ld_wait();
       // Query column c is visible to key row kv_row iff c >= lim (causal: kv <= q + off);
       // keys beyond len_kv see nothing.  Padded query columns already have P = 0.
       const bool need_mask = (p.causal && (q0 + L.off < j * kBlockN + kBlockN - 1)) ||
                              (j * kBlockN + kBlockN > L.len_kv);
       int lim = p.causal ? kv_row - q0 - L.off : -(1 << 30);
       if (kv_row >= L.len_kv) lim = 1 << 30;
-      if (h == 0) {
-        // ---- Pᵀ = exp2(Sᵀ·scale·log2e − LSE·log2e), masked where key > query ----
-        // The step's -LSE vector arrives with its Q tile.  This role's wait comes before it
-        // releases Pᵀ; the Q slot is refilled only after the step's dK MMA, which needs dSᵀ,
-        // which needs Pᵀ: the refill cannot overtake the wait.
-        if (!mbar_wait_warp(&bars.ring_full[n & 1], (n >> 1) & 1, wt)) { ok = false; break; }
-        if (BIAS && n + 1 < n_iter) prefetch_bias_t(p, bi, iter_head(n + 1), kv_row, iter_qblk(n + 1) * kBlockM);
-        if (!mbar_wait_warp(&bars.s_full[b], par, wt)) { ok = false; break; }
-        tc_fence_after();
-        const float* nlse2 = sVec + (b * 2 + 0) * 128;    // -LSE·log2 e per column
-        const float2 sc2 = make_float2(bs.s_log2, bs.s_log2);
-        // ALiBi: the key-row part of the bias (the column part is in the -LSE vector).
-        const float kr = ALIBI ? alibi_slope_log2(p, iter_head(n)) *
-                                     static_cast<float>(kv_row - q0 - L.off) : 0.f;
-        const float2 kr2 = make_float2(kr, kr);
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t sv[64];
-          tmem_ld32(X + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-          tmem_ld32(X + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-          uint4 bz[BIAS ? 8 : 1];
-          if constexpr (BIAS) load_bias_t(p, bi, iter_head(n), kv_row, q0 + 64 * hh, bz);
-          tmem_ld_wait();
-          uint32_t pk[32], pm[DROP ? 32 : 1];
-          const int lh = lim - 64 * hh;
+      uint32_t pk[32], pm[DROP ? 32 : 1];
+      const float2 sc2 = make_float2(bs.s_log2, bs.s_log2);
+      // ALiBi: the key-row part of the bias (the column part is in the -LSE vector).
+      const float kr = ALIBI ? alibi_slope_log2(p, iter_head(n)) *
+                                   static_cast<float>(kv_row - iter_qblk(n) * kBlockM - L.off) : 0.f;
+      const float2 kr2 = make_float2(kr, kr);
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            float2 nl = *reinterpret_cast<const float2*>(nlse2 + 64 * hh + c);
-            if constexpr (ALIBI) nl = add2(nl, kr2);
-            if constexpr (BIAS) nl = fma2(bias_pair<DT>(bz, c), make_float2(kLog2e, kLog2e), nl);
-            const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl);
-            float p0 = ex2(x.x);
-            float p1 = ex2(x.y);
-            if (need_mask) {
-              if (c < lh) p0 = 0.f;
-              if (c + 1 < lh) p1 = 0.f;
-            }
-            pk[c / 2] = pack2(p0, p1, DT);
-            if constexpr (DROP) {
-              // dV takes the kept P only; dS takes every P.  A zero of either 16-bit type is all
-              // zero bits, so the kept pair is the packed pair with dropped halves cleared.  The
-              // pair's keep bits sit at bits i and i + 16 of its word: shifted to bits 15 and 31,
-              // a sign-replicating byte permute spreads them to the two 16-bit lanes.
-              const uint32_t w = hh == 0 ? ((c < 32) ? keep.x : keep.y) : ((c < 32) ? keep.z : keep.w);
-              pm[c / 2] = pk[c / 2] & prmt(w << (15 - (c % 32) / 2), 0u, 0xBB99u);
-            }
-          }
-          // Pᵀ of columns 64hh.. packed over the first 32 of those columns; with dropout the kept
-          // Pᵀ goes there (dV's operand) and every Pᵀ over the next 32 (the dSᵀ role's input).
-          if constexpr (DROP) {
-            tmem_st32(X + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&pm[0]));
-            tmem_st32(X + 64 * hh + 32, pk);
-          } else {
-            tmem_st32(X + 64 * hh, pk);
-          }
+      for (int c = 0; c < 64; c += 2) {
+        float2 nl = *reinterpret_cast<const float2*>(nlse2 + c);
+        if constexpr (ALIBI) nl = add2(nl, kr2);
+        if constexpr (BIAS) nl = fma2(bias_pair<DT>(bz, c), make_float2(kLog2e, kLog2e), nl);
+        const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl);
+        float p0 = ex2(x.x);
+        float p1 = ex2(x.y);
+        if (need_mask) {
+          if (c < lim) p0 = 0.f;
+          if (c + 1 < lim) p1 = 0.f;
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bars.p_full[b]);
+        pk[c / 2] = pack2(p0, p1, DT);
+        if constexpr (DROP) {
+          // dV takes the kept P only; dS below takes every P.  A zero of either 16-bit type
+          // is all zero bits, so the kept pair is the packed pair with dropped halves cleared.
+          // The pair's keep bits sit at bits i and i + 16 of its word: shifted to bits 15 and
+          // 31, a sign-replicating byte permute spreads them to the two 16-bit lanes.
+          const uint32_t w = (c < 32) ? keep.x : keep.y;
+          pm[c / 2] = pk[c / 2] & prmt(w << (15 - (c % 32) / 2), 0u, 0xBB99u);
+        }
+      }
+      if constexpr (DROP) {
+        tmem_st32(X + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pm[0]));
       } else {
-        // ---- dSᵀ = Pᵀ ∘ (dPᵀ − Delta) ----
-        // The step's -Delta vector arrives with its dO tile.  This role's arrival on p_full
-        // (which the dV MMA, the last reader of that dO slot, waits for) comes after its wait,
-        // so the slot's refill cannot overtake the wait.
-        if (!mbar_wait_warp(&bars.ring_full[2 + n % C::NDO], (n / C::NDO) & 1, wt)) { ok = false; break; }
-        mbar_arrive(&bars.p_full[b]);
-        if (!mbar_wait_warp(&bars.p_full[b], par, wt)) { ok = false; break; }
-        if (!mbar_wait_warp(&bars.dp_full[b], par, wt)) { ok = false; break; }
-        tc_fence_after();
-        const float* ndelta = sVec + (b * 2 + 1) * 128;   // -Delta per column
-        // Bias gradient: this key row's 128 query columns of the transposed accumulator.
-        float* dbrow = DBIAS ? dbias_row(p, bi, iter_head(n), kv_row, q0) : nullptr;
-        float2 dbhold = make_float2(0.f, 0.f);            // pairs of dS awaiting a 4-wide reduce-add
-        const float2 dp2 = make_float2(bs.dp, bs.dp);
-#pragma unroll 1
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t sv[64], pk[32], ds[32];
-          tmem_ld32(Y + 64 * hh, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-          tmem_ld32(Y + 64 * hh + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-          tmem_ld32(X + 64 * hh + (DROP ? 32 : 0), pk);
+        tmem_st32(X + 64 * h, pk);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.p_full[b]);
+      // dSᵀ = Pᵀ ∘ (dPᵀ − Delta)
+      if (!mbar_wait_warp(&bars.dp_full[b], par, wt)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t ds[32];
+      float2 dbhold = make_float2(0.f, 0.f);   // pairs of dS awaiting a 4-wide reduce-add
+      if constexpr (DROP) {
+        // dP = keep / (1 - p) * dO·Vᵀ.  Half the columns at a time (fewer live registers):
+        // the second half is read before region Y is released.
+        const float2 rk2 = make_float2(bs.dp, bs.dp);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          tmem_ld32(Y + 64 * h + 32 * half, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
           tmem_ld_wait();
-          if (hh == 1) {
+          if (half == 1) {
             tc_fence_before();
             mbar_arrive(&bars.dp_consumed[b]);   // region Y may now take the next step's Sᵀ
           }
+          const uint32_t w = half == 0 ? keep.x : keep.y;
 #pragma unroll
-          for (int c = 0; c < 64; c += 2) {
-            const float2 nd = *reinterpret_cast<const float2*>(ndelta + 64 * hh + c);
-            float2 dpv = make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
-            if constexpr (DROP) {
-              // dP = keep / (1 - p) * dO·Vᵀ: the pair's keep bits (bits c/2 and c/2 + 16 of its
-              // word) as two all-ones / all-zeros masks.
-              const uint32_t w = hh == 0 ? ((c < 32) ? keep.x : keep.y) : ((c < 32) ? keep.z : keep.w);
-              const uint32_t kx = w << (15 - (c % 32) / 2);
-              dpv = make_float2(__uint_as_float(sv[c] & prmt(kx, 0u, 0x9999u)),
-                                __uint_as_float(sv[c + 1] & prmt(kx, 0u, 0xBBBBu)));
-            }
-            const float2 dd = mul2(unpack2(pk[c / 2], DT), fma2(dpv, dp2, nd));
-            ds[c / 2] = pack2(dd.x, dd.y, DT);
-            if constexpr (DBIAS) dbias_emit(dbrow, 64 * hh + c, dd, dbhold);
-          }
-          // dS in shared memory, one 128-byte swizzled row per key row r, chunk hh holding query
-          // columns 64hh..64hh+63: read K-major (rows = keys) as the A operand of dK += dSᵀ·Q and
-          // MN-major (rows = queries) as the A operand of dQ = dS·K.  The previous step's dQ and
-          // dK MMAs must have finished reading it.
-          if (hh == 0 && n >= 1 && !mbar_wait_warp(&bars.dsbuf_free[b ^ 1], ((n - 1) >> 1) & 1, wt)) {
-            ok = false;
-            break;
-          }
-          uint8_t* rowp = sDS + hh * 16384 + r * 128;
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            uint4 w = make_uint4(ds[u * 4 + 0], ds[u * 4 + 1], ds[u * 4 + 2], ds[u * 4 + 3]);
-            *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) = w;
+          for (int c = 0; c < 32; c += 2) {
+            const float2 nd = *reinterpret_cast<const float2*>(ndelta + 32 * half + c);
+            // The pair's keep bits (bits c/2 and c/2 + 16) as two all-ones / all-zeros masks.
+            const uint32_t kx = w << (15 - c / 2);
+            const float2 dpv = make_float2(__uint_as_float(sv[c] & prmt(kx, 0u, 0x9999u)),
+                                           __uint_as_float(sv[c + 1] & prmt(kx, 0u, 0xBBBBu)));
+            const float2 dd = mul2(unpack2(pk[16 * half + c / 2], DT), fma2(dpv, rk2, nd));
+            ds[16 * half + c / 2] = pack2(dd.x, dd.y, DT);
+            if constexpr (DBIAS) dbias_emit(dbrow, 32 * half + c, dd, dbhold);
           }
         }
-        if (!ok) break;
-        fence_proxy_async_smem();
-        mbar_arrive(&bars.ds_full[b]);
+      } else {
+        tmem_ld32(Y + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(Y + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&bars.dp_consumed[b]);   // region Y may now take the next step's Sᵀ
+        const float2 dp2 = make_float2(bs.dp, bs.dp);
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float2 nd = *reinterpret_cast<const float2*>(ndelta + c);
+          const float2 dd = mul2(unpack2(pk[c / 2], DT),
+                                 fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), dp2, nd));
+          ds[c / 2] = pack2(dd.x, dd.y, DT);
+          if constexpr (DBIAS) dbias_emit(dbrow, c, dd, dbhold);
+        }
       }
+      // dS in shared memory, one 128-byte swizzled row per key row r, chunk h holding query
+      // columns 64h..64h+63: read K-major (rows = keys) as the A operand of dK += dSᵀ·Q and
+      // MN-major (rows = queries) as the A operand of dQ = dS·K.  The previous step's dQ and
+      // dK MMAs must have finished reading it.
+      if (n >= 1 && !mbar_wait_warp(&bars.dsbuf_free[b ^ 1], ((n - 1) >> 1) & 1, wt)) { ok = false; break; }
+      uint8_t* rowp = sDS + h * 16384 + r * 128;
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        uint4 w = make_uint4(ds[u * 4 + 0], ds[u * 4 + 1], ds[u * 4 + 2], ds[u * 4 + 3]);
+        *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) = w;
+      }
+      fence_proxy_async_smem();
+      mbar_arrive(&bars.ds_full[b]);
     }
     // ---- epilogue: dV (h = 0) or dK (h = 1) through shared memory and a TMA store ----
     ok = ok && mbar_wait_warp(&bars.acc_full, 0, wt);
