@@ -378,7 +378,7 @@ sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const void* k, co
   const int rows_per_cta = 128 * (prm.one_tile ? 1 : sdpa::fwd_q_tiles(p->d, p->in_dtype));
   prm.num_m_blocks = (p->s_q + rows_per_cta - 1) / rows_per_cta;
   const long long units = static_cast<long long>(p->b) * p->h_q * prm.num_m_blocks;
-  prm.ctas = sdpa::fwd_persistent_ctas(units, p->d, p->in_dtype, plain, num_sms());
+  prm.ctas = sdpa::fwd_persistent_ctas(units, p->s_kv, p->d, p->in_dtype, plain, num_sms());
   // SDPA_FWD_PERSIST=N overrides the choice where both schedules exist (plain 16-bit,
   // d <= 128): 0 = one CTA per work unit, N >= 1 = min(N, units) CTAs walking the units (a
   // switch for testing and tuning).

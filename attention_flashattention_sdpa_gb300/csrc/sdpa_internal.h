@@ -56,8 +56,9 @@ bool fwd_prefer_one_tile(int b, int h_q, int s_q, int d, int in_dtype, bool plai
 
 // Persistent CTAs for a forward pass of `units` work units: the SM count when the units fill
 // between one and four waves of the GPU (a launch with one CTA per unit would leave the last
-// wave ragged and pay every CTA's set-up), else 0 (one CTA per unit).
-int fwd_persistent_ctas(long long units, int d, int in_dtype, bool plain, int num_sms);
+// wave ragged and pay every CTA's set-up) and are short (s_kv <= 4096), else 0 (one CTA per
+// unit).
+int fwd_persistent_ctas(long long units, int s_kv, int d, int in_dtype, bool plain, int num_sms);
 
 cudaError_t launch_fwd(const FwdParams& p, int d, int in_dtype, int out_dtype, cudaStream_t st);
 uint32_t fwd_take_device_error();
