@@ -231,6 +231,21 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
     mbar_init(&bars.l_ready, 256);
     bars.abort = 0;
     fence_mbar_init();
+    // The first unit's Q tiles and first K block go out before the CTA's set-up (TMEM
+    // allocation, the block barrier): their latency from HBM overlaps it.  Thread 0 is the
+    // producer and carries on from there.
+    if (unit_at(0) < n_units && first.n_blocks > 0) {
+      for (int t = 0; t < NQT; ++t) {
+        mbar_arrive_expect_tx(&bars.q_full[t], C::TILE_BYTES);
+        for (int c = 0; c < C::NCHUNK; ++c)
+          tma_load_4d(sQ + t * C::TILE_BYTES + c * 16384, &p.tm_q, &bars.q_full[t], c * C::CHUNK_ELEMS,
+                      first.m0 + t * kBlockM, first.hq, first.bi);
+      }
+      mbar_arrive_expect_tx(&bars.kv_full[0], C::TILE_BYTES);
+      for (int c = 0; c < C::NCHUNK; ++c)
+        tma_load_4d(sRing + c * 16384, &p.tm_k, &bars.kv_full[0], c * C::CHUNK_ELEMS,
+                    kv_block(0, first.n_blocks) * kBlockN, first.hk, first.bi);
+    }
   }
   if (warp == 1) {
     tmem_alloc(&bars.tmem_base, 512);
@@ -256,12 +271,13 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
   regs_dec<kRegsProd>();
   if (warp == 0) {
     // ================================ TMA producer ====================================
-    if (elect_one_sync()) {
+    if (lane == 0) {
       producer = true;
-      tma_prefetch_desc(&p.tm_q);
-      tma_prefetch_desc(&p.tm_k);
       tma_prefetch_desc(&p.tm_v);
-      int it = 0, qn = 0;
+      // The first unit's Q and first K block were issued before the set-up.
+      bool early = unit_at(0) < n_units && first.n_blocks > 0;
+      int it = early ? 1 : 0, qn = 0;
+      q_issued = kv_issued = it;
       bool ok = true;
       for (int k = 0; ok && k < kMaxUnits; ++k) {
         const int u = unit_at(k);
@@ -269,17 +285,25 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         const FwdUnit w = unit(k, u);
         const int nb = w.n_blocks;
         if (nb == 0) continue;
-        // Q of this unit goes where the previous unit's Q was: wait until its last QKᵀ MMAs
-        // have read it.
-        if (PERSIST && qn > 0 && !mbar_wait(&bars.q_empty, (qn - 1) & 1, wt)) { ok = false; break; }
-        for (int t = 0; t < NQT; ++t) {
-          mbar_arrive_expect_tx(&bars.q_full[t], C::TILE_BYTES);
-          for (int c = 0; c < C::NCHUNK; ++c)
-            tma_load_4d(sQ + t * C::TILE_BYTES + c * 16384, &p.tm_q, &bars.q_full[t],
-                        c * C::CHUNK_ELEMS, w.m0 + t * kBlockM, w.hq, w.bi);
+        if (k == 0 && early) {
+          q_issued = ++qn;
+        } else {
+          // Q of this unit goes where the previous unit's Q was: wait until its last QKᵀ
+          // MMAs have read it.
+          if (PERSIST && qn > 0 && !mbar_wait(&bars.q_empty, (qn - 1) & 1, wt)) { ok = false; break; }
+          for (int t = 0; t < NQT; ++t) {
+            mbar_arrive_expect_tx(&bars.q_full[t], C::TILE_BYTES);
+            for (int c = 0; c < C::NCHUNK; ++c)
+              tma_load_4d(sQ + t * C::TILE_BYTES + c * 16384, &p.tm_q, &bars.q_full[t],
+                          c * C::CHUNK_ELEMS, w.m0 + t * kBlockM, w.hq, w.bi);
+          }
+          q_issued = ++qn;
         }
-        q_issued = ++qn;
         auto load = [&](const CUtensorMap* map, int j) {
+          if (early) {          // K of the first block: issued before the set-up
+            early = false;
+            return true;
+          }
           const int slot = it % NS;
           const uint32_t ph = (it / NS) & 1;
           if (!mbar_wait(&bars.kv_empty[slot], ph ^ 1, wt)) return false;
