@@ -166,7 +166,7 @@ def all_workloads():
     out += [training(s) for s in TRAINING_SEQ_LENS]
     out += [fp8_large_head(), grouped(8), grouped(1), grouped(64), training_alibi(8192),
             training_dropout(8192), training_fp8(8192), training_bias(8192), training_varlen(),
-            prefill_bottom_right()]
+            prefill_bottom_right(), backward_d256(True), backward_d256(False)]
     return out
 
 
