@@ -65,9 +65,25 @@ __device__ __forceinline__ uint32_t keep8(uint64_t g, uint32_t off_lo, uint32_t 
   return bits;
 }
 
+// Transposes the 32 x 32 bit matrix a warp holds (bit c of lane l's word = M[l][c]) so that
+// bit l of lane c's word = M[l][c]: five exchange stages, each swapping the off-diagonal k x k
+// blocks (k = 16, 8, 4, 2, 1) between lanes l and l ^ k.
+__device__ __forceinline__ uint32_t transpose32(uint32_t x, int lane) {
+  constexpr uint32_t kMask[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+  for (int st = 0; st < 5; ++st) {
+    const int k = 16 >> st;
+    const uint32_t m = kMask[st];
+    const uint32_t y = __shfl_xor_sync(0xffffffffu, x, k);
+    x = (lane & k) ? ((x & ~m) | ((y >> k) & m)) : ((x & m) | ((y << k) & ~m));
+  }
+  return x;
+}
+
 // One CTA of 128 threads per (b*h_q, 128-row query block, 128-key block).  Lane L of warp w
 // draws row 32w + L: 16 Philox blocks give its 128 bits, stored as four row-major words.  The
-// transposed words come from 32 ballots per 32x32 bit block and a 2 KB exchange.
+// transposed words come from a five-stage shuffle transpose of each 32x32 bit block and a 2 KB
+// exchange.
 __global__ void __launch_bounds__(128) dropout_mask_kernel(const DropoutParams p) {
   __shared__ uint32_t tile[128][4];   // [key within block][query word]
   const int kb = blockIdx.x, qb = blockIdx.y, bh = blockIdx.z;
@@ -94,15 +110,11 @@ __global__ void __launch_bounds__(128) dropout_mask_kernel(const DropoutParams p
     }
   }
   if (p.cols == nullptr) return;   // uniform over the grid
-  // Transpose: bit c of ballot c' over the warp's 32 rows is key 32i + c's bit for row 32w + lane.
+  // Transpose each 32 x 32 bit block: lane c then holds key 32i + c's bits for the warp's rows
+  // 32w .. 32w + 31 (bit l = row 32w + l).
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint32_t mine = 0;
-#pragma unroll
-    for (int c = 0; c < 32; ++c) {
-      const uint32_t col = __ballot_sync(0xffffffffu, (w[i] >> c) & 1u);
-      if (lane == c) mine = col;
-    }
+    uint32_t mine = transpose32(w[i], lane);
     // Unshuffle: even rows to the low half, odd rows to the high half (four delta swaps).
     uint32_t t = (mine ^ (mine >> 1)) & 0x22222222u;
     mine ^= t ^ (t << 1);
