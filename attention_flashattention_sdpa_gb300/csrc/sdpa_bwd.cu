@@ -395,13 +395,6 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
     }
     bars.abort = 0;
     fence_mbar_init();
-    // K and V go out before the CTA's set-up (TMEM allocation, the block barrier): their
-    // latency from HBM overlaps it.  Thread 0 is the producer and carries on from there.
-    mbar_arrive_expect_tx(&bars.kv_full, 2 * C::TILE);
-    for (int c = 0; c < C::NCHUNK; ++c) {
-      tma_load_4d(sK + c * 16384, &p.tm_k, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
-      tma_load_4d(sV + c * 16384, &p.tm_v, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
-    }
   }
   if (warp == 1) {
     tmem_alloc(&bars.tmem_base, 512);
@@ -428,8 +421,13 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   regs_dec<64>();
   if (warp == 0) {
     // ================================ TMA producer ====================================
-    if (lane == 0) {   // thread 0: K and V are already on their way
+    if (elect_one_sync()) {
       producer = true;
+      mbar_arrive_expect_tx(&bars.kv_full, 2 * C::TILE);
+      for (int c = 0; c < C::NCHUNK; ++c) {
+        tma_load_4d(sK + c * 16384, &p.tm_k, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
+        tma_load_4d(sV + c * 16384, &p.tm_v, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
+      }
       bool ok = true;
       for (int n = 0; n < n_iter && ok; ++n) {
         const int hq = iter_head(n), qb = iter_qblk(n);
