@@ -440,13 +440,17 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&bars.ring_full[slot], C::TILE + 512);
+          // Both per-row vectors (-LSE·log2 e and -Delta) travel with Q: the compute warps then
+          // wait for no dO tile, whose slot is refilled only once dV of the previous step ran.
+          mbar_arrive_expect_tx(&bars.ring_full[slot], which == 0 ? C::TILE + 1024 : C::TILE);
           const CUtensorMap* map = which == 0 ? &p.tm_q : &p.tm_do;
           for (int c = 0; c < C::NCHUNK; ++c)
             tma_load_4d(sRing + slot * C::TILE + c * 16384, map, &bars.ring_full[slot], c * 64,
                         qb * kBlockM, hq, bi);
-          const float* vsrc = (which == 0 ? p.lse2 : p.delta) + vrow;
-          bulk_load(sVec + ((n & 1) * 2 + which) * 128, vsrc, 512, &bars.ring_full[slot]);
+          if (which == 0) {
+            bulk_load(sVec + (n & 1) * 256, p.lse2 + vrow, 512, &bars.ring_full[slot]);
+            bulk_load(sVec + (n & 1) * 256 + 128, p.delta + vrow, 512, &bars.ring_full[slot]);
+          }
           if (which == 0) ++nq; else ++nd;
         }
       }
@@ -579,11 +583,10 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       const float* nlse2 = sVec + (b * 2 + 0) * 128 + 64 * h;    // -LSE·log2 e per column
       const float* ndelta = sVec + (b * 2 + 1) * 128 + 64 * h;   // -Delta per column
       // Pᵀ = exp2(Sᵀ·scale·log2e − LSE·log2e), masked where key > query
-      // This step's -LSE and -Delta vectors arrive with its Q and dO tiles.  Both waits come
-      // before Pᵀ is released: dO's slot is refilled once dV of this step has read it, and
-      // dV needs Pᵀ, so the refill cannot overtake these waits.
+      // This step's -LSE and -Delta vectors arrive with its Q tile.  Q's slot is refilled only
+      // after dK of this step, which needs every thread's dS, so the refill cannot overtake
+      // this wait, and both vectors stay in place until this step's dS is stored.
       if (!mbar_wait_warp(&bars.ring_full[n & 1], (n >> 1) & 1, wt)) { ok = false; break; }
-      if (!mbar_wait_warp(&bars.ring_full[2 + n % C::NDO], (n / C::NDO) & 1, wt)) { ok = false; break; }
       if (!mbar_wait_warp(&bars.s_full[b], par, wt)) { ok = false; break; }
       tc_fence_after();
       uint32_t sv[64];
@@ -602,9 +605,11 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       const float kr = ALIBI ? alibi_slope_log2(p, iter_head(n)) *
                                    static_cast<float>(kv_row - iter_qblk(n) * kBlockM - L.off) : 0.f;
       const float2 kr2 = make_float2(kr, kr);
+      float4 nl4;
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
-        float2 nl = *reinterpret_cast<const float2*>(nlse2 + c);
+        if ((c & 3) == 0) nl4 = *reinterpret_cast<const float4*>(nlse2 + c);
+        float2 nl = (c & 3) ? make_float2(nl4.z, nl4.w) : make_float2(nl4.x, nl4.y);
         if constexpr (ALIBI) nl = add2(nl, kr2);
         if constexpr (BIAS) nl = fma2(bias_pair<DT>(bz, c), make_float2(kLog2e, kLog2e), nl);
         const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl);
@@ -669,9 +674,11 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         tc_fence_before();
         mbar_arrive(&bars.dp_consumed[b]);   // region Y may now take the next step's Sᵀ
         const float2 dp2 = make_float2(bs.dp, bs.dp);
+        float4 nd4;
 #pragma unroll
         for (int c = 0; c < 64; c += 2) {
-          const float2 nd = *reinterpret_cast<const float2*>(ndelta + c);
+          if ((c & 3) == 0) nd4 = *reinterpret_cast<const float4*>(ndelta + c);
+          const float2 nd = (c & 3) ? make_float2(nd4.z, nd4.w) : make_float2(nd4.x, nd4.y);
           const float2 dd = mul2(unpack2(pk[c / 2], DT),
                                  fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), dp2, nd));
           ds[c / 2] = pack2(dd.x, dd.y, DT);
