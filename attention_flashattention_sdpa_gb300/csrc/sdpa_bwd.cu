@@ -100,12 +100,13 @@ __device__ __forceinline__ BwdScales bwd_scales(const BwdParams& p) {
   return s;
 }
 
-// 64 bias values of key row kv_row for queries q0..q0+63 from the transposed copy (zero for
+// 8·NV bias values of key row kv_row for queries q0.. from the transposed copy (zero for
 // a key row beyond s_kv, which sees nothing anyway).
-__device__ __forceinline__ void load_bias_t(const BwdParams& p, int bi, int hq, int kv_row, int q0, uint4 (&bz)[8]) {
+template <int NV>
+__device__ __forceinline__ void load_bias_t(const BwdParams& p, int bi, int hq, int kv_row, int q0, uint4 (&bz)[NV]) {
   if (kv_row >= p.s_kv) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) bz[e] = make_uint4(0u, 0u, 0u, 0u);
+    for (int e = 0; e < NV; ++e) bz[e] = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
   const int nb = p.bias_nb > 1 ? bi : 0, nh = p.bias_nh > 1 ? hq : 0;
@@ -113,7 +114,7 @@ __device__ __forceinline__ void load_bias_t(const BwdParams& p, int bi, int hq, 
       static_cast<const uint16_t*>(p.bias_t) +
       ((static_cast<int64_t>(nb) * p.bias_nh + nh) * p.s_kv + kv_row) * p.s_q_pad + q0);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) bz[e] = __ldg(src + e);
+  for (int e = 0; e < NV; ++e) bz[e] = __ldg(src + e);
 }
 
 // Starts moving the same 128-byte bias row into L2 (a later step's row: its loads then hit L2).
@@ -140,9 +141,9 @@ __device__ __forceinline__ void dbias_emit(float* row, int c, float2 dd, float2&
   }
 }
 
-// Columns c, c+1 of eight packed 16-bit bias vectors, as fp32.
-template <int DT>
-__device__ __forceinline__ float2 bias_pair(const uint4 (&bz)[8], int c) {
+// Columns c, c+1 of NV packed 16-bit bias vectors (eight values each), as fp32.
+template <int DT, int NV>
+__device__ __forceinline__ float2 bias_pair(const uint4 (&bz)[NV], int c) {
   const uint4 v = bz[c / 8];
   const uint32_t w = (c % 8 == 0) ? v.x : (c % 8 == 2) ? v.y : (c % 8 == 4) ? v.z : v.w;
   return unpack2(w, DT);
@@ -846,33 +847,43 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
 // alone take 128 KB of shared memory.  So a CTA owns one half of d of dK and dV, walks
 // 64-row query blocks, and computes its half of dQ transposed (dQᵀ = Kᵀ·dSᵀ: rows = its 128
 // d indices, so M stays 128) into a transposed fp32 accumulator [b·h_q][d][s_q_pad].  Both
-// halves compute the full-d reductions Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ.  One thread issues the
-// copies and MMAs.  Within a step, Pᵀ is computed while the dPᵀ MMAs run and dS while the dV
-// MMAs run; the next step's Q and dO tiles are loaded while this step's dS and dQᵀ are
-// computed and drained.
+// halves compute the full-d reductions Sᵀ = K·Qᵀ and dPᵀ = V·dOᵀ.
+//
+// The roles are those of the d = 128 kernel, linked by mbarriers: one thread loads, one
+// issues the MMAs, two warpgroups compute Pᵀ and dSᵀ (32 query columns each) and one
+// warpgroup drains dQᵀ.  Per step the MMAs run Sᵀ, dPᵀ, dV += Pᵀ·dO, then the next step's
+// Sᵀ while dS is computed, then dK += dSᵀ·Q and dQᵀ.  The own d-half of Q is double-buffered
+// (the next step's lands while this step's dK still reads it); the far half of Q and both
+// halves of dO are refilled as soon as the MMAs that read them are done.  dQᵀ leaves through
+// the dS buffer (two 32-column fp32 chunks, each a TMA reduce-add), which then takes the
+// next step's dS.
 struct D256 {
   static constexpr int BQ = 64;                  // query rows per step
   static constexpr int OFF_K = 0;                // 128 x 256: four 16 KB chunks of 64 columns
   static constexpr int OFF_V = 65536;
-  static constexpr int OFF_Q = 131072;           // 64 x 256: four 8 KB chunks
-  static constexpr int OFF_DO = 163840;
-  static constexpr int OFF_DS = 196608;          // dS: 128 key rows x 64 queries, 16 KB
-  static constexpr int OFF_ST = 212992;          // dQᵀ staging: 128 rows x 32 fp32, 16 KB
-  static constexpr int OFF_VEC = 229376;         // -LSE·log2e and -Delta of the step, 64 each
-  static constexpr int OFF_BAR = OFF_VEC + 512;
+  static constexpr int OFF_QF = 131072;          // the other d-half of Q: two 8 KB chunks
+  static constexpr int OFF_QN = 147456;          // own d-half of Q: two buffers of 16 KB
+  static constexpr int OFF_DO = 180224;          // dO, 64 x 256: four 8 KB chunks
+  static constexpr int OFF_DS = 212992;          // dS (128 key rows x 64 queries), then dQᵀ
+  static constexpr int OFF_VEC = 229376;         // [2][-LSE·log2e, -Delta][64] fp32
+  static constexpr int OFF_BAR = OFF_VEC + 1024;
   static constexpr int SMEM_BYTES = OFF_BAR + 256;
+  static constexpr int THREADS = 512;
   static constexpr int COL_S = 0, COL_DP = 64, COL_DQ = 128, COL_DV = 256, COL_DK = 384;
 };
 static_assert(D256::SMEM_BYTES <= 232448, "shared memory budget");
 
 struct alignas(8) D256Barriers {
-  uint64_t kv_full, ld_far, ld_near, s_done, dp_done, mma_done, drain;
+  uint64_t kv_full, qf_full, qf_empty, qn_full[2], qn_empty[2], df_full, df_empty, dn_full, dn_empty;
+  uint64_t s_full, p_full, dp_full, dp_consumed, ds_full, dq_full, ds_free, stage_full, stage_free;
+  uint64_t acc_full, drain, epi_ready[2];
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(D256Barriers) <= 256, "barrier block");
 
 template <int DT, int FEAT>
-__global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant__ BwdParams p) {
   using C = D256;
   constexpr bool ALIBI = (FEAT & kFeatAlibi) != 0;
   constexpr bool DROP = (FEAT & kFeatDropout) != 0;
@@ -886,22 +897,18 @@ __global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant_
   D256Barriers& bars = *reinterpret_cast<D256Barriers*>(smem + C::OFF_BAR);
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
-  uint8_t* sQ = smem + C::OFF_Q;
+  uint8_t* sQF = smem + C::OFF_QF;
+  uint8_t* sQN = smem + C::OFF_QN;
   uint8_t* sdO = smem + C::OFF_DO;
   uint8_t* sDS = smem + C::OFF_DS;
-  uint8_t* sST = smem + C::OFF_ST;
   float* sVec = reinterpret_cast<float*>(smem + C::OFF_VEC);
   const int warp = threadIdx.x / 32;
-  const int r = threadIdx.x;                     // TMEM lane: key row, or d row of dQᵀ
-  // Warps 0-3 compute (one key row, or one d row of dQᵀ, per thread); one thread of warp 4
-  // issues every copy and MMA, so that no compute warp waits on the issue.
-  constexpr int kIssuer = 128;
-  const bool compute = threadIdx.x < 128;
-  const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+  const int lane = threadIdx.x % 32;
 
   // Launch order: the two d-halves of a unit side by side, units fastest, KV blocks slowest
   // (for causal, the first KV blocks carry the most query blocks and go first).
-  const int dh = blockIdx.x & 1;
+  const int dh = blockIdx.x & 1;                 // own d-half: chunks 2dh, 2dh + 1
+  const int fh = 1 - dh;                         // the other half
   const int rest = blockIdx.x >> 1;
   const int units = p.b * p.h_kv * p.kv_split;
   const int unit = rest % units;
@@ -918,20 +925,37 @@ __global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant_
   const int head0 = hk * p.group + split * p.heads_per_split;
   const int n_heads = max(0, min(p.heads_per_split, (hk + 1) * p.group - head0));
   const int n_iter = per_head * n_heads;
-  const int kv_row = j * kBlockN + r;
+  auto iter_head = [&](int n) { return head0 + n / per_head; };
+  auto iter_q0 = [&](int n) { return (q_first + n % per_head) * C::BQ; };
 
   if (threadIdx.x == 0) {
     mbar_init(&bars.kv_full, 1);
-    mbar_init(&bars.ld_far, 1);
-    mbar_init(&bars.ld_near, 1);
-    mbar_init(&bars.s_done, 1);
-    mbar_init(&bars.dp_done, 1);
-    mbar_init(&bars.mma_done, 1);
+    mbar_init(&bars.qf_full, 1);
+    mbar_init(&bars.qf_empty, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars.qn_full[b], 1);
+      mbar_init(&bars.qn_empty[b], 1);
+      mbar_init(&bars.epi_ready[b], 128);
+    }
+    mbar_init(&bars.df_full, 1);
+    mbar_init(&bars.df_empty, 1);
+    mbar_init(&bars.dn_full, 1);
+    mbar_init(&bars.dn_empty, 1);
+    mbar_init(&bars.s_full, 1);
+    mbar_init(&bars.p_full, 256);
+    mbar_init(&bars.dp_full, 1);
+    mbar_init(&bars.dp_consumed, 256);
+    mbar_init(&bars.ds_full, 256);
+    mbar_init(&bars.dq_full, 1);
+    mbar_init(&bars.ds_free, 1);
+    mbar_init(&bars.stage_full, 128);
+    mbar_init(&bars.stage_free, 1);
+    mbar_init(&bars.acc_full, 1);
     mbar_init(&bars.drain, 1);
     bars.abort = 0;
     fence_mbar_init();
   }
-  if (warp == 0) {
+  if (warp == 1) {
     tmem_alloc(&bars.tmem_base, 512);
     tmem_relinquish();
   }
@@ -941,109 +965,172 @@ __global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant_
   const uint32_t tmem = bars.tmem_base;
   volatile int* abort_flag = &bars.abort;
   const Waiter wt{abort_flag, p.wait_limit};
-  const uint32_t fmt = (DT == kBF16) ? 1u : 0u;
-  const BwdScales bs = bwd_scales(p);
 
-  // Q and dO tiles of step n (one thread), in two parts: the d-half this CTA does not own
-  // (read only by the Sᵀ and dPᵀ MMAs, so it can be refilled once those are done), and its
-  // own d-half with the -LSE/-Delta vectors (refilled after the step's last MMAs).
-  int n_far = 0, n_near = 0;   // loads issued on ld_far / ld_near (one in flight at a time)
-  auto load_far = [&](int n) {
-    ++n_far;
-    const int hq = head0 + n / per_head;
-    const int q0 = (q_first + n % per_head) * C::BQ;
-    mbar_arrive_expect_tx(&bars.ld_far, 32768);
-    for (int c = 2 * (1 - dh); c < 2 * (1 - dh) + 2; ++c) {
-      tma_load_4d(sQ + c * 8192, &p.tm_q, &bars.ld_far, c * 64, q0, hq, bi);
-      tma_load_4d(sdO + c * 8192, &p.tm_do, &bars.ld_far, c * 64, q0, hq, bi);
-    }
-  };
-  auto load_near = [&](int n) {
-    ++n_near;
-    const int hq = head0 + n / per_head;
-    const int q0 = (q_first + n % per_head) * C::BQ;
-    const int64_t vrow = (static_cast<int64_t>(bi) * p.h_q + hq) * p.s_q_pad + q0;
-    mbar_arrive_expect_tx(&bars.ld_near, 32768 + 512);
-    for (int c = 2 * dh; c < 2 * dh + 2; ++c) {
-      tma_load_4d(sQ + c * 8192, &p.tm_q, &bars.ld_near, c * 64, q0, hq, bi);
-      tma_load_4d(sdO + c * 8192, &p.tm_do, &bars.ld_near, c * 64, q0, hq, bi);
-    }
-    bulk_load(sVec, p.lse2 + vrow, 256, &bars.ld_near);
-    bulk_load(sVec + 64, p.delta + vrow, 256, &bars.ld_near);
-  };
-  if (threadIdx.x == kIssuer) {
-    mbar_arrive_expect_tx(&bars.kv_full, 2 * 65536);
-    for (int c = 0; c < 4; ++c) {
-      tma_load_4d(sK + c * 16384, &p.tm_k, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
-      tma_load_4d(sV + c * 16384, &p.tm_v, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
-    }
-    if (n_iter > 0) {
-      load_far(0);
-      load_near(0);
-    }
-  }
-  bool ok = __syncthreads_and(mbar_wait(&bars.kv_full, 0, wt));
-  uint32_t ph_ld = 0, ph_mma = 0;
-  for (int n = 0; n < n_iter && ok; ++n) {
-    const int hq = head0 + n / per_head;
-    const int q0 = (q_first + n % per_head) * C::BQ;
-    // The previous step's dQᵀ reduce-adds read the staging buffer and the dS buffer: both
-    // are rewritten below, after this barrier.
-    if (threadIdx.x == kIssuer) bulk_wait_read<0>();
-    ok = __syncthreads_and(mbar_wait(&bars.ld_far, ph_ld, wt) &&
-                           mbar_wait(&bars.ld_near, ph_ld, wt));
-    ph_ld ^= 1;
-    if (!ok) break;
-    // ---- Sᵀ = K·Qᵀ, then dPᵀ = V·dOᵀ, over all of d: committed separately, so that Pᵀ is
-    // computed while the dPᵀ MMAs run ----
-    if (threadIdx.x == kIssuer) {
-      tc_fence_after();
-      const uint32_t idesc_s = make_idesc(fmt, 128, C::BQ, false, false);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint32_t oa = (k / 4) * 16384 + (k % 4) * 32, ob = (k / 4) * 8192 + (k % 4) * 32;
-        mma_ss(tmem + C::COL_S, make_sdesc_sw128(smem_u32(sK) + oa, 16, 1024),
-               make_sdesc_sw128(smem_u32(sQ) + ob, 16, 1024), idesc_s, k > 0, false);
+  // Loads the producer has issued on each barrier (for the drain should a role give up).
+  bool producer = false;
+  int n_qf = 0, n_qn = 0, n_df = 0, n_dn = 0;
+
+  if (warp == 0) {
+    // ================================ TMA producer ====================================
+    if (lane == 0) {
+      producer = true;
+      mbar_arrive_expect_tx(&bars.kv_full, 2 * 65536);
+      for (int c = 0; c < 4; ++c) {
+        tma_load_4d(sK + c * 16384, &p.tm_k, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
+        tma_load_4d(sV + c * 16384, &p.tm_v, &bars.kv_full, c * 64, j * kBlockN, hk, bi);
       }
-      tc_commit(&bars.s_done);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const uint32_t oa = (k / 4) * 16384 + (k % 4) * 32, ob = (k / 4) * 8192 + (k % 4) * 32;
-        mma_ss(tmem + C::COL_DP, make_sdesc_sw128(smem_u32(sV) + oa, 16, 1024),
-               make_sdesc_sw128(smem_u32(sdO) + ob, 16, 1024), idesc_s, k > 0, false);
+      // In the order the MMAs free the buffers: Q far (after Sᵀ of the previous step), Q own
+      // half (after dK two steps back), dO far (after dPᵀ), dO own half (after dV).
+      for (int n = 0; n < n_iter; ++n) {
+        const int hq = iter_head(n), q0 = iter_q0(n);
+        if (n > 0 && !mbar_wait(&bars.qf_empty, (n - 1) & 1, wt)) break;
+        mbar_arrive_expect_tx(&bars.qf_full, 16384);
+        for (int c = 2 * fh; c < 2 * fh + 2; ++c)
+          tma_load_4d(sQF + (c - 2 * fh) * 8192, &p.tm_q, &bars.qf_full, c * 64, q0, hq, bi);
+        ++n_qf;
+        const int b = n & 1;
+        if (n > 1 && !mbar_wait(&bars.qn_empty[b], ((n - 2) >> 1) & 1, wt)) break;
+        mbar_arrive_expect_tx(&bars.qn_full[b], 16384 + 512);
+        for (int c = 2 * dh; c < 2 * dh + 2; ++c)
+          tma_load_4d(sQN + b * 16384 + (c - 2 * dh) * 8192, &p.tm_q, &bars.qn_full[b], c * 64, q0, hq, bi);
+        const int64_t vrow = (static_cast<int64_t>(bi) * p.h_q + hq) * p.s_q_pad + q0;
+        bulk_load(sVec + b * 128, p.lse2 + vrow, 256, &bars.qn_full[b]);
+        bulk_load(sVec + b * 128 + 64, p.delta + vrow, 256, &bars.qn_full[b]);
+        ++n_qn;
+        if (n > 0 && !mbar_wait(&bars.df_empty, (n - 1) & 1, wt)) break;
+        mbar_arrive_expect_tx(&bars.df_full, 16384);
+        for (int c = 2 * fh; c < 2 * fh + 2; ++c)
+          tma_load_4d(sdO + c * 8192, &p.tm_do, &bars.df_full, c * 64, q0, hq, bi);
+        ++n_df;
+        if (n > 0 && !mbar_wait(&bars.dn_empty, (n - 1) & 1, wt)) break;
+        mbar_arrive_expect_tx(&bars.dn_full, 16384);
+        for (int c = 2 * dh; c < 2 * dh + 2; ++c)
+          tma_load_4d(sdO + c * 8192, &p.tm_do, &bars.dn_full, c * 64, q0, hq, bi);
+        ++n_dn;
       }
-      tc_commit(&bars.dp_done);
     }
-    const bool need_mask = (p.causal && (q0 + L.off < j * kBlockN + kBlockN - 1)) ||
-                           (j * kBlockN + kBlockN > L.len_kv);
-    int lim = p.causal ? kv_row - q0 - L.off : -(1 << 30);  // column c visible iff c >= lim
-    if (kv_row >= L.len_kv) lim = 1 << 30;
-    // Dropout: keep bits of this key row for the 64 query columns (transposed mask).
-    uint2 keep = make_uint2(0u, 0u);
-    if (DROP && compute && kv_row < p.s_kv)
-      keep = __ldg(reinterpret_cast<const uint2*>(
-          p.drop_cols + ((static_cast<int64_t>(bi) * p.h_q + hq) * p.s_kv + kv_row) * p.drop_q_words + q0 / 32));
-    float pf[64];                                  // Pᵀ of key row r (every P, for dS)
-    // ---- Pᵀ for key row r, over Sᵀ in TMEM (the kept P under dropout: dV's operand) ----
-    bool w_ok = !compute || mbar_wait(&bars.s_done, ph_mma, wt);
-    if (w_ok && compute) {
+  } else if (warp == 1) {
+    // ================================ MMA issuer ======================================
+    if (lane == 0) {
+      const uint32_t fmt = (DT == kBF16) ? 1u : 0u;
+      const uint32_t idesc_s = make_idesc(fmt, 128, C::BQ, false, false);    // Sᵀ, dPᵀ
+      const uint32_t idesc_acc = make_idesc(fmt, 128, 128, false, true);     // dV, dK
+      const uint32_t idesc_dq = make_idesc(fmt, 128, C::BQ, true, true);     // dQᵀ
+      const uint32_t kA = smem_u32(sK), vA = smem_u32(sV), qF = smem_u32(sQF), qN = smem_u32(sQN);
+      const uint32_t gA = smem_u32(sdO), dsA = smem_u32(sDS);
+      bool ok = mbar_wait(&bars.kv_full, 0, wt);
+      // Sᵀ = K·Qᵀ of step m over all of d (Q's own half in buffer m % 2, the other half in QF).
+      auto issue_s = [&](int m) -> bool {
+        if (!mbar_wait(&bars.qf_full, m & 1, wt)) return false;
+        if (!mbar_wait(&bars.qn_full[m & 1], (m >> 1) & 1, wt)) return false;
+        tc_fence_after();
+        const uint32_t qn = qN + (m & 1) * 16384;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int c = k / 4;
+          const uint32_t b = ((c >> 1) == dh ? qn + (c - 2 * dh) * 8192 : qF + (c - 2 * fh) * 8192) + (k % 4) * 32;
+          mma_ss(tmem + C::COL_S, make_sdesc_sw128(kA + c * 16384 + (k % 4) * 32, 16, 1024),
+                 make_sdesc_sw128(b, 16, 1024), idesc_s, k > 0, false);
+        }
+        tc_commit(&bars.s_full);
+        tc_commit(&bars.qf_empty);
+        return true;
+      };
+      if (ok && n_iter > 0) ok = issue_s(0);
+      for (int n = 0; n < n_iter && ok; ++n) {
+        // ---- dPᵀ = V·dOᵀ over all of d, once the compute warps have read the last one ----
+        if (!mbar_wait(&bars.df_full, n & 1, wt) || !mbar_wait(&bars.dn_full, n & 1, wt) ||
+            (n > 0 && !mbar_wait(&bars.dp_consumed, (n - 1) & 1, wt))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const uint32_t off_a = (k / 4) * 16384 + (k % 4) * 32, off_b = (k / 4) * 8192 + (k % 4) * 32;
+          mma_ss(tmem + C::COL_DP, make_sdesc_sw128(vA + off_a, 16, 1024),
+                 make_sdesc_sw128(gA + off_b, 16, 1024), idesc_s, k > 0, false);
+        }
+        tc_commit(&bars.dp_full);
+        tc_commit(&bars.df_empty);
+        // ---- dV_h += Pᵀ·dO_h (Pᵀ in TMEM: queries 0..31 at S+0.., 32..63 at S+32..) ----
+        if (!mbar_wait(&bars.p_full, n & 1, wt)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t gh = gA + dh * 2 * 8192;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t a_col = (k < 2) ? k * 8 : 32 + (k - 2) * 8;
+          mma_ts(tmem + C::COL_DV, tmem + C::COL_S + a_col, make_sdesc_sw128(gh + k * 2048, 8192, 1024),
+                 idesc_acc, (n > 0 || k > 0) ? 1u : 0u, false);
+        }
+        tc_commit(&bars.dn_empty);
+        // ---- the next step's Sᵀ (region S is free: Pᵀ was read by the dV MMAs above) ----
+        if (n + 1 < n_iter && !issue_s(n + 1)) { ok = false; break; }
+        // ---- dK_h += dSᵀ·Q_h, then dQᵀ_h = K_hᵀ·dSᵀ ----
+        if (!mbar_wait(&bars.ds_full, n & 1, wt)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t qn = qN + (n & 1) * 16384;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          mma_ss(tmem + C::COL_DK, make_sdesc_sw128(dsA + k * 32, 16, 1024),
+                 make_sdesc_sw128(qn + k * 2048, 8192, 1024), idesc_acc, (n > 0 || k > 0) ? 1u : 0u,
+                 false);
+        tc_commit(&bars.qn_empty[n & 1]);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          mma_ss(tmem + C::COL_DQ, make_sdesc_sw128(kA + dh * 2 * 16384 + k * 2048, 16384, 1024),
+                 make_sdesc_sw128(dsA + k * 2048, 8192, 1024), idesc_dq, k > 0, false);
+        tc_commit(&bars.dq_full);
+      }
+      tc_commit(&bars.acc_full);
+      tc_commit(&bars.drain);
+      mbar_wait_drain(&bars.drain, 0);
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ============================ Pᵀ / dSᵀ (two column halves) ========================
+    const int h = (warp - 4) / 4;                         // query columns [32h, 32h+32)
+    const int quad = warp % 4;
+    const int r = quad * 32 + lane;                       // key row within the block (TMEM lane)
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    const int kv_row = j * kBlockN + r;
+    const BwdScales bs = bwd_scales(p);
+    bool ok = true;
+    for (int n = 0; n < n_iter; ++n) {
+      const int hq = iter_head(n);
+      const int qb = iter_q0(n);                          // first query row of the block
+      const int q0 = qb + 32 * h;                         // first query column of this half
+      // Dropout: keep bits of this key row for the 32 query columns (transposed mask).
+      uint32_t keep = 0u;
+      if (DROP && kv_row < p.s_kv)
+        keep = __ldg(p.drop_cols + ((static_cast<int64_t>(bi) * p.h_q + hq) * p.s_kv + kv_row) * p.drop_q_words +
+                     q0 / 32);
+      uint4 bz[BIAS ? 4 : 1];
+      if constexpr (BIAS) load_bias_t(p, bi, hq, kv_row, q0, bz);
+      const float* nlse2 = sVec + (n & 1) * 128 + 32 * h;
+      const float* ndelta = sVec + (n & 1) * 128 + 64 + 32 * h;
+      // The vectors arrive with Q's own half; its buffer is refilled only after dK of this
+      // step, which needs every thread's dS, so the refill cannot overtake this wait.
+      if (!mbar_wait_warp(&bars.qn_full[n & 1], (n >> 1) & 1, wt)) { ok = false; break; }
+      if (!mbar_wait_warp(&bars.s_full, n & 1, wt)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sv[64];
-      tmem_ld32(tmem + lane_base + C::COL_S, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-      tmem_ld32(tmem + lane_base + C::COL_S + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      uint32_t sv[32];
+      tmem_ld32(tmem + lane_off + C::COL_S + 32 * h, sv);
       tmem_ld_wait();
+      const bool need_mask = (p.causal && (qb + L.off < j * kBlockN + kBlockN - 1)) ||
+                             (j * kBlockN + kBlockN > L.len_kv);
+      int lim = p.causal ? kv_row - q0 - L.off : -(1 << 30);   // column c visible iff c >= lim
+      if (kv_row >= L.len_kv) lim = 1 << 30;
       const float2 sc2 = make_float2(bs.s_log2, bs.s_log2);
       // ALiBi: the key-row part of the bias (the column part is in the -LSE vector, relative
-      // to the 128-aligned block that holds this 64-row query block).
+      // to the 128-aligned block that holds this query block).
       const float kr = ALIBI ? alibi_slope_log2(p, hq) *
-                                   static_cast<float>(kv_row - (q0 / kBlockM) * kBlockM - L.off) : 0.f;
+                                   static_cast<float>(kv_row - (qb / kBlockM) * kBlockM - L.off) : 0.f;
       const float2 kr2 = make_float2(kr, kr);
-      uint4 bz[BIAS ? 8 : 1];
-      if constexpr (BIAS) load_bias_t(p, bi, hq, kv_row, q0, bz);
-      uint32_t pk[32];
+      float pf[32];                                      // every P (dS takes all of them)
+      uint32_t pk[16];                                   // dV's operand: the kept P
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        float2 nl = *reinterpret_cast<const float2*>(sVec + c);
+      for (int c = 0; c < 32; c += 2) {
+        float2 nl = *reinterpret_cast<const float2*>(nlse2 + c);
         if constexpr (ALIBI) nl = add2(nl, kr2);
         if constexpr (BIAS) nl = fma2(bias_pair<DT>(bz, c), make_float2(kLog2e, kLog2e), nl);
         const float2 x = fma2(make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sc2, nl);
@@ -1055,198 +1142,174 @@ __global__ void __launch_bounds__(160, 1) bwd_d256_kernel(const __grid_constant_
         pf[c] = p0;
         pf[c + 1] = p1;
         if constexpr (DROP) {
-          const uint32_t w = (c < 32) ? keep.x : keep.y;   // the pair: bits i and i + 16
-          pk[c / 2] = pack2((w >> ((c % 32) / 2)) & 1u ? p0 : 0.f, (w >> ((c % 32) / 2 + 16)) & 1u ? p1 : 0.f, DT);
+          // The pair's keep bits sit at bits c/2 and c/2 + 16 of the word.
+          pk[c / 2] = pack2((keep >> (c / 2)) & 1u ? p0 : 0.f, (keep >> (c / 2 + 16)) & 1u ? p1 : 0.f, DT);
         } else {
           pk[c / 2] = pack2(p0, p1, DT);
         }
       }
-      tmem_st32(tmem + lane_base + C::COL_S, pk);
+      tmem_st16(tmem + lane_off + C::COL_S + 32 * h, pk);
       tmem_st_wait();
       tc_fence_before();
-    }
-    ok = __syncthreads_and(w_ok);
-    if (!ok) break;
-    // ---- dV_h += Pᵀ·dO_h (runs while dS is computed) ----
-    const uint32_t idesc_acc = make_idesc(fmt, 128, 128, false, true);
-    if (threadIdx.x == kIssuer) {
+      mbar_arrive(&bars.p_full);
+      // ---- dSᵀ = Pᵀ ∘ (dPᵀ − Delta) ----
+      if (!mbar_wait_warp(&bars.dp_full, n & 1, wt)) { ok = false; break; }
       tc_fence_after();
-      const uint32_t gh = smem_u32(sdO) + dh * 2 * 8192;
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ts(tmem + C::COL_DV, tmem + C::COL_S + k * 8, make_sdesc_sw128(gh + k * 2048, 8192, 1024),
-               idesc_acc, (n > 0 || k > 0) ? 1u : 0u, false);
-    }
-    // ---- dS = P ∘ (dPᵀ − Delta) for key row r, to shared memory ----
-    w_ok = mbar_wait(&bars.dp_done, ph_mma, wt);
-    // The Sᵀ and dPᵀ MMAs are done: the other d-half of Q and dO may be refilled.
-    if (threadIdx.x == kIssuer && w_ok && n + 1 < n_iter) load_far(n + 1);
-    if (w_ok && compute) {
-      tc_fence_after();
-      uint32_t dpv[64];
-      tmem_ld32(tmem + lane_base + C::COL_DP, *reinterpret_cast<uint32_t(*)[32]>(&dpv[0]));
-      tmem_ld32(tmem + lane_base + C::COL_DP + 32, *reinterpret_cast<uint32_t(*)[32]>(&dpv[32]));
+      tmem_ld32(tmem + lane_off + C::COL_DP + 32 * h, sv);
       tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(&bars.dp_consumed);
       const float2 rk2 = make_float2(bs.dp, bs.dp);
       // Both d-halves compute the same dS: the first half alone adds it to the bias gradient.
       float* dbrow = (DBIAS && dh == 0) ? dbias_row(p, bi, hq, kv_row, q0) : nullptr;
       float2 dbhold = make_float2(0.f, 0.f);
-      uint32_t ds[32];
+      uint32_t ds[16];
 #pragma unroll
-      for (int c = 0; c < 64; c += 2) {
-        float2 dp = make_float2(__uint_as_float(dpv[c]), __uint_as_float(dpv[c + 1]));
-        const float2 nd = *reinterpret_cast<const float2*>(sVec + 64 + c);
+      for (int c = 0; c < 32; c += 2) {
+        float2 dp = make_float2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1]));
+        const float2 nd = *reinterpret_cast<const float2*>(ndelta + c);
         if constexpr (DROP) {
           // dS = P * (keep / (1 - p) * dO·Vᵀ - Delta) takes every P.
-          const uint32_t w = (c < 32) ? keep.x : keep.y;
-          dp.x = (w >> ((c % 32) / 2)) & 1u ? dp.x : 0.f;
-          dp.y = (w >> ((c % 32) / 2 + 16)) & 1u ? dp.y : 0.f;
+          dp.x = (keep >> (c / 2)) & 1u ? dp.x : 0.f;
+          dp.y = (keep >> (c / 2 + 16)) & 1u ? dp.y : 0.f;
         }
         const float2 dd = mul2(make_float2(pf[c], pf[c + 1]), fma2(dp, rk2, nd));
         ds[c / 2] = pack2(dd.x, dd.y, DT);
         if constexpr (DBIAS) dbias_emit(dbrow, c, dd, dbhold);
       }
+      // dS row r (128 bytes, 128-byte swizzled), this half in 16-byte units 4h..4h+3: read
+      // K-major as dK's A operand and MN-major as dQᵀ's B operand.  The buffer is free once
+      // the previous step's dQᵀ has left it.
+      if (n > 0 && !mbar_wait_warp(&bars.ds_free, (n - 1) & 1, wt)) { ok = false; break; }
       uint8_t* rowp = sDS + r * 128;
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) =
+      for (int u = 0; u < 4; ++u)
+        *reinterpret_cast<uint4*>(rowp + (((4 * h + u) ^ (r & 7)) * 16)) =
             make_uint4(ds[u * 4], ds[u * 4 + 1], ds[u * 4 + 2], ds[u * 4 + 3]);
       fence_proxy_async_smem();
-      tc_fence_before();
+      mbar_arrive(&bars.ds_full);
     }
-    ok = __syncthreads_and(w_ok);
-    if (!ok) break;
-    // ---- dK_h += dSᵀ·Q_h, dQᵀ_h = K_hᵀ·dSᵀ ----
-    if (threadIdx.x == kIssuer) {
-      tc_fence_after();
-      const uint32_t idesc_dq = make_idesc(fmt, 128, C::BQ, true, true);
-      const uint32_t qh = smem_u32(sQ) + dh * 2 * 8192;
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_ss(tmem + C::COL_DK, make_sdesc_sw128(smem_u32(sDS) + k * 32, 16, 1024),
-               make_sdesc_sw128(qh + k * 2048, 8192, 1024), idesc_acc, (n > 0 || k > 0) ? 1u : 0u,
-               false);
-#pragma unroll
-      for (int k = 0; k < 8; ++k)
-        mma_ss(tmem + C::COL_DQ, make_sdesc_sw128(smem_u32(sK) + dh * 2 * 16384 + k * 2048, 16384, 1024),
-               make_sdesc_sw128(smem_u32(sDS) + k * 2048, 8192, 1024), idesc_dq, k > 0, false);
-      tc_commit(&bars.mma_done);
-    }
-    ok = __syncthreads_and(mbar_wait(&bars.mma_done, ph_mma, wt));
-    ph_mma ^= 1;
-    if (!ok) break;
+    // ---- epilogue: dV_h (h = 0) or dK_h (h = 1) ----
+    ok = ok && mbar_wait_warp(&bars.acc_full, 0, wt);
+    uint8_t* stage = sQF + h * 32768;                     // Q and dO buffers: all read by now
     tc_fence_after();
-    // Every MMA of this step has read Q, dO and dS, and the vectors were read above: the
-    // rest of the next step's tiles may land while dQᵀ is drained.
-    if (threadIdx.x == kIssuer && n + 1 < n_iter) load_near(n + 1);
-    // ---- dQᵀ: row r of this half of d, 64 query columns as two 32-column chunks, staged
-    // in the staging buffer and in the (now free) dS buffer ----
-    if (compute) {
+    const uint32_t acc = tmem + lane_off + (h == 0 ? C::COL_DV : C::COL_DK);
+    const float mul = (h == 0) ? bs.dv : bs.dk;
+    if (ok && p.kv_split > 1) {
+      if (n_iter > 0) {
+        float* dst = (h == 0 ? p.dv_acc : p.dk_acc) +
+                     ((static_cast<int64_t>(bi) * p.h_kv + hk) * p.s_kv_pad + kv_row) * 256 + dh * 128;
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(acc + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            red_add_v4(dst + c * 32 + u * 4, __uint_as_float(v[u * 4]) * mul,
+                       __uint_as_float(v[u * 4 + 1]) * mul, __uint_as_float(v[u * 4 + 2]) * mul,
+                       __uint_as_float(v[u * 4 + 3]) * mul);
+        }
+      }
+    } else if (ok) {
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t v[64];
+        if (n_iter > 0) {
+          tmem_ld32(acc + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          tmem_ld32(acc + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) v[i] = 0u;
+        }
+        uint8_t* rowp = stage + c * 16384 + r * 128;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          uint4 w;
+          w.x = pack2(__uint_as_float(v[u * 8 + 0]) * mul, __uint_as_float(v[u * 8 + 1]) * mul, DT);
+          w.y = pack2(__uint_as_float(v[u * 8 + 2]) * mul, __uint_as_float(v[u * 8 + 3]) * mul, DT);
+          w.z = pack2(__uint_as_float(v[u * 8 + 4]) * mul, __uint_as_float(v[u * 8 + 5]) * mul, DT);
+          w.w = pack2(__uint_as_float(v[u * 8 + 6]) * mul, __uint_as_float(v[u * 8 + 7]) * mul, DT);
+          *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) = w;
+        }
+      }
+      fence_proxy_async_smem();
+    }
+    // Every thread of the warpgroup arrives exactly once.
+    mbar_arrive(&bars.epi_ready[h]);
+    if (r == 0) {
+      const bool all_ok = mbar_wait(&bars.epi_ready[h], 0, wt) && ok && !*abort_flag;
+      if (all_ok && p.kv_split == 1) {
+        const CUtensorMap* map = (h == 0) ? &p.tm_dv : &p.tm_dk;
+        for (int c = 0; c < 2; ++c)
+          tma_store_4d(map, stage + c * 16384, (dh * 2 + c) * 64, j * kBlockN, hk, bi);
+        tma_store_commit();
+        tma_store_wait_read_all();
+      }
+    }
+  } else if (warp >= 12) {
+    // ===================== dQᵀ drain: TMEM -> shared memory -> TMA reduce-add ==========
+    // Row r of this half of d, 64 query columns, read at once (TMEM is then free for the
+    // next dQᵀ) and sent as two 32-column chunks through the dS buffer.
+    const int quad = warp % 4;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
+    bool ok = true;
+    for (int n = 0; n < n_iter && ok; ++n) {
+      const int hq = iter_head(n), q0 = iter_q0(n);
+      const int drow = (bi * p.h_q + hq) * 256 + dh * 128;
+      if (!mbar_wait_warp(&bars.dq_full, n & 1, wt)) { ok = false; break; }
+      tc_fence_after();
       uint32_t v[64];
-      tmem_ld32(tmem + lane_base + C::COL_DQ, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-      tmem_ld32(tmem + lane_base + C::COL_DQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+      tmem_ld32(tmem + lane_off + C::COL_DQ, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+      tmem_ld32(tmem + lane_off + C::COL_DQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       tmem_ld_wait();
       tc_fence_before();
 #pragma unroll
-      for (int ch = 0; ch < 2; ++ch) {
-        uint8_t* rowp = (ch == 0 ? sST : sDS) + r * 128;
+      for (int ch = 0; ch < 2 && ok; ++ch) {
+        // Chunk 1 waits until the reduce-add of chunk 0 has read the buffer (one phase of
+        // stage_free per step).
+        if (ch == 1 && !mbar_wait_warp(&bars.stage_free, n & 1, wt)) { ok = false; break; }
+        uint8_t* rowp = sDS + r * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
           *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) =
               make_uint4(v[ch * 32 + u * 4], v[ch * 32 + u * 4 + 1], v[ch * 32 + u * 4 + 2],
                          v[ch * 32 + u * 4 + 3]);
+        fence_proxy_async_smem();
+        mbar_arrive(&bars.stage_full);                    // phase 2n + ch
+        bool issued = true;
+        if (r == 0) {
+          issued = mbar_wait(&bars.stage_full, ch, wt);
+          if (issued) {
+            tma_reduce_add_2d(&p.tm_dqacc, sDS, q0 + 32 * ch, drow);
+            tma_store_commit();
+            bulk_wait_read<0>();
+            mbar_arrive(ch == 0 ? &bars.stage_free : &bars.ds_free);
+          }
+        }
+        ok = __all_sync(0xffffffffu, issued) != 0;        // warp-uniform, for the waits above
       }
-      fence_proxy_async_smem();
     }
-    __syncthreads();
-    if (threadIdx.x == kIssuer) {
-      const int drow = (bi * p.h_q + hq) * 256 + dh * 128;
-      tma_reduce_add_2d(&p.tm_dqacc, sST, q0, drow);
-      tma_reduce_add_2d(&p.tm_dqacc, sDS, q0 + 32, drow);
-      tma_store_commit();
-    }
-  }
-  if (threadIdx.x == kIssuer) {
-    bulk_wait_read<0>();
-    tma_store_wait_all();
-    if (!ok) {
-      // A role gave up: let every MMA and copy this thread issued finish before TMEM and
-      // shared memory are released.
-      tc_commit(&bars.drain);
-      mbar_wait_drain(&bars.drain, 0);
-      mbar_wait_drain(&bars.kv_full, 0);
-      if (n_far > 0) mbar_wait_drain(&bars.ld_far, (n_far - 1) & 1);
-      if (n_near > 0) mbar_wait_drain(&bars.ld_near, (n_near - 1) & 1);
+    if (r == 0) {
+      bulk_wait_read<0>();
+      tma_store_wait_all();
     }
   }
 
-  // ---- epilogue: this half of dV and dK ----
-  tc_fence_after();
-  if (ok) {
-    const uint32_t acc_v = tmem + lane_base + C::COL_DV, acc_k = tmem + lane_base + C::COL_DK;
-    if (p.kv_split > 1) {
-      if (n_iter > 0 && compute) {
-        float* dvp = p.dv_acc + ((static_cast<int64_t>(bi) * p.h_kv + hk) * p.s_kv_pad + kv_row) * 256 + dh * 128;
-        float* dkp = p.dk_acc + ((static_cast<int64_t>(bi) * p.h_kv + hk) * p.s_kv_pad + kv_row) * 256 + dh * 128;
-        for (int c = 0; c < 4; ++c) {
-          uint32_t a[32], k2[32];
-          tmem_ld32(acc_v + c * 32, a);
-          tmem_ld32(acc_k + c * 32, k2);
-          tmem_ld_wait();
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            red_add_v4(dvp + c * 32 + u * 4, __uint_as_float(a[u * 4]) * bs.dv,
-                       __uint_as_float(a[u * 4 + 1]) * bs.dv, __uint_as_float(a[u * 4 + 2]) * bs.dv,
-                       __uint_as_float(a[u * 4 + 3]) * bs.dv);
-            red_add_v4(dkp + c * 32 + u * 4, __uint_as_float(k2[u * 4]) * bs.dk,
-                       __uint_as_float(k2[u * 4 + 1]) * bs.dk, __uint_as_float(k2[u * 4 + 2]) * bs.dk,
-                       __uint_as_float(k2[u * 4 + 3]) * bs.dk);
-          }
-        }
-      }
-    } else {
-      // dV_h -> sQ, dK_h -> sdO as two 64-column chunks (128 rows x 128 bytes) each.
-      for (int which = 0; which < 2 && compute; ++which) {
-        uint8_t* stage = which == 0 ? sQ : sdO;
-        const uint32_t acc = which == 0 ? acc_v : acc_k;
-        const float mul = which == 0 ? bs.dv : bs.dk;
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[64];
-          if (n_iter > 0) {
-            tmem_ld32(acc + c * 64, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-            tmem_ld32(acc + c * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
-            tmem_ld_wait();
-          } else {
-#pragma unroll
-            for (int i = 0; i < 64; ++i) v[i] = 0u;
-          }
-          uint8_t* rowp = stage + c * 16384 + r * 128;
-#pragma unroll
-          for (int u = 0; u < 8; ++u) {
-            uint4 w;
-            w.x = pack2(__uint_as_float(v[u * 8 + 0]) * mul, __uint_as_float(v[u * 8 + 1]) * mul, DT);
-            w.y = pack2(__uint_as_float(v[u * 8 + 2]) * mul, __uint_as_float(v[u * 8 + 3]) * mul, DT);
-            w.z = pack2(__uint_as_float(v[u * 8 + 4]) * mul, __uint_as_float(v[u * 8 + 5]) * mul, DT);
-            w.w = pack2(__uint_as_float(v[u * 8 + 6]) * mul, __uint_as_float(v[u * 8 + 7]) * mul, DT);
-            *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) = w;
-          }
-        }
-      }
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (threadIdx.x == kIssuer) {
-        for (int c = 0; c < 2; ++c) {
-          tma_store_4d(&p.tm_dv, sQ + c * 16384, (dh * 2 + c) * 64, j * kBlockN, hk, bi);
-          tma_store_4d(&p.tm_dk, sdO + c * 16384, (dh * 2 + c) * 64, j * kBlockN, hk, bi);
-        }
-        tma_store_commit();
-        tma_store_wait_read_all();
-      }
-    }
-  }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  // Every role is done.  If one gave up, copies the producer issued may still be in flight:
+  // let them land before the CTA's shared memory is released.
+  if (producer && *abort_flag) {
+    mbar_wait_drain(&bars.kv_full, 0);
+    if (n_qf > 0) mbar_wait_drain(&bars.qf_full, (n_qf - 1) & 1);
+    for (int m = (n_qn > 2 ? n_qn - 2 : 0); m < n_qn; ++m) mbar_wait_drain(&bars.qn_full[m & 1], (m >> 1) & 1);
+    if (n_df > 0) mbar_wait_drain(&bars.df_full, (n_df - 1) & 1);
+    if (n_dn > 0) mbar_wait_drain(&bars.dn_full, (n_dn - 1) & 1);
+  }
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -1300,7 +1363,7 @@ cudaError_t launch_d256(const BwdParams& p, cudaStream_t st) {
   e = set_smem_once(reinterpret_cast<const void*>(kern), D256::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const unsigned grid = 2u * p.b * p.h_kv * p.kv_split * ((p.s_kv + kBlockN - 1) / kBlockN);
-  kern<<<grid, 160, D256::SMEM_BYTES, st>>>(p);
+  kern<<<grid, D256::THREADS, D256::SMEM_BYTES, st>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 gdq(p.s_q_pad / 32, 256 / 32, bh);
