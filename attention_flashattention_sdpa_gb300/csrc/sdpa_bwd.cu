@@ -905,14 +905,23 @@ __global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant_
   const int warp = threadIdx.x / 32;
   const int lane = threadIdx.x % 32;
 
-  // Launch order: the two d-halves of a unit side by side, units fastest, KV blocks slowest
-  // (for causal, the first KV blocks carry the most query blocks and go first).
+  // Launch order: the two d-halves of a KV block side by side; units (batch, KV head, share)
+  // in groups whose Q and dO together take about 32 MB, so that resident CTAs share them in
+  // L2; within a group the heaviest KV blocks of all its units first (for causal, the first
+  // blocks), then the next block index.  Units of 8 MB or more go one at a time.
   const int dh = blockIdx.x & 1;                 // own d-half: chunks 2dh, 2dh + 1
   const int fh = 1 - dh;                         // the other half
   const int rest = blockIdx.x >> 1;
   const int units = p.b * p.h_kv * p.kv_split;
-  const int unit = rest % units;
-  const int j = rest / units;
+  const int n_kvb = (p.s_kv + kBlockN - 1) / kBlockN;
+  const long long unit_bytes = 4ll * p.heads_per_split * p.s_q_pad * 256;
+  int G = static_cast<int>((32ll << 20) / (unit_bytes > 0 ? unit_bytes : 1));
+  G = (unit_bytes >= (8ll << 20) || G < 1) ? 1 : (G > units ? units : G);
+  const int grp = rest / (G * n_kvb);
+  const int gsz = min(G, units - grp * G);
+  const int grem = rest - grp * G * n_kvb;
+  const int j = grem / gsz;                      // KV block
+  const int unit = grp * G + grem % gsz;
   const int split = unit % p.kv_split;
   const int bhk = unit / p.kv_split;
   const int bi = bhk / p.h_kv;
