@@ -854,9 +854,10 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
 // warpgroup drains dQᵀ.  Per step the MMAs run Sᵀ, dPᵀ, dV += Pᵀ·dO, then the next step's
 // Sᵀ while dS is computed, then dK += dSᵀ·Q and dQᵀ.  The own d-half of Q is double-buffered
 // (the next step's lands while this step's dK still reads it); the far half of Q and both
-// halves of dO are refilled as soon as the MMAs that read them are done.  dQᵀ leaves through
-// the dS buffer (two 32-column fp32 chunks, each a TMA reduce-add), which then takes the
-// next step's dS.
+// halves of dO are refilled as soon as the MMAs that read them are done.  Half of dQᵀ (32
+// fp32 columns) leaves through the dS buffer as one TMA reduce-add, which then takes the
+// next step's dS; the other half goes from registers as vector reductions at the same time
+// (the dS buffer holds one chunk, and TMA reduce-adds of one SM drain at a bounded rate).
 struct D256 {
   static constexpr int BQ = 64;                  // query rows per step
   static constexpr int OFF_K = 0;                // 128 x 256: four 16 KB chunks of 64 columns
@@ -875,7 +876,7 @@ static_assert(D256::SMEM_BYTES <= 232448, "shared memory budget");
 
 struct alignas(8) D256Barriers {
   uint64_t kv_full, qf_full, qf_empty, qn_full[2], qn_empty[2], df_full, df_empty, dn_full, dn_empty;
-  uint64_t s_full, p_full, dp_full, dp_consumed, ds_full, dq_full, ds_free, stage_full, stage_free;
+  uint64_t s_full, p_full, dp_full, dp_consumed, ds_full, dq_full, ds_free, stage_full;
   uint64_t acc_full, drain, epi_ready[2];
   uint32_t tmem_base;
   int abort;
@@ -958,7 +959,6 @@ __global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant_
     mbar_init(&bars.dq_full, 1);
     mbar_init(&bars.ds_free, 1);
     mbar_init(&bars.stage_full, 128);
-    mbar_init(&bars.stage_free, 1);
     mbar_init(&bars.acc_full, 1);
     mbar_init(&bars.drain, 1);
     bars.abort = 0;
@@ -1258,9 +1258,9 @@ __global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant_
       }
     }
   } else if (warp >= 12) {
-    // ===================== dQᵀ drain: TMEM -> shared memory -> TMA reduce-add ==========
+    // ===================== dQᵀ drain: TMEM -> fp32 accumulator =======================
     // Row r of this half of d, 64 query columns, read at once (TMEM is then free for the
-    // next dQᵀ) and sent as two 32-column chunks through the dS buffer.
+    // next dQᵀ).
     const int quad = warp % 4;
     const int r = quad * 32 + lane;
     const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
@@ -1275,30 +1275,32 @@ __global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant_
       tmem_ld32(tmem + lane_off + C::COL_DQ + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
       tmem_ld_wait();
       tc_fence_before();
-#pragma unroll
-      for (int ch = 0; ch < 2 && ok; ++ch) {
-        // Chunk 1 waits until the reduce-add of chunk 0 has read the buffer (one phase of
-        // stage_free per step).
-        if (ch == 1 && !mbar_wait_warp(&bars.stage_free, n & 1, wt)) { ok = false; break; }
+      // Columns 0..31 leave through the dS buffer as one TMA reduce-add; columns 32..63 go
+      // straight from registers as vector reductions, while the first chunk is read.
+      {
         uint8_t* rowp = sDS + r * 128;
 #pragma unroll
         for (int u = 0; u < 8; ++u)
           *reinterpret_cast<uint4*>(rowp + ((u ^ (r & 7)) * 16)) =
-              make_uint4(v[ch * 32 + u * 4], v[ch * 32 + u * 4 + 1], v[ch * 32 + u * 4 + 2],
-                         v[ch * 32 + u * 4 + 3]);
+              make_uint4(v[u * 4], v[u * 4 + 1], v[u * 4 + 2], v[u * 4 + 3]);
         fence_proxy_async_smem();
-        mbar_arrive(&bars.stage_full);                    // phase 2n + ch
+        mbar_arrive(&bars.stage_full);                    // phase n
+        float* dst = p.dq_acc + (static_cast<int64_t>(drow) + r) * p.s_q_pad + q0 + 32;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          red_add_v4(dst + u * 4, __uint_as_float(v[32 + u * 4]), __uint_as_float(v[32 + u * 4 + 1]),
+                     __uint_as_float(v[32 + u * 4 + 2]), __uint_as_float(v[32 + u * 4 + 3]));
         bool issued = true;
         if (r == 0) {
-          issued = mbar_wait(&bars.stage_full, ch, wt);
+          issued = mbar_wait(&bars.stage_full, n & 1, wt);
           if (issued) {
-            tma_reduce_add_2d(&p.tm_dqacc, sDS, q0 + 32 * ch, drow);
+            tma_reduce_add_2d(&p.tm_dqacc, sDS, q0, drow);
             tma_store_commit();
             bulk_wait_read<0>();
-            mbar_arrive(ch == 0 ? &bars.stage_free : &bars.ds_free);
+            mbar_arrive(&bars.ds_free);
           }
         }
-        ok = __all_sync(0xffffffffu, issued) != 0;        // warp-uniform, for the waits above
+        ok = __all_sync(0xffffffffu, issued) != 0;
       }
     }
     if (r == 0) {
