@@ -870,7 +870,10 @@ struct D256 {
   static constexpr int OFF_BAR = OFF_VEC + 1024;
   static constexpr int SMEM_BYTES = OFF_BAR + 256;
   static constexpr int THREADS = 512;
-  static constexpr int COL_S = 0, COL_DP = 64, COL_DQ = 128, COL_DV = 256, COL_DK = 384;
+  // Sᵀ/Pᵀ alternates between two regions by step parity, so the next step's Sᵀ never
+  // overwrites the Pᵀ that this step's dV MMAs read.
+  static constexpr int COL_S0 = 0, COL_DP = 64, COL_DQ = 128, COL_S1 = 192, COL_DV = 256, COL_DK = 384;
+  static constexpr int col_s(int n) { return (n & 1) ? COL_S1 : COL_S0; }
 };
 static_assert(D256::SMEM_BYTES <= 232448, "shared memory budget");
 
@@ -1038,7 +1041,7 @@ __global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant_
         for (int k = 0; k < 16; ++k) {
           const int c = k / 4;
           const uint32_t b = ((c >> 1) == dh ? qn + (c - 2 * dh) * 8192 : qF + (c - 2 * fh) * 8192) + (k % 4) * 32;
-          mma_ss(tmem + C::COL_S, make_sdesc_sw128(kA + c * 16384 + (k % 4) * 32, 16, 1024),
+          mma_ss(tmem + C::col_s(m), make_sdesc_sw128(kA + c * 16384 + (k % 4) * 32, 16, 1024),
                  make_sdesc_sw128(b, 16, 1024), idesc_s, k > 0, false);
         }
         tc_commit(&bars.s_full);
@@ -1069,11 +1072,11 @@ __global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant_
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const uint32_t a_col = (k < 2) ? k * 8 : 32 + (k - 2) * 8;
-          mma_ts(tmem + C::COL_DV, tmem + C::COL_S + a_col, make_sdesc_sw128(gh + k * 2048, 8192, 1024),
+          mma_ts(tmem + C::COL_DV, tmem + C::col_s(n) + a_col, make_sdesc_sw128(gh + k * 2048, 8192, 1024),
                  idesc_acc, (n > 0 || k > 0) ? 1u : 0u, false);
         }
         tc_commit(&bars.dn_empty);
-        // ---- the next step's Sᵀ (region S is free: Pᵀ was read by the dV MMAs above) ----
+        // ---- the next step's Sᵀ, into the other Sᵀ region ----
         if (n + 1 < n_iter && !issue_s(n + 1)) { ok = false; break; }
         // ---- dK_h += dSᵀ·Q_h, then dQᵀ_h = K_hᵀ·dSᵀ ----
         if (!mbar_wait(&bars.ds_full, n & 1, wt)) { ok = false; break; }
@@ -1123,7 +1126,7 @@ __global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant_
       if (!mbar_wait_warp(&bars.s_full, n & 1, wt)) { ok = false; break; }
       tc_fence_after();
       uint32_t sv[32];
-      tmem_ld32(tmem + lane_off + C::COL_S + 32 * h, sv);
+      tmem_ld32(tmem + lane_off + C::col_s(n) + 32 * h, sv);
       tmem_ld_wait();
       const bool need_mask = (p.causal && (qb + L.off < j * kBlockN + kBlockN - 1)) ||
                              (j * kBlockN + kBlockN > L.len_kv);
@@ -1157,7 +1160,7 @@ __global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant_
           pk[c / 2] = pack2(p0, p1, DT);
         }
       }
-      tmem_st16(tmem + lane_off + C::COL_S + 32 * h, pk);
+      tmem_st16(tmem + lane_off + C::col_s(n) + 32 * h, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(&bars.p_full);
