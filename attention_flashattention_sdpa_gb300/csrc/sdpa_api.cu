@@ -343,6 +343,26 @@ sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const void* k, co
   if ((st = make_map(&prm.tm_k, "k", k, p->k, p->b, p->h_kv, p->s_kv, p->d, p->in_dtype, 128)) != SDPA_OK) return st;
   if ((st = make_map(&prm.tm_v, "v", v, p->v, p->b, p->h_kv, p->s_kv, p->d, p->in_dtype, 128)) != SDPA_OK) return st;
   if ((st = make_map(&prm.tm_o, "o", o, p->o, p->b, p->h_q, p->s_q, p->d, p->out_dtype, 128)) != SDPA_OK) return st;
+  if (p->bias != nullptr && p->d <= 128) {
+    // Bias tiles for the forward kernel: [nb][nh][s_q][s_kv] (broadcast dimensions have size
+    // 1), boxes of 128 rows x 64 keys (128 bytes), 128-byte swizzle.
+    auto fn = encode_fn();
+    if (fn == nullptr) return fail(SDPA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const sdpa_strides_t& bs = p->bias_strides;
+    const int64_t nb = bs.b == 0 ? 1 : p->b, nh = bs.h == 0 ? 1 : p->h_q;
+    const int64_t row = p->s_q > 1 ? bs.s * 2 : ((int64_t)p->s_kv * 2 + 15) / 16 * 16;
+    const int64_t head = nh > 1 ? bs.h * 2 : ((int64_t)p->s_q * row + 15) / 16 * 16;
+    const int64_t batch = nb > 1 ? bs.b * 2 : ((int64_t)nh * head + 15) / 16 * 16;
+    cuuint64_t dims[4] = {(cuuint64_t)p->s_kv, (cuuint64_t)p->s_q, (cuuint64_t)nh, (cuuint64_t)nb};
+    cuuint64_t strides[3] = {(cuuint64_t)row, (cuuint64_t)head, (cuuint64_t)batch};
+    cuuint32_t box[4] = {64, 128, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(&prm.tm_bias, map_dtype(p->in_dtype), 4, const_cast<void*>(p->bias), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(SDPA_ERR_LAYOUT, "bias: cuTensorMapEncodeTiled rejected the view (CUresult %d)", (int)r);
+  }
   prm.lse = lse;
   prm.descale_q = p->descale_q;
   prm.descale_k = p->descale_k;
@@ -369,6 +389,9 @@ sdpa_status_t sdpa_fwd(const sdpa_problem_t* p, const void* q, const void* k, co
   prm.wait_limit = wait_limit_cycles();
   const bool plain = !prm.alibi && !prm.drop_rows && !prm.bias;
   prm.one_tile = sdpa::fwd_prefer_one_tile(p->b, p->h_q, p->s_q, p->d, p->in_dtype, plain, num_sms()) ? 1 : 0;
+  // With d <= 128 the bias instances run one Q tile per CTA (their bias tiles take the shared
+  // memory of a second one).
+  if (p->bias != nullptr && p->d <= 128) prm.one_tile = 1;
   // SDPA_FWD_Q_TILES=1 or 2 overrides the choice where both schedules exist (plain 16-bit,
   // d <= 128): a switch for testing and tuning.
   if (const char* qt = std::getenv("SDPA_FWD_Q_TILES")) {

@@ -40,7 +40,7 @@ __device__ __forceinline__ float2 unpack16x2(uint32_t w, int dt) {
   return __half22float2(*reinterpret_cast<const __half2*>(&w));
 }
 
-template <int D, int DT, bool ONE = false, bool PERSIST = false>
+template <int D, int DT, bool ONE = false, bool PERSIST = false, bool TMA_BIAS = false>
 struct FwdCfg {
   static constexpr int ES = (DT == kE4M3) ? 1 : 2;               // input element bytes
   static constexpr int NQT = (!ONE && D <= 128) ? 2 : 1;         // Q tiles per work unit
@@ -55,15 +55,19 @@ struct FwdCfg {
   // (unless those are smaller: E4M3 inputs) and one Q tile in the K/V ring.
   static constexpr bool OWN_STAGE = PERSIST || (NQT == 2 && TILE_BYTES < OUT_TILE);
   static constexpr int STAGE_BYTES = OWN_STAGE ? NQT * OUT_TILE : 0;
+  // Additive bias (one Q tile, d <= 128): two stages of the 128 x 128 bias tile of a key
+  // block, loaded by TMA as two 64-key halves (one per softmax warpgroup).
+  static constexpr int BIAS_STAGE = kBlockM * kBlockN * 2;
+  static constexpr int BIAS_BYTES = TMA_BIAS ? 2 * BIAS_STAGE : 0;
   // Shared memory: the per-SM limit (227 KB) less the static arrays (the barriers, and with
   // one Q tile the column halves' exchange arrays) and the 1 KB alignment slack.
   static constexpr int STATIC_BYTES = NQT == 2 ? 512 : 3584;
   static constexpr int RING_BUDGET =
-      (PERSIST ? 232448 - STATIC_BYTES - 1024 : 196608) - Q_BYTES - STAGE_BYTES;
+      (PERSIST ? 232448 - STATIC_BYTES - 1024 : 196608) - Q_BYTES - STAGE_BYTES - BIAS_BYTES;
   static constexpr int NS = (RING_BUDGET / TILE_BYTES) > 8 ? 8 : (RING_BUDGET / TILE_BYTES);
   static constexpr int RING_BYTES = NS * TILE_BYTES;
   static constexpr int OUT_TILE_BYTES = kBlockM * D * 2;          // 16-bit output tile
-  static constexpr int SMEM_BYTES = Q_BYTES + RING_BYTES + STAGE_BYTES + 1024 /*align slack*/;
+  static constexpr int SMEM_BYTES = Q_BYTES + RING_BYTES + STAGE_BYTES + BIAS_BYTES + 1024 /*align slack*/;
   // Two softmax warpgroups: one per Q tile, or, with one Q tile, one per half of the 128
   // score columns of a key block.
   static constexpr int THREADS = 384;
@@ -77,6 +81,7 @@ struct FwdCfg {
   static constexpr float THRESH = (DT == kE4M3) ? 0.8f : 8.0f;    // lazy-rescale threshold
   static constexpr float P_OFFSET = (DT == kE4M3) ? 8.0f : 0.0f;  // P scaled by 2^8 for E4M3
   static_assert(NS >= 2, "K/V ring needs at least two slots");
+  static_assert(!TMA_BIAS || (NQT == 1 && !PERSIST && D <= 128), "bias tiles: one Q tile, d <= 128");
   static_assert(SMEM_BYTES + STATIC_BYTES <= 232448, "shared memory budget");
   static_assert(O_COL0 + NQT * D <= 512, "TMEM budget");
   static_assert(OWN_STAGE || NQT == 2 || OUT_TILE_BYTES <= RING_BYTES, "epilogue staging");
@@ -97,6 +102,8 @@ struct alignas(8) FwdBarriers {
   uint64_t epi_ready[2];
   uint64_t mx_ready[2];   // column halves: row-max candidates exchanged (per block parity)
   uint64_t l_ready;       // column halves: row sums exchanged (once per unit)
+  uint64_t bias_full[2];  // bias tile of a key block landed (by stage)
+  uint64_t bias_empty[2]; // both softmax warpgroups have read it
   uint32_t tmem_base;
   int abort;
 };
@@ -137,10 +144,14 @@ template <int D, int DT, int OUT_DT, int FEAT>
 __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
     sdpa_fwd_kernel(const __grid_constant__ FwdParams p) {
   constexpr bool PERSIST = (FEAT & kFeatPersist) != 0;
-  using C = FwdCfg<D, DT, (FEAT & kFeatOneTile) != 0, PERSIST>;
+  constexpr bool BIAS = (FEAT & kFeatBias) != 0;
+  // d <= 128: the bias reaches the softmax threads as TMA tiles in shared memory (coalesced
+  // bulk copies; per-thread row loads of 16 bytes kept the L1 pipeline ~80% busy).  d = 256
+  // has no room for them and loads its rows per thread.
+  constexpr bool TMA_BIAS = BIAS && D <= 128;
+  using C = FwdCfg<D, DT, (FEAT & kFeatOneTile) != 0, PERSIST, TMA_BIAS>;
   constexpr bool ALIBI = (FEAT & kFeatAlibi) != 0;
   constexpr bool DROP = (FEAT & kFeatDropout) != 0;
-  constexpr bool BIAS = (FEAT & kFeatBias) != 0;
   constexpr int NQT = C::NQT;
   constexpr int NS = C::NS;
   constexpr bool FP8 = (DT == kE4M3);
@@ -151,6 +162,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
   uint8_t* sQ = smem;
   uint8_t* sRing = smem + C::Q_BYTES;
   uint8_t* sStage = sRing + C::RING_BYTES;   // STAGE_BYTES of its own (OWN_STAGE only)
+  uint8_t* sBias = sStage + C::STAGE_BYTES;  // BIAS_BYTES (TMA_BIAS only)
   __shared__ FwdBarriers bars;
   // Column halves (one Q tile): per-row exchange of the row-max candidate (by block parity)
   // and, at the end of a unit, of the row sums.
@@ -229,6 +241,10 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
     mbar_init(&bars.mx_ready[0], 256);
     mbar_init(&bars.mx_ready[1], 256);
     mbar_init(&bars.l_ready, 256);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bars.bias_full[b], 1);
+      mbar_init(&bars.bias_empty[b], 256);
+    }
     bars.abort = 0;
     fence_mbar_init();
     // The first unit's Q tiles and first K block go out before the CTA's set-up (TMEM
@@ -260,7 +276,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
 
   // Copies the producer has issued (for the drain at the end, should a role give up).
   bool producer = false;
-  int q_issued = 0, kv_issued = 0;
+  int q_issued = 0, kv_issued = 0, bias_issued = 0;
 
   // Registers (384 threads, 168 each at launch): the producer / MMA warpgroup gives some to
   // the two softmax warpgroups, 88 + 2 x 200 <= 3 x 168; a bias row needs 8 more per softmax
@@ -315,6 +331,19 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
           kv_issued = ++it;
           return true;
         };
+        // The bias tile of key block j (rows of this unit's Q tile, 128 keys) into stage
+        // bias_issued % 2, as two 64-key halves.
+        auto load_bias = [&](int j) {
+          const int b = bias_issued & 1;
+          if (!mbar_wait(&bars.bias_empty[b], ((bias_issued >> 1) & 1) ^ 1, wt)) return false;
+          mbar_arrive_expect_tx(&bars.bias_full[b], C::BIAS_STAGE);
+          for (int c = 0; c < 2; ++c)
+            tma_load_4d(sBias + b * C::BIAS_STAGE + c * (C::BIAS_STAGE / 2), &p.tm_bias, &bars.bias_full[b],
+                        kv_block(j, nb) * kBlockN + 64 * c, w.m0, p.bias_sh != 0 ? w.hq : 0,
+                        p.bias_sb != 0 ? w.bi : 0);
+          ++bias_issued;
+          return true;
+        };
         if (NQT == 2) {
           for (int j = 0; j < nb && ok; ++j) {
             ok = load(&p.tm_k, j);
@@ -325,6 +354,7 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
           for (int j = 0; j < nb && ok; ++j) {
             if (j + 1 < nb) ok = load(&p.tm_k, j + 1);
             if (ok) ok = load(&p.tm_v, j);
+            if (TMA_BIAS && ok) ok = load_bias(j);
           }
         }
       }
@@ -516,7 +546,15 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
         // The bias of this row and key block, loaded before the scores arrive; the next key
         // block's part of the row is sent to L2 first, so those loads find it there.
         uint4 bz[BIAS ? SC / 8 : 1];
-        if constexpr (BIAS) {
+        if constexpr (TMA_BIAS) {
+          // This row's 64 keys of the key block's bias tile (128-byte rows, 128-byte swizzle).
+          const int bs = jg & 1;
+          if (!mbar_wait_warp(&bars.bias_full[bs], (jg >> 1) & 1, wt)) { ok = false; break; }
+          const uint8_t* rowp = sBias + bs * C::BIAS_STAGE + hc * (C::BIAS_STAGE / 2) + r * 128;
+#pragma unroll
+          for (int e = 0; e < SC / 8; ++e) bz[e] = *reinterpret_cast<const uint4*>(rowp + ((e ^ (r & 7)) * 16));
+          mbar_arrive(&bars.bias_empty[bs]);
+        } else if constexpr (BIAS) {
           if (bias_row != nullptr && j + 1 < n_blocks) {
             const int kn = kv_block(j + 1, n_blocks) * kBlockN + col0;
             if (kn + SC <= p.s_kv) {
@@ -775,6 +813,8 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
       for (int t = 0; t < NQT; ++t) mbar_wait_drain(&bars.q_full[t], (q_issued - 1) & 1);
     for (int k = (kv_issued > NS ? kv_issued - NS : 0); k < kv_issued; ++k)
       mbar_wait_drain(&bars.kv_full[k % NS], (k / NS) & 1);
+    for (int k = (bias_issued > 2 ? bias_issued - 2 : 0); k < bias_issued; ++k)
+      mbar_wait_drain(&bars.bias_full[k & 1], (k >> 1) & 1);
   }
   if (warp == 1) {
     tc_fence_after();
@@ -801,8 +841,14 @@ cudaError_t launch_t(const FwdParams& p, cudaStream_t st) {
     if (feat == kFeatAlibi) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatAlibi>;
     if (feat == kFeatDropout) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatDropout>;
     if (feat == (kFeatAlibi | kFeatDropout)) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatAlibi | kFeatDropout>;
-    if (feat == kFeatBias) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatBias>;
-    if (feat == (kFeatBias | kFeatDropout)) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatBias | kFeatDropout>;
+    // With d <= 128 the bias instances run one Q tile per CTA (the bias tiles take the
+    // shared memory of the second one; the caller sizes the grid accordingly).
+    constexpr int kBiasTile = D <= 128 ? kFeatOneTile : 0;
+    if (feat == kFeatBias) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatBias | kBiasTile>;
+    if (feat == (kFeatBias | kFeatDropout)) kern = sdpa_fwd_kernel<D, DT, OUT_DT, kFeatBias | kFeatDropout | kBiasTile>;
+    if constexpr (D <= 128) {
+      if (feat & kFeatBias) smem = FwdCfg<D, DT, true, false, true>::SMEM_BYTES;
+    }
   }
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), smem);
   if (e != cudaSuccess) return e;

@@ -20,6 +20,7 @@ enum DType : int { kF16 = 0, kBF16 = 1, kE4M3 = 2 };
 // 128-byte swizzled, box = (128 bytes of d, 128 rows, 1, 1).
 struct FwdParams {
   CUtensorMap tm_q, tm_k, tm_v, tm_o;
+  CUtensorMap tm_bias;        // bias tiles of 128 rows x 64 keys (bias with d <= 128), else unused
   float* lse;                 // [b][h_q][s_q] fp32 or nullptr
   const float* descale_q;     // E4M3 only
   const float* descale_k;
