@@ -342,6 +342,13 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
                         kv_block(j, nb) * kBlockN + 64 * c, w.m0, p.bias_sh != 0 ? w.hq : 0,
                         p.bias_sb != 0 ? w.bi : 0);
           ++bias_issued;
+          // The tiles two and three key blocks ahead start towards L2 (HBM latency is long
+          // against two 32 KB stages): j + 2 and j + 3 from the first block, then j + 3.
+          for (int a = (j == 0 ? 2 : 3); a <= 3; ++a)
+            if (j + a < nb)
+              for (int c = 0; c < 2; ++c)
+                tma_prefetch_4d(&p.tm_bias, kv_block(j + a, nb) * kBlockN + 64 * c, w.m0,
+                                p.bias_sh != 0 ? w.hq : 0, p.bias_sb != 0 ? w.bi : 0);
           return true;
         };
         if (NQT == 2) {
