@@ -83,6 +83,13 @@ def test_with_lengths_and_bottom_right():
     _case(w, 3, 1, seed=8, lq=[150, 40, 1], lkv=[270, 100, 63], bottom_right=True)
 
 
+@pytest.mark.parametrize("d", [64, 128])
+def test_single_query_row(d):
+    # One query row: the bias tile's rows beyond s_q come back zero and are never used.
+    w = Workload("t", 2, 2, 2, 1, 300, d, "bf16", backward=False)
+    _case(w, 2, 2, seed=12 + d, backward=False)
+
+
 def test_split_groups():
     w = Workload("t", 1, 16, 1, 512, 512, 64, "f16", causal=True, backward=True)
     _case(w, 1, 16, seed=9)

@@ -5,7 +5,8 @@ MMAs already issued are drained, tensor memory is freed) and report SDPA_ERR_TIM
 A child process shortens the bound to one SM cycle (SDPA_WAIT_LIMIT_CYCLES), so that every
 wait not already satisfied at its first test gives up (the waits for the first tiles of a
 normal problem do), and checks the status of the forward pass and of both backward kernels
-(d = 128 and d = 256) under SDPA_DEBUG_SYNC.  It
+(d = 128 and d = 256), of the forward pass with a bias tensor and of a forward pass on
+persistent CTAs, under SDPA_DEBUG_SYNC.  It
 then restores the default bound in the same process and checks that the same calls give
 correct results: the context is still usable."""
 import os
@@ -60,6 +61,37 @@ for d in (128, 256):
     dQ, dK, dV = oracle.backward(q64, k64, v64, do64, w.scale, True)
     for g, r, n in ((dq, dQ, "dQ"), (dk, dK, "dK"), (dv, dV, "dV")):
         assert_grad_close(f64(g), r, n)
+# Forward-only instances with waits of their own: TMA bias tiles (one Q tile per CTA) and
+# persistent CTAs walking several work units (b4 h12 s1024 d64: 192 units on the SMs).
+def fwd_only(w, x, bias=None):
+    q, k, v = to_dev(x.q), to_dev(x.k), to_dev(x.v)
+    o = torch.empty_like(q)
+    lse = torch.empty(w.b, w.h_q, w.s_q, device="cuda")
+    try:
+        m.sdpa_fwd(q, k, v, o, lse, attn_scale=w.scale, causal=True, bias=bias)
+        st = 0
+    except m.SdpaError as e:
+        st = e.status
+    torch.cuda.synchronize()
+    return st, o
+
+g = torch.Generator().manual_seed(7)
+wb = Workload("t", 2, 4, 4, 512, 512, 128, "bf16", causal=True)
+bias = (2.0 * torch.randn(1, 4, 512, 512, generator=g)).to(torch.bfloat16)
+wp = Workload("t", 4, 12, 12, 1024, 1024, 64, "f16", causal=True)
+for w, b in ((wb, bias), (wp, None)):
+    x = make_inputs(w, seed=w.d, with_do=False)
+    bd = None if b is None else b.cuda()
+    os.environ["SDPA_WAIT_LIMIT_CYCLES"] = "1"
+    st, _ = fwd_only(w, x, bd)
+    assert st == 6, f"forward {w.b}x{w.h_q}x{w.s_q}x{w.d}: status {st}, want SDPA_ERR_TIMEOUT"
+    assert m.sdpa_device_error() == 0
+    del os.environ["SDPA_WAIT_LIMIT_CYCLES"]
+    st, o = fwd_only(w, x, bd)
+    assert st == 0
+    O, _ = oracle.forward(f64(x.q), f64(x.k), f64(x.v), w.scale, True,
+                          bias=None if b is None else f64(b))
+    assert_fwd_close(f64(o), O)
 print("WAIT_TIMEOUT_OK")
 '''
 
