@@ -79,12 +79,13 @@ size_t widen_bytes(const sdpa_problem_t* p, size_t* off_k, size_t* off_v, size_t
   return p->in_dtype == SDPA_DTYPE_E4M3 ? 2 * nq + 2 * nkv : 0;
 }
 
-// Transposed bias copy of a backward pass: [1 or b][1 or h_q][s_kv][s_q rounded up to 128].
+// Transposed bias copy of a backward pass: [1 or b][1 or h_q] x 128 x 128 tiles over keys
+// (s_kv rounded up to 128) and queries (s_q rounded up to 128).
 size_t bias_t_bytes(const sdpa_problem_t* p) {
   if (p->bias == nullptr) return 0;
   const size_t nb = p->bias_strides.b == 0 ? 1 : p->b, nh = p->bias_strides.h == 0 ? 1 : p->h_q;
-  const size_t pad = (p->s_q + 127) / 128 * 128;
-  return (nb * nh * p->s_kv * pad * 2 + 255) & ~size_t(255);
+  const size_t pad = (p->s_q + 127) / 128 * 128, kpad = (p->s_kv + 127) / 128 * 128;
+  return (nb * nh * kpad * pad * 2 + 255) & ~size_t(255);
 }
 
 // fp32 bias-gradient accumulator, laid out like the transposed bias copy.

@@ -100,8 +100,22 @@ __device__ __forceinline__ BwdScales bwd_scales(const BwdParams& p) {
   return s;
 }
 
-// 8·NV bias values of key row kv_row for queries q0.. from the transposed copy (zero for
-// a key row beyond s_kv, which sees nothing anyway).
+// The transposed bias copy and the bias-gradient accumulator are stored in 128 x 128 tiles
+// (key block kb, query block qb) ordered [nb][nh][kb][qb].  Inside a tile, for each half of
+// the 64 queries (hq2) and each quarter of 32 key rows (one warp's TMEM lanes), the 16-byte
+// chunks of a key row follow one another 32 rows apart: chunk e of key row 32·quad + lane is
+// 16-byte unit (hq2·4 + quad)·U·32 + e·32 + lane, U = 8 chunks of eight 16-bit values (copy)
+// or 16 chunks of four fp32 values (accumulator).  A warp that loads or reduce-adds chunk e of
+// its 32 key rows then touches one contiguous 512-byte run instead of 32 rows.
+__device__ __forceinline__ int64_t bias_tile_elems(const BwdParams& p, int bi, int hq, int kv_row, int q0) {
+  const int nb = p.bias_nb > 1 ? bi : 0, nh = p.bias_nh > 1 ? hq : 0;
+  const int n_kvb = (p.s_kv + kBlockN - 1) / kBlockN, n_qb = p.s_q_pad / kBlockM;
+  return ((static_cast<int64_t>(nb) * p.bias_nh + nh) * n_kvb + kv_row / kBlockN) * n_qb * 16384 +
+         static_cast<int64_t>(q0 / kBlockM) * 16384;
+}
+
+// 8·NV bias values of key row kv_row for queries q0.. (q0 a multiple of 8·NV within a 64-query
+// half) from the tiled copy; zero for a key row beyond s_kv, which sees nothing anyway.
 template <int NV>
 __device__ __forceinline__ void load_bias_t(const BwdParams& p, int bi, int hq, int kv_row, int q0, uint4 (&bz)[NV]) {
   if (kv_row >= p.s_kv) {
@@ -109,27 +123,32 @@ __device__ __forceinline__ void load_bias_t(const BwdParams& p, int bi, int hq, 
     for (int e = 0; e < NV; ++e) bz[e] = make_uint4(0u, 0u, 0u, 0u);
     return;
   }
-  const int nb = p.bias_nb > 1 ? bi : 0, nh = p.bias_nh > 1 ? hq : 0;
-  const uint4* src = reinterpret_cast<const uint4*>(
-      static_cast<const uint16_t*>(p.bias_t) +
-      ((static_cast<int64_t>(nb) * p.bias_nh + nh) * p.s_kv + kv_row) * p.s_q_pad + q0);
+  const int r = kv_row % kBlockN, hq2 = (q0 % kBlockM) / 64, e0 = (q0 % 64) / 8;
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.bias_t) +
+                                                    bias_tile_elems(p, bi, hq, kv_row, q0)) +
+                     ((hq2 * 4 + r / 32) * 8 + e0) * 32 + r % 32;
 #pragma unroll
-  for (int e = 0; e < NV; ++e) bz[e] = __ldg(src + e);
+  for (int e = 0; e < NV; ++e) bz[e] = __ldg(src + e * 32);
 }
 
-// Starts moving the same 128-byte bias row into L2 (a later step's row: its loads then hit L2).
+// Starts moving a later step's bias chunks of this warp's 32 key rows (4 KB, one 128-byte
+// line per lane) into L2, so that load_bias_t then hits there.
 __device__ __forceinline__ void prefetch_bias_t(const BwdParams& p, int bi, int hq, int kv_row, int q0) {
   if (kv_row >= p.s_kv) return;
-  const int nb = p.bias_nb > 1 ? bi : 0, nh = p.bias_nh > 1 ? hq : 0;
-  prefetch_l2(static_cast<const uint16_t*>(p.bias_t) +
-              ((static_cast<int64_t>(nb) * p.bias_nh + nh) * p.s_kv + kv_row) * p.s_q_pad + q0);
+  const int r = kv_row % kBlockN, hq2 = (q0 % kBlockM) / 64;
+  const uint4* run = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(p.bias_t) +
+                                                    bias_tile_elems(p, bi, hq, kv_row, q0)) +
+                     (hq2 * 4 + r / 32) * 8 * 32;
+  prefetch_l2(run + (r % 32) * 8);
 }
 
-// Row of the bias-gradient accumulator for key row kv_row and queries q0.. (nullptr past s_kv).
+// This thread's first accumulator chunk for key row kv_row and queries q0.. (q0 a multiple of
+// 4 within a 64-query half); chunk k of the thread is 128 floats further (nullptr past s_kv).
 __device__ __forceinline__ float* dbias_row(const BwdParams& p, int bi, int hq, int kv_row, int q0) {
   if (kv_row >= p.s_kv) return nullptr;
-  const int nb = p.bias_nb > 1 ? bi : 0, nh = p.bias_nh > 1 ? hq : 0;
-  return p.dbias_acc + ((static_cast<int64_t>(nb) * p.bias_nh + nh) * p.s_kv + kv_row) * p.s_q_pad + q0;
+  const int r = kv_row % kBlockN, hq2 = (q0 % kBlockM) / 64, e0 = (q0 % 64) / 4;
+  return p.dbias_acc + bias_tile_elems(p, bi, hq, kv_row, q0) +
+         static_cast<int64_t>(((hq2 * 4 + r / 32) * 16 + e0) * 32 + r % 32) * 4;
 }
 
 // dS of columns c, c+1 into the accumulator, four at a time (c is a compile-time constant).
@@ -137,7 +156,7 @@ __device__ __forceinline__ void dbias_emit(float* row, int c, float2 dd, float2&
   if (c % 4 == 0) {
     hold = dd;
   } else if (row != nullptr) {
-    red_add_v4(row + c - 2, hold.x, hold.y, dd.x, dd.y);
+    red_add_v4(row + (c / 4) * 128, hold.x, hold.y, dd.x, dd.y);
   }
 }
 
@@ -1509,21 +1528,22 @@ __global__ void __launch_bounds__(256) fp8_widen_kernel(const uint8_t* src, int6
 
 namespace {
 
-// [nb][nh][s_q][s_kv] (strided, 16-bit) -> [nb][nh][s_kv][s_q_pad] (dense) through 64 x 64
-// shared-memory tiles, 16-byte loads and stores; padded query columns get zeros.  With
-// skip_above, tiles whose keys all lie beyond every query's causal limit (key > query +
-// diag_off) are not written: the backward pass never reads them.
+// [nb][nh][s_q][s_kv] (strided, 16-bit) -> the tiled transposed copy (see bias_tile_elems):
+// one 128 x 128 tile per CTA through shared memory, 16-byte loads and stores; query rows
+// beyond s_q and keys beyond s_kv get zeros.  With skip_above, tiles whose keys all lie beyond
+// every query's causal limit (key > query + diag_off) are not written: the backward pass
+// never reads them.
 __global__ void __launch_bounds__(256) bias_transpose_kernel(const uint16_t* src, int64_t sb, int64_t sh,
                                                              int64_t ss, int nh, int s_q, int s_kv, int s_q_pad,
                                                              int skip_above, int diag_off, uint16_t* dst) {
-  __shared__ uint16_t tile[64][72];   // [query][key], rows padded against bank conflicts
+  __shared__ uint16_t tile[128][136];   // [query][key], rows padded against bank conflicts
   const int z = blockIdx.z;
   const int nbi = z / nh, nhi = z % nh;
-  const int i0 = blockIdx.x * 64, j0 = blockIdx.y * 64;
-  if (skip_above && j0 > i0 + 63 + diag_off) return;
+  const int i0 = blockIdx.x * 128, j0 = blockIdx.y * 128;
+  if (skip_above && j0 > i0 + 127 + diag_off) return;
   const uint16_t* s = src + nbi * sb + nhi * sh;
-  for (int t = threadIdx.x; t < 512; t += 256) {   // 64 query rows x 8 chunks of 8 keys
-    const int r = t / 8, c = t % 8;
+  for (int t = threadIdx.x; t < 2048; t += 256) {   // 128 query rows x 16 chunks of 8 keys
+    const int r = t / 16, c = t % 16;
     const int i = i0 + r, j = j0 + 8 * c;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (i < s_q) {
@@ -1539,16 +1559,16 @@ __global__ void __launch_bounds__(256) bias_transpose_kernel(const uint16_t* src
     *reinterpret_cast<uint4*>(&tile[r][8 * c]) = v;
   }
   __syncthreads();
-  uint16_t* d = dst + static_cast<int64_t>(z) * s_kv * s_q_pad;
-  for (int t = threadIdx.x; t < 512; t += 256) {   // 64 key rows x 8 chunks of 8 queries
-    const int r = t / 8, c = t % 8;
-    const int j = j0 + r, i = i0 + 8 * c;
-    if (j >= s_kv || i >= s_q_pad) continue;
+  const int n_qb = s_q_pad / 128;
+  uint4* d = reinterpret_cast<uint4*>(dst + ((static_cast<int64_t>(z) * gridDim.y + blockIdx.y) * n_qb + blockIdx.x) * 16384);
+  for (int o = threadIdx.x; o < 2048; o += 256) {   // 16-byte unit ((hq2 * 4 + quad) * 8 + e) * 32 + lane
+    const int lane = o % 32, e = (o / 32) % 8, quad = (o / 256) % 4, hq2 = o / 1024;
+    const int key = quad * 32 + lane, q = hq2 * 64 + e * 8;
     uint32_t h[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u)
-      h[u] = static_cast<uint32_t>(tile[8 * c + 2 * u][r]) | (static_cast<uint32_t>(tile[8 * c + 2 * u + 1][r]) << 16);
-    *reinterpret_cast<uint4*>(d + static_cast<int64_t>(j) * s_q_pad + i) = make_uint4(h[0], h[1], h[2], h[3]);
+      h[u] = static_cast<uint32_t>(tile[q + 2 * u][key]) | (static_cast<uint32_t>(tile[q + 2 * u + 1][key]) << 16);
+    d[o] = make_uint4(h[0], h[1], h[2], h[3]);
   }
 }
 
@@ -1557,7 +1577,7 @@ __global__ void __launch_bounds__(256) bias_transpose_kernel(const uint16_t* src
 cudaError_t launch_bias_transpose(const void* src, int64_t sb, int64_t sh, int64_t ss, int nb, int nh,
                                   int s_q, int s_kv, int s_q_pad, int skip_above, int diag_off, void* dst,
                                   cudaStream_t st) {
-  dim3 grid((s_q_pad + 63) / 64, (s_kv + 63) / 64, nb * nh);
+  dim3 grid(s_q_pad / 128, (s_kv + 127) / 128, nb * nh);
   bias_transpose_kernel<<<grid, 256, 0, st>>>(static_cast<const uint16_t*>(src), sb, sh, ss, nh, s_q, s_kv,
                                               s_q_pad, skip_above, diag_off, static_cast<uint16_t*>(dst));
   return cudaGetLastError();
@@ -1565,31 +1585,34 @@ cudaError_t launch_bias_transpose(const void* src, int64_t sb, int64_t sh, int64
 
 namespace {
 
-// Transposed fp32 accumulator [nb][nh][s_kv][s_q_pad] -> dbias [nb][nh][s_q][s_kv] (16-bit,
-// caller strides) through 64 x 64 shared-memory tiles.
+// Tiled fp32 accumulator (see bias_tile_elems) -> dbias [nb][nh][s_q][s_kv] (16-bit, caller
+// strides): one CTA per 64 queries (one half, hq2) of a 128 x 128 tile, through shared memory.
 template <typename T>
 __global__ void __launch_bounds__(256) dbias_convert_kernel(const float* acc, int nh, int s_q, int s_kv,
                                                             int s_q_pad, T* dst, int64_t sb, int64_t sh,
                                                             int64_t ss) {
-  __shared__ float tile[64][65];   // [key][query]
+  __shared__ float tile[64][129];   // [query][key]
   const int z = blockIdx.z;
   const int nbi = z / nh, nhi = z % nh;
-  const int i0 = blockIdx.x * 64, j0 = blockIdx.y * 64;
-  const float* a = acc + static_cast<int64_t>(z) * s_kv * s_q_pad;
-  for (int t = threadIdx.x; t < 1024; t += 256) {   // 64 key rows x 16 chunks of 4 queries
-    const int r = t / 16, c = t % 16;
-    const int j = j0 + r, i = i0 + 4 * c;
-    float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (j < s_kv && i < s_q_pad) v = *reinterpret_cast<const float4*>(a + static_cast<int64_t>(j) * s_q_pad + i);
-    tile[r][4 * c] = v.x;
-    tile[r][4 * c + 1] = v.y;
-    tile[r][4 * c + 2] = v.z;
-    tile[r][4 * c + 3] = v.w;
+  const int qb = blockIdx.x / 2, hq2 = blockIdx.x % 2, kb = blockIdx.y;
+  const int i0 = qb * 128 + hq2 * 64, j0 = kb * 128;
+  if (i0 >= s_q) return;
+  const int n_qb = s_q_pad / 128;
+  const float4* a = reinterpret_cast<const float4*>(acc + ((static_cast<int64_t>(z) * gridDim.y + kb) * n_qb + qb) * 16384) +
+                    hq2 * 2048;
+  for (int o = threadIdx.x; o < 2048; o += 256) {   // float4 unit (quad * 16 + e) * 32 + lane of this half
+    const int lane = o % 32, e = (o / 32) % 16, quad = o / 512;
+    const float4 v = a[o];
+    const int key = quad * 32 + lane, q = e * 4;
+    tile[q][key] = v.x;
+    tile[q + 1][key] = v.y;
+    tile[q + 2][key] = v.z;
+    tile[q + 3][key] = v.w;
   }
   __syncthreads();
   T* d = dst + nbi * sb + nhi * sh;
-  for (int t = threadIdx.x; t < 512; t += 256) {    // 64 query rows x 8 chunks of 8 keys
-    const int r = t / 8, c = t % 8;
+  for (int t = threadIdx.x; t < 1024; t += 256) {   // 64 query rows x 16 chunks of 8 keys
+    const int r = t / 16, c = t % 16;
     const int i = i0 + r, j = j0 + 8 * c;
     if (i >= s_q || j >= s_kv) continue;
     T* row = d + static_cast<int64_t>(i) * ss + j;
@@ -1599,11 +1622,11 @@ __global__ void __launch_bounds__(256) dbias_convert_kernel(const float* acc, in
       for (int u = 0; u < 4; ++u) {
         T lo, hi;
         if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-          lo = __float2bfloat16_rn(tile[8 * c + 2 * u][r]);
-          hi = __float2bfloat16_rn(tile[8 * c + 2 * u + 1][r]);
+          lo = __float2bfloat16_rn(tile[r][8 * c + 2 * u]);
+          hi = __float2bfloat16_rn(tile[r][8 * c + 2 * u + 1]);
         } else {
-          lo = __float2half_rn(tile[8 * c + 2 * u][r]);
-          hi = __float2half_rn(tile[8 * c + 2 * u + 1][r]);
+          lo = __float2half_rn(tile[r][8 * c + 2 * u]);
+          hi = __float2half_rn(tile[r][8 * c + 2 * u + 1]);
         }
         h[u] = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&lo)) |
                (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(&hi)) << 16);
@@ -1611,8 +1634,8 @@ __global__ void __launch_bounds__(256) dbias_convert_kernel(const float* acc, in
       *reinterpret_cast<uint4*>(row) = make_uint4(h[0], h[1], h[2], h[3]);
     } else {
       for (int u = 0; j + u < s_kv; ++u) {
-        if constexpr (std::is_same<T, __nv_bfloat16>::value) row[u] = __float2bfloat16_rn(tile[8 * c + u][r]);
-        else row[u] = __float2half_rn(tile[8 * c + u][r]);
+        if constexpr (std::is_same<T, __nv_bfloat16>::value) row[u] = __float2bfloat16_rn(tile[r][8 * c + u]);
+        else row[u] = __float2half_rn(tile[r][8 * c + u]);
       }
     }
   }
@@ -1622,7 +1645,7 @@ __global__ void __launch_bounds__(256) dbias_convert_kernel(const float* acc, in
 
 cudaError_t launch_dbias_convert(const float* acc, int nb, int nh, int s_q, int s_kv, int s_q_pad, void* dst,
                                  int64_t sb, int64_t sh, int64_t ss, int dtype, cudaStream_t st) {
-  dim3 grid((s_q + 63) / 64, (s_kv + 63) / 64, nb * nh);
+  dim3 grid(s_q_pad / 128 * 2, (s_kv + 127) / 128, nb * nh);
   if (dtype == kBF16)
     dbias_convert_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(acc, nh, s_q, s_kv, s_q_pad,
                                                               static_cast<__nv_bfloat16*>(dst), sb, sh, ss);
