@@ -238,6 +238,17 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdParams p) {
 
 // Split groups only: zero the fp32 dK/dV accumulators before the main kernel, and write
 // dK, dV in the output dtype and strides after it.
+// Split groups add dK and dV shares into fp32 accumulators [b][h_kv] x 128-row key blocks of
+// D columns.  Inside a block, chunk e (four columns) of key row 32·quad + lane is float4 unit
+// (quad·D/4 + e)·32 + lane, so a warp's reduction of one chunk of its 32 rows is one contiguous
+// 512-byte run.  This returns the float offset of chunk 0 of key row kv_row; chunk e is 128
+// floats further.
+__device__ __forceinline__ int64_t kv_acc_offset(const BwdParams& p, int bi, int hk, int kv_row, int D) {
+  const int r = kv_row % kBlockN;
+  return ((static_cast<int64_t>(bi) * p.h_kv + hk) * p.s_kv_pad + (kv_row - r)) * D +
+         static_cast<int64_t>((r / 32) * (D / 4) * 32 + r % 32) * 4;
+}
+
 __global__ void __launch_bounds__(256) bwd_zero_kv_kernel(const BwdParams p) {
   const int64_t n4 = static_cast<int64_t>(p.b) * p.h_kv * p.s_kv_pad * p.d / 4;
   float4* a = reinterpret_cast<float4*>(p.dk_acc);
@@ -258,11 +269,11 @@ __global__ void __launch_bounds__(256) bwd_kv_convert_kernel(const BwdParams p) 
   const int part = threadIdx.x % TPR;
   if (row >= p.s_kv) return;
   const int dt = std::is_same<T, __nv_bfloat16>::value ? kBF16 : kF16;
-  const int64_t off = (static_cast<int64_t>(bh) * p.s_kv_pad + row) * D + part * 8;
+  const int64_t off = kv_acc_offset(p, bi, hk, row, D) + static_cast<int64_t>(2 * part) * 128;
   for (int which = 0; which < 2; ++which) {
     const float* src = (which == 0 ? p.dk_acc : p.dv_acc) + off;
-    const float4 a = reinterpret_cast<const float4*>(src)[0];
-    const float4 c = reinterpret_cast<const float4*>(src)[1];
+    const float4 a = reinterpret_cast<const float4*>(src)[0];         // columns 8·part ..
+    const float4 c = reinterpret_cast<const float4*>(src + 128)[0];   // 8·part + 4 ..
     uint4 w;
     w.x = pack2(a.x, a.y, dt);
     w.y = pack2(a.z, a.w, dt);
@@ -727,8 +738,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       tc_fence_after();
       const uint32_t acc = tmem + lane_off + (h == 0 ? C::DV_COL : C::DK_COL);
       const float mul = (h == 0) ? bs.dv : bs.dk;
-      float* dst = (h == 0 ? p.dv_acc : p.dk_acc) +
-                   ((static_cast<int64_t>(bi) * p.h_kv + hk) * p.s_kv_pad + kv_row) * D;
+      float* dst = (h == 0 ? p.dv_acc : p.dk_acc) + kv_acc_offset(p, bi, hk, kv_row, D);
 #pragma unroll 1
       for (int c = 0; c < D / 32 && n_iter > 0; ++c) {
         uint32_t v[32];
@@ -736,7 +746,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
         tmem_ld_wait();
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          red_add_v4(dst + c * 32 + u * 4, __uint_as_float(v[u * 4]) * mul,
+          red_add_v4(dst + (c * 8 + u) * 128, __uint_as_float(v[u * 4]) * mul,
                      __uint_as_float(v[u * 4 + 1]) * mul, __uint_as_float(v[u * 4 + 2]) * mul,
                      __uint_as_float(v[u * 4 + 3]) * mul);
       }
@@ -1228,8 +1238,7 @@ __global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant_
     const float mul = (h == 0) ? bs.dv : bs.dk;
     if (ok && p.kv_split > 1) {
       if (n_iter > 0) {
-        float* dst = (h == 0 ? p.dv_acc : p.dk_acc) +
-                     ((static_cast<int64_t>(bi) * p.h_kv + hk) * p.s_kv_pad + kv_row) * 256 + dh * 128;
+        float* dst = (h == 0 ? p.dv_acc : p.dk_acc) + kv_acc_offset(p, bi, hk, kv_row, 256);
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t v[32];
@@ -1237,7 +1246,7 @@ __global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant_
           tmem_ld_wait();
 #pragma unroll
           for (int u = 0; u < 8; ++u)
-            red_add_v4(dst + c * 32 + u * 4, __uint_as_float(v[u * 4]) * mul,
+            red_add_v4(dst + (dh * 32 + c * 8 + u) * 128, __uint_as_float(v[u * 4]) * mul,
                        __uint_as_float(v[u * 4 + 1]) * mul, __uint_as_float(v[u * 4 + 2]) * mul,
                        __uint_as_float(v[u * 4 + 3]) * mul);
         }

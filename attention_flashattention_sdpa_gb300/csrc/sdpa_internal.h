@@ -93,7 +93,8 @@ struct BwdParams {
   int kv_split;                 // CTAs per (batch, KV head, KV block); 1 = no split
   int heads_per_split;          // query heads one such CTA visits
   int s_kv_pad;                 // s_kv rounded up to 128
-  float* dk_acc;                // workspace [b][h_kv][s_kv_pad][d] fp32 (split only)
+  float* dk_acc;                // workspace, b * h_kv * s_kv_pad * d fp32 in 128-row key-block
+                                // tiles (split only; layout at kv_acc_offset)
   float* dv_acc;
   void* dk;                     // outputs (split only: written by the convert pass)
   void* dv;
