@@ -394,6 +394,13 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       : "memory");
 }
 
+// After tmem_ld_wait: marks the 32 registers a tcgen05.ld wrote as produced here, so that no
+// use of them is moved above the wait.
+__device__ __forceinline__ void reg_fence32(uint32_t* r) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

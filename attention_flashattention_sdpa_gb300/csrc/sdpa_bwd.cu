@@ -620,10 +620,18 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       if (!mbar_wait_warp(&bars.ring_full[n & 1], (n >> 1) & 1, wt)) { ok = false; break; }
       if (!mbar_wait_warp(&bars.s_full[b], par, wt)) { ok = false; break; }
       tc_fence_after();
+      // With dropout or a bias (more work per score) the first 32 columns of Sᵀ are computed
+      // while the second 32 are read from TMEM, and their Pᵀ is stored while the second 32
+      // are computed; the plain instance reads all 64 at once (measured no faster split).
+      constexpr bool SPLIT = DROP || BIAS;
       uint32_t sv[64];
       tmem_ld32(X + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      if constexpr (SPLIT) {
+        tmem_ld_wait();
+        reg_fence32(&sv[0]);
+      }
       tmem_ld32(X + 64 * h + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-      tmem_ld_wait();
+      if constexpr (!SPLIT) tmem_ld_wait();
       // Query column c is visible to key row kv_row iff c >= lim (causal: kv <= q + off);
       // keys beyond len_kv see nothing.  Padded query columns already have P = 0.
       const bool need_mask = (p.causal && (q0 + L.off < j * kBlockN + kBlockN - 1)) ||
@@ -639,6 +647,16 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       float4 nl4;
 #pragma unroll
       for (int c = 0; c < 64; c += 2) {
+        if (SPLIT && c == 32) {
+          // First half of Pᵀ to TMEM; the second half of Sᵀ has landed.
+          if constexpr (DROP) {
+            tmem_st16(X + 64 * h, *reinterpret_cast<uint32_t(*)[16]>(&pm[0]));
+          } else {
+            tmem_st16(X + 64 * h, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+          }
+          tmem_ld_wait();
+          reg_fence32(&sv[32]);
+        }
         if ((c & 3) == 0) nl4 = *reinterpret_cast<const float4*>(nlse2 + c);
         float2 nl = (c & 3) ? make_float2(nl4.z, nl4.w) : make_float2(nl4.x, nl4.y);
         if constexpr (ALIBI) nl = add2(nl, kr2);
@@ -660,8 +678,12 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
           pm[c / 2] = pk[c / 2] & prmt(w << (15 - (c % 32) / 2), 0u, 0xBB99u);
         }
       }
-      if constexpr (DROP) {
-        tmem_st32(X + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&pm[0]));
+      if constexpr (SPLIT) {
+        if constexpr (DROP) {
+          tmem_st16(X + 64 * h + 16, *reinterpret_cast<uint32_t(*)[16]>(&pm[16]));
+        } else {
+          tmem_st16(X + 64 * h + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+        }
       } else {
         tmem_st32(X + 64 * h, pk);
       }
