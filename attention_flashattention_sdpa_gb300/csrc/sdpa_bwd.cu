@@ -620,10 +620,10 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
       if (!mbar_wait_warp(&bars.ring_full[n & 1], (n >> 1) & 1, wt)) { ok = false; break; }
       if (!mbar_wait_warp(&bars.s_full[b], par, wt)) { ok = false; break; }
       tc_fence_after();
-      // With dropout or a bias (more work per score) the first 32 columns of Sᵀ are computed
+      // With dropout, a bias or ALiBi (more work per score) the first 32 columns of Sᵀ are computed
       // while the second 32 are read from TMEM, and their Pᵀ is stored while the second 32
       // are computed; the plain instance reads all 64 at once (measured no faster split).
-      constexpr bool SPLIT = DROP || BIAS;
+      constexpr bool SPLIT = DROP || BIAS || ALIBI;
       uint32_t sv[64];
       tmem_ld32(X + 64 * h, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
       if constexpr (SPLIT) {
