@@ -249,6 +249,20 @@ __device__ __forceinline__ int64_t kv_acc_offset(const BwdParams& p, int bi, int
          static_cast<int64_t>((r / 32) * (D / 4) * 32 + r % 32) * 4;
 }
 
+// Zeros for columns [c0, c0 + ncols) of the dK and dV rows of key block j of (bi, hk) that lie
+// below s_kv: what a CTA whose key block no query sees contributes (16-bit zeros are zero bits).
+__device__ __forceinline__ void zero_kv_block(const BwdParams& p, int bi, int hk, int j, int c0, int ncols) {
+  const int chunks = ncols / 8;
+  for (int i = threadIdx.x; i < kBlockN * chunks; i += blockDim.x) {
+    const int row = j * kBlockN + i / chunks, col = c0 + (i % chunks) * 8;
+    if (row >= p.s_kv) continue;
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dk) + bi * p.dk_sb + hk * p.dk_sh + row * p.dk_ss + col) =
+        make_uint4(0u, 0u, 0u, 0u);
+    *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.dv) + bi * p.dv_sb + hk * p.dv_sh + row * p.dv_ss + col) =
+        make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
 __global__ void __launch_bounds__(256) bwd_zero_kv_kernel(const BwdParams p) {
   const int64_t n4 = static_cast<int64_t>(p.b) * p.h_kv * p.s_kv_pad * p.d / 4;
   float4* a = reinterpret_cast<float4*>(p.dk_acc);
@@ -391,6 +405,13 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   const int head0 = hk * p.group + split * p.heads_per_split;
   const int n_heads = max(0, min(p.heads_per_split, (hk + 1) * p.group - head0));
   const int n_iter = per_head * n_heads;
+  // No query sees this key block (it lies beyond len_kv, or above a causal diagonal): its dK
+  // and dV rows are zero (split groups: the zeroed accumulators already hold its share), and
+  // the CTA needs neither its K/V tiles nor tensor memory.
+  if (n_iter == 0) {
+    if (p.kv_split == 1) zero_kv_block(p, bi, hk, j, 0, D);
+    return;
+  }
 
   // The 128-byte swizzle of every tile assumes a 1024-byte aligned base (the budget leaves
   // no room for manual alignment).  If that ever fails, report it and do nothing.
@@ -989,6 +1010,10 @@ __global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant_
   const int head0 = hk * p.group + split * p.heads_per_split;
   const int n_heads = max(0, min(p.heads_per_split, (hk + 1) * p.group - head0));
   const int n_iter = per_head * n_heads;
+  if (n_iter == 0) {   // no query sees this key block: zero dK/dV rows of this half of d
+    if (p.kv_split == 1) zero_kv_block(p, bi, hk, j, dh * 128, 128);
+    return;
+  }
   auto iter_head = [&](int n) { return head0 + n / per_head; };
   auto iter_q0 = [&](int n) { return (q_first + n % per_head) * C::BQ; };
 
