@@ -11,9 +11,10 @@
 //
 // One kernel writes the bits twice: row-major for the forward pass (a thread owns a query
 // row) and transposed for the backward pass (a thread owns a key row), so neither attention
-// kernel runs the generator.  In the transposed words the two rows of an even/odd pair sit
-// 16 bits apart (row i at bit 16 * (i % 2) + (i % 32) / 2 of word i / 32): the backward pass
-// keeps or drops a packed pair of 16-bit values with one shift and one byte permute.
+// kernel runs the generator.  In both, the two elements of an even/odd pair sit 16 bits apart
+// (key j of a row at bit 16 * (j % 2) + (j % 32) / 2 of word j / 32; row i of a key likewise):
+// the attention kernels keep or drop a packed pair of 16-bit values with one shift and one
+// byte permute.
 #include <cstdint>
 
 #include "sdpa_internal.h"
@@ -68,6 +69,20 @@ __device__ __forceinline__ uint32_t keep8(uint64_t g, uint32_t off_lo, uint32_t 
 // Transposes the 32 x 32 bit matrix a warp holds (bit c of lane l's word = M[l][c]) so that
 // bit l of lane c's word = M[l][c]: five exchange stages, each swapping the off-diagonal k x k
 // blocks (k = 16, 8, 4, 2, 1) between lanes l and l ^ k.
+// Even bits of x to the low half, odd bits to the high half (bit 2k -> k, 2k + 1 -> 16 + k):
+// four delta swaps.
+__device__ __forceinline__ uint32_t unshuffle_pairs(uint32_t x) {
+  uint32_t t = (x ^ (x >> 1)) & 0x22222222u;
+  x ^= t ^ (t << 1);
+  t = (x ^ (x >> 2)) & 0x0C0C0C0Cu;
+  x ^= t ^ (t << 2);
+  t = (x ^ (x >> 4)) & 0x00F000F0u;
+  x ^= t ^ (t << 4);
+  t = (x ^ (x >> 8)) & 0x0000FF00u;
+  x ^= t ^ (t << 8);
+  return x;
+}
+
 __device__ __forceinline__ uint32_t transpose32(uint32_t x, int lane) {
   constexpr uint32_t kMask[5] = {0x0000FFFFu, 0x00FF00FFu, 0x0F0F0F0Fu, 0x33333333u, 0x55555555u};
 #pragma unroll
@@ -81,7 +96,8 @@ __device__ __forceinline__ uint32_t transpose32(uint32_t x, int lane) {
 }
 
 // One CTA of 128 threads per (b*h_q, 128-row query block, 128-key block).  Lane L of warp w
-// draws row 32w + L: 16 Philox blocks give its 128 bits, stored as four row-major words.  The
+// draws row 32w + L: 16 Philox blocks give its 128 bits, stored as four row-major words (keys
+// paired 16 bits apart).  The
 // transposed words come from a five-stage shuffle transpose of each 32x32 bit block and a 2 KB
 // exchange.
 __global__ void __launch_bounds__(128) dropout_mask_kernel(const DropoutParams p) {
@@ -106,7 +122,8 @@ __global__ void __launch_bounds__(128) dropout_mask_kernel(const DropoutParams p
     if (p.rows != nullptr) {
       uint4* dst = reinterpret_cast<uint4*>(p.rows + (static_cast<int64_t>(bh) * p.s_q + row) * p.kv_words +
                                             kb * 4);
-      *dst = make_uint4(w[0], w[1], w[2], w[3]);
+      *dst = make_uint4(unshuffle_pairs(w[0]), unshuffle_pairs(w[1]), unshuffle_pairs(w[2]),
+                        unshuffle_pairs(w[3]));
     }
   }
   if (p.cols == nullptr) return;   // uniform over the grid
@@ -114,17 +131,8 @@ __global__ void __launch_bounds__(128) dropout_mask_kernel(const DropoutParams p
   // 32w .. 32w + 31 (bit l = row 32w + l).
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint32_t mine = transpose32(w[i], lane);
-    // Unshuffle: even rows to the low half, odd rows to the high half (four delta swaps).
-    uint32_t t = (mine ^ (mine >> 1)) & 0x22222222u;
-    mine ^= t ^ (t << 1);
-    t = (mine ^ (mine >> 2)) & 0x0C0C0C0Cu;
-    mine ^= t ^ (t << 2);
-    t = (mine ^ (mine >> 4)) & 0x00F000F0u;
-    mine ^= t ^ (t << 4);
-    t = (mine ^ (mine >> 8)) & 0x0000FF00u;
-    mine ^= t ^ (t << 8);
-    tile[32 * i + lane][warp] = mine;
+    // Even rows to the low half, odd rows to the high half.
+    tile[32 * i + lane][warp] = unshuffle_pairs(transpose32(w[i], lane));
   }
   __syncthreads();
   const int key = kb * 128 + threadIdx.x;

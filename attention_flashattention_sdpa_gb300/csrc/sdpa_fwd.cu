@@ -670,21 +670,22 @@ __global__ void __launch_bounds__(FwdCfg<D, DT>::THREADS, 1)
           float2 p23 = make_float2(ex2(x23.x), ex2(x23.y));
           acc0 = add2(acc0, p01);
           acc1 = add2(acc1, p23);
-          if constexpr (DROP) {
-            // Row sums take every P; P·V only the kept ones.
-            const int cg = c + col0;   // column within the key block
-            const uint32_t wd = (cg < 32) ? keep.x : (cg < 64) ? keep.y : (cg < 96) ? keep.z : keep.w;
-            const uint32_t b4 = wd >> (c % 32);
-            p01.x = (b4 & 1u) ? p01.x : 0.f;
-            p01.y = (b4 & 2u) ? p01.y : 0.f;
-            p23.x = (b4 & 4u) ? p23.x : 0.f;
-            p23.y = (b4 & 8u) ? p23.y : 0.f;
-          }
           if (FP8) {
             pk[c / 4] = pack4_e4m3(p01.x, p01.y, p23.x, p23.y);
           } else {
             pk[c / 2] = pack2(p01.x, p01.y, DT);
             pk[c / 2 + 1] = pack2(p23.x, p23.y, DT);
+          }
+          if constexpr (DROP && !FP8) {
+            // Row sums take every P; P·V only the kept ones.  A pair's keep bits sit at bits
+            // e/2 and e/2 + 16 of its word (e = its even column within the word): shifted to
+            // bits 15 and 31, a sign-replicating byte permute spreads them to the two 16-bit
+            // lanes, and a 16-bit zero is all zero bits.
+            const int cg = c + col0;   // column within the key block
+            const uint32_t wd = (cg < 32) ? keep.x : (cg < 64) ? keep.y : (cg < 96) ? keep.z : keep.w;
+            const int e = cg % 32;
+            pk[c / 2] &= prmt(wd << (15 - e / 2), 0u, 0xBB99u);
+            pk[c / 2 + 1] &= prmt(wd << (14 - e / 2), 0u, 0xBB99u);
           }
         }
         const float rowsum = (acc0.x + acc0.y) + (acc1.x + acc1.y);

@@ -228,7 +228,8 @@ SDPA_API sdpa_status_t sdpa_bwd_noalloc(const sdpa_problem_t* p, const void* q, 
 
 /*
  * Byte sizes of the two dropout keep-mask arrays of `p` (b, h_q, s_q, s_kv are read):
- *   mask:   uint32 [b*h_q][s_q][ceil(s_kv/128)*4]   (bit j%32 of word j/32: key j of row i)
+ *   mask:   uint32 [b*h_q][s_q][ceil(s_kv/128)*4]   (key j of row i at bit 16*(j%2) + (j%32)/2
+ *           of word j/32: the two keys of an even/odd pair sit 16 bits apart)
  *   mask_t: uint32 [b*h_q][s_kv][ceil(s_q/128)*4]   (row i of key j at bit 16*(i%2) + (i%32)/2
  *           of word i/32: the two rows of an even/odd pair sit 16 bits apart)
  */

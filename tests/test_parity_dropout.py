@@ -18,18 +18,18 @@ pytestmark = pytest.mark.gpu
 MODES = {"none": (False, False), "top_left": (True, False), "bottom_right": (True, True)}
 
 
-def _unpack(words: torch.Tensor, n_rows: int, n_words: int, n_valid: int) -> np.ndarray:
-    """Row-major keep bits: element j at bit j % 32 of word j / 32."""
-    w = words.cpu().numpy().view(np.uint32).reshape(n_rows, n_words)
-    j = np.arange(n_valid)
-    return ((w[:, j // 32] >> (j % 32).astype(np.uint32)) & 1).astype(bool)
-
-
 def _tbit(i):
-    """Bit of query row i within its word of the transposed mask (an even/odd pair of rows
-    sits 16 bits apart): 16 * (i % 2) + (i % 32) / 2."""
+    """Bit of element i within its word of either mask (an even/odd pair sits 16 bits apart):
+    16 * (i % 2) + (i % 32) / 2."""
     i = np.asarray(i)
     return (16 * (i % 2) + (i % 32) // 2).astype(np.uint32)
+
+
+def _unpack(words: torch.Tensor, n_rows: int, n_words: int, n_valid: int) -> np.ndarray:
+    """Row-major keep bits: key j of a row at bit _tbit(j) of word j / 32."""
+    w = words.cpu().numpy().view(np.uint32).reshape(n_rows, n_words)
+    j = np.arange(n_valid)
+    return ((w[:, j // 32] >> _tbit(j)) & 1).astype(bool)
 
 
 def _unpack_t(words: torch.Tensor, n_rows: int, n_words: int, n_valid: int) -> np.ndarray:
