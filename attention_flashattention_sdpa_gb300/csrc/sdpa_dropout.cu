@@ -45,8 +45,9 @@ __device__ __forceinline__ RoundKeys round_keys(uint64_t seed) {
   return rk;
 }
 
-// 8 keep bits (bit e = element 8g + e) of counter block g: keep iff the 16-bit draw u is at
-// least the threshold T, i.e. iff u + (65536 - T) reaches bit 16.
+// 8 keep bits of counter block g, in the paired order: element 8g + e at bit e / 2 for even e
+// and at bit 16 + e / 2 for odd e.  Keep iff the 16-bit draw u is at least the threshold T,
+// i.e. iff u + (65536 - T) reaches bit 16.
 __device__ __forceinline__ uint32_t keep8(uint64_t g, uint32_t off_lo, uint32_t off_hi, const RoundKeys& rk,
                                           uint32_t c) {
   uint32_t x0 = static_cast<uint32_t>(g), x1 = static_cast<uint32_t>(g >> 32), x2 = off_lo, x3 = off_hi;
@@ -62,7 +63,7 @@ __device__ __forceinline__ uint32_t keep8(uint64_t g, uint32_t off_lo, uint32_t 
   const uint32_t w[4] = {x0, x1, x2, x3};
   uint32_t bits = 0;
 #pragma unroll
-  for (int e = 0; e < 8; ++e) bits |= (((w[e / 2] >> (16 * (e % 2))) & 0xFFFFu) + c) >> 16 << e;
+  for (int e = 0; e < 8; ++e) bits |= (((w[e / 2] >> (16 * (e % 2))) & 0xFFFFu) + c) >> 16 << (16 * (e % 2) + e / 2);
   return bits;
 }
 
@@ -117,23 +118,22 @@ __global__ void __launch_bounds__(128) dropout_mask_kernel(const DropoutParams p
     const uint32_t c = 65536u - p.threshold;
 #pragma unroll
     for (int i = 0; i < 4; ++i)
-      w[i] = keep8(g0 + 4 * i, off_lo, off_hi, rk, c) | (keep8(g0 + 4 * i + 1, off_lo, off_hi, rk, c) << 8) |
-             (keep8(g0 + 4 * i + 2, off_lo, off_hi, rk, c) << 16) | (keep8(g0 + 4 * i + 3, off_lo, off_hi, rk, c) << 24);
+      w[i] = keep8(g0 + 4 * i, off_lo, off_hi, rk, c) | (keep8(g0 + 4 * i + 1, off_lo, off_hi, rk, c) << 4) |
+             (keep8(g0 + 4 * i + 2, off_lo, off_hi, rk, c) << 8) | (keep8(g0 + 4 * i + 3, off_lo, off_hi, rk, c) << 12);
     if (p.rows != nullptr) {
       uint4* dst = reinterpret_cast<uint4*>(p.rows + (static_cast<int64_t>(bh) * p.s_q + row) * p.kv_words +
                                             kb * 4);
-      *dst = make_uint4(unshuffle_pairs(w[0]), unshuffle_pairs(w[1]), unshuffle_pairs(w[2]),
-                        unshuffle_pairs(w[3]));
+      *dst = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
   if (p.cols == nullptr) return;   // uniform over the grid
-  // Transpose each 32 x 32 bit block: lane c then holds key 32i + c's bits for the warp's rows
-  // 32w .. 32w + 31 (bit l = row 32w + l).
+  // Transpose each 32 x 32 bit block: lane c then holds the bits of the key at bit position c
+  // of the row words, key 32i + 2 (c % 16) + c / 16 (paired order), for the warp's rows
+  // 32w .. 32w + 31 (bit l = row 32w + l); the rows are then paired the same way (even rows to
+  // the low half, odd rows to the high half).
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    // Even rows to the low half, odd rows to the high half.
-    tile[32 * i + lane][warp] = unshuffle_pairs(transpose32(w[i], lane));
-  }
+  for (int i = 0; i < 4; ++i)
+    tile[32 * i + 2 * (lane % 16) + lane / 16][warp] = unshuffle_pairs(transpose32(w[i], lane));
   __syncthreads();
   const int key = kb * 128 + threadIdx.x;
   if (key < p.s_kv) {
