@@ -73,7 +73,8 @@ from typing import Iterable, Sequence, Tuple
 import numpy as np
 
 __all__ = [
-    "philox4x32", "dropout_threshold", "dropout_keep", "bias_gradient",
+    "philox4x32", "philox4x32_arrays", "dropout_threshold", "dropout_keep", "dropout_keep_range",
+    "bias_gradient",
     "visible_mask", "kv_head_of", "alibi_default_slopes", "alibi_bias", "head_forward", "forward", "forward_rows",
     "backward", "backward_dq_rows", "backward_ds_rows", "backward_kv_rows", "backward_kv_head",
     "e4m3_decode_table",
@@ -353,6 +354,42 @@ def forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, causal: b
     return O, L
 
 
+def philox4x32_arrays(c0, c1, c2, c3, key: Sequence[int], rounds: int = 10):
+    """philox4x32 on arrays of counters: the same rounds, elementwise, in numpy uint64 (a 32 x
+    32-bit product fits).  c0..c3: integer arrays of 32-bit counter words (broadcast
+    together).  Returns the four output word arrays (uint64 holding 32-bit values)."""
+    m32 = np.uint64(_MASK32)
+    x0, x1, x2, x3 = (np.asarray(c, dtype=np.uint64) & m32 for c in (c0, c1, c2, c3))
+    x0, x1, x2, x3 = np.broadcast_arrays(x0, x1, x2, x3)
+    k0, k1 = (int(k) & _MASK32 for k in key)
+    for r in range(rounds):
+        if r > 0:
+            k0 = (k0 + PHILOX_W0) & _MASK32
+            k1 = (k1 + PHILOX_W1) & _MASK32
+        p0 = np.uint64(PHILOX_M0) * x0
+        p1 = np.uint64(PHILOX_M1) * x2
+        hi0, lo0 = p0 >> np.uint64(32), p0 & m32
+        hi1, lo1 = p1 >> np.uint64(32), p1 & m32
+        x0, x1, x2, x3 = hi1 ^ x1 ^ np.uint64(k0), lo1, hi0 ^ x3 ^ np.uint64(k1), lo0
+    return x0, x1, x2, x3
+
+
+def dropout_keep_range(b: int, h_q: int, s_q: int, s_kv: int, p: float, seed: int, offset: int,
+                       bh: int, r0: int, r1: int) -> np.ndarray:
+    """Keep mask [r1 - r0, s_kv] (bool) of query rows r0..r1-1 of (batch·h_q + head) bh: the
+    draw of dropout_keep, with the blocks of all those rows generated at once by
+    philox4x32_arrays (whole heads at s = 8192 in seconds)."""
+    t = dropout_threshold(p)
+    row_pitch = (s_kv + 127) // 128 * 128
+    n0 = (bh * s_q + np.arange(r0, r1, dtype=np.uint64)) * np.uint64(row_pitch)   # first element of each row
+    blk = (n0 // np.uint64(8))[:, None] + np.arange(row_pitch // 8, dtype=np.uint64)[None, :]
+    words = philox4x32_arrays(blk & np.uint64(_MASK32), blk >> np.uint64(32), offset & _MASK32,
+                              (offset >> 32) & _MASK32, (seed & _MASK32, (seed >> 32) & _MASK32))
+    # element 8g + e of a row: 16-bit half e % 2 of word e // 2 of block g
+    u = np.stack([(words[e // 2] >> np.uint64(16 * (e % 2))) & np.uint64(0xFFFF) for e in range(8)], axis=-1)
+    return (u.reshape(r1 - r0, row_pitch) >= np.uint64(t))[:, :s_kv]
+
+
 def _rows_mask(rows, s_kv: int, causal: bool) -> np.ndarray:
     rows = np.asarray(rows)
     if causal:
@@ -361,14 +398,17 @@ def _rows_mask(rows, s_kv: int, causal: bool) -> np.ndarray:
 
 
 def forward_rows(q_rows: np.ndarray, rows: Sequence[int], kh: np.ndarray, vh: np.ndarray,
-                 scale: float, causal: bool, bias: np.ndarray | None = None):
+                 scale: float, causal: bool, bias: np.ndarray | None = None,
+                 zdrop: np.ndarray | None = None):
     """Forward for selected query rows of one (batch, head).
 
     q_rows: [n, d] fp64 rows of Q; rows: their sequence positions; kh, vh: the
     row's KV head [s_kv, d]; bias: optional [n, s_kv] additive term on these rows' scaled
-    scores (a slice of a bias tensor, or ALiBi's rows).  Returns (O rows [n, d], LSE [n]).
+    scores (a slice of a bias tensor, or ALiBi's rows); zdrop: optional [n, s_kv] dropout
+    factor keep / (1 - p) of these rows (as in head_forward).  Returns (O rows [n, d], LSE [n]).
     Cost O(n·s_kv·d), which lets large shapes be checked row by row."""
-    O, lse, _ = head_forward(q_rows, kh, vh, scale, _rows_mask(rows, kh.shape[0], causal), bias=bias)
+    O, lse, _ = head_forward(q_rows, kh, vh, scale, _rows_mask(rows, kh.shape[0], causal), bias=bias,
+                             zdrop=zdrop)
     return O, lse
 
 
@@ -440,34 +480,37 @@ def bias_gradient(q, k, v, do, scale: float, causal: bool, bias, seq_lens_q=None
 
 
 def backward_ds_rows(q_rows, do_rows, rows: Sequence[int], kh, vh, scale: float, causal: bool,
-                     bias: np.ndarray | None = None):
+                     bias: np.ndarray | None = None, zdrop: np.ndarray | None = None):
     """dS = P ∘ (dP − Delta) for selected query rows of one (batch, head): [n, s_kv] — the
     gradient of the scaled scores, and so of an additive bias on them.
 
-    Row i needs only its own P_i, dP_i = dO_i Vᵀ and Delta_i = Σ_j P_ij dP_ij, so the cost is
-    O(n·s_kv·d)."""
+    Row i needs only its own P_i, dP_i = Z_i ∘ (dO_i Vᵀ) and Delta_i = Σ_j P_ij dP_ij (Z the
+    dropout factor zdrop of these rows, 1 without dropout), so the cost is O(n·s_kv·d)."""
     _, _, P = head_forward(q_rows, kh, vh, scale, _rows_mask(rows, kh.shape[0], causal), bias=bias)
     dP = do_rows @ vh.T
+    if zdrop is not None:
+        dP = zdrop * dP
     delta = (P * dP).sum(axis=1)
     return P * (dP - delta[:, None])
 
 
 def backward_dq_rows(q_rows, do_rows, rows: Sequence[int], kh, vh, scale: float, causal: bool,
-                     bias: np.ndarray | None = None):
-    """dQ = scale · dS K for selected query rows of one (batch, head): [n, d] (bias as in
-    forward_rows)."""
-    return scale * (backward_ds_rows(q_rows, do_rows, rows, kh, vh, scale, causal, bias) @ kh)
+                     bias: np.ndarray | None = None, zdrop: np.ndarray | None = None):
+    """dQ = scale · dS K for selected query rows of one (batch, head): [n, d] (bias and zdrop
+    as in forward_rows)."""
+    return scale * (backward_ds_rows(q_rows, do_rows, rows, kh, vh, scale, causal, bias, zdrop) @ kh)
 
 
 def backward_kv_rows(q_rows, do_rows, rows: Sequence[int], kh, vh, scale: float, causal: bool,
-                     bias: np.ndarray | None = None):
+                     bias: np.ndarray | None = None, zdrop: np.ndarray | None = None):
     """The contribution of selected query rows of one head to dK and dV: ([s_kv, d], [s_kv, d]).
 
     dK and dV of a KV head are the sums of these contributions over every query row of
-    every query head in its group (bias as in forward_rows)."""
+    every query head in its group (bias and zdrop as in forward_rows)."""
     _, _, P = head_forward(q_rows, kh, vh, scale, _rows_mask(rows, kh.shape[0], causal), bias=bias)
-    dV = P.T @ do_rows
-    dP = do_rows @ vh.T
+    Z = 1.0 if zdrop is None else zdrop
+    dV = (P * Z).T @ do_rows
+    dP = Z * (do_rows @ vh.T)
     delta = (P * dP).sum(axis=1)
     dS = P * (dP - delta[:, None])
     dK = scale * (dS.T @ q_rows)
@@ -475,13 +518,14 @@ def backward_kv_rows(q_rows, do_rows, rows: Sequence[int], kh, vh, scale: float,
 
 
 def backward_kv_head(q, k, v, do, scale: float, causal: bool, bi: int, hk: int,
-                     row_chunk: int = 1024, bias_rows=None):
+                     row_chunk: int = 1024, bias_rows=None, zdrop_rows=None):
     """dK, dV of one (batch, KV head) at any size: [s_kv, d] each.
 
     Sums over the KV head's group of query heads, visiting query rows in chunks
     so that at most row_chunk x s_kv scores are held at a time.  bias_rows: optional
     function (hq, r0, r1) -> [r1 - r0, s_kv] fp64, the additive term on the scaled scores of
-    query rows r0..r1-1 of head hq (a bias tensor's slice, or ALiBi's rows)."""
+    query rows r0..r1-1 of head hq (a bias tensor's slice, or ALiBi's rows); zdrop_rows: the
+    same for the dropout factor keep / (1 - p)."""
     b, h_q, s_q, _ = q.shape
     h_kv, s_kv = k.shape[1], k.shape[2]
     g = h_q // h_kv
@@ -492,8 +536,9 @@ def backward_kv_head(q, k, v, do, scale: float, causal: bool, bi: int, hk: int,
         for r0 in range(0, s_q, row_chunk):
             r1 = min(s_q, r0 + row_chunk)
             bias = None if bias_rows is None else bias_rows(hq, r0, r1)
+            z = None if zdrop_rows is None else zdrop_rows(hq, r0, r1)
             gk, gv = backward_kv_rows(q[bi, hq, r0:r1], do[bi, hq, r0:r1], np.arange(r0, r1),
-                                      kh, vh, scale, causal, bias)
+                                      kh, vh, scale, causal, bias, z)
             dK += gk
             dV += gv
     return dK, dV

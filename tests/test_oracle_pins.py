@@ -879,3 +879,64 @@ def test_row_forms_with_a_bias_or_alibi():
     gk, gv = oracle.backward_kv_head(q, k1, v1, do, 0.6, True, 0, 0, row_chunk=2, bias_rows=fn)
     np.testing.assert_allclose(gk, dK[0, 0], atol=1e-12)
     np.testing.assert_allclose(gv, dV[0, 0], atol=1e-12)
+
+
+def test_philox4x32_arrays_known_answers_and_scalar_form():
+    """The array form of the generator: the published known-answer vectors, and the scalar
+    form on random counters and keys (including words with the top bit set)."""
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.json")) as f:
+        kat = json.load(f)
+    for v in kat["vectors"]:
+        c = [int(x, 16) for x in v["counter"]]
+        k = [int(x, 16) for x in v["key"]]
+        got = oracle.philox4x32_arrays(*(np.array([w]) for w in c), k)
+        assert [int(w[0]) for w in got] == [int(x, 16) for x in v["out"]]
+    rng = np.random.default_rng(11)
+    ctr = rng.integers(0, 2 ** 32, size=(4, 64), dtype=np.uint64)
+    for key in [(0, 0), (0xFFFFFFFF, 0x80000001), (int(rng.integers(0, 2 ** 32)), int(rng.integers(0, 2 ** 32)))]:
+        got = oracle.philox4x32_arrays(ctr[0], ctr[1], ctr[2], ctr[3], key)
+        for n in range(64):
+            want = oracle.philox4x32([int(ctr[i, n]) for i in range(4)], key)
+            assert tuple(int(w[n]) for w in got) == want
+
+
+@pytest.mark.parametrize("s_q,s_kv,p", [(5, 200, 0.1), (3, 128, 0.5), (4, 9, 0.25)])
+def test_dropout_keep_range_is_the_row_draw(s_q, s_kv, p):
+    """The range draw equals dropout_keep's element-by-element draw, row for row (ragged key
+    lengths, so that rows start in a new 128-element stretch; a large offset and seed)."""
+    seed, offset = (1 << 40) + 77, (3 << 33) + 5
+    b, h = 2, 3
+    full = oracle.dropout_keep(b, h, s_q, s_kv, p, seed, offset)
+    for bh in (0, 4, 5):
+        got = oracle.dropout_keep_range(b, h, s_q, s_kv, p, seed, offset, bh, 1, s_q)
+        np.testing.assert_array_equal(got, full[bh // h, bh % h, 1:s_q])
+
+
+def test_row_forms_with_dropout():
+    """The row forms with a dropout factor, as the full-size dropout test uses them: rows of
+    the full forward (O, LSE) and backward (dQ), and whole KV heads of dK, dV, causal and not,
+    with GQA (2 query heads on 1 KV head)."""
+    b, h_q, h_kv, s, d, p = 2, 4, 2, 9, 3, 0.3
+    q, do = _rand(b, h_q, s, d), _rand(b, h_q, s, d)
+    k, v = _rand(b, h_kv, s, d), _rand(b, h_kv, s, d)
+    keep = oracle.dropout_keep(b, h_q, s, s, p, 99, 1)
+    z = keep.astype(np.float64) / (1.0 - p)
+    rows = [0, 4, 8]
+    for causal in (False, True):
+        O, L = oracle.forward(q, k, v, 0.6, causal, dropout_p=p, keep=keep)
+        dQ, dK, dV = oracle.backward(q, k, v, do, 0.6, causal, dropout_p=p, keep=keep)
+        for bi in range(b):
+            for hq in range(h_q):
+                hk = oracle.kv_head_of(hq, h_q, h_kv)
+                Or, Lr = oracle.forward_rows(q[bi, hq, rows], rows, k[bi, hk], v[bi, hk], 0.6, causal,
+                                             zdrop=z[bi, hq, rows])
+                np.testing.assert_allclose(Or, O[bi, hq, rows], atol=1e-13)
+                np.testing.assert_allclose(Lr, L[bi, hq, rows], atol=1e-13)
+                g = oracle.backward_dq_rows(q[bi, hq, rows], do[bi, hq, rows], rows, k[bi, hk], v[bi, hk], 0.6,
+                                            causal, zdrop=z[bi, hq, rows])
+                np.testing.assert_allclose(g, dQ[bi, hq, rows], atol=1e-12)
+        for bi, hk in ((0, 1), (1, 0)):
+            fn = lambda hq, r0, r1, bi=bi: z[bi, hq, r0:r1]
+            gk, gv = oracle.backward_kv_head(q, k, v, do, 0.6, causal, bi, hk, row_chunk=4, zdrop_rows=fn)
+            np.testing.assert_allclose(gk, dK[bi, hk], atol=1e-12)
+            np.testing.assert_allclose(gv, dV[bi, hk], atol=1e-12)
