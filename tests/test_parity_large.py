@@ -15,7 +15,7 @@ import torch
 import oracle
 from sdpa_workloads import (backward_d256, fp8_large_head, gpt2_inference, grouped, make_bias,
                             make_inputs, prefill_bottom_right, sample_kv_heads, sample_rows, training,
-                            training_alibi, training_bias, training_fp8, training_varlen)
+                            training_alibi, training_bias, training_dropout, training_fp8, training_varlen)
 from sdpa_testlib import (FP8_REL_L2, FWD_MAX_ABS, GRAD_REL_L2, LSE_ABS, assert_fwd_close,
                           assert_grad_close, f64, guarded_empty_like, check_guard, rel_l2, run_bwd,
                           run_bwd_fp8, run_fwd)
@@ -35,10 +35,11 @@ def _rows_f64(t, bi, h, rows, descale=1.0):
 
 
 def _check_rows(w, x, o, lse, dq=None, descales=(1.0, 1.0, 1.0, 1.0), rel=None, bias_rows=None,
-                grad_rel=None):
+                grad_rel=None, zdrop_rows=None):
     """O, LSE (and dQ) of the sampled rows against the row forms.  bias_rows: optional
-    function (bi, hq, rows) -> [len(rows), s_kv] fp64 additive term (ALiBi or a bias tensor).
-    rel / grad_rel: relative-L2 bounds replacing the 16-bit ones (FP8)."""
+    function (bi, hq, rows) -> [len(rows), s_kv] fp64 additive term (ALiBi or a bias tensor);
+    zdrop_rows: the same for the dropout factor keep / (1 - p).  rel / grad_rel: relative-L2
+    bounds replacing the 16-bit ones (FP8)."""
     dsq, dsk, dsv, dsdo = descales
     by_head = {}
     for bi, h, r in sample_rows(w, N_ROWS):
@@ -51,7 +52,8 @@ def _check_rows(w, x, o, lse, dq=None, descales=(1.0, 1.0, 1.0, 1.0), rel=None, 
         vh = _rows_f64(x.v, bi, hk, slice(None), dsv)
         qr = _rows_f64(x.q, bi, h, rows, dsq)
         br = None if bias_rows is None else bias_rows(bi, h, rows)
-        O, L = oracle.forward_rows(qr, rows, kh, vh, w.scale, w.causal, br)
+        zr = None if zdrop_rows is None else zdrop_rows(bi, h, rows)
+        O, L = oracle.forward_rows(qr, rows, kh, vh, w.scale, w.causal, br, zr)
         got_o.append(f64(o[bi, h, rows]))
         want_o.append(O)
         if lse is not None:
@@ -59,7 +61,7 @@ def _check_rows(w, x, o, lse, dq=None, descales=(1.0, 1.0, 1.0, 1.0), rel=None, 
             want_l.append(L)
         if dq is not None:
             dor = _rows_f64(x.do, bi, h, rows, dsdo)
-            want_q.append(oracle.backward_dq_rows(qr, dor, rows, kh, vh, w.scale, w.causal, br))
+            want_q.append(oracle.backward_dq_rows(qr, dor, rows, kh, vh, w.scale, w.causal, br, zr))
             got_q.append(f64(dq[bi, h, rows]))
     go, wo = np.concatenate(got_o), np.concatenate(want_o)
     if rel is None:
@@ -77,13 +79,17 @@ def _check_rows(w, x, o, lse, dq=None, descales=(1.0, 1.0, 1.0, 1.0), rel=None, 
             assert rel_l2(gq, wq) <= grad_rel, f"dQ rows rel-L2 {rel_l2(gq, wq):.3e}"
 
 
-def _check_kv_heads(w, x, dk, dv, n_pairs, descales=(1.0, 1.0, 1.0, 1.0), kv_bias_rows=None, grad_rel=None):
+def _check_kv_heads(w, x, dk, dv, n_pairs, descales=(1.0, 1.0, 1.0, 1.0), kv_bias_rows=None, grad_rel=None,
+                    kv_zdrop_rows=None):
     """Whole dK, dV of seeded (batch, KV head) pairs.  kv_bias_rows: optional function
-    (bi, hq, r0, r1) -> fp64 additive term of query rows r0..r1-1."""
+    (bi, hq, r0, r1) -> fp64 additive term of query rows r0..r1-1; kv_zdrop_rows: the same for
+    the dropout factor."""
     q64, k64, v64, do64 = (oracle.to_f64(t, ds) for t, ds in zip((x.q, x.k, x.v, x.do), descales))
     for bi, hk in sample_kv_heads(w, n_pairs)[:n_pairs]:
         fn = None if kv_bias_rows is None else (lambda hq, r0, r1, bi=bi: kv_bias_rows(bi, hq, r0, r1))
-        gk, gv = oracle.backward_kv_head(q64, k64, v64, do64, w.scale, w.causal, bi, hk, bias_rows=fn)
+        zf = None if kv_zdrop_rows is None else (lambda hq, r0, r1, bi=bi: kv_zdrop_rows(bi, hq, r0, r1))
+        gk, gv = oracle.backward_kv_head(q64, k64, v64, do64, w.scale, w.causal, bi, hk, bias_rows=fn,
+                                         zdrop_rows=zf)
         for got, want, n in ((dk, gk, "dK"), (dv, gv, "dV")):
             if grad_rel is None:
                 assert_grad_close(f64(got[bi, hk]), want, f"{n}[{bi},{hk}]")
@@ -274,6 +280,23 @@ def test_training_bias_s8192_as_benchmarked():
     _check_kv_heads(w, x, dk, dv, 2, kv_bias_rows=lambda bi, hq, r0, r1: oracle.to_f64(bias_cpu[0, hq, r0:r1]))
 
 
+def test_training_dropout_s8192_as_benchmarked():
+    """The training step with dropout p = 0.1, as the sweep runs it: the library draws the keep
+    mask (seed 1234, offset 0; both layouts, tiles above the diagonal skipped), the kernels read
+    it, and the oracle draws its own keep bits for the rows it checks (O, LSE, dQ of sampled rows;
+    two whole KV heads of dK, dV)."""
+    w = training_dropout(8192)
+    drop = (w.dropout, 1234, 0)
+    x = make_inputs(w, seed=0, with_do=True)
+    o, lse, dev = run_fwd(w, x, dropout=drop)
+    dq, dk, dv = run_bwd(w, dev, o, lse, x.do, dropout=drop)
+    zf = lambda bi, hq, r0, r1: oracle.dropout_keep_range(w.b, w.h_q, w.s_q, w.s_kv, drop[0], drop[1], drop[2],
+                                                           bi * w.h_q + hq, r0, r1) / (1.0 - drop[0])
+    rows_fn = lambda bi, hq, rows: np.concatenate([zf(bi, hq, r, r + 1) for r in rows])
+    _check_rows(w, x, o, lse, dq, zdrop_rows=rows_fn)
+    _check_kv_heads(w, x, dk, dv, 2, kv_zdrop_rows=zf)
+
+
 def test_training_fp8_s8192_as_benchmarked():
     """The FP8 training step (E4M3 Q, K, V with a bf16 O; E5M2 dO; bf16 gradients) as the sweep
     runs it, against the oracle on the decoded inputs.  The forward's E4M3 rounding of P enters
@@ -288,7 +311,8 @@ def test_training_fp8_s8192_as_benchmarked():
     _check_kv_heads(w, x, dk, dv, 2, descales=ds, grad_rel=FP8_REL_L2)
 
 
-def test_backward_d256_as_benchmarked():
-    """The d = 256 backward pass at b4 h16 s4096 (bf16, causal): sampled rows and two whole KV
-    heads."""
-    _full_case(backward_d256(True), dkv_pairs=2)
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_d256_as_benchmarked(causal):
+    """The d = 256 backward pass at b4 h16 s4096 (bf16, causal and without a mask): sampled rows
+    and two whole KV heads."""
+    _full_case(backward_d256(causal), dkv_pairs=2)
