@@ -213,8 +213,8 @@ class Step:
         self.sdpa.sdpa_bwd(self.q, self.k, self.v, self.o, self.do, self.lse, self.dq, self.dk,
                            self.dv, self.ws, attn_scale=w.scale, causal=w.causal)
 
-    def h2d(self):
-        for dst, src in zip((self.q, self.k, self.v, self.do), self.host):
+    def h2d(self, which=slice(None)):
+        for dst, src in list(zip((self.q, self.k, self.v, self.do), self.host))[which]:
             dst.copy_(src, non_blocking=True)
 
     def d2h(self):
@@ -267,11 +267,12 @@ def time_e2e(pair, steps: int, warmup: int, clocks=None):
     dO in from pinned memory, runs fwd + bwd, and copies dQ, dK, dV out, all inside the
     timed region.  Two buffer sets and three streams (H2D, compute, D2H) let step n+1's
     inputs travel while step n computes and step n-1's gradients travel back, as a training
-    loop would overlap them; events order each buffer set's reuse."""
+    loop would overlap them; events order each buffer set's reuse.  dO is copied after Q, K, V
+    and only the backward pass waits for it, so it travels while the forward pass runs."""
     import torch
     comp = torch.cuda.current_stream()
     h2d_st, d2h_st = torch.cuda.Stream(), torch.cuda.Stream()
-    ev = {"h2d": [None, None], "comp": [None, None], "d2h": [None, None]}
+    ev = {"h2d": [None, None], "h2d_do": [None, None], "comp": [None, None], "d2h": [None, None]}
 
     def event(stream):
         e = torch.cuda.Event()
@@ -284,12 +285,15 @@ def time_e2e(pair, steps: int, warmup: int, clocks=None):
         with torch.cuda.stream(h2d_st):
             if ev["comp"][i] is not None:          # this set's inputs are free again
                 h2d_st.wait_event(ev["comp"][i])
-            s.h2d()
+            s.h2d(slice(0, 3))                     # Q, K, V
             ev["h2d"][i] = event(h2d_st)
+            s.h2d(slice(3, 4))                     # dO
+            ev["h2d_do"][i] = event(h2d_st)
         comp.wait_event(ev["h2d"][i])
         if ev["d2h"][i] is not None:               # this set's gradients have left
             comp.wait_event(ev["d2h"][i])
         s.fwd()
+        comp.wait_event(ev["h2d_do"][i])
         s.bwd()
         ev["comp"][i] = event(comp)
         with torch.cuda.stream(d2h_st):
