@@ -152,6 +152,21 @@ __device__ __forceinline__ void bulk_wait_read() {
 }
 
 // ---------------------------------------------------------------------------
+// programmatic dependent launch
+// ---------------------------------------------------------------------------
+
+// A kernel launched with the programmatic-stream-serialization attribute may start before the
+// kernel ahead of it on the stream has finished.  griddep_wait() blocks until that kernel has
+// completed and its memory operations are visible; for a kernel launched without the
+// attribute it returns at once.  griddep_launch_dependents() lets such a dependent kernel
+// start once every CTA of this grid has issued it (or exited).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // fences
 // ---------------------------------------------------------------------------
 

@@ -171,6 +171,9 @@ __device__ __forceinline__ float2 bias_pair(const uint4 (&bz)[NV], int c) {
 // One group of D/8 threads per row; each thread reads 8 elements (16 bytes) of O and dO.
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
+  // The main kernel may start its set-up and its K/V loads now; it waits for this grid before
+  // it reads Delta, -LSE·log2 e or the zeroed dQ accumulator.
+  griddep_launch_dependents();
   constexpr int TPR = D / 8;              // threads per row
   constexpr int ROWS = 256 / TPR;         // rows per block
   const int bh = blockIdx.y;
@@ -215,6 +218,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
 
 template <typename T, int D>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdParams p) {
+  griddep_wait();   // the main kernel's reduce-adds into the accumulator are complete
   constexpr int TPR = D / 8;
   constexpr int ROWS = 256 / TPR;
   const int bh = blockIdx.y;
@@ -369,6 +373,14 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   constexpr bool BIAS = (FEAT & kFeatBias) != 0;
   constexpr bool DBIAS = (FEAT & kFeatDBias) != 0;
   extern __shared__ __align__(1024) uint8_t smem[];
+  // The dQ conversion kernel may be launched now; it waits for this grid to complete.  This
+  // grid in turn may run alongside the pre-pass (Delta, -LSE·log2 e, the zeroed dQ
+  // accumulator): the producer waits for it (griddep_wait) before it loads the first vectors,
+  // and every other read of those results follows from that load (the vectors reach the
+  // compute warps through shared memory, the dQ reduce-adds follow the MMAs that follow the
+  // Q tiles).  The producer waits again at its exit, so a CTA that gave up early still
+  // completes after the pre-pass.
+  griddep_launch_dependents();
   BwdBarriers& bars = *reinterpret_cast<BwdBarriers*>(smem + C::OFF_BAR);
   uint8_t* sK = smem + C::OFF_K;
   uint8_t* sV = smem + C::OFF_V;
@@ -409,6 +421,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   // and dV rows are zero (split groups: the zeroed accumulators already hold its share), and
   // the CTA needs neither its K/V tiles nor tensor memory.
   if (n_iter == 0) {
+    griddep_wait();
     if (p.kv_split == 1) zero_kv_block(p, bi, hk, j, 0, D);
     return;
   }
@@ -416,6 +429,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   // The 128-byte swizzle of every tile assumes a 1024-byte aligned base (the budget leaves
   // no room for manual alignment).  If that ever fails, report it and do nothing.
   if (smem_u32(smem) & 1023u) {
+    griddep_wait();
     if (threadIdx.x == 0) atomicOr(&g_device_error, kErrSmemAlign);
     return;
   }
@@ -500,6 +514,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
             tma_load_4d(sRing + slot * C::TILE + c * 16384, map, &bars.ring_full[slot], c * 64,
                         qb * kBlockM, hq, bi);
           if (which == 0) {
+            if (n == 0) griddep_wait();   // K/V and the first Q tile are already on their way
             bulk_load(sVec + (n & 1) * 256, p.lse2 + vrow, 512, &bars.ring_full[slot]);
             bulk_load(sVec + (n & 1) * 256 + 128, p.delta + vrow, 512, &bars.ring_full[slot]);
           }
@@ -900,6 +915,7 @@ __global__ void __launch_bounds__(512, 1) bwd_main_kernel(const __grid_constant_
   // Every role is done.  If one gave up (the abort flag, visible to all after the barrier),
   // copies the producer issued may still be in flight: let them land before the CTA's shared
   // memory is released.  (Each ring slot holds at most one copy in flight.)
+  if (producer) griddep_wait();   // returns at once unless the producer gave up before its wait
   if (producer && *abort_flag) {
     mbar_wait_drain(&bars.kv_full, 0);
     for (int m = (nq > 2 ? nq - 2 : 0); m < nq; ++m) mbar_wait_drain(&bars.ring_full[m & 1], (m >> 1) & 1);
@@ -966,7 +982,12 @@ __global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant_
   constexpr bool BIAS = (FEAT & kFeatBias) != 0;
   constexpr bool DBIAS = (FEAT & kFeatDBias) != 0;
   extern __shared__ __align__(1024) uint8_t smem[];
+  // Programmatic dependent launch, as in the d <= 128 kernel: the dQ conversion may launch now,
+  // and the producer waits for the pre-pass before it loads the first vectors (every other
+  // use of the pre-pass's results follows from that load) and again at its exit.
+  griddep_launch_dependents();
   if (smem_u32(smem) & 1023u) {
+    griddep_wait();
     if (threadIdx.x == 0) atomicOr(&g_device_error, kErrSmemAlign);
     return;
   }
@@ -1011,6 +1032,7 @@ __global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant_
   const int n_heads = max(0, min(p.heads_per_split, (hk + 1) * p.group - head0));
   const int n_iter = per_head * n_heads;
   if (n_iter == 0) {   // no query sees this key block: zero dK/dV rows of this half of d
+    griddep_wait();
     if (p.kv_split == 1) zero_kv_block(p, bi, hk, j, dh * 128, 128);
     return;
   }
@@ -1082,6 +1104,7 @@ __global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant_
         for (int c = 2 * dh; c < 2 * dh + 2; ++c)
           tma_load_4d(sQN + b * 16384 + (c - 2 * dh) * 8192, &p.tm_q, &bars.qn_full[b], c * 64, q0, hq, bi);
         const int64_t vrow = (static_cast<int64_t>(bi) * p.h_q + hq) * p.s_q_pad + q0;
+        if (n == 0) griddep_wait();   // K/V and the first Q tiles are already on their way
         bulk_load(sVec + b * 128, p.lse2 + vrow, 256, &bars.qn_full[b]);
         bulk_load(sVec + b * 128 + 64, p.delta + vrow, 256, &bars.qn_full[b]);
         ++n_qn;
@@ -1391,6 +1414,7 @@ __global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant_
   __syncthreads();
   // Every role is done.  If one gave up, copies the producer issued may still be in flight:
   // let them land before the CTA's shared memory is released.
+  if (producer) griddep_wait();   // returns at once unless the producer gave up before its wait
   if (producer && *abort_flag) {
     mbar_wait_drain(&bars.kv_full, 0);
     if (n_qf > 0) mbar_wait_drain(&bars.qf_full, (n_qf - 1) & 1);
@@ -1407,6 +1431,7 @@ __global__ void __launch_bounds__(512, 1) bwd_d256_kernel(const __grid_constant_
 // dQ = scale · (transposed accumulator)ᵀ for d = 256, through 32 x 32 shared-memory tiles.
 template <typename T>
 __global__ void __launch_bounds__(256) bwd_dqT_kernel(const BwdParams p) {
+  griddep_wait();   // the main kernel's reduce-adds into the accumulator are complete
   __shared__ float tile[32][33];
   const int bh = blockIdx.z;
   const int bi = bh / p.h_q, hq = bh % p.h_q;
@@ -1423,6 +1448,24 @@ __global__ void __launch_bounds__(256) bwd_dqT_kernel(const BwdParams p) {
     if constexpr (std::is_same<T, __nv_bfloat16>::value) *dst = __float2bfloat16_rn(v);
     else *dst = __float2half_rn(v);
   }
+}
+
+// Launches `kern` so that it may start while the kernel ahead of it on the stream is still
+// running (programmatic dependent launch); the kernel waits (griddep_wait) before it touches
+// that kernel's results.
+cudaError_t launch_dependent(void (*kern)(BwdParams), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             const BwdParams& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
 template <int DT>
@@ -1452,12 +1495,10 @@ cudaError_t launch_d256(const BwdParams& p, cudaStream_t st) {
   e = set_smem_once(reinterpret_cast<const void*>(kern), D256::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const unsigned grid = 2u * p.b * p.h_kv * p.kv_split * ((p.s_kv + kBlockN - 1) / kBlockN);
-  kern<<<grid, D256::THREADS, D256::SMEM_BYTES, st>>>(p);
-  e = cudaGetLastError();
+  e = launch_dependent(kern, dim3(grid), dim3(D256::THREADS), D256::SMEM_BYTES, st, p);
   if (e != cudaSuccess) return e;
   dim3 gdq(p.s_q_pad / 32, 256 / 32, bh);
-  bwd_dqT_kernel<T><<<gdq, 256, 0, st>>>(p);
-  e = cudaGetLastError();
+  e = launch_dependent(bwd_dqT_kernel<T>, gdq, dim3(256), 0, st, p);
   if (e != cudaSuccess || p.kv_split == 1) return e;
   dim3 gkv((p.s_kv + ROWS - 1) / ROWS, p.b * p.h_kv);
   bwd_kv_convert_kernel<T, 256><<<gkv, 256, 0, st>>>(p);
@@ -1492,12 +1533,10 @@ cudaError_t launch_t(const BwdParams& p, cudaStream_t st) {
   e = set_smem_once(reinterpret_cast<const void*>(kern), C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
   const unsigned gmain = static_cast<unsigned>(p.b) * p.h_kv * p.kv_split * ((p.s_kv + kBlockN - 1) / kBlockN);
-  kern<<<gmain, C::THREADS, C::SMEM_BYTES, st>>>(p);
-  e = cudaGetLastError();
+  e = launch_dependent(kern, dim3(gmain), dim3(C::THREADS), C::SMEM_BYTES, st, p);
   if (e != cudaSuccess) return e;
   dim3 gdq((p.s_q + ROWS - 1) / ROWS, bh);
-  bwd_dq_kernel<T, D><<<gdq, 256, 0, st>>>(p);
-  e = cudaGetLastError();
+  e = launch_dependent(bwd_dq_kernel<T, D>, gdq, dim3(256), 0, st, p);
   if (e != cudaSuccess || p.kv_split == 1) return e;
   dim3 gkv((p.s_kv + ROWS - 1) / ROWS, p.b * p.h_kv);
   bwd_kv_convert_kernel<T, D><<<gkv, 256, 0, st>>>(p);
